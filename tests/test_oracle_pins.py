@@ -1,0 +1,243 @@
+"""Pins for the fp64 oracle: each test checks it against something other than
+itself -- the quadratic (dual) form, closed forms, a hand-derived example,
+invariances the mathematics fixes.
+
+The recurrence being pinned is the Mamba-2 state update of the CGLA kernel
+page ("Mamba-Family State-Space Model Kernels on a Programmable CGLA",
+section III.A): h_t = exp(dt_t A) h_{t-1} + dt_t B_t x_t^T,
+y_t = C_t . h_t + D x_t, with diagonal per-head dynamics ("Compiler-First
+State Space Duality ...", abstract).  The pages print no SSD values, so no pin
+is a value taken from them.
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+from state_space_model_chunked_gb300 import inputs as gen
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+def _quadratic(x, dt, A, B, C, D, init):
+    """The dual (masked, attention-like) form of the scan, written from the
+    unrolled recurrence: y_t = sum_{s<=t} (C_t.B_s) exp(cum_t - cum_s) dt_s x_s
+    + exp(cum_t) C_t.h0 + D x_t, cum = inclusive cumsum of dt*A."""
+    b, L, H, P = x.shape
+    G, N = B.shape[2], B.shape[3]
+    y = np.zeros((b, L, H, P))
+    fin = np.zeros((b, H, P, N))
+    t_idx = np.arange(L)
+    causal = t_idx[:, None] >= t_idx[None, :]
+    for bi in range(b):
+        for h in range(H):
+            g = h // (H // G)
+            cum = np.cumsum(dt[bi, :, h].astype(np.float64) * float(A[h]))
+            diff = np.where(causal, cum[:, None] - cum[None, :], -np.inf)
+            Lmask = np.exp(diff)
+            Cg = C[bi, :, g, :].astype(np.float64)
+            Bg = B[bi, :, g, :].astype(np.float64)
+            X = x[bi, :, h, :].astype(np.float64)
+            M = (Cg @ Bg.T) * Lmask * dt[bi, :, h].astype(np.float64)[None, :]
+            yy = M @ X
+            if init is not None:
+                h0 = init[bi, h].astype(np.float64)          # [P][N]
+                yy += np.exp(cum)[:, None] * (Cg @ h0.T)
+            if D is not None:
+                yy += float(D[h]) * X
+            y[bi, :, h, :] = yy
+            w = np.exp(cum[-1] - cum) * dt[bi, :, h]
+            f = (X * w[:, None]).T @ Bg                       # [P][N]
+            if init is not None:
+                f += np.exp(cum[-1]) * init[bi, h].astype(np.float64)
+            fin[bi, h] = f
+    return y, fin
+
+
+def _rel(a, b):
+    return oracle.rel_l2(a, b)
+
+
+@pytest.mark.parametrize("H,G,P,N,L", [(1, 1, 4, 5, 37), (3, 1, 5, 4, 64),
+                                        (3, 3, 4, 4, 50), (4, 2, 5, 4, 41)])
+@pytest.mark.parametrize("with_init", [False, True])
+def test_seq_matches_quadratic_form(H, G, P, N, L, with_init):
+    inp = gen.scan_inputs(2, L, H, P, N, G, "f32", seed=11 + H + L,
+                          random_init=with_init)
+    y, fin = oracle.scan_seq(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"],
+                             inp["D"], inp["init"], nthreads=2)
+    yq, fq = _quadratic(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"],
+                        inp["D"], inp["init"])
+    assert _rel(y, yq) < 1e-10
+    assert _rel(fin, fq) < 1e-10
+
+
+def test_hand_worked_example():
+    g = json.load(open(os.path.join(HERE, "golden", "hand_example_L3.json")))
+    i = g["inputs"]
+    x = np.array(i["x"]).reshape(1, 3, 1, 1)
+    dt = np.array(i["dt"]).reshape(1, 3, 1)
+    A = np.array(i["A"])
+    B = np.array(i["B"]).reshape(1, 3, 1, 2)
+    C = np.array(i["C"]).reshape(1, 3, 1, 2)
+    D = np.array(i["D"])
+    init = np.array(i["init"]).reshape(1, 1, 1, 2)
+    y, fin = oracle.scan_seq(x, dt, A, B, C, D, init)
+    tol = g["tolerance"]
+    np.testing.assert_allclose(y.ravel(), g["expected"]["y"], rtol=tol, atol=tol)
+    np.testing.assert_allclose(fin.ravel(), np.ravel(g["expected"]["final_state"]),
+                               rtol=tol, atol=tol)
+
+
+def test_A_zero_is_prefix_sum():
+    inp = gen.scan_inputs(1, 40, 2, 3, 4, 1, "f32", seed=3, random_init=True)
+    A = np.zeros(2)
+    y, fin = oracle.scan_seq(inp["x"], inp["dt"], A, inp["B"], inp["C"], None,
+                             inp["init"])
+    x, dt, B, C, h0 = (inp[k].astype(np.float64) for k in ("x", "dt", "B", "C", "init"))
+    for h in range(2):
+        # outer products dt_s x_s B_s^T, accumulated
+        terms = dt[0, :, h, None, None] * x[0, :, h, :, None] * B[0, :, 0, None, :]
+        hs = h0[0, h][None] + np.cumsum(terms, axis=0)          # [L][P][N]
+        ys = np.einsum("tpn,tn->tp", hs, C[0, :, 0, :])
+        assert _rel(y[0, :, h], ys) < 1e-12
+        assert _rel(fin[0, h], hs[-1]) < 1e-12
+
+
+def test_constant_decay_is_geometric_series():
+    L, P, N = 30, 3, 4
+    rng = np.random.default_rng(5)
+    alpha_dt, A = 0.05, -2.0            # dt*A = -0.1 for every token
+    x1 = rng.standard_normal(P)
+    B1 = rng.standard_normal(N)
+    C1 = rng.standard_normal(N)
+    h0 = rng.standard_normal((P, N))
+    x = np.tile(x1, (1, L, 1, 1)).reshape(1, L, 1, P)
+    dt = np.full((1, L, 1), alpha_dt)
+    B = np.tile(B1, (1, L, 1, 1)).reshape(1, L, 1, N)
+    C = np.tile(C1, (1, L, 1, 1)).reshape(1, L, 1, N)
+    y, fin = oracle.scan_seq(x, dt, np.array([A]), B, C, np.array([0.7]),
+                             h0.reshape(1, 1, P, N))
+    a = alpha_dt * A
+    for t in range(L):
+        k = t + 1
+        ht = np.exp(a * k) * h0 + alpha_dt * np.outer(x1, B1) * (1 - np.exp(a * k)) / (1 - np.exp(a))
+        np.testing.assert_allclose(y[0, t, 0], ht @ C1 + 0.7 * x1, rtol=1e-12, atol=1e-12)
+    hL = np.exp(a * L) * h0 + alpha_dt * np.outer(x1, B1) * (1 - np.exp(a * L)) / (1 - np.exp(a))
+    np.testing.assert_allclose(fin[0, 0], hL, rtol=1e-12, atol=1e-12)
+
+
+def test_zero_input_is_pure_decay():
+    inp = gen.scan_inputs(2, 33, 3, 4, 5, 1, "f32", seed=9, random_init=True)
+    x = np.zeros_like(inp["x"])
+    y, fin = oracle.scan_seq(x, inp["dt"], inp["A"], inp["B"], inp["C"], inp["D"],
+                             inp["init"])
+    for b in range(2):
+        for h in range(3):
+            cum = np.cumsum(inp["dt"][b, :, h].astype(np.float64) * float(inp["A"][h]))
+            h0 = inp["init"][b, h].astype(np.float64)
+            ys = np.exp(cum)[:, None] * (inp["C"][b, :, 0, :].astype(np.float64) @ h0.T)
+            assert _rel(y[b, :, h], ys) < 1e-12
+            assert _rel(fin[b, h], np.exp(cum[-1]) * h0) < 1e-12
+
+
+@pytest.mark.parametrize("Q", [16, 32, 64, 256, 48])
+def test_chunk_size_invariance(Q):
+    inp = gen.scan_inputs(2, 200, 3, 8, 16, 1, "bf16", seed=21, random_init=True)
+    ys, fs = oracle.scan_seq(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"],
+                             inp["D"], inp["init"])
+    yc, fc, S, Hp = oracle.scan_chunked(inp["x"], inp["dt"], inp["A"], inp["B"],
+                                        inp["C"], Q, inp["D"], inp["init"],
+                                        want_intermediates=True)
+    assert _rel(yc, ys) < 1e-12
+    assert _rel(fc, fs) < 1e-12
+    # exposed intermediates obey the inter-chunk recurrence
+    nc = S.shape[1]
+    assert _rel(Hp[:, 0], inp["init"]) < 1e-15
+    for c in range(nc - 1):
+        lo, hi = c * Q, min((c + 1) * Q, 200)
+        dec = np.exp(np.sum(inp["dt"][:, lo:hi, :].astype(np.float64) * inp["A"][None, None, :], axis=1))
+        nxt = dec[:, :, None, None] * Hp[:, c] + S[:, c]
+        assert _rel(Hp[:, c + 1], nxt) < 1e-12
+
+
+def test_chunk_intermediates_are_their_definition():
+    # S_c of one chunk equals the final state of that chunk scanned alone
+    # from a zero state (the definition of a chunk's own contribution).
+    inp = gen.scan_inputs(1, 96, 2, 4, 8, 1, "f32", seed=4)
+    Q = 32
+    _, _, S, Hp = oracle.scan_chunked(inp["x"], inp["dt"], inp["A"], inp["B"],
+                                      inp["C"], Q, inp["D"], None,
+                                      want_intermediates=True)
+    for c in range(3):
+        sl = slice(c * Q, (c + 1) * Q)
+        _, fq = _quadratic(inp["x"][:, sl], inp["dt"][:, sl], inp["A"],
+                           inp["B"][:, sl], inp["C"][:, sl], None, None)
+        assert _rel(S[:, c], fq) < 1e-12
+
+
+@pytest.mark.parametrize("k", [1, 57, 128])
+def test_split_resume_invariance(k):
+    inp = gen.scan_inputs(2, 160, 2, 6, 8, 1, "bf16", seed=31, random_init=True)
+    y, fin = oracle.scan_seq(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"],
+                             inp["D"], inp["init"])
+    a = {kk: (v[:, :k] if kk in ("x", "dt", "B", "C") else v) for kk, v in inp.items()}
+    b = {kk: (v[:, k:] if kk in ("x", "dt", "B", "C") else v) for kk, v in inp.items()}
+    y1, f1 = oracle.scan_seq(a["x"], a["dt"], a["A"], a["B"], a["C"], a["D"], a["init"])
+    y2, f2 = oracle.scan_seq(b["x"], b["dt"], b["A"], b["B"], b["C"], b["D"], f1)
+    assert _rel(np.concatenate([y1, y2], axis=1), y) < 1e-13
+    assert _rel(f2, fin) < 1e-13
+
+
+def test_prefill_equals_decode_steps():
+    inp = gen.scan_inputs(2, 24, 4, 4, 8, 2, "bf16", seed=41, random_init=True)
+    y, fin = oracle.scan_seq(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"],
+                             inp["D"], inp["init"])
+    st = inp["init"].astype(np.float64)
+    for t in range(24):
+        yt, st = oracle.step(st, inp["x"][:, t], inp["dt"][:, t], inp["A"],
+                             inp["B"][:, t], inp["C"][:, t], inp["D"])
+        assert _rel(yt, y[:, t]) < 1e-13
+    assert _rel(st, fin) < 1e-13
+
+
+def test_linearity_in_x_and_init():
+    i1 = gen.scan_inputs(1, 50, 2, 4, 6, 1, "f32", seed=51, random_init=True)
+    i2 = gen.scan_inputs(1, 50, 2, 4, 6, 1, "f32", seed=52, random_init=True)
+    al, be = 0.75, -1.25
+    common = dict(dt=i1["dt"], A=i1["A"], B=i1["B"], C=i1["C"], D=i1["D"])
+    y1, f1 = oracle.scan_seq(i1["x"], init=i1["init"], **common)
+    y2, f2 = oracle.scan_seq(i2["x"], init=i2["init"], **common)
+    x1, x2 = i1["x"].astype(np.float64), i2["x"].astype(np.float64)
+    h1, h2 = i1["init"].astype(np.float64), i2["init"].astype(np.float64)
+    y3, f3 = oracle.scan_seq(al * x1 + be * x2, init=al * h1 + be * h2,
+                             **common)
+    assert _rel(y3, al * y1 + be * y2) < 1e-13
+    assert _rel(f3, al * f1 + be * f2) < 1e-13
+
+
+def test_thread_count_does_not_change_result():
+    inp = gen.scan_inputs(3, 70, 5, 4, 8, 1, "bf16", seed=61, random_init=True)
+    y1, f1 = oracle.scan_seq(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"],
+                             inp["D"], inp["init"], nthreads=1)
+    y4, f4 = oracle.scan_seq(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"],
+                             inp["D"], inp["init"], nthreads=4)
+    assert np.array_equal(y1, y4) and np.array_equal(f1, f4)
+
+
+def test_bf16_rounding_is_nearest_even():
+    # values chosen at and around bf16 rounding boundaries
+    vals = np.array([1.0, 1.0 + 2**-8, 1.0 + 2**-8 + 2**-20, 1.0 + 3 * 2**-8,
+                     -2.5, 3.0e-3], np.float32)
+    got, bits = gen.bf16_round(vals)
+    # 1 + 2^-8 is a tie between 1 and 1 + 2^-7: even mantissa -> 1.0
+    # 1 + 3*2^-8 is a tie between 1+2^-7 and 1+2^-6 ... even -> 1 + 2^-6
+    assert got[0] == 1.0
+    assert got[1] == 1.0
+    assert got[2] == np.float32(1.0 + 2**-7)
+    assert got[3] == np.float32(1.0 + 2**-6)
+    assert got[4] == -2.5
+    assert abs(got[5] - 3.0e-3) <= 3.0e-3 * 2**-8
+    assert bits[0] == 0x3F80
