@@ -1,0 +1,465 @@
+#!/usr/bin/env python3
+"""Benchmark of the SSD hot path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+One step = one ssd_scan_fwd over the Mamba-2-130M-shaped prefill layer
+(batch 1, seqlen 4096, 24 heads, headdim 64, d_state 128, bf16 x/B/C, fp32
+dt/A/D and states): every row of the hot path -- chunk cumsum and decays,
+C.B^T, the decay mask, the intra-chunk product, chunk states, inter-chunk
+state passing, the off-diagonal output and the D skip.  The line also carries
+the decode state update (64-layer 2.7B-shaped stack at batch 1/16/64/256) and
+the long-context 2.7B-shaped prefill, each with its own roofline.
+
+Inputs are seeded synthetic data generated on the device.  Between timed
+steps the prefill rotates through enough input/output sets to exceed twice
+the L2 cache, so no step reads another step's data from L2.
+
+--impl reference times the fp64 CPU oracle (the only other program that
+computes this path here) on the host cores, on a bounded sample of the same
+workload, and prints the same line with "impl": "reference".
+
+Under torchrun each rank runs its own copy of the workload on its own GPU
+(independent problems, no collective in the data path): weak scaling, value =
+all ranks' tokens / max over ranks of the timed region.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+WORKLOAD = "mamba2_130m_L4096"
+LONG_WORKLOAD = "mamba2_2p7b_L65536"
+METRIC = "SSD prefill Mtokens/s & decode state-update GB/s, % of roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ----------------------------------------------------------------- helpers
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        hbm = d.get("hbm_gbs") or d.get("hbm_GBs") or d.get("copy_gbs")
+        tf = d.get("bf16_tflops")
+        tfs = d.get("bf16_tflops_sustained", tf)
+        if hbm and tf:
+            return {"hbm_gbs": float(hbm), "bf16_tflops": float(tf),
+                    "bf16_tflops_sustained": float(tfs), "source": "measured"}
+    except (OSError, ValueError):
+        pass
+    out = dict(FALLBACK_PEAKS)
+    out["source"] = "fallback"
+    return out
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 200 ms."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{index}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        try:
+            for line in open(self.path):
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9 and parts[1].replace(".", "").isdigit():
+                    rows.append(parts)
+        except OSError:
+            pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows]
+        mx = max(float(r[2]) for r in rows)
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        busy = [s for s in sm if s > 0.5 * mx] or sm
+        return {"sm_mhz": statistics.median(busy), "sm_max_mhz": mx, "reasons": reasons,
+                "samples": len(rows)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+# ------------------------------------------------------------- workloads
+def scan_flops_bytes(shape, with_init):
+    """Algorithmic work of one scan: causal-triangle FLOPs (C.B^T once per
+    group) and compulsory bytes (inputs read once, outputs written once)."""
+    b, L, H, P, N, G, Q = (shape.batch, shape.seqlen, shape.nheads, shape.headdim,
+                           shape.dstate, shape.ngroups, shape.chunk)
+    nc = L // Q
+    per_chunk = G * Q * (Q + 1) * N + H * (Q * (Q + 1) * P + 4 * Q * N * P + 2 * N * P)
+    flops = b * nc * per_chunk
+    es = 2 if shape.dtype == "bf16" else 4
+    byts = (2 * b * L * H * P * es          # x read, y written
+            + b * L * H * 4                 # dt
+            + 2 * b * L * G * N * es        # B, C
+            + 2 * H * 4                     # A, D
+            + b * H * P * N * 4 * (2 if with_init else 1))  # init (if any), final
+    return flops, byts
+
+
+def make_scan_set(shape, seed, device):
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    b, L, H, P, N, G = (shape.batch, shape.seqlen, shape.nheads, shape.headdim,
+                        shape.dstate, shape.ngroups)
+    dt_ = torch.bfloat16 if shape.dtype == "bf16" else torch.float32
+    lo, hi = -6.907755278982137, -2.3025850929940455
+    t = {
+        "x": torch.randn((b, L, H, P), generator=g, device=device).to(dt_),
+        "dt": torch.exp(lo + (hi - lo) * torch.rand((b, L, H), generator=g, device=device)),
+        "A": -torch.exp(2.772588722239781 * torch.rand((H,), generator=g, device=device)),
+        "B": torch.randn((b, L, G, N), generator=g, device=device).to(dt_),
+        "C": torch.randn((b, L, G, N), generator=g, device=device).to(dt_),
+        "D": torch.randn((H,), generator=g, device=device),
+        "init": (0.1 * torch.randn((b, H, P, N), generator=g, device=device)
+                 if shape.random_init else None),
+    }
+    t["y"] = torch.empty_like(t["x"])
+    t["final"] = torch.empty((b, H, P, N), dtype=torch.float32, device=device)
+    return t
+
+
+def time_scan(shape, steps, warmup, device, l2_bytes, dist=None):
+    """Returns (ms_per_step, sets, launches_per_step)."""
+    import torch
+    import state_space_model_chunked_gb300 as ssd
+    _, byts = scan_flops_bytes(shape, shape.random_init)
+    nsets = max(1, -(-2 * l2_bytes // max(byts, 1)))
+    sets = [make_scan_set(shape, 1000 + i, device) for i in range(nsets)]
+    ws_bytes = ssd.scan_workspace_bytes(shape.batch, shape.seqlen, shape.nheads, shape.headdim,
+                                        shape.dstate, shape.ngroups, shape.chunk, device=device)
+    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=device)
+
+    def step(i):
+        s = sets[i % nsets]
+        ssd.scan_fwd(s["x"], s["dt"], s["A"], s["B"], s["C"], s["D"], shape.chunk, s["init"],
+                     y=s["y"], final_state=s["final"], workspace=ws)
+
+    for i in range(warmup):
+        step(i)
+    torch.cuda.synchronize(device)
+    stream = torch.cuda.current_stream(device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(device)
+    e0.record(stream)
+    for i in range(steps):
+        step(warmup + i)
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    if dist is not None:
+        dist.barrier()
+    ms = e0.elapsed_time(e1) / steps
+    return ms, nsets, byts
+
+
+def time_scan_e2e(shape, steps, warmup, device):
+    """Mtokens/s through the public API with pinned host buffers: per step the
+    host->device copy of the inputs, the scan, and the device->host copy of y
+    and the final state."""
+    import torch
+    import state_space_model_chunked_gb300 as ssd
+    s = make_scan_set(shape, 77, device)
+    host = {k: (v.cpu().pin_memory() if v is not None else None)
+            for k, v in s.items() if k not in ("y", "final")}
+    out = (torch.empty(s["y"].shape, dtype=s["y"].dtype, pin_memory=True),
+           torch.empty(s["final"].shape, dtype=torch.float32, pin_memory=True))
+    staging = {}
+
+    def step():
+        ssd.scan_fwd_host(host["x"], host["dt"], host["A"], host["B"], host["C"], host["D"],
+                          shape.chunk, host["init"], device=device, staging=staging, out=out)
+
+    for _ in range(max(warmup, 1)):
+        step()
+    torch.cuda.synchronize(device)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        step()
+    torch.cuda.synchronize(device)
+    dt = (time.perf_counter() - t0) / steps
+    h2d = sum(v.numel() * v.element_size() for v in host.values() if v is not None)
+    d2h = out[0].numel() * out[0].element_size() + out[1].numel() * 4
+    return dt, h2d, d2h
+
+
+def time_decode(batch, steps, device, peaks):
+    """One ssd_state_update per token over the 64-layer 2.7B-shaped stack,
+    layers flattened into heads (one group per layer)."""
+    import torch
+    import state_space_model_chunked_gb300 as ssd
+    from state_space_model_chunked_gb300 import inputs as gen
+    ds = gen.DECODE_SHAPE
+    Hf, G, P, N = ds.layers * ds.nheads, ds.layers, ds.headdim, ds.dstate
+    state = gen.device_decode_state(batch, Hf, P, N, seed=batch, device=device)
+    A, D = gen.decode_params(Hf, seed=batch)
+    A, D = torch.from_numpy(A).to(device), torch.from_numpy(D).to(device)
+    ntok = 4
+    toks = [gen.device_decode_token_inputs(batch, Hf, P, N, G, seed=batch, step=i, device=device)
+            for i in range(ntok)]
+    y = torch.empty((batch, Hf, P), dtype=torch.bfloat16, device=device)
+    for i in range(3):
+        t = toks[i % ntok]
+        ssd.state_update(state, t["x"], t["dt"], A, t["B"], t["C"], D, y=y)
+    stream = torch.cuda.current_stream(device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(device)
+    e0.record(stream)
+    for i in range(steps):
+        t = toks[i % ntok]
+        ssd.state_update(state, t["x"], t["dt"], A, t["B"], t["C"], D, y=y)
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    ms = e0.elapsed_time(e1) / steps
+    byts = (2 * batch * Hf * P * N * 4 + 2 * batch * Hf * P * 2 + batch * Hf * 4
+            + 2 * batch * G * N * 2 + 2 * Hf * 4)
+    gbs = byts / (ms * 1e-3) / 1e9
+    del state, toks
+    torch.cuda.empty_cache()
+    return {"batch": batch, "steps": steps, "ms_per_step": ms, "bytes_per_step": byts,
+            "GB_per_s": gbs, "frac_of_measured_hbm": gbs / peaks["hbm_gbs"],
+            "frac_of_8TBs_nominal": gbs / 8000.0}
+
+
+def cpu_oracle_sample(shape, target_s=10.0):
+    """The oracle as it stands, on all host cores, on whole heads of the
+    workload (every head is an independent recurrence): returns (Mtokens/s
+    scaled to the full layer, cores, sample description)."""
+    import oracle
+    from state_space_model_chunked_gb300 import inputs as gen
+    cores = os.cpu_count() or 1
+    heads = shape.nheads
+    inp = gen.scan_inputs(shape.batch, shape.seqlen, heads, shape.headdim, shape.dstate,
+                          shape.ngroups, shape.dtype, seed=5, random_init=shape.random_init)
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        oracle.scan_seq(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], inp["D"],
+                        inp["init"], nthreads=cores)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= target_s or reps >= 50:
+            break
+    tok_s = reps * shape.tokens / el
+    desc = (f"{reps} full passes of the {shape.name} workload ({shape.tokens} tokens x "
+            f"{heads} heads) through the fp64 oracle, {el:.1f} s")
+    return tok_s / 1e6, cores, desc
+
+
+# ------------------------------------------------------------------ arms
+def run_reference(args):
+    world, rank, _ = dist_setup()
+    if rank != 0:
+        return 0
+    from state_space_model_chunked_gb300 import inputs as gen
+    import oracle
+    oracle.build()
+    shape = gen.SCAN_SHAPES[WORKLOAD]
+    per = []
+    cores = os.cpu_count() or 1
+    for _ in range(args.warmup):
+        cpu_oracle_sample(shape, target_s=0.0)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        v, cores, desc = cpu_oracle_sample(shape, target_s=0.0)
+        per.append(v)
+    el = time.perf_counter() - t0
+    value = args.steps * shape.tokens / el / 1e6
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "Mtokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded PCG64)",
+        "config": {"workload": WORKLOAD, "batch": shape.batch, "seqlen": shape.seqlen,
+                   "nheads": shape.nheads, "headdim": shape.headdim, "dstate": shape.dstate,
+                   "ngroups": shape.ngroups, "chunk": shape.chunk},
+        "cpu_baseline": {"value": value, "unit": "Mtokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{args.steps} full passes of {WORKLOAD} on the host cores"},
+        "e2e": {"value": value, "unit": "Mtokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_only(args):
+    """One secondary workload alone, a few launches: used for ncu captures."""
+    import torch
+    device = torch.device("cuda:0")
+    torch.cuda.set_device(device)
+    from state_space_model_chunked_gb300 import build as ssd_build
+    from state_space_model_chunked_gb300 import inputs as gen
+    ssd_build.build()
+    peaks = load_peaks()
+    if args.only == "decode":
+        r = time_decode(args.decode_batch, args.steps, device, peaks)
+    else:
+        props = torch.cuda.get_device_properties(device)
+        l2 = getattr(props, "L2_cache_size", 126 * 1024 * 1024) or 126 * 1024 * 1024
+        lshape = gen.SCAN_SHAPES[LONG_WORKLOAD]
+        lms, _, lbytes = time_scan(lshape, args.steps, args.warmup, device, l2)
+        r = {"workload": LONG_WORKLOAD, "ms_per_step": lms,
+             "GB_per_s": lbytes / (lms * 1e-3) / 1e9}
+    print(json.dumps({"only": args.only, **r}), flush=True)
+    return 0
+
+
+def run_gpu(args):
+    import torch
+    world, rank, local = dist_setup()
+    dist = None
+    if world > 1:
+        import torch.distributed as tdist
+        torch.cuda.set_device(local)
+        tdist.init_process_group("nccl")
+        dist = tdist
+    device = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(device)
+    import state_space_model_chunked_gb300 as ssd
+    from state_space_model_chunked_gb300 import build as ssd_build
+    from state_space_model_chunked_gb300 import inputs as gen
+    if rank == 0 or world == 1:
+        ssd_build.build()
+    if dist is not None:
+        dist.barrier()
+    ssd.load()
+    peaks = load_peaks()
+    props = torch.cuda.get_device_properties(device)
+    l2 = getattr(props, "L2_cache_size", 126 * 1024 * 1024) or 126 * 1024 * 1024
+    shape = gen.SCAN_SHAPES[WORKLOAD]
+    flops, _ = scan_flops_bytes(shape, shape.random_init)
+
+    with ClockSampler(local) as clk:
+        ms, nsets, byts = time_scan(shape, args.steps, args.warmup, device, l2, dist)
+        if dist is not None:
+            t = torch.tensor([ms], device=device)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ms = float(t.item())
+        extra = {}
+        if rank == 0 and not args.quick:
+            lshape = gen.SCAN_SHAPES[LONG_WORKLOAD]
+            lms, _, lbytes = time_scan(lshape, 5, 3, device, l2)
+            lflops, _ = scan_flops_bytes(lshape, lshape.random_init)
+            extra["long_prefill"] = {
+                "workload": LONG_WORKLOAD, "ms_per_step": lms,
+                "Mtokens_per_s": lshape.tokens / (lms * 1e-3) / 1e6,
+                "roofline": {"bound": "hbm", "achieved": lbytes / (lms * 1e-3) / 1e9,
+                             "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                             "frac": lbytes / (lms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                             "traffic": None},
+                "tensor_tflops": lflops / (lms * 1e-3) / 1e12}
+            torch.cuda.empty_cache()
+            extra["decode"] = [time_decode(b, 128, device, peaks) for b in (1, 16, 64, 256)]
+    clocks = clk.summary()
+
+    e2e_s, h2d, d2h = time_scan_e2e(shape, max(args.steps // 4, 3), args.warmup, device)
+    tokens = shape.tokens * world
+    value = tokens / (ms * 1e-3) / 1e6
+    achieved = byts / (ms * 1e-3) / 1e9
+    launches = ssd.scan_kernel_launches(shape.batch, shape.seqlen, shape.nheads, shape.headdim,
+                                        shape.dstate, shape.ngroups, shape.chunk, device=device)
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return 0
+    line = {
+        "metric": METRIC, "value": value, "unit": "Mtokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded, generated on device)",
+        "config": {"workload": WORKLOAD, "batch": shape.batch, "seqlen": shape.seqlen,
+                   "nheads": shape.nheads, "headdim": shape.headdim, "dstate": shape.dstate,
+                   "ngroups": shape.ngroups, "chunk": shape.chunk,
+                   "l2": f"rotating {nsets} input/output sets ({nsets * byts / 1e6:.0f} MB > 2x L2)",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+                     "peak_source": peaks["source"],
+                     "scope": "whole ssd_scan_fwd call (all its kernels)",
+                     "tensor_tflops": flops / (ms * 1e-3) / 1e12},
+        "e2e": {"value": shape.tokens / e2e_s / 1e6, "unit": "Mtokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches * args.steps,
+        "clocks": clocks,
+    }
+    line.update(extra)
+    if not args.no_cpu:
+        v, cores, desc = cpu_oracle_sample(shape, target_s=args.cpu_seconds)
+        line["cpu_baseline"] = {"value": v, "unit": "Mtokens/s", "cores": cores,
+                                "kind": "oracle", "sample": desc}
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--quick", action="store_true", help="headline workload only")
+    ap.add_argument("--only", choices=["decode", "long"], default=None,
+                    help="run one secondary workload alone (for profiler captures)")
+    ap.add_argument("--decode-batch", type=int, default=16)
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    if args.only:
+        return run_only(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

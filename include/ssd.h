@@ -1,0 +1,156 @@
+/*
+ * ssd.h -- C ABI of libssd.so, the GB300 (sm_103a) Mamba-2 state-space-duality
+ * (SSD) hot path: the chunked scan for prefill and the single-token state
+ * update for decode.
+ *
+ * Where the operations come from:
+ *   - "Mamba-Family State-Space Model Kernels on a Programmable CGLA",
+ *     section III.A (Mamba-2 layer with three kernel shapes): SSD Step-1 is
+ *     GEMM1 (reduction over the state size N) -> Hadamard mask -> GEMM2
+ *     (reduction over the chunk length Q); Step-3 updates the recurrent state
+ *     h sequentially across chunks, with an input-dependent diagonal
+ *     transition A_c; section III.C: the per-chunk recurrence is an N x d
+ *     product (128 x 64 for Mamba-370M).
+ *   - "Compiler-First State Space Duality and Portable O(1) Autoregressive
+ *     Caching for Inference", abstract: diagonal per-head dynamics,
+ *     fixed-size chunking, and an O(1) cached decode step.
+ *   - "Mambalaya: Einsum-Based Fusion Optimizations on State-Space Models",
+ *     abstract and Figures 4-5: fuse neighbouring Einsums so intermediates
+ *     do not round-trip off-chip memory.
+ *
+ * The recurrence, for each batch row b and head h (group g = h / (H / G)):
+ *     h_t = exp(dt_t * A_h) * h_{t-1} + dt_t * B_t x_t^T      (state N x P)
+ *     y_t = C_t . h_t + D_h * x_t                             (uses updated h)
+ * with h_{-1} = init_state (or zero) and final_state = h_{L-1}.  dt is used
+ * exactly as given (no softplus or bias).
+ *
+ * Layouts (row-major, contiguous, element strides implied by the sizes):
+ *     x, y            [batch][seqlen][nheads][headdim]          in_dtype
+ *     dt              [batch][seqlen][nheads]                    float
+ *     A, D            [nheads]                                   float
+ *     B, C            [batch][seqlen][ngroups][dstate]           in_dtype
+ *     init_state, final_state, decode state
+ *                     [batch][nheads][headdim][dstate]           float
+ * For decode, drop the seqlen dimension.
+ *
+ * Ownership: every pointer is a DEVICE pointer owned by the caller, except
+ * where an entry point says otherwise.  The library allocates no memory;
+ * scratch memory is the caller's workspace, sized by
+ * ssd_scan_workspace_bytes().
+ *
+ * Asynchrony: work is enqueued on `stream` and the call returns without
+ * synchronising.  Argument errors are detected on the host before anything
+ * is enqueued and are returned synchronously.  Device-side faults the kernels
+ * detect themselves (a bounded wait that ran out, a misaligned shared-memory
+ * carve-out) set a device error word read by ssd_last_device_error().
+ *
+ * Aliasing: y and final_state must not overlap any input.  The decode state
+ * is updated in place.
+ */
+#ifndef SSD_GB300_H
+#define SSD_GB300_H
+
+#include <stddef.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    SSD_OK = 0,
+    SSD_ERR_INVALID_ARG = 1,   /* null pointer, size <= 0, H % G != 0, misaligned pointer */
+    SSD_ERR_UNSUPPORTED = 2,   /* a valid shape the requested kernel does not handle */
+    SSD_ERR_CUDA = 3,          /* a CUDA runtime call or launch failed */
+    SSD_ERR_TIMEOUT = 4,       /* a bounded device-side wait ran out (read via ssd_last_device_error) */
+    SSD_ERR_WORKSPACE = 5      /* workspace pointer null or smaller than ssd_scan_workspace_bytes() */
+} ssd_status;
+
+typedef enum { SSD_F32 = 0, SSD_BF16 = 1 } ssd_dtype;
+
+/* Which kernels ssd_scan_fwd_algo uses.  AUTO takes the tensor-core path when
+ * the shape allows it and the SIMT path otherwise; both run on the GPU. */
+typedef enum {
+    SSD_ALGO_AUTO = 0,
+    SSD_ALGO_SIMT = 1,      /* exact-fp32 FFMA chunked scan, any shape */
+    SSD_ALGO_TCGEN05 = 2    /* tcgen05/TMEM/TMA chunked scan: bf16 inputs, headdim 64,
+                               dstate 64 or 128 */
+} ssd_algo;
+
+/* Bytes of device workspace ssd_scan_fwd needs for this shape on the CURRENT
+ * device (the segment plan depends on its SM count).  Returns 0 when the
+ * shape needs none, and (size_t)-1 for invalid sizes. */
+size_t ssd_scan_workspace_bytes(int batch, int seqlen, int nheads, int headdim,
+                                int dstate, int ngroups, int chunk,
+                                ssd_dtype in_dtype);
+
+/* Number of kernel launches ssd_scan_fwd enqueues for this shape on the
+ * current device (for launch accounting and CUDA-graph planning); -1 for
+ * invalid sizes. */
+int ssd_scan_kernel_launches(int batch, int seqlen, int nheads, int headdim,
+                             int dstate, int ngroups, int chunk,
+                             ssd_dtype in_dtype);
+
+/* Prefill: the chunked SSD scan over a whole sequence (section III.A of the
+ * CGLA page: Step-1 intra-chunk dual form, chunk states, Step-3 inter-chunk
+ * recurrence, plus the off-diagonal output and the D skip).
+ *
+ *   x, B, C     in_dtype device arrays (layouts above).
+ *   dt, A       float.  D: float [nheads] or NULL (no skip term).
+ *   chunk       the chunk length Q: one of 16, 32, 64, 128, 256.  The result
+ *               does not depend on Q (the chunked form is an exact
+ *               re-association of the recurrence); the kernels tile the
+ *               sequence in their own block sizes.
+ *   init_state  float [batch][nheads][headdim][dstate] or NULL (zeros).
+ *   y           in_dtype output.  final_state: float output or NULL.
+ *   workspace   device scratch of at least ssd_scan_workspace_bytes() bytes
+ *               (may be NULL when that is 0), 256-byte aligned.
+ * Requirements: all sizes > 0, nheads % ngroups == 0, dstate % 4 == 0,
+ * dstate <= 256, base pointers 16-byte aligned.  seqlen may be any length
+ * (the last block is ragged). */
+ssd_status ssd_scan_fwd(const void *x, const float *dt, const float *A,
+                        const void *B, const void *C, const float *D,
+                        ssd_dtype in_dtype, int batch, int seqlen, int nheads,
+                        int headdim, int dstate, int ngroups, int chunk,
+                        const float *init_state, void *y, float *final_state,
+                        void *workspace, size_t workspace_bytes,
+                        cudaStream_t stream);
+
+/* Same as ssd_scan_fwd with an explicit kernel choice.  SSD_ALGO_TCGEN05
+ * returns SSD_ERR_UNSUPPORTED for shapes it does not handle. */
+ssd_status ssd_scan_fwd_algo(ssd_algo algo, const void *x, const float *dt,
+                             const float *A, const void *B, const void *C,
+                             const float *D, ssd_dtype in_dtype, int batch,
+                             int seqlen, int nheads, int headdim, int dstate,
+                             int ngroups, int chunk, const float *init_state,
+                             void *y, float *final_state, void *workspace,
+                             size_t workspace_bytes, cudaStream_t stream);
+
+/* Decode: one token of the recurrence for every (batch, head), the O(1)
+ * cached step of the compiler-first SSD page.
+ *   state  float [batch][nheads][headdim][dstate], read and updated IN PLACE.
+ *   x      in_dtype [batch][nheads][headdim];  dt float [batch][nheads];
+ *   B, C   in_dtype [batch][ngroups][dstate];  A, D float [nheads] (D may be NULL).
+ *   y      in_dtype [batch][nheads][headdim], computed from the updated state.
+ * A stack of layers can be updated in one call by treating (layer, head) as
+ * the head index and giving every layer its own group (ngroups = layers).
+ * Requirements: sizes > 0, nheads % ngroups == 0, dstate a power of two in
+ * [4, 256], 16-byte aligned state / B / C. */
+ssd_status ssd_state_update(float *state, const void *x, const float *dt,
+                            const float *A, const void *B, const void *C,
+                            const float *D, ssd_dtype in_dtype, int batch,
+                            int nheads, int headdim, int dstate, int ngroups,
+                            void *y, cudaStream_t stream);
+
+/* Human-readable name of a status code (static storage). */
+const char *ssd_status_string(ssd_status s);
+
+/* Reads and clears the device error word on the current device
+ * (synchronises the device).  SSD_OK when no kernel reported a fault. */
+ssd_status ssd_last_device_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SSD_GB300_H */

@@ -1,1 +1,29 @@
-"""GB300-native Mamba-2 SSD hot path (binding filled in below)."""
+"""GB300-native Mamba-2 state-space-duality (SSD) hot path.
+
+A thin ctypes binding over ``libssd.so`` (C ABI in ``include/ssd.h``): it
+checks tensor dtypes and devices, allocates outputs and workspace with torch,
+passes raw device pointers and the current CUDA stream, and turns status codes
+into exceptions.  Every step of the computation runs in the library's CUDA
+kernels; there is no CPU or PyTorch fallback.  If the library is missing or
+cannot load, every call raises.
+
+    y, final = scan_fwd(x, dt, A, B, C, D, chunk=256, init_state=None)
+    y = state_update(state, x, dt, A, B, C, D)          # state updated in place
+"""
+from __future__ import annotations
+
+from ._binding import (  # noqa: F401
+    SsdError,
+    lib_path,
+    load,
+    last_device_error,
+    scan_fwd,
+    scan_fwd_host,
+    scan_kernel_launches,
+    scan_workspace_bytes,
+    state_update,
+    ALGO_AUTO,
+    ALGO_SIMT,
+    ALGO_TCGEN05,
+    EXPORTED_SYMBOLS,
+)

@@ -1,0 +1,249 @@
+"""ctypes binding of libssd.so: argument marshalling only (see include/ssd.h)."""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "_lib", "libssd.so")
+
+EXPORTED_SYMBOLS = (
+    "ssd_scan_workspace_bytes",
+    "ssd_scan_kernel_launches",
+    "ssd_scan_fwd",
+    "ssd_scan_fwd_algo",
+    "ssd_state_update",
+    "ssd_status_string",
+    "ssd_last_device_error",
+)
+
+ALGO_AUTO, ALGO_SIMT, ALGO_TCGEN05 = 0, 1, 2
+_F32, _BF16 = 0, 1
+
+_lock = threading.Lock()
+_lib = None
+
+_vp = ctypes.c_void_p
+_int = ctypes.c_int
+_sz = ctypes.c_size_t
+
+
+class SsdError(RuntimeError):
+    """A libssd.so call returned a non-OK status."""
+
+    def __init__(self, fn, code, msg):
+        super().__init__(f"{fn}: {msg} (status {code})")
+        self.code = code
+
+
+def lib_path() -> str:
+    return _LIB_PATH
+
+
+def load():
+    """Load libssd.so (built in-tree by state_space_model_chunked_gb300.build).
+    Raises if it is missing: there is no fallback path."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(_LIB_PATH):
+            raise ImportError(
+                f"libssd.so not found at {_LIB_PATH}; build it with "
+                "`python -m state_space_model_chunked_gb300.build` (needs nvcc)")
+        lib = ctypes.CDLL(_LIB_PATH)
+        lib.ssd_scan_workspace_bytes.restype = _sz
+        lib.ssd_scan_workspace_bytes.argtypes = [_int] * 7 + [_int]
+        lib.ssd_scan_kernel_launches.restype = _int
+        lib.ssd_scan_kernel_launches.argtypes = [_int] * 7 + [_int]
+        scan_args = [_vp] * 6 + [_int] * 8 + [_vp, _vp, _vp, _vp, _sz, _vp]
+        lib.ssd_scan_fwd.restype = _int
+        lib.ssd_scan_fwd.argtypes = scan_args
+        lib.ssd_scan_fwd_algo.restype = _int
+        lib.ssd_scan_fwd_algo.argtypes = [_int] + scan_args
+        lib.ssd_state_update.restype = _int
+        lib.ssd_state_update.argtypes = [_vp] * 7 + [_int] * 6 + [_vp, _vp]
+        lib.ssd_status_string.restype = ctypes.c_char_p
+        lib.ssd_status_string.argtypes = [_int]
+        lib.ssd_last_device_error.restype = _int
+        lib.ssd_last_device_error.argtypes = []
+        _lib = lib
+        return lib
+
+
+def _check(fn, code):
+    if code != 0:
+        msg = load().ssd_status_string(code).decode()
+        raise SsdError(fn, code, msg)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _dtype_code(t):
+    if t.dtype == torch.float32:
+        return _F32
+    if t.dtype == torch.bfloat16:
+        return _BF16
+    raise TypeError(f"x/B/C must be float32 or bfloat16, got {t.dtype}")
+
+
+def _need(t, name, dtype=None, device=None, shape=None):
+    if t is None:
+        raise ValueError(f"{name} is required")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def scan_workspace_bytes(batch, seqlen, nheads, headdim, dstate, ngroups, chunk,
+                         dtype=torch.bfloat16, device=None):
+    lib = load()
+    code = _BF16 if dtype == torch.bfloat16 else _F32
+    dev = torch.device("cuda") if device is None else torch.device(device)
+    with torch.cuda.device(dev):
+        n = lib.ssd_scan_workspace_bytes(batch, seqlen, nheads, headdim, dstate,
+                                         ngroups, chunk, code)
+    if n == ctypes.c_size_t(-1).value:
+        raise SsdError("ssd_scan_workspace_bytes", 1, "invalid sizes")
+    return int(n)
+
+
+def scan_kernel_launches(batch, seqlen, nheads, headdim, dstate, ngroups, chunk,
+                         dtype=torch.bfloat16, device=None):
+    """Kernels one scan_fwd call enqueues for this shape on the device."""
+    lib = load()
+    code = _BF16 if dtype == torch.bfloat16 else _F32
+    dev = torch.device("cuda") if device is None else torch.device(device)
+    with torch.cuda.device(dev):
+        n = lib.ssd_scan_kernel_launches(batch, seqlen, nheads, headdim, dstate, ngroups,
+                                         chunk, code)
+    if n < 0:
+        raise SsdError("ssd_scan_kernel_launches", 1, "invalid sizes")
+    return int(n)
+
+
+def scan_fwd(x, dt, A, B, C, D=None, chunk=256, init_state=None, *, y=None,
+             final_state=None, workspace=None, algo=ALGO_AUTO, return_final=True):
+    """Chunked SSD scan (prefill).  x [b,L,H,P], dt [b,L,H] f32, A [H] f32,
+    B/C [b,L,G,N] (x's dtype), D [H] f32 or None, init_state [b,H,P,N] f32 or
+    None.  Returns (y, final_state) on x's device and the current stream."""
+    lib = load()
+    _need(x, "x")
+    dev = x.device
+    b, L, H, P = x.shape
+    _need(B, "B", x.dtype, dev)
+    G, N = B.shape[2], B.shape[3]
+    _need(dt, "dt", torch.float32, dev, (b, L, H))
+    _need(A, "A", torch.float32, dev, (H,))
+    _need(B, "B", x.dtype, dev, (b, L, G, N))
+    _need(C, "C", x.dtype, dev, (b, L, G, N))
+    if D is not None:
+        _need(D, "D", torch.float32, dev, (H,))
+    if init_state is not None:
+        _need(init_state, "init_state", torch.float32, dev, (b, H, P, N))
+    if y is None:
+        y = torch.empty_like(x)
+    else:
+        _need(y, "y", x.dtype, dev, x.shape)
+    if final_state is None and return_final:
+        final_state = torch.empty((b, H, P, N), dtype=torch.float32, device=dev)
+    elif final_state is not None:
+        _need(final_state, "final_state", torch.float32, dev, (b, H, P, N))
+    code = _dtype_code(x)
+    with torch.cuda.device(dev):
+        need = lib.ssd_scan_workspace_bytes(b, L, H, P, N, G, chunk, code)
+        if need == ctypes.c_size_t(-1).value:
+            raise SsdError("ssd_scan_workspace_bytes", 1, "invalid sizes")
+        if need > 0 and (workspace is None or workspace.numel() * workspace.element_size() < need):
+            workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+        wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+        stream = torch.cuda.current_stream(dev).cuda_stream
+        rc = lib.ssd_scan_fwd_algo(algo, _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C),
+                                   _ptr(D), code, b, L, H, P, N, G, chunk,
+                                   _ptr(init_state), _ptr(y), _ptr(final_state),
+                                   _ptr(workspace), wbytes, ctypes.c_void_p(stream))
+    _check("ssd_scan_fwd", rc)
+    return y, final_state
+
+
+def scan_fwd_host(x, dt, A, B, C, D=None, chunk=256, init_state=None, *, device="cuda",
+                  staging=None, out=None):
+    """Scan with HOST (CPU) tensors: copies the inputs to the device, runs
+    ssd_scan_fwd there and copies y and the final state back.  ``staging`` (a
+    dict) keeps device buffers between calls; ``out`` = (y_host, final_host)
+    receives the results (pinned for asynchronous copies).  Returns the host
+    (y, final_state) after the stream has finished."""
+    dev = torch.device(device)
+    st = staging if staging is not None else {}
+    host = {"x": x, "dt": dt, "A": A, "B": B, "C": C, "D": D, "init": init_state}
+    devt = {}
+    for k, v in host.items():
+        if v is None:
+            devt[k] = None
+            continue
+        buf = st.get(k)
+        if buf is None or buf.shape != v.shape or buf.dtype != v.dtype:
+            buf = torch.empty(v.shape, dtype=v.dtype, device=dev)
+            st[k] = buf
+        buf.copy_(v, non_blocking=True)
+        devt[k] = buf
+    yd, fd = scan_fwd(devt["x"], devt["dt"], devt["A"], devt["B"], devt["C"], devt["D"],
+                      chunk, devt["init"], y=st.get("y"), final_state=st.get("final"),
+                      workspace=st.get("ws"))
+    st["y"], st["final"] = yd, fd
+    if out is None:
+        out = (torch.empty(yd.shape, dtype=yd.dtype, pin_memory=True),
+               torch.empty(fd.shape, dtype=fd.dtype, pin_memory=True))
+    out[0].copy_(yd, non_blocking=True)
+    out[1].copy_(fd, non_blocking=True)
+    torch.cuda.current_stream(dev).synchronize()
+    return out
+
+
+def state_update(state, x, dt, A, B, C, D=None, *, y=None):
+    """One decode token.  state [b,H,P,N] f32 (updated in place), x [b,H,P],
+    dt [b,H] f32, A [H] f32, B/C [b,G,N] (x's dtype), D [H] f32 or None.
+    Returns y [b,H,P] in x's dtype."""
+    lib = load()
+    _need(state, "state", torch.float32)
+    dev = state.device
+    b, H, P, N = state.shape
+    _need(x, "x", None, dev, (b, H, P))
+    _need(dt, "dt", torch.float32, dev, (b, H))
+    _need(A, "A", torch.float32, dev, (H,))
+    _need(B, "B", x.dtype, dev)
+    G = B.shape[1]
+    _need(B, "B", x.dtype, dev, (b, G, N))
+    _need(C, "C", x.dtype, dev, (b, G, N))
+    if D is not None:
+        _need(D, "D", torch.float32, dev, (H,))
+    if y is None:
+        y = torch.empty_like(x)
+    else:
+        _need(y, "y", x.dtype, dev, (b, H, P))
+    code = _dtype_code(x)
+    with torch.cuda.device(dev):
+        stream = torch.cuda.current_stream(dev).cuda_stream
+        rc = lib.ssd_state_update(_ptr(state), _ptr(x), _ptr(dt), _ptr(A), _ptr(B),
+                                  _ptr(C), _ptr(D), code, b, H, P, N, G, _ptr(y),
+                                  ctypes.c_void_p(stream))
+    _check("ssd_state_update", rc)
+    return y
+
+
+def last_device_error():
+    """Reads and clears the device error word (synchronises the device)."""
+    rc = load().ssd_last_device_error()
+    _check("ssd_last_device_error", rc)

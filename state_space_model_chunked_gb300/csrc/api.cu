@@ -1,0 +1,180 @@
+// C ABI of libssd.so (declarations and contracts: include/ssd.h).
+//
+// This layer validates every argument on the host, picks the kernel path,
+// and enqueues launches on the caller's stream.  It never allocates device
+// memory and never synchronises (except ssd_last_device_error, which must).
+#include <stdint.h>
+#include <stdio.h>
+
+#include "../../include/ssd.h"
+#include "common.cuh"
+#include "launch.h"
+
+namespace {
+
+// One error word per device: kernels report self-detected faults here.
+__device__ unsigned int g_ssd_device_error;
+
+constexpr int kMaxDevices = 64;
+unsigned int *g_err_ptr[kMaxDevices];   // cached device address per device ordinal
+
+unsigned int *device_error_word() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    unsigned int *p = __atomic_load_n(&g_err_ptr[dev], __ATOMIC_ACQUIRE);
+    if (p) return p;
+    void *addr = nullptr;
+    if (cudaGetSymbolAddress(&addr, g_ssd_device_error) != cudaSuccess) return nullptr;
+    __atomic_store_n(&g_err_ptr[dev], (unsigned int *)addr, __ATOMIC_RELEASE);
+    return (unsigned int *)addr;
+}
+
+int current_sm_count() {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    return sms;
+}
+
+bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+bool valid_chunk(int q) {
+    return q == 16 || q == 32 || q == 64 || q == 128 || q == 256;
+}
+
+bool pow2(int v) { return v > 0 && (v & (v - 1)) == 0; }
+
+ssd_status check_scan_args(const void *x, const float *dt, const float *A, const void *B,
+                           const void *C, const float *D, ssd_dtype dtype, int batch,
+                           int L, int H, int P, int N, int G, int chunk,
+                           const float *init, const void *y, const float *fin) {
+    if (!x || !dt || !A || !B || !C || !y) return SSD_ERR_INVALID_ARG;
+    if (dtype != SSD_F32 && dtype != SSD_BF16) return SSD_ERR_INVALID_ARG;
+    if (batch <= 0 || L <= 0 || H <= 0 || P <= 0 || N <= 0 || G <= 0) return SSD_ERR_INVALID_ARG;
+    if (H % G != 0) return SSD_ERR_INVALID_ARG;
+    if (!valid_chunk(chunk)) return SSD_ERR_INVALID_ARG;
+    if (N % 4 != 0 || N > 256) return SSD_ERR_UNSUPPORTED;
+    const void *ptrs[] = {x, dt, A, B, C, D, init, y, fin};
+    for (const void *p : ptrs)
+        if (p && !aligned16(p)) return SSD_ERR_INVALID_ARG;
+    if ((size_t)batch * L * H * P >= ((size_t)1 << 40)) return SSD_ERR_UNSUPPORTED;
+    return SSD_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *ssd_status_string(ssd_status s) {
+    switch (s) {
+        case SSD_OK: return "SSD_OK";
+        case SSD_ERR_INVALID_ARG: return "SSD_ERR_INVALID_ARG: invalid argument";
+        case SSD_ERR_UNSUPPORTED: return "SSD_ERR_UNSUPPORTED: shape not handled by this kernel";
+        case SSD_ERR_CUDA: return "SSD_ERR_CUDA: CUDA runtime or launch failure";
+        case SSD_ERR_TIMEOUT: return "SSD_ERR_TIMEOUT: a bounded device-side wait ran out";
+        case SSD_ERR_WORKSPACE: return "SSD_ERR_WORKSPACE: workspace missing or too small";
+    }
+    return "SSD_ERR_UNKNOWN";
+}
+
+ssd_status ssd_last_device_error(void) {
+    unsigned int *p = device_error_word();
+    if (!p) return SSD_ERR_CUDA;
+    if (cudaDeviceSynchronize() != cudaSuccess) return SSD_ERR_CUDA;
+    unsigned int v = 0;
+    if (cudaMemcpy(&v, p, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) return SSD_ERR_CUDA;
+    const unsigned int zero = 0;
+    if (cudaMemcpy(p, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess) return SSD_ERR_CUDA;
+    if (v == SSD_DEVERR_NONE) return SSD_OK;
+    if (v == SSD_DEVERR_TIMEOUT) return SSD_ERR_TIMEOUT;
+    return SSD_ERR_CUDA;
+}
+
+size_t ssd_scan_workspace_bytes(int batch, int seqlen, int nheads, int headdim, int dstate,
+                                int ngroups, int chunk, ssd_dtype in_dtype) {
+    if (batch <= 0 || seqlen <= 0 || nheads <= 0 || headdim <= 0 || dstate <= 0 ||
+        ngroups <= 0 || nheads % ngroups != 0 || !valid_chunk(chunk))
+        return (size_t)-1;
+    if (in_dtype != SSD_BF16) return 0;
+    const SsdTcPlan plan = ssd_tc_plan(batch, seqlen, nheads, headdim, dstate, ngroups,
+                                       current_sm_count());
+    return plan.supported ? plan.workspace : 0;
+}
+
+int ssd_scan_kernel_launches(int batch, int seqlen, int nheads, int headdim, int dstate,
+                             int ngroups, int chunk, ssd_dtype in_dtype) {
+    if (batch <= 0 || seqlen <= 0 || nheads <= 0 || headdim <= 0 || dstate <= 0 ||
+        ngroups <= 0 || nheads % ngroups != 0 || !valid_chunk(chunk))
+        return -1;
+    if (in_dtype != SSD_BF16) return 1;
+    const SsdTcPlan plan = ssd_tc_plan(batch, seqlen, nheads, headdim, dstate, ngroups,
+                                       current_sm_count());
+    return plan.supported ? plan.launches : 1;
+}
+
+ssd_status ssd_scan_fwd_algo(ssd_algo algo, const void *x, const float *dt, const float *A,
+                             const void *B, const void *C, const float *D,
+                             ssd_dtype in_dtype, int batch, int seqlen, int nheads,
+                             int headdim, int dstate, int ngroups, int chunk,
+                             const float *init_state, void *y, float *final_state,
+                             void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+    ssd_status st = check_scan_args(x, dt, A, B, C, D, in_dtype, batch, seqlen, nheads,
+                                    headdim, dstate, ngroups, chunk, init_state, y,
+                                    final_state);
+    if (st != SSD_OK) return st;
+    if (algo != SSD_ALGO_AUTO && algo != SSD_ALGO_SIMT && algo != SSD_ALGO_TCGEN05)
+        return SSD_ERR_INVALID_ARG;
+    const bool bf16 = in_dtype == SSD_BF16;
+    bool use_tc = false;
+    SsdTcPlan plan{};
+    if (algo != SSD_ALGO_SIMT && bf16) {
+        plan = ssd_tc_plan(batch, seqlen, nheads, headdim, dstate, ngroups, current_sm_count());
+        use_tc = plan.supported;
+    }
+    if (algo == SSD_ALGO_TCGEN05 && !use_tc) return SSD_ERR_UNSUPPORTED;
+    cudaError_t e;
+    if (use_tc) {
+        if (plan.workspace > 0) {
+            if (!workspace || workspace_bytes < plan.workspace) return SSD_ERR_WORKSPACE;
+            if (((uintptr_t)workspace & 255u) != 0) return SSD_ERR_INVALID_ARG;
+        }
+        e = ssd_launch_scan_tc(plan, x, dt, A, B, C, D, init_state, y, final_state, batch,
+                               seqlen, nheads, headdim, dstate, ngroups, workspace,
+                               device_error_word(), stream);
+    } else {
+        e = ssd_launch_scan_simt(x, dt, A, B, C, D, init_state, y, final_state, bf16, batch,
+                                 seqlen, nheads, headdim, dstate, ngroups, stream);
+    }
+    return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+}
+
+ssd_status ssd_scan_fwd(const void *x, const float *dt, const float *A, const void *B,
+                        const void *C, const float *D, ssd_dtype in_dtype, int batch,
+                        int seqlen, int nheads, int headdim, int dstate, int ngroups,
+                        int chunk, const float *init_state, void *y, float *final_state,
+                        void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+    return ssd_scan_fwd_algo(SSD_ALGO_AUTO, x, dt, A, B, C, D, in_dtype, batch, seqlen,
+                             nheads, headdim, dstate, ngroups, chunk, init_state, y,
+                             final_state, workspace, workspace_bytes, stream);
+}
+
+ssd_status ssd_state_update(float *state, const void *x, const float *dt, const float *A,
+                            const void *B, const void *C, const float *D, ssd_dtype in_dtype,
+                            int batch, int nheads, int headdim, int dstate, int ngroups,
+                            void *y, cudaStream_t stream) {
+    if (!state || !x || !dt || !A || !B || !C || !y) return SSD_ERR_INVALID_ARG;
+    if (in_dtype != SSD_F32 && in_dtype != SSD_BF16) return SSD_ERR_INVALID_ARG;
+    if (batch <= 0 || nheads <= 0 || headdim <= 0 || dstate <= 0 || ngroups <= 0)
+        return SSD_ERR_INVALID_ARG;
+    if (nheads % ngroups != 0) return SSD_ERR_INVALID_ARG;
+    if (!pow2(dstate) || dstate < 4 || dstate > 256) return SSD_ERR_UNSUPPORTED;
+    const void *ptrs[] = {state, x, dt, A, B, C, D, y};
+    for (const void *p : ptrs)
+        if (p && !aligned16(p)) return SSD_ERR_INVALID_ARG;
+    if ((size_t)batch * nheads >= ((size_t)1 << 31)) return SSD_ERR_UNSUPPORTED;
+    cudaError_t e = ssd_launch_decode(state, x, dt, A, B, C, D, y, in_dtype == SSD_BF16, batch,
+                                      nheads, headdim, dstate, ngroups, stream);
+    return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,38 @@
+// Internal launchers behind the C ABI (include/ssd.h).  Arguments are
+// validated by the ABI layer before any of these is called.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+
+cudaError_t ssd_launch_decode(float *state, const void *x, const float *dt,
+                              const float *A, const void *B, const void *C,
+                              const float *D, void *y, bool bf16, int batch,
+                              int H, int P, int N, int G, cudaStream_t stream);
+
+size_t ssd_simt_smem_bytes(int N);
+
+cudaError_t ssd_launch_scan_simt(const void *x, const float *dt, const float *A,
+                                 const void *B, const void *C, const float *D,
+                                 const float *init, void *y, float *fin, bool bf16,
+                                 int batch, int L, int H, int P, int N, int G,
+                                 cudaStream_t stream);
+
+// Tensor-core (tcgen05/TMEM/TMA) chunked scan.
+struct SsdTcPlan {
+    bool supported;
+    int tiles;            // 128-token tiles per sequence (last may be ragged)
+    int heads_per_cta;    // heads sharing one C.B^T product
+    int seg_tiles;        // tiles per segment (the unit of sequence parallelism)
+    int nseg;             // segments per sequence
+    size_t workspace;     // bytes of workspace required
+    int launches;         // kernels enqueued per call
+};
+
+SsdTcPlan ssd_tc_plan(int batch, int L, int H, int P, int N, int G, int num_sms);
+
+cudaError_t ssd_launch_scan_tc(const SsdTcPlan &plan, const void *x, const float *dt,
+                               const float *A, const void *B, const void *C,
+                               const float *D, const float *init, void *y, float *fin,
+                               int batch, int L, int H, int P, int N, int G,
+                               void *workspace, unsigned int *err, cudaStream_t stream);

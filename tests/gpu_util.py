@@ -1,0 +1,41 @@
+"""Helpers shared by the GPU parity tests: move seeded numpy inputs to the
+device in the dtype the workload names, and compare with the oracle."""
+import numpy as np
+import torch
+
+import oracle
+
+TOL = {"f32": 1e-4, "bf16": 1e-2}   # relative L2 bars: fp32 / bf16-input workloads
+
+
+def dev(a, dtype="f32"):
+    """numpy float32 -> CUDA tensor; bf16 values are exactly representable so
+    the conversion is exact."""
+    if a is None:
+        return None
+    t = torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32))
+    if dtype == "bf16":
+        t = t.to(torch.bfloat16)
+    return t.cuda()
+
+
+def host(t):
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+def scan_on_gpu(inp, dtype, chunk, algo=0):
+    import state_space_model_chunked_gb300 as ssd
+    y, fin = ssd.scan_fwd(dev(inp["x"], dtype), dev(inp["dt"]), dev(inp["A"]),
+                          dev(inp["B"], dtype), dev(inp["C"], dtype), dev(inp["D"]),
+                          chunk, dev(inp["init"]), algo=algo)
+    torch.cuda.synchronize()
+    return host(y), host(fin)
+
+
+def scan_oracle(inp):
+    return oracle.scan_seq(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"],
+                           inp["D"], inp["init"])
+
+
+def rel(a, b):
+    return oracle.rel_l2(a, b)

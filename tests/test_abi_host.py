@@ -1,0 +1,124 @@
+"""Host-side checks of the C ABI (no GPU needed): the library builds and loads,
+exports every function include/ssd.h declares, and rejects bad arguments
+before enqueuing anything."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import state_space_model_chunked_gb300 as ssd
+from state_space_model_chunked_gb300 import build as ssd_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ssd.h")
+
+OK, INVALID, UNSUPPORTED = 0, 1, 2
+
+
+@pytest.fixture(scope="module")
+def lib():
+    ssd_build.build()
+    return ssd.load()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"\b(ssd_[a-z_0-9]+)\s*\(", text)
+    return sorted(set(names))
+
+
+def test_header_declares_the_binding_symbols():
+    assert sorted(ssd.EXPORTED_SYMBOLS) == _declared_functions()
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), f"libssd.so does not export {name}"
+
+
+def test_status_strings(lib):
+    for code in range(6):
+        s = lib.ssd_status_string(code).decode()
+        assert s.startswith("SSD_")
+    assert "UNKNOWN" in lib.ssd_status_string(99).decode()
+
+
+def _fake(addr):
+    return ctypes.c_void_p(addr)
+
+
+def _scan(lib, **kw):
+    a = dict(x=_fake(0x1000), dt=_fake(0x2000), A=_fake(0x3000), B=_fake(0x4000),
+             C=_fake(0x5000), D=None, dtype=1, b=1, L=256, H=4, P=64, N=64, G=1, Q=64,
+             init=None, y=_fake(0x6000), fin=None, ws=None, wsb=0, stream=None)
+    a.update(kw)
+    return lib.ssd_scan_fwd(a["x"], a["dt"], a["A"], a["B"], a["C"], a["D"], a["dtype"],
+                            a["b"], a["L"], a["H"], a["P"], a["N"], a["G"], a["Q"],
+                            a["init"], a["y"], a["fin"], a["ws"], a["wsb"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(x=None), INVALID),
+    (dict(dt=None), INVALID),
+    (dict(y=None), INVALID),
+    (dict(b=0), INVALID),
+    (dict(L=-3), INVALID),
+    (dict(H=6, G=4), INVALID),          # heads not a multiple of groups
+    (dict(Q=48), INVALID),              # chunk not in {16,32,64,128,256}
+    (dict(dtype=7), INVALID),
+    (dict(x=_fake(0x1008)), INVALID),   # 8-byte aligned only
+    (dict(fin=_fake(0x7004)), INVALID),
+    (dict(N=66), UNSUPPORTED),          # dstate not a multiple of 4
+    (dict(N=512), UNSUPPORTED),
+])
+def test_scan_rejects_bad_arguments(lib, kw, expect):
+    assert _scan(lib, **kw) == expect
+
+
+def test_scan_algo_rejects_unknown_algo(lib):
+    a = [_fake(0x1000), _fake(0x2000), _fake(0x3000), _fake(0x4000), _fake(0x5000), None,
+         1, 1, 256, 4, 64, 64, 1, 64, None, _fake(0x6000), None, None, 0, None]
+    assert lib.ssd_scan_fwd_algo(9, *a) == INVALID
+
+
+def _dec(lib, **kw):
+    a = dict(state=_fake(0x1000), x=_fake(0x2000), dt=_fake(0x3000), A=_fake(0x4000),
+             B=_fake(0x5000), C=_fake(0x6000), D=None, dtype=1, b=2, H=4, P=16, N=16, G=1,
+             y=_fake(0x7000), stream=None)
+    a.update(kw)
+    return lib.ssd_state_update(a["state"], a["x"], a["dt"], a["A"], a["B"], a["C"], a["D"],
+                                a["dtype"], a["b"], a["H"], a["P"], a["N"], a["G"], a["y"],
+                                a["stream"])
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(state=None), INVALID),
+    (dict(C=None), INVALID),
+    (dict(H=0), INVALID),
+    (dict(H=5, G=2), INVALID),
+    (dict(B=_fake(0x5004)), INVALID),
+    (dict(N=24), UNSUPPORTED),          # not a power of two
+    (dict(N=512), UNSUPPORTED),
+    (dict(N=2), UNSUPPORTED),
+])
+def test_decode_rejects_bad_arguments(lib, kw, expect):
+    assert _dec(lib, **kw) == expect
+
+
+def test_workspace_query_rejects_bad_sizes(lib):
+    bad = ctypes.c_size_t(-1).value
+    assert lib.ssd_scan_workspace_bytes(0, 256, 4, 64, 64, 1, 64, 1) == bad
+    assert lib.ssd_scan_workspace_bytes(1, 256, 6, 64, 64, 4, 64, 1) == bad
+    assert lib.ssd_scan_workspace_bytes(1, 256, 4, 64, 64, 1, 100, 1) == bad
+    # the fp32 path needs no workspace
+    assert lib.ssd_scan_workspace_bytes(1, 256, 4, 64, 64, 1, 64, 0) == 0
+
+
+def test_binding_refuses_cpu_tensors():
+    import torch
+    x = torch.zeros(1, 4, 2, 8)
+    with pytest.raises((ValueError, ImportError)):
+        ssd.scan_fwd(x, torch.zeros(1, 4, 2), torch.zeros(2), torch.zeros(1, 4, 1, 8),
+                     torch.zeros(1, 4, 1, 8))

@@ -1,0 +1,63 @@
+"""GPU parity of the chunked SSD scan (ssd_scan_fwd) against the fp64 oracle,
+through the C ABI: every kernel path, the workloads' shapes, ragged and
+degenerate edges."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from state_space_model_chunked_gb300 import inputs as gen
+from tests.gpu_util import TOL, dev, host, rel, scan_on_gpu, scan_oracle
+
+pytestmark = pytest.mark.gpu
+
+AUTO, SIMT, TC = 0, 1, 2
+
+
+def _check(inp, dtype, chunk, algo, tol=None):
+    y, f = scan_on_gpu(inp, dtype, chunk, algo)
+    yr, fr = scan_oracle(inp)
+    tol = TOL[dtype] if tol is None else tol
+    ey, ef = rel(y, yr), rel(f, fr)
+    assert ey <= tol and ef <= tol, (ey, ef)
+    return ey, ef
+
+
+def test_fp32_workload_L256_H4_P64_N64():
+    s = gen.SCAN_SHAPES["ssd_fp32_L256_H4_P64_N64"]
+    inp = gen.scan_inputs_for(s, seed=0)
+    _check(inp, "f32", s.chunk, AUTO)
+
+
+@pytest.mark.parametrize("b,L,H,P,N,G", [
+    (1, 1, 1, 16, 16, 1),        # one token
+    (2, 200, 3, 16, 16, 1),      # ragged last tile
+    (1, 130, 6, 20, 32, 3),      # ragged state-row block, several groups
+    (3, 64, 4, 64, 64, 2),
+    (1, 257, 2, 64, 128, 1),
+    (1, 96, 2, 8, 256, 1),       # widest supported state
+])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("with_init", [False, True])
+def test_simt_path_shapes(b, L, H, P, N, G, dtype, with_init):
+    inp = gen.scan_inputs(b, L, H, P, N, G, dtype, seed=L + N + b, random_init=with_init)
+    _check(inp, dtype, 64, SIMT)
+
+
+def test_simt_without_skip_term():
+    inp = gen.scan_inputs(2, 100, 4, 32, 64, 2, "f32", seed=8, with_D=False)
+    _check(inp, "f32", 32, SIMT)
+
+
+@pytest.mark.parametrize("name", ["mamba2_130m_L4096", "mamba2_370m_b8_L2048"])
+def test_prefill_workloads_full(name):
+    s = gen.SCAN_SHAPES[name]
+    inp = gen.scan_inputs_for(s, seed=0)
+    _check(inp, s.dtype, s.chunk, AUTO)
+
+
+def test_chunk_parameter_does_not_change_result():
+    inp = gen.scan_inputs(1, 512, 4, 64, 128, 1, "bf16", seed=12, random_init=True)
+    outs = [scan_on_gpu(inp, "bf16", q, AUTO) for q in (16, 64, 256)]
+    for y, f in outs[1:]:
+        assert rel(y, outs[0][0]) <= 1e-2 and rel(f, outs[0][1]) <= 1e-2
