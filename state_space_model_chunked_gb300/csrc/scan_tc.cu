@@ -1,7 +1,844 @@
-// placeholder: tensor-core path not built yet
+// Tensor-core chunked SSD scan for sm_103a (tcgen05 + TMEM + TMA).
+//
+// The chunk steps follow "Mamba-Family State-Space Model Kernels on a
+// Programmable CGLA", section III.A: Step-1 inside a chunk is GEMM1 (C.B^T,
+// reduction over the state size N) -> Hadamard decay mask -> GEMM2
+// (reduction over the chunk); Step-3 carries the N x P state across chunks.
+// Section IV.B of the same page names the boundary between the mask and
+// GEMM2 as the overhead that fusion should remove, and the Mambalaya page
+// (Figures 4-5: RI and RSb fusion) fuses Einsums that share an iteration
+// space or drop a rank.  Here every step of a 128-token tile stays on chip:
+//
+//   G     = C . B^T                (tcgen05, smem x smem -> TMEM fp32)
+//   M     = G o exp(a_t - a_s) dt_s, s <= t, plus D on the diagonal
+//                                  (TMEM -> registers -> TMEM as bf16, in place)
+//   Yd    = M . X                  (tcgen05 with A read from TMEM)
+//   Yo    = C . H_prev^T           (off-diagonal term from the entering state)
+//   H    <- exp(a_end) H + B^T . (w o X),  w_s = exp(a_end - a_s) dt_s
+//   y     = Yd + exp(a_t) Yo       (epilogue, bf16 store)
+//
+// The D skip is folded into the mask diagonal (M[t][t] += D): the skip is the
+// s = t term of the same contraction.  Exponents are always differences or
+// non-positive partial sums; the mask uses exp(a_t + u_s) with
+// u_s = log(dt_s) - a_s, which needs dt >= 0 (a time step).
+//
+// Parallelism over the sequence: a segment is a run of consecutive tiles
+// handled by one CTA with the state carried in TMEM.  When a sequence has more
+// than one segment, a first kernel computes each segment's own state
+// contribution F (tiles walked backwards so the decay to the segment end is a
+// running sum), a small kernel chains them into every segment's entering
+// state, and the scan kernel starts each segment from it.  Heads that share a
+// group (ngroups divides nheads) are paired in one CTA so C.B^T is computed
+// once for both.
+//
+// Warp roles (320 threads): warp 0 issues TMA loads, warp 1 allocates TMEM and
+// issues tcgen05.mma from one thread, warps 2-9 (two warpgroups) do the
+// cumsum, the mask, the state bookkeeping and the epilogue.  Every wait is on
+// an mbarrier with a time limit; a wait that runs out sets the device error
+// word and the CTA fast-forwards to its exit without further loads or stores.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "common.cuh"
 #include "launch.h"
-SsdTcPlan ssd_tc_plan(int, int, int, int, int, int, int) { SsdTcPlan p{}; p.supported = false; p.launches = 1; return p; }
-cudaError_t ssd_launch_scan_tc(const SsdTcPlan &, const void *, const float *, const float *,
-                               const void *, const void *, const float *, const float *, void *,
-                               float *, int, int, int, int, int, int, void *, unsigned int *,
-                               cudaStream_t) { return cudaErrorNotSupported; }
+#include "ptx.cuh"
+
+using namespace ssdptx;
+
+namespace {
+
+constexpr int kTile = 128;                 // tokens per tile
+constexpr int kP = 64;                     // headdim handled by this path
+constexpr int kN = 128;                    // dstate handled by this path
+constexpr int kXWarps = 8;                 // transform/epilogue warps
+constexpr int kThreads = 64 + 32 * kXWarps;
+constexpr uint64_t kWaitNs = 2000000000ull;
+
+constexpr uint32_t kBlk = 16384;           // 128 rows x 128 bytes, 128B-swizzled
+constexpr uint32_t kCBytes = 2 * kBlk;     // C tile: 128 tokens x 128 n
+constexpr uint32_t kBBytes = 2 * kBlk;     // B tile
+constexpr uint32_t kXBytes = kBlk;         // X tile: 128 tokens x 64 p
+constexpr uint32_t kHbBytes = 16384;       // bf16 entering state, 64 p x 128 n
+constexpr uint32_t kCtrl = 3072;           // barriers and per-tile scalars
+
+// TMEM columns of the scan kernel
+constexpr uint32_t kColG = 0;              // G, then M for both heads in place
+constexpr uint32_t kColYd = 128;           // + 64 h : intra-chunk output
+constexpr uint32_t kColYo = 256;           // + 64 h : off-diagonal output
+constexpr uint32_t kColH = 384;            // + 64 h : carried state (lane = n, column = p)
+
+constexpr uint32_t kIdG = idesc_bf16_f32(128, 128, false, false);   // C . B^T
+constexpr uint32_t kIdOff = idesc_bf16_f32(128, 64, false, false);  // C . Hb^T
+constexpr uint32_t kIdS = idesc_bf16_f32(128, 64, true, true);      // B^T . Xt
+constexpr uint32_t kIdY = idesc_bf16_f32(128, 64, false, true);     // M(TMEM) . X
+
+// control-region offsets (bytes)
+constexpr uint32_t kOffTslot = 128;
+constexpr uint32_t kOffAbort = 132;
+constexpr uint32_t kOffAend = 160;        // float[2]
+constexpr uint32_t kOffWtot = 192;        // float[2 warpgroups][4]
+constexpr uint32_t kOffU = 256;           // float[2][128]: log(dt_s) - a_s
+constexpr uint32_t kOffA = 1280;          // float[2][128]: a_t
+
+struct TcArgs {
+    const float *dt, *A, *D, *init;
+    float *ws_state;       // [b][nseg-1][H][P][N]: segment contributions, then entering states
+    float *ws_decay;       // [b][nseg-1][H]: segment total decay
+    __nv_bfloat16 *y;
+    float *fin;
+    unsigned int *err;
+    int L, H, G, tiles, seg_tiles, nseg;
+};
+
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                         unsigned int *err) {
+    if (*abort_flag) return false;
+    if (mbar_wait(bar, parity, kWaitNs)) return true;
+    *abort_flag = 1;
+    ssd_report(err, SSD_DEVERR_TIMEOUT);
+    return false;
+}
+
+// Warp-uniform wait (every lane polls; the warp proceeds only if all saw it).
+__device__ __forceinline__ bool wait_bar_warp(uint32_t bar, uint32_t parity,
+                                              volatile int *abort_flag, unsigned int *err) {
+    const bool ok = wait_bar(bar, parity, abort_flag, err);
+    return __all_sync(0xffffffffu, ok);
+}
+
+// Byte offset of element (row, col) in a 128-byte-swizzled tile whose rows are
+// 64 bf16 wide (row r of an 8-row, 1024-byte atom; 16-byte chunk c lands at
+// c ^ (r % 8)).
+__device__ __forceinline__ uint32_t sw128(uint32_t row, uint32_t col) {
+    return (row >> 3) * 1024u + (row & 7u) * 128u + ((((col >> 3) ^ row) & 7u) << 4) +
+           (col & 7u) * 2u;
+}
+
+__device__ __forceinline__ uint4 scale_bf16x8(uint4 v, float w) {
+    uint32_t in[4] = {v.x, v.y, v.z, v.w};
+    uint32_t out[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float lo = __uint_as_float(in[i] << 16) * w;
+        const float hi = __uint_as_float(in[i] & 0xffff0000u) * w;
+        out[i] = pack_bf16x2(lo, hi);
+    }
+    return make_uint4(out[0], out[1], out[2], out[3]);
+}
+
+// Chunk-local inclusive cumulative sum of dt*A over the 128 tokens of a tile,
+// computed by one warpgroup (thread = token).  Returns a_t; *aend = a_127.
+__device__ __forceinline__ float tile_cumsum(float v, int q, int lane, float *wtot, int bar_id,
+                                             float *aend) {
+    float incl = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const float o = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += o;
+    }
+    if (lane == 31) wtot[q] = incl;
+    named_bar_sync(bar_id, 128);
+    float pre = 0.f;
+    for (int j = 0; j < q; ++j) pre += wtot[j];
+    *aend = ((wtot[0] + wtot[1]) + wtot[2]) + wtot[3];
+    return pre + incl;
+}
+
+// ============================================================ scan kernel
+template <int HG>
+__global__ void __launch_bounds__(kThreads, 1)
+ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
+                   const __grid_constant__ CUtensorMap mapB,
+                   const __grid_constant__ CUtensorMap mapX, const TcArgs a) {
+    extern __shared__ __align__(1024) uint8_t smem[];
+    constexpr uint32_t kStage = kCBytes + kBBytes + HG * kXBytes;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int h0 = blockIdx.x * HG;
+    const int sigma = blockIdx.y;
+    const int b = blockIdx.z;
+    const int g = h0 / (a.H / a.G);
+    const int k0 = sigma * a.seg_tiles;
+    const int k1 = min(a.tiles, k0 + a.seg_tiles);
+    const int ntile = k1 - k0;
+
+    const uint32_t sbase = smem_u32(smem);
+    if ((sbase & 1023u) != 0u) {
+        if (threadIdx.x == 0) ssd_report(a.err, SSD_DEVERR_SMEM_ALIGN);
+        return;
+    }
+    // barriers: 0,1 full[stage]; 2,3 empty[stage]; 4 g_full; 5 m_ready;
+    //           6 hx_ready; 7 hx_free; 8 y_full; 9 y_free
+    auto bar = [&](int i) { return sbase + 8u * (uint32_t)i; };
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + kOffTslot);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kOffAbort);
+    float *aend_s = reinterpret_cast<float *>(smem + kOffAend);
+    float *wtot_s = reinterpret_cast<float *>(smem + kOffWtot);
+    float *u_s = reinterpret_cast<float *>(smem + kOffU);
+    float *a_s = reinterpret_cast<float *>(smem + kOffA);
+    const uint32_t tiles_base = sbase + kCtrl;
+    const uint32_t hb_base = tiles_base + 2 * kStage;
+    const uint32_t xt_base = hb_base + kHbBytes;
+    uint8_t *tiles_ptr = smem + kCtrl;
+    uint8_t *hb_ptr = tiles_ptr + 2 * kStage;
+    uint8_t *xt_ptr = hb_ptr + kHbBytes;
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar(0), 1);
+        mbar_init(bar(1), 1);
+        mbar_init(bar(2), 1);
+        mbar_init(bar(3), 1);
+        mbar_init(bar(4), 1);
+        mbar_init(bar(5), kXWarps);
+        mbar_init(bar(6), kXWarps);
+        mbar_init(bar(7), 1);
+        mbar_init(bar(8), 1);
+        mbar_init(bar(9), kXWarps);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tslot), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            tma_prefetch_desc(&mapC);
+            tma_prefetch_desc(&mapB);
+            tma_prefetch_desc(&mapX);
+            for (int it = 0; it < ntile; ++it) {
+                const int stage = it & 1;
+                if (it >= 2 && !wait_bar(bar(2 + stage), ((it >> 1) - 1) & 1, abort_flag, a.err))
+                    break;
+                const uint32_t stg = tiles_base + stage * kStage;
+                const int t0 = (k0 + it) * kTile;
+                mbar_arrive_expect_tx(bar(stage), kStage);
+                tma_load_4d(stg, &mapC, bar(stage), 0, g, t0, b);
+                tma_load_4d(stg + kBlk, &mapC, bar(stage), 64, g, t0, b);
+                tma_load_4d(stg + kCBytes, &mapB, bar(stage), 0, g, t0, b);
+                tma_load_4d(stg + kCBytes + kBlk, &mapB, bar(stage), 64, g, t0, b);
+#pragma unroll
+                for (int h = 0; h < HG; ++h)
+                    tma_load_4d(stg + kCBytes + kBBytes + h * kXBytes, &mapX, bar(stage), 0,
+                                h0 + h, t0, b);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            int hs = 0;
+            for (int it = 0; it < ntile; ++it) {
+                const int stage = it & 1;
+                const uint32_t stg = tiles_base + stage * kStage;
+                if (!wait_bar(bar(stage), (it >> 1) & 1, abort_flag, a.err)) break;
+                tc_fence_after();
+                // G = C . B^T  (M = 128 tokens t, N = 128 tokens s, K = 128 n)
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t koff = (kk >> 2) * kBlk + (kk & 3) * 32;
+                    mma_ss(tmem + kColG, smem_desc(stg + koff, 16, 1024, kSwizzle128B),
+                           smem_desc(stg + kCBytes + koff, 16, 1024, kSwizzle128B), kIdG, kk > 0);
+                }
+                mma_commit(bar(4));
+                for (int h = 0; h < HG; ++h) {
+                    if (h == 1) {
+                        // intra-chunk outputs once the mask is in TMEM
+                        if (!wait_bar(bar(5), it & 1, abort_flag, a.err)) break;
+                        tc_fence_after();
+                        for (int hh = 0; hh < HG; ++hh) {
+#pragma unroll
+                            for (int kk = 0; kk < 8; ++kk) {
+                                const uint32_t acol =
+                                    kColG + 32 * (kk >> 1) + 16 * hh + 8 * (kk & 1);
+                                mma_ts(tmem + kColYd + 64 * hh, tmem + acol,
+                                       smem_desc(stg + kCBytes + kBBytes + hh * kXBytes + kk * 2048,
+                                                 kBlk, 1024, kSwizzle128B),
+                                       kIdY, kk > 0);
+                            }
+                        }
+                    }
+                    if (!wait_bar(bar(6), hs & 1, abort_flag, a.err)) break;
+                    if (h == 0 && it > 0 && !wait_bar(bar(9), (it - 1) & 1, abort_flag, a.err))
+                        break;
+                    tc_fence_after();
+                    // Yo_h = C . Hb^T  (off-diagonal term from the entering state)
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint32_t koff = (kk >> 2) * kBlk + (kk & 3) * 32;
+                        const uint32_t hoff = (kk >> 2) * 8192 + (kk & 3) * 32;
+                        mma_ss(tmem + kColYo + 64 * h, smem_desc(stg + koff, 16, 1024, kSwizzle128B),
+                               smem_desc(hb_base + hoff, 16, 1024, kSwizzle128B), kIdOff, kk > 0);
+                    }
+                    // H_h += B^T . Xt_h  (chunk state added to the decayed state)
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        mma_ss(tmem + kColH + 64 * h,
+                               smem_desc(stg + kCBytes + kk * 2048, kBlk, 1024, kSwizzle128B),
+                               smem_desc(xt_base + kk * 2048, kBlk, 1024, kSwizzle128B), kIdS, 1);
+                    }
+                    mma_commit(bar(7));
+                    ++hs;
+                }
+                if (*abort_flag) break;
+                if (HG == 1) {
+                    if (!wait_bar(bar(5), it & 1, abort_flag, a.err)) break;
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint32_t acol = kColG + 32 * (kk >> 1) + 8 * (kk & 1);
+                        mma_ts(tmem + kColYd, tmem + acol,
+                               smem_desc(stg + kCBytes + kBBytes + kk * 2048, kBlk, 1024,
+                                         kSwizzle128B),
+                               kIdY, kk > 0);
+                    }
+                }
+                mma_commit(bar(2 + stage));
+                mma_commit(bar(8));
+            }
+        }
+    } else {
+        // ------------------------------------------- transform / epilogue
+        const int tw = warp - 2;
+        const int wg = tw >> 2;               // warpgroup
+        const int q = warp & 3;               // TMEM lane quarter
+        const int row = 32 * q + lane;        // token t (or state index n) of this thread
+        const uint32_t tq = tmem + ((uint32_t)(32 * q) << 16);
+        const int hown = wg % HG;             // head whose cumsum this warpgroup computes
+        const float A_own = a.A[h0 + hown];
+        float Dh[HG];
+#pragma unroll
+        for (int h = 0; h < HG; ++h) Dh[h] = a.D ? a.D[h0 + h] : 0.f;
+        int hs = 0;
+        for (int it = 0; it < ntile; ++it) {
+            const int t0 = (k0 + it) * kTile;
+            const int stage = it & 1;
+            const uint8_t *stg_ptr = tiles_ptr + stage * kStage;
+            // ---- chunk-local cumsum of dt*A
+            named_bar_sync(3, 32 * kXWarps);
+            const int tok = t0 + row;
+            float dtv = 0.f;
+            if (tok < a.L) dtv = a.dt[((size_t)b * a.L + tok) * a.H + h0 + hown];
+            float aend;
+            const float at =
+                tile_cumsum(dtv * A_own, q, lane, wtot_s + 4 * wg, 1 + wg, &aend);
+            const float e_at = __expf(at);
+            if (wg < HG) {
+                u_s[hown * kTile + row] = dtv > 0.f ? __logf(dtv) - at : -INFINITY;
+                a_s[hown * kTile + row] = at;
+                if (row == 0) aend_s[hown] = aend;
+            }
+            named_bar_sync(3, 32 * kXWarps);
+
+            // ---- entering state -> bf16 operand; state scaled by the tile decay;
+            //      w o X operand.  One head at a time (the operand buffers are shared).
+            auto prep_head = [&](int h) {
+                if (hs > 0) wait_bar_warp(bar(7), (hs - 1) & 1, abort_flag, a.err);
+                tc_fence_after();
+                const float de = __expf(aend_s[h]);
+                const uint32_t colH = kColH + 64 * h + 32 * wg;
+                uint32_t r[32];
+                if (it == 0) {
+                    const float *src =
+                        sigma == 0 ? (a.init ? a.init + ((size_t)b * a.H + h0 + h) * kP * kN
+                                             : nullptr)
+                                   : a.ws_state +
+                                         (((size_t)b * (a.nseg - 1) + sigma - 1) * a.H + h0 + h) *
+                                             kP * kN;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        r[j] = __float_as_uint(src ? src[(size_t)(32 * wg + j) * kN + row] : 0.f);
+                } else {
+                    tmem_ld32(tq + colH, r);
+                    tmem_ld_wait();
+                }
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const int p = 32 * wg + j;
+                    const float v = __uint_as_float(r[j]);
+                    *reinterpret_cast<__nv_bfloat16 *>(hb_ptr + (row >> 6) * 8192 +
+                                                       sw128(p, row & 63)) = __float2bfloat16_rn(v);
+                    r[j] = __float_as_uint(v * de);
+                }
+                tmem_st32(tq + colH, r);
+                // Xt = w o X for this thread's token row, this warpgroup's 32 columns
+                const float w = __expf(aend_s[h] + u_s[h * kTile + row]);
+                const uint8_t *xs = stg_ptr + kCBytes + kBBytes + h * kXBytes;
+#pragma unroll
+                for (int c = 4 * wg; c < 4 * wg + 4; ++c) {
+                    const uint32_t off = sw128(row, 8 * c);
+                    const uint4 v = *reinterpret_cast<const uint4 *>(xs + off);
+                    *reinterpret_cast<uint4 *>(xt_ptr + off) = scale_bf16x8(v, w);
+                }
+                fence_proxy_async_smem();
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(6));
+                ++hs;
+            };
+
+            wait_bar_warp(bar(stage), (it >> 1) & 1, abort_flag, a.err);   // X tile landed
+            prep_head(0);
+
+            // ---- mask: M = G o exp(a_t - a_s) dt_s (s <= t) + D on the diagonal
+            wait_bar_warp(bar(4), it & 1, abort_flag, a.err);
+            tc_fence_after();
+#pragma unroll 1
+            for (int jj = 0; jj < 2; ++jj) {
+                const int j = 2 * wg + jj;            // 32-token column chunk
+                uint32_t gr[32];
+                tmem_ld32(tq + kColG + 32 * j, gr);
+                tmem_ld_wait();
+#pragma unroll
+                for (int hh = 0; hh < HG; ++hh) {
+                    uint32_t mr[16];
+                    if (32 * j > row) {
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) mr[e] = 0u;
+                    } else {
+                        const float ath = a_s[hh * kTile + row];
+                        const float *uh = u_s + hh * kTile + 32 * j;
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            const int s0 = 32 * j + 2 * e;
+                            float m0 = s0 <= row ? __uint_as_float(gr[2 * e]) * __expf(ath + uh[2 * e]) : 0.f;
+                            float m1 = s0 + 1 <= row
+                                           ? __uint_as_float(gr[2 * e + 1]) * __expf(ath + uh[2 * e + 1])
+                                           : 0.f;
+                            if (s0 == row) m0 += Dh[hh];
+                            if (s0 + 1 == row) m1 += Dh[hh];
+                            mr[e] = pack_bf16x2(m0, m1);
+                        }
+                    }
+                    tmem_st16(tq + kColG + 32 * j + 16 * hh, mr);
+                }
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(5));
+
+            if (HG == 2) prep_head(1);
+
+            // ---- epilogue: y = Yd + exp(a_t) Yo
+            wait_bar_warp(bar(8), it & 1, abort_flag, a.err);
+            tc_fence_after();
+            {
+                const bool store = tok < a.L && !*abort_flag;
+                if (HG == 2) {
+                    __nv_bfloat16 *yrow = a.y + (((size_t)b * a.L + tok) * a.H + h0 + wg) * kP;
+#pragma unroll
+                    for (int half = 0; half < 2; ++half) {
+                        uint32_t yd[32], yo[32];
+                        tmem_ld32(tq + kColYd + 64 * wg + 32 * half, yd);
+                        tmem_ld32(tq + kColYo + 64 * wg + 32 * half, yo);
+                        tmem_ld_wait();
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int e = 0; e < 16; ++e)
+                            pk[e] = pack_bf16x2(
+                                fmaf(e_at, __uint_as_float(yo[2 * e]), __uint_as_float(yd[2 * e])),
+                                fmaf(e_at, __uint_as_float(yo[2 * e + 1]),
+                                     __uint_as_float(yd[2 * e + 1])));
+                        if (store) {
+                            uint4 *dst = reinterpret_cast<uint4 *>(yrow + 32 * half);
+#pragma unroll
+                            for (int v = 0; v < 4; ++v)
+                                dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2],
+                                                    pk[4 * v + 3]);
+                        }
+                    }
+                } else {
+                    __nv_bfloat16 *yrow = a.y + (((size_t)b * a.L + tok) * a.H + h0) * kP + 32 * wg;
+                    uint32_t yd[32], yo[32];
+                    tmem_ld32(tq + kColYd + 32 * wg, yd);
+                    tmem_ld32(tq + kColYo + 32 * wg, yo);
+                    tmem_ld_wait();
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        pk[e] = pack_bf16x2(
+                            fmaf(e_at, __uint_as_float(yo[2 * e]), __uint_as_float(yd[2 * e])),
+                            fmaf(e_at, __uint_as_float(yo[2 * e + 1]), __uint_as_float(yd[2 * e + 1])));
+                    if (store) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(yrow);
+#pragma unroll
+                        for (int v = 0; v < 4; ++v)
+                            dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(9));
+        }
+        // ---- final state of the sequence (all MMAs completed: y_full of the last tile)
+        if (sigma == a.nseg - 1 && a.fin && ntile > 0 && !*abort_flag) {
+            tc_fence_after();
+#pragma unroll 1
+            for (int h = 0; h < HG; ++h) {
+                uint32_t r[32];
+                tmem_ld32(tq + kColH + 64 * h + 32 * wg, r);
+                tmem_ld_wait();
+                float *dst = a.fin + ((size_t)b * a.H + h0 + h) * kP * kN;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) dst[(size_t)(32 * wg + j) * kN + row] = __uint_as_float(r[j]);
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+// ============================================= segment contribution kernel
+// F_sigma = sum over the segment's tokens of exp(a_end(segment) - a_s) dt_s
+//           x_s B_s^T, with tiles visited last to first so the decay from a
+// tile's end to the segment's end is a running sum of tile totals.
+template <int HG>
+__global__ void __launch_bounds__(kThreads, 1)
+ssd_tc_segment_kernel(const __grid_constant__ CUtensorMap mapB,
+                      const __grid_constant__ CUtensorMap mapX, const TcArgs a) {
+    extern __shared__ __align__(1024) uint8_t smem[];
+    constexpr int kStages = 3;
+    constexpr uint32_t kStage = kBBytes + HG * kXBytes;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int h0 = blockIdx.x * HG;
+    const int sigma = blockIdx.y;                 // < nseg - 1
+    const int b = blockIdx.z;
+    const int g = h0 / (a.H / a.G);
+    const int k0 = sigma * a.seg_tiles;
+    const int k1 = min(a.tiles, k0 + a.seg_tiles);
+    const int ntile = k1 - k0;
+
+    const uint32_t sbase = smem_u32(smem);
+    if ((sbase & 1023u) != 0u) {
+        if (threadIdx.x == 0) ssd_report(a.err, SSD_DEVERR_SMEM_ALIGN);
+        return;
+    }
+    // barriers: 0..2 full, 3..5 empty, 6 xt_ready, 7 xt_free
+    auto bar = [&](int i) { return sbase + 8u * (uint32_t)i; };
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + kOffTslot);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kOffAbort);
+    float *aend_s = reinterpret_cast<float *>(smem + kOffAend);
+    float *wtot_s = reinterpret_cast<float *>(smem + kOffWtot);
+    float *u_s = reinterpret_cast<float *>(smem + kOffU);
+    const uint32_t tiles_base = sbase + kCtrl;
+    const uint32_t xt_base = tiles_base + kStages * kStage;
+    uint8_t *tiles_ptr = smem + kCtrl;
+    uint8_t *xt_ptr = tiles_ptr + kStages * kStage;
+    constexpr uint32_t kCols = HG == 2 ? 128 : 64;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < 6; ++i) mbar_init(bar(i), 1);
+        mbar_init(bar(6), kXWarps);
+        mbar_init(bar(7), 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tslot), kCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            tma_prefetch_desc(&mapB);
+            tma_prefetch_desc(&mapX);
+            for (int it = 0; it < ntile; ++it) {
+                const int stage = it % kStages;
+                if (it >= kStages &&
+                    !wait_bar(bar(3 + stage), ((it / kStages) - 1) & 1, abort_flag, a.err))
+                    break;
+                const uint32_t stg = tiles_base + stage * kStage;
+                const int t0 = (k1 - 1 - it) * kTile;
+                mbar_arrive_expect_tx(bar(stage), kStage);
+                tma_load_4d(stg, &mapB, bar(stage), 0, g, t0, b);
+                tma_load_4d(stg + kBlk, &mapB, bar(stage), 64, g, t0, b);
+#pragma unroll
+                for (int h = 0; h < HG; ++h)
+                    tma_load_4d(stg + kBBytes + h * kXBytes, &mapX, bar(stage), 0, h0 + h, t0, b);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            for (int it = 0; it < ntile; ++it) {
+                const int stage = it % kStages;
+                const uint32_t stg = tiles_base + stage * kStage;
+                if (!wait_bar(bar(stage), (it / kStages) & 1, abort_flag, a.err)) break;
+                if (!wait_bar(bar(6), it & 1, abort_flag, a.err)) break;
+                tc_fence_after();
+                for (int h = 0; h < HG; ++h) {
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)
+                        mma_ss(tmem + 64 * h, smem_desc(stg + kk * 2048, kBlk, 1024, kSwizzle128B),
+                               smem_desc(xt_base + h * kXBytes + kk * 2048, kBlk, 1024,
+                                         kSwizzle128B),
+                               kIdS, (it > 0 || kk > 0) ? 1u : 0u);
+                }
+                mma_commit(bar(3 + stage));
+                mma_commit(bar(7));
+            }
+        }
+    } else {
+        const int tw = warp - 2;
+        const int wg = tw >> 2;
+        const int q = warp & 3;
+        const int row = 32 * q + lane;
+        const uint32_t tq = tmem + ((uint32_t)(32 * q) << 16);
+        const int hown = wg % HG;
+        const float A_own = a.A[h0 + hown];
+        float suf[HG];
+#pragma unroll
+        for (int h = 0; h < HG; ++h) suf[h] = 0.f;
+        for (int it = 0; it < ntile; ++it) {
+            const int stage = it % kStages;
+            const int t0 = (k1 - 1 - it) * kTile;
+            const uint8_t *stg_ptr = tiles_ptr + stage * kStage;
+            named_bar_sync(3, 32 * kXWarps);
+            const int tok = t0 + row;
+            float dtv = 0.f;
+            if (tok < a.L) dtv = a.dt[((size_t)b * a.L + tok) * a.H + h0 + hown];
+            float aend;
+            const float at = tile_cumsum(dtv * A_own, q, lane, wtot_s + 4 * wg, 1 + wg, &aend);
+            if (wg < HG) {
+                u_s[hown * kTile + row] = dtv > 0.f ? __logf(dtv) - at : -INFINITY;
+                if (row == 0) aend_s[hown] = aend;
+            }
+            named_bar_sync(3, 32 * kXWarps);
+            if (it > 0) wait_bar_warp(bar(7), (it - 1) & 1, abort_flag, a.err);
+            wait_bar_warp(bar(stage), (it / kStages) & 1, abort_flag, a.err);
+#pragma unroll
+            for (int h = 0; h < HG; ++h) {
+                const float w = __expf(suf[h] + aend_s[h] + u_s[h * kTile + row]);
+                const uint8_t *xs = stg_ptr + kBBytes + h * kXBytes;
+                uint8_t *xt = xt_ptr + h * kXBytes;
+#pragma unroll
+                for (int c = 4 * wg; c < 4 * wg + 4; ++c) {
+                    const uint32_t off = sw128(row, 8 * c);
+                    *reinterpret_cast<uint4 *>(xt + off) =
+                        scale_bf16x8(*reinterpret_cast<const uint4 *>(xs + off), w);
+                }
+                suf[h] += aend_s[h];
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(6));
+        }
+        if (ntile > 0) wait_bar_warp(bar(7), (ntile - 1) & 1, abort_flag, a.err);
+        tc_fence_after();
+        if (!*abort_flag) {
+#pragma unroll 1
+            for (int h = 0; h < HG; ++h) {
+                uint32_t r[32];
+                tmem_ld32(tq + 64 * h + 32 * wg, r);
+                tmem_ld_wait();
+                float *dst = a.ws_state +
+                             (((size_t)b * (a.nseg - 1) + sigma) * a.H + h0 + h) * kP * kN;
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    dst[(size_t)(32 * wg + j) * kN + row] = ntile > 0 ? __uint_as_float(r[j]) : 0.f;
+                if (wg == 0 && row == 0)
+                    a.ws_decay[((size_t)b * (a.nseg - 1) + sigma) * a.H + h0 + h] = __expf(suf[h]);
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kCols);
+    }
+}
+
+// ============================================ entering state of each segment
+// Step-3 at segment granularity: H_in[s+1] = decay_s * H_in[s] + F_s, with
+// H_in[0] = init.  Overwrites slot s (F_s) with H_in[s+1].
+__global__ void __launch_bounds__(256)
+ssd_tc_segment_pass_kernel(float *__restrict__ ws_state, const float *__restrict__ ws_decay,
+                           const float *__restrict__ init, int batch, int H, int nseg) {
+    const size_t per_head = (size_t)kP * kN / 4;
+    const size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const size_t total = (size_t)batch * H * per_head;
+    if (idx >= total) return;
+    const int b = (int)(idx / ((size_t)H * per_head));
+    const size_t rem = idx - (size_t)b * H * per_head;
+    const int h = (int)(rem / per_head);
+    const size_t e = rem - (size_t)h * per_head;
+    float4 hv = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (init) hv = reinterpret_cast<const float4 *>(init)[((size_t)b * H + h) * per_head + e];
+    for (int s = 0; s < nseg - 1; ++s) {
+        const size_t slot = ((size_t)b * (nseg - 1) + s) * H + h;
+        float4 *p = reinterpret_cast<float4 *>(ws_state) + slot * per_head + e;
+        const float4 f = *p;
+        const float d = ws_decay[slot];
+        hv.x = fmaf(d, hv.x, f.x);
+        hv.y = fmaf(d, hv.y, f.y);
+        hv.z = fmaf(d, hv.z, f.z);
+        hv.w = fmaf(d, hv.w, f.w);
+        *p = hv;
+    }
+}
+
+// ------------------------------------------------------------------ host
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+    std::call_once(g_encode_once, [] {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    return g_encode;
+}
+
+// 4-D bf16 map over [batch][L][d1][inner] with a box of 64 x 1 x 128 x 1,
+// 128-byte swizzle; out-of-range tokens read as zero.
+bool make_map(CUtensorMap *m, const void *base, uint64_t inner, uint64_t d1, uint64_t L,
+              uint64_t batch) {
+    auto enc = encoder();
+    if (!enc) return false;
+    cuuint64_t dims[4] = {inner, d1, L, batch};
+    cuuint64_t strides[3] = {inner * 2, inner * d1 * 2, inner * d1 * L * 2};
+    cuuint32_t box[4] = {64, 1, (cuuint32_t)kTile, 1};
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides,
+               box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int HG>
+constexpr size_t scan_smem() {
+    return kCtrl + 2 * (size_t)(kCBytes + kBBytes + HG * kXBytes) + kHbBytes + kXBytes;
+}
+template <int HG>
+constexpr size_t seg_smem() {
+    return kCtrl + 3 * (size_t)(kBBytes + HG * kXBytes) + HG * (size_t)kXBytes;
+}
+static_assert(scan_smem<2>() <= 232448, "scan kernel shared memory exceeds 227 KB");
+static_assert(seg_smem<2>() <= 232448, "segment kernel shared memory exceeds 227 KB");
+
+template <int HG>
+cudaError_t launch_hg(const SsdTcPlan &plan, const CUtensorMap &mC, const CUtensorMap &mB,
+                      const CUtensorMap &mX, const TcArgs &args, int batch, int H,
+                      cudaStream_t stream) {
+    static std::once_flag attr_once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(attr_once, [] {
+        attr_err = cudaFuncSetAttribute(ssd_tc_scan_kernel<HG>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        (int)scan_smem<HG>());
+        if (attr_err == cudaSuccess)
+            attr_err = cudaFuncSetAttribute(ssd_tc_segment_kernel<HG>,
+                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                            (int)seg_smem<HG>());
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+    if (plan.nseg > 1) {
+        dim3 g1(H / HG, plan.nseg - 1, batch);
+        ssd_tc_segment_kernel<HG><<<g1, kThreads, seg_smem<HG>(), stream>>>(mB, mX, args);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        const size_t total = (size_t)batch * H * kP * kN / 4;
+        ssd_tc_segment_pass_kernel<<<(unsigned)((total + 255) / 256), 256, 0, stream>>>(
+            args.ws_state, args.ws_decay, args.init, batch, H, plan.nseg);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    dim3 g2(H / HG, plan.nseg, batch);
+    ssd_tc_scan_kernel<HG><<<g2, kThreads, scan_smem<HG>(), stream>>>(mC, mB, mX, args);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+SsdTcPlan ssd_tc_plan(int batch, int L, int H, int P, int N, int G, int num_sms) {
+    SsdTcPlan p{};
+    p.launches = 1;
+    p.supported = P == kP && N == kN && num_sms > 0 && batch > 0 && L > 0 && H > 0 && G > 0 &&
+                  H % G == 0 && encoder() != nullptr;
+    if (!p.supported) return p;
+    p.heads_per_cta = ((H / G) % 2 == 0) ? 2 : 1;
+    p.tiles = (L + kTile - 1) / kTile;
+    const long units = (long)batch * (H / p.heads_per_cta);
+    // Segments trade sequence parallelism against the extra pass over x that
+    // the segment contributions cost: estimate per-SM time as waves x tiles
+    // per segment, with that extra pass weighted 0.4 of a scan tile.
+    double best = 1e300;
+    int best_n = 1;
+    const int max_n = p.tiles < 64 ? p.tiles : 64;
+    for (int n = 1; n <= max_n; ++n) {
+        const int seg = (p.tiles + n - 1) / n;
+        const int nseg = (p.tiles + seg - 1) / seg;
+        if (nseg != n) continue;
+        const long ctas = units * nseg;
+        const long waves = (ctas + num_sms - 1) / num_sms;
+        const double cost = (double)waves * seg * (nseg > 1 ? 1.4 : 1.0);
+        if (cost < best * 0.999) {
+            best = cost;
+            best_n = nseg;
+        }
+    }
+    p.seg_tiles = (p.tiles + best_n - 1) / best_n;
+    p.nseg = (p.tiles + p.seg_tiles - 1) / p.seg_tiles;
+    if (p.nseg > 1) {
+        const size_t state = (size_t)batch * (p.nseg - 1) * H * kP * kN * sizeof(float);
+        const size_t decay = (size_t)batch * (p.nseg - 1) * H * sizeof(float);
+        p.workspace = ((state + 255) / 256) * 256 + ((decay + 255) / 256) * 256;
+        p.launches = 3;
+    }
+    return p;
+}
+
+cudaError_t ssd_launch_scan_tc(const SsdTcPlan &plan, const void *x, const float *dt,
+                               const float *A, const void *B, const void *C, const float *D,
+                               const float *init, void *y, float *fin, int batch, int L, int H,
+                               int P, int N, int G, void *workspace, unsigned int *err,
+                               cudaStream_t stream) {
+    (void)P;
+    (void)N;
+    CUtensorMap mC, mB, mX;
+    if (!make_map(&mC, C, kN, G, L, batch) || !make_map(&mB, B, kN, G, L, batch) ||
+        !make_map(&mX, x, kP, H, L, batch))
+        return cudaErrorInvalidValue;
+    TcArgs args{};
+    args.dt = dt;
+    args.A = A;
+    args.D = D;
+    args.init = init;
+    if (plan.nseg > 1) {
+        const size_t state = (size_t)batch * (plan.nseg - 1) * H * kP * kN * sizeof(float);
+        args.ws_state = static_cast<float *>(workspace);
+        args.ws_decay = reinterpret_cast<float *>(static_cast<char *>(workspace) +
+                                                  ((state + 255) / 256) * 256);
+    }
+    args.y = static_cast<__nv_bfloat16 *>(y);
+    args.fin = fin;
+    args.err = err;
+    args.L = L;
+    args.H = H;
+    args.G = G;
+    args.tiles = plan.tiles;
+    args.seg_tiles = plan.seg_tiles;
+    args.nseg = plan.nseg;
+    if (plan.heads_per_cta == 2) return launch_hg<2>(plan, mC, mB, mX, args, batch, H, stream);
+    return launch_hg<1>(plan, mC, mB, mX, args, batch, H, stream);
+}
