@@ -364,6 +364,7 @@ def run_gpu(args):
     import state_space_model_chunked_gb300 as ssd
     from state_space_model_chunked_gb300 import build as ssd_build
     from state_space_model_chunked_gb300 import inputs as gen
+    from state_space_model_chunked_gb300.sharding import max_over_ranks
     if rank == 0 or world == 1:
         ssd_build.build()
     if dist is not None:
@@ -377,10 +378,7 @@ def run_gpu(args):
 
     with ClockSampler(local) as clk:
         ms, nsets, byts = time_scan(shape, args.steps, args.warmup, device, l2, dist)
-        if dist is not None:
-            t = torch.tensor([ms], device=device)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ms = float(t.item())
+        ms = max_over_ranks(ms, dist, device)
         extra = {}
         if rank == 0 and not args.quick:
             lshape = gen.SCAN_SHAPES[LONG_WORKLOAD]

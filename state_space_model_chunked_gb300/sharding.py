@@ -1,0 +1,44 @@
+"""Splitting the SSD path across GPUs.
+
+Every (batch row, head) recurrence is independent, so the scan and the
+decode step shard over batch rows and heads with no exchange in the data
+path: each GPU runs ssd_scan_fwd / ssd_state_update on its own slice.  Heads
+are split on group boundaries so each GPU keeps whole groups (heads of one
+group share B and C, and the tensor-core kernel pairs them).
+
+Timing across ranks takes the maximum over ranks (the slowest GPU finishes
+the job).
+"""
+from __future__ import annotations
+
+
+def head_range(nheads: int, ngroups: int, world: int, rank: int):
+    """Contiguous [start, stop) head range for `rank` of `world`, cut on group
+    boundaries and as even as whole groups allow.  With more ranks than
+    groups, the trailing ranks get empty ranges."""
+    if nheads % ngroups:
+        raise ValueError("nheads must be a multiple of ngroups")
+    if not 0 <= rank < world:
+        raise ValueError("rank out of range")
+    per_group = nheads // ngroups
+    g0 = (ngroups * rank) // world
+    g1 = (ngroups * (rank + 1)) // world
+    return g0 * per_group, g1 * per_group
+
+
+def batch_range(batch: int, world: int, rank: int):
+    """Contiguous [start, stop) batch-row range for `rank` of `world`."""
+    if not 0 <= rank < world:
+        raise ValueError("rank out of range")
+    return (batch * rank) // world, (batch * (rank + 1)) // world
+
+
+def max_over_ranks(value: float, dist=None, device=None) -> float:
+    """Maximum of a per-rank float over the process group (identity without one)."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return float(value)
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64,
+                     device=device if device is not None else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
