@@ -126,6 +126,30 @@ ssd_status ssd_scan_fwd_algo(ssd_algo algo, const void *x, const float *dt,
                              void *y, float *final_state, void *workspace,
                              size_t workspace_bytes, cudaStream_t stream);
 
+/* Size of the scratch array built into the library for ssd_scan_fwd_static. */
+#define SSD_STATIC_SCRATCH_BYTES (32u << 20)
+
+/* ssd_scan_fwd for callers that cannot allocate device memory (the pages
+ * have no counterpart: this exists for callers whose memory is fixed at
+ * start-up, such as an engine plugin handed only its inputs and outputs, or a
+ * runtime that forbids device allocation after initialisation).  Same
+ * arguments and results as ssd_scan_fwd without the workspace: the scratch is
+ * a fixed array of SSD_STATIC_SCRATCH_BYTES inside the library, held on every
+ * GPU that loads the library until the process exits.  Allocates nothing.
+ *   - Returns SSD_ERR_WORKSPACE when the shape needs more scratch than
+ *     SSD_STATIC_SCRATCH_BYTES (ssd_scan_workspace_bytes() tells how much).
+ *   - The first call on each device looks up the scratch address for that
+ *     device; make that first call before any stream capture.
+ *   - All calls share the one scratch array: calls whose work overlaps on the
+ *     GPU (unordered streams) race.  No scratch contents need clearing. */
+ssd_status ssd_scan_fwd_static(const void *x, const float *dt, const float *A,
+                               const void *B, const void *C, const float *D,
+                               ssd_dtype in_dtype, int batch, int seqlen,
+                               int nheads, int headdim, int dstate,
+                               int ngroups, int chunk,
+                               const float *init_state, void *y,
+                               float *final_state, cudaStream_t stream);
+
 /* Decode: one token of the recurrence for every (batch, head), the O(1)
  * cached step of the compiler-first SSD page.
  *   state  float [batch][nheads][headdim][dstate], read and updated IN PLACE.

@@ -15,6 +15,7 @@ EXPORTED_SYMBOLS = (
     "ssd_scan_kernel_launches",
     "ssd_scan_fwd",
     "ssd_scan_fwd_algo",
+    "ssd_scan_fwd_static",
     "ssd_state_update",
     "ssd_status_string",
     "ssd_last_device_error",
@@ -64,6 +65,8 @@ def load():
         lib.ssd_scan_fwd.argtypes = scan_args
         lib.ssd_scan_fwd_algo.restype = _int
         lib.ssd_scan_fwd_algo.argtypes = [_int] + scan_args
+        lib.ssd_scan_fwd_static.restype = _int
+        lib.ssd_scan_fwd_static.argtypes = [_vp] * 6 + [_int] * 8 + [_vp, _vp, _vp, _vp]
         lib.ssd_state_update.restype = _int
         lib.ssd_state_update.argtypes = [_vp] * 7 + [_int] * 6 + [_vp, _vp]
         lib.ssd_status_string.restype = ctypes.c_char_p
