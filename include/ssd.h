@@ -126,6 +126,14 @@ ssd_status ssd_scan_fwd_algo(ssd_algo algo, const void *x, const float *dt,
                              void *y, float *final_state, void *workspace,
                              size_t workspace_bytes, cudaStream_t stream);
 
+/* Profiling hook (process-wide, not for concurrent callers): while both
+ * events are non-NULL, every following ssd_scan_fwd / ssd_scan_fwd_algo
+ * records `before` immediately before and `after` immediately after the
+ * kernel that writes y, on the call's stream, so cudaEventElapsedTime gives
+ * that kernel's device time.  Works inside stream capture (the records become
+ * graph nodes).  Pass NULL, NULL to stop.  Always returns SSD_OK. */
+ssd_status ssd_scan_profile_events(cudaEvent_t before, cudaEvent_t after);
+
 /* Size of the scratch array built into the library for ssd_scan_fwd_static. */
 #define SSD_STATIC_SCRATCH_BYTES (32u << 20)
 

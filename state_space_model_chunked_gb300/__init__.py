@@ -20,6 +20,7 @@ from ._binding import (  # noqa: F401
     scan_fwd,
     scan_fwd_host,
     scan_kernel_launches,
+    scan_profile_events,
     scan_workspace_bytes,
     state_update,
     ALGO_AUTO,

@@ -16,6 +16,7 @@ EXPORTED_SYMBOLS = (
     "ssd_scan_fwd",
     "ssd_scan_fwd_algo",
     "ssd_scan_fwd_static",
+    "ssd_scan_profile_events",
     "ssd_state_update",
     "ssd_status_string",
     "ssd_last_device_error",
@@ -67,6 +68,8 @@ def load():
         lib.ssd_scan_fwd_algo.argtypes = [_int] + scan_args
         lib.ssd_scan_fwd_static.restype = _int
         lib.ssd_scan_fwd_static.argtypes = [_vp] * 6 + [_int] * 8 + [_vp, _vp, _vp, _vp]
+        lib.ssd_scan_profile_events.restype = _int
+        lib.ssd_scan_profile_events.argtypes = [_vp, _vp]
         lib.ssd_state_update.restype = _int
         lib.ssd_state_update.argtypes = [_vp] * 7 + [_int] * 6 + [_vp, _vp]
         lib.ssd_status_string.restype = ctypes.c_char_p
@@ -244,6 +247,18 @@ def state_update(state, x, dt, A, B, C, D=None, *, y=None):
                                   ctypes.c_void_p(stream))
     _check("ssd_state_update", rc)
     return y
+
+
+def scan_profile_events(before=None, after=None):
+    """Record torch.cuda.Event `before`/`after` around the y-writing kernel of
+    every following scan_fwd call (None, None to stop).  The events must have
+    been created on the device (record them once first)."""
+    lib = load()
+    if before is None or after is None:
+        lib.ssd_scan_profile_events(None, None)
+    else:
+        lib.ssd_scan_profile_events(ctypes.c_void_p(before.cuda_event),
+                                    ctypes.c_void_p(after.cuda_event))
 
 
 def last_device_error():

@@ -38,6 +38,8 @@ int current_sm_count() {
 
 bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
+SsdProfileEvents g_profile = {nullptr, nullptr};
+
 bool valid_chunk(int q) {
     return q == 16 || q == 32 || q == 64 || q == 128 || q == 256;
 }
@@ -75,6 +77,12 @@ const char *ssd_status_string(ssd_status s) {
         case SSD_ERR_WORKSPACE: return "SSD_ERR_WORKSPACE: workspace missing or too small";
     }
     return "SSD_ERR_UNKNOWN";
+}
+
+ssd_status ssd_scan_profile_events(cudaEvent_t before, cudaEvent_t after) {
+    g_profile.before = before;
+    g_profile.after = after;
+    return SSD_OK;
 }
 
 ssd_status ssd_last_device_error(void) {
@@ -140,10 +148,10 @@ ssd_status ssd_scan_fwd_algo(ssd_algo algo, const void *x, const float *dt, cons
         }
         e = ssd_launch_scan_tc(plan, x, dt, A, B, C, D, init_state, y, final_state, batch,
                                seqlen, nheads, headdim, dstate, ngroups, workspace,
-                               device_error_word(), stream);
+                               device_error_word(), g_profile, stream);
     } else {
         e = ssd_launch_scan_simt(x, dt, A, B, C, D, init_state, y, final_state, bf16, batch,
-                                 seqlen, nheads, headdim, dstate, ngroups, stream);
+                                 seqlen, nheads, headdim, dstate, ngroups, g_profile, stream);
     }
     return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
 }
@@ -173,7 +181,8 @@ ssd_status ssd_state_update(float *state, const void *x, const float *dt, const 
         if (p && !aligned16(p)) return SSD_ERR_INVALID_ARG;
     if ((size_t)batch * nheads >= ((size_t)1 << 31)) return SSD_ERR_UNSUPPORTED;
     cudaError_t e = ssd_launch_decode(state, x, dt, A, B, C, D, y, in_dtype == SSD_BF16, batch,
-                                      nheads, headdim, dstate, ngroups, stream);
+                                      nheads, headdim, dstate, ngroups, current_sm_count(),
+                                      device_error_word(), stream);
     return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
 }
 

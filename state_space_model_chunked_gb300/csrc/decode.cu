@@ -13,8 +13,11 @@
 // before any arithmetic to keep enough bytes in flight, and the state uses
 // streaming (evict-first) loads and stores because it is touched once per
 // call.  y reduces C . h across the TPR threads of a row with shuffles.
+#include <algorithm>
+
 #include "common.cuh"
 #include "launch.h"
+#include "ptx.cuh"
 
 namespace {
 
@@ -100,11 +103,224 @@ ssd_decode_kernel(float *__restrict__ state, const T *__restrict__ x,
     }
 }
 
+// Streaming variant for large stacks: a persistent CTA per SM walks its
+// (batch, head) states through a ring of shared-memory stages.  Each stage
+// receives, by bulk copies, one state (32 KB at P 64, N 128) plus that
+// unit's x row and its group's B and C rows, so no global-memory latency sits
+// between the update of one state and the next; the copy engine keeps several
+// states in flight without occupying registers.  The state is updated in
+// place in shared memory and written back by one bulk store.
+constexpr int kStreamThreads = 512;
+constexpr int kStreamRows = 4;          // rows each thread updates per pass
+constexpr uint32_t kStreamRing = 229376;   // ring capacity in bytes
+constexpr uint64_t kStreamWaitNs = 2000000000ull;
+
+struct StreamLayout {
+    uint32_t state_bytes, x_bytes, bc_bytes, stage_bytes;
+};
+
+__host__ __device__ inline StreamLayout stream_layout(int P, int N, int es) {
+    StreamLayout l;
+    l.state_bytes = (uint32_t)P * N * 4u;
+    l.x_bytes = (uint32_t)P * es;
+    l.bc_bytes = (uint32_t)N * es;
+    const uint32_t raw = l.state_bytes + l.x_bytes + 2 * l.bc_bytes;
+    l.stage_bytes = (raw + 127u) & ~127u;
+    return l;
+}
+
+template <typename T, int VPT>
+__global__ void __launch_bounds__(kStreamThreads + 32, 1)
+ssd_decode_stream_kernel(float *__restrict__ state, const T *__restrict__ x,
+                         const float *__restrict__ dt, const float *__restrict__ A,
+                         const T *__restrict__ Bm, const T *__restrict__ Cm,
+                         const float *__restrict__ D, T *__restrict__ y, int batch, int H, int P,
+                         int N, int G, int stages, unsigned int *err) {
+    using namespace ssdptx;
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const StreamLayout L = stream_layout(P, N, (int)sizeof(T));
+    const long units = (long)batch * H;
+    const int tid = threadIdx.x;
+    // barriers: full[stages] (bulk loads landed), done[stages] (update finished)
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)stages * L.stage_bytes);
+    uint64_t *done = full + stages;
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(done + stages);
+    const uint32_t sbase = smem_u32(smem);
+    constexpr int kComputeWarps = kStreamThreads / 32;
+    if (tid == 0) {
+        for (int i = 0; i < stages; ++i) {
+            mbar_init(smem_u32(full + i), 1);
+            mbar_init(smem_u32(done + i), kComputeWarps);
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    const long nk = blockIdx.x < units ? (units - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+    auto unit_of = [&](long k) { return (long)blockIdx.x + k * (long)gridDim.x; };
+
+    if (tid >= kStreamThreads) {
+        // ---- copy warp: loads run stages-1 units ahead; each updated state is
+        //      written back as soon as its compute warps are done with it
+        if (tid == kStreamThreads) {
+            auto issue_load = [&](long k) {
+                const int st = (int)(k % stages);
+                const long u = unit_of(k);
+                const int b = (int)(u / H), h = (int)(u - (long)b * H);
+                const size_t grow = ((size_t)b * G + h / (H / G)) * N;
+                const uint32_t dst = sbase + st * L.stage_bytes;
+                const uint32_t bar = smem_u32(full + st);
+                mbar_arrive_expect_tx(bar, L.state_bytes + L.x_bytes + 2 * L.bc_bytes);
+                bulk_load(dst, state + (size_t)u * P * N, L.state_bytes, bar);
+                bulk_load(dst + L.state_bytes, x + (size_t)u * P, L.x_bytes, bar);
+                bulk_load(dst + L.state_bytes + L.x_bytes, Bm + grow, L.bc_bytes, bar);
+                bulk_load(dst + L.state_bytes + L.x_bytes + L.bc_bytes, Cm + grow, L.bc_bytes, bar);
+            };
+            for (long k = 0; k < nk && k < stages - 1; ++k) issue_load(k);
+            for (long k = 0; k < nk; ++k) {
+                const int st = (int)(k % stages);
+                if (!mbar_wait(smem_u32(done + st), (uint32_t)((k / stages) & 1), kStreamWaitNs)) {
+                    *abort_flag = 1;
+                    ssd_report(err, SSD_DEVERR_TIMEOUT);
+                    break;
+                }
+                bulk_store(state + (size_t)unit_of(k) * P * N, sbase + st * L.stage_bytes,
+                           L.state_bytes);
+                bulk_commit();
+                if (k + stages - 1 < nk) {
+                    // its stage last held unit k-1, whose store must be done reading
+                    bulk_wait_read<1>();
+                    issue_load(k + stages - 1);
+                }
+            }
+            bulk_wait_all();
+        }
+    } else {
+        // ---- compute warps
+        const int tpr = N / (4 * VPT);
+        const int lane_n = tid % tpr;
+        const int total = P * tpr;
+        float dt_next = nk > 0 ? dt[unit_of(0)] : 0.f;
+        for (long k = 0; k < nk; ++k) {
+            const int st = (int)(k % stages);
+            const long u = unit_of(k);
+            const int h = (int)(u % H);
+            const float dtv = dt_next;
+            if (k + 1 < nk) dt_next = dt[unit_of(k + 1)];
+            const float decay = expf(dtv * A[h]);
+            const float Dh = D ? D[h] : 0.0f;
+            bool ok = !*abort_flag &&
+                      mbar_wait(smem_u32(full + st), (uint32_t)((k / stages) & 1), kStreamWaitNs);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) {
+                *abort_flag = 1;
+                ssd_report(err, SSD_DEVERR_TIMEOUT);
+                break;
+            }
+            uint8_t *stage = smem + (size_t)st * L.stage_bytes;
+            float *sm = reinterpret_cast<float *>(stage);
+            const T *xs = reinterpret_cast<const T *>(stage + L.state_bytes);
+            const T *Bs = reinterpret_cast<const T *>(stage + L.state_bytes + L.x_bytes);
+            const T *Cs = reinterpret_cast<const T *>(stage + L.state_bytes + L.x_bytes + L.bc_bytes);
+            float4 Bv[VPT], Cv[VPT];
+#pragma unroll
+            for (int v = 0; v < VPT; ++v) {
+                const int n0 = 4 * (lane_n + v * tpr);
+                Bv[v] = ssd_ld4(Bs + n0);
+                Cv[v] = ssd_ld4(Cs + n0);
+            }
+            // kStreamRows independent rows per thread per pass: all shared-memory
+            // reads first, then the updates, then the interleaved row reductions
+            for (int e0 = 0; e0 < total; e0 += kStreamThreads * kStreamRows) {
+                float4 q[kStreamRows][VPT];
+                float xv[kStreamRows], acc[kStreamRows];
+#pragma unroll
+                for (int i = 0; i < kStreamRows; ++i) {
+                    const int e = e0 + i * kStreamThreads + tid;
+                    const int p = e / tpr;
+                    acc[i] = 0.0f;
+                    xv[i] = 0.0f;
+                    if (e < total) {
+                        xv[i] = ssd_ld(xs + p);
+#pragma unroll
+                        for (int v = 0; v < VPT; ++v)
+                            q[i][v] = *reinterpret_cast<const float4 *>(
+                                sm + (size_t)p * N + 4 * (lane_n + v * tpr));
+                    }
+                }
+#pragma unroll
+                for (int i = 0; i < kStreamRows; ++i) {
+                    const int e = e0 + i * kStreamThreads + tid;
+                    const int p = e / tpr;
+                    if (e < total) {
+                        const float dx = dtv * xv[i];
+#pragma unroll
+                        for (int v = 0; v < VPT; ++v) {
+                            float4 w = q[i][v];
+                            w.x = fmaf(decay, w.x, dx * Bv[v].x);
+                            w.y = fmaf(decay, w.y, dx * Bv[v].y);
+                            w.z = fmaf(decay, w.z, dx * Bv[v].z);
+                            w.w = fmaf(decay, w.w, dx * Bv[v].w);
+                            *reinterpret_cast<float4 *>(sm + (size_t)p * N + 4 * (lane_n + v * tpr)) = w;
+                            acc[i] = fmaf(Cv[v].x, w.x, acc[i]);
+                            acc[i] = fmaf(Cv[v].y, w.y, acc[i]);
+                            acc[i] = fmaf(Cv[v].z, w.z, acc[i]);
+                            acc[i] = fmaf(Cv[v].w, w.w, acc[i]);
+                        }
+                    }
+                }
+                for (int off = tpr >> 1; off > 0; off >>= 1) {
+#pragma unroll
+                    for (int i = 0; i < kStreamRows; ++i)
+                        acc[i] += __shfl_xor_sync(0xffffffffu, acc[i], off);
+                }
+#pragma unroll
+                for (int i = 0; i < kStreamRows; ++i) {
+                    const int e = e0 + i * kStreamThreads + tid;
+                    if (e < total && lane_n == 0)
+                        ssd_st(y + (size_t)u * P + e / tpr, acc[i] + Dh * xv[i]);
+                }
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if ((tid & 31) == 0) mbar_arrive(smem_u32(done + st));
+        }
+    }
+    __syncthreads();
+}
+
 template <typename T>
 cudaError_t launch_t(float *state, const void *x, const float *dt, const float *A,
                      const void *B, const void *C, const float *D, void *y, int batch,
-                     int H, int P, int N, int G, cudaStream_t stream) {
-    const unsigned grid = (unsigned)((size_t)batch * H);
+                     int H, int P, int N, int G, int num_sms, unsigned int *err,
+                     cudaStream_t stream) {
+    const size_t units = (size_t)batch * H;
+    const StreamLayout lay = stream_layout(P, N, (int)sizeof(T));
+    const int stages = (int)std::min<size_t>(8, kStreamRing / lay.stage_bytes);
+    // the streaming ring pays off once every SM has several states to walk;
+    // its bulk copies need 16-byte multiples for the x, B and C rows
+    if (num_sms > 0 && stages >= 3 && units >= (size_t)num_sms * 4 && lay.x_bytes % 16 == 0 &&
+        lay.bc_bytes % 16 == 0) {
+        const size_t smem = (size_t)stages * lay.stage_bytes + 16 * stages + 16;
+        cudaError_t e;
+        if (N <= 128) {
+            e = cudaFuncSetAttribute(ssd_decode_stream_kernel<T, 1>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            if (e != cudaSuccess) return e;
+            ssd_decode_stream_kernel<T, 1><<<num_sms, kStreamThreads + 32, smem, stream>>>(
+                state, (const T *)x, dt, A, (const T *)B, (const T *)C, D, (T *)y, batch, H, P,
+                N, G, stages, err);
+        } else {
+            e = cudaFuncSetAttribute(ssd_decode_stream_kernel<T, 2>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            if (e != cudaSuccess) return e;
+            ssd_decode_stream_kernel<T, 2><<<num_sms, kStreamThreads + 32, smem, stream>>>(
+                state, (const T *)x, dt, A, (const T *)B, (const T *)C, D, (T *)y, batch, H, P,
+                N, G, stages, err);
+        }
+        return cudaGetLastError();
+    }
+    const unsigned grid = (unsigned)units;
     if (N <= 128) {
         ssd_decode_kernel<T, 1><<<grid, kThreads, 0, stream>>>(
             state, (const T *)x, dt, A, (const T *)B, (const T *)C, D, (T *)y, H, P, N, G);
@@ -120,8 +336,10 @@ cudaError_t launch_t(float *state, const void *x, const float *dt, const float *
 cudaError_t ssd_launch_decode(float *state, const void *x, const float *dt,
                               const float *A, const void *B, const void *C,
                               const float *D, void *y, bool bf16, int batch,
-                              int H, int P, int N, int G, cudaStream_t stream) {
+                              int H, int P, int N, int G, int num_sms, unsigned int *err,
+                              cudaStream_t stream) {
     if (bf16)
-        return launch_t<__nv_bfloat16>(state, x, dt, A, B, C, D, y, batch, H, P, N, G, stream);
-    return launch_t<float>(state, x, dt, A, B, C, D, y, batch, H, P, N, G, stream);
+        return launch_t<__nv_bfloat16>(state, x, dt, A, B, C, D, y, batch, H, P, N, G, num_sms,
+                                       err, stream);
+    return launch_t<float>(state, x, dt, A, B, C, D, y, batch, H, P, N, G, num_sms, err, stream);
 }

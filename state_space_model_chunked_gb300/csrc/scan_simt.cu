@@ -215,15 +215,19 @@ template <typename T>
 cudaError_t launch_t(const void *x, const float *dt, const float *A, const void *B,
                      const void *C, const float *D, const float *init, void *y,
                      float *fin, int batch, int L, int H, int P, int N, int G,
-                     cudaStream_t stream) {
+                     SsdProfileEvents prof, cudaStream_t stream) {
     const size_t smem = simt_smem_bytes(N);
     cudaError_t e = cudaFuncSetAttribute(ssd_scan_simt_kernel<T>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid((P + kPB - 1) / kPB, H, batch);
+    if (prof.before && prof.after && (e = cudaEventRecordWithFlags(prof.before, stream, cudaEventRecordExternal)) != cudaSuccess)
+        return e;
     ssd_scan_simt_kernel<T><<<grid, kThreads, smem, stream>>>(
         (const T *)x, dt, A, (const T *)B, (const T *)C, D, init, (T *)y, fin, L, H, P, N, G);
-    return cudaGetLastError();
+    e = cudaGetLastError();
+    if (e == cudaSuccess && prof.before && prof.after) e = cudaEventRecordWithFlags(prof.after, stream, cudaEventRecordExternal);
+    return e;
 }
 
 }  // namespace
@@ -234,8 +238,9 @@ cudaError_t ssd_launch_scan_simt(const void *x, const float *dt, const float *A,
                                  const void *B, const void *C, const float *D,
                                  const float *init, void *y, float *fin, bool bf16,
                                  int batch, int L, int H, int P, int N, int G,
-                                 cudaStream_t stream) {
+                                 SsdProfileEvents prof, cudaStream_t stream) {
     if (bf16)
-        return launch_t<__nv_bfloat16>(x, dt, A, B, C, D, init, y, fin, batch, L, H, P, N, G, stream);
-    return launch_t<float>(x, dt, A, B, C, D, init, y, fin, batch, L, H, P, N, G, stream);
+        return launch_t<__nv_bfloat16>(x, dt, A, B, C, D, init, y, fin, batch, L, H, P, N, G,
+                                       prof, stream);
+    return launch_t<float>(x, dt, A, B, C, D, init, y, fin, batch, L, H, P, N, G, prof, stream);
 }

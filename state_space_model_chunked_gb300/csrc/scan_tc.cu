@@ -51,15 +51,22 @@ namespace {
 constexpr int kTile = 128;                 // tokens per tile
 constexpr int kP = 64;                     // headdim handled by this path
 constexpr int kN = 128;                    // dstate handled by this path
-constexpr int kXWarps = 8;                 // transform/epilogue warps
+constexpr int kXWarps = 16;                // scan kernel: transform/epilogue warps
 constexpr int kThreads = 64 + 32 * kXWarps;
+constexpr int kSegXWarps = 8;              // segment kernel: transform warps
+constexpr int kSegThreads = 64 + 32 * kSegXWarps;
 constexpr uint64_t kWaitNs = 2000000000ull;
+// named barriers: 1 + warpgroup for one warpgroup, kBarAll for all transform warps
+constexpr int kBarAll = 8;
+// Largest decay (in log units) across one 32-token block for which the mask's
+// diagonal block uses the factored form (its R_t factor stays below e^60).
+constexpr float kMaxBlockDecay = 60.f;
 
 constexpr uint32_t kBlk = 16384;           // 128 rows x 128 bytes, 128B-swizzled
 constexpr uint32_t kCBytes = 2 * kBlk;     // C tile: 128 tokens x 128 n
 constexpr uint32_t kBBytes = 2 * kBlk;     // B tile
 constexpr uint32_t kXBytes = kBlk;         // X tile: 128 tokens x 64 p
-constexpr uint32_t kHbBytes = 16384;       // bf16 entering state, 64 p x 128 n
+constexpr uint32_t kHbBytes = 16384;       // bf16 entering state, 128 n rows x 64 p
 constexpr uint32_t kCtrl = 3072;           // barriers and per-tile scalars
 
 // TMEM columns of the scan kernel
@@ -69,7 +76,7 @@ constexpr uint32_t kColYo = 256;           // + 64 h : off-diagonal output
 constexpr uint32_t kColH = 384;            // + 64 h : carried state (lane = n, column = p)
 
 constexpr uint32_t kIdG = idesc_bf16_f32(128, 128, false, false);   // C . B^T
-constexpr uint32_t kIdOff = idesc_bf16_f32(128, 64, false, false);  // C . Hb^T
+constexpr uint32_t kIdOff = idesc_bf16_f32(128, 64, false, true);   // C . Hb (Hb rows = n)
 constexpr uint32_t kIdS = idesc_bf16_f32(128, 64, true, true);      // B^T . Xt
 constexpr uint32_t kIdY = idesc_bf16_f32(128, 64, false, true);     // M(TMEM) . X
 
@@ -77,9 +84,9 @@ constexpr uint32_t kIdY = idesc_bf16_f32(128, 64, false, true);     // M(TMEM) .
 constexpr uint32_t kOffTslot = 128;
 constexpr uint32_t kOffAbort = 132;
 constexpr uint32_t kOffAend = 160;        // float[2]
-constexpr uint32_t kOffWtot = 192;        // float[2 warpgroups][4]
-constexpr uint32_t kOffU = 256;           // float[2][128]: log(dt_s) - a_s
-constexpr uint32_t kOffA = 1280;          // float[2][128]: a_t
+constexpr uint32_t kOffWtot = 256;        // float[4 warpgroups][2 heads][4 warps]
+constexpr uint32_t kOffU = 512;           // float[2][128]: log(dt_s) - a_s
+constexpr uint32_t kOffV = 1536;          // float[2][128]: exp(a_end(32-block of s) - a_s) dt_s
 
 struct TcArgs {
     const float *dt, *A, *D, *init;
@@ -127,30 +134,13 @@ __device__ __forceinline__ uint4 scale_bf16x8(uint4 v, float w) {
     return make_uint4(out[0], out[1], out[2], out[3]);
 }
 
-// Chunk-local inclusive cumulative sum of dt*A over the 128 tokens of a tile,
-// computed by one warpgroup (thread = token).  Returns a_t; *aend = a_127.
-__device__ __forceinline__ float tile_cumsum(float v, int q, int lane, float *wtot, int bar_id,
-                                             float *aend) {
-    float incl = v;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        const float o = __shfl_up_sync(0xffffffffu, incl, off);
-        if (lane >= off) incl += o;
-    }
-    if (lane == 31) wtot[q] = incl;
-    named_bar_sync(bar_id, 128);
-    float pre = 0.f;
-    for (int j = 0; j < q; ++j) pre += wtot[j];
-    *aend = ((wtot[0] + wtot[1]) + wtot[2]) + wtot[3];
-    return pre + incl;
-}
-
 // ============================================================ scan kernel
 template <int HG>
 __global__ void __launch_bounds__(kThreads, 1)
 ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
                    const __grid_constant__ CUtensorMap mapB,
-                   const __grid_constant__ CUtensorMap mapX, const TcArgs a) {
+                   const __grid_constant__ CUtensorMap mapX,
+                   const __grid_constant__ CUtensorMap mapY, const TcArgs a) {
     extern __shared__ __align__(1024) uint8_t smem[];
     constexpr uint32_t kStage = kCBytes + kBBytes + HG * kXBytes;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -175,7 +165,7 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
     float *aend_s = reinterpret_cast<float *>(smem + kOffAend);
     float *wtot_s = reinterpret_cast<float *>(smem + kOffWtot);
     float *u_s = reinterpret_cast<float *>(smem + kOffU);
-    float *a_s = reinterpret_cast<float *>(smem + kOffA);
+    float *v_s = reinterpret_cast<float *>(smem + kOffV);
     const uint32_t tiles_base = sbase + kCtrl;
     const uint32_t hb_base = tiles_base + 2 * kStage;
     const uint32_t xt_base = hb_base + kHbBytes;
@@ -186,8 +176,10 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
     if (threadIdx.x == 0) {
         mbar_init(bar(0), 1);
         mbar_init(bar(1), 1);
-        mbar_init(bar(2), 1);
-        mbar_init(bar(3), 1);
+        // a stage is free once its MMAs are done and the tile's y store has been
+        // issued (so the next loads queue behind that store on the copy engine)
+        mbar_init(bar(2), 2);
+        mbar_init(bar(3), 2);
         mbar_init(bar(4), 1);
         mbar_init(bar(5), kXWarps);
         mbar_init(bar(6), kXWarps);
@@ -231,118 +223,147 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
         }
     } else if (warp == 1) {
         // ------------------------------------------------------ MMA issuer
+        // Descriptors are built once; a K step only adds its byte offset / 16 to
+        // the start-address field, so the issue loop is a handful of adds.
         if (lane == 0) {
+            const uint64_t cK0 = smem_desc(tiles_base, 16, 1024, kSwizzle128B);
+            const uint64_t bMN0 = smem_desc(tiles_base + kCBytes, kBlk, 1024, kSwizzle128B);
+            const uint64_t x00 = smem_desc(tiles_base + kCBytes + kBBytes, kBlk, 1024, kSwizzle128B);
+            const uint64_t hbD = smem_desc(hb_base, kBlk, 1024, kSwizzle128B);
+            const uint64_t xtD = smem_desc(xt_base, kBlk, 1024, kSwizzle128B);
             int hs = 0;
             for (int it = 0; it < ntile; ++it) {
                 const int stage = it & 1;
-                const uint32_t stg = tiles_base + stage * kStage;
+                const uint64_t so = stage ? (uint64_t)(kStage >> 4) : 0ull;
+                const uint64_t cK = cK0 + so, bK = cK + (kCBytes >> 4), bMN = bMN0 + so,
+                               xD = x00 + so;
                 if (!wait_bar(bar(stage), (it >> 1) & 1, abort_flag, a.err)) break;
                 tc_fence_after();
                 // G = C . B^T  (M = 128 tokens t, N = 128 tokens s, K = 128 n)
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
-                    const uint32_t koff = (kk >> 2) * kBlk + (kk & 3) * 32;
-                    mma_ss(tmem + kColG, smem_desc(stg + koff, 16, 1024, kSwizzle128B),
-                           smem_desc(stg + kCBytes + koff, 16, 1024, kSwizzle128B), kIdG, kk > 0);
+                    const uint64_t ko = ((kk >> 2) * kBlk + (kk & 3) * 32) >> 4;
+                    mma_ss(tmem + kColG, cK + ko, bK + ko, kIdG, kk > 0);
                 }
                 mma_commit(bar(4));
+                // intra-chunk outputs once the masks are in TMEM and the previous
+                // tile's outputs have been drained
+                if (!wait_bar(bar(5), it & 1, abort_flag, a.err)) break;
+                if (it > 0 && !wait_bar(bar(9), (it - 1) & 1, abort_flag, a.err)) break;
+                tc_fence_after();
+#pragma unroll
+                for (int hh = 0; hh < HG; ++hh) {
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint32_t acol = kColG + 32 * (kk >> 1) + 16 * hh + 8 * (kk & 1);
+                        mma_ts(tmem + kColYd + 64 * hh, tmem + acol,
+                               xD + (uint64_t)((hh * kXBytes) >> 4) + (uint64_t)(kk * 128), kIdY,
+                               kk > 0);
+                    }
+                }
+                // per head: off-diagonal term from the entering state, then the
+                // state update (operands prepared by the transform warps)
+                bool stop = false;
                 for (int h = 0; h < HG; ++h) {
-                    if (h == 1) {
-                        // intra-chunk outputs once the mask is in TMEM
-                        if (!wait_bar(bar(5), it & 1, abort_flag, a.err)) break;
-                        tc_fence_after();
-                        for (int hh = 0; hh < HG; ++hh) {
-#pragma unroll
-                            for (int kk = 0; kk < 8; ++kk) {
-                                const uint32_t acol =
-                                    kColG + 32 * (kk >> 1) + 16 * hh + 8 * (kk & 1);
-                                mma_ts(tmem + kColYd + 64 * hh, tmem + acol,
-                                       smem_desc(stg + kCBytes + kBBytes + hh * kXBytes + kk * 2048,
-                                                 kBlk, 1024, kSwizzle128B),
-                                       kIdY, kk > 0);
-                            }
-                        }
-                    }
-                    if (!wait_bar(bar(6), hs & 1, abort_flag, a.err)) break;
-                    if (h == 0 && it > 0 && !wait_bar(bar(9), (it - 1) & 1, abort_flag, a.err))
+                    if (!wait_bar(bar(6), hs & 1, abort_flag, a.err)) {
+                        stop = true;
                         break;
+                    }
                     tc_fence_after();
-                    // Yo_h = C . Hb^T  (off-diagonal term from the entering state)
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk) {
-                        const uint32_t koff = (kk >> 2) * kBlk + (kk & 3) * 32;
-                        const uint32_t hoff = (kk >> 2) * 8192 + (kk & 3) * 32;
-                        mma_ss(tmem + kColYo + 64 * h, smem_desc(stg + koff, 16, 1024, kSwizzle128B),
-                               smem_desc(hb_base + hoff, 16, 1024, kSwizzle128B), kIdOff, kk > 0);
+                        const uint64_t ko = ((kk >> 2) * kBlk + (kk & 3) * 32) >> 4;
+                        mma_ss(tmem + kColYo + 64 * h, cK + ko, hbD + (uint64_t)(kk * 128), kIdOff,
+                               kk > 0);
                     }
-                    // H_h += B^T . Xt_h  (chunk state added to the decayed state)
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
-                        mma_ss(tmem + kColH + 64 * h,
-                               smem_desc(stg + kCBytes + kk * 2048, kBlk, 1024, kSwizzle128B),
-                               smem_desc(xt_base + kk * 2048, kBlk, 1024, kSwizzle128B), kIdS, 1);
-                    }
+                    for (int kk = 0; kk < 8; ++kk)
+                        mma_ss(tmem + kColH + 64 * h, bMN + (uint64_t)(kk * 128),
+                               xtD + (uint64_t)(kk * 128), kIdS, 1);
                     mma_commit(bar(7));
                     ++hs;
                 }
-                if (*abort_flag) break;
-                if (HG == 1) {
-                    if (!wait_bar(bar(5), it & 1, abort_flag, a.err)) break;
-                    tc_fence_after();
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
-                        const uint32_t acol = kColG + 32 * (kk >> 1) + 8 * (kk & 1);
-                        mma_ts(tmem + kColYd, tmem + acol,
-                               smem_desc(stg + kCBytes + kBBytes + kk * 2048, kBlk, 1024,
-                                         kSwizzle128B),
-                               kIdY, kk > 0);
-                    }
-                }
+                if (stop) break;
                 mma_commit(bar(2 + stage));
                 mma_commit(bar(8));
             }
         }
     } else {
         // ------------------------------------------- transform / epilogue
+        // 16 warps = 4 warpgroups.  Thread `row` owns TMEM lane row: token t
+        // for the G / M / Y accumulators, state index n for H.
         const int tw = warp - 2;
-        const int wg = tw >> 2;               // warpgroup
+        const int wg = tw >> 2;               // warpgroup 0..3
         const int q = warp & 3;               // TMEM lane quarter
-        const int row = 32 * q + lane;        // token t (or state index n) of this thread
+        const int row = 32 * q + lane;
         const uint32_t tq = tmem + ((uint32_t)(32 * q) << 16);
-        const int hown = wg % HG;             // head whose cumsum this warpgroup computes
-        const float A_own = a.A[h0 + hown];
-        float Dh[HG];
+        float Ah[HG], Dh[HG], dt_next[HG];
 #pragma unroll
-        for (int h = 0; h < HG; ++h) Dh[h] = a.D ? a.D[h0 + h] : 0.f;
+        for (int h = 0; h < HG; ++h) {
+            Ah[h] = a.A[h0 + h];
+            Dh[h] = a.D ? a.D[h0 + h] : 0.f;
+        }
+        auto load_dt = [&](int k, float (&d)[HG]) {
+            const int tok = k * kTile + row;
+#pragma unroll
+            for (int h = 0; h < HG; ++h)
+                d[h] = tok < a.L ? a.dt[((size_t)b * a.L + tok) * a.H + h0 + h] : 0.f;
+        };
+        if (ntile > 0) load_dt(k0, dt_next);
         int hs = 0;
         for (int it = 0; it < ntile; ++it) {
             const int t0 = (k0 + it) * kTile;
             const int stage = it & 1;
             const uint8_t *stg_ptr = tiles_ptr + stage * kStage;
-            // ---- chunk-local cumsum of dt*A
-            named_bar_sync(3, 32 * kXWarps);
-            const int tok = t0 + row;
-            float dtv = 0.f;
-            if (tok < a.L) dtv = a.dt[((size_t)b * a.L + tok) * a.H + h0 + hown];
-            float aend;
-            const float at =
-                tile_cumsum(dtv * A_own, q, lane, wtot_s + 4 * wg, 1 + wg, &aend);
-            const float e_at = __expf(at);
-            if (wg < HG) {
-                u_s[hown * kTile + row] = dtv > 0.f ? __logf(dtv) - at : -INFINITY;
-                a_s[hown * kTile + row] = at;
-                if (row == 0) aend_s[hown] = aend;
-            }
-            named_bar_sync(3, 32 * kXWarps);
+            float dtv[HG];
+#pragma unroll
+            for (int h = 0; h < HG; ++h) dtv[h] = dt_next[h];
+            if (it + 1 < ntile) load_dt(k0 + it + 1, dt_next);   // one tile ahead
 
-            // ---- entering state -> bf16 operand; state scaled by the tile decay;
-            //      w o X operand.  One head at a time (the operand buffers are shared).
+            // ---- chunk-local inclusive cumsum of dt*A, both heads, every warpgroup
+            named_bar_sync(kBarAll, 32 * kXWarps);       // previous tile's readers are done
+            float at[HG], ach[HG][4];
+#pragma unroll
+            for (int h = 0; h < HG; ++h) {
+                float incl = dtv[h] * Ah[h];
+#pragma unroll
+                for (int off = 1; off < 32; off <<= 1) {
+                    const float o = __shfl_up_sync(0xffffffffu, incl, off);
+                    if (lane >= off) incl += o;
+                }
+                at[h] = incl;
+                if (lane == 31) wtot_s[(wg * 2 + h) * 4 + q] = incl;
+            }
+            named_bar_sync(1 + wg, 128);
+#pragma unroll
+            for (int h = 0; h < HG; ++h) {
+                const float *wt = wtot_s + (wg * 2 + h) * 4;
+                ach[h][0] = wt[0];
+                ach[h][1] = ach[h][0] + wt[1];
+                ach[h][2] = ach[h][1] + wt[2];
+                ach[h][3] = ach[h][2] + wt[3];
+                at[h] += q == 0 ? 0.f : (q == 1 ? ach[h][0] : (q == 2 ? ach[h][1] : ach[h][2]));
+            }
+            if (wg < HG) {
+                // per-column factors of this warpgroup's head:
+                //   u_s = log(dt_s) - a_s                 (diagonal 32-block: exp(a_t + u_s))
+                //   v_s = exp(a_end(block of s) - a_s) dt_s   (blocks left of the diagonal)
+                const int h = wg;
+                const float aq = q == 0 ? ach[h][0] : (q == 1 ? ach[h][1] : (q == 2 ? ach[h][2] : ach[h][3]));
+                u_s[h * kTile + row] = dtv[h] > 0.f ? __logf(dtv[h]) - at[h] : -INFINITY;
+                v_s[h * kTile + row] = __expf(aq - at[h]) * dtv[h];
+                if (row == 0) aend_s[h] = ach[h][3];
+            }
+            named_bar_sync(kBarAll, 32 * kXWarps);
+
+            // ---- entering state -> bf16 operand (MN-major rows n); state scaled by
+            //      the tile decay; w o X operand.  Heads one at a time (shared buffers).
             auto prep_head = [&](int h) {
                 if (hs > 0) wait_bar_warp(bar(7), (hs - 1) & 1, abort_flag, a.err);
                 tc_fence_after();
-                const float de = __expf(aend_s[h]);
-                const uint32_t colH = kColH + 64 * h + 32 * wg;
-                uint32_t r[32];
+                const float de = __expf(ach[h][3]);
+                const uint32_t colH = kColH + 64 * h + 16 * wg;
+                uint32_t r[16];
                 if (it == 0) {
                     const float *src =
                         sigma == 0 ? (a.init ? a.init + ((size_t)b * a.H + h0 + h) * kP * kN
@@ -351,29 +372,31 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
                                          (((size_t)b * (a.nseg - 1) + sigma - 1) * a.H + h0 + h) *
                                              kP * kN;
 #pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        r[j] = __float_as_uint(src ? src[(size_t)(32 * wg + j) * kN + row] : 0.f);
+                    for (int j = 0; j < 16; ++j)
+                        r[j] = __float_as_uint(src ? src[(size_t)(16 * wg + j) * kN + row] : 0.f);
                 } else {
-                    tmem_ld32(tq + colH, r);
+                    tmem_ld16(tq + colH, r);
                     tmem_ld_wait();
                 }
+                uint32_t pk[8];
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const int p = 32 * wg + j;
-                    const float v = __uint_as_float(r[j]);
-                    *reinterpret_cast<__nv_bfloat16 *>(hb_ptr + (row >> 6) * 8192 +
-                                                       sw128(p, row & 63)) = __float2bfloat16_rn(v);
-                    r[j] = __float_as_uint(v * de);
-                }
-                tmem_st32(tq + colH, r);
-                // Xt = w o X for this thread's token row, this warpgroup's 32 columns
-                const float w = __expf(aend_s[h] + u_s[h * kTile + row]);
+                for (int e = 0; e < 8; ++e)
+                    pk[e] = pack_bf16x2(__uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1]));
+                *reinterpret_cast<uint4 *>(hb_ptr + sw128(row, 16 * wg)) =
+                    make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                *reinterpret_cast<uint4 *>(hb_ptr + sw128(row, 16 * wg + 8)) =
+                    make_uint4(pk[4], pk[5], pk[6], pk[7]);
+#pragma unroll
+                for (int j = 0; j < 16; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * de);
+                tmem_st16(tq + colH, r);
+                // Xt = w o X, w_s = exp(a_end - a_s) dt_s, for this thread's token row
+                const float w = __expf(ach[h][3] - at[h]) * dtv[h];
                 const uint8_t *xs = stg_ptr + kCBytes + kBBytes + h * kXBytes;
 #pragma unroll
-                for (int c = 4 * wg; c < 4 * wg + 4; ++c) {
+                for (int c = 2 * wg; c < 2 * wg + 2; ++c) {
                     const uint32_t off = sw128(row, 8 * c);
-                    const uint4 v = *reinterpret_cast<const uint4 *>(xs + off);
-                    *reinterpret_cast<uint4 *>(xt_ptr + off) = scale_bf16x8(v, w);
+                    *reinterpret_cast<uint4 *>(xt_ptr + off) =
+                        scale_bf16x8(*reinterpret_cast<const uint4 *>(xs + off), w);
                 }
                 fence_proxy_async_smem();
                 tmem_st_wait();
@@ -383,37 +406,69 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
                 ++hs;
             };
 
-            wait_bar_warp(bar(stage), (it >> 1) & 1, abort_flag, a.err);   // X tile landed
-            prep_head(0);
+            wait_bar_warp(bar(stage), (it >> 1) & 1, abort_flag, a.err);   // tile landed
 
-            // ---- mask: M = G o exp(a_t - a_s) dt_s (s <= t) + D on the diagonal
+            // ---- mask for the 32-token column block j = wg, both heads:
+            //      M = G o exp(a_t - a_s) dt_s (s <= t) + D on the diagonal.
+            //      exp(a_t - a_s) dt_s = R_t v_s with R_t = exp(a_t - a_e(j)) and
+            //      v_s = exp(a_e(j) - a_s) dt_s, e(j) the block's last token: left of
+            //      the diagonal both factors are <= 1; on the diagonal block R_t is
+            //      >= 1 but bounded by the block's own decay, and a block whose decay
+            //      exceeds kMaxBlockDecay falls back to one exponential per element.
             wait_bar_warp(bar(4), it & 1, abort_flag, a.err);
             tc_fence_after();
-#pragma unroll 1
-            for (int jj = 0; jj < 2; ++jj) {
-                const int j = 2 * wg + jj;            // 32-token column chunk
+            {
+                const int j = wg;
                 uint32_t gr[32];
                 tmem_ld32(tq + kColG + 32 * j, gr);
                 tmem_ld_wait();
 #pragma unroll
                 for (int hh = 0; hh < HG; ++hh) {
+                    // a at the end of block j and at the end of block j-1 (selects, no
+                    // dynamic register indexing)
+                    const float aej = j == 0 ? ach[hh][0] : (j == 1 ? ach[hh][1] : (j == 2 ? ach[hh][2] : ach[hh][3]));
+                    const float abj = j == 0 ? 0.f : (j == 1 ? ach[hh][0] : (j == 2 ? ach[hh][1] : ach[hh][2]));
                     uint32_t mr[16];
-                    if (32 * j > row) {
+                    if (q < j) {
 #pragma unroll
                         for (int e = 0; e < 16; ++e) mr[e] = 0u;
-                    } else {
-                        const float ath = a_s[hh * kTile + row];
+                    } else if (q == j && abj - aej > kMaxBlockDecay) {
                         const float *uh = u_s + hh * kTile + 32 * j;
 #pragma unroll
                         for (int e = 0; e < 16; ++e) {
-                            const int s0 = 32 * j + 2 * e;
-                            float m0 = s0 <= row ? __uint_as_float(gr[2 * e]) * __expf(ath + uh[2 * e]) : 0.f;
-                            float m1 = s0 + 1 <= row
-                                           ? __uint_as_float(gr[2 * e + 1]) * __expf(ath + uh[2 * e + 1])
-                                           : 0.f;
-                            if (s0 == row) m0 += Dh[hh];
-                            if (s0 + 1 == row) m1 += Dh[hh];
+                            const int s0 = 2 * e;
+                            float m0 = s0 <= lane ? __uint_as_float(gr[2 * e]) * __expf(at[hh] + uh[s0]) : 0.f;
+                            float m1 = s0 + 1 <= lane ? __uint_as_float(gr[2 * e + 1]) * __expf(at[hh] + uh[s0 + 1]) : 0.f;
+                            if (s0 == lane) m0 += Dh[hh];
+                            if (s0 + 1 == lane) m1 += Dh[hh];
                             mr[e] = pack_bf16x2(m0, m1);
+                        }
+                    } else {
+                        const float R = __expf(at[hh] - aej);
+                        const uint64_t rr = pack_f32x2(R, R);
+                        const float4 *vh = reinterpret_cast<const float4 *>(v_s + hh * kTile + 32 * j);
+#pragma unroll
+                        for (int e4 = 0; e4 < 8; ++e4) {
+                            const float4 v = vh[e4];
+                            const uint64_t g01 = pack_f32x2(__uint_as_float(gr[4 * e4]), __uint_as_float(gr[4 * e4 + 1]));
+                            const uint64_t g23 = pack_f32x2(__uint_as_float(gr[4 * e4 + 2]), __uint_as_float(gr[4 * e4 + 3]));
+                            uint64_t m01 = mul_f32x2(mul_f32x2(g01, pack_f32x2(v.x, v.y)), rr);
+                            uint64_t m23 = mul_f32x2(mul_f32x2(g23, pack_f32x2(v.z, v.w)), rr);
+                            if (q == j) {
+                                // causal cut and D on the diagonal inside the diagonal block
+                                float f[4] = {__uint_as_float((uint32_t)m01), __uint_as_float((uint32_t)(m01 >> 32)),
+                                              __uint_as_float((uint32_t)m23), __uint_as_float((uint32_t)(m23 >> 32))};
+#pragma unroll
+                                for (int c = 0; c < 4; ++c) {
+                                    const int s = 4 * e4 + c;
+                                    f[c] = s < lane ? f[c] : (s == lane ? f[c] + Dh[hh] : 0.f);
+                                }
+                                mr[2 * e4] = pack_bf16x2(f[0], f[1]);
+                                mr[2 * e4 + 1] = pack_bf16x2(f[2], f[3]);
+                            } else {
+                                mr[2 * e4] = pack_bf16x2_from_f32x2(m01);
+                                mr[2 * e4 + 1] = pack_bf16x2_from_f32x2(m23);
+                            }
                         }
                     }
                     tmem_st16(tq + kColG + 32 * j + 16 * hh, mr);
@@ -424,74 +479,81 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(5));
 
+            // the previous tile's y store reads the Hb / Xt buffers that the state
+            // prep below rewrites
+            if (warp == 2 && lane == 0) bulk_wait_read<0>();
+            named_bar_sync(kBarAll, 32 * kXWarps);
+            prep_head(0);
             if (HG == 2) prep_head(1);
 
-            // ---- epilogue: y = Yd + exp(a_t) Yo
+            // ---- epilogue: y = Yd + exp(a_t) Yo, staged as bf16 in the Hb / Xt
+            //      buffers (free once the tile's MMAs are done; head 0 / head 1) and
+            //      written by TMA stores
             wait_bar_warp(bar(8), it & 1, abort_flag, a.err);
             tc_fence_after();
-            {
-                const bool store = tok < a.L && !*abort_flag;
-                if (HG == 2) {
-                    __nv_bfloat16 *yrow = a.y + (((size_t)b * a.L + tok) * a.H + h0 + wg) * kP;
+            if (HG == 2) {
+                const int hh = wg & 1, ph = wg >> 1;
+                const float e_at = __expf(at[hh]);
+                uint32_t yd[32], yo[32];
+                tmem_ld32(tq + kColYd + 64 * hh + 32 * ph, yd);
+                tmem_ld32(tq + kColYo + 64 * hh + 32 * ph, yo);
+                tmem_ld_wait();
+                uint32_t pk[16];
 #pragma unroll
-                    for (int half = 0; half < 2; ++half) {
-                        uint32_t yd[32], yo[32];
-                        tmem_ld32(tq + kColYd + 64 * wg + 32 * half, yd);
-                        tmem_ld32(tq + kColYo + 64 * wg + 32 * half, yo);
-                        tmem_ld_wait();
-                        uint32_t pk[16];
+                for (int e = 0; e < 16; ++e)
+                    pk[e] = pack_bf16x2(
+                        fmaf(e_at, __uint_as_float(yo[2 * e]), __uint_as_float(yd[2 * e])),
+                        fmaf(e_at, __uint_as_float(yo[2 * e + 1]), __uint_as_float(yd[2 * e + 1])));
+                uint8_t *ybuf = hh == 0 ? hb_ptr : xt_ptr;
 #pragma unroll
-                        for (int e = 0; e < 16; ++e)
-                            pk[e] = pack_bf16x2(
-                                fmaf(e_at, __uint_as_float(yo[2 * e]), __uint_as_float(yd[2 * e])),
-                                fmaf(e_at, __uint_as_float(yo[2 * e + 1]),
-                                     __uint_as_float(yd[2 * e + 1])));
-                        if (store) {
-                            uint4 *dst = reinterpret_cast<uint4 *>(yrow + 32 * half);
+                for (int c = 0; c < 4; ++c)
+                    *reinterpret_cast<uint4 *>(ybuf + sw128(row, 32 * ph + 8 * c)) =
+                        make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+            } else {
+                const float e_at = __expf(at[0]);
+                uint32_t yd[16], yo[16];
+                tmem_ld16(tq + kColYd + 16 * wg, yd);
+                tmem_ld16(tq + kColYo + 16 * wg, yo);
+                tmem_ld_wait();
+                uint32_t pk[8];
 #pragma unroll
-                            for (int v = 0; v < 4; ++v)
-                                dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2],
-                                                    pk[4 * v + 3]);
-                        }
-                    }
-                } else {
-                    __nv_bfloat16 *yrow = a.y + (((size_t)b * a.L + tok) * a.H + h0) * kP + 32 * wg;
-                    uint32_t yd[32], yo[32];
-                    tmem_ld32(tq + kColYd + 32 * wg, yd);
-                    tmem_ld32(tq + kColYo + 32 * wg, yo);
-                    tmem_ld_wait();
-                    uint32_t pk[16];
+                for (int e = 0; e < 8; ++e)
+                    pk[e] = pack_bf16x2(
+                        fmaf(e_at, __uint_as_float(yo[2 * e]), __uint_as_float(yd[2 * e])),
+                        fmaf(e_at, __uint_as_float(yo[2 * e + 1]), __uint_as_float(yd[2 * e + 1])));
 #pragma unroll
-                    for (int e = 0; e < 16; ++e)
-                        pk[e] = pack_bf16x2(
-                            fmaf(e_at, __uint_as_float(yo[2 * e]), __uint_as_float(yd[2 * e])),
-                            fmaf(e_at, __uint_as_float(yo[2 * e + 1]), __uint_as_float(yd[2 * e + 1])));
-                    if (store) {
-                        uint4 *dst = reinterpret_cast<uint4 *>(yrow);
-#pragma unroll
-                        for (int v = 0; v < 4; ++v)
-                            dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
-                    }
-                }
+                for (int c = 0; c < 2; ++c)
+                    *reinterpret_cast<uint4 *>(hb_ptr + sw128(row, 16 * wg + 8 * c)) =
+                        make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
             }
+            fence_proxy_async_smem();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(9));
+            named_bar_sync(kBarAll, 32 * kXWarps);        // the whole y tile is staged
+            if (warp == 2 && lane == 0 && !*abort_flag) {
+#pragma unroll
+                for (int h = 0; h < HG; ++h)
+                    tma_store_4d(&mapY, h == 0 ? hb_base : xt_base, 0, h0 + h, t0, b);
+                bulk_commit();
+            }
+            if (warp == 2 && lane == 0) mbar_arrive(bar(2 + stage));
         }
         // ---- final state of the sequence (all MMAs completed: y_full of the last tile)
         if (sigma == a.nseg - 1 && a.fin && ntile > 0 && !*abort_flag) {
             tc_fence_after();
 #pragma unroll 1
             for (int h = 0; h < HG; ++h) {
-                uint32_t r[32];
-                tmem_ld32(tq + kColH + 64 * h + 32 * wg, r);
+                uint32_t r[16];
+                tmem_ld16(tq + kColH + 64 * h + 16 * wg, r);
                 tmem_ld_wait();
                 float *dst = a.fin + ((size_t)b * a.H + h0 + h) * kP * kN;
 #pragma unroll
-                for (int j = 0; j < 32; ++j) dst[(size_t)(32 * wg + j) * kN + row] = __uint_as_float(r[j]);
+                for (int j = 0; j < 16; ++j) dst[(size_t)(16 * wg + j) * kN + row] = __uint_as_float(r[j]);
             }
         }
     }
+    if (warp == 2 && lane == 0) bulk_wait_all();     // y stores complete before exit
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
@@ -505,7 +567,7 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
 //           x_s B_s^T, with tiles visited last to first so the decay from a
 // tile's end to the segment's end is a running sum of tile totals.
 template <int HG>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kSegThreads, 1)
 ssd_tc_segment_kernel(const __grid_constant__ CUtensorMap mapB,
                       const __grid_constant__ CUtensorMap mapX, const TcArgs a) {
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -529,9 +591,7 @@ ssd_tc_segment_kernel(const __grid_constant__ CUtensorMap mapB,
     auto bar = [&](int i) { return sbase + 8u * (uint32_t)i; };
     uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + kOffTslot);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kOffAbort);
-    float *aend_s = reinterpret_cast<float *>(smem + kOffAend);
     float *wtot_s = reinterpret_cast<float *>(smem + kOffWtot);
-    float *u_s = reinterpret_cast<float *>(smem + kOffU);
     const uint32_t tiles_base = sbase + kCtrl;
     const uint32_t xt_base = tiles_base + kStages * kStage;
     uint8_t *tiles_ptr = smem + kCtrl;
@@ -540,7 +600,7 @@ ssd_tc_segment_kernel(const __grid_constant__ CUtensorMap mapB,
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < 6; ++i) mbar_init(bar(i), 1);
-        mbar_init(bar(6), kXWarps);
+        mbar_init(bar(6), kSegXWarps);
         mbar_init(bar(7), 1);
         *abort_flag = 0;
         fence_mbar_init();
@@ -595,35 +655,57 @@ ssd_tc_segment_kernel(const __grid_constant__ CUtensorMap mapB,
         }
     } else {
         const int tw = warp - 2;
-        const int wg = tw >> 2;
+        const int wg = tw >> 2;               // warpgroup 0..1
         const int q = warp & 3;
         const int row = 32 * q + lane;
         const uint32_t tq = tmem + ((uint32_t)(32 * q) << 16);
-        const int hown = wg % HG;
-        const float A_own = a.A[h0 + hown];
-        float suf[HG];
+        float Ah[HG], suf[HG], dt_next[HG];
 #pragma unroll
-        for (int h = 0; h < HG; ++h) suf[h] = 0.f;
+        for (int h = 0; h < HG; ++h) {
+            Ah[h] = a.A[h0 + h];
+            suf[h] = 0.f;
+        }
+        auto load_dt = [&](int k, float (&d)[HG]) {
+            const int tok = k * kTile + row;
+#pragma unroll
+            for (int h = 0; h < HG; ++h)
+                d[h] = tok < a.L ? a.dt[((size_t)b * a.L + tok) * a.H + h0 + h] : 0.f;
+        };
+        if (ntile > 0) load_dt(k1 - 1, dt_next);
         for (int it = 0; it < ntile; ++it) {
             const int stage = it % kStages;
-            const int t0 = (k1 - 1 - it) * kTile;
             const uint8_t *stg_ptr = tiles_ptr + stage * kStage;
-            named_bar_sync(3, 32 * kXWarps);
-            const int tok = t0 + row;
-            float dtv = 0.f;
-            if (tok < a.L) dtv = a.dt[((size_t)b * a.L + tok) * a.H + h0 + hown];
-            float aend;
-            const float at = tile_cumsum(dtv * A_own, q, lane, wtot_s + 4 * wg, 1 + wg, &aend);
-            if (wg < HG) {
-                u_s[hown * kTile + row] = dtv > 0.f ? __logf(dtv) - at : -INFINITY;
-                if (row == 0) aend_s[hown] = aend;
+            float dtv[HG];
+#pragma unroll
+            for (int h = 0; h < HG; ++h) dtv[h] = dt_next[h];
+            if (it + 1 < ntile) load_dt(k1 - 2 - it, dt_next);
+            named_bar_sync(kBarAll, 32 * kSegXWarps);
+            float at[HG], aend[HG];
+#pragma unroll
+            for (int h = 0; h < HG; ++h) {
+                float incl = dtv[h] * Ah[h];
+#pragma unroll
+                for (int off = 1; off < 32; off <<= 1) {
+                    const float o = __shfl_up_sync(0xffffffffu, incl, off);
+                    if (lane >= off) incl += o;
+                }
+                at[h] = incl;
+                if (lane == 31) wtot_s[(wg * 2 + h) * 4 + q] = incl;
             }
-            named_bar_sync(3, 32 * kXWarps);
+            named_bar_sync(1 + wg, 128);
+#pragma unroll
+            for (int h = 0; h < HG; ++h) {
+                const float *wt = wtot_s + (wg * 2 + h) * 4;
+                const float c1 = wt[0] + wt[1], c2 = c1 + wt[2];
+                aend[h] = c2 + wt[3];
+                at[h] += q == 0 ? 0.f : (q == 1 ? wt[0] : (q == 2 ? c1 : c2));
+            }
             if (it > 0) wait_bar_warp(bar(7), (it - 1) & 1, abort_flag, a.err);
             wait_bar_warp(bar(stage), (it / kStages) & 1, abort_flag, a.err);
 #pragma unroll
             for (int h = 0; h < HG; ++h) {
-                const float w = __expf(suf[h] + aend_s[h] + u_s[h * kTile + row]);
+                // decay from this token to the end of the segment, times dt
+                const float w = __expf(suf[h] + aend[h] - at[h]) * dtv[h];
                 const uint8_t *xs = stg_ptr + kBBytes + h * kXBytes;
                 uint8_t *xt = xt_ptr + h * kXBytes;
 #pragma unroll
@@ -632,7 +714,7 @@ ssd_tc_segment_kernel(const __grid_constant__ CUtensorMap mapB,
                     *reinterpret_cast<uint4 *>(xt + off) =
                         scale_bf16x8(*reinterpret_cast<const uint4 *>(xs + off), w);
                 }
-                suf[h] += aend_s[h];
+                suf[h] += aend[h];
             }
             fence_proxy_async_smem();
             __syncwarp();
@@ -650,7 +732,7 @@ ssd_tc_segment_kernel(const __grid_constant__ CUtensorMap mapB,
                              (((size_t)b * (a.nseg - 1) + sigma) * a.H + h0 + h) * kP * kN;
 #pragma unroll
                 for (int j = 0; j < 32; ++j)
-                    dst[(size_t)(32 * wg + j) * kN + row] = ntile > 0 ? __uint_as_float(r[j]) : 0.f;
+                    dst[(size_t)(32 * wg + j) * kN + row] = __uint_as_float(r[j]);
                 if (wg == 0 && row == 0)
                     a.ws_decay[((size_t)b * (a.nseg - 1) + sigma) * a.H + h0 + h] = __expf(suf[h]);
             }
@@ -666,10 +748,12 @@ ssd_tc_segment_kernel(const __grid_constant__ CUtensorMap mapB,
 
 // ============================================ entering state of each segment
 // Step-3 at segment granularity: H_in[s+1] = decay_s * H_in[s] + F_s, with
-// H_in[0] = init.  Overwrites slot s (F_s) with H_in[s+1].
+// H_in[0] = init.  Overwrites slot s (F_s) with H_in[s+1].  Loads are issued
+// a batch ahead of the dependent FMA chain.
 __global__ void __launch_bounds__(256)
 ssd_tc_segment_pass_kernel(float *__restrict__ ws_state, const float *__restrict__ ws_decay,
                            const float *__restrict__ init, int batch, int H, int nseg) {
+    constexpr int kBatch = 8;
     const size_t per_head = (size_t)kP * kN / 4;
     const size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
     const size_t total = (size_t)batch * H * per_head;
@@ -680,16 +764,29 @@ ssd_tc_segment_pass_kernel(float *__restrict__ ws_state, const float *__restrict
     const size_t e = rem - (size_t)h * per_head;
     float4 hv = make_float4(0.f, 0.f, 0.f, 0.f);
     if (init) hv = reinterpret_cast<const float4 *>(init)[((size_t)b * H + h) * per_head + e];
-    for (int s = 0; s < nseg - 1; ++s) {
-        const size_t slot = ((size_t)b * (nseg - 1) + s) * H + h;
-        float4 *p = reinterpret_cast<float4 *>(ws_state) + slot * per_head + e;
-        const float4 f = *p;
-        const float d = ws_decay[slot];
-        hv.x = fmaf(d, hv.x, f.x);
-        hv.y = fmaf(d, hv.y, f.y);
-        hv.z = fmaf(d, hv.z, f.z);
-        hv.w = fmaf(d, hv.w, f.w);
-        *p = hv;
+    float4 *base = reinterpret_cast<float4 *>(ws_state);
+    for (int s0 = 0; s0 < nseg - 1; s0 += kBatch) {
+        float4 f[kBatch];
+        float d[kBatch];
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) {
+            if (s0 + i < nseg - 1) {
+                const size_t slot = ((size_t)b * (nseg - 1) + s0 + i) * H + h;
+                f[i] = base[slot * per_head + e];
+                d[i] = ws_decay[slot];
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) {
+            if (s0 + i < nseg - 1) {
+                const size_t slot = ((size_t)b * (nseg - 1) + s0 + i) * H + h;
+                hv.x = fmaf(d[i], hv.x, f[i].x);
+                hv.y = fmaf(d[i], hv.y, f[i].y);
+                hv.z = fmaf(d[i], hv.z, f[i].z);
+                hv.w = fmaf(d[i], hv.w, f[i].w);
+                base[slot * per_head + e] = hv;
+            }
+        }
     }
 }
 
@@ -738,8 +835,8 @@ static_assert(seg_smem<2>() <= 232448, "segment kernel shared memory exceeds 227
 
 template <int HG>
 cudaError_t launch_hg(const SsdTcPlan &plan, const CUtensorMap &mC, const CUtensorMap &mB,
-                      const CUtensorMap &mX, const TcArgs &args, int batch, int H,
-                      cudaStream_t stream) {
+                      const CUtensorMap &mX, const CUtensorMap &mY, const TcArgs &args,
+                      int batch, int H, SsdProfileEvents prof, cudaStream_t stream) {
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(attr_once, [] {
@@ -754,7 +851,7 @@ cudaError_t launch_hg(const SsdTcPlan &plan, const CUtensorMap &mC, const CUtens
     if (attr_err != cudaSuccess) return attr_err;
     if (plan.nseg > 1) {
         dim3 g1(H / HG, plan.nseg - 1, batch);
-        ssd_tc_segment_kernel<HG><<<g1, kThreads, seg_smem<HG>(), stream>>>(mB, mX, args);
+        ssd_tc_segment_kernel<HG><<<g1, kSegThreads, seg_smem<HG>(), stream>>>(mB, mX, args);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
         const size_t total = (size_t)batch * H * kP * kN / 4;
@@ -764,8 +861,14 @@ cudaError_t launch_hg(const SsdTcPlan &plan, const CUtensorMap &mC, const CUtens
         if (e != cudaSuccess) return e;
     }
     dim3 g2(H / HG, plan.nseg, batch);
-    ssd_tc_scan_kernel<HG><<<g2, kThreads, scan_smem<HG>(), stream>>>(mC, mB, mX, args);
-    return cudaGetLastError();
+    if (prof.before && prof.after) {
+        cudaError_t e = cudaEventRecordWithFlags(prof.before, stream, cudaEventRecordExternal);
+        if (e != cudaSuccess) return e;
+    }
+    ssd_tc_scan_kernel<HG><<<g2, kThreads, scan_smem<HG>(), stream>>>(mC, mB, mX, mY, args);
+    cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess && prof.before && prof.after) e = cudaEventRecordWithFlags(prof.after, stream, cudaEventRecordExternal);
+    return e;
 }
 
 }  // namespace
@@ -812,12 +915,12 @@ cudaError_t ssd_launch_scan_tc(const SsdTcPlan &plan, const void *x, const float
                                const float *A, const void *B, const void *C, const float *D,
                                const float *init, void *y, float *fin, int batch, int L, int H,
                                int P, int N, int G, void *workspace, unsigned int *err,
-                               cudaStream_t stream) {
+                               SsdProfileEvents prof, cudaStream_t stream) {
     (void)P;
     (void)N;
-    CUtensorMap mC, mB, mX;
+    CUtensorMap mC, mB, mX, mY;
     if (!make_map(&mC, C, kN, G, L, batch) || !make_map(&mB, B, kN, G, L, batch) ||
-        !make_map(&mX, x, kP, H, L, batch))
+        !make_map(&mX, x, kP, H, L, batch) || !make_map(&mY, y, kP, H, L, batch))
         return cudaErrorInvalidValue;
     TcArgs args{};
     args.dt = dt;
@@ -839,6 +942,7 @@ cudaError_t ssd_launch_scan_tc(const SsdTcPlan &plan, const void *x, const float
     args.tiles = plan.tiles;
     args.seg_tiles = plan.seg_tiles;
     args.nseg = plan.nseg;
-    if (plan.heads_per_cta == 2) return launch_hg<2>(plan, mC, mB, mX, args, batch, H, stream);
-    return launch_hg<1>(plan, mC, mB, mX, args, batch, H, stream);
+    if (plan.heads_per_cta == 2)
+        return launch_hg<2>(plan, mC, mB, mX, mY, args, batch, H, prof, stream);
+    return launch_hg<1>(plan, mC, mB, mX, mY, args, batch, H, prof, stream);
 }

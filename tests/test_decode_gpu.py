@@ -89,3 +89,23 @@ def test_decode_full_stack_sampled():
         y_ref, s_ref = oracle.step(before[(bi, li)][None], x, dt, A[hs], Bg, Cg, D[hs])
         assert rel(host(y[bi:bi + 1, hs]), y_ref) <= 1e-2
         assert rel(host(state[bi:bi + 1, hs]), s_ref) <= 1e-6
+
+
+@pytest.mark.parametrize("N,dtype", [(128, "bf16"), (256, "bf16"), (64, "f32"), (16, "bf16")])
+def test_decode_streaming_path_multi_step(N, dtype):
+    """Enough (batch, head) states that every SM walks several of them through
+    the shared-memory ring (the launch used for large decode stacks)."""
+    import state_space_model_chunked_gb300 as ssd
+    b, H, P, G = 8, 160, 64, 4
+    state = gen.decode_state(b, H, P, N, seed=N)
+    A, D = gen.decode_params(H, seed=N)
+    s_dev = dev(state)
+    s_ref = state.astype(np.float64)
+    for t in range(3):
+        tok = gen.decode_token_inputs(b, H, P, N, G, dtype, seed=N, step=t)
+        y = ssd.state_update(s_dev, dev(tok["x"], dtype), dev(tok["dt"]), dev(A),
+                             dev(tok["B"], dtype), dev(tok["C"], dtype), dev(D))
+        y_ref, s_ref = oracle.step(s_ref, tok["x"], tok["dt"], A, tok["B"], tok["C"], D)
+        assert rel(host(y), y_ref) <= TOL[dtype]
+    assert rel(host(s_dev), s_ref) <= 1e-6
+    ssd.last_device_error()
