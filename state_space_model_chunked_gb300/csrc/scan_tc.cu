@@ -365,6 +365,9 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
                 const uint32_t colH = kColH + 64 * h + 16 * wg;
                 uint32_t r[16];
                 if (it == 0) {
+                    // entering states of later segments come from the chaining kernel,
+                    // which may still be finishing (programmatic dependent launch)
+                    if (sigma > 0) griddep_wait();
                     const float *src =
                         sigma == 0 ? (a.init ? a.init + ((size_t)b * a.H + h0 + h) * kP * kN
                                              : nullptr)
@@ -597,6 +600,7 @@ ssd_tc_segment_kernel(const __grid_constant__ CUtensorMap mapB,
     uint8_t *tiles_ptr = smem + kCtrl;
     uint8_t *xt_ptr = tiles_ptr + kStages * kStage;
     constexpr uint32_t kCols = HG == 2 ? 128 : 64;
+    griddep_launch_dependents();
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < 6; ++i) mbar_init(bar(i), 1);
@@ -754,6 +758,8 @@ __global__ void __launch_bounds__(256)
 ssd_tc_segment_pass_kernel(float *__restrict__ ws_state, const float *__restrict__ ws_decay,
                            const float *__restrict__ init, int batch, int H, int nseg) {
     constexpr int kBatch = 8;
+    griddep_wait();                 // segment contributions are complete and visible
+    griddep_launch_dependents();
     const size_t per_head = (size_t)kP * kN / 4;
     const size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
     const size_t total = (size_t)batch * H * per_head;
@@ -833,6 +839,25 @@ constexpr size_t seg_smem() {
 static_assert(scan_smem<2>() <= 232448, "scan kernel shared memory exceeds 227 KB");
 static_assert(seg_smem<2>() <= 232448, "segment kernel shared memory exceeds 227 KB");
 
+// Launch with programmatic stream serialization: the kernel may begin while
+// the previous kernel in the stream finishes; it calls griddepcontrol.wait
+// before touching that kernel's results.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 template <int HG>
 cudaError_t launch_hg(const SsdTcPlan &plan, const CUtensorMap &mC, const CUtensorMap &mB,
                       const CUtensorMap &mX, const CUtensorMap &mY, const TcArgs &args,
@@ -855,9 +880,9 @@ cudaError_t launch_hg(const SsdTcPlan &plan, const CUtensorMap &mC, const CUtens
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
         const size_t total = (size_t)batch * H * kP * kN / 4;
-        ssd_tc_segment_pass_kernel<<<(unsigned)((total + 255) / 256), 256, 0, stream>>>(
-            args.ws_state, args.ws_decay, args.init, batch, H, plan.nseg);
-        e = cudaGetLastError();
+        e = launch_pdl(ssd_tc_segment_pass_kernel, dim3((unsigned)((total + 255) / 256)),
+                       dim3(256), 0, stream, args.ws_state, args.ws_decay, args.init, batch, H,
+                       plan.nseg);
         if (e != cudaSuccess) return e;
     }
     dim3 g2(H / HG, plan.nseg, batch);
@@ -865,8 +890,15 @@ cudaError_t launch_hg(const SsdTcPlan &plan, const CUtensorMap &mC, const CUtens
         cudaError_t e = cudaEventRecordWithFlags(prof.before, stream, cudaEventRecordExternal);
         if (e != cudaSuccess) return e;
     }
-    ssd_tc_scan_kernel<HG><<<g2, kThreads, scan_smem<HG>(), stream>>>(mC, mB, mX, mY, args);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e;
+    if (plan.nseg > 1) {
+        // overlaps the scan kernel's prologue and first tile with the chaining kernel
+        e = launch_pdl(ssd_tc_scan_kernel<HG>, g2, dim3(kThreads), scan_smem<HG>(), stream, mC, mB,
+                       mX, mY, args);
+    } else {
+        ssd_tc_scan_kernel<HG><<<g2, kThreads, scan_smem<HG>(), stream>>>(mC, mB, mX, mY, args);
+        e = cudaGetLastError();
+    }
     if (e == cudaSuccess && prof.before && prof.after) e = cudaEventRecordWithFlags(prof.after, stream, cudaEventRecordExternal);
     return e;
 }
