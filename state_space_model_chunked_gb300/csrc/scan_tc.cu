@@ -135,6 +135,21 @@ __device__ __forceinline__ uint4 scale_bf16x8(uint4 v, float w) {
 }
 
 // ============================================================ scan kernel
+// Shared memory (HG heads per CTA): two stages of {C tile, X tile per head},
+// one B tile, the bf16 entering states of all heads (Hb) and the w o X
+// operands of all heads (Xt).  Merging the heads' off-diagonal and
+// state-update products into one N = 64 * HG instruction stream halves their
+// instruction count: the tensor core spends about the same time on an
+// M = 128 instruction with N = 64 as with N = 128.
+template <int HG>
+struct ScanLayout {
+    static constexpr uint32_t kStage = kCBytes + HG * kXBytes;      // C + X of each head
+    static constexpr uint32_t kOffB = 2 * kStage;
+    static constexpr uint32_t kOffHb = kOffB + kBBytes;
+    static constexpr uint32_t kOffXt = kOffHb + HG * kXBytes;
+    static constexpr uint32_t kBytes = kOffXt + HG * kXBytes;
+};
+
 template <int HG>
 __global__ void __launch_bounds__(kThreads, 1)
 ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
@@ -142,7 +157,8 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
                    const __grid_constant__ CUtensorMap mapX,
                    const __grid_constant__ CUtensorMap mapY, const TcArgs a) {
     extern __shared__ __align__(1024) uint8_t smem[];
-    constexpr uint32_t kStage = kCBytes + kBBytes + HG * kXBytes;
+    using Lay = ScanLayout<HG>;
+    constexpr uint32_t kStage = Lay::kStage;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int h0 = blockIdx.x * HG;
     const int sigma = blockIdx.y;
@@ -157,35 +173,37 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
         if (threadIdx.x == 0) ssd_report(a.err, SSD_DEVERR_SMEM_ALIGN);
         return;
     }
-    // barriers: 0,1 full[stage]; 2,3 empty[stage]; 4 g_full; 5 m_ready;
-    //           6 hx_ready; 7 hx_free; 8 y_full; 9 y_free
+    // barriers: 0,1 fullCX[stage]; 2,3 emptyCX[stage]; 4 fullB; 5 emptyB;
+    //           6 g_full; 7 m_ready; 8 hx_ready; 9 hx_free; 10 y_full; 11 y_free
     auto bar = [&](int i) { return sbase + 8u * (uint32_t)i; };
     uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + kOffTslot);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kOffAbort);
-    float *aend_s = reinterpret_cast<float *>(smem + kOffAend);
     float *wtot_s = reinterpret_cast<float *>(smem + kOffWtot);
     float *u_s = reinterpret_cast<float *>(smem + kOffU);
     float *v_s = reinterpret_cast<float *>(smem + kOffV);
     const uint32_t tiles_base = sbase + kCtrl;
-    const uint32_t hb_base = tiles_base + 2 * kStage;
-    const uint32_t xt_base = hb_base + kHbBytes;
+    const uint32_t b_base = tiles_base + Lay::kOffB;
+    const uint32_t hb_base = tiles_base + Lay::kOffHb;
+    const uint32_t xt_base = tiles_base + Lay::kOffXt;
     uint8_t *tiles_ptr = smem + kCtrl;
-    uint8_t *hb_ptr = tiles_ptr + 2 * kStage;
-    uint8_t *xt_ptr = hb_ptr + kHbBytes;
+    uint8_t *hb_ptr = tiles_ptr + Lay::kOffHb;
+    uint8_t *xt_ptr = tiles_ptr + Lay::kOffXt;
 
     if (threadIdx.x == 0) {
         mbar_init(bar(0), 1);
         mbar_init(bar(1), 1);
-        // a stage is free once its MMAs are done and the tile's y store has been
-        // issued (so the next loads queue behind that store on the copy engine)
+        // a C/X stage is free once its MMAs are done and the tile's y store (staged
+        // in its C block) has been issued
         mbar_init(bar(2), 2);
         mbar_init(bar(3), 2);
         mbar_init(bar(4), 1);
-        mbar_init(bar(5), kXWarps);
-        mbar_init(bar(6), kXWarps);
-        mbar_init(bar(7), 1);
-        mbar_init(bar(8), 1);
-        mbar_init(bar(9), kXWarps);
+        mbar_init(bar(5), 1);
+        mbar_init(bar(6), 1);
+        mbar_init(bar(7), kXWarps);
+        mbar_init(bar(8), kXWarps);
+        mbar_init(bar(9), 1);
+        mbar_init(bar(10), 1);
+        mbar_init(bar(11), kXWarps);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -206,38 +224,44 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
             tma_prefetch_desc(&mapX);
             for (int it = 0; it < ntile; ++it) {
                 const int stage = it & 1;
+                const int t0 = (k0 + it) * kTile;
+                // C and X of this tile (stage last used two tiles ago)
                 if (it >= 2 && !wait_bar(bar(2 + stage), ((it >> 1) - 1) & 1, abort_flag, a.err))
                     break;
                 const uint32_t stg = tiles_base + stage * kStage;
-                const int t0 = (k0 + it) * kTile;
                 mbar_arrive_expect_tx(bar(stage), kStage);
                 tma_load_4d(stg, &mapC, bar(stage), 0, g, t0, b);
                 tma_load_4d(stg + kBlk, &mapC, bar(stage), 64, g, t0, b);
-                tma_load_4d(stg + kCBytes, &mapB, bar(stage), 0, g, t0, b);
-                tma_load_4d(stg + kCBytes + kBlk, &mapB, bar(stage), 64, g, t0, b);
 #pragma unroll
                 for (int h = 0; h < HG; ++h)
-                    tma_load_4d(stg + kCBytes + kBBytes + h * kXBytes, &mapX, bar(stage), 0,
-                                h0 + h, t0, b);
+                    tma_load_4d(stg + kCBytes + h * kXBytes, &mapX, bar(stage), 0, h0 + h, t0, b);
+                // B of this tile (single buffer: free once the previous tile's state
+                // update has read it)
+                if (it >= 1 && !wait_bar(bar(5), (it - 1) & 1, abort_flag, a.err)) break;
+                mbar_arrive_expect_tx(bar(4), kBBytes);
+                tma_load_4d(b_base, &mapB, bar(4), 0, g, t0, b);
+                tma_load_4d(b_base + kBlk, &mapB, bar(4), 64, g, t0, b);
             }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------ MMA issuer
         // Descriptors are built once; a K step only adds its byte offset / 16 to
-        // the start-address field, so the issue loop is a handful of adds.
+        // the start-address field.
         if (lane == 0) {
+            constexpr uint32_t kIdOffAll = idesc_bf16_f32(128, 64 * HG, false, true);
+            constexpr uint32_t kIdSAll = idesc_bf16_f32(128, 64 * HG, true, true);
             const uint64_t cK0 = smem_desc(tiles_base, 16, 1024, kSwizzle128B);
-            const uint64_t bMN0 = smem_desc(tiles_base + kCBytes, kBlk, 1024, kSwizzle128B);
-            const uint64_t x00 = smem_desc(tiles_base + kCBytes + kBBytes, kBlk, 1024, kSwizzle128B);
-            const uint64_t hbD = smem_desc(hb_base, kBlk, 1024, kSwizzle128B);
-            const uint64_t xtD = smem_desc(xt_base, kBlk, 1024, kSwizzle128B);
-            int hs = 0;
+            const uint64_t x00 = smem_desc(tiles_base + kCBytes, kBlk, 1024, kSwizzle128B);
+            const uint64_t bK = smem_desc(b_base, 16, 1024, kSwizzle128B);
+            const uint64_t bMN = smem_desc(b_base, kBlk, 1024, kSwizzle128B);
+            const uint64_t hbD = smem_desc(hb_base, kXBytes, 1024, kSwizzle128B);
+            const uint64_t xtD = smem_desc(xt_base, kXBytes, 1024, kSwizzle128B);
             for (int it = 0; it < ntile; ++it) {
                 const int stage = it & 1;
                 const uint64_t so = stage ? (uint64_t)(kStage >> 4) : 0ull;
-                const uint64_t cK = cK0 + so, bK = cK + (kCBytes >> 4), bMN = bMN0 + so,
-                               xD = x00 + so;
+                const uint64_t cK = cK0 + so, xD = x00 + so;
                 if (!wait_bar(bar(stage), (it >> 1) & 1, abort_flag, a.err)) break;
+                if (!wait_bar(bar(4), it & 1, abort_flag, a.err)) break;
                 tc_fence_after();
                 // G = C . B^T  (M = 128 tokens t, N = 128 tokens s, K = 128 n)
 #pragma unroll
@@ -245,11 +269,26 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
                     const uint64_t ko = ((kk >> 2) * kBlk + (kk & 3) * 32) >> 4;
                     mma_ss(tmem + kColG, cK + ko, bK + ko, kIdG, kk > 0);
                 }
-                mma_commit(bar(4));
-                // intra-chunk outputs once the masks are in TMEM and the previous
-                // tile's outputs have been drained
-                if (!wait_bar(bar(5), it & 1, abort_flag, a.err)) break;
-                if (it > 0 && !wait_bar(bar(9), (it - 1) & 1, abort_flag, a.err)) break;
+                mma_commit(bar(6));
+                // all heads' state update: H += B^T . Xt (chunk state onto the decayed
+                // state), then the off-diagonal term Yo = C . Hb from the entering state
+                if (!wait_bar(bar(8), it & 1, abort_flag, a.err)) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_ss(tmem + kColH, bMN + (uint64_t)(kk * 128), xtD + (uint64_t)(kk * 128),
+                           kIdSAll, 1);
+                mma_commit(bar(5));                     // B may be reloaded
+                if (it > 0 && !wait_bar(bar(11), (it - 1) & 1, abort_flag, a.err)) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint64_t ko = ((kk >> 2) * kBlk + (kk & 3) * 32) >> 4;
+                    mma_ss(tmem + kColYo, cK + ko, hbD + (uint64_t)(kk * 128), kIdOffAll, kk > 0);
+                }
+                mma_commit(bar(9));                     // Hb / Xt free, H updated
+                // intra-chunk outputs once the masks are in TMEM
+                if (!wait_bar(bar(7), it & 1, abort_flag, a.err)) break;
                 tc_fence_after();
 #pragma unroll
                 for (int hh = 0; hh < HG; ++hh) {
@@ -261,31 +300,8 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
                                kk > 0);
                     }
                 }
-                // per head: off-diagonal term from the entering state, then the
-                // state update (operands prepared by the transform warps)
-                bool stop = false;
-                for (int h = 0; h < HG; ++h) {
-                    if (!wait_bar(bar(6), hs & 1, abort_flag, a.err)) {
-                        stop = true;
-                        break;
-                    }
-                    tc_fence_after();
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
-                        const uint64_t ko = ((kk >> 2) * kBlk + (kk & 3) * 32) >> 4;
-                        mma_ss(tmem + kColYo + 64 * h, cK + ko, hbD + (uint64_t)(kk * 128), kIdOff,
-                               kk > 0);
-                    }
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)
-                        mma_ss(tmem + kColH + 64 * h, bMN + (uint64_t)(kk * 128),
-                               xtD + (uint64_t)(kk * 128), kIdS, 1);
-                    mma_commit(bar(7));
-                    ++hs;
-                }
-                if (stop) break;
                 mma_commit(bar(2 + stage));
-                mma_commit(bar(8));
+                mma_commit(bar(10));
             }
         }
     } else {
@@ -310,7 +326,6 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
                 d[h] = tok < a.L ? a.dt[((size_t)b * a.L + tok) * a.H + h0 + h] : 0.f;
         };
         if (ntile > 0) load_dt(k0, dt_next);
-        int hs = 0;
         for (int it = 0; it < ntile; ++it) {
             const int t0 = (k0 + it) * kTile;
             const int stage = it & 1;
@@ -320,7 +335,7 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
             for (int h = 0; h < HG; ++h) dtv[h] = dt_next[h];
             if (it + 1 < ntile) load_dt(k0 + it + 1, dt_next);   // one tile ahead
 
-            // ---- chunk-local inclusive cumsum of dt*A, both heads, every warpgroup
+            // ---- chunk-local inclusive cumsum of dt*A, all heads, every warpgroup
             named_bar_sync(kBarAll, 32 * kXWarps);       // previous tile's readers are done
             float at[HG], ach[HG][4];
 #pragma unroll
@@ -352,22 +367,21 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
                 const float aq = q == 0 ? ach[h][0] : (q == 1 ? ach[h][1] : (q == 2 ? ach[h][2] : ach[h][3]));
                 u_s[h * kTile + row] = dtv[h] > 0.f ? __logf(dtv[h]) - at[h] : -INFINITY;
                 v_s[h * kTile + row] = __expf(aq - at[h]) * dtv[h];
-                if (row == 0) aend_s[h] = ach[h][3];
             }
             named_bar_sync(kBarAll, 32 * kXWarps);
 
-            // ---- entering state -> bf16 operand (MN-major rows n); state scaled by
-            //      the tile decay; w o X operand.  Heads one at a time (shared buffers).
-            auto prep_head = [&](int h) {
-                if (hs > 0) wait_bar_warp(bar(7), (hs - 1) & 1, abort_flag, a.err);
-                tc_fence_after();
+            // ---- all heads: entering state -> bf16 operand (MN-major rows n), state
+            //      scaled by the tile decay, and Xt = w o X, w_s = exp(a_end - a_s) dt_s
+            wait_bar_warp(bar(stage), (it >> 1) & 1, abort_flag, a.err);    // X landed
+            if (it > 0) wait_bar_warp(bar(9), (it - 1) & 1, abort_flag, a.err);
+            tc_fence_after();
+            if (it == 0 && sigma > 0) griddep_wait();   // entering states of later segments
+#pragma unroll
+            for (int h = 0; h < HG; ++h) {
                 const float de = __expf(ach[h][3]);
                 const uint32_t colH = kColH + 64 * h + 16 * wg;
                 uint32_t r[16];
                 if (it == 0) {
-                    // entering states of later segments come from the chaining kernel,
-                    // which may still be finishing (programmatic dependent launch)
-                    if (sigma > 0) griddep_wait();
                     const float *src =
                         sigma == 0 ? (a.init ? a.init + ((size_t)b * a.H + h0 + h) * kP * kN
                                              : nullptr)
@@ -385,40 +399,38 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
 #pragma unroll
                 for (int e = 0; e < 8; ++e)
                     pk[e] = pack_bf16x2(__uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1]));
-                *reinterpret_cast<uint4 *>(hb_ptr + sw128(row, 16 * wg)) =
+                uint8_t *hb = hb_ptr + h * kXBytes;
+                *reinterpret_cast<uint4 *>(hb + sw128(row, 16 * wg)) =
                     make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                *reinterpret_cast<uint4 *>(hb_ptr + sw128(row, 16 * wg + 8)) =
+                *reinterpret_cast<uint4 *>(hb + sw128(row, 16 * wg + 8)) =
                     make_uint4(pk[4], pk[5], pk[6], pk[7]);
 #pragma unroll
                 for (int j = 0; j < 16; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * de);
                 tmem_st16(tq + colH, r);
-                // Xt = w o X, w_s = exp(a_end - a_s) dt_s, for this thread's token row
                 const float w = __expf(ach[h][3] - at[h]) * dtv[h];
-                const uint8_t *xs = stg_ptr + kCBytes + kBBytes + h * kXBytes;
+                const uint8_t *xs = stg_ptr + kCBytes + h * kXBytes;
+                uint8_t *xt = xt_ptr + h * kXBytes;
 #pragma unroll
                 for (int c = 2 * wg; c < 2 * wg + 2; ++c) {
                     const uint32_t off = sw128(row, 8 * c);
-                    *reinterpret_cast<uint4 *>(xt_ptr + off) =
+                    *reinterpret_cast<uint4 *>(xt + off) =
                         scale_bf16x8(*reinterpret_cast<const uint4 *>(xs + off), w);
                 }
-                fence_proxy_async_smem();
-                tmem_st_wait();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar(6));
-                ++hs;
-            };
+            }
+            fence_proxy_async_smem();
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(8));
 
-            wait_bar_warp(bar(stage), (it >> 1) & 1, abort_flag, a.err);   // tile landed
-
-            // ---- mask for the 32-token column block j = wg, both heads:
+            // ---- mask for the 32-token column block j = wg, all heads:
             //      M = G o exp(a_t - a_s) dt_s (s <= t) + D on the diagonal.
             //      exp(a_t - a_s) dt_s = R_t v_s with R_t = exp(a_t - a_e(j)) and
             //      v_s = exp(a_e(j) - a_s) dt_s, e(j) the block's last token: left of
             //      the diagonal both factors are <= 1; on the diagonal block R_t is
             //      >= 1 but bounded by the block's own decay, and a block whose decay
             //      exceeds kMaxBlockDecay falls back to one exponential per element.
-            wait_bar_warp(bar(4), it & 1, abort_flag, a.err);
+            wait_bar_warp(bar(6), it & 1, abort_flag, a.err);
             tc_fence_after();
             {
                 const int j = wg;
@@ -427,8 +439,6 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
                 tmem_ld_wait();
 #pragma unroll
                 for (int hh = 0; hh < HG; ++hh) {
-                    // a at the end of block j and at the end of block j-1 (selects, no
-                    // dynamic register indexing)
                     const float aej = j == 0 ? ach[hh][0] : (j == 1 ? ach[hh][1] : (j == 2 ? ach[hh][2] : ach[hh][3]));
                     const float abj = j == 0 ? 0.f : (j == 1 ? ach[hh][0] : (j == 2 ? ach[hh][1] : ach[hh][2]));
                     uint32_t mr[16];
@@ -480,20 +490,14 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(5));
+            if (lane == 0) mbar_arrive(bar(7));
 
-            // the previous tile's y store reads the Hb / Xt buffers that the state
-            // prep below rewrites
-            if (warp == 2 && lane == 0) bulk_wait_read<0>();
-            named_bar_sync(kBarAll, 32 * kXWarps);
-            prep_head(0);
-            if (HG == 2) prep_head(1);
-
-            // ---- epilogue: y = Yd + exp(a_t) Yo, staged as bf16 in the Hb / Xt
-            //      buffers (free once the tile's MMAs are done; head 0 / head 1) and
+            // ---- epilogue: y = Yd + exp(a_t) Yo, staged as bf16 in this stage's C
+            //      blocks (free once the tile's MMAs are done; head h in block h) and
             //      written by TMA stores
-            wait_bar_warp(bar(8), it & 1, abort_flag, a.err);
+            wait_bar_warp(bar(10), it & 1, abort_flag, a.err);
             tc_fence_after();
+            uint8_t *ystage = tiles_ptr + stage * kStage;
             if (HG == 2) {
                 const int hh = wg & 1, ph = wg >> 1;
                 const float e_at = __expf(at[hh]);
@@ -507,7 +511,7 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
                     pk[e] = pack_bf16x2(
                         fmaf(e_at, __uint_as_float(yo[2 * e]), __uint_as_float(yd[2 * e])),
                         fmaf(e_at, __uint_as_float(yo[2 * e + 1]), __uint_as_float(yd[2 * e + 1])));
-                uint8_t *ybuf = hh == 0 ? hb_ptr : xt_ptr;
+                uint8_t *ybuf = ystage + hh * kBlk;
 #pragma unroll
                 for (int c = 0; c < 4; ++c)
                     *reinterpret_cast<uint4 *>(ybuf + sw128(row, 32 * ph + 8 * c)) =
@@ -526,21 +530,23 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
                         fmaf(e_at, __uint_as_float(yo[2 * e + 1]), __uint_as_float(yd[2 * e + 1])));
 #pragma unroll
                 for (int c = 0; c < 2; ++c)
-                    *reinterpret_cast<uint4 *>(hb_ptr + sw128(row, 16 * wg + 8 * c)) =
+                    *reinterpret_cast<uint4 *>(ystage + sw128(row, 16 * wg + 8 * c)) =
                         make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
             }
             fence_proxy_async_smem();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(9));
+            if (lane == 0) mbar_arrive(bar(11));
             named_bar_sync(kBarAll, 32 * kXWarps);        // the whole y tile is staged
-            if (warp == 2 && lane == 0 && !*abort_flag) {
+            if (warp == 2 && lane == 0) {
+                if (!*abort_flag) {
 #pragma unroll
-                for (int h = 0; h < HG; ++h)
-                    tma_store_4d(&mapY, h == 0 ? hb_base : xt_base, 0, h0 + h, t0, b);
-                bulk_commit();
+                    for (int h = 0; h < HG; ++h)
+                        tma_store_4d(&mapY, tiles_base + stage * kStage + h * kBlk, 0, h0 + h, t0, b);
+                    bulk_commit();
+                }
+                mbar_arrive(bar(2 + stage));   // loads into this stage queue behind the store
             }
-            if (warp == 2 && lane == 0) mbar_arrive(bar(2 + stage));
         }
         // ---- final state of the sequence (all MMAs completed: y_full of the last tile)
         if (sigma == a.nseg - 1 && a.fin && ntile > 0 && !*abort_flag) {
@@ -645,14 +651,13 @@ ssd_tc_segment_kernel(const __grid_constant__ CUtensorMap mapB,
                 if (!wait_bar(bar(stage), (it / kStages) & 1, abort_flag, a.err)) break;
                 if (!wait_bar(bar(6), it & 1, abort_flag, a.err)) break;
                 tc_fence_after();
-                for (int h = 0; h < HG; ++h) {
+                // all heads at once: F += B^T . [Xt_0 | Xt_1]  (N = 64 * HG)
+                constexpr uint32_t kIdSAll = idesc_bf16_f32(128, 64 * HG, true, true);
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)
-                        mma_ss(tmem + 64 * h, smem_desc(stg + kk * 2048, kBlk, 1024, kSwizzle128B),
-                               smem_desc(xt_base + h * kXBytes + kk * 2048, kBlk, 1024,
-                                         kSwizzle128B),
-                               kIdS, (it > 0 || kk > 0) ? 1u : 0u);
-                }
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_ss(tmem, smem_desc(stg + kk * 2048, kBlk, 1024, kSwizzle128B),
+                           smem_desc(xt_base + kk * 2048, kXBytes, 1024, kSwizzle128B), kIdSAll,
+                           (it > 0 || kk > 0) ? 1u : 0u);
                 mma_commit(bar(3 + stage));
                 mma_commit(bar(7));
             }
@@ -830,7 +835,7 @@ bool make_map(CUtensorMap *m, const void *base, uint64_t inner, uint64_t d1, uin
 
 template <int HG>
 constexpr size_t scan_smem() {
-    return kCtrl + 2 * (size_t)(kCBytes + kBBytes + HG * kXBytes) + kHbBytes + kXBytes;
+    return kCtrl + (size_t)ScanLayout<HG>::kBytes;
 }
 template <int HG>
 constexpr size_t seg_smem() {
