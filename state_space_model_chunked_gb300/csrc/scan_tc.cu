@@ -313,7 +313,7 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
         const int q = warp & 3;               // TMEM lane quarter
         const int row = 32 * q + lane;
         const uint32_t tq = tmem + ((uint32_t)(32 * q) << 16);
-        float Ah[HG], Dh[HG], dt_next[HG];
+        float Ah[HG], Dh[HG], dt_next[HG], dtv[HG];
 #pragma unroll
         for (int h = 0; h < HG; ++h) {
             Ah[h] = a.A[h0 + h];
@@ -325,19 +325,16 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
             for (int h = 0; h < HG; ++h)
                 d[h] = tok < a.L ? a.dt[((size_t)b * a.L + tok) * a.H + h0 + h] : 0.f;
         };
-        if (ntile > 0) load_dt(k0, dt_next);
-        for (int it = 0; it < ntile; ++it) {
-            const int t0 = (k0 + it) * kTile;
-            const int stage = it & 1;
-            const uint8_t *stg_ptr = tiles_ptr + stage * kStage;
-            float dtv[HG];
+        float at[HG], ach[HG][4];
+
+        // ---- chunk-local inclusive cumsum of dt*A for tile it, all heads, every
+        //      warpgroup; leaves a_t and the 32-block ends in registers and the
+        //      per-column mask factors in shared memory
+        auto cumsum_tile = [&](int it) {
 #pragma unroll
             for (int h = 0; h < HG; ++h) dtv[h] = dt_next[h];
             if (it + 1 < ntile) load_dt(k0 + it + 1, dt_next);   // one tile ahead
-
-            // ---- chunk-local inclusive cumsum of dt*A, all heads, every warpgroup
-            named_bar_sync(kBarAll, 32 * kXWarps);       // previous tile's readers are done
-            float at[HG], ach[HG][4];
+            named_bar_sync(kBarAll, 32 * kXWarps);       // previous readers of u/v are done
 #pragma unroll
             for (int h = 0; h < HG; ++h) {
                 float incl = dtv[h] * Ah[h];
@@ -369,10 +366,13 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
                 v_s[h * kTile + row] = __expf(aq - at[h]) * dtv[h];
             }
             named_bar_sync(kBarAll, 32 * kXWarps);
+        };
 
-            // ---- all heads: entering state -> bf16 operand (MN-major rows n), state
-            //      scaled by the tile decay, and Xt = w o X, w_s = exp(a_end - a_s) dt_s
-            wait_bar_warp(bar(stage), (it >> 1) & 1, abort_flag, a.err);    // X landed
+        // ---- all heads of tile it: entering state -> bf16 operand (MN-major rows n),
+        //      state scaled by the tile decay, and Xt = w o X, w_s = exp(a_end - a_s) dt_s
+        auto prep_tile = [&](int it) {
+            const uint8_t *stg_ptr = tiles_ptr + (it & 1) * kStage;
+            wait_bar_warp(bar(it & 1), (it >> 1) & 1, abort_flag, a.err);   // X landed
             if (it > 0) wait_bar_warp(bar(9), (it - 1) & 1, abort_flag, a.err);
             tc_fence_after();
             if (it == 0 && sigma > 0) griddep_wait();   // entering states of later segments
@@ -422,6 +422,19 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(8));
+        };
+
+        // Software pipeline: the next tile's cumsum and state prep run while the
+        // tensor core finishes this tile, then this tile's epilogue.
+        if (ntile > 0) {
+            load_dt(k0, dt_next);
+            cumsum_tile(0);
+            prep_tile(0);
+        }
+        for (int it = 0; it < ntile; ++it) {
+            const int t0 = (k0 + it) * kTile;
+            const int stage = it & 1;
+            const uint8_t *stg_ptr = tiles_ptr + stage * kStage;
 
             // ---- mask for the 32-token column block j = wg, all heads:
             //      M = G o exp(a_t - a_s) dt_s (s <= t) + D on the diagonal.
@@ -450,10 +463,8 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
 #pragma unroll
                         for (int e = 0; e < 16; ++e) {
                             const int s0 = 2 * e;
-                            float m0 = s0 <= lane ? __uint_as_float(gr[2 * e]) * __expf(at[hh] + uh[s0]) : 0.f;
-                            float m1 = s0 + 1 <= lane ? __uint_as_float(gr[2 * e + 1]) * __expf(at[hh] + uh[s0 + 1]) : 0.f;
-                            if (s0 == lane) m0 += Dh[hh];
-                            if (s0 + 1 == lane) m1 += Dh[hh];
+                            const float m0 = s0 <= lane ? __uint_as_float(gr[2 * e]) * __expf(at[hh] + uh[s0]) : 0.f;
+                            const float m1 = s0 + 1 <= lane ? __uint_as_float(gr[2 * e + 1]) * __expf(at[hh] + uh[s0 + 1]) : 0.f;
                             mr[e] = pack_bf16x2(m0, m1);
                         }
                     } else {
@@ -465,22 +476,18 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
                             const float4 v = vh[e4];
                             const uint64_t g01 = pack_f32x2(__uint_as_float(gr[4 * e4]), __uint_as_float(gr[4 * e4 + 1]));
                             const uint64_t g23 = pack_f32x2(__uint_as_float(gr[4 * e4 + 2]), __uint_as_float(gr[4 * e4 + 3]));
-                            uint64_t m01 = mul_f32x2(mul_f32x2(g01, pack_f32x2(v.x, v.y)), rr);
-                            uint64_t m23 = mul_f32x2(mul_f32x2(g23, pack_f32x2(v.z, v.w)), rr);
-                            if (q == j) {
-                                // causal cut and D on the diagonal inside the diagonal block
-                                float f[4] = {__uint_as_float((uint32_t)m01), __uint_as_float((uint32_t)(m01 >> 32)),
-                                              __uint_as_float((uint32_t)m23), __uint_as_float((uint32_t)(m23 >> 32))};
+                            const uint64_t m01 = mul_f32x2(mul_f32x2(g01, pack_f32x2(v.x, v.y)), rr);
+                            const uint64_t m23 = mul_f32x2(mul_f32x2(g23, pack_f32x2(v.z, v.w)), rr);
+                            mr[2 * e4] = pack_bf16x2_from_f32x2(m01);
+                            mr[2 * e4 + 1] = pack_bf16x2_from_f32x2(m23);
+                        }
+                        if (q == j) {
+                            // causal cut inside the diagonal block: keep s <= t (= lane)
 #pragma unroll
-                                for (int c = 0; c < 4; ++c) {
-                                    const int s = 4 * e4 + c;
-                                    f[c] = s < lane ? f[c] : (s == lane ? f[c] + Dh[hh] : 0.f);
-                                }
-                                mr[2 * e4] = pack_bf16x2(f[0], f[1]);
-                                mr[2 * e4 + 1] = pack_bf16x2(f[2], f[3]);
-                            } else {
-                                mr[2 * e4] = pack_bf16x2_from_f32x2(m01);
-                                mr[2 * e4 + 1] = pack_bf16x2_from_f32x2(m23);
+                            for (int e = 0; e < 16; ++e) {
+                                const int s0 = 2 * e;
+                                const uint32_t keep = s0 + 1 <= lane ? 0xffffffffu : (s0 <= lane ? 0x0000ffffu : 0u);
+                                mr[e] &= keep;
                             }
                         }
                     }
@@ -492,46 +499,60 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(7));
 
+            // exp(a_t) of this tile for its epilogue, before the next tile's cumsum
+            float e_at_t[HG];
+#pragma unroll
+            for (int h = 0; h < HG; ++h) e_at_t[h] = __expf(at[h]);
+            if (it + 1 < ntile) {
+                cumsum_tile(it + 1);
+                prep_tile(it + 1);
+            }
+
             // ---- epilogue: y = Yd + exp(a_t) Yo, staged as bf16 in this stage's C
             //      blocks (free once the tile's MMAs are done; head h in block h) and
             //      written by TMA stores
             wait_bar_warp(bar(10), it & 1, abort_flag, a.err);
             tc_fence_after();
             uint8_t *ystage = tiles_ptr + stage * kStage;
-            if (HG == 2) {
-                const int hh = wg & 1, ph = wg >> 1;
-                const float e_at = __expf(at[hh]);
-                uint32_t yd[32], yo[32];
-                tmem_ld32(tq + kColYd + 64 * hh + 32 * ph, yd);
-                tmem_ld32(tq + kColYo + 64 * hh + 32 * ph, yo);
-                tmem_ld_wait();
-                uint32_t pk[16];
-#pragma unroll
-                for (int e = 0; e < 16; ++e)
-                    pk[e] = pack_bf16x2(
-                        fmaf(e_at, __uint_as_float(yo[2 * e]), __uint_as_float(yd[2 * e])),
-                        fmaf(e_at, __uint_as_float(yo[2 * e + 1]), __uint_as_float(yd[2 * e + 1])));
+            {
+                // (head, 32-column range) of this warpgroup: HG = 2 -> head wg & 1,
+                // columns 32 (wg >> 1) ..; HG = 1 -> head 0, columns 16 wg ..
+                const int hh = HG == 2 ? (wg & 1) : 0;
+                const int p0 = HG == 2 ? 32 * (wg >> 1) : 16 * wg;
+                const int np = HG == 2 ? 32 : 16;
+                // selects, not dynamic indexing (which would move the arrays to local memory)
+                const float e_at = (HG == 2 && hh == 1) ? e_at_t[HG - 1] : e_at_t[0];
+                const float dsk = (HG == 2 && hh == 1) ? Dh[HG - 1] : Dh[0];
+                const uint8_t *xs = stg_ptr + kCBytes + hh * kXBytes;
                 uint8_t *ybuf = ystage + hh * kBlk;
 #pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    *reinterpret_cast<uint4 *>(ybuf + sw128(row, 32 * ph + 8 * c)) =
-                        make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-            } else {
-                const float e_at = __expf(at[0]);
-                uint32_t yd[16], yo[16];
-                tmem_ld16(tq + kColYd + 16 * wg, yd);
-                tmem_ld16(tq + kColYo + 16 * wg, yo);
-                tmem_ld_wait();
-                uint32_t pk[8];
+                for (int c16 = 0; c16 < np; c16 += 16) {
+                    const int pc = p0 + c16;
+                    uint32_t yd[16], yo[16];
+                    tmem_ld16(tq + kColYd + 64 * hh + pc, yd);
+                    tmem_ld16(tq + kColYo + 64 * hh + pc, yo);
+                    tmem_ld_wait();
+                    uint32_t pk[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    pk[e] = pack_bf16x2(
-                        fmaf(e_at, __uint_as_float(yo[2 * e]), __uint_as_float(yd[2 * e])),
-                        fmaf(e_at, __uint_as_float(yo[2 * e + 1]), __uint_as_float(yd[2 * e + 1])));
+                    for (int half = 0; half < 2; ++half) {
+                        // D x for these 8 columns from the X tile in the stage
+                        const uint4 xv = *reinterpret_cast<const uint4 *>(xs + sw128(row, pc + 8 * half));
+                        const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
 #pragma unroll
-                for (int c = 0; c < 2; ++c)
-                    *reinterpret_cast<uint4 *>(ystage + sw128(row, 16 * wg + 8 * c)) =
-                        make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+                        for (int e = 0; e < 4; ++e) {
+                            const int i = 8 * half + 2 * e;
+                            const float x0 = __uint_as_float(xw[e] << 16);
+                            const float x1 = __uint_as_float(xw[e] & 0xffff0000u);
+                            pk[4 * half + e] = pack_bf16x2(
+                                fmaf(dsk, x0, fmaf(e_at, __uint_as_float(yo[i]), __uint_as_float(yd[i]))),
+                                fmaf(dsk, x1, fmaf(e_at, __uint_as_float(yo[i + 1]), __uint_as_float(yd[i + 1]))));
+                        }
+                    }
+                    *reinterpret_cast<uint4 *>(ybuf + sw128(row, pc)) =
+                        make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                    *reinterpret_cast<uint4 *>(ybuf + sw128(row, pc + 8)) =
+                        make_uint4(pk[4], pk[5], pk[6], pk[7]);
+                }
             }
             fence_proxy_async_smem();
             tc_fence_before();
@@ -763,8 +784,10 @@ __global__ void __launch_bounds__(256)
 ssd_tc_segment_pass_kernel(float *__restrict__ ws_state, const float *__restrict__ ws_decay,
                            const float *__restrict__ init, int batch, int H, int nseg) {
     constexpr int kBatch = 8;
-    griddep_wait();                 // segment contributions are complete and visible
+    // let the scan kernel start right away: its first-segment CTAs need nothing
+    // from here, the others wait for this grid before reading entering states
     griddep_launch_dependents();
+    griddep_wait();                 // segment contributions are complete and visible
     const size_t per_head = (size_t)kP * kN / 4;
     const size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
     const size_t total = (size_t)batch * H * per_head;
