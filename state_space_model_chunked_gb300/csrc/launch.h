@@ -18,6 +18,18 @@ struct SsdProfileEvents {
     cudaEvent_t before, after;
 };
 
+// Records a profiling event on `stream`; inside stream capture it becomes an
+// event-record node of the graph (an external record), not a capture-internal
+// dependency.
+inline cudaError_t ssd_record_event(cudaEvent_t ev, cudaStream_t stream) {
+    cudaStreamCaptureStatus st = cudaStreamCaptureStatusNone;
+    cudaError_t e = cudaStreamIsCapturing(stream, &st);
+    if (e != cudaSuccess) return e;
+    if (st == cudaStreamCaptureStatusActive)
+        return cudaEventRecordWithFlags(ev, stream, cudaEventRecordExternal);
+    return cudaEventRecord(ev, stream);
+}
+
 cudaError_t ssd_launch_scan_simt(const void *x, const float *dt, const float *A,
                                  const void *B, const void *C, const float *D,
                                  const float *init, void *y, float *fin, bool bf16,

@@ -221,12 +221,12 @@ cudaError_t launch_t(const void *x, const float *dt, const float *A, const void 
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid((P + kPB - 1) / kPB, H, batch);
-    if (prof.before && prof.after && (e = cudaEventRecordWithFlags(prof.before, stream, cudaEventRecordExternal)) != cudaSuccess)
+    if (prof.before && prof.after && (e = ssd_record_event(prof.before, stream)) != cudaSuccess)
         return e;
     ssd_scan_simt_kernel<T><<<grid, kThreads, smem, stream>>>(
         (const T *)x, dt, A, (const T *)B, (const T *)C, D, init, (T *)y, fin, L, H, P, N, G);
     e = cudaGetLastError();
-    if (e == cudaSuccess && prof.before && prof.after) e = cudaEventRecordWithFlags(prof.after, stream, cudaEventRecordExternal);
+    if (e == cudaSuccess && prof.before && prof.after) e = ssd_record_event(prof.after, stream);
     return e;
 }
 

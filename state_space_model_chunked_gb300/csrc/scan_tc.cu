@@ -31,9 +31,12 @@
 // group (ngroups divides nheads) are paired in one CTA so C.B^T is computed
 // once for both.
 //
-// Warp roles (320 threads): warp 0 issues TMA loads, warp 1 allocates TMEM and
-// issues tcgen05.mma from one thread, warps 2-9 (two warpgroups) do the
-// cumsum, the mask, the state bookkeeping and the epilogue.  Every wait is on
+// Warp roles of the scan kernel (608 threads): warp 0 issues TMA loads, warp 1
+// allocates TMEM and issues C.B^T, the state update and the off-diagonal
+// product, warps 2-17 (four warpgroups) do the cumsum, the mask, the state
+// bookkeeping and the epilogue, and warp 18 issues the masked intra-chunk
+// product M.X.  The segment kernel uses warps 0-9 the same way with one
+// issuer.  Every wait is on
 // an mbarrier with a time limit; a wait that runs out sets the device error
 // word and the CTA fast-forwards to its exit without further loads or stores.
 #include <cudaTypedefs.h>
@@ -52,7 +55,12 @@ constexpr int kTile = 128;                 // tokens per tile
 constexpr int kP = 64;                     // headdim handled by this path
 constexpr int kN = 128;                    // dstate handled by this path
 constexpr int kXWarps = 16;                // scan kernel: transform/epilogue warps
-constexpr int kThreads = 64 + 32 * kXWarps;
+// scan kernel: producer, MMA issuer A, 16 transform warps, MMA issuer B.  One
+// thread issues a tcgen05.mma only every ~70-100 cycles, longer than an
+// M = 128, N <= 128 instruction takes to execute, so two issuing warps feed
+// the tensor core from two independent instruction streams.
+constexpr int kThreads = 64 + 32 * kXWarps + 32;
+constexpr int kIssuerB = 2 + kXWarps;      // warp index of the second MMA issuer
 constexpr int kSegXWarps = 8;              // segment kernel: transform warps
 constexpr int kSegThreads = 64 + 32 * kSegXWarps;
 constexpr uint64_t kWaitNs = 2000000000ull;
@@ -174,7 +182,8 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
         return;
     }
     // barriers: 0,1 fullCX[stage]; 2,3 emptyCX[stage]; 4 fullB; 5 emptyB;
-    //           6 g_full; 7 m_ready; 8 hx_ready; 9 hx_free; 10 y_full; 11 y_free
+    //           6 g_full; 7 m_ready; 8 hx_ready; 9 hx_free; 10 y_full; 11 y_free;
+    //           12 g_free (the masks in TMEM have been consumed)
     auto bar = [&](int i) { return sbase + 8u * (uint32_t)i; };
     uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + kOffTslot);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kOffAbort);
@@ -192,18 +201,19 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
     if (threadIdx.x == 0) {
         mbar_init(bar(0), 1);
         mbar_init(bar(1), 1);
-        // a C/X stage is free once its MMAs are done and the tile's y store (staged
-        // in its C block) has been issued
-        mbar_init(bar(2), 2);
-        mbar_init(bar(3), 2);
+        // a C/X stage is free once both issuers' MMAs on it are done and the
+        // tile's y store (staged in its C block) has been issued
+        mbar_init(bar(2), 3);
+        mbar_init(bar(3), 3);
         mbar_init(bar(4), 1);
         mbar_init(bar(5), 1);
         mbar_init(bar(6), 1);
         mbar_init(bar(7), kXWarps);
         mbar_init(bar(8), kXWarps);
         mbar_init(bar(9), 1);
-        mbar_init(bar(10), 1);
+        mbar_init(bar(10), 2);
         mbar_init(bar(11), kXWarps);
+        mbar_init(bar(12), 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -251,7 +261,6 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
             constexpr uint32_t kIdOffAll = idesc_bf16_f32(128, 64 * HG, false, true);
             constexpr uint32_t kIdSAll = idesc_bf16_f32(128, 64 * HG, true, true);
             const uint64_t cK0 = smem_desc(tiles_base, 16, 1024, kSwizzle128B);
-            const uint64_t x00 = smem_desc(tiles_base + kCBytes, kBlk, 1024, kSwizzle128B);
             const uint64_t bK = smem_desc(b_base, 16, 1024, kSwizzle128B);
             const uint64_t bMN = smem_desc(b_base, kBlk, 1024, kSwizzle128B);
             const uint64_t hbD = smem_desc(hb_base, kXBytes, 1024, kSwizzle128B);
@@ -259,9 +268,11 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
             for (int it = 0; it < ntile; ++it) {
                 const int stage = it & 1;
                 const uint64_t so = stage ? (uint64_t)(kStage >> 4) : 0ull;
-                const uint64_t cK = cK0 + so, xD = x00 + so;
+                const uint64_t cK = cK0 + so;
                 if (!wait_bar(bar(stage), (it >> 1) & 1, abort_flag, a.err)) break;
                 if (!wait_bar(bar(4), it & 1, abort_flag, a.err)) break;
+                // the previous tile's masks (in the G columns) must have been read
+                if (it > 0 && !wait_bar(bar(12), (it - 1) & 1, abort_flag, a.err)) break;
                 tc_fence_after();
                 // G = C . B^T  (M = 128 tokens t, N = 128 tokens s, K = 128 n)
 #pragma unroll
@@ -287,8 +298,20 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
                     mma_ss(tmem + kColYo, cK + ko, hbD + (uint64_t)(kk * 128), kIdOffAll, kk > 0);
                 }
                 mma_commit(bar(9));                     // Hb / Xt free, H updated
-                // intra-chunk outputs once the masks are in TMEM
+                mma_commit(bar(2 + stage));
+                mma_commit(bar(10));
+            }
+        }
+    } else if (warp == kIssuerB) {
+        // ------------------------------------------------ MMA issuer B
+        // intra-chunk outputs Yd_h = M_h . X_h once the masks are in TMEM
+        if (lane == 0) {
+            const uint64_t x00 = smem_desc(tiles_base + kCBytes, kBlk, 1024, kSwizzle128B);
+            for (int it = 0; it < ntile; ++it) {
+                const int stage = it & 1;
+                const uint64_t xD = x00 + (stage ? (uint64_t)(kStage >> 4) : 0ull);
                 if (!wait_bar(bar(7), it & 1, abort_flag, a.err)) break;
+                if (it > 0 && !wait_bar(bar(11), (it - 1) & 1, abort_flag, a.err)) break;
                 tc_fence_after();
 #pragma unroll
                 for (int hh = 0; hh < HG; ++hh) {
@@ -300,6 +323,7 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
                                kk > 0);
                     }
                 }
+                mma_commit(bar(12));
                 mma_commit(bar(2 + stage));
                 mma_commit(bar(10));
             }
@@ -915,7 +939,7 @@ cudaError_t launch_hg(const SsdTcPlan &plan, const CUtensorMap &mC, const CUtens
     }
     dim3 g2(H / HG, plan.nseg, batch);
     if (prof.before && prof.after) {
-        cudaError_t e = cudaEventRecordWithFlags(prof.before, stream, cudaEventRecordExternal);
+        cudaError_t e = ssd_record_event(prof.before, stream);
         if (e != cudaSuccess) return e;
     }
     cudaError_t e;
@@ -927,7 +951,7 @@ cudaError_t launch_hg(const SsdTcPlan &plan, const CUtensorMap &mC, const CUtens
         ssd_tc_scan_kernel<HG><<<g2, kThreads, scan_smem<HG>(), stream>>>(mC, mB, mX, mY, args);
         e = cudaGetLastError();
     }
-    if (e == cudaSuccess && prof.before && prof.after) e = cudaEventRecordWithFlags(prof.after, stream, cudaEventRecordExternal);
+    if (e == cudaSuccess && prof.before && prof.after) e = ssd_record_event(prof.after, stream);
     return e;
 }
 

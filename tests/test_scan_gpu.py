@@ -118,3 +118,34 @@ def test_long_context_2p7b_sampled_heads():
     yr, fr = oracle.scan_seq(sub["x"], sub["dt"], sub["A"], sub["B"], sub["C"], sub["D"], None)
     assert rel(y[:, :, heads], yr) <= 1e-2
     assert rel(f[:, heads], fr) <= 1e-2
+
+
+def test_profile_events_hook_eager_and_in_graph():
+    """The profiling hook times the y-writing kernel both in eager launches and
+    inside a captured CUDA graph, without changing the result."""
+    import state_space_model_chunked_gb300 as ssd
+    inp = gen.scan_inputs(1, 2048, 4, 64, 128, 1, "bf16", seed=5, random_init=True)
+    x, Bm, Cm = dev(inp["x"], "bf16"), dev(inp["B"], "bf16"), dev(inp["C"], "bf16")
+    dt, A, D, init = dev(inp["dt"]), dev(inp["A"]), dev(inp["D"]), dev(inp["init"])
+    ws = torch.empty(max(ssd.scan_workspace_bytes(1, 2048, 4, 64, 128, 1, 256), 1),
+                     dtype=torch.uint8, device=x.device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    e1.record()
+    torch.cuda.synchronize()
+    ssd.scan_profile_events(e0, e1)
+    y_eager, f_eager = ssd.scan_fwd(x, dt, A, Bm, Cm, D, 256, init, workspace=ws)
+    ssd.scan_profile_events(None, None)
+    torch.cuda.synchronize()
+    assert e0.elapsed_time(e1) > 0
+    y = torch.empty_like(x)
+    f = torch.empty_like(f_eager)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        ssd.scan_profile_events(e0, e1)
+        ssd.scan_fwd(x, dt, A, Bm, Cm, D, 256, init, y=y, final_state=f, workspace=ws)
+        ssd.scan_profile_events(None, None)
+    g.replay()
+    torch.cuda.synchronize()
+    assert e0.elapsed_time(e1) > 0
+    assert torch.equal(y, y_eager) and torch.equal(f, f_eager)
