@@ -31,12 +31,13 @@
 // group (ngroups divides nheads) are paired in one CTA so C.B^T is computed
 // once for both.
 //
-// Warp roles of the scan kernel (608 threads): warp 0 issues TMA loads, warp 1
+// Warp roles of the scan kernel (672 threads): warp 0 issues TMA loads, warp 1
 // allocates TMEM and issues C.B^T, the state update and the off-diagonal
-// product, warps 2-17 (four warpgroups) do the cumsum, the mask, the state
-// bookkeeping and the epilogue, and warp 18 issues the masked intra-chunk
-// product M.X.  The segment kernel uses warps 0-9 the same way with one
-// issuer.  Every wait is on
+// product, warps 2-17 (four warpgroups) build the masks, keep the state and
+// run the epilogue, warp 18 issues the masked intra-chunk product M.X, warp 19
+// computes each tile's decay factors (cumsum of dt A and its exponentials)
+// ahead of use, and warp 20 issues the y stores.  The segment kernel uses
+// warps 0-9 with one issuer and the cumsum done by its transform warps.  Every wait is on
 // an mbarrier with a time limit; a wait that runs out sets the device error
 // word and the CTA fast-forwards to its exit without further loads or stores.
 #include <cudaTypedefs.h>
@@ -55,12 +56,15 @@ constexpr int kTile = 128;                 // tokens per tile
 constexpr int kP = 64;                     // headdim handled by this path
 constexpr int kN = 128;                    // dstate handled by this path
 constexpr int kXWarps = 16;                // scan kernel: transform/epilogue warps
-// scan kernel: producer, MMA issuer A, 16 transform warps, MMA issuer B.  One
-// thread issues a tcgen05.mma only every ~70-100 cycles, longer than an
-// M = 128, N <= 128 instruction takes to execute, so two issuing warps feed
-// the tensor core from two independent instruction streams.
-constexpr int kThreads = 64 + 32 * kXWarps + 32;
+// scan kernel: producer, MMA issuer A, 16 transform warps, MMA issuer B and a
+// factor warp: 20 warps, 5 per SM sub-partition, which keeps the register cap
+// at 96 (a 21st warp would lower it to 80).  One thread issues a tcgen05.mma
+// only every ~70-100 cycles, longer than an M = 128, N <= 128 instruction
+// takes to execute, so two issuing warps feed the tensor core from two
+// instruction streams.
+constexpr int kThreads = 64 + 32 * kXWarps + 64;
 constexpr int kIssuerB = 2 + kXWarps;      // warp index of the second MMA issuer
+constexpr int kFacWarp = 3 + kXWarps;      // warp index of the factor warp
 constexpr int kSegXWarps = 8;              // segment kernel: transform warps
 constexpr int kSegThreads = 64 + 32 * kSegXWarps;
 constexpr uint64_t kWaitNs = 2000000000ull;
@@ -89,11 +93,12 @@ constexpr uint32_t kIdS = idesc_bf16_f32(128, 64, true, true);      // B^T . Xt
 constexpr uint32_t kIdY = idesc_bf16_f32(128, 64, false, true);     // M(TMEM) . X
 
 // control-region offsets (bytes)
-constexpr uint32_t kOffTslot = 128;
-constexpr uint32_t kOffAbort = 132;
-constexpr uint32_t kOffAend = 160;        // float[2]
-constexpr uint32_t kOffWtot = 256;        // float[4 warpgroups][2 heads][4 warps]
-constexpr uint32_t kOffU = 512;           // float[2][128]: log(dt_s) - a_s
+constexpr uint32_t kOffTslot = 192;       // (barriers occupy bytes 0 .. 143)
+constexpr uint32_t kOffAbort = 196;
+constexpr uint32_t kOffWtot = 256;        // segment kernel: float[2 warpgroups][2 heads][4 warps]
+// scan kernel factor slot, written by the factor warp for one tile at a time
+constexpr uint32_t kOffAch = 256;         // float[2][4]: a at the end of each 32-token block
+constexpr uint32_t kOffAt = 512;          // float[2][128]: a_t, chunk-local inclusive cumsum of dt A
 constexpr uint32_t kOffV = 1536;          // float[2][128]: exp(a_end(32-block of s) - a_s) dt_s
 
 struct TcArgs {
@@ -181,14 +186,16 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
         if (threadIdx.x == 0) ssd_report(a.err, SSD_DEVERR_SMEM_ALIGN);
         return;
     }
-    // barriers: 0,1 fullCX[stage]; 2,3 emptyCX[stage]; 4 fullB; 5 emptyB;
-    //           6 g_full; 7 m_ready; 8 hx_ready; 9 hx_free; 10 y_full; 11 y_free;
-    //           12 g_free (the masks in TMEM have been consumed)
+    // barriers: 0,1 fullC[stage]; 2,3 emptyC[stage]; 4 fullB; 5 emptyB;
+    //           6 g_full; 7 m_ready; 8 hx_ready; 9 hx_free; 10 y_full;
+    //           11 y_done (Yd / Yo read, y staged over C); 12 g_free (the masks
+    //           in TMEM have been consumed); 13 fac_ready (factor slot written);
+    //           14,15 fullX[stage]; 16,17 emptyX[stage]
     auto bar = [&](int i) { return sbase + 8u * (uint32_t)i; };
     uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + kOffTslot);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kOffAbort);
-    float *wtot_s = reinterpret_cast<float *>(smem + kOffWtot);
-    float *u_s = reinterpret_cast<float *>(smem + kOffU);
+    float *ach_s = reinterpret_cast<float *>(smem + kOffAch);
+    float *at_s = reinterpret_cast<float *>(smem + kOffAt);
     float *v_s = reinterpret_cast<float *>(smem + kOffV);
     const uint32_t tiles_base = sbase + kCtrl;
     const uint32_t b_base = tiles_base + Lay::kOffB;
@@ -201,10 +208,16 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
     if (threadIdx.x == 0) {
         mbar_init(bar(0), 1);
         mbar_init(bar(1), 1);
-        // a C/X stage is free once both issuers' MMAs on it are done and the
-        // tile's y store (staged in its C block) has been issued
-        mbar_init(bar(2), 3);
-        mbar_init(bar(3), 3);
+        // a C tile (which holds the tile's y once the epilogue is done) is free
+        // once the tile's off-diagonal product is done and the y store has read
+        // it; an X tile once the masked product and the epilogue's skip term
+        // (every transform warp) have read it
+        mbar_init(bar(2), 2);
+        mbar_init(bar(3), 2);
+        mbar_init(bar(14), 1);
+        mbar_init(bar(15), 1);
+        mbar_init(bar(16), 1 + kXWarps);
+        mbar_init(bar(17), 1 + kXWarps);
         mbar_init(bar(4), 1);
         mbar_init(bar(5), 1);
         mbar_init(bar(6), 1);
@@ -214,6 +227,7 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
         mbar_init(bar(10), 2);
         mbar_init(bar(11), kXWarps);
         mbar_init(bar(12), 1);
+        mbar_init(bar(13), 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -235,22 +249,29 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
             for (int it = 0; it < ntile; ++it) {
                 const int stage = it & 1;
                 const int t0 = (k0 + it) * kTile;
-                // C and X of this tile (stage last used two tiles ago)
-                if (it >= 2 && !wait_bar(bar(2 + stage), ((it >> 1) - 1) & 1, abort_flag, a.err))
-                    break;
+                // Loads go out in the order their buffers free up: X (read last by
+                // the epilogue two tiles ago), B (by the previous state update),
+                // then C (by the y store two tiles ago).
                 const uint32_t stg = tiles_base + stage * kStage;
-                mbar_arrive_expect_tx(bar(stage), kStage);
-                tma_load_4d(stg, &mapC, bar(stage), 0, g, t0, b);
-                tma_load_4d(stg + kBlk, &mapC, bar(stage), 64, g, t0, b);
+                // X of this tile
+                if (it >= 2 && !wait_bar(bar(16 + stage), ((it >> 1) - 1) & 1, abort_flag, a.err))
+                    break;
+                mbar_arrive_expect_tx(bar(14 + stage), HG * kXBytes);
 #pragma unroll
                 for (int h = 0; h < HG; ++h)
-                    tma_load_4d(stg + kCBytes + h * kXBytes, &mapX, bar(stage), 0, h0 + h, t0, b);
+                    tma_load_4d(stg + kCBytes + h * kXBytes, &mapX, bar(14 + stage), 0, h0 + h, t0, b);
                 // B of this tile (single buffer: free once the previous tile's state
                 // update has read it)
                 if (it >= 1 && !wait_bar(bar(5), (it - 1) & 1, abort_flag, a.err)) break;
                 mbar_arrive_expect_tx(bar(4), kBBytes);
                 tma_load_4d(b_base, &mapB, bar(4), 0, g, t0, b);
                 tma_load_4d(b_base + kBlk, &mapB, bar(4), 64, g, t0, b);
+                // C of this tile (stage last used two tiles ago)
+                if (it >= 2 && !wait_bar(bar(2 + stage), ((it >> 1) - 1) & 1, abort_flag, a.err))
+                    break;
+                mbar_arrive_expect_tx(bar(stage), kCBytes);
+                tma_load_4d(stg, &mapC, bar(stage), 0, g, t0, b);
+                tma_load_4d(stg + kBlk, &mapC, bar(stage), 64, g, t0, b);
             }
         }
     } else if (warp == 1) {
@@ -304,14 +325,34 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
         }
     } else if (warp == kIssuerB) {
         // ------------------------------------------------ MMA issuer B
-        // intra-chunk outputs Yd_h = M_h . X_h once the masks are in TMEM
+        // Intra-chunk outputs Yd_h = M_h . X_h once the masks are in TMEM.  It
+        // also sends out each tile's y (staged over its C tile by the epilogue)
+        // by TMA as soon as the epilogue is done, and releases that C buffer
+        // once the store has read it.
         if (lane == 0) {
             const uint64_t x00 = smem_desc(tiles_base + kCBytes, kBlk, 1024, kSwizzle128B);
-            for (int it = 0; it < ntile; ++it) {
+            auto store_y = [&](int k) {
+                const uint32_t ys = tiles_base + (k & 1) * kStage;
+#pragma unroll
+                for (int h = 0; h < HG; ++h)
+                    tma_store_4d(&mapY, ys + h * kBlk, 0, h0 + h, (k0 + k) * kTile, b);
+                bulk_commit();
+            };
+            int it = 0;
+            for (; it < ntile; ++it) {
                 const int stage = it & 1;
                 const uint64_t xD = x00 + (stage ? (uint64_t)(kStage >> 4) : 0ull);
+                if (it > 0) {
+                    // tile it-1's y is staged and its Yd read: store it, reuse Yd
+                    if (!wait_bar(bar(11), (it - 1) & 1, abort_flag, a.err)) break;
+                    store_y(it - 1);
+                }
+                if (!wait_bar(bar(14 + stage), (it >> 1) & 1, abort_flag, a.err)) break;
                 if (!wait_bar(bar(7), it & 1, abort_flag, a.err)) break;
-                if (it > 0 && !wait_bar(bar(11), (it - 1) & 1, abort_flag, a.err)) break;
+                if (it > 0) {
+                    bulk_wait_read<0>();
+                    mbar_arrive(bar(2 + (stage ^ 1)));       // tile it-1's C buffer
+                }
                 tc_fence_after();
 #pragma unroll
                 for (int hh = 0; hh < HG; ++hh) {
@@ -324,9 +365,92 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
                     }
                 }
                 mma_commit(bar(12));
-                mma_commit(bar(2 + stage));
+                mma_commit(bar(16 + stage));
                 mma_commit(bar(10));
             }
+            if (it == ntile && ntile > 0 &&
+                wait_bar(bar(11), (ntile - 1) & 1, abort_flag, a.err))
+                store_y(ntile - 1);
+            bulk_wait_all();                                 // y stores complete before exit
+        }
+    } else if (warp == kFacWarp) {
+        // ------------------------------------------ decay factors and y stores
+        // Lane l owns tokens 4l .. 4l+3 of a tile.  The factors of tile k are
+        // computed in registers ahead of time and written to the factor slot as
+        // soon as every mask of tile k-1 is built (the masks are the last readers
+        // of the slot's v_s).
+        float Af[HG], dn[HG][4];
+        float fa[HG][4], fv[HG][4], fe[HG][4];
+#pragma unroll
+        for (int h = 0; h < HG; ++h) Af[h] = a.A[h0 + h];
+        auto load_dt4 = [&](int it) {
+            const int tok0 = (k0 + it) * kTile + 4 * lane;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int tok = tok0 + i;
+#pragma unroll
+                for (int h = 0; h < HG; ++h)
+                    dn[h][i] = tok < a.L ? a.dt[((size_t)b * a.L + tok) * a.H + h0 + h] : 0.f;
+            }
+        };
+        // chunk-local inclusive cumsum a_t of dt A, the 32-block ends a_e(j) and
+        // v_s = exp(a_e(block of s) - a_s) dt_s, from the dt values in dn
+        auto factors = [&]() {
+#pragma unroll
+            for (int h = 0; h < HG; ++h) {
+                float c[4];
+                c[0] = dn[h][0] * Af[h];
+#pragma unroll
+                for (int i = 1; i < 4; ++i) c[i] = c[i - 1] + dn[h][i] * Af[h];
+                float incl = c[3];
+#pragma unroll
+                for (int off = 1; off < 32; off <<= 1) {
+                    const float o = __shfl_up_sync(0xffffffffu, incl, off);
+                    if (lane >= off) incl += o;
+                }
+                float excl = __shfl_up_sync(0xffffffffu, incl, 1);
+                if (lane == 0) excl = 0.f;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) fa[h][i] = excl + c[i];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) fe[h][j] = __shfl_sync(0xffffffffu, fa[h][3], 8 * j + 7);
+                const int jb = lane >> 3;
+                const float ae = jb == 0 ? fe[h][0] : (jb == 1 ? fe[h][1] : (jb == 2 ? fe[h][2] : fe[h][3]));
+#pragma unroll
+                for (int i = 0; i < 4; ++i) fv[h][i] = __expf(ae - fa[h][i]) * dn[h][i];
+            }
+        };
+        auto publish = [&]() {
+#pragma unroll
+            for (int h = 0; h < HG; ++h) {
+                *reinterpret_cast<float4 *>(at_s + h * kTile + 4 * lane) =
+                    make_float4(fa[h][0], fa[h][1], fa[h][2], fa[h][3]);
+                *reinterpret_cast<float4 *>(v_s + h * kTile + 4 * lane) =
+                    make_float4(fv[h][0], fv[h][1], fv[h][2], fv[h][3]);
+            }
+            if (lane < 4 * HG) {
+                float e = 0.f;       // fe[lane / 4][lane % 4] by selects
+#pragma unroll
+                for (int h = 0; h < HG; ++h)
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        if (lane == 4 * h + j) e = fe[h][j];
+                ach_s[lane] = e;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(13));
+        };
+        if (ntile > 0) {
+            load_dt4(0);
+            factors();
+            publish();
+            if (ntile > 1) load_dt4(1);
+        }
+        for (int it = 0; it + 1 < ntile; ++it) {
+            factors();                                       // tile it + 1
+            if (it + 2 < ntile) load_dt4(it + 2);            // in flight meanwhile
+            wait_bar_warp(bar(7), it & 1, abort_flag, a.err);       // masks of tile it built
+            publish();
         }
     } else {
         // ------------------------------------------- transform / epilogue
@@ -337,66 +461,32 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
         const int q = warp & 3;               // TMEM lane quarter
         const int row = 32 * q + lane;
         const uint32_t tq = tmem + ((uint32_t)(32 * q) << 16);
-        float Ah[HG], Dh[HG], dt_next[HG], dtv[HG];
+        float Dh[HG];
 #pragma unroll
-        for (int h = 0; h < HG; ++h) {
-            Ah[h] = a.A[h0 + h];
-            Dh[h] = a.D ? a.D[h0 + h] : 0.f;
-        }
-        auto load_dt = [&](int k, float (&d)[HG]) {
-            const int tok = k * kTile + row;
-#pragma unroll
-            for (int h = 0; h < HG; ++h)
-                d[h] = tok < a.L ? a.dt[((size_t)b * a.L + tok) * a.H + h0 + h] : 0.f;
-        };
-        float at[HG], ach[HG][4];
-
-        // ---- chunk-local inclusive cumsum of dt*A for tile it, all heads, every
-        //      warpgroup; leaves a_t and the 32-block ends in registers and the
-        //      per-column mask factors in shared memory
-        auto cumsum_tile = [&](int it) {
-#pragma unroll
-            for (int h = 0; h < HG; ++h) dtv[h] = dt_next[h];
-            if (it + 1 < ntile) load_dt(k0 + it + 1, dt_next);   // one tile ahead
-            named_bar_sync(kBarAll, 32 * kXWarps);       // previous readers of u/v are done
+        for (int h = 0; h < HG; ++h) Dh[h] = a.D ? a.D[h0 + h] : 0.f;
+        // this thread's token: a_t, the tile's 32-block ends a_e(j) and the state
+        // weight w_t = exp(a_end - a_t) dt_t = v_t exp(a_end - a_e(block of t))
+        float at[HG], ach[HG][4], wt[HG];
+        auto load_factors = [&](int it) {
+            wait_bar_warp(bar(13), it & 1, abort_flag, a.err);
 #pragma unroll
             for (int h = 0; h < HG; ++h) {
-                float incl = dtv[h] * Ah[h];
-#pragma unroll
-                for (int off = 1; off < 32; off <<= 1) {
-                    const float o = __shfl_up_sync(0xffffffffu, incl, off);
-                    if (lane >= off) incl += o;
-                }
-                at[h] = incl;
-                if (lane == 31) wtot_s[(wg * 2 + h) * 4 + q] = incl;
+                const float4 e = *reinterpret_cast<const float4 *>(ach_s + 4 * h);
+                ach[h][0] = e.x;
+                ach[h][1] = e.y;
+                ach[h][2] = e.z;
+                ach[h][3] = e.w;
+                at[h] = at_s[h * kTile + row];
+                const float aq = q == 0 ? e.x : (q == 1 ? e.y : (q == 2 ? e.z : e.w));
+                wt[h] = v_s[h * kTile + row] * __expf(e.w - aq);
             }
-            named_bar_sync(1 + wg, 128);
-#pragma unroll
-            for (int h = 0; h < HG; ++h) {
-                const float *wt = wtot_s + (wg * 2 + h) * 4;
-                ach[h][0] = wt[0];
-                ach[h][1] = ach[h][0] + wt[1];
-                ach[h][2] = ach[h][1] + wt[2];
-                ach[h][3] = ach[h][2] + wt[3];
-                at[h] += q == 0 ? 0.f : (q == 1 ? ach[h][0] : (q == 2 ? ach[h][1] : ach[h][2]));
-            }
-            if (wg < HG) {
-                // per-column factors of this warpgroup's head:
-                //   u_s = log(dt_s) - a_s                 (diagonal 32-block: exp(a_t + u_s))
-                //   v_s = exp(a_end(block of s) - a_s) dt_s   (blocks left of the diagonal)
-                const int h = wg;
-                const float aq = q == 0 ? ach[h][0] : (q == 1 ? ach[h][1] : (q == 2 ? ach[h][2] : ach[h][3]));
-                u_s[h * kTile + row] = dtv[h] > 0.f ? __logf(dtv[h]) - at[h] : -INFINITY;
-                v_s[h * kTile + row] = __expf(aq - at[h]) * dtv[h];
-            }
-            named_bar_sync(kBarAll, 32 * kXWarps);
         };
 
         // ---- all heads of tile it: entering state -> bf16 operand (MN-major rows n),
-        //      state scaled by the tile decay, and Xt = w o X, w_s = exp(a_end - a_s) dt_s
+        //      state scaled by the tile decay, and Xt = w o X
         auto prep_tile = [&](int it) {
             const uint8_t *stg_ptr = tiles_ptr + (it & 1) * kStage;
-            wait_bar_warp(bar(it & 1), (it >> 1) & 1, abort_flag, a.err);   // X landed
+            wait_bar_warp(bar(14 + (it & 1)), (it >> 1) & 1, abort_flag, a.err);   // X landed
             if (it > 0) wait_bar_warp(bar(9), (it - 1) & 1, abort_flag, a.err);
             tc_fence_after();
             if (it == 0 && sigma > 0) griddep_wait();   // entering states of later segments
@@ -431,14 +521,13 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
 #pragma unroll
                 for (int j = 0; j < 16; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * de);
                 tmem_st16(tq + colH, r);
-                const float w = __expf(ach[h][3] - at[h]) * dtv[h];
                 const uint8_t *xs = stg_ptr + kCBytes + h * kXBytes;
                 uint8_t *xt = xt_ptr + h * kXBytes;
 #pragma unroll
                 for (int c = 2 * wg; c < 2 * wg + 2; ++c) {
                     const uint32_t off = sw128(row, 8 * c);
                     *reinterpret_cast<uint4 *>(xt + off) =
-                        scale_bf16x8(*reinterpret_cast<const uint4 *>(xs + off), w);
+                        scale_bf16x8(*reinterpret_cast<const uint4 *>(xs + off), wt[h]);
                 }
             }
             fence_proxy_async_smem();
@@ -448,11 +537,10 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
             if (lane == 0) mbar_arrive(bar(8));
         };
 
-        // Software pipeline: the next tile's cumsum and state prep run while the
-        // tensor core finishes this tile, then this tile's epilogue.
+        // Software pipeline: the next tile's state prep runs while the tensor core
+        // finishes this tile, then this tile's epilogue.
         if (ntile > 0) {
-            load_dt(k0, dt_next);
-            cumsum_tile(0);
+            load_factors(0);
             prep_tile(0);
         }
         for (int it = 0; it < ntile; ++it) {
@@ -461,7 +549,7 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
             const uint8_t *stg_ptr = tiles_ptr + stage * kStage;
 
             // ---- mask for the 32-token column block j = wg, all heads:
-            //      M = G o exp(a_t - a_s) dt_s (s <= t) + D on the diagonal.
+            //      M = G o exp(a_t - a_s) dt_s (s <= t).
             //      exp(a_t - a_s) dt_s = R_t v_s with R_t = exp(a_t - a_e(j)) and
             //      v_s = exp(a_e(j) - a_s) dt_s, e(j) the block's last token: left of
             //      the diagonal both factors are <= 1; on the diagonal block R_t is
@@ -483,12 +571,19 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
 #pragma unroll
                         for (int e = 0; e < 16; ++e) mr[e] = 0u;
                     } else if (q == j && abj - aej > kMaxBlockDecay) {
-                        const float *uh = u_s + hh * kTile + 32 * j;
+                        // exp(a_t - a_s) dt_s = exp(a_t - a_s + log dt_s) element by element
+                        const float *ah = at_s + hh * kTile + 32 * j;
+                        const int tb = t0 + 32 * j;
+                        auto lw = [&](int s) {
+                            const int tok = tb + s;
+                            const float d = tok < a.L ? a.dt[((size_t)b * a.L + tok) * a.H + h0 + hh] : 0.f;
+                            return d > 0.f ? __expf(at[hh] - ah[s] + __logf(d)) : 0.f;
+                        };
 #pragma unroll
                         for (int e = 0; e < 16; ++e) {
                             const int s0 = 2 * e;
-                            const float m0 = s0 <= lane ? __uint_as_float(gr[2 * e]) * __expf(at[hh] + uh[s0]) : 0.f;
-                            const float m1 = s0 + 1 <= lane ? __uint_as_float(gr[2 * e + 1]) * __expf(at[hh] + uh[s0 + 1]) : 0.f;
+                            const float m0 = s0 <= lane ? __uint_as_float(gr[2 * e]) * lw(s0) : 0.f;
+                            const float m1 = s0 + 1 <= lane ? __uint_as_float(gr[2 * e + 1]) * lw(s0 + 1) : 0.f;
                             mr[e] = pack_bf16x2(m0, m1);
                         }
                     } else {
@@ -523,21 +618,20 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(7));
 
-            // exp(a_t) of this tile for its epilogue, before the next tile's cumsum
+            // exp(a_t) of this tile for its epilogue, before the next tile's factors
             float e_at_t[HG];
 #pragma unroll
             for (int h = 0; h < HG; ++h) e_at_t[h] = __expf(at[h]);
             if (it + 1 < ntile) {
-                cumsum_tile(it + 1);
+                load_factors(it + 1);
                 prep_tile(it + 1);
             }
 
-            // ---- epilogue: y = Yd + exp(a_t) Yo, staged as bf16 in this stage's C
-            //      blocks (free once the tile's MMAs are done; head h in block h) and
-            //      written by TMA stores
+            // ---- epilogue: y = Yd + exp(a_t) Yo + D x, staged as bf16 in this
+            //      stage's C blocks (free once the tile's off-diagonal product is
+            //      done; head h in block h) for issuer B's TMA stores
             wait_bar_warp(bar(10), it & 1, abort_flag, a.err);
             tc_fence_after();
-            uint8_t *ystage = tiles_ptr + stage * kStage;
             {
                 // (head, 32-column range) of this warpgroup: HG = 2 -> head wg & 1,
                 // columns 32 (wg >> 1) ..; HG = 1 -> head 0, columns 16 wg ..
@@ -547,8 +641,8 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
                 // selects, not dynamic indexing (which would move the arrays to local memory)
                 const float e_at = (HG == 2 && hh == 1) ? e_at_t[HG - 1] : e_at_t[0];
                 const float dsk = (HG == 2 && hh == 1) ? Dh[HG - 1] : Dh[0];
-                const uint8_t *xs = stg_ptr + kCBytes + hh * kXBytes;
-                uint8_t *ybuf = ystage + hh * kBlk;
+                const uint8_t *xs = tiles_ptr + stage * kStage + kCBytes + hh * kXBytes;
+                uint8_t *ybuf = tiles_ptr + stage * kStage + hh * kBlk;
 #pragma unroll
                 for (int c16 = 0; c16 < np; c16 += 16) {
                     const int pc = p0 + c16;
@@ -581,16 +675,9 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
             fence_proxy_async_smem();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(11));
-            named_bar_sync(kBarAll, 32 * kXWarps);        // the whole y tile is staged
-            if (warp == 2 && lane == 0) {
-                if (!*abort_flag) {
-#pragma unroll
-                    for (int h = 0; h < HG; ++h)
-                        tma_store_4d(&mapY, tiles_base + stage * kStage + h * kBlk, 0, h0 + h, t0, b);
-                    bulk_commit();
-                }
-                mbar_arrive(bar(2 + stage));   // loads into this stage queue behind the store
+            if (lane == 0) {
+                mbar_arrive(bar(11));          // y staged, Yd / Yo read
+                mbar_arrive(bar(16 + stage));  // this tile's X read
             }
         }
         // ---- final state of the sequence (all MMAs completed: y_full of the last tile)
@@ -607,7 +694,6 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
             }
         }
     }
-    if (warp == 2 && lane == 0) bulk_wait_all();     // y stores complete before exit
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {

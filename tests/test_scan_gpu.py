@@ -85,6 +85,17 @@ def test_tc_path_many_segments():
     _check(inp, "bf16", 256, TC)
 
 
+@pytest.mark.parametrize("scale", [20.0, 200.0])
+def test_tc_path_strong_decay(scale):
+    """Step sizes up to 2 (or 20) with |A| up to 16: the decay across one
+    32-token block reaches hundreds of e-folds, beyond the factored mask's
+    range, so diagonal blocks take the one-exponential-per-element form and
+    long stretches of the state underflow to zero."""
+    inp = gen.scan_inputs(2, 700, 4, 64, 128, 2, "bf16", seed=23, random_init=True)
+    inp["dt"] = (inp["dt"] * scale).astype(np.float32)
+    _check(inp, "bf16", 256, TC)
+
+
 def test_tc_path_without_skip():
     inp = gen.scan_inputs(1, 512, 4, 64, 128, 1, "bf16", seed=7, with_D=False)
     _check(inp, "bf16", 256, TC)
