@@ -284,6 +284,12 @@ __device__ __forceinline__ uint64_t mul_f32x2(uint64_t a, uint64_t b) {
     asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
     return d;
 }
+// d = a * b + c lane-wise, one rounding per lane
+__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
 __device__ __forceinline__ uint32_t pack_bf16x2_from_f32x2(uint64_t v) {
     return pack_bf16x2(__uint_as_float((uint32_t)v), __uint_as_float((uint32_t)(v >> 32)));
 }

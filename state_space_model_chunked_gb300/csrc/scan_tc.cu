@@ -93,7 +93,7 @@ constexpr uint32_t kIdS = idesc_bf16_f32(128, 64, true, true);      // B^T . Xt
 constexpr uint32_t kIdY = idesc_bf16_f32(128, 64, false, true);     // M(TMEM) . X
 
 // control-region offsets (bytes)
-constexpr uint32_t kOffTslot = 192;       // (barriers occupy bytes 0 .. 143)
+constexpr uint32_t kOffTslot = 192;       // (barriers occupy bytes 0 .. 151)
 constexpr uint32_t kOffAbort = 196;
 constexpr uint32_t kOffWtot = 256;        // segment kernel: float[2 warpgroups][2 heads][4 warps]
 // scan kernel factor slot, written by the factor warp for one tile at a time
@@ -136,14 +136,13 @@ __device__ __forceinline__ uint32_t sw128(uint32_t row, uint32_t col) {
 }
 
 __device__ __forceinline__ uint4 scale_bf16x8(uint4 v, float w) {
-    uint32_t in[4] = {v.x, v.y, v.z, v.w};
+    const uint32_t in[4] = {v.x, v.y, v.z, v.w};
+    const uint64_t w2 = pack_f32x2(w, w);
     uint32_t out[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const float lo = __uint_as_float(in[i] << 16) * w;
-        const float hi = __uint_as_float(in[i] & 0xffff0000u) * w;
-        out[i] = pack_bf16x2(lo, hi);
-    }
+    for (int i = 0; i < 4; ++i)
+        out[i] = pack_bf16x2_from_f32x2(mul_f32x2(
+            pack_f32x2(__uint_as_float(in[i] << 16), __uint_as_float(in[i] & 0xffff0000u)), w2));
     return make_uint4(out[0], out[1], out[2], out[3]);
 }
 
@@ -189,8 +188,9 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
     // barriers: 0,1 fullC[stage]; 2,3 emptyC[stage]; 4 fullB; 5 emptyB;
     //           6 g_full; 7 m_ready; 8 hx_ready; 9 hx_free; 10 y_full;
     //           11 y_done (Yd / Yo read, y staged over C); 12 g_free (the masks
-    //           in TMEM have been consumed); 13 fac_ready (factor slot written);
-    //           14,15 fullX[stage]; 16,17 emptyX[stage]
+    //           in TMEM have been consumed); 13 at_ready (a_t and block ends of
+    //           the next tile written); 14,15 fullX[stage]; 16,17 emptyX[stage];
+    //           18 v_ready (v_s of the next tile written)
     auto bar = [&](int i) { return sbase + 8u * (uint32_t)i; };
     uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + kOffTslot);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kOffAbort);
@@ -216,8 +216,8 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
         mbar_init(bar(3), 2);
         mbar_init(bar(14), 1);
         mbar_init(bar(15), 1);
-        mbar_init(bar(16), 1 + kXWarps);
-        mbar_init(bar(17), 1 + kXWarps);
+        mbar_init(bar(16), HG + kXWarps);
+        mbar_init(bar(17), HG + kXWarps);
         mbar_init(bar(4), 1);
         mbar_init(bar(5), 1);
         mbar_init(bar(6), 1);
@@ -226,7 +226,7 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
         mbar_init(bar(9), 1);
         mbar_init(bar(10), 2);
         mbar_init(bar(11), kXWarps);
-        mbar_init(bar(12), 1);
+        mbar_init(bar(12), HG);                // one commit per masked-product issuer
         mbar_init(bar(13), 1);
         *abort_flag = 0;
         fence_mbar_init();
@@ -286,6 +286,8 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
             const uint64_t bMN = smem_desc(b_base, kBlk, 1024, kSwizzle128B);
             const uint64_t hbD = smem_desc(hb_base, kXBytes, 1024, kSwizzle128B);
             const uint64_t xtD = smem_desc(xt_base, kXBytes, 1024, kSwizzle128B);
+            const uint64_t xlastD = smem_desc(tiles_base + kCBytes + (HG - 1) * kXBytes, kBlk, 1024,
+                                              kSwizzle128B);
             for (int it = 0; it < ntile; ++it) {
                 const int stage = it & 1;
                 const uint64_t so = stage ? (uint64_t)(kStage >> 4) : 0ull;
@@ -320,12 +322,27 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
                 }
                 mma_commit(bar(9));                     // Hb / Xt free, H updated
                 mma_commit(bar(2 + stage));
+                if (HG == 2) {
+                    // the second head's masked product, split off issuer B's stream
+                    if (!wait_bar(bar(14 + stage), (it >> 1) & 1, abort_flag, a.err)) break;
+                    if (!wait_bar(bar(7), it & 1, abort_flag, a.err)) break;
+                    tc_fence_after();
+                    const uint64_t xD = xlastD + (stage ? (uint64_t)(kStage >> 4) : 0ull);
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint32_t acol = kColG + 32 * (kk >> 1) + 16 * (HG - 1) + 8 * (kk & 1);
+                        mma_ts(tmem + kColYd + 64 * (HG - 1), tmem + acol, xD + (uint64_t)(kk * 128),
+                               kIdY, kk > 0);
+                    }
+                    mma_commit(bar(12));
+                    mma_commit(bar(16 + stage));
+                }
                 mma_commit(bar(10));
             }
         }
     } else if (warp == kIssuerB) {
         // ------------------------------------------------ MMA issuer B
-        // Intra-chunk outputs Yd_h = M_h . X_h once the masks are in TMEM.  It
+        // Intra-chunk output Yd_0 = M_0 . X_0 once the masks are in TMEM.  It
         // also sends out each tile's y (staged over its C tile by the epilogue)
         // by TMA as soon as the epilogue is done, and releases that C buffer
         // once the store has read it.
@@ -354,15 +371,11 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
                     mbar_arrive(bar(2 + (stage ^ 1)));       // tile it-1's C buffer
                 }
                 tc_fence_after();
+                // head 0 (issuer A takes the second head of a pair)
 #pragma unroll
-                for (int hh = 0; hh < HG; ++hh) {
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
-                        const uint32_t acol = kColG + 32 * (kk >> 1) + 16 * hh + 8 * (kk & 1);
-                        mma_ts(tmem + kColYd + 64 * hh, tmem + acol,
-                               xD + (uint64_t)((hh * kXBytes) >> 4) + (uint64_t)(kk * 128), kIdY,
-                               kk > 0);
-                    }
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t acol = kColG + 32 * (kk >> 1) + 8 * (kk & 1);
+                    mma_ts(tmem + kColYd, tmem + acol, xD + (uint64_t)(kk * 128), kIdY, kk > 0);
                 }
                 mma_commit(bar(12));
                 mma_commit(bar(16 + stage));
@@ -376,9 +389,10 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
     } else if (warp == kFacWarp) {
         // ------------------------------------------ decay factors and y stores
         // Lane l owns tokens 4l .. 4l+3 of a tile.  The factors of tile k are
-        // computed in registers ahead of time and written to the factor slot as
-        // soon as every mask of tile k-1 is built (the masks are the last readers
-        // of the slot's v_s).
+        // computed in registers ahead of time.  a_t and the block ends go to
+        // the slot once every transform warp has loaded tile k-1's (its state
+        // prep is done); v_s once every mask of tile k-1 is built (the masks
+        // are the only readers of v_s).
         float Af[HG], dn[HG][4];
         float fa[HG][4], fv[HG][4], fe[HG][4];
 #pragma unroll
@@ -464,8 +478,9 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
         float Dh[HG];
 #pragma unroll
         for (int h = 0; h < HG; ++h) Dh[h] = a.D ? a.D[h0 + h] : 0.f;
-        // this thread's token: a_t, the tile's 32-block ends a_e(j) and the state
-        // weight w_t = exp(a_end - a_t) dt_t = v_t exp(a_end - a_e(block of t))
+        // this thread's token: dt_t (this tile's and, in flight, the next
+        // tile's), a_t, the tile's 32-block ends a_e(j) and the state weight
+        // w_t = exp(a_end - a_t) dt_t
         float at[HG], ach[HG][4], wt[HG];
         auto load_factors = [&](int it) {
             wait_bar_warp(bar(13), it & 1, abort_flag, a.err);
@@ -518,8 +533,13 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
                     make_uint4(pk[0], pk[1], pk[2], pk[3]);
                 *reinterpret_cast<uint4 *>(hb + sw128(row, 16 * wg + 8)) =
                     make_uint4(pk[4], pk[5], pk[6], pk[7]);
+                const uint64_t de2 = pack_f32x2(de, de);
 #pragma unroll
-                for (int j = 0; j < 16; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * de);
+                for (int j = 0; j < 16; j += 2) {
+                    const uint64_t v = mul_f32x2(pack_f32x2(__uint_as_float(r[j]), __uint_as_float(r[j + 1])), de2);
+                    r[j] = (uint32_t)v;
+                    r[j + 1] = (uint32_t)(v >> 32);
+                }
                 tmem_st16(tq + colH, r);
                 const uint8_t *xs = stg_ptr + kCBytes + h * kXBytes;
                 uint8_t *xt = xt_ptr + h * kXBytes;
@@ -571,7 +591,6 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
 #pragma unroll
                         for (int e = 0; e < 16; ++e) mr[e] = 0u;
                     } else if (q == j && abj - aej > kMaxBlockDecay) {
-                        // exp(a_t - a_s) dt_s = exp(a_t - a_s + log dt_s) element by element
                         const float *ah = at_s + hh * kTile + 32 * j;
                         const int tb = t0 + 32 * j;
                         auto lw = [&](int s) {
@@ -641,6 +660,7 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
                 // selects, not dynamic indexing (which would move the arrays to local memory)
                 const float e_at = (HG == 2 && hh == 1) ? e_at_t[HG - 1] : e_at_t[0];
                 const float dsk = (HG == 2 && hh == 1) ? Dh[HG - 1] : Dh[0];
+                const uint64_t ea2 = pack_f32x2(e_at, e_at), dsk2 = pack_f32x2(dsk, dsk);
                 const uint8_t *xs = tiles_ptr + stage * kStage + kCBytes + hh * kXBytes;
                 uint8_t *ybuf = tiles_ptr + stage * kStage + hh * kBlk;
 #pragma unroll
@@ -659,11 +679,12 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
                             const int i = 8 * half + 2 * e;
-                            const float x0 = __uint_as_float(xw[e] << 16);
-                            const float x1 = __uint_as_float(xw[e] & 0xffff0000u);
-                            pk[4 * half + e] = pack_bf16x2(
-                                fmaf(dsk, x0, fmaf(e_at, __uint_as_float(yo[i]), __uint_as_float(yd[i]))),
-                                fmaf(dsk, x1, fmaf(e_at, __uint_as_float(yo[i + 1]), __uint_as_float(yd[i + 1]))));
+                            const uint64_t x01 = pack_f32x2(__uint_as_float(xw[e] << 16),
+                                                            __uint_as_float(xw[e] & 0xffff0000u));
+                            const uint64_t y01 = fma_f32x2(
+                                ea2, pack_f32x2(__uint_as_float(yo[i]), __uint_as_float(yo[i + 1])),
+                                pack_f32x2(__uint_as_float(yd[i]), __uint_as_float(yd[i + 1])));
+                            pk[4 * half + e] = pack_bf16x2_from_f32x2(fma_f32x2(dsk2, x01, y01));
                         }
                     }
                     *reinterpret_cast<uint4 *>(ybuf + sw128(row, pc)) =
