@@ -65,11 +65,11 @@ constexpr int kXWarps = 16;                // scan kernel: transform/epilogue wa
 constexpr int kThreads = 64 + 32 * kXWarps + 64;
 constexpr int kIssuerB = 2 + kXWarps;      // warp index of the second MMA issuer
 constexpr int kFacWarp = 3 + kXWarps;      // warp index of the factor warp
-constexpr int kSegXWarps = 8;              // segment kernel: transform warps
-constexpr int kSegThreads = 64 + 32 * kSegXWarps;
+constexpr int kSegXWarps = 8;              // segment kernel: X scaling warps
+constexpr int kSegFacWarp = 2 + kSegXWarps;  // segment kernel: token weight warp
+constexpr int kSegThreads = 64 + 32 * kSegXWarps + 32;
+constexpr int kSegStages = 3;              // segment kernel: B + X stages
 constexpr uint64_t kWaitNs = 2000000000ull;
-// named barriers: 1 + warpgroup for one warpgroup, kBarAll for all transform warps
-constexpr int kBarAll = 8;
 // Largest decay (in log units) across one 32-token block for which the mask's
 // diagonal block uses the factored form (its R_t factor stays below e^60).
 constexpr float kMaxBlockDecay = 60.f;
@@ -95,7 +95,6 @@ constexpr uint32_t kIdY = idesc_bf16_f32(128, 64, false, true);     // M(TMEM) .
 // control-region offsets (bytes)
 constexpr uint32_t kOffTslot = 192;       // (barriers occupy bytes 0 .. 151)
 constexpr uint32_t kOffAbort = 196;
-constexpr uint32_t kOffWtot = 256;        // segment kernel: float[2 warpgroups][2 heads][4 warps]
 // scan kernel factor slot, written by the factor warp for one tile at a time
 constexpr uint32_t kOffAch = 256;         // float[2][4]: a at the end of each 32-token block
 constexpr uint32_t kOffAt = 512;          // float[2][128]: a_t, chunk-local inclusive cumsum of dt A
@@ -727,12 +726,18 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
 // F_sigma = sum over the segment's tokens of exp(a_end(segment) - a_s) dt_s
 //           x_s B_s^T, with tiles visited last to first so the decay from a
 // tile's end to the segment's end is a running sum of tile totals.
+//
+// Warp roles: warp 0 issues TMA loads (B and X of a tile per stage), warp 1
+// issues F += B^T . (w o X) for all heads of the CTA at once, warps 2-9 scale
+// each X tile in place by its token weights, and warp 10 computes the weights
+// w_s = exp(decay from s to the segment end) dt_s of each tile into a ring
+// with one slot per stage.
 template <int HG>
 __global__ void __launch_bounds__(kSegThreads, 1)
 ssd_tc_segment_kernel(const __grid_constant__ CUtensorMap mapB,
                       const __grid_constant__ CUtensorMap mapX, const TcArgs a) {
     extern __shared__ __align__(1024) uint8_t smem[];
-    constexpr int kStages = 3;
+    constexpr int kStages = kSegStages;
     constexpr uint32_t kStage = kBBytes + HG * kXBytes;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int h0 = blockIdx.x * HG;
@@ -748,22 +753,25 @@ ssd_tc_segment_kernel(const __grid_constant__ CUtensorMap mapB,
         if (threadIdx.x == 0) ssd_report(a.err, SSD_DEVERR_SMEM_ALIGN);
         return;
     }
-    // barriers: 0..2 full, 3..5 empty, 6 xt_ready, 7 xt_free
+    // barriers: 0..2 full[stage] (B, X landed); 3..5 empty[stage] (MMA done);
+    //           6..8 xt_ready[stage] (X scaled); 9..11 w_ready[stage]; 12 done
     auto bar = [&](int i) { return sbase + 8u * (uint32_t)i; };
     uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + kOffTslot);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kOffAbort);
-    float *wtot_s = reinterpret_cast<float *>(smem + kOffWtot);
     const uint32_t tiles_base = sbase + kCtrl;
-    const uint32_t xt_base = tiles_base + kStages * kStage;
     uint8_t *tiles_ptr = smem + kCtrl;
-    uint8_t *xt_ptr = tiles_ptr + kStages * kStage;
+    float *w_ring = reinterpret_cast<float *>(tiles_ptr + kStages * kStage);   // [stage][HG][128]
     constexpr uint32_t kCols = HG == 2 ? 128 : 64;
     griddep_launch_dependents();
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < 6; ++i) mbar_init(bar(i), 1);
-        mbar_init(bar(6), kSegXWarps);
-        mbar_init(bar(7), 1);
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(bar(i), 1);
+            mbar_init(bar(3 + i), 1);
+            mbar_init(bar(6 + i), kSegXWarps);
+            mbar_init(bar(9 + i), 1);
+        }
+        mbar_init(bar(12), 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -777,6 +785,7 @@ ssd_tc_segment_kernel(const __grid_constant__ CUtensorMap mapB,
     const uint32_t tmem = *tslot;
 
     if (warp == 0) {
+        // ------------------------------------------------------ TMA producer
         if (lane == 0) {
             tma_prefetch_desc(&mapB);
             tma_prefetch_desc(&mapX);
@@ -796,92 +805,129 @@ ssd_tc_segment_kernel(const __grid_constant__ CUtensorMap mapB,
             }
         }
     } else if (warp == 1) {
+        // ------------------------------------------------------ MMA issuer
         if (lane == 0) {
+            constexpr uint32_t kIdSAll = idesc_bf16_f32(128, 64 * HG, true, true);
+            const uint64_t bD = smem_desc(tiles_base, kBlk, 1024, kSwizzle128B);
+            const uint64_t xD = smem_desc(tiles_base + kBBytes, kXBytes, 1024, kSwizzle128B);
             for (int it = 0; it < ntile; ++it) {
                 const int stage = it % kStages;
-                const uint32_t stg = tiles_base + stage * kStage;
-                if (!wait_bar(bar(stage), (it / kStages) & 1, abort_flag, a.err)) break;
-                if (!wait_bar(bar(6), it & 1, abort_flag, a.err)) break;
+                const uint64_t so = (uint64_t)((stage * kStage) >> 4);
+                if (!wait_bar(bar(6 + stage), (it / kStages) & 1, abort_flag, a.err)) break;
                 tc_fence_after();
-                // all heads at once: F += B^T . [Xt_0 | Xt_1]  (N = 64 * HG)
-                constexpr uint32_t kIdSAll = idesc_bf16_f32(128, 64 * HG, true, true);
+                // all heads at once: F += B^T . [w o X_0 | w o X_1]  (N = 64 * HG)
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
-                    mma_ss(tmem, smem_desc(stg + kk * 2048, kBlk, 1024, kSwizzle128B),
-                           smem_desc(xt_base + kk * 2048, kXBytes, 1024, kSwizzle128B), kIdSAll,
-                           (it > 0 || kk > 0) ? 1u : 0u);
+                    mma_ss(tmem, bD + so + (uint64_t)(kk * 128), xD + so + (uint64_t)(kk * 128),
+                           kIdSAll, (it > 0 || kk > 0) ? 1u : 0u);
                 mma_commit(bar(3 + stage));
-                mma_commit(bar(7));
             }
+            mma_commit(bar(12));
         }
-    } else {
-        const int tw = warp - 2;
-        const int wg = tw >> 2;               // warpgroup 0..1
-        const int q = warp & 3;
-        const int row = 32 * q + lane;
-        const uint32_t tq = tmem + ((uint32_t)(32 * q) << 16);
-        float Ah[HG], suf[HG], dt_next[HG];
+    } else if (warp == kSegFacWarp) {
+        // ------------------------------------------------- token weights
+        // Lane l owns tokens 4l .. 4l+3 of a tile: w_s = exp(suffix of dt A from
+        // s to the segment end) dt_s; suf carries the totals of the tiles done.
+        // dt is loaded three tiles ahead (a tile takes about a microsecond here,
+        // less than a loaded memory system's latency).
+        float Af[HG], suf[HG], d0[HG][4], d1[HG][4], d2[HG][4];
 #pragma unroll
         for (int h = 0; h < HG; ++h) {
-            Ah[h] = a.A[h0 + h];
+            Af[h] = a.A[h0 + h];
             suf[h] = 0.f;
         }
-        auto load_dt = [&](int k, float (&d)[HG]) {
-            const int tok = k * kTile + row;
+        auto load_dt4 = [&](int it, float (&dn)[HG][4]) {
+            const int tok0 = (k1 - 1 - it) * kTile + 4 * lane;
 #pragma unroll
-            for (int h = 0; h < HG; ++h)
-                d[h] = tok < a.L ? a.dt[((size_t)b * a.L + tok) * a.H + h0 + h] : 0.f;
+            for (int i = 0; i < 4; ++i) {
+                const int tok = tok0 + i;
+#pragma unroll
+                for (int h = 0; h < HG; ++h)
+                    dn[h][i] = (it < ntile && tok < a.L) ? a.dt[((size_t)b * a.L + tok) * a.H + h0 + h]
+                                                         : 0.f;
+            }
         };
-        if (ntile > 0) load_dt(k1 - 1, dt_next);
+        load_dt4(0, d0);
+        load_dt4(1, d1);
+        load_dt4(2, d2);
         for (int it = 0; it < ntile; ++it) {
             const int stage = it % kStages;
-            const uint8_t *stg_ptr = tiles_ptr + stage * kStage;
-            float dtv[HG];
+            float d[HG][4];
 #pragma unroll
-            for (int h = 0; h < HG; ++h) dtv[h] = dt_next[h];
-            if (it + 1 < ntile) load_dt(k1 - 2 - it, dt_next);
-            named_bar_sync(kBarAll, 32 * kSegXWarps);
-            float at[HG], aend[HG];
+            for (int h = 0; h < HG; ++h)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    d[h][i] = d0[h][i];
+                    d0[h][i] = d1[h][i];
+                    d1[h][i] = d2[h][i];
+                }
+            load_dt4(it + 3, d2);
+            float wv[HG][4];
 #pragma unroll
             for (int h = 0; h < HG; ++h) {
-                float incl = dtv[h] * Ah[h];
+                float c[4];
+                c[0] = d[h][0] * Af[h];
+#pragma unroll
+                for (int i = 1; i < 4; ++i) c[i] = c[i - 1] + d[h][i] * Af[h];
+                float incl = c[3];
 #pragma unroll
                 for (int off = 1; off < 32; off <<= 1) {
                     const float o = __shfl_up_sync(0xffffffffu, incl, off);
                     if (lane >= off) incl += o;
                 }
-                at[h] = incl;
-                if (lane == 31) wtot_s[(wg * 2 + h) * 4 + q] = incl;
+                float excl = __shfl_up_sync(0xffffffffu, incl, 1);
+                if (lane == 0) excl = 0.f;
+                const float tot = __shfl_sync(0xffffffffu, incl, 31);
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    wv[h][i] = __expf(suf[h] + tot - (excl + c[i])) * d[h][i];
+                suf[h] += tot;
             }
-            named_bar_sync(1 + wg, 128);
+            // the slot was last read by the scaling of tile it - kStages
+            if (it >= kStages)
+                wait_bar_warp(bar(6 + stage), ((it / kStages) - 1) & 1, abort_flag, a.err);
+            float *slot = w_ring + stage * HG * kTile;
+#pragma unroll
+            for (int h = 0; h < HG; ++h)
+                *reinterpret_cast<float4 *>(slot + h * kTile + 4 * lane) =
+                    make_float4(wv[h][0], wv[h][1], wv[h][2], wv[h][3]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(9 + stage));
+        }
+        if (lane == 0 && !*abort_flag) {
+#pragma unroll
+            for (int h = 0; h < HG; ++h)
+                a.ws_decay[((size_t)b * (a.nseg - 1) + sigma) * a.H + h0 + h] = __expf(suf[h]);
+        }
+    } else {
+        // ------------------------------------------- X scaling, then F out
+        const int tw = warp - 2;
+        const int wg = tw >> 2;               // warpgroup 0..1: X columns 32 wg ..
+        const int q = warp & 3;
+        const int row = 32 * q + lane;
+        const uint32_t tq = tmem + ((uint32_t)(32 * q) << 16);
+        for (int it = 0; it < ntile; ++it) {
+            const int stage = it % kStages;
+            uint8_t *stg_ptr = tiles_ptr + stage * kStage;
+            wait_bar_warp(bar(9 + stage), (it / kStages) & 1, abort_flag, a.err);   // weights
+            wait_bar_warp(bar(stage), (it / kStages) & 1, abort_flag, a.err);       // X landed
+            const float *slot = w_ring + stage * HG * kTile;
 #pragma unroll
             for (int h = 0; h < HG; ++h) {
-                const float *wt = wtot_s + (wg * 2 + h) * 4;
-                const float c1 = wt[0] + wt[1], c2 = c1 + wt[2];
-                aend[h] = c2 + wt[3];
-                at[h] += q == 0 ? 0.f : (q == 1 ? wt[0] : (q == 2 ? c1 : c2));
-            }
-            if (it > 0) wait_bar_warp(bar(7), (it - 1) & 1, abort_flag, a.err);
-            wait_bar_warp(bar(stage), (it / kStages) & 1, abort_flag, a.err);
-#pragma unroll
-            for (int h = 0; h < HG; ++h) {
-                // decay from this token to the end of the segment, times dt
-                const float w = __expf(suf[h] + aend[h] - at[h]) * dtv[h];
-                const uint8_t *xs = stg_ptr + kBBytes + h * kXBytes;
-                uint8_t *xt = xt_ptr + h * kXBytes;
+                const float w = slot[h * kTile + row];
+                uint8_t *xs = stg_ptr + kBBytes + h * kXBytes;
 #pragma unroll
                 for (int c = 4 * wg; c < 4 * wg + 4; ++c) {
                     const uint32_t off = sw128(row, 8 * c);
-                    *reinterpret_cast<uint4 *>(xt + off) =
+                    *reinterpret_cast<uint4 *>(xs + off) =
                         scale_bf16x8(*reinterpret_cast<const uint4 *>(xs + off), w);
                 }
-                suf[h] += aend[h];
             }
             fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(6));
+            if (lane == 0) mbar_arrive(bar(6 + stage));
         }
-        if (ntile > 0) wait_bar_warp(bar(7), (ntile - 1) & 1, abort_flag, a.err);
+        if (ntile > 0) wait_bar_warp(bar(12), 0, abort_flag, a.err);
         tc_fence_after();
         if (!*abort_flag) {
 #pragma unroll 1
@@ -894,8 +940,6 @@ ssd_tc_segment_kernel(const __grid_constant__ CUtensorMap mapB,
 #pragma unroll
                 for (int j = 0; j < 32; ++j)
                     dst[(size_t)(32 * wg + j) * kN + row] = __uint_as_float(r[j]);
-                if (wg == 0 && row == 0)
-                    a.ws_decay[((size_t)b * (a.nseg - 1) + sigma) * a.H + h0 + h] = __expf(suf[h]);
             }
         }
     }
@@ -993,7 +1037,7 @@ constexpr size_t scan_smem() {
 }
 template <int HG>
 constexpr size_t seg_smem() {
-    return kCtrl + 3 * (size_t)(kBBytes + HG * kXBytes) + HG * (size_t)kXBytes;
+    return kCtrl + kSegStages * (size_t)(kBBytes + HG * kXBytes) + kSegStages * HG * kTile * sizeof(float);
 }
 static_assert(scan_smem<2>() <= 232448, "scan kernel shared memory exceeds 227 KB");
 static_assert(seg_smem<2>() <= 232448, "segment kernel shared memory exceeds 227 KB");
