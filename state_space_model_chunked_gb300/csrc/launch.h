@@ -43,6 +43,7 @@ struct SsdTcPlan {
     int heads_per_cta;    // heads sharing one C.B^T product
     int seg_tiles;        // tiles per segment (the unit of sequence parallelism)
     int nseg;             // segments per sequence
+    int seg_heads;        // heads per CTA of the segment-contribution kernel
     size_t workspace;     // bytes of workspace required
     int launches;         // kernels enqueued per call
 };

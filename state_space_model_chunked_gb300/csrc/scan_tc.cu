@@ -68,7 +68,8 @@ constexpr int kFacWarp = 3 + kXWarps;      // warp index of the factor warp
 constexpr int kSegXWarps = 8;              // segment kernel: X scaling warps
 constexpr int kSegFacWarp = 2 + kSegXWarps;  // segment kernel: token weight warp
 constexpr int kSegThreads = 64 + 32 * kSegXWarps + 32;
-constexpr int kSegStages = 3;              // segment kernel: B + X stages
+// segment kernel: B + X stages (4 heads per CTA: 96 KB stages, two fit)
+constexpr int seg_stages(int hg) { return hg == 4 ? 2 : 3; }
 constexpr uint64_t kWaitNs = 2000000000ull;
 // Largest decay (in log units) across one 32-token block for which the mask's
 // diagonal block uses the factored form (its R_t factor stays below e^60).
@@ -725,7 +726,8 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
 // ============================================= segment contribution kernel
 // F_sigma = sum over the segment's tokens of exp(a_end(segment) - a_s) dt_s
 //           x_s B_s^T, with tiles visited last to first so the decay from a
-// tile's end to the segment's end is a running sum of tile totals.
+// tile's end to the segment's end is a running sum of tile totals.  HG heads
+// of one group (1, 2 or 4) share each B tile.
 //
 // Warp roles: warp 0 issues TMA loads (B and X of a tile per stage), warp 1
 // issues F += B^T . (w o X) for all heads of the CTA at once, warps 2-9 scale
@@ -737,7 +739,7 @@ __global__ void __launch_bounds__(kSegThreads, 1)
 ssd_tc_segment_kernel(const __grid_constant__ CUtensorMap mapB,
                       const __grid_constant__ CUtensorMap mapX, const TcArgs a) {
     extern __shared__ __align__(1024) uint8_t smem[];
-    constexpr int kStages = kSegStages;
+    constexpr int kStages = seg_stages(HG);
     constexpr uint32_t kStage = kBBytes + HG * kXBytes;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int h0 = blockIdx.x * HG;
@@ -761,7 +763,7 @@ ssd_tc_segment_kernel(const __grid_constant__ CUtensorMap mapB,
     const uint32_t tiles_base = sbase + kCtrl;
     uint8_t *tiles_ptr = smem + kCtrl;
     float *w_ring = reinterpret_cast<float *>(tiles_ptr + kStages * kStage);   // [stage][HG][128]
-    constexpr uint32_t kCols = HG == 2 ? 128 : 64;
+    constexpr uint32_t kCols = 64 * HG;        // F of every head (lane n, column p)
     griddep_launch_dependents();
 
     if (threadIdx.x == 0) {
@@ -1037,10 +1039,28 @@ constexpr size_t scan_smem() {
 }
 template <int HG>
 constexpr size_t seg_smem() {
-    return kCtrl + kSegStages * (size_t)(kBBytes + HG * kXBytes) + kSegStages * HG * kTile * sizeof(float);
+    return kCtrl + seg_stages(HG) * ((size_t)(kBBytes + HG * kXBytes) + HG * kTile * sizeof(float));
 }
 static_assert(scan_smem<2>() <= 232448, "scan kernel shared memory exceeds 227 KB");
 static_assert(seg_smem<2>() <= 232448, "segment kernel shared memory exceeds 227 KB");
+static_assert(seg_smem<4>() <= 232448, "segment kernel shared memory exceeds 227 KB");
+
+// Segment contributions with SG heads per CTA.
+template <int SG>
+cudaError_t launch_segment(const SsdTcPlan &plan, const CUtensorMap &mB, const CUtensorMap &mX,
+                           const TcArgs &args, int batch, int H, cudaStream_t stream) {
+    static std::once_flag attr_once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(attr_once, [] {
+        attr_err = cudaFuncSetAttribute(ssd_tc_segment_kernel<SG>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        (int)seg_smem<SG>());
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+    dim3 g1(H / SG, plan.nseg - 1, batch);
+    ssd_tc_segment_kernel<SG><<<g1, kSegThreads, seg_smem<SG>(), stream>>>(mB, mX, args);
+    return cudaGetLastError();
+}
 
 // Launch with programmatic stream serialization: the kernel may begin while
 // the previous kernel in the stream finishes; it calls griddepcontrol.wait
@@ -1071,16 +1091,12 @@ cudaError_t launch_hg(const SsdTcPlan &plan, const CUtensorMap &mC, const CUtens
         attr_err = cudaFuncSetAttribute(ssd_tc_scan_kernel<HG>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         (int)scan_smem<HG>());
-        if (attr_err == cudaSuccess)
-            attr_err = cudaFuncSetAttribute(ssd_tc_segment_kernel<HG>,
-                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                            (int)seg_smem<HG>());
     });
     if (attr_err != cudaSuccess) return attr_err;
     if (plan.nseg > 1) {
-        dim3 g1(H / HG, plan.nseg - 1, batch);
-        ssd_tc_segment_kernel<HG><<<g1, kSegThreads, seg_smem<HG>(), stream>>>(mB, mX, args);
-        cudaError_t e = cudaGetLastError();
+        cudaError_t e = plan.seg_heads == 4
+                            ? launch_segment<4>(plan, mB, mX, args, batch, H, stream)
+                            : launch_segment<HG>(plan, mB, mX, args, batch, H, stream);
         if (e != cudaSuccess) return e;
         const size_t total = (size_t)batch * H * kP * kN / 4;
         e = launch_pdl(ssd_tc_segment_pass_kernel, dim3((unsigned)((total + 255) / 256)),
@@ -1137,6 +1153,10 @@ SsdTcPlan ssd_tc_plan(int batch, int L, int H, int P, int N, int G, int num_sms)
     }
     p.seg_tiles = (p.tiles + best_n - 1) / best_n;
     p.nseg = (p.tiles + p.seg_tiles - 1) / p.seg_tiles;
+    // Four heads of a group share each B tile in the segment kernel, if that
+    // grid still covers every SM.
+    p.seg_heads = p.heads_per_cta;
+    if ((H / G) % 4 == 0 && (long)batch * (H / 4) * (p.nseg - 1) >= num_sms) p.seg_heads = 4;
     if (p.nseg > 1) {
         const size_t state = (size_t)batch * (p.nseg - 1) * H * kP * kN * sizeof(float);
         const size_t decay = (size_t)batch * (p.nseg - 1) * H * sizeof(float);

@@ -85,6 +85,15 @@ def test_tc_path_many_segments():
     _check(inp, "bf16", 256, TC)
 
 
+@pytest.mark.parametrize("b,H,G", [(4, 8, 2), (2, 16, 1)])
+def test_tc_path_many_segments_four_heads_per_group(b, H, G):
+    """Groups of four or more heads with enough segments (64 here) that the
+    segment contributions are computed four heads per CTA over one shared B
+    tile."""
+    inp = gen.scan_inputs(b, 8192, H, 64, 128, G, "bf16", seed=41 + G, random_init=True)
+    _check(inp, "bf16", 256, TC)
+
+
 @pytest.mark.parametrize("scale", [20.0, 200.0])
 def test_tc_path_strong_decay(scale):
     """Step sizes up to 2 (or 20) with |A| up to 16: the decay across one
