@@ -44,6 +44,24 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 
 
 # ----------------------------------------------------------------- helpers
+def ncu_traffic(kernel, workload):
+    """DRAM bytes per launch of `kernel` on `workload` from one ncu capture
+    (dram__bytes_read.sum + dram__bytes_write.sum), as recorded in
+    profiles/dram_traffic.json with the hash of the kernel's sources at capture
+    time; None when there is no capture or the sources have changed since."""
+    import hashlib
+    try:
+        with open(os.path.join(ROOT, "profiles", "dram_traffic.json")) as f:
+            entry = json.load(f)[kernel][workload]
+        h = hashlib.sha256()
+        for src in entry["sources"]:
+            with open(os.path.join(ROOT, src), "rb") as f:
+                h.update(f.read())
+    except (OSError, ValueError, KeyError, TypeError):
+        return None
+    return entry["bytes_per_launch"] if h.hexdigest() == entry["sources_sha256"] else None
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -432,7 +450,8 @@ def run_gpu(args):
                 "roofline": {"bound": "hbm", "achieved": lbytes / (lkern * 1e-3) / 1e9,
                              "peak": peaks["hbm_gbs"], "unit": "GB/s",
                              "frac": lbytes / (lkern * 1e-3) / 1e9 / peaks["hbm_gbs"],
-                             "traffic": None, "kernel": "ssd_tc_scan_kernel",
+                             "traffic": ncu_traffic("ssd_tc_scan_kernel", LONG_WORKLOAD),
+                             "kernel": "ssd_tc_scan_kernel",
                              "call_frac": lbytes / (lms * 1e-3) / 1e9 / peaks["hbm_gbs"]},
                 "tensor_tflops": lflops / (lms * 1e-3) / 1e12}
             torch.cuda.empty_cache()
@@ -462,7 +481,8 @@ def run_gpu(args):
                    "launch": "K calls captured in one CUDA graph, timed as one replay",
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
-                     "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+                     "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                     "traffic": ncu_traffic("ssd_tc_scan_kernel", WORKLOAD),
                      "peak_source": peaks["source"], "kernel": "ssd_tc_scan_kernel",
                      "kernel_ms": kern_ms,
                      "algorithmic_bytes": byts,
