@@ -145,6 +145,13 @@ __device__ __forceinline__ uint4 scale_bf16x8(uint4 v, float w) {
             pack_f32x2(__uint_as_float(in[i] << 16), __uint_as_float(in[i] & 0xffff0000u)), w2));
     return make_uint4(out[0], out[1], out[2], out[3]);
 }
+// The same with w rounded to bf16 first and bf16x2 multiplies (four instructions
+// instead of about twenty, for an extra relative error of at most 2^-9 from w).
+__device__ __forceinline__ uint4 scale_bf16x8_bf(uint4 v, float w) {
+    const uint32_t w2 = pack_bf16x2(w, w);
+    return make_uint4(mul_bf16x2(v.x, w2), mul_bf16x2(v.y, w2), mul_bf16x2(v.z, w2),
+                      mul_bf16x2(v.w, w2));
+}
 
 // ============================================================ scan kernel
 // Shared memory (HG heads per CTA): two stages of {C tile, X tile per head},
@@ -922,7 +929,7 @@ ssd_tc_segment_kernel(const __grid_constant__ CUtensorMap mapB,
                 for (int c = 4 * wg; c < 4 * wg + 4; ++c) {
                     const uint32_t off = sw128(row, 8 * c);
                     *reinterpret_cast<uint4 *>(xs + off) =
-                        scale_bf16x8(*reinterpret_cast<const uint4 *>(xs + off), w);
+                        scale_bf16x8_bf(*reinterpret_cast<const uint4 *>(xs + off), w);
                 }
             }
             fence_proxy_async_smem();

@@ -94,6 +94,21 @@ def test_tc_path_many_segments_four_heads_per_group(b, H, G):
     _check(inp, "bf16", 256, TC)
 
 
+def test_tc_path_48_heads_two_groups_32k_tokens():
+    """48 heads in two groups over 32768 tokens: 19 segments of 14 tiles, four
+    heads per segment-kernel CTA, head pairs in the scan kernel.  The oracle
+    checks six whole heads across both groups."""
+    inp = gen.scan_inputs(1, 32768, 48, 64, 128, 2, "bf16", seed=77, random_init=True)
+    y, f = scan_on_gpu(inp, "bf16", 256, TC)
+    heads = [0, 5, 23, 24, 30, 47]
+    g = [h // 24 for h in heads]
+    yr, fr = oracle.scan_seq(inp["x"][:, :, heads], inp["dt"][:, :, heads], inp["A"][heads],
+                             inp["B"][:, :, g], inp["C"][:, :, g], inp["D"][heads],
+                             inp["init"][:, heads])
+    assert rel(y[:, :, heads], yr) <= 1e-2
+    assert rel(f[:, heads], fr) <= 1e-2
+
+
 @pytest.mark.parametrize("scale", [20.0, 200.0])
 def test_tc_path_strong_decay(scale):
     """Step sizes up to 2 (or 20) with |A| up to 16: the decay across one
