@@ -163,6 +163,7 @@ ssd_decode_stream_kernel(float *__restrict__ state, const T *__restrict__ x,
         // ---- copy warp: loads run stages-1 units ahead; each updated state is
         //      written back as soon as its compute warps are done with it
         if (tid == kStreamThreads) {
+            const uint64_t evict_first = l2_evict_first_policy();   // states: touched once
             auto issue_load = [&](long k) {
                 const int st = (int)(k % stages);
                 const long u = unit_of(k);
@@ -171,7 +172,8 @@ ssd_decode_stream_kernel(float *__restrict__ state, const T *__restrict__ x,
                 const uint32_t dst = sbase + st * L.stage_bytes;
                 const uint32_t bar = smem_u32(full + st);
                 mbar_arrive_expect_tx(bar, L.state_bytes + L.x_bytes + 2 * L.bc_bytes);
-                bulk_load(dst, state + (size_t)u * P * N, L.state_bytes, bar);
+                bulk_load_evict_first(dst, state + (size_t)u * P * N, L.state_bytes, bar,
+                                      evict_first);
                 bulk_load(dst + L.state_bytes, x + (size_t)u * P, L.x_bytes, bar);
                 bulk_load(dst + L.state_bytes + L.x_bytes, Bm + grow, L.bc_bytes, bar);
                 bulk_load(dst + L.state_bytes + L.x_bytes + L.bc_bytes, Cm + grow, L.bc_bytes, bar);
@@ -184,8 +186,8 @@ ssd_decode_stream_kernel(float *__restrict__ state, const T *__restrict__ x,
                     ssd_report(err, SSD_DEVERR_TIMEOUT);
                     break;
                 }
-                bulk_store(state + (size_t)unit_of(k) * P * N, sbase + st * L.stage_bytes,
-                           L.state_bytes);
+                bulk_store_evict_first(state + (size_t)unit_of(k) * P * N,
+                                       sbase + st * L.stage_bytes, L.state_bytes, evict_first);
                 bulk_commit();
                 if (k + stages - 1 < nk) {
                     // its stage last held unit k-1, whose store must be done reading

@@ -120,6 +120,31 @@ __device__ __forceinline__ void bulk_store(void *dst, uint32_t src, uint32_t byt
                  "r"(src), "r"(bytes)
                  : "memory");
 }
+// L2 eviction priority for data touched once: a policy that marks the lines a
+// bulk copy brings in (or writes) as first to evict.  On the decode stream
+// (each state read once and written once per token) this lets the dirty lines
+// of the write stream drain without displacing anything still in use.
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ void bulk_load_evict_first(uint32_t dst, const void *src,
+                                                      uint32_t bytes, uint32_t bar,
+                                                      uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+        "[%0], [%1], %2, [%3], %4;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar), "l"(pol)
+        : "memory");
+}
+__device__ __forceinline__ void bulk_store_evict_first(void *dst, uint32_t src, uint32_t bytes,
+                                                       uint64_t pol) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group.L2::cache_hint [%0], [%1], %2, %3;" ::"l"(
+                     reinterpret_cast<uint64_t>(dst)),
+                 "r"(src), "r"(bytes), "l"(pol)
+                 : "memory");
+}
 __device__ __forceinline__ void bulk_commit() {
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
