@@ -31,15 +31,16 @@
 // group (ngroups divides nheads) are paired in one CTA so C.B^T is computed
 // once for both.
 //
-// Warp roles of the scan kernel (672 threads): warp 0 issues TMA loads, warp 1
-// allocates TMEM and issues C.B^T, the state update and the off-diagonal
-// product, warps 2-17 (four warpgroups) build the masks, keep the state and
-// run the epilogue, warp 18 issues the masked intra-chunk product M.X, warp 19
-// computes each tile's decay factors (cumsum of dt A and its exponentials)
-// ahead of use, and warp 20 issues the y stores.  The segment kernel uses
-// warps 0-9 with one issuer and the cumsum done by its transform warps.  Every wait is on
-// an mbarrier with a time limit; a wait that runs out sets the device error
-// word and the CTA fast-forwards to its exit without further loads or stores.
+// Warp roles of the scan kernel (640 threads): warp 1 allocates TMEM and issues
+// C.B^T, the state update, the off-diagonal product and the second head's
+// masked product; warps 2-17 (four warpgroups) build the masks, keep the state
+// and run the epilogue; warp 18 issues the first head's masked product and the
+// y stores; warps 0 and 19 are the TMA producer and the factor warp (each
+// tile's cumsum of dt A and its exponentials, computed ahead of use), in the
+// order the launch picks (template parameter kFacLow).  The segment kernel: warp 0 loads, warp 1 issues,
+// warps 2-9 scale X, warp 10 computes the token weights.  Every wait is on an
+// mbarrier with a time limit; a wait that runs out sets the device error word
+// and the CTA fast-forwards to its exit without further loads or stores.
 #include <cudaTypedefs.h>
 
 #include <mutex>
@@ -63,8 +64,16 @@ constexpr int kXWarps = 16;                // scan kernel: transform/epilogue wa
 // takes to execute, so two issuing warps feed the tensor core from two
 // instruction streams.
 constexpr int kThreads = 64 + 32 * kXWarps + 64;
-constexpr int kIssuerB = 2 + kXWarps;      // warp index of the second MMA issuer
-constexpr int kFacWarp = 3 + kXWarps;      // warp index of the factor warp
+// Warp w runs on SM sub-partition w % 4, and the transform warps' sub-partition
+// is fixed by their TMEM lane quarter (warp % 4): quarter 3 has the most mask
+// work, quarter 0 the least.  The producer and the factor warp take warps 0 and
+// 3 + kXWarps in an order chosen per launch (kFacLow): the factor warp
+// on the light sub-partition pays on long segments, the producer there on short
+// ones (its first loads are then the critical path).
+constexpr int kIssuerA = 1;                // first MMA issuer (also allocates TMEM)
+constexpr int kIssuerB = 2 + kXWarps;      // second MMA issuer
+constexpr int kSpareWarpLo = 0, kSpareWarpHi = 3 + kXWarps;   // producer / factor warp
+constexpr int kLongSegTiles = 24;          // from this many tiles per segment on
 constexpr int kSegXWarps = 8;              // segment kernel: X scaling warps
 constexpr int kSegFacWarp = 2 + kSegXWarps;  // segment kernel: token weight warp
 constexpr int kSegThreads = 64 + 32 * kSegXWarps + 32;
@@ -169,7 +178,7 @@ struct ScanLayout {
     static constexpr uint32_t kBytes = kOffXt + HG * kXBytes;
 };
 
-template <int HG>
+template <int HG, bool kFacLow>
 __global__ void __launch_bounds__(kThreads, 1)
 ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
                    const __grid_constant__ CUtensorMap mapB,
@@ -247,7 +256,9 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
     tc_fence_after();
     const uint32_t tmem = *tslot;
 
-    if (warp == 0) {
+    constexpr int fac_warp = kFacLow ? kSpareWarpLo : kSpareWarpHi;
+    constexpr int producer_warp = kFacLow ? kSpareWarpHi : kSpareWarpLo;
+    if (warp == producer_warp) {
         // ------------------------------------------------------ TMA producer
         if (lane == 0) {
             tma_prefetch_desc(&mapC);
@@ -281,7 +292,7 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
                 tma_load_4d(stg + kBlk, &mapC, bar(stage), 64, g, t0, b);
             }
         }
-    } else if (warp == 1) {
+    } else if (warp == kIssuerA) {
         // ------------------------------------------------------ MMA issuer
         // Descriptors are built once; a K step only adds its byte offset / 16 to
         // the start-address field.
@@ -393,13 +404,12 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
                 store_y(ntile - 1);
             bulk_wait_all();                                 // y stores complete before exit
         }
-    } else if (warp == kFacWarp) {
-        // ------------------------------------------ decay factors and y stores
+    } else if (warp == fac_warp) {
+        // ------------------------------------------------------ decay factors
         // Lane l owns tokens 4l .. 4l+3 of a tile.  The factors of tile k are
-        // computed in registers ahead of time.  a_t and the block ends go to
-        // the slot once every transform warp has loaded tile k-1's (its state
-        // prep is done); v_s once every mask of tile k-1 is built (the masks
-        // are the only readers of v_s).
+        // computed in registers ahead of time and written to the slot (a_t, the
+        // block ends, v_s) once every mask of tile k-1 is built: the masks are
+        // the last readers of the previous tile's v_s.
         float Af[HG], dn[HG][4];
         float fa[HG][4], fv[HG][4], fe[HG][4];
 #pragma unroll
@@ -1095,11 +1105,19 @@ cudaError_t launch_hg(const SsdTcPlan &plan, const CUtensorMap &mC, const CUtens
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(attr_once, [] {
-        attr_err = cudaFuncSetAttribute(ssd_tc_scan_kernel<HG>,
+        attr_err = cudaFuncSetAttribute(ssd_tc_scan_kernel<HG, false>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         (int)scan_smem<HG>());
+        if (attr_err == cudaSuccess)
+            attr_err = cudaFuncSetAttribute(ssd_tc_scan_kernel<HG, true>,
+                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                            (int)scan_smem<HG>());
     });
     if (attr_err != cudaSuccess) return attr_err;
+    // factor warp on the light sub-partition for long segments, the producer
+    // there for short ones (A/B timed on the 130M and 2.7B layers)
+    auto kernel = plan.seg_tiles >= kLongSegTiles ? ssd_tc_scan_kernel<HG, true>
+                                                  : ssd_tc_scan_kernel<HG, false>;
     if (plan.nseg > 1) {
         cudaError_t e = plan.seg_heads == 4
                             ? launch_segment<4>(plan, mB, mX, args, batch, H, stream)
@@ -1119,10 +1137,9 @@ cudaError_t launch_hg(const SsdTcPlan &plan, const CUtensorMap &mC, const CUtens
     cudaError_t e;
     if (plan.nseg > 1) {
         // overlaps the scan kernel's prologue and first tile with the chaining kernel
-        e = launch_pdl(ssd_tc_scan_kernel<HG>, g2, dim3(kThreads), scan_smem<HG>(), stream, mC, mB,
-                       mX, mY, args);
+        e = launch_pdl(kernel, g2, dim3(kThreads), scan_smem<HG>(), stream, mC, mB, mX, mY, args);
     } else {
-        ssd_tc_scan_kernel<HG><<<g2, kThreads, scan_smem<HG>(), stream>>>(mC, mB, mX, mY, args);
+        kernel<<<g2, kThreads, scan_smem<HG>(), stream>>>(mC, mB, mX, mY, args);
         e = cudaGetLastError();
     }
     if (e == cudaSuccess && prof.before && prof.after) e = ssd_record_event(prof.after, stream);
