@@ -260,27 +260,33 @@ def time_scan(shape, steps, warmup, device, l2_bytes, dist=None, graph=True):
 def time_scan_e2e(shape, steps, warmup, device):
     """Mtokens/s through the public API with pinned host buffers: per step the
     host->device copy of the inputs, the scan, and the device->host copy of y
-    and the final state."""
+    and the final state, with consecutive steps overlapped by the library's
+    HostScanPipeline (one step's inputs in flight while the previous one
+    computes and the one before returns its outputs).  Host wall time from the
+    first copy of the first timed step to the last byte of the last one."""
     import torch
     import state_space_model_chunked_gb300 as ssd
     s = make_scan_set(shape, 77, device)
     host = {k: (v.cpu().pin_memory() if v is not None else None)
             for k, v in s.items() if k not in ("y", "final")}
-    out = (torch.empty(s["y"].shape, dtype=s["y"].dtype, pin_memory=True),
-           torch.empty(s["final"].shape, dtype=torch.float32, pin_memory=True))
-    staging = {}
+    pipe = ssd.HostScanPipeline(device)
+    outs = [(torch.empty(s["y"].shape, dtype=s["y"].dtype, pin_memory=True),
+             torch.empty(s["final"].shape, dtype=torch.float32, pin_memory=True))
+            for _ in range(pipe.depth)]
+    out = outs[0]
 
-    def step():
-        ssd.scan_fwd_host(host["x"], host["dt"], host["A"], host["B"], host["C"], host["D"],
-                          shape.chunk, host["init"], device=device, staging=staging, out=out)
+    def step(i):
+        pipe.submit(host["x"], host["dt"], host["A"], host["B"], host["C"], host["D"],
+                    shape.chunk, host["init"], out=outs[i % pipe.depth])
 
-    for _ in range(max(warmup, 1)):
-        step()
+    for i in range(max(warmup, 1)):
+        step(i)
+    pipe.synchronize()
     torch.cuda.synchronize(device)
     t0 = time.perf_counter()
-    for _ in range(steps):
-        step()
-    torch.cuda.synchronize(device)
+    for i in range(steps):
+        step(i)
+    pipe.synchronize()
     dt = (time.perf_counter() - t0) / steps
     h2d = sum(v.numel() * v.element_size() for v in host.values() if v is not None)
     d2h = out[0].numel() * out[0].element_size() + out[1].numel() * 4

@@ -9,10 +9,12 @@ cannot load, every call raises.
 
     y, final = scan_fwd(x, dt, A, B, C, D, chunk=256, init_state=None)
     y = state_update(state, x, dt, A, B, C, D)          # state updated in place
+    pipe = HostScanPipeline(); pipe.submit(..., out=(y_host, final_host))  # host tensors
 """
 from __future__ import annotations
 
 from ._binding import (  # noqa: F401
+    HostScanPipeline,
     SsdError,
     lib_path,
     load,

@@ -218,6 +218,74 @@ def scan_fwd_host(x, dt, A, B, C, D=None, chunk=256, init_state=None, *, device=
     return out
 
 
+class HostScanPipeline:
+    """ssd_scan_fwd on host (CPU) tensors with the copies of consecutive calls
+    overlapped: the inputs of call k+1 go to the device on one stream while
+    call k computes on a second and the outputs of call k-1 come back on a
+    third (the two copy directions use the link's two directions).  ``depth``
+    staging slots of device buffers rotate; events order every reuse of a
+    slot.  ``submit`` enqueues one call and returns at once; ``synchronize``
+    waits for every call submitted so far.  Host tensors should be pinned."""
+
+    def __init__(self, device="cuda", depth=2):
+        self.dev = torch.device(device)
+        self.depth = depth
+        self.s_in = torch.cuda.Stream(self.dev)
+        self.s_comp = torch.cuda.Stream(self.dev)
+        self.s_out = torch.cuda.Stream(self.dev)
+        self.slots = [{"loaded": torch.cuda.Event(), "computed": torch.cuda.Event(),
+                       "drained": torch.cuda.Event()} for _ in range(depth)]
+        self.ws = None
+        self.n = 0
+
+    def submit(self, x, dt, A, B, C, D=None, chunk=256, init_state=None, *, out):
+        """Enqueue one call; ``out`` = (y_host, final_host) receives its results
+        once ``synchronize`` (or the returned event) has completed."""
+        st = self.slots[self.n % self.depth]
+        host = {"x": x, "dt": dt, "A": A, "B": B, "C": C, "D": D, "init": init_state}
+        devt = {}
+        # inputs: the slot's buffers are free once its previous call has computed
+        self.s_in.wait_event(st["computed"])
+        with torch.cuda.stream(self.s_in):
+            for k, v in host.items():
+                if v is None:
+                    devt[k] = None
+                    continue
+                buf = st.get(k)
+                if buf is None or buf.shape != v.shape or buf.dtype != v.dtype:
+                    buf = torch.empty(v.shape, dtype=v.dtype, device=self.dev)
+                    st[k] = buf
+                buf.copy_(v, non_blocking=True)
+                devt[k] = buf
+            st["loaded"].record(self.s_in)
+        # compute: inputs landed, and the slot's previous outputs have been read back
+        self.s_comp.wait_event(st["loaded"])
+        self.s_comp.wait_event(st["drained"])
+        with torch.cuda.stream(self.s_comp):
+            if self.ws is None:
+                b, L, H, P = x.shape
+                nbytes = scan_workspace_bytes(b, L, H, P, B.shape[3], B.shape[2], chunk,
+                                              dtype=x.dtype, device=self.dev)
+                self.ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=self.dev)
+            yd, fd = scan_fwd(devt["x"], devt["dt"], devt["A"], devt["B"], devt["C"], devt["D"],
+                              chunk, devt["init"], y=st.get("y"), final_state=st.get("final"),
+                              workspace=self.ws)
+            st["y"], st["final"] = yd, fd
+            st["computed"].record(self.s_comp)
+        # outputs back to the host
+        self.s_out.wait_event(st["computed"])
+        with torch.cuda.stream(self.s_out):
+            out[0].copy_(yd, non_blocking=True)
+            out[1].copy_(fd, non_blocking=True)
+            st["drained"].record(self.s_out)
+        self.n += 1
+        return st["drained"]
+
+    def synchronize(self):
+        for s in (self.s_in, self.s_comp, self.s_out):
+            s.synchronize()
+
+
 def state_update(state, x, dt, A, B, C, D=None, *, y=None):
     """One decode token.  state [b,H,P,N] f32 (updated in place), x [b,H,P],
     dt [b,H] f32, A [H] f32, B/C [b,G,N] (x's dtype), D [H] f32 or None.

@@ -184,3 +184,29 @@ def test_profile_events_hook_eager_and_in_graph():
     torch.cuda.synchronize()
     assert e0.elapsed_time(e1) > 0
     assert torch.equal(y, y_eager) and torch.equal(f, f_eager)
+
+
+def test_host_pipeline_matches_device_calls():
+    """Host-buffer calls through HostScanPipeline (copies of consecutive calls
+    overlapped, staging slots reused) give exactly the results of the same
+    scans run on device tensors."""
+    import state_space_model_chunked_gb300 as ssd
+    pipe = ssd.HostScanPipeline(depth=2)
+    cases, outs = [], []
+    for i in range(5):
+        inp = gen.scan_inputs(1, 1024, 4, 64, 128, 1, "bf16", seed=300 + i, random_init=True)
+        host = {k: (torch.from_numpy(v).to(torch.bfloat16) if k in ("x", "B", "C")
+                    else torch.from_numpy(v)).pin_memory() for k, v in inp.items()}
+        out = (torch.empty(host["x"].shape, dtype=torch.bfloat16, pin_memory=True),
+               torch.empty(host["init"].shape, dtype=torch.float32, pin_memory=True))
+        pipe.submit(host["x"], host["dt"], host["A"], host["B"], host["C"], host["D"], 256,
+                    host["init"], out=out)
+        cases.append(host)
+        outs.append(out)
+    pipe.synchronize()
+    for host, (yh, fh) in zip(cases, outs):
+        d = {k: v.cuda() for k, v in host.items()}
+        y, f = ssd.scan_fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], 256, d["init"])
+        torch.cuda.synchronize()
+        assert torch.equal(yh, y.cpu()) and torch.equal(fh, f.cpu())
+
