@@ -331,6 +331,79 @@ def time_decode(batch, steps, device, peaks):
             "frac_of_8TBs_nominal": gbs / 8000.0}
 
 
+def time_decode_per_layer(batch, steps, device, peaks):
+    """The same decode stack as 64 per-layer ssd_state_update calls per token
+    (each layer's state, x, B, C contiguous; 80 heads, one group), the 64 calls
+    of one token captured in a CUDA graph; four tokens' inputs rotate."""
+    import torch
+    import state_space_model_chunked_gb300 as ssd
+    from state_space_model_chunked_gb300 import inputs as gen
+    ds = gen.DECODE_SHAPE
+    nl, H, P, N = ds.layers, ds.nheads, ds.headdim, ds.dstate
+    states = [gen.device_decode_state(batch, H, P, N, seed=batch * 100 + l, device=device)
+              for l in range(nl)]
+    A, D = gen.decode_params(nl * H, seed=batch)
+    A = torch.from_numpy(A).to(device).view(nl, H)
+    D = torch.from_numpy(D).to(device).view(nl, H)
+    ntok = 4
+    toks = [[gen.device_decode_token_inputs(batch, H, P, N, 1, seed=batch * 100 + l, step=i,
+                                            device=device) for l in range(nl)]
+            for i in range(ntok)]
+    ys = [torch.empty((batch, H, P), dtype=torch.bfloat16, device=device) for _ in range(nl)]
+
+    def token(i):
+        for l in range(nl):
+            t = toks[i][l]
+            ssd.state_update(states[l], t["x"], t["dt"], A[l], t["B"], t["C"], D[l], y=ys[l])
+
+    stream = torch.cuda.Stream(device)
+    graphs = []
+    with torch.cuda.stream(stream):
+        for i in range(ntok):
+            token(i)                      # warm-up outside capture
+        torch.cuda.synchronize(device)
+        for i in range(ntok):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                token(i)
+            graphs.append(g)
+        for i in range(3):
+            graphs[i % ntok].replay()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(device)
+        e0.record(stream)
+        for i in range(steps):
+            graphs[i % ntok].replay()
+        e1.record(stream)
+    torch.cuda.synchronize(device)
+    ms = e0.elapsed_time(e1) / steps
+    Hf, G = nl * H, nl
+    byts = (2 * batch * Hf * P * N * 4 + 2 * batch * Hf * P * 2 + batch * Hf * 4
+            + 2 * batch * G * N * 2 + 2 * Hf * 4)
+    gbs = byts / (ms * 1e-3) / 1e9
+    del states, toks, graphs
+    torch.cuda.empty_cache()
+    return {"batch": batch, "steps": steps, "launch": "64 per-layer calls per token in a CUDA graph",
+            "ms_per_step": ms, "GB_per_s": gbs, "frac_of_measured_hbm": gbs / peaks["hbm_gbs"]}
+
+
+def cpu_oracle_sample_one_core(shape, heads=2):
+    """The oracle on one host core over `heads` whole heads of the workload,
+    scaled to the full layer (heads are independent recurrences)."""
+    import oracle
+    from state_space_model_chunked_gb300 import inputs as gen
+    inp = gen.scan_inputs(shape.batch, shape.seqlen, heads, shape.headdim, shape.dstate,
+                          min(shape.ngroups, heads), shape.dtype, seed=5,
+                          random_init=shape.random_init)
+    t0 = time.perf_counter()
+    oracle.scan_seq(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], inp["D"], inp["init"],
+                    nthreads=1)
+    el = time.perf_counter() - t0
+    tok_s = shape.tokens * heads / shape.nheads / el
+    return tok_s / 1e6, (f"{heads} of {shape.nheads} heads of {shape.name} on 1 core, "
+                         f"{el:.1f} s, scaled to the layer")
+
+
 def cpu_oracle_sample(shape, target_s=10.0):
     """The oracle as it stands, on all host cores, on whole heads of the
     workload (every head is an independent recurrence): returns (Mtokens/s
@@ -462,6 +535,8 @@ def run_gpu(args):
                 "tensor_tflops": lflops / (lms * 1e-3) / 1e12}
             torch.cuda.empty_cache()
             extra["decode"] = [time_decode(b, 128, device, peaks) for b in (1, 16, 64, 256)]
+            extra["decode_per_layer"] = [time_decode_per_layer(b, 32, device, peaks)
+                                         for b in (1, 16)]
     clocks = clk.summary()
 
     e2e_s, h2d, d2h = time_scan_e2e(shape, max(args.steps // 4, 3), args.warmup, device)
@@ -503,8 +578,10 @@ def run_gpu(args):
     line.update(extra)
     if not args.no_cpu:
         v, cores, desc = cpu_oracle_sample(shape, target_s=args.cpu_seconds)
+        v1, desc1 = cpu_oracle_sample_one_core(shape)
         line["cpu_baseline"] = {"value": v, "unit": "Mtokens/s", "cores": cores,
-                                "kind": "oracle", "sample": desc}
+                                "kind": "oracle", "sample": desc,
+                                "one_core": {"value": v1, "unit": "Mtokens/s", "sample": desc1}}
     print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()

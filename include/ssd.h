@@ -126,6 +126,36 @@ ssd_status ssd_scan_fwd_algo(ssd_algo algo, const void *x, const float *dt,
                              void *y, float *final_state, void *workspace,
                              size_t workspace_bytes, cudaStream_t stream);
 
+/* Optional transform of the raw step size, applied inside the kernels to
+ * every dt they read (the pages take the step Delta from the input
+ * projection, CGLA section III.A, without spelling out how it is made
+ * positive; this is the usual bias + softplus parameterisation):
+ *
+ *   dt <- min(max(sp(dt_raw + dt_bias[h]), dt_min), dt_max)
+ *   sp(u) = log(1 + e^u) when softplus != 0, else sp(u) = u.
+ *
+ * dt_bias: float [nheads] device array or NULL (no bias).  dt_min <= dt_max
+ * (NaN rejected); use -INFINITY / INFINITY for no clamp.  The tensor-core
+ * path needs the transformed dt >= 0 (softplus, or dt_min >= 0, ensures it).
+ * The caller owns dt_bias; it is read during the call's kernels. */
+typedef struct ssd_dt_transform {
+    const float *dt_bias;
+    int softplus;
+    float dt_min, dt_max;
+} ssd_dt_transform;
+
+/* ssd_scan_fwd_algo with a dt transform (NULL = identity: exactly
+ * ssd_scan_fwd_algo).  Returns SSD_ERR_INVALID_ARG when dt_min > dt_max or
+ * either is NaN. */
+ssd_status ssd_scan_fwd_dt(ssd_algo algo, const void *x, const float *dt,
+                           const float *A, const void *B, const void *C,
+                           const float *D, const ssd_dt_transform *dt_transform,
+                           ssd_dtype in_dtype, int batch, int seqlen, int nheads,
+                           int headdim, int dstate, int ngroups, int chunk,
+                           const float *init_state, void *y, float *final_state,
+                           void *workspace, size_t workspace_bytes,
+                           cudaStream_t stream);
+
 /* Profiling hook (process-wide, not for concurrent callers): while both
  * events are non-NULL, every following ssd_scan_fwd / ssd_scan_fwd_algo
  * records `before` immediately before and `after` immediately after the
@@ -173,6 +203,15 @@ ssd_status ssd_state_update(float *state, const void *x, const float *dt,
                             const float *D, ssd_dtype in_dtype, int batch,
                             int nheads, int headdim, int dstate, int ngroups,
                             void *y, cudaStream_t stream);
+
+/* ssd_state_update with a dt transform (see ssd_dt_transform; NULL =
+ * identity). */
+ssd_status ssd_state_update_dt(float *state, const void *x, const float *dt,
+                               const float *A, const void *B, const void *C,
+                               const float *D, const ssd_dt_transform *dt_transform,
+                               ssd_dtype in_dtype, int batch, int nheads,
+                               int headdim, int dstate, int ngroups, void *y,
+                               cudaStream_t stream);
 
 /* Human-readable name of a status code (static storage). */
 const char *ssd_status_string(ssd_status s);

@@ -141,6 +141,21 @@ def scan_chunked(x, dt, A, B, C, chunk, D=None, init=None, nthreads=None,
     return y, fin
 
 
+def dt_transform(dt, bias=None, softplus=False, lo=-np.inf, hi=np.inf):
+    """The step size the kernels use when given a raw dt and a transform, in
+    fp64: clamp(sp(dt + bias[h]), lo, hi) with sp(u) = log(1 + e^u) when
+    ``softplus`` (evaluated as logaddexp(0, u), the same quantity without
+    overflow), else sp(u) = u.  The head axis is dt's last axis.  The pages
+    take the step from the input projection (CGLA section III.A) and do not
+    say how it is made positive; this is the usual bias + softplus form."""
+    u = np.asarray(dt, dtype=np.float64)
+    if bias is not None:
+        u = u + np.asarray(bias, dtype=np.float64)
+    if softplus:
+        u = np.logaddexp(0.0, u)
+    return np.minimum(np.maximum(u, lo), hi)
+
+
 def rel_l2(got, ref):
     """||got - ref||_2 / ||ref||_2 in float64 (absolute norm when ref == 0)."""
     got = np.asarray(got, dtype=np.float64)

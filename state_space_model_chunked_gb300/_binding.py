@@ -15,9 +15,11 @@ EXPORTED_SYMBOLS = (
     "ssd_scan_kernel_launches",
     "ssd_scan_fwd",
     "ssd_scan_fwd_algo",
+    "ssd_scan_fwd_dt",
     "ssd_scan_fwd_static",
     "ssd_scan_profile_events",
     "ssd_state_update",
+    "ssd_state_update_dt",
     "ssd_status_string",
     "ssd_last_device_error",
 )
@@ -31,6 +33,12 @@ _lib = None
 _vp = ctypes.c_void_p
 _int = ctypes.c_int
 _sz = ctypes.c_size_t
+
+
+class _DtTransform(ctypes.Structure):
+    """ssd_dt_transform: dt <- min(max(sp(dt + dt_bias[h]), dt_min), dt_max)."""
+    _fields_ = [("dt_bias", ctypes.c_void_p), ("softplus", ctypes.c_int),
+                ("dt_min", ctypes.c_float), ("dt_max", ctypes.c_float)]
 
 
 class SsdError(RuntimeError):
@@ -66,6 +74,11 @@ def load():
         lib.ssd_scan_fwd.argtypes = scan_args
         lib.ssd_scan_fwd_algo.restype = _int
         lib.ssd_scan_fwd_algo.argtypes = [_int] + scan_args
+        lib.ssd_scan_fwd_dt.restype = _int
+        lib.ssd_scan_fwd_dt.argtypes = [_int] + [_vp] * 7 + [_int] * 8 + [_vp, _vp, _vp, _vp,
+                                                                            _sz, _vp]
+        lib.ssd_state_update_dt.restype = _int
+        lib.ssd_state_update_dt.argtypes = [_vp] * 8 + [_int] * 6 + [_vp, _vp]
         lib.ssd_scan_fwd_static.restype = _int
         lib.ssd_scan_fwd_static.argtypes = [_vp] * 6 + [_int] * 8 + [_vp, _vp, _vp, _vp]
         lib.ssd_scan_profile_events.restype = _int
@@ -140,11 +153,28 @@ def scan_kernel_launches(batch, seqlen, nheads, headdim, dstate, ngroups, chunk,
     return int(n)
 
 
+def _dt_transform(dt_bias, dt_softplus, dt_limit, H, dev):
+    """A ctypes ssd_dt_transform for the keyword arguments, or None (identity)
+    when none is set; the second value keeps dt_bias alive for the call."""
+    if dt_bias is None and not dt_softplus and dt_limit is None:
+        return None, None
+    if dt_bias is not None:
+        _need(dt_bias, "dt_bias", torch.float32, dev, (H,))
+    lo, hi = dt_limit if dt_limit is not None else (float("-inf"), float("inf"))
+    t = _DtTransform(dt_bias.data_ptr() if dt_bias is not None else None,
+                     1 if dt_softplus else 0, lo, hi)
+    return ctypes.byref(t), (t, dt_bias)
+
+
 def scan_fwd(x, dt, A, B, C, D=None, chunk=256, init_state=None, *, y=None,
-             final_state=None, workspace=None, algo=ALGO_AUTO, return_final=True):
+             final_state=None, workspace=None, algo=ALGO_AUTO, return_final=True,
+             dt_bias=None, dt_softplus=False, dt_limit=None):
     """Chunked SSD scan (prefill).  x [b,L,H,P], dt [b,L,H] f32, A [H] f32,
     B/C [b,L,G,N] (x's dtype), D [H] f32 or None, init_state [b,H,P,N] f32 or
-    None.  Returns (y, final_state) on x's device and the current stream."""
+    None.  dt_bias [H] f32, dt_softplus and dt_limit = (lo, hi) transform the
+    raw dt inside the kernels: dt <- clamp(softplus(dt + dt_bias), lo, hi)
+    (softplus only when dt_softplus).  Returns (y, final_state) on x's device
+    and the current stream."""
     lib = load()
     _need(x, "x")
     dev = x.device
@@ -176,10 +206,11 @@ def scan_fwd(x, dt, A, B, C, D=None, chunk=256, init_state=None, *, y=None,
             workspace = torch.empty(need, dtype=torch.uint8, device=dev)
         wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
         stream = torch.cuda.current_stream(dev).cuda_stream
-        rc = lib.ssd_scan_fwd_algo(algo, _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C),
-                                   _ptr(D), code, b, L, H, P, N, G, chunk,
-                                   _ptr(init_state), _ptr(y), _ptr(final_state),
-                                   _ptr(workspace), wbytes, ctypes.c_void_p(stream))
+        tptr, _keep = _dt_transform(dt_bias, dt_softplus, dt_limit, H, dev)
+        rc = lib.ssd_scan_fwd_dt(algo, _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C),
+                                 _ptr(D), tptr, code, b, L, H, P, N, G, chunk,
+                                 _ptr(init_state), _ptr(y), _ptr(final_state),
+                                 _ptr(workspace), wbytes, ctypes.c_void_p(stream))
     _check("ssd_scan_fwd", rc)
     return y, final_state
 
@@ -286,10 +317,12 @@ class HostScanPipeline:
             s.synchronize()
 
 
-def state_update(state, x, dt, A, B, C, D=None, *, y=None):
+def state_update(state, x, dt, A, B, C, D=None, *, y=None, dt_bias=None, dt_softplus=False,
+                 dt_limit=None):
     """One decode token.  state [b,H,P,N] f32 (updated in place), x [b,H,P],
-    dt [b,H] f32, A [H] f32, B/C [b,G,N] (x's dtype), D [H] f32 or None.
-    Returns y [b,H,P] in x's dtype."""
+    dt [b,H] f32, A [H] f32, B/C [b,G,N] (x's dtype), D [H] f32 or None;
+    dt_bias / dt_softplus / dt_limit as in scan_fwd.  Returns y [b,H,P] in x's
+    dtype."""
     lib = load()
     _need(state, "state", torch.float32)
     dev = state.device
@@ -310,9 +343,10 @@ def state_update(state, x, dt, A, B, C, D=None, *, y=None):
     code = _dtype_code(x)
     with torch.cuda.device(dev):
         stream = torch.cuda.current_stream(dev).cuda_stream
-        rc = lib.ssd_state_update(_ptr(state), _ptr(x), _ptr(dt), _ptr(A), _ptr(B),
-                                  _ptr(C), _ptr(D), code, b, H, P, N, G, _ptr(y),
-                                  ctypes.c_void_p(stream))
+        tptr, _keep = _dt_transform(dt_bias, dt_softplus, dt_limit, H, dev)
+        rc = lib.ssd_state_update_dt(_ptr(state), _ptr(x), _ptr(dt), _ptr(A), _ptr(B),
+                                     _ptr(C), _ptr(D), tptr, code, b, H, P, N, G, _ptr(y),
+                                     ctypes.c_void_p(stream))
     _check("ssd_state_update", rc)
     return y
 

@@ -63,6 +63,21 @@ ssd_status check_scan_args(const void *x, const float *dt, const float *A, const
     return SSD_OK;
 }
 
+// The device-side form of a caller's dt transform; NULL is the identity.
+ssd_status dt_transform_of(const ssd_dt_transform *t, SsdDt *out) {
+    out->bias = nullptr;
+    out->softplus = 0;
+    out->lo = -INFINITY;
+    out->hi = INFINITY;
+    if (!t) return SSD_OK;
+    if (!(t->dt_min <= t->dt_max)) return SSD_ERR_INVALID_ARG;   // also rejects NaN
+    out->bias = t->dt_bias;
+    out->softplus = t->softplus != 0;
+    out->lo = t->dt_min;
+    out->hi = t->dt_max;
+    return SSD_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -120,16 +135,18 @@ int ssd_scan_kernel_launches(int batch, int seqlen, int nheads, int headdim, int
     return plan.supported ? plan.launches : 1;
 }
 
-ssd_status ssd_scan_fwd_algo(ssd_algo algo, const void *x, const float *dt, const float *A,
-                             const void *B, const void *C, const float *D,
-                             ssd_dtype in_dtype, int batch, int seqlen, int nheads,
-                             int headdim, int dstate, int ngroups, int chunk,
-                             const float *init_state, void *y, float *final_state,
-                             void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+ssd_status ssd_scan_fwd_dt(ssd_algo algo, const void *x, const float *dt, const float *A,
+                           const void *B, const void *C, const float *D,
+                           const ssd_dt_transform *dt_transform, ssd_dtype in_dtype, int batch,
+                           int seqlen, int nheads, int headdim, int dstate, int ngroups,
+                           int chunk, const float *init_state, void *y, float *final_state,
+                           void *workspace, size_t workspace_bytes, cudaStream_t stream) {
     ssd_status st = check_scan_args(x, dt, A, B, C, D, in_dtype, batch, seqlen, nheads,
                                     headdim, dstate, ngroups, chunk, init_state, y,
                                     final_state);
     if (st != SSD_OK) return st;
+    SsdDt dtt;
+    if ((st = dt_transform_of(dt_transform, &dtt)) != SSD_OK) return st;
     if (algo != SSD_ALGO_AUTO && algo != SSD_ALGO_SIMT && algo != SSD_ALGO_TCGEN05)
         return SSD_ERR_INVALID_ARG;
     const bool bf16 = in_dtype == SSD_BF16;
@@ -148,12 +165,24 @@ ssd_status ssd_scan_fwd_algo(ssd_algo algo, const void *x, const float *dt, cons
         }
         e = ssd_launch_scan_tc(plan, x, dt, A, B, C, D, init_state, y, final_state, batch,
                                seqlen, nheads, headdim, dstate, ngroups, workspace,
-                               device_error_word(), g_profile, stream);
+                               device_error_word(), dtt, g_profile, stream);
     } else {
         e = ssd_launch_scan_simt(x, dt, A, B, C, D, init_state, y, final_state, bf16, batch,
-                                 seqlen, nheads, headdim, dstate, ngroups, g_profile, stream);
+                                 seqlen, nheads, headdim, dstate, ngroups, dtt, g_profile,
+                                 stream);
     }
     return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+}
+
+ssd_status ssd_scan_fwd_algo(ssd_algo algo, const void *x, const float *dt, const float *A,
+                             const void *B, const void *C, const float *D,
+                             ssd_dtype in_dtype, int batch, int seqlen, int nheads,
+                             int headdim, int dstate, int ngroups, int chunk,
+                             const float *init_state, void *y, float *final_state,
+                             void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+    return ssd_scan_fwd_dt(algo, x, dt, A, B, C, D, nullptr, in_dtype, batch, seqlen, nheads,
+                           headdim, dstate, ngroups, chunk, init_state, y, final_state,
+                           workspace, workspace_bytes, stream);
 }
 
 ssd_status ssd_scan_fwd(const void *x, const float *dt, const float *A, const void *B,
@@ -166,10 +195,11 @@ ssd_status ssd_scan_fwd(const void *x, const float *dt, const float *A, const vo
                              final_state, workspace, workspace_bytes, stream);
 }
 
-ssd_status ssd_state_update(float *state, const void *x, const float *dt, const float *A,
-                            const void *B, const void *C, const float *D, ssd_dtype in_dtype,
-                            int batch, int nheads, int headdim, int dstate, int ngroups,
-                            void *y, cudaStream_t stream) {
+ssd_status ssd_state_update_dt(float *state, const void *x, const float *dt, const float *A,
+                               const void *B, const void *C, const float *D,
+                               const ssd_dt_transform *dt_transform, ssd_dtype in_dtype,
+                               int batch, int nheads, int headdim, int dstate, int ngroups,
+                               void *y, cudaStream_t stream) {
     if (!state || !x || !dt || !A || !B || !C || !y) return SSD_ERR_INVALID_ARG;
     if (in_dtype != SSD_F32 && in_dtype != SSD_BF16) return SSD_ERR_INVALID_ARG;
     if (batch <= 0 || nheads <= 0 || headdim <= 0 || dstate <= 0 || ngroups <= 0)
@@ -180,10 +210,21 @@ ssd_status ssd_state_update(float *state, const void *x, const float *dt, const 
     for (const void *p : ptrs)
         if (p && !aligned16(p)) return SSD_ERR_INVALID_ARG;
     if ((size_t)batch * nheads >= ((size_t)1 << 31)) return SSD_ERR_UNSUPPORTED;
+    SsdDt dtt;
+    const ssd_status st = dt_transform_of(dt_transform, &dtt);
+    if (st != SSD_OK) return st;
     cudaError_t e = ssd_launch_decode(state, x, dt, A, B, C, D, y, in_dtype == SSD_BF16, batch,
                                       nheads, headdim, dstate, ngroups, current_sm_count(),
-                                      device_error_word(), stream);
+                                      device_error_word(), dtt, stream);
     return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+}
+
+ssd_status ssd_state_update(float *state, const void *x, const float *dt, const float *A,
+                            const void *B, const void *C, const float *D, ssd_dtype in_dtype,
+                            int batch, int nheads, int headdim, int dstate, int ngroups,
+                            void *y, cudaStream_t stream) {
+    return ssd_state_update_dt(state, x, dt, A, B, C, D, nullptr, in_dtype, batch, nheads,
+                               headdim, dstate, ngroups, y, stream);
 }
 
 }  // extern "C"

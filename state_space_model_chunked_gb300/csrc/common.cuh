@@ -17,6 +17,38 @@ __device__ __forceinline__ void ssd_report(unsigned int *err, unsigned int code)
     if (err) atomicCAS(err, 0u, code);
 }
 
+// Optional transform of the raw step size before it is used, the usual
+// parameterisation of a positive step from the input projection's output:
+//   dt <- clamp(sp(dt_raw + bias[h]), lo, hi),  sp = softplus when enabled,
+// softplus(u) = log(1 + e^u) (u itself above 20, where they agree in fp32).
+// bias = nullptr, softplus = 0, lo = -inf, hi = +inf is the identity.
+struct SsdDt {
+    const float *bias;
+    int softplus;
+    float lo, hi;
+};
+
+// Kernels are instantiated with and without the transform (kOn): its code,
+// even untaken, costs the scan kernel a quarter of its speed, so the identity
+// instantiation carries none of it.
+template <bool kOn>
+__device__ __forceinline__ float ssd_dt(const SsdDt &t, float raw, int h) {
+    if constexpr (!kOn) {
+        (void)t;
+        (void)h;
+        return raw;
+    } else {
+        float v = raw;
+        if (t.bias) v += t.bias[h];
+        if (t.softplus) v = v > 20.f ? v : log1pf(expf(v));
+        return fminf(fmaxf(v, t.lo), t.hi);
+    }
+}
+
+inline bool ssd_dt_active(const SsdDt &t) {
+    return t.bias != nullptr || t.softplus != 0 || t.lo > -INFINITY || t.hi < INFINITY;
+}
+
 // Element loads/stores for the two input dtypes.
 __device__ __forceinline__ float ssd_ld(const float *p) { return *p; }
 __device__ __forceinline__ float ssd_ld(const __nv_bfloat16 *p) { return __bfloat162float(*p); }

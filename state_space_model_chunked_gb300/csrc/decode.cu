@@ -24,13 +24,13 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kBatchRows = 8;   // rows each thread has in flight at once
 
-template <typename T, int VPT>
+template <typename T, int VPT, bool kDtX>
 __global__ void __launch_bounds__(kThreads)
 ssd_decode_kernel(float *__restrict__ state, const T *__restrict__ x,
                   const float *__restrict__ dt, const float *__restrict__ A,
                   const T *__restrict__ Bm, const T *__restrict__ Cm,
                   const float *__restrict__ D, T *__restrict__ y, int H, int P,
-                  int N, int G) {
+                  int N, int G, const SsdDt dtt) {
     const int bh = blockIdx.x;             // b * H + h
     const int b = bh / H, h = bh - b * H;
     const int g = h / (H / G);
@@ -39,7 +39,7 @@ ssd_decode_kernel(float *__restrict__ state, const T *__restrict__ x,
     const int lane_n = threadIdx.x % tpr;
     const int r0 = threadIdx.x / tpr;
 
-    const float dtv = dt[bh];
+    const float dtv = ssd_dt<kDtX>(dtt, dt[bh], h);
     const float decay = expf(dtv * A[h]);
     const float Dh = D ? D[h] : 0.0f;
 
@@ -129,13 +129,13 @@ __host__ __device__ inline StreamLayout stream_layout(int P, int N, int es) {
     return l;
 }
 
-template <typename T, int VPT>
+template <typename T, int VPT, bool kDtX>
 __global__ void __launch_bounds__(kStreamThreads + 32, 1)
 ssd_decode_stream_kernel(float *__restrict__ state, const T *__restrict__ x,
                          const float *__restrict__ dt, const float *__restrict__ A,
                          const T *__restrict__ Bm, const T *__restrict__ Cm,
                          const float *__restrict__ D, T *__restrict__ y, int batch, int H, int P,
-                         int N, int G, int stages, unsigned int *err) {
+                         int N, int G, int stages, unsigned int *err, const SsdDt dtt) {
     using namespace ssdptx;
     extern __shared__ __align__(1024) uint8_t smem[];
     const StreamLayout L = stream_layout(P, N, (int)sizeof(T));
@@ -202,12 +202,12 @@ ssd_decode_stream_kernel(float *__restrict__ state, const T *__restrict__ x,
         const int tpr = N / (4 * VPT);
         const int lane_n = tid % tpr;
         const int total = P * tpr;
-        float dt_next = nk > 0 ? dt[unit_of(0)] : 0.f;
+        float dt_next = nk > 0 ? dt[unit_of(0)] : 0.f;   // raw; transformed at use
         for (long k = 0; k < nk; ++k) {
             const int st = (int)(k % stages);
             const long u = unit_of(k);
             const int h = (int)(u % H);
-            const float dtv = dt_next;
+            const float dtv = ssd_dt<kDtX>(dtt, dt_next, h);
             if (k + 1 < nk) dt_next = dt[unit_of(k + 1)];
             const float decay = expf(dtv * A[h]);
             const float Dh = D ? D[h] : 0.0f;
@@ -291,11 +291,11 @@ ssd_decode_stream_kernel(float *__restrict__ state, const T *__restrict__ x,
     __syncthreads();
 }
 
-template <typename T>
+template <typename T, bool kDtX>
 cudaError_t launch_t(float *state, const void *x, const float *dt, const float *A,
                      const void *B, const void *C, const float *D, void *y, int batch,
                      int H, int P, int N, int G, int num_sms, unsigned int *err,
-                     cudaStream_t stream) {
+                     const SsdDt &dtt, cudaStream_t stream) {
     const size_t units = (size_t)batch * H;
     const StreamLayout lay = stream_layout(P, N, (int)sizeof(T));
     const int stages = (int)std::min<size_t>(8, kStreamRing / lay.stage_bytes);
@@ -306,29 +306,29 @@ cudaError_t launch_t(float *state, const void *x, const float *dt, const float *
         const size_t smem = (size_t)stages * lay.stage_bytes + 16 * stages + 16;
         cudaError_t e;
         if (N <= 128) {
-            e = cudaFuncSetAttribute(ssd_decode_stream_kernel<T, 1>,
+            e = cudaFuncSetAttribute(ssd_decode_stream_kernel<T, 1, kDtX>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
             if (e != cudaSuccess) return e;
-            ssd_decode_stream_kernel<T, 1><<<num_sms, kStreamThreads + 32, smem, stream>>>(
+            ssd_decode_stream_kernel<T, 1, kDtX><<<num_sms, kStreamThreads + 32, smem, stream>>>(
                 state, (const T *)x, dt, A, (const T *)B, (const T *)C, D, (T *)y, batch, H, P,
-                N, G, stages, err);
+                N, G, stages, err, dtt);
         } else {
-            e = cudaFuncSetAttribute(ssd_decode_stream_kernel<T, 2>,
+            e = cudaFuncSetAttribute(ssd_decode_stream_kernel<T, 2, kDtX>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
             if (e != cudaSuccess) return e;
-            ssd_decode_stream_kernel<T, 2><<<num_sms, kStreamThreads + 32, smem, stream>>>(
+            ssd_decode_stream_kernel<T, 2, kDtX><<<num_sms, kStreamThreads + 32, smem, stream>>>(
                 state, (const T *)x, dt, A, (const T *)B, (const T *)C, D, (T *)y, batch, H, P,
-                N, G, stages, err);
+                N, G, stages, err, dtt);
         }
         return cudaGetLastError();
     }
     const unsigned grid = (unsigned)units;
     if (N <= 128) {
-        ssd_decode_kernel<T, 1><<<grid, kThreads, 0, stream>>>(
-            state, (const T *)x, dt, A, (const T *)B, (const T *)C, D, (T *)y, H, P, N, G);
+        ssd_decode_kernel<T, 1, kDtX><<<grid, kThreads, 0, stream>>>(
+            state, (const T *)x, dt, A, (const T *)B, (const T *)C, D, (T *)y, H, P, N, G, dtt);
     } else {
-        ssd_decode_kernel<T, 2><<<grid, kThreads, 0, stream>>>(
-            state, (const T *)x, dt, A, (const T *)B, (const T *)C, D, (T *)y, H, P, N, G);
+        ssd_decode_kernel<T, 2, kDtX><<<grid, kThreads, 0, stream>>>(
+            state, (const T *)x, dt, A, (const T *)B, (const T *)C, D, (T *)y, H, P, N, G, dtt);
     }
     return cudaGetLastError();
 }
@@ -339,9 +339,15 @@ cudaError_t ssd_launch_decode(float *state, const void *x, const float *dt,
                               const float *A, const void *B, const void *C,
                               const float *D, void *y, bool bf16, int batch,
                               int H, int P, int N, int G, int num_sms, unsigned int *err,
-                              cudaStream_t stream) {
+                              const SsdDt &dtt, cudaStream_t stream) {
+    const bool dtx = ssd_dt_active(dtt);
     if (bf16)
-        return launch_t<__nv_bfloat16>(state, x, dt, A, B, C, D, y, batch, H, P, N, G, num_sms,
-                                       err, stream);
-    return launch_t<float>(state, x, dt, A, B, C, D, y, batch, H, P, N, G, num_sms, err, stream);
+        return dtx ? launch_t<__nv_bfloat16, true>(state, x, dt, A, B, C, D, y, batch, H, P, N,
+                                                   G, num_sms, err, dtt, stream)
+                   : launch_t<__nv_bfloat16, false>(state, x, dt, A, B, C, D, y, batch, H, P, N,
+                                                    G, num_sms, err, dtt, stream);
+    return dtx ? launch_t<float, true>(state, x, dt, A, B, C, D, y, batch, H, P, N, G, num_sms,
+                                       err, dtt, stream)
+               : launch_t<float, false>(state, x, dt, A, B, C, D, y, batch, H, P, N, G, num_sms,
+                                        err, dtt, stream);
 }

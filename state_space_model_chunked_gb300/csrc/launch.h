@@ -5,11 +5,13 @@
 #include <cuda_runtime.h>
 #include <stddef.h>
 
+#include "common.cuh"
+
 cudaError_t ssd_launch_decode(float *state, const void *x, const float *dt,
                               const float *A, const void *B, const void *C,
                               const float *D, void *y, bool bf16, int batch,
                               int H, int P, int N, int G, int num_sms, unsigned int *err,
-                              cudaStream_t stream);
+                              const SsdDt &dtt, cudaStream_t stream);
 
 size_t ssd_simt_smem_bytes(int N);
 
@@ -34,7 +36,7 @@ cudaError_t ssd_launch_scan_simt(const void *x, const float *dt, const float *A,
                                  const void *B, const void *C, const float *D,
                                  const float *init, void *y, float *fin, bool bf16,
                                  int batch, int L, int H, int P, int N, int G,
-                                 SsdProfileEvents prof, cudaStream_t stream);
+                                 const SsdDt &dtt, SsdProfileEvents prof, cudaStream_t stream);
 
 // Tensor-core (tcgen05/TMEM/TMA) chunked scan.
 struct SsdTcPlan {
@@ -54,5 +56,5 @@ cudaError_t ssd_launch_scan_tc(const SsdTcPlan &plan, const void *x, const float
                                const float *A, const void *B, const void *C,
                                const float *D, const float *init, void *y, float *fin,
                                int batch, int L, int H, int P, int N, int G,
-                               void *workspace, unsigned int *err, SsdProfileEvents prof,
-                               cudaStream_t stream);
+                               void *workspace, unsigned int *err, const SsdDt &dtt,
+                               SsdProfileEvents prof, cudaStream_t stream);

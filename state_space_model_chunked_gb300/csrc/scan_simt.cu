@@ -43,13 +43,14 @@ __host__ inline size_t simt_smem_bytes(int N) {
                             (size_t)kT * kMS + 4 * kT);
 }
 
-template <typename T>
+template <typename T, bool kDtX>
 __global__ void __launch_bounds__(kThreads)
 ssd_scan_simt_kernel(const T *__restrict__ x, const float *__restrict__ dt,
                      const float *__restrict__ A, const T *__restrict__ Bm,
                      const T *__restrict__ Cm, const float *__restrict__ D,
                      const float *__restrict__ init, T *__restrict__ y,
-                     float *__restrict__ fin, int L, int H, int P, int N, int G) {
+                     float *__restrict__ fin, int L, int H, int P, int N, int G,
+                     const SsdDt dtt) {
     extern __shared__ __align__(16) float sm[];
     const int np = simt_np(N);
     float *Cs = sm;                       // [kT][np]
@@ -105,8 +106,8 @@ ssd_scan_simt_kernel(const T *__restrict__ x, const float *__restrict__ dt,
         if (tid < 32) {
             // inclusive cumsum of dt*A over the tile: two tokens per lane
             const int ta = 2 * tid, tb = 2 * tid + 1;
-            const float da = ta < len ? dt[((size_t)b * L + t0 + ta) * H + h] : 0.f;
-            const float db = tb < len ? dt[((size_t)b * L + t0 + tb) * H + h] : 0.f;
+            const float da = ta < len ? ssd_dt<kDtX>(dtt, dt[((size_t)b * L + t0 + ta) * H + h], h) : 0.f;
+            const float db = tb < len ? ssd_dt<kDtX>(dtt, dt[((size_t)b * L + t0 + tb) * H + h], h) : 0.f;
             const float va = da * Ah, vb = db * Ah;
             float pair = va + vb;
             float incl = pair;
@@ -211,20 +212,21 @@ ssd_scan_simt_kernel(const T *__restrict__ x, const float *__restrict__ dt,
     }
 }
 
-template <typename T>
+template <typename T, bool kDtX>
 cudaError_t launch_t(const void *x, const float *dt, const float *A, const void *B,
                      const void *C, const float *D, const float *init, void *y,
                      float *fin, int batch, int L, int H, int P, int N, int G,
-                     SsdProfileEvents prof, cudaStream_t stream) {
+                     const SsdDt &dtt, SsdProfileEvents prof, cudaStream_t stream) {
     const size_t smem = simt_smem_bytes(N);
-    cudaError_t e = cudaFuncSetAttribute(ssd_scan_simt_kernel<T>,
+    cudaError_t e = cudaFuncSetAttribute(ssd_scan_simt_kernel<T, kDtX>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid((P + kPB - 1) / kPB, H, batch);
     if (prof.before && prof.after && (e = ssd_record_event(prof.before, stream)) != cudaSuccess)
         return e;
-    ssd_scan_simt_kernel<T><<<grid, kThreads, smem, stream>>>(
-        (const T *)x, dt, A, (const T *)B, (const T *)C, D, init, (T *)y, fin, L, H, P, N, G);
+    ssd_scan_simt_kernel<T, kDtX><<<grid, kThreads, smem, stream>>>(
+        (const T *)x, dt, A, (const T *)B, (const T *)C, D, init, (T *)y, fin, L, H, P, N, G,
+        dtt);
     e = cudaGetLastError();
     if (e == cudaSuccess && prof.before && prof.after) e = ssd_record_event(prof.after, stream);
     return e;
@@ -238,9 +240,15 @@ cudaError_t ssd_launch_scan_simt(const void *x, const float *dt, const float *A,
                                  const void *B, const void *C, const float *D,
                                  const float *init, void *y, float *fin, bool bf16,
                                  int batch, int L, int H, int P, int N, int G,
-                                 SsdProfileEvents prof, cudaStream_t stream) {
+                                 const SsdDt &dtt, SsdProfileEvents prof, cudaStream_t stream) {
+    const bool dtx = ssd_dt_active(dtt);
     if (bf16)
-        return launch_t<__nv_bfloat16>(x, dt, A, B, C, D, init, y, fin, batch, L, H, P, N, G,
-                                       prof, stream);
-    return launch_t<float>(x, dt, A, B, C, D, init, y, fin, batch, L, H, P, N, G, prof, stream);
+        return dtx ? launch_t<__nv_bfloat16, true>(x, dt, A, B, C, D, init, y, fin, batch, L, H,
+                                                   P, N, G, dtt, prof, stream)
+                   : launch_t<__nv_bfloat16, false>(x, dt, A, B, C, D, init, y, fin, batch, L,
+                                                    H, P, N, G, dtt, prof, stream);
+    return dtx ? launch_t<float, true>(x, dt, A, B, C, D, init, y, fin, batch, L, H, P, N, G,
+                                       dtt, prof, stream)
+               : launch_t<float, false>(x, dt, A, B, C, D, init, y, fin, batch, L, H, P, N, G,
+                                        dtt, prof, stream);
 }

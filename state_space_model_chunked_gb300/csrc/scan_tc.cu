@@ -118,6 +118,7 @@ struct TcArgs {
     float *fin;
     unsigned int *err;
     int L, H, G, tiles, seg_tiles, nseg;
+    SsdDt dtt;             // transform of the raw step size
 };
 
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int *abort_flag,
@@ -178,7 +179,7 @@ struct ScanLayout {
     static constexpr uint32_t kBytes = kOffXt + HG * kXBytes;
 };
 
-template <int HG, bool kFacLow>
+template <int HG, bool kFacLow, bool kDtX>
 __global__ void __launch_bounds__(kThreads, 1)
 ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
                    const __grid_constant__ CUtensorMap mapB,
@@ -425,8 +426,16 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
             }
         };
         // chunk-local inclusive cumsum a_t of dt A, the 32-block ends a_e(j) and
-        // v_s = exp(a_e(block of s) - a_s) dt_s, from the dt values in dn
-        auto factors = [&]() {
+        // v_s = exp(a_e(block of s) - a_s) dt_s, from the raw dt values in dn
+        // (tile it); the transform is applied here, not at the load, so the
+        // loads stay in flight until the values are needed
+        auto factors = [&](int it) {
+            const int tok0 = (k0 + it) * kTile + 4 * lane;
+#pragma unroll
+            for (int h = 0; h < HG; ++h)
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    dn[h][i] = tok0 + i < a.L ? ssd_dt<kDtX>(a.dtt, dn[h][i], h0 + h) : 0.f;
 #pragma unroll
             for (int h = 0; h < HG; ++h) {
                 float c[4];
@@ -473,12 +482,12 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
         };
         if (ntile > 0) {
             load_dt4(0);
-            factors();
+            factors(0);
             publish();
             if (ntile > 1) load_dt4(1);
         }
         for (int it = 0; it + 1 < ntile; ++it) {
-            factors();                                       // tile it + 1
+            factors(it + 1);                                 // tile it + 1
             if (it + 2 < ntile) load_dt4(it + 2);            // in flight meanwhile
             wait_bar_warp(bar(7), it & 1, abort_flag, a.err);       // masks of tile it built
             publish();
@@ -612,7 +621,10 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
                         const int tb = t0 + 32 * j;
                         auto lw = [&](int s) {
                             const int tok = tb + s;
-                            const float d = tok < a.L ? a.dt[((size_t)b * a.L + tok) * a.H + h0 + hh] : 0.f;
+                            const float d =
+                                tok < a.L
+                                    ? ssd_dt<kDtX>(a.dtt, a.dt[((size_t)b * a.L + tok) * a.H + h0 + hh], h0 + hh)
+                                    : 0.f;
                             return d > 0.f ? __expf(at[hh] - ah[s] + __logf(d)) : 0.f;
                         };
 #pragma unroll
@@ -751,7 +763,7 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
 // each X tile in place by its token weights, and warp 10 computes the weights
 // w_s = exp(decay from s to the segment end) dt_s of each tile into a ring
 // with one slot per stage.
-template <int HG>
+template <int HG, bool kDtX>
 __global__ void __launch_bounds__(kSegThreads, 1)
 ssd_tc_segment_kernel(const __grid_constant__ CUtensorMap mapB,
                       const __grid_constant__ CUtensorMap mapX, const TcArgs a) {
@@ -876,7 +888,9 @@ ssd_tc_segment_kernel(const __grid_constant__ CUtensorMap mapB,
             for (int h = 0; h < HG; ++h)
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    d[h][i] = d0[h][i];
+                    // the transform at use keeps the three tiles of loads in flight
+                    const int tok = (k1 - 1 - it) * kTile + 4 * lane + i;
+                    d[h][i] = tok < a.L ? ssd_dt<kDtX>(a.dtt, d0[h][i], h0 + h) : 0.f;
                     d0[h][i] = d1[h][i];
                     d1[h][i] = d2[h][i];
                 }
@@ -1063,19 +1077,19 @@ static_assert(seg_smem<2>() <= 232448, "segment kernel shared memory exceeds 227
 static_assert(seg_smem<4>() <= 232448, "segment kernel shared memory exceeds 227 KB");
 
 // Segment contributions with SG heads per CTA.
-template <int SG>
+template <int SG, bool kDtX>
 cudaError_t launch_segment(const SsdTcPlan &plan, const CUtensorMap &mB, const CUtensorMap &mX,
                            const TcArgs &args, int batch, int H, cudaStream_t stream) {
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(attr_once, [] {
-        attr_err = cudaFuncSetAttribute(ssd_tc_segment_kernel<SG>,
+        attr_err = cudaFuncSetAttribute(ssd_tc_segment_kernel<SG, kDtX>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         (int)seg_smem<SG>());
     });
     if (attr_err != cudaSuccess) return attr_err;
     dim3 g1(H / SG, plan.nseg - 1, batch);
-    ssd_tc_segment_kernel<SG><<<g1, kSegThreads, seg_smem<SG>(), stream>>>(mB, mX, args);
+    ssd_tc_segment_kernel<SG, kDtX><<<g1, kSegThreads, seg_smem<SG>(), stream>>>(mB, mX, args);
     return cudaGetLastError();
 }
 
@@ -1098,30 +1112,30 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
     return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
-template <int HG>
+template <int HG, bool kDtX>
 cudaError_t launch_hg(const SsdTcPlan &plan, const CUtensorMap &mC, const CUtensorMap &mB,
                       const CUtensorMap &mX, const CUtensorMap &mY, const TcArgs &args,
                       int batch, int H, SsdProfileEvents prof, cudaStream_t stream) {
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(attr_once, [] {
-        attr_err = cudaFuncSetAttribute(ssd_tc_scan_kernel<HG, false>,
+        attr_err = cudaFuncSetAttribute(ssd_tc_scan_kernel<HG, false, kDtX>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         (int)scan_smem<HG>());
         if (attr_err == cudaSuccess)
-            attr_err = cudaFuncSetAttribute(ssd_tc_scan_kernel<HG, true>,
+            attr_err = cudaFuncSetAttribute(ssd_tc_scan_kernel<HG, true, kDtX>,
                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
                                             (int)scan_smem<HG>());
     });
     if (attr_err != cudaSuccess) return attr_err;
     // factor warp on the light sub-partition for long segments, the producer
     // there for short ones (A/B timed on the 130M and 2.7B layers)
-    auto kernel = plan.seg_tiles >= kLongSegTiles ? ssd_tc_scan_kernel<HG, true>
-                                                  : ssd_tc_scan_kernel<HG, false>;
+    auto kernel = plan.seg_tiles >= kLongSegTiles ? ssd_tc_scan_kernel<HG, true, kDtX>
+                                                  : ssd_tc_scan_kernel<HG, false, kDtX>;
     if (plan.nseg > 1) {
         cudaError_t e = plan.seg_heads == 4
-                            ? launch_segment<4>(plan, mB, mX, args, batch, H, stream)
-                            : launch_segment<HG>(plan, mB, mX, args, batch, H, stream);
+                            ? launch_segment<4, kDtX>(plan, mB, mX, args, batch, H, stream)
+                            : launch_segment<HG, kDtX>(plan, mB, mX, args, batch, H, stream);
         if (e != cudaSuccess) return e;
         const size_t total = (size_t)batch * H * kP * kN / 4;
         e = launch_pdl(ssd_tc_segment_pass_kernel, dim3((unsigned)((total + 255) / 256)),
@@ -1194,7 +1208,7 @@ cudaError_t ssd_launch_scan_tc(const SsdTcPlan &plan, const void *x, const float
                                const float *A, const void *B, const void *C, const float *D,
                                const float *init, void *y, float *fin, int batch, int L, int H,
                                int P, int N, int G, void *workspace, unsigned int *err,
-                               SsdProfileEvents prof, cudaStream_t stream) {
+                               const SsdDt &dtt, SsdProfileEvents prof, cudaStream_t stream) {
     (void)P;
     (void)N;
     CUtensorMap mC, mB, mX, mY;
@@ -1203,6 +1217,7 @@ cudaError_t ssd_launch_scan_tc(const SsdTcPlan &plan, const void *x, const float
         return cudaErrorInvalidValue;
     TcArgs args{};
     args.dt = dt;
+    args.dtt = dtt;
     args.A = A;
     args.D = D;
     args.init = init;
@@ -1221,7 +1236,10 @@ cudaError_t ssd_launch_scan_tc(const SsdTcPlan &plan, const void *x, const float
     args.tiles = plan.tiles;
     args.seg_tiles = plan.seg_tiles;
     args.nseg = plan.nseg;
+    const bool dtx = ssd_dt_active(dtt);
     if (plan.heads_per_cta == 2)
-        return launch_hg<2>(plan, mC, mB, mX, mY, args, batch, H, prof, stream);
-    return launch_hg<1>(plan, mC, mB, mX, mY, args, batch, H, prof, stream);
+        return dtx ? launch_hg<2, true>(plan, mC, mB, mX, mY, args, batch, H, prof, stream)
+                   : launch_hg<2, false>(plan, mC, mB, mX, mY, args, batch, H, prof, stream);
+    return dtx ? launch_hg<1, true>(plan, mC, mB, mX, mY, args, batch, H, prof, stream)
+               : launch_hg<1, false>(plan, mC, mB, mX, mY, args, batch, H, prof, stream);
 }

@@ -23,11 +23,13 @@ def host(t):
     return t.detach().float().cpu().numpy().astype(np.float64)
 
 
-def scan_on_gpu(inp, dtype, chunk, algo=0):
+def scan_on_gpu(inp, dtype, chunk, algo=0, **dt_kw):
     import state_space_model_chunked_gb300 as ssd
+    if dt_kw.get("dt_bias") is not None:
+        dt_kw = dict(dt_kw, dt_bias=dev(dt_kw["dt_bias"]))
     y, fin = ssd.scan_fwd(dev(inp["x"], dtype), dev(inp["dt"]), dev(inp["A"]),
                           dev(inp["B"], dtype), dev(inp["C"], dtype), dev(inp["D"]),
-                          chunk, dev(inp["init"]), algo=algo)
+                          chunk, dev(inp["init"]), algo=algo, **dt_kw)
     torch.cuda.synchronize()
     return host(y), host(fin)
 

@@ -109,3 +109,28 @@ def test_decode_streaming_path_multi_step(N, dtype):
         assert rel(host(y), y_ref) <= TOL[dtype]
     assert rel(host(s_dev), s_ref) <= 1e-6
     ssd.last_device_error()
+
+
+@pytest.mark.parametrize("units", [(3, 10), (8, 160)])     # classic and streaming launch
+def test_decode_dt_softplus_bias(units):
+    """The decode update with dt <- clamp(softplus(dt_raw + bias), lo, hi)
+    computed in the kernel, against the oracle step on the fp64 transform."""
+    import state_space_model_chunked_gb300 as ssd
+    b, H = units
+    P, N, G = 64, 128, 2
+    state = gen.decode_state(b, H, P, N, seed=9)
+    A, D = gen.decode_params(H, seed=9)
+    tok = gen.decode_token_inputs(b, H, P, N, G, "bf16", seed=9, step=0)
+    rng = np.random.default_rng(9)
+    raw = rng.normal(-3.0, 1.0, size=(b, H)).astype(np.float32)
+    bias = rng.uniform(-1.0, 1.0, size=(H,)).astype(np.float32)
+    s_dev = dev(state)
+    y = ssd.state_update(s_dev, dev(tok["x"], "bf16"), dev(raw), dev(A), dev(tok["B"], "bf16"),
+                         dev(tok["C"], "bf16"), dev(D), dt_bias=dev(bias), dt_softplus=True,
+                         dt_limit=(1e-3, 0.08))
+    torch.cuda.synchronize()
+    dt_eff = oracle.dt_transform(raw, bias, True, 1e-3, 0.08)
+    y_ref, s_ref = oracle.step(state, tok["x"], dt_eff, A, tok["B"], tok["C"], D)
+    assert rel(host(y), y_ref) <= 1e-2
+    assert rel(host(s_dev), s_ref) <= 1e-6
+

@@ -241,3 +241,37 @@ def test_bf16_rounding_is_nearest_even():
     assert got[4] == -2.5
     assert abs(got[5] - 3.0e-3) <= 3.0e-3 * 2**-8
     assert bits[0] == 0x3F80
+
+
+# ------------------------------------------------------------- dt transform
+def test_dt_transform_identity_by_default():
+    dt = np.random.default_rng(1).uniform(-3, 3, size=(2, 5, 3)).astype(np.float32)
+    out = oracle.dt_transform(dt)
+    assert out.dtype == np.float64 and np.array_equal(out, dt.astype(np.float64))
+
+
+def test_dt_transform_softplus_closed_forms():
+    """softplus(0) = ln 2; for large u, softplus(u) = u + log1p(e^-u); for very
+    negative u, softplus(u) = e^u (1 - e^u/2 + ...)."""
+    assert oracle.dt_transform(np.zeros(1), softplus=True)[0] == np.log(2.0)
+    u = np.array([30.0, 50.0, 800.0])
+    assert np.allclose(oracle.dt_transform(u, softplus=True), u + np.log1p(np.exp(-u)),
+                       rtol=0, atol=1e-12)
+    v = np.array([-30.0, -50.0])
+    assert np.allclose(oracle.dt_transform(v, softplus=True), np.exp(v), rtol=1e-12)
+    w = np.linspace(-5, 5, 101)
+    assert np.allclose(oracle.dt_transform(w, softplus=True), np.log(1.0 + np.exp(w)),
+                       rtol=1e-14)
+
+
+def test_dt_transform_bias_per_head_then_clamp():
+    dt = np.zeros((1, 4, 3))
+    bias = np.array([-1.0, 0.5, 3.0])
+    out = oracle.dt_transform(dt, bias)
+    assert np.array_equal(out, np.broadcast_to(bias, (1, 4, 3)))
+    out = oracle.dt_transform(dt, bias, lo=0.0, hi=1.0)
+    assert np.array_equal(out[0, 0], [0.0, 0.5, 1.0])
+    # softplus of the biased value, then the clamp (order matters)
+    out = oracle.dt_transform(dt, bias, softplus=True, lo=0.5, hi=2.0)
+    assert np.allclose(out[0, 0], [0.5, np.log1p(np.exp(0.5)), 2.0], rtol=1e-15)
+

@@ -210,3 +210,37 @@ def test_host_pipeline_matches_device_calls():
         torch.cuda.synchronize()
         assert torch.equal(yh, y.cpu()) and torch.equal(fh, f.cpu())
 
+
+# --------------------------------------------------------- dt transform fused
+def _raw_dt_case(b, L, H, G, dtype, seed):
+    """Inputs whose dt is a raw projection output (about N(-3, 1)), a per-head
+    bias, and the fp64 step the transform makes of them."""
+    inp = gen.scan_inputs(b, L, H, 64, 128, G, dtype, seed=seed, random_init=True)
+    rng = np.random.default_rng(seed)
+    inp["dt"] = rng.normal(-3.0, 1.0, size=inp["dt"].shape).astype(np.float32)
+    bias = rng.uniform(-1.0, 1.0, size=(H,)).astype(np.float32)
+    return inp, bias
+
+
+@pytest.mark.parametrize("algo,dtype", [(TC, "bf16"), (SIMT, "f32"), (SIMT, "bf16")])
+@pytest.mark.parametrize("limit", [None, (1e-3, 0.08)])
+def test_scan_dt_softplus_bias_clamp(algo, dtype, limit):
+    """dt <- clamp(softplus(dt_raw + bias), lo, hi) computed inside the kernels
+    matches the oracle run on the fp64 transform of the same raw values."""
+    inp, bias = _raw_dt_case(2, 700, 4, 2, dtype, seed=61)
+    kw = dict(dt_bias=bias, dt_softplus=True, dt_limit=limit)
+    y, f = scan_on_gpu(inp, dtype, 256, algo, **kw)
+    lo, hi = limit if limit else (-np.inf, np.inf)
+    ref = dict(inp, dt=oracle.dt_transform(inp["dt"], bias, True, lo, hi))
+    yr, fr = scan_oracle(ref)
+    tol = TOL[dtype]
+    assert rel(y, yr) <= tol and rel(f, fr) <= tol, (rel(y, yr), rel(f, fr))
+
+
+def test_scan_dt_transform_rejects_inverted_limits():
+    import state_space_model_chunked_gb300 as ssd
+    inp, bias = _raw_dt_case(1, 128, 2, 1, "bf16", seed=62)
+    with pytest.raises(ssd.SsdError) as e:
+        scan_on_gpu(inp, "bf16", 128, AUTO, dt_softplus=True, dt_limit=(1.0, 0.5))
+    assert e.value.code == 1
+
