@@ -387,6 +387,128 @@ def time_decode_per_layer(batch, steps, device, peaks):
             "ms_per_step": ms, "GB_per_s": gbs, "frac_of_measured_hbm": gbs / peaks["hbm_gbs"]}
 
 
+def time_decode_vs_recompute(device, prefixes=(4096, 65536), reps=20):
+    """One 2.7B-shaped layer (80 heads, headdim 64, d_state 128), batch 1: the
+    next token's output from the cached state (one ssd_state_update) against
+    recomputing it from scratch (ssd_scan_fwd over the prefix plus the token)."""
+    import torch
+    import state_space_model_chunked_gb300 as ssd
+    from state_space_model_chunked_gb300 import inputs as gen
+    H, P, N = 80, 64, 128
+    out = []
+    A, D = gen.decode_params(H, seed=3)
+    A, D = torch.from_numpy(A).to(device), torch.from_numpy(D).to(device)
+    state = gen.device_decode_state(1, H, P, N, seed=3, device=device)
+    tok = gen.device_decode_token_inputs(1, H, P, N, 1, seed=3, step=0, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(device)
+        e0.record(stream)
+        for _ in range(reps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize(device)
+        return e0.elapsed_time(e1) / reps
+
+    dec_ms = timed(lambda: ssd.state_update(state, tok["x"], tok["dt"], A, tok["B"], tok["C"], D))
+    for T in prefixes:
+        g = torch.Generator(device=device)
+        g.manual_seed(T)
+        L = T + 1
+        x = torch.randn((1, L, H, P), generator=g, device=device).to(torch.bfloat16)
+        dt = torch.exp(-6.9 + 4.6 * torch.rand((1, L, H), generator=g, device=device))
+        B = torch.randn((1, L, 1, N), generator=g, device=device).to(torch.bfloat16)
+        C = torch.randn((1, L, 1, N), generator=g, device=device).to(torch.bfloat16)
+        ws = torch.empty(max(ssd.scan_workspace_bytes(1, L, H, P, N, 1, 256, device=device), 1),
+                         dtype=torch.uint8, device=device)
+        y = torch.empty_like(x)
+        fin = torch.empty((1, H, P, N), dtype=torch.float32, device=device)
+        scan_ms = timed(lambda: ssd.scan_fwd(x, dt, A, B, C, D, 256, None, y=y, final_state=fin,
+                                             workspace=ws))
+        out.append({"prefix_tokens": T, "recompute_ms": scan_ms, "cached_decode_ms": dec_ms,
+                    "speedup": scan_ms / dec_ms})
+        del x, dt, B, C, ws, y
+    torch.cuda.empty_cache()
+    return out
+
+
+def time_varlen(device, peaks, total=65536, reps=10):
+    """A packed batch of the 80-head layer (headdim 64, d_state 128): sequences
+    of log-uniform lengths in [64, 8192] tokens, `total` tokens in all, as one
+    ssd_scan_fwd_varlen call, against the batched call on the same sequences
+    each padded to the longest (what the batched entry point needs)."""
+    import numpy as np
+    import torch
+    import state_space_model_chunked_gb300 as ssd
+    from state_space_model_chunked_gb300 import inputs as gen
+    H, P, N = 80, 64, 128
+    lengths, acc = [], 0
+    for v in gen.packed_lengths(256, 64, 8192, seed=5):
+        v = min(v, total - acc)
+        lengths.append(v)
+        acc += v
+        if acc == total:
+            break
+    nseq, Lmax = len(lengths), max(lengths)
+    cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
+    g = torch.Generator(device=device)
+    g.manual_seed(77)
+
+    def tensors(shape_x, shape_dt, shape_bc):
+        return (torch.randn(shape_x, generator=g, device=device).to(torch.bfloat16),
+                torch.exp(-6.9 + 4.6 * torch.rand(shape_dt, generator=g, device=device)),
+                torch.randn(shape_bc, generator=g, device=device).to(torch.bfloat16),
+                torch.randn(shape_bc, generator=g, device=device).to(torch.bfloat16))
+
+    A = -torch.exp(2.77 * torch.rand((H,), generator=g, device=device))
+    D = torch.randn((H,), generator=g, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(device)
+        e0.record(stream)
+        for _ in range(reps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize(device)
+        return e0.elapsed_time(e1) / reps
+
+    x, dt, B, C = tensors((total, H, P), (total, H), (total, 1, N))
+    y = torch.empty_like(x)
+    fin = torch.empty((nseq, H, P, N), dtype=torch.float32, device=device)
+    cu_dev = torch.from_numpy(cu).to(device)
+    ws = torch.empty(max(ssd.scan_varlen_workspace_bytes(cu, H, P, N, 1, 256, device=device), 1),
+                     dtype=torch.uint8, device=device)
+    packed_ms = timed(lambda: ssd.scan_fwd_varlen(x, dt, A, B, C, cu, D, 256, None, y=y,
+                                                  final_state=fin, workspace=ws,
+                                                  cu_seqlens_dev=cu_dev))
+    byts = 2 * total * H * P * 2 + total * H * 4 + 2 * total * N * 2 + nseq * H * P * N * 4
+    del x, dt, B, C, y, ws
+    xp, dtp, Bp, Cp = tensors((nseq, Lmax, H, P), (nseq, Lmax, H), (nseq, Lmax, 1, N))
+    yp = torch.empty_like(xp)
+    finp = torch.empty((nseq, H, P, N), dtype=torch.float32, device=device)
+    wsp = torch.empty(max(ssd.scan_workspace_bytes(nseq, Lmax, H, P, N, 1, 256, device=device),
+                          1), dtype=torch.uint8, device=device)
+    padded_ms = timed(lambda: ssd.scan_fwd(xp, dtp, A, Bp, Cp, D, 256, None, y=yp,
+                                           final_state=finp, workspace=wsp))
+    del xp, dtp, Bp, Cp, yp, wsp
+    torch.cuda.empty_cache()
+    achieved = byts / (packed_ms * 1e-3) / 1e9
+    return {"workload": f"mamba2_2p7b packed: {nseq} sequences, log-uniform lengths "
+                        f"64..8192, {total} tokens (longest {Lmax})",
+            "packed_ms": packed_ms, "packed_Mtokens_per_s": total / (packed_ms * 1e-3) / 1e6,
+            "padded_ms": padded_ms, "padded_Mtokens_per_s": total / (padded_ms * 1e-3) / 1e6,
+            "call_roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                              "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"]}}
+
+
 def cpu_oracle_sample_one_core(shape, heads=2):
     """The oracle on one host core over `heads` whole heads of the workload,
     scaled to the full layer (heads are independent recurrences)."""
@@ -537,6 +659,8 @@ def run_gpu(args):
             extra["decode"] = [time_decode(b, 128, device, peaks) for b in (1, 16, 64, 256)]
             extra["decode_per_layer"] = [time_decode_per_layer(b, 32, device, peaks)
                                          for b in (1, 16)]
+            extra["decode_vs_recompute"] = time_decode_vs_recompute(device)
+            extra["varlen"] = time_varlen(device, peaks)
     clocks = clk.summary()
 
     e2e_s, h2d, d2h = time_scan_e2e(shape, max(args.steps // 4, 3), args.warmup, device)

@@ -156,6 +156,44 @@ ssd_status ssd_scan_fwd_dt(ssd_algo algo, const void *x, const float *dt,
                            void *workspace, size_t workspace_bytes,
                            cudaStream_t stream);
 
+/* Packed variable-length sequences: the scan of ssd_scan_fwd_dt run on each
+ * of nseq independent sequences laid end to end on one token axis (each
+ * sequence is its own recurrence with its own initial and final state, as
+ * the pages define the scan per sequence; the packing is this library's
+ * layout, not the pages').  Sequence s is tokens cu[s] .. cu[s+1]-1 of
+ * T = cu[nseq] tokens:
+ *   x, y   in_dtype [T][nheads][headdim];  dt float [T][nheads];
+ *   B, C   in_dtype [T][ngroups][dstate];
+ *   init_state, final_state  float [nseq][nheads][headdim][dstate] or NULL.
+ *   cu_seqlens_host  int [nseq + 1] HOST array: cu[0] = 0, non-decreasing.
+ *                    Empty sequences are allowed (final = initial state, or
+ *                    zeros); with T = 0 the token arrays may be NULL.  It
+ *                    sizes the grid and the workspace.
+ *   cu_seqlens_dev   the same nseq + 1 values in a DEVICE int array, read by
+ *                    the kernels; the two copies must agree (not checked).
+ * Other arguments and requirements as ssd_scan_fwd_dt.  The workspace is
+ * sized by ssd_scan_varlen_workspace_bytes() for the same offsets.
+ * Returns SSD_ERR_INVALID_ARG for offsets that do not start at 0 or decrease. */
+ssd_status ssd_scan_fwd_varlen(ssd_algo algo, const void *x, const float *dt,
+                               const float *A, const void *B, const void *C,
+                               const float *D, const ssd_dt_transform *dt_transform,
+                               ssd_dtype in_dtype, int nseq,
+                               const int *cu_seqlens_host,
+                               const int *cu_seqlens_dev, int nheads, int headdim,
+                               int dstate, int ngroups, int chunk,
+                               const float *init_state, void *y,
+                               float *final_state, void *workspace,
+                               size_t workspace_bytes, cudaStream_t stream);
+
+/* Workspace bytes and kernel launches of ssd_scan_fwd_varlen for these
+ * offsets on the current device ((size_t)-1 / -1 for invalid arguments). */
+size_t ssd_scan_varlen_workspace_bytes(int nseq, const int *cu_seqlens_host,
+                                       int nheads, int headdim, int dstate,
+                                       int ngroups, int chunk, ssd_dtype in_dtype);
+int ssd_scan_varlen_kernel_launches(int nseq, const int *cu_seqlens_host,
+                                    int nheads, int headdim, int dstate,
+                                    int ngroups, int chunk, ssd_dtype in_dtype);
+
 /* Profiling hook (process-wide, not for concurrent callers): while both
  * events are non-NULL, every following ssd_scan_fwd / ssd_scan_fwd_algo
  * records `before` immediately before and `after` immediately after the

@@ -95,6 +95,33 @@ def scan_seq(x, dt, A, B, C, D=None, init=None, nthreads=None):
     return y, fin
 
 
+def scan_varlen(x, dt, A, B, C, cu, D=None, init=None, nthreads=None):
+    """Packed sequences: x [T,H,P], dt [T,H], B/C [T,G,N], cu [nseq+1]
+    offsets (sequence s is tokens cu[s] .. cu[s+1]-1), init [nseq,H,P,N] or
+    None.  Each sequence is the recurrence on its own from its own initial
+    state (the pages define the scan per sequence; an empty one leaves its
+    state as it was).  Returns (y [T,H,P], final [nseq,H,P,N]) in float64."""
+    x, dt, B, C = _d(x), _d(dt), _d(B), _d(C)
+    cu = [int(v) for v in np.asarray(cu)]
+    nseq = len(cu) - 1
+    T, H, P = x.shape
+    N = B.shape[2]
+    y = np.empty((T, H, P), np.float64)
+    fin = np.zeros((nseq, H, P, N), np.float64)
+    for s in range(nseq):
+        a, b = cu[s], cu[s + 1]
+        h0 = None if init is None else _d(init)[s:s + 1]
+        if b == a:
+            if h0 is not None:
+                fin[s] = h0[0]
+            continue
+        ys, fs = scan_seq(x[None, a:b], dt[None, a:b], A, B[None, a:b], C[None, a:b],
+                          D, h0, nthreads)
+        y[a:b] = ys[0]
+        fin[s] = fs[0]
+    return y, fin
+
+
 def step(state, x, dt, A, B, C, D=None, nthreads=None):
     """One decode token.  state [b,H,P,N] (not modified; a float64 copy is
     updated and returned), x [b,H,P], dt [b,H], B/C [b,G,N].  Returns

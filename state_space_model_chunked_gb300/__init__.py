@@ -8,6 +8,7 @@ kernels; there is no CPU or PyTorch fallback.  If the library is missing or
 cannot load, every call raises.
 
     y, final = scan_fwd(x, dt, A, B, C, D, chunk=256, init_state=None)
+    y, finals = scan_fwd_varlen(x, dt, A, B, C, cu_seqlens, D)   # packed sequences
     y = state_update(state, x, dt, A, B, C, D)          # state updated in place
     pipe = HostScanPipeline(); pipe.submit(..., out=(y_host, final_host))  # host tensors
 """
@@ -21,8 +22,11 @@ from ._binding import (  # noqa: F401
     last_device_error,
     scan_fwd,
     scan_fwd_host,
+    scan_fwd_varlen,
     scan_kernel_launches,
     scan_profile_events,
+    scan_varlen_kernel_launches,
+    scan_varlen_workspace_bytes,
     scan_workspace_bytes,
     state_update,
     ALGO_AUTO,

@@ -17,6 +17,9 @@ EXPORTED_SYMBOLS = (
     "ssd_scan_fwd_algo",
     "ssd_scan_fwd_dt",
     "ssd_scan_fwd_static",
+    "ssd_scan_fwd_varlen",
+    "ssd_scan_varlen_workspace_bytes",
+    "ssd_scan_varlen_kernel_launches",
     "ssd_scan_profile_events",
     "ssd_state_update",
     "ssd_state_update_dt",
@@ -77,6 +80,13 @@ def load():
         lib.ssd_scan_fwd_dt.restype = _int
         lib.ssd_scan_fwd_dt.argtypes = [_int] + [_vp] * 7 + [_int] * 8 + [_vp, _vp, _vp, _vp,
                                                                             _sz, _vp]
+        lib.ssd_scan_fwd_varlen.restype = _int
+        lib.ssd_scan_fwd_varlen.argtypes = ([_int] + [_vp] * 7 + [_int, _int, _vp, _vp] +
+                                            [_int] * 5 + [_vp, _vp, _vp, _vp, _sz, _vp])
+        lib.ssd_scan_varlen_workspace_bytes.restype = _sz
+        lib.ssd_scan_varlen_workspace_bytes.argtypes = [_int, _vp] + [_int] * 6
+        lib.ssd_scan_varlen_kernel_launches.restype = _int
+        lib.ssd_scan_varlen_kernel_launches.argtypes = [_int, _vp] + [_int] * 6
         lib.ssd_state_update_dt.restype = _int
         lib.ssd_state_update_dt.argtypes = [_vp] * 8 + [_int] * 6 + [_vp, _vp]
         lib.ssd_scan_fwd_static.restype = _int
@@ -153,6 +163,36 @@ def scan_kernel_launches(batch, seqlen, nheads, headdim, dstate, ngroups, chunk,
     return int(n)
 
 
+def scan_varlen_workspace_bytes(cu_seqlens, nheads, headdim, dstate, ngroups, chunk,
+                                dtype=torch.bfloat16, device=None):
+    """Workspace bytes of scan_fwd_varlen for these offsets on the device."""
+    lib = load()
+    cu, cu_ptr = _host_offsets(cu_seqlens)
+    code = _BF16 if dtype == torch.bfloat16 else _F32
+    dev = torch.device("cuda") if device is None else torch.device(device)
+    with torch.cuda.device(dev):
+        n = lib.ssd_scan_varlen_workspace_bytes(cu.size - 1, cu_ptr, nheads, headdim, dstate,
+                                                ngroups, chunk, code)
+    if n == ctypes.c_size_t(-1).value:
+        raise SsdError("ssd_scan_varlen_workspace_bytes", 1, "invalid sizes or offsets")
+    return int(n)
+
+
+def scan_varlen_kernel_launches(cu_seqlens, nheads, headdim, dstate, ngroups, chunk,
+                                dtype=torch.bfloat16, device=None):
+    """Kernels one scan_fwd_varlen call enqueues for these offsets."""
+    lib = load()
+    cu, cu_ptr = _host_offsets(cu_seqlens)
+    code = _BF16 if dtype == torch.bfloat16 else _F32
+    dev = torch.device("cuda") if device is None else torch.device(device)
+    with torch.cuda.device(dev):
+        n = lib.ssd_scan_varlen_kernel_launches(cu.size - 1, cu_ptr, nheads, headdim, dstate,
+                                                ngroups, chunk, code)
+    if n < 0:
+        raise SsdError("ssd_scan_varlen_kernel_launches", 1, "invalid sizes or offsets")
+    return int(n)
+
+
 def _dt_transform(dt_bias, dt_softplus, dt_limit, H, dev):
     """A ctypes ssd_dt_transform for the keyword arguments, or None (identity)
     when none is set; the second value keeps dt_bias alive for the call."""
@@ -212,6 +252,79 @@ def scan_fwd(x, dt, A, B, C, D=None, chunk=256, init_state=None, *, y=None,
                                  _ptr(init_state), _ptr(y), _ptr(final_state),
                                  _ptr(workspace), wbytes, ctypes.c_void_p(stream))
     _check("ssd_scan_fwd", rc)
+    return y, final_state
+
+
+def _host_offsets(cu_seqlens):
+    """(numpy int32 host copy, ctypes pointer) of packed sequence offsets."""
+    import numpy as np
+    if isinstance(cu_seqlens, torch.Tensor):
+        cu_seqlens = cu_seqlens.detach().cpu().numpy()
+    cu = np.ascontiguousarray(np.asarray(cu_seqlens, dtype=np.int64))
+    if cu.ndim != 1 or cu.size < 2:
+        raise ValueError("cu_seqlens must hold nseq + 1 offsets")
+    if cu.max() >= 2 ** 31 or cu.min() < 0:
+        raise ValueError("cu_seqlens out of the int32 range")
+    cu = cu.astype(np.int32)
+    return cu, cu.ctypes.data_as(ctypes.c_void_p)
+
+
+def scan_fwd_varlen(x, dt, A, B, C, cu_seqlens, D=None, chunk=256, init_state=None, *,
+                    y=None, final_state=None, workspace=None, algo=ALGO_AUTO,
+                    return_final=True, dt_bias=None, dt_softplus=False, dt_limit=None,
+                    cu_seqlens_dev=None):
+    """Scan of nseq packed sequences.  x [T,H,P], dt [T,H] f32, B/C [T,G,N];
+    cu_seqlens: nseq + 1 token offsets (a list, numpy array or tensor; 0 first,
+    non-decreasing; sequence s is tokens cu[s]..cu[s+1]-1).  init_state and the
+    returned final_state are [nseq,H,P,N] f32.  ``cu_seqlens_dev`` (int32 on
+    x's device, same values) saves the host-to-device copy of the offsets.
+    dt transform keywords as scan_fwd.  Returns (y, final_state)."""
+    lib = load()
+    _need(x, "x")
+    dev = x.device
+    T, H, P = x.shape
+    _need(B, "B", x.dtype, dev)
+    G, N = B.shape[1], B.shape[2]
+    cu, cu_ptr = _host_offsets(cu_seqlens)
+    nseq = cu.size - 1
+    if int(cu[-1]) != T:
+        raise ValueError(f"cu_seqlens ends at {int(cu[-1])}, x holds {T} tokens")
+    _need(dt, "dt", torch.float32, dev, (T, H))
+    _need(A, "A", torch.float32, dev, (H,))
+    _need(B, "B", x.dtype, dev, (T, G, N))
+    _need(C, "C", x.dtype, dev, (T, G, N))
+    if D is not None:
+        _need(D, "D", torch.float32, dev, (H,))
+    if init_state is not None:
+        _need(init_state, "init_state", torch.float32, dev, (nseq, H, P, N))
+    if y is None:
+        y = torch.empty_like(x)
+    else:
+        _need(y, "y", x.dtype, dev, x.shape)
+    if final_state is None and return_final:
+        final_state = torch.empty((nseq, H, P, N), dtype=torch.float32, device=dev)
+    elif final_state is not None:
+        _need(final_state, "final_state", torch.float32, dev, (nseq, H, P, N))
+    if cu_seqlens_dev is None:
+        cu_seqlens_dev = torch.from_numpy(cu).to(dev, non_blocking=False)
+    else:
+        _need(cu_seqlens_dev, "cu_seqlens_dev", torch.int32, dev, (nseq + 1,))
+    code = _dtype_code(x)
+    with torch.cuda.device(dev):
+        need = lib.ssd_scan_varlen_workspace_bytes(nseq, cu_ptr, H, P, N, G, chunk, code)
+        if need == ctypes.c_size_t(-1).value:
+            raise SsdError("ssd_scan_varlen_workspace_bytes", 1, "invalid sizes or offsets")
+        if need > 0 and (workspace is None or workspace.numel() * workspace.element_size() < need):
+            workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+        wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+        stream = torch.cuda.current_stream(dev).cuda_stream
+        tptr, _keep = _dt_transform(dt_bias, dt_softplus, dt_limit, H, dev)
+        rc = lib.ssd_scan_fwd_varlen(algo, _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C),
+                                     _ptr(D), tptr, code, nseq, cu_ptr, _ptr(cu_seqlens_dev),
+                                     H, P, N, G, chunk, _ptr(init_state), _ptr(y),
+                                     _ptr(final_state), _ptr(workspace), wbytes,
+                                     ctypes.c_void_p(stream))
+    _check("ssd_scan_fwd_varlen", rc)
     return y, final_state
 
 

@@ -78,6 +78,68 @@ ssd_status dt_transform_of(const ssd_dt_transform *t, SsdDt *out) {
     return SSD_OK;
 }
 
+// Packed sequence offsets: nseq + 1 host ints from 0, non-decreasing, the
+// total within the int range the kernels index tokens with.
+ssd_status check_cu(int nseq, const int *cu) {
+    if (nseq <= 0 || !cu || cu[0] != 0) return SSD_ERR_INVALID_ARG;
+    for (int s = 0; s < nseq; ++s)
+        if (cu[s + 1] < cu[s]) return SSD_ERR_INVALID_ARG;
+    return SSD_OK;
+}
+
+// Both scan entry points: batched (cu_host == NULL; `batch` rows of `L`
+// tokens) and packed (`batch` sequences on one axis of L = cu_host[batch]).
+ssd_status scan_any(ssd_algo algo, const void *x, const float *dt, const float *A,
+                    const void *B, const void *C, const float *D,
+                    const ssd_dt_transform *dt_transform, ssd_dtype in_dtype, int batch, int L,
+                    int nheads, int headdim, int dstate, int ngroups, int chunk,
+                    const int *cu_host, const int *cu_dev, const float *init_state, void *y,
+                    float *final_state, void *workspace, size_t workspace_bytes,
+                    cudaStream_t stream) {
+    const bool packed = cu_host != nullptr;
+    // an all-empty packed batch has no token rows (the token arrays may be
+    // NULL): only final states are written
+    const bool rowless = packed && L == 0;
+    const void *tok = A;   // stands in for absent token arrays in the checks
+    ssd_status st = check_scan_args(rowless && !x ? tok : x, rowless && !dt ? A : dt, A,
+                                    rowless && !B ? tok : B, rowless && !C ? tok : C, D,
+                                    in_dtype, packed ? 1 : batch, rowless ? 1 : L, nheads,
+                                    headdim, dstate, ngroups, chunk, init_state,
+                                    rowless && !y ? tok : y, final_state);
+    if (st != SSD_OK) return st;
+    SsdDt dtt;
+    if ((st = dt_transform_of(dt_transform, &dtt)) != SSD_OK) return st;
+    if (algo != SSD_ALGO_AUTO && algo != SSD_ALGO_SIMT && algo != SSD_ALGO_TCGEN05)
+        return SSD_ERR_INVALID_ARG;
+    const bool bf16 = in_dtype == SSD_BF16;
+    bool use_tc = false;
+    SsdTcPlan plan{};
+    if (algo != SSD_ALGO_SIMT && bf16) {
+        plan = packed ? ssd_tc_plan_varlen(batch, cu_host, nheads, headdim, dstate, ngroups,
+                                           current_sm_count())
+                      : ssd_tc_plan(batch, L, nheads, headdim, dstate, ngroups,
+                                    current_sm_count());
+        use_tc = plan.supported;
+    }
+    if (algo == SSD_ALGO_TCGEN05 && !use_tc) return SSD_ERR_UNSUPPORTED;
+    if (!use_tc && batch > 65535) return SSD_ERR_UNSUPPORTED;   // grid z: one per sequence
+    cudaError_t e;
+    if (use_tc) {
+        if (plan.workspace > 0) {
+            if (!workspace || workspace_bytes < plan.workspace) return SSD_ERR_WORKSPACE;
+            if (((uintptr_t)workspace & 255u) != 0) return SSD_ERR_INVALID_ARG;
+        }
+        e = ssd_launch_scan_tc(plan, x, dt, A, B, C, D, init_state, y, final_state, batch, L,
+                               nheads, headdim, dstate, ngroups, workspace, device_error_word(),
+                               dtt, g_profile, stream, cu_dev);
+    } else {
+        e = ssd_launch_scan_simt(x, dt, A, B, C, D, init_state, y, final_state, bf16, batch, L,
+                                 nheads, headdim, dstate, ngroups, dtt, cu_dev, g_profile,
+                                 stream);
+    }
+    return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+}
+
 }  // namespace
 
 extern "C" {
@@ -141,37 +203,50 @@ ssd_status ssd_scan_fwd_dt(ssd_algo algo, const void *x, const float *dt, const 
                            int seqlen, int nheads, int headdim, int dstate, int ngroups,
                            int chunk, const float *init_state, void *y, float *final_state,
                            void *workspace, size_t workspace_bytes, cudaStream_t stream) {
-    ssd_status st = check_scan_args(x, dt, A, B, C, D, in_dtype, batch, seqlen, nheads,
-                                    headdim, dstate, ngroups, chunk, init_state, y,
-                                    final_state);
+    return scan_any(algo, x, dt, A, B, C, D, dt_transform, in_dtype, batch, seqlen, nheads,
+                    headdim, dstate, ngroups, chunk, nullptr, nullptr, init_state, y,
+                    final_state, workspace, workspace_bytes, stream);
+}
+
+size_t ssd_scan_varlen_workspace_bytes(int nseq, const int *cu_seqlens_host, int nheads,
+                                       int headdim, int dstate, int ngroups, int chunk,
+                                       ssd_dtype in_dtype) {
+    if (check_cu(nseq, cu_seqlens_host) != SSD_OK || nheads <= 0 || headdim <= 0 ||
+        dstate <= 0 || ngroups <= 0 || nheads % ngroups != 0 || !valid_chunk(chunk))
+        return (size_t)-1;
+    if (in_dtype != SSD_BF16) return 0;
+    const SsdTcPlan plan = ssd_tc_plan_varlen(nseq, cu_seqlens_host, nheads, headdim, dstate,
+                                              ngroups, current_sm_count());
+    return plan.supported ? plan.workspace : 0;
+}
+
+int ssd_scan_varlen_kernel_launches(int nseq, const int *cu_seqlens_host, int nheads,
+                                    int headdim, int dstate, int ngroups, int chunk,
+                                    ssd_dtype in_dtype) {
+    if (check_cu(nseq, cu_seqlens_host) != SSD_OK || nheads <= 0 || headdim <= 0 ||
+        dstate <= 0 || ngroups <= 0 || nheads % ngroups != 0 || !valid_chunk(chunk))
+        return -1;
+    if (in_dtype != SSD_BF16) return 1;
+    const SsdTcPlan plan = ssd_tc_plan_varlen(nseq, cu_seqlens_host, nheads, headdim, dstate,
+                                              ngroups, current_sm_count());
+    return plan.supported ? plan.launches : 1;
+}
+
+ssd_status ssd_scan_fwd_varlen(ssd_algo algo, const void *x, const float *dt, const float *A,
+                               const void *B, const void *C, const float *D,
+                               const ssd_dt_transform *dt_transform, ssd_dtype in_dtype,
+                               int nseq, const int *cu_seqlens_host,
+                               const int *cu_seqlens_dev, int nheads, int headdim, int dstate,
+                               int ngroups, int chunk, const float *init_state, void *y,
+                               float *final_state, void *workspace, size_t workspace_bytes,
+                               cudaStream_t stream) {
+    ssd_status st = check_cu(nseq, cu_seqlens_host);
     if (st != SSD_OK) return st;
-    SsdDt dtt;
-    if ((st = dt_transform_of(dt_transform, &dtt)) != SSD_OK) return st;
-    if (algo != SSD_ALGO_AUTO && algo != SSD_ALGO_SIMT && algo != SSD_ALGO_TCGEN05)
-        return SSD_ERR_INVALID_ARG;
-    const bool bf16 = in_dtype == SSD_BF16;
-    bool use_tc = false;
-    SsdTcPlan plan{};
-    if (algo != SSD_ALGO_SIMT && bf16) {
-        plan = ssd_tc_plan(batch, seqlen, nheads, headdim, dstate, ngroups, current_sm_count());
-        use_tc = plan.supported;
-    }
-    if (algo == SSD_ALGO_TCGEN05 && !use_tc) return SSD_ERR_UNSUPPORTED;
-    cudaError_t e;
-    if (use_tc) {
-        if (plan.workspace > 0) {
-            if (!workspace || workspace_bytes < plan.workspace) return SSD_ERR_WORKSPACE;
-            if (((uintptr_t)workspace & 255u) != 0) return SSD_ERR_INVALID_ARG;
-        }
-        e = ssd_launch_scan_tc(plan, x, dt, A, B, C, D, init_state, y, final_state, batch,
-                               seqlen, nheads, headdim, dstate, ngroups, workspace,
-                               device_error_word(), dtt, g_profile, stream);
-    } else {
-        e = ssd_launch_scan_simt(x, dt, A, B, C, D, init_state, y, final_state, bf16, batch,
-                                 seqlen, nheads, headdim, dstate, ngroups, dtt, g_profile,
-                                 stream);
-    }
-    return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+    if (!cu_seqlens_dev || ((uintptr_t)cu_seqlens_dev & 3u) != 0) return SSD_ERR_INVALID_ARG;
+    return scan_any(algo, x, dt, A, B, C, D, dt_transform, in_dtype, nseq,
+                    cu_seqlens_host[nseq], nheads, headdim, dstate, ngroups, chunk,
+                    cu_seqlens_host, cu_seqlens_dev, init_state, y, final_state, workspace,
+                    workspace_bytes, stream);
 }
 
 ssd_status ssd_scan_fwd_algo(ssd_algo algo, const void *x, const float *dt, const float *A,

@@ -36,7 +36,8 @@ cudaError_t ssd_launch_scan_simt(const void *x, const float *dt, const float *A,
                                  const void *B, const void *C, const float *D,
                                  const float *init, void *y, float *fin, bool bf16,
                                  int batch, int L, int H, int P, int N, int G,
-                                 const SsdDt &dtt, SsdProfileEvents prof, cudaStream_t stream);
+                                 const SsdDt &dtt, const int *cu, SsdProfileEvents prof,
+                                 cudaStream_t stream);
 
 // Tensor-core (tcgen05/TMEM/TMA) chunked scan.
 struct SsdTcPlan {
@@ -48,13 +49,22 @@ struct SsdTcPlan {
     int seg_heads;        // heads per CTA of the segment-contribution kernel
     size_t workspace;     // bytes of workspace required
     int launches;         // kernels enqueued per call
+    // work items: sequences, segment contributions (every segment but each
+    // sequence's last) and scan segments; batched plans have nseqs equal
+    // sequences of `tiles` tiles, packed plans (varlen) per-sequence lengths
+    bool varlen;
+    int nseqs, nslots, items;
 };
 
 SsdTcPlan ssd_tc_plan(int batch, int L, int H, int P, int N, int G, int num_sms);
+// Plan for nseq packed sequences, token offsets cu_host[0..nseq] (host copy).
+SsdTcPlan ssd_tc_plan_varlen(int nseq, const int *cu_host, int H, int P, int N, int G,
+                             int num_sms);
 
 cudaError_t ssd_launch_scan_tc(const SsdTcPlan &plan, const void *x, const float *dt,
                                const float *A, const void *B, const void *C,
                                const float *D, const float *init, void *y, float *fin,
                                int batch, int L, int H, int P, int N, int G,
                                void *workspace, unsigned int *err, const SsdDt &dtt,
-                               SsdProfileEvents prof, cudaStream_t stream);
+                               SsdProfileEvents prof, cudaStream_t stream,
+                               const int *cu_dev = nullptr);

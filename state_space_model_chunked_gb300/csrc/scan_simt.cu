@@ -50,7 +50,7 @@ ssd_scan_simt_kernel(const T *__restrict__ x, const float *__restrict__ dt,
                      const T *__restrict__ Cm, const float *__restrict__ D,
                      const float *__restrict__ init, T *__restrict__ y,
                      float *__restrict__ fin, int L, int H, int P, int N, int G,
-                     const SsdDt dtt) {
+                     const SsdDt dtt, const int *__restrict__ cu) {
     extern __shared__ __align__(16) float sm[];
     const int np = simt_np(N);
     float *Cs = sm;                       // [kT][np]
@@ -66,7 +66,10 @@ ssd_scan_simt_kernel(const T *__restrict__ x, const float *__restrict__ dt,
     const int tid = threadIdx.x;
     const int p0 = blockIdx.x * kPB;
     const int h = blockIdx.y;
-    const int b = blockIdx.z;
+    const int b = blockIdx.z;             // sequence (a batch row, or one of cu's)
+    // packed sequences: tokens cu[b] .. cu[b+1]-1 of the flattened token axis
+    const size_t grow0 = cu ? (size_t)cu[b] : (size_t)b * L;
+    const int Ls = cu ? cu[b + 1] - cu[b] : L;
     const int g = h / (H / G);
     const int pw = min(kPB, P - p0);
     const float Ah = A[h];
@@ -82,15 +85,15 @@ ssd_scan_simt_kernel(const T *__restrict__ x, const float *__restrict__ dt,
         *reinterpret_cast<float4 *>(Hs + p * np + n4) = v;
     }
 
-    for (int t0 = 0; t0 < L; t0 += kT) {
-        const int len = min(kT, L - t0);
+    for (int t0 = 0; t0 < Ls; t0 += kT) {
+        const int len = min(kT, Ls - t0);
         __syncthreads();   // previous tile fully consumed
         // ---- load the tile: dt, C, B (all N), x (this CTA's PB columns)
         for (int i = tid; i < kT * nq; i += kThreads) {
             const int t = i / nq, n4 = (i - t * nq) * 4;
             float4 c = make_float4(0.f, 0.f, 0.f, 0.f), bb = c;
             if (t < len) {
-                const size_t row = (((size_t)b * L + t0 + t) * G + g) * N + n4;
+                const size_t row = ((grow0 + t0 + t) * G + g) * N + n4;
                 c = ssd_ld4(Cm + row);
                 bb = ssd_ld4(Bm + row);
             }
@@ -100,14 +103,14 @@ ssd_scan_simt_kernel(const T *__restrict__ x, const float *__restrict__ dt,
         for (int i = tid; i < kT * kPB; i += kThreads) {
             const int t = i / kPB, p = i - t * kPB;
             float v = 0.f;
-            if (t < len && p < pw) v = ssd_ld(x + (((size_t)b * L + t0 + t) * H + h) * P + p0 + p);
+            if (t < len && p < pw) v = ssd_ld(x + ((grow0 + t0 + t) * H + h) * P + p0 + p);
             Xs[i] = v;
         }
         if (tid < 32) {
             // inclusive cumsum of dt*A over the tile: two tokens per lane
             const int ta = 2 * tid, tb = 2 * tid + 1;
-            const float da = ta < len ? ssd_dt<kDtX>(dtt, dt[((size_t)b * L + t0 + ta) * H + h], h) : 0.f;
-            const float db = tb < len ? ssd_dt<kDtX>(dtt, dt[((size_t)b * L + t0 + tb) * H + h], h) : 0.f;
+            const float da = ta < len ? ssd_dt<kDtX>(dtt, dt[(grow0 + t0 + ta) * H + h], h) : 0.f;
+            const float db = tb < len ? ssd_dt<kDtX>(dtt, dt[(grow0 + t0 + tb) * H + h], h) : 0.f;
             const float va = da * Ah, vb = db * Ah;
             float pair = va + vb;
             float incl = pair;
@@ -178,7 +181,7 @@ ssd_scan_simt_kernel(const T *__restrict__ x, const float *__restrict__ dt,
                     off = fmaf(c.w, hh.w, off);
                 }
                 const float v = acc + ea[t] * off + Dh * Xs[t * kPB + p];
-                if (p < pw) ssd_st(y + (((size_t)b * L + t0 + t) * H + h) * P + p0 + p, v);
+                if (p < pw) ssd_st(y + ((grow0 + t0 + t) * H + h) * P + p0 + p, v);
             }
         }
         __syncthreads();   // all reads of the entering state done
@@ -216,7 +219,8 @@ template <typename T, bool kDtX>
 cudaError_t launch_t(const void *x, const float *dt, const float *A, const void *B,
                      const void *C, const float *D, const float *init, void *y,
                      float *fin, int batch, int L, int H, int P, int N, int G,
-                     const SsdDt &dtt, SsdProfileEvents prof, cudaStream_t stream) {
+                     const SsdDt &dtt, const int *cu, SsdProfileEvents prof,
+                     cudaStream_t stream) {
     const size_t smem = simt_smem_bytes(N);
     cudaError_t e = cudaFuncSetAttribute(ssd_scan_simt_kernel<T, kDtX>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -226,7 +230,7 @@ cudaError_t launch_t(const void *x, const float *dt, const float *A, const void 
         return e;
     ssd_scan_simt_kernel<T, kDtX><<<grid, kThreads, smem, stream>>>(
         (const T *)x, dt, A, (const T *)B, (const T *)C, D, init, (T *)y, fin, L, H, P, N, G,
-        dtt);
+        dtt, cu);
     e = cudaGetLastError();
     if (e == cudaSuccess && prof.before && prof.after) e = ssd_record_event(prof.after, stream);
     return e;
@@ -240,15 +244,16 @@ cudaError_t ssd_launch_scan_simt(const void *x, const float *dt, const float *A,
                                  const void *B, const void *C, const float *D,
                                  const float *init, void *y, float *fin, bool bf16,
                                  int batch, int L, int H, int P, int N, int G,
-                                 const SsdDt &dtt, SsdProfileEvents prof, cudaStream_t stream) {
+                                 const SsdDt &dtt, const int *cu, SsdProfileEvents prof,
+                                 cudaStream_t stream) {
     const bool dtx = ssd_dt_active(dtt);
     if (bf16)
         return dtx ? launch_t<__nv_bfloat16, true>(x, dt, A, B, C, D, init, y, fin, batch, L, H,
-                                                   P, N, G, dtt, prof, stream)
+                                                   P, N, G, dtt, cu, prof, stream)
                    : launch_t<__nv_bfloat16, false>(x, dt, A, B, C, D, init, y, fin, batch, L,
-                                                    H, P, N, G, dtt, prof, stream);
+                                                    H, P, N, G, dtt, cu, prof, stream);
     return dtx ? launch_t<float, true>(x, dt, A, B, C, D, init, y, fin, batch, L, H, P, N, G,
-                                       dtt, prof, stream)
+                                       dtt, cu, prof, stream)
                : launch_t<float, false>(x, dt, A, B, C, D, init, y, fin, batch, L, H, P, N, G,
-                                        dtt, prof, stream);
+                                        dtt, cu, prof, stream);
 }

@@ -119,7 +119,124 @@ struct TcArgs {
     unsigned int *err;
     int L, H, G, tiles, seg_tiles, nseg;
     SsdDt dtt;             // transform of the raw step size
+    // packed sequences (cu != nullptr): tokens cu[s] .. cu[s+1]-1 of the
+    // flattened token axis form sequence s; item0 / fslot0 [nseq + 1] are the
+    // prefix sums of each sequence's segments and of its segments but the last
+    const int *cu;
+    const int *item0, *fslot0;
+    int nseq;
 };
+
+// Where one CTA's segment lies: its sequence, the sequence's first row in the
+// flattened token axis, its length, tiles and segments, the segment's index,
+// and the workspace slot of the sequence's first segment contribution.
+struct SegWork {
+    size_t grow0;
+    int seq, len, tiles, nseg, sigma, fslot;
+};
+
+// The segment of CTA (item, z): batched sequences are z with `item` the
+// segment; packed ones are found by binary search of the prefix tables (over
+// all segments, or over all but each sequence's last when `nonlast`).
+__device__ __forceinline__ SegWork seg_work(const TcArgs &a, int item, int z, bool nonlast) {
+    SegWork w;
+    if (!a.cu) {
+        w.seq = z;
+        w.grow0 = (size_t)z * a.L;
+        w.len = a.L;
+        w.tiles = a.tiles;
+        w.nseg = a.nseg;
+        w.sigma = item;
+        w.fslot = z * (a.nseg - 1);
+        return w;
+    }
+    const int *pre = nonlast ? a.fslot0 : a.item0;
+    int lo = 0, hi = a.nseq;                  // the last s with pre[s] <= item
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (pre[mid] <= item) lo = mid;
+        else hi = mid;
+    }
+    w.seq = lo;
+    w.grow0 = (size_t)a.cu[lo];
+    w.len = a.cu[lo + 1] - a.cu[lo];
+    w.tiles = (w.len + kTile - 1) / kTile;
+    w.nseg = (w.tiles + a.seg_tiles - 1) / a.seg_tiles;
+    w.sigma = item - pre[lo];
+    w.fslot = a.fslot0[lo];
+    return w;
+}
+
+// Prefix tables of packed sequences for the kernels above: item0[s] = segments
+// of sequences before s, fslot0[s] = their segments but each one's last.  One
+// block walks the sequences 1024 at a time.  An empty sequence has no segment
+// (no CTA visits it), so this kernel also gives it its final state: the
+// initial one (zeros without init), `hpn` = heads x P x N floats.
+__global__ void __launch_bounds__(1024)
+ssd_varlen_plan_kernel(const int *__restrict__ cu, int nseq, int seg_tiles, int *item0,
+                       int *fslot0, const float *__restrict__ init, float *__restrict__ fin,
+                       int hpn) {
+    __shared__ int wsum[2][32];
+    __shared__ int carry[2];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (tid == 0) carry[0] = carry[1] = 0;
+    __syncthreads();
+    for (int base = 0; base < nseq; base += 1024) {
+        const int s = base + tid;
+        int n = 0;
+        if (s < nseq) {
+            const int tiles = (cu[s + 1] - cu[s] + kTile - 1) / kTile;
+            n = (tiles + seg_tiles - 1) / seg_tiles;
+        }
+        int v[2] = {n, n > 0 ? n - 1 : 0};
+        int incl[2];
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            incl[k] = v[k];
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int o = __shfl_up_sync(0xffffffffu, incl[k], off);
+                if (lane >= off) incl[k] += o;
+            }
+            if (lane == 31) wsum[k][warp] = incl[k];
+        }
+        __syncthreads();
+        if (warp == 0) {
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                int t = wsum[k][lane];
+#pragma unroll
+                for (int off = 1; off < 32; off <<= 1) {
+                    const int o = __shfl_up_sync(0xffffffffu, t, off);
+                    if (lane >= off) t += o;
+                }
+                wsum[k][lane] = t;        // inclusive over warps
+            }
+        }
+        __syncthreads();
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const int before = carry[k] + (warp > 0 ? wsum[k][warp - 1] : 0) + incl[k] - v[k];
+            if (s < nseq) (k == 0 ? item0 : fslot0)[s] = before;
+        }
+        __syncthreads();
+        if (tid == 0) {
+            carry[0] += wsum[0][31];
+            carry[1] += wsum[1][31];
+        }
+        __syncthreads();
+    }
+    if (tid == 0) {
+        item0[nseq] = carry[0];
+        fslot0[nseq] = carry[1];
+    }
+    if (!fin) return;
+    for (int s = 0; s < nseq; ++s) {
+        if (cu[s + 1] != cu[s]) continue;
+        const size_t o = (size_t)s * hpn;
+        for (int i = tid; i < hpn; i += 1024) fin[o + i] = init ? init[o + i] : 0.f;
+    }
+}
 
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int *abort_flag,
                                          unsigned int *err) {
@@ -190,12 +307,18 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
     constexpr uint32_t kStage = Lay::kStage;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int h0 = blockIdx.x * HG;
-    const int sigma = blockIdx.y;
-    const int b = blockIdx.z;
+    const SegWork w = seg_work(a, blockIdx.y, blockIdx.z, false);
+    const int sigma = w.sigma;
     const int g = h0 / (a.H / a.G);
     const int k0 = sigma * a.seg_tiles;
-    const int k1 = min(a.tiles, k0 + a.seg_tiles);
+    const int k1 = min(w.tiles, k0 + a.seg_tiles);
     const int ntile = k1 - k0;
+    // TMA coordinates of the sequence's token t: row trow + t of batch tb
+    const int trow = a.cu ? (int)w.grow0 : 0;
+    const int tb = a.cu ? 0 : w.seq;
+    // a packed sequence's partial last tile is written row by row, not by a
+    // TMA store (whose box would run into the next sequence)
+    auto partial = [&](int it) { return a.cu != nullptr && (k0 + it + 1) * kTile > w.len; };
 
     const uint32_t sbase = smem_u32(smem);
     if ((sbase & 1023u) != 0u) {
@@ -205,9 +328,8 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
     // barriers: 0,1 fullC[stage]; 2,3 emptyC[stage]; 4 fullB; 5 emptyB;
     //           6 g_full; 7 m_ready; 8 hx_ready; 9 hx_free; 10 y_full;
     //           11 y_done (Yd / Yo read, y staged over C); 12 g_free (the masks
-    //           in TMEM have been consumed); 13 at_ready (a_t and block ends of
-    //           the next tile written); 14,15 fullX[stage]; 16,17 emptyX[stage];
-    //           18 v_ready (v_s of the next tile written)
+    //           in TMEM have been consumed); 13 fac_ready (factor slot written);
+    //           14,15 fullX[stage]; 16,17 emptyX[stage]
     auto bar = [&](int i) { return sbase + 8u * (uint32_t)i; };
     uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + kOffTslot);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kOffAbort);
@@ -278,19 +400,20 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
                 mbar_arrive_expect_tx(bar(14 + stage), HG * kXBytes);
 #pragma unroll
                 for (int h = 0; h < HG; ++h)
-                    tma_load_4d(stg + kCBytes + h * kXBytes, &mapX, bar(14 + stage), 0, h0 + h, t0, b);
+                    tma_load_4d(stg + kCBytes + h * kXBytes, &mapX, bar(14 + stage), 0, h0 + h,
+                                trow + t0, tb);
                 // B of this tile (single buffer: free once the previous tile's state
                 // update has read it)
                 if (it >= 1 && !wait_bar(bar(5), (it - 1) & 1, abort_flag, a.err)) break;
                 mbar_arrive_expect_tx(bar(4), kBBytes);
-                tma_load_4d(b_base, &mapB, bar(4), 0, g, t0, b);
-                tma_load_4d(b_base + kBlk, &mapB, bar(4), 64, g, t0, b);
+                tma_load_4d(b_base, &mapB, bar(4), 0, g, trow + t0, tb);
+                tma_load_4d(b_base + kBlk, &mapB, bar(4), 64, g, trow + t0, tb);
                 // C of this tile (stage last used two tiles ago)
                 if (it >= 2 && !wait_bar(bar(2 + stage), ((it >> 1) - 1) & 1, abort_flag, a.err))
                     break;
                 mbar_arrive_expect_tx(bar(stage), kCBytes);
-                tma_load_4d(stg, &mapC, bar(stage), 0, g, t0, b);
-                tma_load_4d(stg + kBlk, &mapC, bar(stage), 64, g, t0, b);
+                tma_load_4d(stg, &mapC, bar(stage), 0, g, trow + t0, tb);
+                tma_load_4d(stg + kBlk, &mapC, bar(stage), 64, g, trow + t0, tb);
             }
         }
     } else if (warp == kIssuerA) {
@@ -369,9 +492,11 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
             const uint64_t x00 = smem_desc(tiles_base + kCBytes, kBlk, 1024, kSwizzle128B);
             auto store_y = [&](int k) {
                 const uint32_t ys = tiles_base + (k & 1) * kStage;
+                if (!partial(k)) {
 #pragma unroll
-                for (int h = 0; h < HG; ++h)
-                    tma_store_4d(&mapY, ys + h * kBlk, 0, h0 + h, (k0 + k) * kTile, b);
+                    for (int h = 0; h < HG; ++h)
+                        tma_store_4d(&mapY, ys + h * kBlk, 0, h0 + h, trow + (k0 + k) * kTile, tb);
+                }
                 bulk_commit();
             };
             int it = 0;
@@ -422,7 +547,7 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
                 const int tok = tok0 + i;
 #pragma unroll
                 for (int h = 0; h < HG; ++h)
-                    dn[h][i] = tok < a.L ? a.dt[((size_t)b * a.L + tok) * a.H + h0 + h] : 0.f;
+                    dn[h][i] = tok < w.len ? a.dt[(w.grow0 + tok) * a.H + h0 + h] : 0.f;
             }
         };
         // chunk-local inclusive cumsum a_t of dt A, the 32-block ends a_e(j) and
@@ -435,7 +560,7 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
             for (int h = 0; h < HG; ++h)
 #pragma unroll
                 for (int i = 0; i < 4; ++i)
-                    dn[h][i] = tok0 + i < a.L ? ssd_dt<kDtX>(a.dtt, dn[h][i], h0 + h) : 0.f;
+                    dn[h][i] = tok0 + i < w.len ? ssd_dt<kDtX>(a.dtt, dn[h][i], h0 + h) : 0.f;
 #pragma unroll
             for (int h = 0; h < HG; ++h) {
                 float c[4];
@@ -538,11 +663,10 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
                 uint32_t r[16];
                 if (it == 0) {
                     const float *src =
-                        sigma == 0 ? (a.init ? a.init + ((size_t)b * a.H + h0 + h) * kP * kN
+                        sigma == 0 ? (a.init ? a.init + ((size_t)w.seq * a.H + h0 + h) * kP * kN
                                              : nullptr)
                                    : a.ws_state +
-                                         (((size_t)b * (a.nseg - 1) + sigma - 1) * a.H + h0 + h) *
-                                             kP * kN;
+                                         ((size_t)(w.fslot + sigma - 1) * a.H + h0 + h) * kP * kN;
 #pragma unroll
                     for (int j = 0; j < 16; ++j)
                         r[j] = __float_as_uint(src ? src[(size_t)(16 * wg + j) * kN + row] : 0.f);
@@ -622,8 +746,8 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
                         auto lw = [&](int s) {
                             const int tok = tb + s;
                             const float d =
-                                tok < a.L
-                                    ? ssd_dt<kDtX>(a.dtt, a.dt[((size_t)b * a.L + tok) * a.H + h0 + hh], h0 + hh)
+                                tok < w.len
+                                    ? ssd_dt<kDtX>(a.dtt, a.dt[(w.grow0 + tok) * a.H + h0 + hh], h0 + hh)
                                     : 0.f;
                             return d > 0.f ? __expf(at[hh] - ah[s] + __logf(d)) : 0.f;
                         };
@@ -692,6 +816,7 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
                 const uint64_t ea2 = pack_f32x2(e_at, e_at), dsk2 = pack_f32x2(dsk, dsk);
                 const uint8_t *xs = tiles_ptr + stage * kStage + kCBytes + hh * kXBytes;
                 uint8_t *ybuf = tiles_ptr + stage * kStage + hh * kBlk;
+                const bool direct = partial(it);
 #pragma unroll
                 for (int c16 = 0; c16 < np; c16 += 16) {
                     const int pc = p0 + c16;
@@ -716,10 +841,16 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
                             pk[4 * half + e] = pack_bf16x2_from_f32x2(fma_f32x2(dsk2, x01, y01));
                         }
                     }
-                    *reinterpret_cast<uint4 *>(ybuf + sw128(row, pc)) =
-                        make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                    *reinterpret_cast<uint4 *>(ybuf + sw128(row, pc + 8)) =
-                        make_uint4(pk[4], pk[5], pk[6], pk[7]);
+                    if (!direct) {
+                        *reinterpret_cast<uint4 *>(ybuf + sw128(row, pc)) =
+                            make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                        *reinterpret_cast<uint4 *>(ybuf + sw128(row, pc + 8)) =
+                            make_uint4(pk[4], pk[5], pk[6], pk[7]);
+                    } else if (t0 + row < w.len) {
+                        __nv_bfloat16 *yr = a.y + ((w.grow0 + t0 + row) * a.H + h0 + hh) * kP + pc;
+                        *reinterpret_cast<uint4 *>(yr) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                        *reinterpret_cast<uint4 *>(yr + 8) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+                    }
                 }
             }
             fence_proxy_async_smem();
@@ -731,14 +862,14 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
             }
         }
         // ---- final state of the sequence (all MMAs completed: y_full of the last tile)
-        if (sigma == a.nseg - 1 && a.fin && ntile > 0 && !*abort_flag) {
+        if (sigma == w.nseg - 1 && a.fin && ntile > 0 && !*abort_flag) {
             tc_fence_after();
 #pragma unroll 1
             for (int h = 0; h < HG; ++h) {
                 uint32_t r[16];
                 tmem_ld16(tq + kColH + 64 * h + 16 * wg, r);
                 tmem_ld_wait();
-                float *dst = a.fin + ((size_t)b * a.H + h0 + h) * kP * kN;
+                float *dst = a.fin + ((size_t)w.seq * a.H + h0 + h) * kP * kN;
 #pragma unroll
                 for (int j = 0; j < 16; ++j) dst[(size_t)(16 * wg + j) * kN + row] = __uint_as_float(r[j]);
             }
@@ -772,12 +903,14 @@ ssd_tc_segment_kernel(const __grid_constant__ CUtensorMap mapB,
     constexpr uint32_t kStage = kBBytes + HG * kXBytes;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int h0 = blockIdx.x * HG;
-    const int sigma = blockIdx.y;                 // < nseg - 1
-    const int b = blockIdx.z;
+    const SegWork w = seg_work(a, blockIdx.y, blockIdx.z, true);
+    const int sigma = w.sigma;                    // < the sequence's last segment
     const int g = h0 / (a.H / a.G);
     const int k0 = sigma * a.seg_tiles;
-    const int k1 = min(a.tiles, k0 + a.seg_tiles);
+    const int k1 = min(w.tiles, k0 + a.seg_tiles);
     const int ntile = k1 - k0;
+    const int trow = a.cu ? (int)w.grow0 : 0;    // TMA row / batch of token 0
+    const int tb = a.cu ? 0 : w.seq;
 
     const uint32_t sbase = smem_u32(smem);
     if ((sbase & 1023u) != 0u) {
@@ -828,11 +961,12 @@ ssd_tc_segment_kernel(const __grid_constant__ CUtensorMap mapB,
                 const uint32_t stg = tiles_base + stage * kStage;
                 const int t0 = (k1 - 1 - it) * kTile;
                 mbar_arrive_expect_tx(bar(stage), kStage);
-                tma_load_4d(stg, &mapB, bar(stage), 0, g, t0, b);
-                tma_load_4d(stg + kBlk, &mapB, bar(stage), 64, g, t0, b);
+                tma_load_4d(stg, &mapB, bar(stage), 0, g, trow + t0, tb);
+                tma_load_4d(stg + kBlk, &mapB, bar(stage), 64, g, trow + t0, tb);
 #pragma unroll
                 for (int h = 0; h < HG; ++h)
-                    tma_load_4d(stg + kBBytes + h * kXBytes, &mapX, bar(stage), 0, h0 + h, t0, b);
+                    tma_load_4d(stg + kBBytes + h * kXBytes, &mapX, bar(stage), 0, h0 + h,
+                                trow + t0, tb);
             }
         }
     } else if (warp == 1) {
@@ -874,8 +1008,8 @@ ssd_tc_segment_kernel(const __grid_constant__ CUtensorMap mapB,
                 const int tok = tok0 + i;
 #pragma unroll
                 for (int h = 0; h < HG; ++h)
-                    dn[h][i] = (it < ntile && tok < a.L) ? a.dt[((size_t)b * a.L + tok) * a.H + h0 + h]
-                                                         : 0.f;
+                    dn[h][i] = (it < ntile && tok < w.len) ? a.dt[(w.grow0 + tok) * a.H + h0 + h]
+                                                           : 0.f;
             }
         };
         load_dt4(0, d0);
@@ -890,7 +1024,7 @@ ssd_tc_segment_kernel(const __grid_constant__ CUtensorMap mapB,
                 for (int i = 0; i < 4; ++i) {
                     // the transform at use keeps the three tiles of loads in flight
                     const int tok = (k1 - 1 - it) * kTile + 4 * lane + i;
-                    d[h][i] = tok < a.L ? ssd_dt<kDtX>(a.dtt, d0[h][i], h0 + h) : 0.f;
+                    d[h][i] = tok < w.len ? ssd_dt<kDtX>(a.dtt, d0[h][i], h0 + h) : 0.f;
                     d0[h][i] = d1[h][i];
                     d1[h][i] = d2[h][i];
                 }
@@ -930,7 +1064,7 @@ ssd_tc_segment_kernel(const __grid_constant__ CUtensorMap mapB,
         if (lane == 0 && !*abort_flag) {
 #pragma unroll
             for (int h = 0; h < HG; ++h)
-                a.ws_decay[((size_t)b * (a.nseg - 1) + sigma) * a.H + h0 + h] = __expf(suf[h]);
+                a.ws_decay[(size_t)(w.fslot + sigma) * a.H + h0 + h] = __expf(suf[h]);
         }
     } else {
         // ------------------------------------------- X scaling, then F out
@@ -969,7 +1103,7 @@ ssd_tc_segment_kernel(const __grid_constant__ CUtensorMap mapB,
                 tmem_ld32(tq + 64 * h + 32 * wg, r);
                 tmem_ld_wait();
                 float *dst = a.ws_state +
-                             (((size_t)b * (a.nseg - 1) + sigma) * a.H + h0 + h) * kP * kN;
+                             ((size_t)(w.fslot + sigma) * a.H + h0 + h) * kP * kN;
 #pragma unroll
                 for (int j = 0; j < 32; ++j)
                     dst[(size_t)(32 * wg + j) * kN + row] = __uint_as_float(r[j]);
@@ -986,11 +1120,14 @@ ssd_tc_segment_kernel(const __grid_constant__ CUtensorMap mapB,
 
 // ============================================ entering state of each segment
 // Step-3 at segment granularity: H_in[s+1] = decay_s * H_in[s] + F_s, with
-// H_in[0] = init.  Overwrites slot s (F_s) with H_in[s+1].  Loads are issued
-// a batch ahead of the dependent FMA chain.
+// H_in[0] = the sequence's initial state.  Overwrites slot s (F_s) with
+// H_in[s+1].  A sequence's slots are nseg-1 consecutive ones from base
+// (batched: sequence q has base q (nseg-1); packed: fslot0[q] .. fslot0[q+1]).
+// Loads are issued a batch ahead of the dependent FMA chain.
 __global__ void __launch_bounds__(256)
 ssd_tc_segment_pass_kernel(float *__restrict__ ws_state, const float *__restrict__ ws_decay,
-                           const float *__restrict__ init, int batch, int H, int nseg) {
+                           const float *__restrict__ init, int nseqs, int H, int nseg,
+                           const int *__restrict__ fslot0) {
     constexpr int kBatch = 8;
     // let the scan kernel start right away: its first-segment CTAs need nothing
     // from here, the others wait for this grid before reading entering states
@@ -998,35 +1135,37 @@ ssd_tc_segment_pass_kernel(float *__restrict__ ws_state, const float *__restrict
     griddep_wait();                 // segment contributions are complete and visible
     const size_t per_head = (size_t)kP * kN / 4;
     const size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
-    const size_t total = (size_t)batch * H * per_head;
+    const size_t total = (size_t)nseqs * H * per_head;
     if (idx >= total) return;
-    const int b = (int)(idx / ((size_t)H * per_head));
-    const size_t rem = idx - (size_t)b * H * per_head;
+    const int q = (int)(idx / ((size_t)H * per_head));
+    const size_t rem = idx - (size_t)q * H * per_head;
     const int h = (int)(rem / per_head);
     const size_t e = rem - (size_t)h * per_head;
+    const int base = fslot0 ? fslot0[q] : q * (nseg - 1);
+    const int count = fslot0 ? fslot0[q + 1] - base : nseg - 1;
     float4 hv = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (init) hv = reinterpret_cast<const float4 *>(init)[((size_t)b * H + h) * per_head + e];
-    float4 *base = reinterpret_cast<float4 *>(ws_state);
-    for (int s0 = 0; s0 < nseg - 1; s0 += kBatch) {
+    if (init) hv = reinterpret_cast<const float4 *>(init)[((size_t)q * H + h) * per_head + e];
+    float4 *st = reinterpret_cast<float4 *>(ws_state);
+    for (int s0 = 0; s0 < count; s0 += kBatch) {
         float4 f[kBatch];
         float d[kBatch];
 #pragma unroll
         for (int i = 0; i < kBatch; ++i) {
-            if (s0 + i < nseg - 1) {
-                const size_t slot = ((size_t)b * (nseg - 1) + s0 + i) * H + h;
-                f[i] = base[slot * per_head + e];
+            if (s0 + i < count) {
+                const size_t slot = (size_t)(base + s0 + i) * H + h;
+                f[i] = st[slot * per_head + e];
                 d[i] = ws_decay[slot];
             }
         }
 #pragma unroll
         for (int i = 0; i < kBatch; ++i) {
-            if (s0 + i < nseg - 1) {
-                const size_t slot = ((size_t)b * (nseg - 1) + s0 + i) * H + h;
+            if (s0 + i < count) {
+                const size_t slot = (size_t)(base + s0 + i) * H + h;
                 hv.x = fmaf(d[i], hv.x, f[i].x);
                 hv.y = fmaf(d[i], hv.y, f[i].y);
                 hv.z = fmaf(d[i], hv.z, f[i].z);
                 hv.w = fmaf(d[i], hv.w, f[i].w);
-                base[slot * per_head + e] = hv;
+                st[slot * per_head + e] = hv;
             }
         }
     }
@@ -1088,7 +1227,7 @@ cudaError_t launch_segment(const SsdTcPlan &plan, const CUtensorMap &mB, const C
                                         (int)seg_smem<SG>());
     });
     if (attr_err != cudaSuccess) return attr_err;
-    dim3 g1(H / SG, plan.nseg - 1, batch);
+    dim3 g1(H / SG, plan.varlen ? plan.nslots : plan.nseg - 1, plan.varlen ? 1 : batch);
     ssd_tc_segment_kernel<SG, kDtX><<<g1, kSegThreads, seg_smem<SG>(), stream>>>(mB, mX, args);
     return cudaGetLastError();
 }
@@ -1132,24 +1271,32 @@ cudaError_t launch_hg(const SsdTcPlan &plan, const CUtensorMap &mC, const CUtens
     // there for short ones (A/B timed on the 130M and 2.7B layers)
     auto kernel = plan.seg_tiles >= kLongSegTiles ? ssd_tc_scan_kernel<HG, true, kDtX>
                                                   : ssd_tc_scan_kernel<HG, false, kDtX>;
-    if (plan.nseg > 1) {
+    if (plan.varlen) {
+        ssd_varlen_plan_kernel<<<1, 1024, 0, stream>>>(
+            args.cu, args.nseq, plan.seg_tiles, const_cast<int *>(args.item0),
+            const_cast<int *>(args.fslot0), args.init, args.fin, H * kP * kN);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    const bool chained = plan.nslots > 0;
+    if (chained) {
         cudaError_t e = plan.seg_heads == 4
                             ? launch_segment<4, kDtX>(plan, mB, mX, args, batch, H, stream)
                             : launch_segment<HG, kDtX>(plan, mB, mX, args, batch, H, stream);
         if (e != cudaSuccess) return e;
-        const size_t total = (size_t)batch * H * kP * kN / 4;
+        const size_t total = (size_t)plan.nseqs * H * kP * kN / 4;
         e = launch_pdl(ssd_tc_segment_pass_kernel, dim3((unsigned)((total + 255) / 256)),
-                       dim3(256), 0, stream, args.ws_state, args.ws_decay, args.init, batch, H,
-                       plan.nseg);
+                       dim3(256), 0, stream, args.ws_state, args.ws_decay, args.init,
+                       plan.nseqs, H, plan.nseg, plan.varlen ? args.fslot0 : nullptr);
         if (e != cudaSuccess) return e;
     }
-    dim3 g2(H / HG, plan.nseg, batch);
+    dim3 g2(H / HG, plan.varlen ? plan.items : plan.nseg, plan.varlen ? 1 : batch);
     if (prof.before && prof.after) {
         cudaError_t e = ssd_record_event(prof.before, stream);
         if (e != cudaSuccess) return e;
     }
     cudaError_t e;
-    if (plan.nseg > 1) {
+    if (chained) {
         // overlaps the scan kernel's prologue and first tile with the chaining kernel
         e = launch_pdl(kernel, g2, dim3(kThreads), scan_smem<HG>(), stream, mC, mB, mX, mY, args);
     } else {
@@ -1195,6 +1342,10 @@ SsdTcPlan ssd_tc_plan(int batch, int L, int H, int P, int N, int G, int num_sms)
     // grid still covers every SM.
     p.seg_heads = p.heads_per_cta;
     if ((H / G) % 4 == 0 && (long)batch * (H / 4) * (p.nseg - 1) >= num_sms) p.seg_heads = 4;
+    p.varlen = false;
+    p.nseqs = batch;
+    p.nslots = batch * (p.nseg - 1);
+    p.items = batch * p.nseg;
     if (p.nseg > 1) {
         const size_t state = (size_t)batch * (p.nseg - 1) * H * kP * kN * sizeof(float);
         const size_t decay = (size_t)batch * (p.nseg - 1) * H * sizeof(float);
@@ -1204,16 +1355,91 @@ SsdTcPlan ssd_tc_plan(int batch, int L, int H, int P, int N, int G, int num_sms)
     return p;
 }
 
+SsdTcPlan ssd_tc_plan_varlen(int nseq, const int *cu, int H, int P, int N, int G, int num_sms) {
+    SsdTcPlan p{};
+    p.launches = 1;
+    p.supported = P == kP && N == kN && num_sms > 0 && nseq > 0 && cu != nullptr && H > 0 &&
+                  G > 0 && H % G == 0 && encoder() != nullptr;
+    if (!p.supported) return p;
+    int max_tiles = 0;
+    for (int s = 0; s < nseq; ++s) {
+        const int len = cu[s + 1] - cu[s];
+        if (len < 0) {
+            p.supported = false;
+            return p;
+        }
+        max_tiles = max_tiles > (len + kTile - 1) / kTile ? max_tiles : (len + kTile - 1) / kTile;
+    }
+    if (max_tiles == 0) {   // no token at all: the SIMT path gives final = initial
+        p.supported = false;
+        return p;
+    }
+    p.varlen = true;
+    p.nseqs = nseq;
+    p.heads_per_cta = ((H / G) % 2 == 0) ? 2 : 1;
+    p.tiles = max_tiles;
+    const long units = H / p.heads_per_cta;
+    // The batched cost model over candidate segment lengths: waves x tiles per
+    // segment, 1.4x when any sequence is split.
+    auto segments = [&](int seg, long *items, long *slots) {
+        *items = 0;
+        *slots = 0;
+        for (int s = 0; s < nseq; ++s) {
+            const int tiles = (cu[s + 1] - cu[s] + kTile - 1) / kTile;
+            const int n = (tiles + seg - 1) / seg;
+            *items += n;
+            *slots += n > 0 ? n - 1 : 0;   // an empty sequence has no segment
+        }
+    };
+    static const int kCand[] = {1, 2, 3, 4, 6, 8, 12, 16, 24, 32, 48, 64, 96, 128, 192, 256};
+    double best = 1e300;
+    int best_seg = max_tiles;
+    for (int i = -1; i < (int)(sizeof(kCand) / sizeof(kCand[0])); ++i) {
+        const int seg = i < 0 ? max_tiles : kCand[i];
+        if (seg > max_tiles) continue;
+        long items, slots;
+        segments(seg, &items, &slots);
+        const long waves = (units * items + num_sms - 1) / num_sms;
+        const double cost = (double)waves * seg * (slots > 0 ? 1.4 : 1.0);
+        if (cost < best * 0.999) {
+            best = cost;
+            best_seg = seg;
+        }
+    }
+    p.seg_tiles = best_seg;
+    long items, slots;
+    segments(best_seg, &items, &slots);
+    if (items > 65535) {   // grid y holds the work items
+        p.supported = false;
+        return p;
+    }
+    p.items = (int)items;
+    p.nslots = (int)slots;
+    p.nseg = 0;                    // per sequence
+    p.seg_heads = p.heads_per_cta;
+    if ((H / G) % 4 == 0 && (long)(H / 4) * slots >= num_sms) p.seg_heads = 4;
+    const size_t state = (size_t)slots * H * kP * kN * sizeof(float);
+    const size_t decay = (size_t)slots * H * sizeof(float);
+    const size_t table = 2 * (size_t)(nseq + 1) * sizeof(int);
+    p.workspace = ((state + 255) / 256) * 256 + ((decay + 255) / 256) * 256 +
+                  ((table + 255) / 256) * 256;
+    p.launches = slots > 0 ? 4 : 2;
+    return p;
+}
+
 cudaError_t ssd_launch_scan_tc(const SsdTcPlan &plan, const void *x, const float *dt,
                                const float *A, const void *B, const void *C, const float *D,
                                const float *init, void *y, float *fin, int batch, int L, int H,
                                int P, int N, int G, void *workspace, unsigned int *err,
-                               const SsdDt &dtt, SsdProfileEvents prof, cudaStream_t stream) {
+                               const SsdDt &dtt, SsdProfileEvents prof, cudaStream_t stream,
+                               const int *cu_dev) {
     (void)P;
     (void)N;
+    // packed sequences: one batch row of L = total tokens
+    const int mrows = L, mbatch = plan.varlen ? 1 : batch;
     CUtensorMap mC, mB, mX, mY;
-    if (!make_map(&mC, C, kN, G, L, batch) || !make_map(&mB, B, kN, G, L, batch) ||
-        !make_map(&mX, x, kP, H, L, batch) || !make_map(&mY, y, kP, H, L, batch))
+    if (!make_map(&mC, C, kN, G, mrows, mbatch) || !make_map(&mB, B, kN, G, mrows, mbatch) ||
+        !make_map(&mX, x, kP, H, mrows, mbatch) || !make_map(&mY, y, kP, H, mrows, mbatch))
         return cudaErrorInvalidValue;
     TcArgs args{};
     args.dt = dt;
@@ -1221,12 +1447,21 @@ cudaError_t ssd_launch_scan_tc(const SsdTcPlan &plan, const void *x, const float
     args.A = A;
     args.D = D;
     args.init = init;
-    if (plan.nseg > 1) {
-        const size_t state = (size_t)batch * (plan.nseg - 1) * H * kP * kN * sizeof(float);
-        args.ws_state = static_cast<float *>(workspace);
-        args.ws_decay = reinterpret_cast<float *>(static_cast<char *>(workspace) +
-                                                  ((state + 255) / 256) * 256);
+    if (plan.nslots > 0 || plan.varlen) {
+        const size_t state = (size_t)plan.nslots * H * kP * kN * sizeof(float);
+        const size_t decay = (size_t)plan.nslots * H * sizeof(float);
+        char *ws = static_cast<char *>(workspace);
+        args.ws_state = reinterpret_cast<float *>(ws);
+        args.ws_decay = reinterpret_cast<float *>(ws + ((state + 255) / 256) * 256);
+        if (plan.varlen) {
+            int *table = reinterpret_cast<int *>(ws + ((state + 255) / 256) * 256 +
+                                                 ((decay + 255) / 256) * 256);
+            args.item0 = table;
+            args.fslot0 = table + (batch + 1);
+        }
     }
+    args.cu = plan.varlen ? cu_dev : nullptr;
+    args.nseq = plan.varlen ? batch : 0;
     args.y = static_cast<__nv_bfloat16 *>(y);
     args.fin = fin;
     args.err = err;

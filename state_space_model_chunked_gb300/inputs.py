@@ -115,6 +115,34 @@ def scan_inputs_for(shape: ScanShape, seed=0):
                        shape.random_init)
 
 
+def packed_lengths(nseq, lo, hi, seed=0):
+    """nseq sequence lengths, log-uniform in [lo, hi] (rounded down), a mix
+    of short and long sequences for a packed batch."""
+    rng = np.random.Generator(np.random.PCG64([seed, 7727]))
+    return [int(v) for v in np.exp(rng.uniform(np.log(lo), np.log(hi + 1), size=nseq))
+            .astype(np.int64).clip(lo, hi)]
+
+
+def varlen_inputs(lengths, nheads, headdim, dstate, ngroups, dtype="bf16", seed=0,
+                  random_init=False, with_D=True):
+    """Inputs for a scan of packed sequences laid end to end, sequence s being
+    tokens cu[s] .. cu[s+1]-1.  Token arrays are drawn as one scan_inputs row
+    of T = sum(lengths) tokens.  Returns the scan_inputs keys with the batch
+    axis dropped (x [T,H,P], dt [T,H], B, C [T,G,N]), init [nseq,H,P,N] (or
+    None) and cu [nseq+1] int32."""
+    lengths = [int(v) for v in lengths]
+    T = sum(lengths)
+    out = scan_inputs(1, T, nheads, headdim, dstate, ngroups, dtype, seed, False, with_D)
+    for k in ("x", "dt", "B", "C"):
+        out[k] = out[k][0]
+    out["cu"] = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
+    if random_init:
+        rng = np.random.Generator(np.random.PCG64([seed, 65537]))
+        out["init"] = (rng.standard_normal(size=(len(lengths), nheads, headdim, dstate),
+                                           dtype=np.float32) * np.float32(0.1)).astype(np.float32)
+    return out
+
+
 def decode_params(nheads, seed=0):
     """Per-head A and D for a decode layer stack (float32)."""
     rng = np.random.Generator(np.random.PCG64(seed + 7919))

@@ -122,3 +122,45 @@ def test_binding_refuses_cpu_tensors():
     with pytest.raises((ValueError, ImportError)):
         ssd.scan_fwd(x, torch.zeros(1, 4, 2), torch.zeros(2), torch.zeros(1, 4, 1, 8),
                      torch.zeros(1, 4, 1, 8))
+
+
+def _cu(vals):
+    arr = (ctypes.c_int * len(vals))(*vals)
+    return arr, ctypes.cast(arr, ctypes.c_void_p)
+
+
+def _varlen(lib, cu_vals, **kw):
+    keep, cu = _cu(cu_vals)
+    a = dict(algo=0, x=_fake(0x1000), dt=_fake(0x2000), A=_fake(0x3000), B=_fake(0x4000),
+             C=_fake(0x5000), D=None, tr=None, dtype=1, nseq=len(cu_vals) - 1, cu=cu,
+             cu_dev=_fake(0x8000), H=4, P=64, N=64, G=1, Q=64, init=None, y=_fake(0x6000),
+             fin=None, ws=None, wsb=0, stream=None)
+    a.update(kw)
+    return lib.ssd_scan_fwd_varlen(a["algo"], a["x"], a["dt"], a["A"], a["B"], a["C"], a["D"],
+                                   a["tr"], a["dtype"], a["nseq"], a["cu"], a["cu_dev"],
+                                   a["H"], a["P"], a["N"], a["G"], a["Q"], a["init"], a["y"],
+                                   a["fin"], a["ws"], a["wsb"], a["stream"])
+
+
+@pytest.mark.parametrize("cu_vals,kw", [
+    ([1, 5], {}),                        # offsets must start at 0
+    ([0, 5, 3], {}),                     # and never decrease
+    ([0, 5], dict(nseq=0)),
+    ([0, 5], dict(cu=None)),
+    ([0, 5], dict(cu_dev=None)),
+    ([0, 5], dict(cu_dev=_fake(0x8002))),  # int-misaligned device offsets
+    ([0, 5], dict(x=None)),              # tokens present: token arrays required
+    ([0, 5], dict(H=6, G=4)),
+])
+def test_varlen_rejects_bad_arguments(lib, cu_vals, kw):
+    assert _varlen(lib, cu_vals, **kw) == INVALID
+
+
+def test_varlen_queries(lib):
+    bad = ctypes.c_size_t(-1).value
+    keep, cu = _cu([0, 3, 2])
+    assert lib.ssd_scan_varlen_workspace_bytes(2, cu, 4, 64, 64, 1, 64, 1) == bad
+    assert lib.ssd_scan_varlen_kernel_launches(2, cu, 4, 64, 64, 1, 64, 1) == -1
+    keep, cu = _cu([0, 3, 9])
+    assert lib.ssd_scan_varlen_workspace_bytes(2, cu, 4, 64, 64, 1, 64, 0) == 0   # fp32: SIMT
+    assert lib.ssd_scan_varlen_kernel_launches(2, cu, 4, 64, 64, 1, 64, 0) == 1

@@ -275,3 +275,49 @@ def test_dt_transform_bias_per_head_then_clamp():
     out = oracle.dt_transform(dt, bias, softplus=True, lo=0.5, hi=2.0)
     assert np.allclose(out[0, 0], [0.5, np.log1p(np.exp(0.5)), 2.0], rtol=1e-15)
 
+
+
+# ---------------------------------------------------------------- packed sequences
+def test_varlen_is_each_sequence_alone_by_quadratic_form():
+    """Packed sequences: every sequence is its own scan from its own initial
+    state (the per-sequence recurrence of CGLA section III.A); checked per
+    sequence against the dual form, so state leaking across a boundary, a
+    shifted offset or a shared initial state fails.  An empty sequence keeps
+    its initial state."""
+    lengths = [5, 0, 13, 1, 9]
+    inp = gen.varlen_inputs(lengths, 3, 4, 8, 1, "bf16", seed=77, random_init=True)
+    y, fin = oracle.scan_varlen(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"],
+                                inp["cu"], inp["D"], inp["init"])
+    cu = inp["cu"]
+    for s in range(len(lengths)):
+        a, b = cu[s], cu[s + 1]
+        if a == b:
+            np.testing.assert_array_equal(fin[s], inp["init"][s])
+            continue
+        yq, fq = _quadratic(inp["x"][None, a:b], inp["dt"][None, a:b], inp["A"],
+                            inp["B"][None, a:b], inp["C"][None, a:b], inp["D"],
+                            inp["init"][s:s + 1])
+        assert _rel(y[a:b], yq[0]) < 1e-12
+        assert _rel(fin[s], fq[0]) < 1e-12
+
+
+def test_varlen_equal_lengths_is_the_batched_scan():
+    """Sequences of one length packed end to end are the batched layout with
+    the batch axis flattened into the token axis."""
+    b, L = 3, 17
+    inp = gen.scan_inputs(b, L, 2, 4, 8, 2, "f32", seed=5, random_init=True)
+    cu = np.arange(b + 1) * L
+    y, fin = oracle.scan_varlen(inp["x"].reshape(b * L, 2, 4), inp["dt"].reshape(b * L, 2),
+                                inp["A"], inp["B"].reshape(b * L, 2, 8),
+                                inp["C"].reshape(b * L, 2, 8), cu, inp["D"], inp["init"])
+    yb, fb = oracle.scan_seq(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], inp["D"],
+                             inp["init"])
+    np.testing.assert_array_equal(y, yb.reshape(b * L, 2, 4))
+    np.testing.assert_array_equal(fin, fb)
+
+
+def test_varlen_empty_sequence_without_init_is_zero_state():
+    inp = gen.varlen_inputs([0, 4], 2, 4, 8, 1, "f32", seed=3)
+    _, fin = oracle.scan_varlen(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"],
+                                inp["cu"], inp["D"])
+    assert not fin[0].any() and fin[1].any()

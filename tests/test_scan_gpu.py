@@ -244,3 +244,90 @@ def test_scan_dt_transform_rejects_inverted_limits():
         scan_on_gpu(inp, "bf16", 128, AUTO, dt_softplus=True, dt_limit=(1.0, 0.5))
     assert e.value.code == 1
 
+
+
+# ---------------------------------------------------------------- packed sequences
+def _varlen_on_gpu(inp, dtype, algo, chunk=256, **dt_kw):
+    import state_space_model_chunked_gb300 as ssd
+    if dt_kw.get("dt_bias") is not None:
+        dt_kw = dict(dt_kw, dt_bias=dev(dt_kw["dt_bias"]))
+    y, f = ssd.scan_fwd_varlen(dev(inp["x"], dtype), dev(inp["dt"]), dev(inp["A"]),
+                               dev(inp["B"], dtype), dev(inp["C"], dtype), inp["cu"],
+                               dev(inp["D"]), chunk, dev(inp["init"]), algo=algo, **dt_kw)
+    torch.cuda.synchronize()
+    return host(y), host(f)
+
+
+def _check_varlen(inp, dtype, algo, dt=None, **dt_kw):
+    """Whole-output and per-sequence relative L2 against the oracle (so the
+    error of a short sequence is not hidden by the long ones)."""
+    y, f = _varlen_on_gpu(inp, dtype, algo, **dt_kw)
+    d = inp["dt"] if dt is None else dt
+    yr, fr = oracle.scan_varlen(inp["x"], d, inp["A"], inp["B"], inp["C"], inp["cu"],
+                                inp["D"], inp["init"])
+    tol = TOL[dtype]
+    assert rel(y, yr) <= tol and rel(f, fr) <= tol, (rel(y, yr), rel(f, fr))
+    cu = inp["cu"]
+    for s in range(len(cu) - 1):
+        a, b = cu[s], cu[s + 1]
+        if a < b:
+            assert rel(y[a:b], yr[a:b]) <= tol, (s, rel(y[a:b], yr[a:b]))
+        assert rel(f[s], fr[s]) <= tol, (s, rel(f[s], fr[s]))
+
+
+@pytest.mark.parametrize("lengths,H,G,with_init", [
+    ([1, 127, 128, 129, 1000, 5000], 4, 1, True),    # ragged tails; long one split
+    ([300, 0, 2], 2, 1, True),                        # empty sequence in the middle
+    ([128] * 8, 4, 2, False),                         # tile-aligned boundaries
+    ([5000, 3], 3, 1, True),                          # odd heads per group
+    ([700, 64, 1, 2000, 333], 8, 1, False),           # four heads per group
+])
+@pytest.mark.parametrize("algo", [TC, SIMT])
+def test_varlen_matches_oracle(lengths, H, G, with_init, algo):
+    inp = gen.varlen_inputs(lengths, H, 64, 128, G, "bf16", seed=sum(lengths) + H,
+                            random_init=with_init)
+    _check_varlen(inp, "bf16", algo)
+
+
+def test_varlen_many_short_sequences():
+    """More sequences than the offset-table kernel's block (1024) walks at
+    once; lengths 1..40 tokens."""
+    lengths = gen.packed_lengths(2500, 1, 40, seed=3)
+    inp = gen.varlen_inputs(lengths, 2, 64, 128, 1, "bf16", seed=4, random_init=True)
+    _check_varlen(inp, "bf16", TC)
+
+
+def test_varlen_2p7b_heads_mixed_lengths():
+    """The 80-head model's shape on a packed batch of 16 log-uniform lengths
+    in [64, 8192] tokens."""
+    lengths = gen.packed_lengths(16, 64, 8192, seed=11)
+    inp = gen.varlen_inputs(lengths, 80, 64, 128, 1, "bf16", seed=12, random_init=True)
+    _check_varlen(inp, "bf16", AUTO)
+
+
+def test_varlen_dt_transform():
+    inp = gen.varlen_inputs([900, 17, 2100], 4, 64, 128, 1, "bf16", seed=21, random_init=True)
+    rng = np.random.default_rng(22)
+    inp["dt"] = rng.normal(-3.0, 1.0, size=inp["dt"].shape).astype(np.float32)
+    bias = rng.normal(0.0, 0.5, size=(4,)).astype(np.float32)
+    d = oracle.dt_transform(inp["dt"], bias, True, 1e-3, 0.2)
+    _check_varlen(inp, "bf16", TC, dt=d, dt_bias=bias, dt_softplus=True, dt_limit=(1e-3, 0.2))
+
+
+def test_varlen_without_tokens_returns_initial_states():
+    import state_space_model_chunked_gb300 as ssd
+    inp = gen.varlen_inputs([0, 0, 0], 2, 64, 128, 1, "bf16", seed=1, random_init=True)
+    y, f = _varlen_on_gpu(inp, "bf16", AUTO)
+    assert y.shape == (0, 2, 64)
+    np.testing.assert_array_equal(f, inp["init"])
+    with pytest.raises(ssd.SsdError):
+        _varlen_on_gpu(inp, "bf16", TC)
+
+
+def test_varlen_one_sequence_matches_batched_call():
+    inp = gen.scan_inputs(1, 3000, 4, 64, 128, 1, "bf16", seed=9, random_init=True)
+    yb, fb = scan_on_gpu(inp, "bf16", 256, TC)
+    packed = {k: (v[0] if k in ("x", "dt", "B", "C") else v) for k, v in inp.items()}
+    packed["cu"] = np.array([0, 3000], np.int32)
+    yv, fv = _varlen_on_gpu(packed, "bf16", TC)
+    assert rel(yv, yb[0]) <= 1e-3 and rel(fv, fb) <= 1e-3
