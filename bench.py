@@ -509,6 +509,56 @@ def time_varlen(device, peaks, total=65536, reps=10):
                               "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"]}}
 
 
+def time_fused_steps(shape, device, reps=20):
+    """The workload's scan with the layer's neighbouring steps fused (dt bias +
+    softplus + clamp on the input side, the silu(z) gate on the output side)
+    against the plain scan, on rotating input sets larger than L2."""
+    import torch
+    import state_space_model_chunked_gb300 as ssd
+    nsets = 10
+    sets = [make_scan_set(shape, 2000 + i, device) for i in range(nsets)]
+    g = torch.Generator(device=device)
+    g.manual_seed(5)
+    for s in sets:
+        s["z"] = torch.randn(s["x"].shape, generator=g, device=device).to(s["x"].dtype)
+    bias = torch.randn((shape.nheads,), generator=g, device=device) * 0.5
+    ws = torch.empty(max(ssd.scan_workspace_bytes(shape.batch, shape.seqlen, shape.nheads,
+                                                  shape.headdim, shape.dstate, shape.ngroups,
+                                                  shape.chunk, device=device), 1),
+                     dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def timed(dt_on, gate_on):
+        def call(i):
+            s = sets[i % nsets]
+            extra = {}
+            if dt_on:
+                extra.update(dt_bias=bias, dt_softplus=True, dt_limit=(1e-4, 0.1))
+            if gate_on:
+                extra["z"] = s["z"]
+            ssd.scan_fwd(s["x"], s["dt"], s["A"], s["B"], s["C"], s["D"], shape.chunk,
+                         s["init"], y=s["y"], final_state=s["final"], workspace=ws, **extra)
+        for i in range(3):
+            call(i)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(device)
+        e0.record(stream)
+        for i in range(reps):
+            call(i)
+        e1.record(stream)
+        torch.cuda.synchronize(device)
+        return e0.elapsed_time(e1) / reps
+
+    plain, dt_only, gate_only, fused = (timed(False, False), timed(True, False),
+                                        timed(False, True), timed(True, True))
+    del sets, ws
+    torch.cuda.empty_cache()
+    return {"workload": shape.name, "plain_ms": plain, "dt_transform_ms": dt_only,
+            "gate_ms": gate_only, "fused_ms": fused,
+            "fused_extra_bytes": shape.batch * shape.seqlen * shape.nheads * shape.headdim * 2,
+            "note": "eager calls (host overhead included in both)"}
+
+
 def cpu_oracle_sample_one_core(shape, heads=2):
     """The oracle on one host core over `heads` whole heads of the workload,
     scaled to the full layer (heads are independent recurrences)."""
@@ -661,6 +711,8 @@ def run_gpu(args):
                                          for b in (1, 16)]
             extra["decode_vs_recompute"] = time_decode_vs_recompute(device)
             extra["varlen"] = time_varlen(device, peaks)
+            extra["fused_steps"] = [time_fused_steps(gen.SCAN_SHAPES[n], device)
+                                    for n in (WORKLOAD, LONG_WORKLOAD)]
     clocks = clk.summary()
 
     e2e_s, h2d, d2h = time_scan_e2e(shape, max(args.steps // 4, 3), args.warmup, device)

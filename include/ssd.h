@@ -77,16 +77,20 @@ typedef enum {
                                dstate 64 or 128 */
 } ssd_algo;
 
-/* Bytes of device workspace ssd_scan_fwd needs for this shape on the CURRENT
- * device (the segment plan depends on its SM count).  Returns 0 when the
- * shape needs none, and (size_t)-1 for invalid sizes. */
+/* Bytes of device workspace a scan call needs for this shape on the CURRENT
+ * device (the segment plan depends on its SM count), enough for every entry
+ * point: on the tensor-core path it includes batch x seqlen x nheads floats
+ * for the transformed step sizes, which only a call with a dt transform uses
+ * (a call without one accepts a workspace that much smaller).  Returns 0 when
+ * the shape needs none, and (size_t)-1 for invalid sizes. */
 size_t ssd_scan_workspace_bytes(int batch, int seqlen, int nheads, int headdim,
                                 int dstate, int ngroups, int chunk,
                                 ssd_dtype in_dtype);
 
 /* Number of kernel launches ssd_scan_fwd enqueues for this shape on the
  * current device (for launch accounting and CUDA-graph planning); -1 for
- * invalid sizes. */
+ * invalid sizes.  A dt transform on the tensor-core path adds one (the
+ * elementwise pass that transforms every dt once). */
 int ssd_scan_kernel_launches(int batch, int seqlen, int nheads, int headdim,
                              int dstate, int ngroups, int chunk,
                              ssd_dtype in_dtype);
@@ -126,10 +130,12 @@ ssd_status ssd_scan_fwd_algo(ssd_algo algo, const void *x, const float *dt,
                              void *y, float *final_state, void *workspace,
                              size_t workspace_bytes, cudaStream_t stream);
 
-/* Optional transform of the raw step size, applied inside the kernels to
- * every dt they read (the pages take the step Delta from the input
- * projection, CGLA section III.A, without spelling out how it is made
- * positive; this is the usual bias + softplus parameterisation):
+/* Optional transform of the raw step size, applied to every dt the kernels
+ * read (the pages take the step Delta from the input projection, CGLA
+ * section III.A, without spelling out how it is made positive; this is the
+ * usual bias + softplus parameterisation).  The fp32 and decode kernels apply
+ * it where they read dt; the tensor-core path transforms every dt once, in an
+ * elementwise pass into the workspace, before its kernels run:
  *
  *   dt <- min(max(sp(dt_raw + dt_bias[h]), dt_min), dt_max)
  *   sp(u) = log(1 + e^u) when softplus != 0, else sp(u) = u.
@@ -171,13 +177,15 @@ ssd_status ssd_scan_fwd_dt(ssd_algo algo, const void *x, const float *dt,
  *                    sizes the grid and the workspace.
  *   cu_seqlens_dev   the same nseq + 1 values in a DEVICE int array, read by
  *                    the kernels; the two copies must agree (not checked).
+ *   z      in_dtype [T][nheads][headdim] or NULL: the output gate of
+ *          ssd_scan_fwd_fused.
  * Other arguments and requirements as ssd_scan_fwd_dt.  The workspace is
  * sized by ssd_scan_varlen_workspace_bytes() for the same offsets.
  * Returns SSD_ERR_INVALID_ARG for offsets that do not start at 0 or decrease. */
 ssd_status ssd_scan_fwd_varlen(ssd_algo algo, const void *x, const float *dt,
                                const float *A, const void *B, const void *C,
                                const float *D, const ssd_dt_transform *dt_transform,
-                               ssd_dtype in_dtype, int nseq,
+                               const void *z, ssd_dtype in_dtype, int nseq,
                                const int *cu_seqlens_host,
                                const int *cu_seqlens_dev, int nheads, int headdim,
                                int dstate, int ngroups, int chunk,
@@ -193,6 +201,26 @@ size_t ssd_scan_varlen_workspace_bytes(int nseq, const int *cu_seqlens_host,
 int ssd_scan_varlen_kernel_launches(int nseq, const int *cu_seqlens_host,
                                     int nheads, int headdim, int dstate,
                                     int ngroups, int chunk, ssd_dtype in_dtype);
+
+/* Output gate of the layer step after the scan, fused into the kernels that
+ * write y (the fusion of neighbouring layer steps into the scan that the
+ * compiler-first SSD page and the Mambalaya cascade describe; the gate's
+ * form is the usual Mamba-2 one, not spelled out on the pages):
+ *
+ *   y <- y * silu(z),   silu(z) = z / (1 + e^-z),
+ *
+ * applied after the D skip, before y is rounded to in_dtype.  z: in_dtype
+ * device array with y's layout, 16-byte aligned, or NULL (no gate).  The
+ * normalisation that may follow the gate in a layer is not fused (it reduces
+ * over all heads of a token).  Everything else as ssd_scan_fwd_dt. */
+ssd_status ssd_scan_fwd_fused(ssd_algo algo, const void *x, const float *dt,
+                              const float *A, const void *B, const void *C,
+                              const float *D, const ssd_dt_transform *dt_transform,
+                              const void *z, ssd_dtype in_dtype, int batch,
+                              int seqlen, int nheads, int headdim, int dstate,
+                              int ngroups, int chunk, const float *init_state,
+                              void *y, float *final_state, void *workspace,
+                              size_t workspace_bytes, cudaStream_t stream);
 
 /* Profiling hook (process-wide, not for concurrent callers): while both
  * events are non-NULL, every following ssd_scan_fwd / ssd_scan_fwd_algo
@@ -250,6 +278,15 @@ ssd_status ssd_state_update_dt(float *state, const void *x, const float *dt,
                                ssd_dtype in_dtype, int batch, int nheads,
                                int headdim, int dstate, int ngroups, void *y,
                                cudaStream_t stream);
+
+/* ssd_state_update_dt with the output gate of ssd_scan_fwd_fused: z is
+ * in_dtype [batch][nheads][headdim] (y's layout), 16-byte aligned, or NULL. */
+ssd_status ssd_state_update_fused(float *state, const void *x, const float *dt,
+                                  const float *A, const void *B, const void *C,
+                                  const float *D, const ssd_dt_transform *dt_transform,
+                                  const void *z, ssd_dtype in_dtype, int batch,
+                                  int nheads, int headdim, int dstate, int ngroups,
+                                  void *y, cudaStream_t stream);
 
 /* Human-readable name of a status code (static storage). */
 const char *ssd_status_string(ssd_status s);

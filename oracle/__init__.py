@@ -183,6 +183,15 @@ def dt_transform(dt, bias=None, softplus=False, lo=-np.inf, hi=np.inf):
     return np.minimum(np.maximum(u, lo), hi)
 
 
+def gate(y, z):
+    """The output gate in fp64: y * silu(z), silu(z) = z * sigmoid(z), with
+    sigmoid(z) = exp(-log(1 + e^-z)) (logaddexp, so no overflow).  The pages
+    fuse the layer's neighbouring steps into the scan without spelling the
+    gate out; this is the usual Mamba-2 form."""
+    z = np.asarray(z, dtype=np.float64)
+    return np.asarray(y, dtype=np.float64) * (z * np.exp(-np.logaddexp(0.0, -z)))
+
+
 def rel_l2(got, ref):
     """||got - ref||_2 / ||ref||_2 in float64 (absolute norm when ref == 0)."""
     got = np.asarray(got, dtype=np.float64)

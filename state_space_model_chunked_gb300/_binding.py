@@ -16,6 +16,7 @@ EXPORTED_SYMBOLS = (
     "ssd_scan_fwd",
     "ssd_scan_fwd_algo",
     "ssd_scan_fwd_dt",
+    "ssd_scan_fwd_fused",
     "ssd_scan_fwd_static",
     "ssd_scan_fwd_varlen",
     "ssd_scan_varlen_workspace_bytes",
@@ -23,6 +24,7 @@ EXPORTED_SYMBOLS = (
     "ssd_scan_profile_events",
     "ssd_state_update",
     "ssd_state_update_dt",
+    "ssd_state_update_fused",
     "ssd_status_string",
     "ssd_last_device_error",
 )
@@ -80,8 +82,11 @@ def load():
         lib.ssd_scan_fwd_dt.restype = _int
         lib.ssd_scan_fwd_dt.argtypes = [_int] + [_vp] * 7 + [_int] * 8 + [_vp, _vp, _vp, _vp,
                                                                             _sz, _vp]
+        lib.ssd_scan_fwd_fused.restype = _int
+        lib.ssd_scan_fwd_fused.argtypes = [_int] + [_vp] * 8 + [_int] * 8 + [_vp, _vp, _vp, _vp,
+                                                                               _sz, _vp]
         lib.ssd_scan_fwd_varlen.restype = _int
-        lib.ssd_scan_fwd_varlen.argtypes = ([_int] + [_vp] * 7 + [_int, _int, _vp, _vp] +
+        lib.ssd_scan_fwd_varlen.argtypes = ([_int] + [_vp] * 8 + [_int, _int, _vp, _vp] +
                                             [_int] * 5 + [_vp, _vp, _vp, _vp, _sz, _vp])
         lib.ssd_scan_varlen_workspace_bytes.restype = _sz
         lib.ssd_scan_varlen_workspace_bytes.argtypes = [_int, _vp] + [_int] * 6
@@ -89,6 +94,8 @@ def load():
         lib.ssd_scan_varlen_kernel_launches.argtypes = [_int, _vp] + [_int] * 6
         lib.ssd_state_update_dt.restype = _int
         lib.ssd_state_update_dt.argtypes = [_vp] * 8 + [_int] * 6 + [_vp, _vp]
+        lib.ssd_state_update_fused.restype = _int
+        lib.ssd_state_update_fused.argtypes = [_vp] * 9 + [_int] * 6 + [_vp, _vp]
         lib.ssd_scan_fwd_static.restype = _int
         lib.ssd_scan_fwd_static.argtypes = [_vp] * 6 + [_int] * 8 + [_vp, _vp, _vp, _vp]
         lib.ssd_scan_profile_events.restype = _int
@@ -208,13 +215,14 @@ def _dt_transform(dt_bias, dt_softplus, dt_limit, H, dev):
 
 def scan_fwd(x, dt, A, B, C, D=None, chunk=256, init_state=None, *, y=None,
              final_state=None, workspace=None, algo=ALGO_AUTO, return_final=True,
-             dt_bias=None, dt_softplus=False, dt_limit=None):
+             dt_bias=None, dt_softplus=False, dt_limit=None, z=None):
     """Chunked SSD scan (prefill).  x [b,L,H,P], dt [b,L,H] f32, A [H] f32,
     B/C [b,L,G,N] (x's dtype), D [H] f32 or None, init_state [b,H,P,N] f32 or
     None.  dt_bias [H] f32, dt_softplus and dt_limit = (lo, hi) transform the
     raw dt inside the kernels: dt <- clamp(softplus(dt + dt_bias), lo, hi)
-    (softplus only when dt_softplus).  Returns (y, final_state) on x's device
-    and the current stream."""
+    (softplus only when dt_softplus).  z (x's shape and dtype) gates the
+    output inside the kernels: y <- y * silu(z).  Returns (y, final_state) on
+    x's device and the current stream."""
     lib = load()
     _need(x, "x")
     dev = x.device
@@ -229,6 +237,8 @@ def scan_fwd(x, dt, A, B, C, D=None, chunk=256, init_state=None, *, y=None,
         _need(D, "D", torch.float32, dev, (H,))
     if init_state is not None:
         _need(init_state, "init_state", torch.float32, dev, (b, H, P, N))
+    if z is not None:
+        _need(z, "z", x.dtype, dev, x.shape)
     if y is None:
         y = torch.empty_like(x)
     else:
@@ -247,10 +257,10 @@ def scan_fwd(x, dt, A, B, C, D=None, chunk=256, init_state=None, *, y=None,
         wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
         stream = torch.cuda.current_stream(dev).cuda_stream
         tptr, _keep = _dt_transform(dt_bias, dt_softplus, dt_limit, H, dev)
-        rc = lib.ssd_scan_fwd_dt(algo, _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C),
-                                 _ptr(D), tptr, code, b, L, H, P, N, G, chunk,
-                                 _ptr(init_state), _ptr(y), _ptr(final_state),
-                                 _ptr(workspace), wbytes, ctypes.c_void_p(stream))
+        rc = lib.ssd_scan_fwd_fused(algo, _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C),
+                                    _ptr(D), tptr, _ptr(z), code, b, L, H, P, N, G, chunk,
+                                    _ptr(init_state), _ptr(y), _ptr(final_state),
+                                    _ptr(workspace), wbytes, ctypes.c_void_p(stream))
     _check("ssd_scan_fwd", rc)
     return y, final_state
 
@@ -272,13 +282,13 @@ def _host_offsets(cu_seqlens):
 def scan_fwd_varlen(x, dt, A, B, C, cu_seqlens, D=None, chunk=256, init_state=None, *,
                     y=None, final_state=None, workspace=None, algo=ALGO_AUTO,
                     return_final=True, dt_bias=None, dt_softplus=False, dt_limit=None,
-                    cu_seqlens_dev=None):
+                    z=None, cu_seqlens_dev=None):
     """Scan of nseq packed sequences.  x [T,H,P], dt [T,H] f32, B/C [T,G,N];
     cu_seqlens: nseq + 1 token offsets (a list, numpy array or tensor; 0 first,
     non-decreasing; sequence s is tokens cu[s]..cu[s+1]-1).  init_state and the
     returned final_state are [nseq,H,P,N] f32.  ``cu_seqlens_dev`` (int32 on
     x's device, same values) saves the host-to-device copy of the offsets.
-    dt transform keywords as scan_fwd.  Returns (y, final_state)."""
+    dt transform and gate (z [T,H,P]) keywords as scan_fwd.  Returns (y, final_state)."""
     lib = load()
     _need(x, "x")
     dev = x.device
@@ -297,6 +307,8 @@ def scan_fwd_varlen(x, dt, A, B, C, cu_seqlens, D=None, chunk=256, init_state=No
         _need(D, "D", torch.float32, dev, (H,))
     if init_state is not None:
         _need(init_state, "init_state", torch.float32, dev, (nseq, H, P, N))
+    if z is not None:
+        _need(z, "z", x.dtype, dev, x.shape)
     if y is None:
         y = torch.empty_like(x)
     else:
@@ -320,7 +332,8 @@ def scan_fwd_varlen(x, dt, A, B, C, cu_seqlens, D=None, chunk=256, init_state=No
         stream = torch.cuda.current_stream(dev).cuda_stream
         tptr, _keep = _dt_transform(dt_bias, dt_softplus, dt_limit, H, dev)
         rc = lib.ssd_scan_fwd_varlen(algo, _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C),
-                                     _ptr(D), tptr, code, nseq, cu_ptr, _ptr(cu_seqlens_dev),
+                                     _ptr(D), tptr, _ptr(z), code, nseq, cu_ptr,
+                                     _ptr(cu_seqlens_dev),
                                      H, P, N, G, chunk, _ptr(init_state), _ptr(y),
                                      _ptr(final_state), _ptr(workspace), wbytes,
                                      ctypes.c_void_p(stream))
@@ -431,11 +444,11 @@ class HostScanPipeline:
 
 
 def state_update(state, x, dt, A, B, C, D=None, *, y=None, dt_bias=None, dt_softplus=False,
-                 dt_limit=None):
+                 dt_limit=None, z=None):
     """One decode token.  state [b,H,P,N] f32 (updated in place), x [b,H,P],
     dt [b,H] f32, A [H] f32, B/C [b,G,N] (x's dtype), D [H] f32 or None;
-    dt_bias / dt_softplus / dt_limit as in scan_fwd.  Returns y [b,H,P] in x's
-    dtype."""
+    dt_bias / dt_softplus / dt_limit and the gate z [b,H,P] as in scan_fwd.
+    Returns y [b,H,P] in x's dtype."""
     lib = load()
     _need(state, "state", torch.float32)
     dev = state.device
@@ -449,6 +462,8 @@ def state_update(state, x, dt, A, B, C, D=None, *, y=None, dt_bias=None, dt_soft
     _need(C, "C", x.dtype, dev, (b, G, N))
     if D is not None:
         _need(D, "D", torch.float32, dev, (H,))
+    if z is not None:
+        _need(z, "z", x.dtype, dev, (b, H, P))
     if y is None:
         y = torch.empty_like(x)
     else:
@@ -457,9 +472,9 @@ def state_update(state, x, dt, A, B, C, D=None, *, y=None, dt_bias=None, dt_soft
     with torch.cuda.device(dev):
         stream = torch.cuda.current_stream(dev).cuda_stream
         tptr, _keep = _dt_transform(dt_bias, dt_softplus, dt_limit, H, dev)
-        rc = lib.ssd_state_update_dt(_ptr(state), _ptr(x), _ptr(dt), _ptr(A), _ptr(B),
-                                     _ptr(C), _ptr(D), tptr, code, b, H, P, N, G, _ptr(y),
-                                     ctypes.c_void_p(stream))
+        rc = lib.ssd_state_update_fused(_ptr(state), _ptr(x), _ptr(dt), _ptr(A), _ptr(B),
+                                        _ptr(C), _ptr(D), tptr, _ptr(z), code, b, H, P, N, G,
+                                        _ptr(y), ctypes.c_void_p(stream))
     _check("ssd_state_update", rc)
     return y
 

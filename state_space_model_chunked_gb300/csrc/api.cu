@@ -64,11 +64,12 @@ ssd_status check_scan_args(const void *x, const float *dt, const float *A, const
 }
 
 // The device-side form of a caller's dt transform; NULL is the identity.
-ssd_status dt_transform_of(const ssd_dt_transform *t, SsdDt *out) {
+ssd_status dt_transform_of(const ssd_dt_transform *t, SsdFuse *out) {
     out->bias = nullptr;
     out->softplus = 0;
     out->lo = -INFINITY;
     out->hi = INFINITY;
+    out->z = nullptr;
     if (!t) return SSD_OK;
     if (!(t->dt_min <= t->dt_max)) return SSD_ERR_INVALID_ARG;   // also rejects NaN
     out->bias = t->dt_bias;
@@ -91,8 +92,8 @@ ssd_status check_cu(int nseq, const int *cu) {
 // tokens) and packed (`batch` sequences on one axis of L = cu_host[batch]).
 ssd_status scan_any(ssd_algo algo, const void *x, const float *dt, const float *A,
                     const void *B, const void *C, const float *D,
-                    const ssd_dt_transform *dt_transform, ssd_dtype in_dtype, int batch, int L,
-                    int nheads, int headdim, int dstate, int ngroups, int chunk,
+                    const ssd_dt_transform *dt_transform, const void *z, ssd_dtype in_dtype,
+                    int batch, int L, int nheads, int headdim, int dstate, int ngroups, int chunk,
                     const int *cu_host, const int *cu_dev, const float *init_state, void *y,
                     float *final_state, void *workspace, size_t workspace_bytes,
                     cudaStream_t stream) {
@@ -107,8 +108,10 @@ ssd_status scan_any(ssd_algo algo, const void *x, const float *dt, const float *
                                     headdim, dstate, ngroups, chunk, init_state,
                                     rowless && !y ? tok : y, final_state);
     if (st != SSD_OK) return st;
-    SsdDt dtt;
-    if ((st = dt_transform_of(dt_transform, &dtt)) != SSD_OK) return st;
+    if (z && !aligned16(z)) return SSD_ERR_INVALID_ARG;
+    SsdFuse fuse;
+    if ((st = dt_transform_of(dt_transform, &fuse)) != SSD_OK) return st;
+    fuse.z = z;
     if (algo != SSD_ALGO_AUTO && algo != SSD_ALGO_SIMT && algo != SSD_ALGO_TCGEN05)
         return SSD_ERR_INVALID_ARG;
     const bool bf16 = in_dtype == SSD_BF16;
@@ -125,16 +128,19 @@ ssd_status scan_any(ssd_algo algo, const void *x, const float *dt, const float *
     if (!use_tc && batch > 65535) return SSD_ERR_UNSUPPORTED;   // grid z: one per sequence
     cudaError_t e;
     if (use_tc) {
-        if (plan.workspace > 0) {
-            if (!workspace || workspace_bytes < plan.workspace) return SSD_ERR_WORKSPACE;
+        // the transformed step sizes take the workspace's last region, needed
+        // only with a dt transform
+        const size_t need = ssd_dt_transform_active(fuse) ? plan.workspace : plan.dt_offset;
+        if (need > 0) {
+            if (!workspace || workspace_bytes < need) return SSD_ERR_WORKSPACE;
             if (((uintptr_t)workspace & 255u) != 0) return SSD_ERR_INVALID_ARG;
         }
         e = ssd_launch_scan_tc(plan, x, dt, A, B, C, D, init_state, y, final_state, batch, L,
                                nheads, headdim, dstate, ngroups, workspace, device_error_word(),
-                               dtt, g_profile, stream, cu_dev);
+                               fuse, g_profile, stream, cu_dev);
     } else {
         e = ssd_launch_scan_simt(x, dt, A, B, C, D, init_state, y, final_state, bf16, batch, L,
-                                 nheads, headdim, dstate, ngroups, dtt, cu_dev, g_profile,
+                                 nheads, headdim, dstate, ngroups, fuse, cu_dev, g_profile,
                                  stream);
     }
     return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
@@ -197,15 +203,27 @@ int ssd_scan_kernel_launches(int batch, int seqlen, int nheads, int headdim, int
     return plan.supported ? plan.launches : 1;
 }
 
+ssd_status ssd_scan_fwd_fused(ssd_algo algo, const void *x, const float *dt, const float *A,
+                              const void *B, const void *C, const float *D,
+                              const ssd_dt_transform *dt_transform, const void *z,
+                              ssd_dtype in_dtype, int batch, int seqlen, int nheads, int headdim,
+                              int dstate, int ngroups, int chunk, const float *init_state,
+                              void *y, float *final_state, void *workspace,
+                              size_t workspace_bytes, cudaStream_t stream) {
+    return scan_any(algo, x, dt, A, B, C, D, dt_transform, z, in_dtype, batch, seqlen, nheads,
+                    headdim, dstate, ngroups, chunk, nullptr, nullptr, init_state, y,
+                    final_state, workspace, workspace_bytes, stream);
+}
+
 ssd_status ssd_scan_fwd_dt(ssd_algo algo, const void *x, const float *dt, const float *A,
                            const void *B, const void *C, const float *D,
                            const ssd_dt_transform *dt_transform, ssd_dtype in_dtype, int batch,
                            int seqlen, int nheads, int headdim, int dstate, int ngroups,
                            int chunk, const float *init_state, void *y, float *final_state,
                            void *workspace, size_t workspace_bytes, cudaStream_t stream) {
-    return scan_any(algo, x, dt, A, B, C, D, dt_transform, in_dtype, batch, seqlen, nheads,
-                    headdim, dstate, ngroups, chunk, nullptr, nullptr, init_state, y,
-                    final_state, workspace, workspace_bytes, stream);
+    return ssd_scan_fwd_fused(algo, x, dt, A, B, C, D, dt_transform, nullptr, in_dtype, batch,
+                              seqlen, nheads, headdim, dstate, ngroups, chunk, init_state, y,
+                              final_state, workspace, workspace_bytes, stream);
 }
 
 size_t ssd_scan_varlen_workspace_bytes(int nseq, const int *cu_seqlens_host, int nheads,
@@ -234,8 +252,8 @@ int ssd_scan_varlen_kernel_launches(int nseq, const int *cu_seqlens_host, int nh
 
 ssd_status ssd_scan_fwd_varlen(ssd_algo algo, const void *x, const float *dt, const float *A,
                                const void *B, const void *C, const float *D,
-                               const ssd_dt_transform *dt_transform, ssd_dtype in_dtype,
-                               int nseq, const int *cu_seqlens_host,
+                               const ssd_dt_transform *dt_transform, const void *z,
+                               ssd_dtype in_dtype, int nseq, const int *cu_seqlens_host,
                                const int *cu_seqlens_dev, int nheads, int headdim, int dstate,
                                int ngroups, int chunk, const float *init_state, void *y,
                                float *final_state, void *workspace, size_t workspace_bytes,
@@ -243,7 +261,7 @@ ssd_status ssd_scan_fwd_varlen(ssd_algo algo, const void *x, const float *dt, co
     ssd_status st = check_cu(nseq, cu_seqlens_host);
     if (st != SSD_OK) return st;
     if (!cu_seqlens_dev || ((uintptr_t)cu_seqlens_dev & 3u) != 0) return SSD_ERR_INVALID_ARG;
-    return scan_any(algo, x, dt, A, B, C, D, dt_transform, in_dtype, nseq,
+    return scan_any(algo, x, dt, A, B, C, D, dt_transform, z, in_dtype, nseq,
                     cu_seqlens_host[nseq], nheads, headdim, dstate, ngroups, chunk,
                     cu_seqlens_host, cu_seqlens_dev, init_state, y, final_state, workspace,
                     workspace_bytes, stream);
@@ -270,28 +288,38 @@ ssd_status ssd_scan_fwd(const void *x, const float *dt, const float *A, const vo
                              final_state, workspace, workspace_bytes, stream);
 }
 
-ssd_status ssd_state_update_dt(float *state, const void *x, const float *dt, const float *A,
-                               const void *B, const void *C, const float *D,
-                               const ssd_dt_transform *dt_transform, ssd_dtype in_dtype,
-                               int batch, int nheads, int headdim, int dstate, int ngroups,
-                               void *y, cudaStream_t stream) {
+ssd_status ssd_state_update_fused(float *state, const void *x, const float *dt, const float *A,
+                                  const void *B, const void *C, const float *D,
+                                  const ssd_dt_transform *dt_transform, const void *z,
+                                  ssd_dtype in_dtype, int batch, int nheads, int headdim,
+                                  int dstate, int ngroups, void *y, cudaStream_t stream) {
     if (!state || !x || !dt || !A || !B || !C || !y) return SSD_ERR_INVALID_ARG;
     if (in_dtype != SSD_F32 && in_dtype != SSD_BF16) return SSD_ERR_INVALID_ARG;
     if (batch <= 0 || nheads <= 0 || headdim <= 0 || dstate <= 0 || ngroups <= 0)
         return SSD_ERR_INVALID_ARG;
     if (nheads % ngroups != 0) return SSD_ERR_INVALID_ARG;
     if (!pow2(dstate) || dstate < 4 || dstate > 256) return SSD_ERR_UNSUPPORTED;
-    const void *ptrs[] = {state, x, dt, A, B, C, D, y};
+    const void *ptrs[] = {state, x, dt, A, B, C, D, y, z};
     for (const void *p : ptrs)
         if (p && !aligned16(p)) return SSD_ERR_INVALID_ARG;
     if ((size_t)batch * nheads >= ((size_t)1 << 31)) return SSD_ERR_UNSUPPORTED;
-    SsdDt dtt;
-    const ssd_status st = dt_transform_of(dt_transform, &dtt);
+    SsdFuse fuse;
+    const ssd_status st = dt_transform_of(dt_transform, &fuse);
     if (st != SSD_OK) return st;
+    fuse.z = z;
     cudaError_t e = ssd_launch_decode(state, x, dt, A, B, C, D, y, in_dtype == SSD_BF16, batch,
                                       nheads, headdim, dstate, ngroups, current_sm_count(),
-                                      device_error_word(), dtt, stream);
+                                      device_error_word(), fuse, stream);
     return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+}
+
+ssd_status ssd_state_update_dt(float *state, const void *x, const float *dt, const float *A,
+                               const void *B, const void *C, const float *D,
+                               const ssd_dt_transform *dt_transform, ssd_dtype in_dtype,
+                               int batch, int nheads, int headdim, int dstate, int ngroups,
+                               void *y, cudaStream_t stream) {
+    return ssd_state_update_fused(state, x, dt, A, B, C, D, dt_transform, nullptr, in_dtype,
+                                  batch, nheads, headdim, dstate, ngroups, y, stream);
 }
 
 ssd_status ssd_state_update(float *state, const void *x, const float *dt, const float *A,

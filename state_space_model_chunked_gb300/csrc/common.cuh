@@ -17,43 +17,93 @@ __device__ __forceinline__ void ssd_report(unsigned int *err, unsigned int code)
     if (err) atomicCAS(err, 0u, code);
 }
 
-// Optional transform of the raw step size before it is used, the usual
-// parameterisation of a positive step from the input projection's output:
+// The neighbouring steps of a Mamba-2 layer fused into the kernels.
+// Input side, the transform of the raw step size (the usual parameterisation
+// of a positive step from the input projection's output):
 //   dt <- clamp(sp(dt_raw + bias[h]), lo, hi),  sp = softplus when enabled,
-// softplus(u) = log(1 + e^u) (u itself above 20, where they agree in fp32).
+// softplus(u) = log(1 + e^u) (u itself above 20, where they agree in fp32);
 // bias = nullptr, softplus = 0, lo = -inf, hi = +inf is the identity.
-struct SsdDt {
+// Output side, the gate: y <- y * silu(z), silu(z) = z / (1 + e^-z), with z
+// (the input dtype, y's layout) from the same projection; nullptr = no gate.
+struct SsdFuse {
     const float *bias;
     int softplus;
     float lo, hi;
+    const void *z;
 };
 
-// Kernels are instantiated with and without the transform (kOn): its code,
-// even untaken, costs the scan kernel a quarter of its speed, so the identity
-// instantiation carries none of it.
+// softplus(u) = log(1 + e^u) = max(u, 0) + log1p(e^-|u|) from the hardware
+// exponential and logarithm approximations: log1p(e) by its Taylor series
+// e - e^2/2 + e^3/3 - e^4/4 below e = 1/16 (truncation below e^5/5, relative
+// error under 3e-6), else log(1 + e), whose argument is then at least 1/16
+// away from 1 (relative error near 1e-5).  A few instructions instead of the
+// libm pair, for the single warps that compute per-token factors.
+__device__ __forceinline__ float ssd_softplus_fast(float u) {
+    const float e = __expf(-fabsf(u));
+    const float l = e < 0.0625f ? e * (1.f - e * (0.5f - e * (0.33333334f - 0.25f * e)))
+                                : __logf(1.f + e);
+    return fmaxf(u, 0.f) + l;
+}
+
+// The transform's per-head bias, read once per kernel and head (0 without).
 template <bool kOn>
-__device__ __forceinline__ float ssd_dt(const SsdDt &t, float raw, int h) {
+__device__ __forceinline__ float ssd_dt_bias(const SsdFuse &t, int h) {
     if constexpr (!kOn) {
         (void)t;
         (void)h;
+        return 0.f;
+    } else {
+        return t.bias ? t.bias[h] : 0.f;
+    }
+}
+
+// Kernels are instantiated with and without these steps (kOn): their code,
+// even untaken, costs the scan kernel a quarter of its speed, so the plain
+// instantiation carries none of it.  kFast selects ssd_softplus_fast (the
+// tensor-core kernels) over the libm form (fp32 paths).
+template <bool kOn, bool kFast = false>
+__device__ __forceinline__ float ssd_dt(const SsdFuse &t, float raw, float bias) {
+    if constexpr (!kOn) {
+        (void)t;
+        (void)bias;
         return raw;
     } else {
-        float v = raw;
-        if (t.bias) v += t.bias[h];
-        if (t.softplus) v = v > 20.f ? v : log1pf(expf(v));
+        float v = raw + bias;
+        if (t.softplus) {
+            if constexpr (kFast) v = ssd_softplus_fast(v);
+            else v = v > 20.f ? v : log1pf(expf(v));
+        }
         return fminf(fmaxf(v, t.lo), t.hi);
     }
 }
 
-inline bool ssd_dt_active(const SsdDt &t) {
+inline bool ssd_dt_transform_active(const SsdFuse &t) {
     return t.bias != nullptr || t.softplus != 0 || t.lo > -INFINITY || t.hi < INFINITY;
 }
+inline bool ssd_fuse_active(const SsdFuse &t) { return ssd_dt_transform_active(t) || t.z != nullptr; }
+
+// silu(z) = z * sigmoid(z) = z / (1 + e^-z) with the hardware exponential and
+// reciprocal approximations (relative error near 1e-6); for very negative z,
+// e^-z overflows to inf and the quotient is 0.
+__device__ __forceinline__ float ssd_silu(float z) { return __fdividef(z, 1.f + __expf(-z)); }
 
 // Element loads/stores for the two input dtypes.
 __device__ __forceinline__ float ssd_ld(const float *p) { return *p; }
 __device__ __forceinline__ float ssd_ld(const __nv_bfloat16 *p) { return __bfloat162float(*p); }
 __device__ __forceinline__ void ssd_st(float *p, float v) { *p = v; }
 __device__ __forceinline__ void ssd_st(__nv_bfloat16 *p, float v) { *p = __float2bfloat16_rn(v); }
+
+// The output gate applied to y at flat element index i of the y layout.
+template <bool kOn, typename T>
+__device__ __forceinline__ float ssd_gate(const SsdFuse &f, float y, size_t i) {
+    if constexpr (!kOn) {
+        (void)f;
+        (void)i;
+        return y;
+    } else {
+        return f.z ? y * ssd_silu(ssd_ld(static_cast<const T *>(f.z) + i)) : y;
+    }
+}
 
 // Four consecutive elements starting at a 4-element-aligned index.
 __device__ __forceinline__ float4 ssd_ld4(const float *p) {

@@ -24,13 +24,13 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kBatchRows = 8;   // rows each thread has in flight at once
 
-template <typename T, int VPT, bool kDtX>
+template <typename T, int VPT, bool kFuse>
 __global__ void __launch_bounds__(kThreads)
 ssd_decode_kernel(float *__restrict__ state, const T *__restrict__ x,
                   const float *__restrict__ dt, const float *__restrict__ A,
                   const T *__restrict__ Bm, const T *__restrict__ Cm,
                   const float *__restrict__ D, T *__restrict__ y, int H, int P,
-                  int N, int G, const SsdDt dtt) {
+                  int N, int G, const SsdFuse fuse) {
     const int bh = blockIdx.x;             // b * H + h
     const int b = bh / H, h = bh - b * H;
     const int g = h / (H / G);
@@ -39,7 +39,7 @@ ssd_decode_kernel(float *__restrict__ state, const T *__restrict__ x,
     const int lane_n = threadIdx.x % tpr;
     const int r0 = threadIdx.x / tpr;
 
-    const float dtv = ssd_dt<kDtX>(dtt, dt[bh], h);
+    const float dtv = ssd_dt<kFuse>(fuse, dt[bh], ssd_dt_bias<kFuse>(fuse, h));
     const float decay = expf(dtv * A[h]);
     const float Dh = D ? D[h] : 0.0f;
 
@@ -98,7 +98,8 @@ ssd_decode_kernel(float *__restrict__ state, const T *__restrict__ x,
             // reduce over the tpr threads of this row (aligned power-of-two group)
             for (int off = tpr >> 1; off > 0; off >>= 1)
                 acc += __shfl_xor_sync(0xffffffffu, acc, off);
-            if (p < P && lane_n == 0) ssd_st(yr + p, acc + Dh * xv[i]);
+            if (p < P && lane_n == 0)
+                ssd_st(yr + p, ssd_gate<kFuse, T>(fuse, acc + Dh * xv[i], (size_t)bh * P + p));
         }
     }
 }
@@ -129,13 +130,13 @@ __host__ __device__ inline StreamLayout stream_layout(int P, int N, int es) {
     return l;
 }
 
-template <typename T, int VPT, bool kDtX>
+template <typename T, int VPT, bool kFuse>
 __global__ void __launch_bounds__(kStreamThreads + 32, 1)
 ssd_decode_stream_kernel(float *__restrict__ state, const T *__restrict__ x,
                          const float *__restrict__ dt, const float *__restrict__ A,
                          const T *__restrict__ Bm, const T *__restrict__ Cm,
                          const float *__restrict__ D, T *__restrict__ y, int batch, int H, int P,
-                         int N, int G, int stages, unsigned int *err, const SsdDt dtt) {
+                         int N, int G, int stages, unsigned int *err, const SsdFuse fuse) {
     using namespace ssdptx;
     extern __shared__ __align__(1024) uint8_t smem[];
     const StreamLayout L = stream_layout(P, N, (int)sizeof(T));
@@ -207,7 +208,7 @@ ssd_decode_stream_kernel(float *__restrict__ state, const T *__restrict__ x,
             const int st = (int)(k % stages);
             const long u = unit_of(k);
             const int h = (int)(u % H);
-            const float dtv = ssd_dt<kDtX>(dtt, dt_next, h);
+            const float dtv = ssd_dt<kFuse>(fuse, dt_next, ssd_dt_bias<kFuse>(fuse, h));
             if (k + 1 < nk) dt_next = dt[unit_of(k + 1)];
             const float decay = expf(dtv * A[h]);
             const float Dh = D ? D[h] : 0.0f;
@@ -280,7 +281,9 @@ ssd_decode_stream_kernel(float *__restrict__ state, const T *__restrict__ x,
                 for (int i = 0; i < kStreamRows; ++i) {
                     const int e = e0 + i * kStreamThreads + tid;
                     if (e < total && lane_n == 0)
-                        ssd_st(y + (size_t)u * P + e / tpr, acc[i] + Dh * xv[i]);
+                        ssd_st(y + (size_t)u * P + e / tpr,
+                               ssd_gate<kFuse, T>(fuse, acc[i] + Dh * xv[i],
+                                                  (size_t)u * P + e / tpr));
                 }
             }
             fence_proxy_async_smem();
@@ -291,11 +294,11 @@ ssd_decode_stream_kernel(float *__restrict__ state, const T *__restrict__ x,
     __syncthreads();
 }
 
-template <typename T, bool kDtX>
+template <typename T, bool kFuse>
 cudaError_t launch_t(float *state, const void *x, const float *dt, const float *A,
                      const void *B, const void *C, const float *D, void *y, int batch,
                      int H, int P, int N, int G, int num_sms, unsigned int *err,
-                     const SsdDt &dtt, cudaStream_t stream) {
+                     const SsdFuse &fuse, cudaStream_t stream) {
     const size_t units = (size_t)batch * H;
     const StreamLayout lay = stream_layout(P, N, (int)sizeof(T));
     const int stages = (int)std::min<size_t>(8, kStreamRing / lay.stage_bytes);
@@ -306,29 +309,29 @@ cudaError_t launch_t(float *state, const void *x, const float *dt, const float *
         const size_t smem = (size_t)stages * lay.stage_bytes + 16 * stages + 16;
         cudaError_t e;
         if (N <= 128) {
-            e = cudaFuncSetAttribute(ssd_decode_stream_kernel<T, 1, kDtX>,
+            e = cudaFuncSetAttribute(ssd_decode_stream_kernel<T, 1, kFuse>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
             if (e != cudaSuccess) return e;
-            ssd_decode_stream_kernel<T, 1, kDtX><<<num_sms, kStreamThreads + 32, smem, stream>>>(
+            ssd_decode_stream_kernel<T, 1, kFuse><<<num_sms, kStreamThreads + 32, smem, stream>>>(
                 state, (const T *)x, dt, A, (const T *)B, (const T *)C, D, (T *)y, batch, H, P,
-                N, G, stages, err, dtt);
+                N, G, stages, err, fuse);
         } else {
-            e = cudaFuncSetAttribute(ssd_decode_stream_kernel<T, 2, kDtX>,
+            e = cudaFuncSetAttribute(ssd_decode_stream_kernel<T, 2, kFuse>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
             if (e != cudaSuccess) return e;
-            ssd_decode_stream_kernel<T, 2, kDtX><<<num_sms, kStreamThreads + 32, smem, stream>>>(
+            ssd_decode_stream_kernel<T, 2, kFuse><<<num_sms, kStreamThreads + 32, smem, stream>>>(
                 state, (const T *)x, dt, A, (const T *)B, (const T *)C, D, (T *)y, batch, H, P,
-                N, G, stages, err, dtt);
+                N, G, stages, err, fuse);
         }
         return cudaGetLastError();
     }
     const unsigned grid = (unsigned)units;
     if (N <= 128) {
-        ssd_decode_kernel<T, 1, kDtX><<<grid, kThreads, 0, stream>>>(
-            state, (const T *)x, dt, A, (const T *)B, (const T *)C, D, (T *)y, H, P, N, G, dtt);
+        ssd_decode_kernel<T, 1, kFuse><<<grid, kThreads, 0, stream>>>(
+            state, (const T *)x, dt, A, (const T *)B, (const T *)C, D, (T *)y, H, P, N, G, fuse);
     } else {
-        ssd_decode_kernel<T, 2, kDtX><<<grid, kThreads, 0, stream>>>(
-            state, (const T *)x, dt, A, (const T *)B, (const T *)C, D, (T *)y, H, P, N, G, dtt);
+        ssd_decode_kernel<T, 2, kFuse><<<grid, kThreads, 0, stream>>>(
+            state, (const T *)x, dt, A, (const T *)B, (const T *)C, D, (T *)y, H, P, N, G, fuse);
     }
     return cudaGetLastError();
 }
@@ -339,15 +342,15 @@ cudaError_t ssd_launch_decode(float *state, const void *x, const float *dt,
                               const float *A, const void *B, const void *C,
                               const float *D, void *y, bool bf16, int batch,
                               int H, int P, int N, int G, int num_sms, unsigned int *err,
-                              const SsdDt &dtt, cudaStream_t stream) {
-    const bool dtx = ssd_dt_active(dtt);
+                              const SsdFuse &fuse, cudaStream_t stream) {
+    const bool fused = ssd_fuse_active(fuse);
     if (bf16)
-        return dtx ? launch_t<__nv_bfloat16, true>(state, x, dt, A, B, C, D, y, batch, H, P, N,
-                                                   G, num_sms, err, dtt, stream)
+        return fused ? launch_t<__nv_bfloat16, true>(state, x, dt, A, B, C, D, y, batch, H, P, N,
+                                                   G, num_sms, err, fuse, stream)
                    : launch_t<__nv_bfloat16, false>(state, x, dt, A, B, C, D, y, batch, H, P, N,
-                                                    G, num_sms, err, dtt, stream);
-    return dtx ? launch_t<float, true>(state, x, dt, A, B, C, D, y, batch, H, P, N, G, num_sms,
-                                       err, dtt, stream)
+                                                    G, num_sms, err, fuse, stream);
+    return fused ? launch_t<float, true>(state, x, dt, A, B, C, D, y, batch, H, P, N, G, num_sms,
+                                       err, fuse, stream)
                : launch_t<float, false>(state, x, dt, A, B, C, D, y, batch, H, P, N, G, num_sms,
-                                        err, dtt, stream);
+                                        err, fuse, stream);
 }

@@ -11,7 +11,7 @@ cudaError_t ssd_launch_decode(float *state, const void *x, const float *dt,
                               const float *A, const void *B, const void *C,
                               const float *D, void *y, bool bf16, int batch,
                               int H, int P, int N, int G, int num_sms, unsigned int *err,
-                              const SsdDt &dtt, cudaStream_t stream);
+                              const SsdFuse &fuse, cudaStream_t stream);
 
 size_t ssd_simt_smem_bytes(int N);
 
@@ -36,7 +36,7 @@ cudaError_t ssd_launch_scan_simt(const void *x, const float *dt, const float *A,
                                  const void *B, const void *C, const float *D,
                                  const float *init, void *y, float *fin, bool bf16,
                                  int batch, int L, int H, int P, int N, int G,
-                                 const SsdDt &dtt, const int *cu, SsdProfileEvents prof,
+                                 const SsdFuse &fuse, const int *cu, SsdProfileEvents prof,
                                  cudaStream_t stream);
 
 // Tensor-core (tcgen05/TMEM/TMA) chunked scan.
@@ -54,6 +54,7 @@ struct SsdTcPlan {
     // sequences of `tiles` tiles, packed plans (varlen) per-sequence lengths
     bool varlen;
     int nseqs, nslots, items;
+    size_t dt_offset;     // workspace bytes before the transformed step sizes
 };
 
 SsdTcPlan ssd_tc_plan(int batch, int L, int H, int P, int N, int G, int num_sms);
@@ -65,6 +66,6 @@ cudaError_t ssd_launch_scan_tc(const SsdTcPlan &plan, const void *x, const float
                                const float *A, const void *B, const void *C,
                                const float *D, const float *init, void *y, float *fin,
                                int batch, int L, int H, int P, int N, int G,
-                               void *workspace, unsigned int *err, const SsdDt &dtt,
+                               void *workspace, unsigned int *err, const SsdFuse &fuse,
                                SsdProfileEvents prof, cudaStream_t stream,
                                const int *cu_dev = nullptr);

@@ -43,14 +43,14 @@ __host__ inline size_t simt_smem_bytes(int N) {
                             (size_t)kT * kMS + 4 * kT);
 }
 
-template <typename T, bool kDtX>
+template <typename T, bool kFuse>
 __global__ void __launch_bounds__(kThreads)
 ssd_scan_simt_kernel(const T *__restrict__ x, const float *__restrict__ dt,
                      const float *__restrict__ A, const T *__restrict__ Bm,
                      const T *__restrict__ Cm, const float *__restrict__ D,
                      const float *__restrict__ init, T *__restrict__ y,
                      float *__restrict__ fin, int L, int H, int P, int N, int G,
-                     const SsdDt dtt, const int *__restrict__ cu) {
+                     const SsdFuse fuse, const int *__restrict__ cu) {
     extern __shared__ __align__(16) float sm[];
     const int np = simt_np(N);
     float *Cs = sm;                       // [kT][np]
@@ -73,6 +73,7 @@ ssd_scan_simt_kernel(const T *__restrict__ x, const float *__restrict__ dt,
     const int g = h / (H / G);
     const int pw = min(kPB, P - p0);
     const float Ah = A[h];
+    const float dtb = ssd_dt_bias<kFuse>(fuse, h);
     const float Dh = D ? D[h] : 0.0f;
     const int nq = N / 4;
 
@@ -109,8 +110,8 @@ ssd_scan_simt_kernel(const T *__restrict__ x, const float *__restrict__ dt,
         if (tid < 32) {
             // inclusive cumsum of dt*A over the tile: two tokens per lane
             const int ta = 2 * tid, tb = 2 * tid + 1;
-            const float da = ta < len ? ssd_dt<kDtX>(dtt, dt[(grow0 + t0 + ta) * H + h], h) : 0.f;
-            const float db = tb < len ? ssd_dt<kDtX>(dtt, dt[(grow0 + t0 + tb) * H + h], h) : 0.f;
+            const float da = ta < len ? ssd_dt<kFuse>(fuse, dt[(grow0 + t0 + ta) * H + h], dtb) : 0.f;
+            const float db = tb < len ? ssd_dt<kFuse>(fuse, dt[(grow0 + t0 + tb) * H + h], dtb) : 0.f;
             const float va = da * Ah, vb = db * Ah;
             float pair = va + vb;
             float incl = pair;
@@ -181,7 +182,10 @@ ssd_scan_simt_kernel(const T *__restrict__ x, const float *__restrict__ dt,
                     off = fmaf(c.w, hh.w, off);
                 }
                 const float v = acc + ea[t] * off + Dh * Xs[t * kPB + p];
-                if (p < pw) ssd_st(y + ((grow0 + t0 + t) * H + h) * P + p0 + p, v);
+                if (p < pw) {
+                    const size_t yi = ((grow0 + t0 + t) * H + h) * P + p0 + p;
+                    ssd_st(y + yi, ssd_gate<kFuse, T>(fuse, v, yi));
+                }
             }
         }
         __syncthreads();   // all reads of the entering state done
@@ -215,22 +219,22 @@ ssd_scan_simt_kernel(const T *__restrict__ x, const float *__restrict__ dt,
     }
 }
 
-template <typename T, bool kDtX>
+template <typename T, bool kFuse>
 cudaError_t launch_t(const void *x, const float *dt, const float *A, const void *B,
                      const void *C, const float *D, const float *init, void *y,
                      float *fin, int batch, int L, int H, int P, int N, int G,
-                     const SsdDt &dtt, const int *cu, SsdProfileEvents prof,
+                     const SsdFuse &fuse, const int *cu, SsdProfileEvents prof,
                      cudaStream_t stream) {
     const size_t smem = simt_smem_bytes(N);
-    cudaError_t e = cudaFuncSetAttribute(ssd_scan_simt_kernel<T, kDtX>,
+    cudaError_t e = cudaFuncSetAttribute(ssd_scan_simt_kernel<T, kFuse>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid((P + kPB - 1) / kPB, H, batch);
     if (prof.before && prof.after && (e = ssd_record_event(prof.before, stream)) != cudaSuccess)
         return e;
-    ssd_scan_simt_kernel<T, kDtX><<<grid, kThreads, smem, stream>>>(
+    ssd_scan_simt_kernel<T, kFuse><<<grid, kThreads, smem, stream>>>(
         (const T *)x, dt, A, (const T *)B, (const T *)C, D, init, (T *)y, fin, L, H, P, N, G,
-        dtt, cu);
+        fuse, cu);
     e = cudaGetLastError();
     if (e == cudaSuccess && prof.before && prof.after) e = ssd_record_event(prof.after, stream);
     return e;
@@ -244,16 +248,16 @@ cudaError_t ssd_launch_scan_simt(const void *x, const float *dt, const float *A,
                                  const void *B, const void *C, const float *D,
                                  const float *init, void *y, float *fin, bool bf16,
                                  int batch, int L, int H, int P, int N, int G,
-                                 const SsdDt &dtt, const int *cu, SsdProfileEvents prof,
+                                 const SsdFuse &fuse, const int *cu, SsdProfileEvents prof,
                                  cudaStream_t stream) {
-    const bool dtx = ssd_dt_active(dtt);
+    const bool fused = ssd_fuse_active(fuse);
     if (bf16)
-        return dtx ? launch_t<__nv_bfloat16, true>(x, dt, A, B, C, D, init, y, fin, batch, L, H,
-                                                   P, N, G, dtt, cu, prof, stream)
+        return fused ? launch_t<__nv_bfloat16, true>(x, dt, A, B, C, D, init, y, fin, batch, L, H,
+                                                   P, N, G, fuse, cu, prof, stream)
                    : launch_t<__nv_bfloat16, false>(x, dt, A, B, C, D, init, y, fin, batch, L,
-                                                    H, P, N, G, dtt, cu, prof, stream);
-    return dtx ? launch_t<float, true>(x, dt, A, B, C, D, init, y, fin, batch, L, H, P, N, G,
-                                       dtt, cu, prof, stream)
+                                                    H, P, N, G, fuse, cu, prof, stream);
+    return fused ? launch_t<float, true>(x, dt, A, B, C, D, init, y, fin, batch, L, H, P, N, G,
+                                       fuse, cu, prof, stream)
                : launch_t<float, false>(x, dt, A, B, C, D, init, y, fin, batch, L, H, P, N, G,
-                                        dtt, cu, prof, stream);
+                                        fuse, cu, prof, stream);
 }

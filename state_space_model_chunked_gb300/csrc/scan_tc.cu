@@ -118,7 +118,7 @@ struct TcArgs {
     float *fin;
     unsigned int *err;
     int L, H, G, tiles, seg_tiles, nseg;
-    SsdDt dtt;             // transform of the raw step size
+    SsdFuse fuse;             // transform of the raw step size
     // packed sequences (cu != nullptr): tokens cu[s] .. cu[s+1]-1 of the
     // flattened token axis form sequence s; item0 / fslot0 [nseq + 1] are the
     // prefix sums of each sequence's segments and of its segments but the last
@@ -166,6 +166,19 @@ __device__ __forceinline__ SegWork seg_work(const TcArgs &a, int item, int z, bo
     w.sigma = item - pre[lo];
     w.fslot = a.fslot0[lo];
     return w;
+}
+
+// The step-size transform of a layer (bias, softplus, clamp) applied once to
+// every dt of the call, into the workspace, before the tensor-core kernels
+// read it.  Elementwise and HBM-bound: a round trip of 8 bytes per (token,
+// head), about 1% of a scan's traffic, where carrying the transform inside
+// the single warps that make the per-token factors put it on their critical
+// path (the segment kernel ran 45% slower).
+__global__ void __launch_bounds__(256)
+ssd_dt_prepass_kernel(const float *__restrict__ dt, float *__restrict__ out, size_t n, int H,
+                      const SsdFuse f) {
+    for (size_t i = (size_t)blockIdx.x * 256 + threadIdx.x; i < n; i += (size_t)gridDim.x * 256)
+        out[i] = ssd_dt<true>(f, dt[i], ssd_dt_bias<true>(f, (int)(i % (size_t)H)));
 }
 
 // Prefix tables of packed sequences for the kernels above: item0[s] = segments
@@ -297,12 +310,13 @@ struct ScanLayout {
     static constexpr uint32_t kBytes = kOffXt + HG * kXBytes;
 };
 
-template <int HG, bool kFacLow, bool kDtX, bool kPacked>
+template <int HG, bool kFacLow, bool kGate, bool kPacked>
 __global__ void __launch_bounds__(kThreads, 1)
 ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
                    const __grid_constant__ CUtensorMap mapB,
                    const __grid_constant__ CUtensorMap mapX,
-                   const __grid_constant__ CUtensorMap mapY, const TcArgs a) {
+                   const __grid_constant__ CUtensorMap mapY,
+                   const __grid_constant__ CUtensorMap mapZ, const TcArgs a) {
     extern __shared__ __align__(1024) uint8_t smem[];
     using Lay = ScanLayout<HG>;
     constexpr uint32_t kStage = Lay::kStage;
@@ -412,6 +426,13 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
                 for (int h = 0; h < HG; ++h)
                     tma_load_4d(stg + kCBytes + h * kXBytes, &mapX, bar(14 + stage), 0, h0 + h,
                                 trow + t0, tb);
+                if constexpr (kGate) {
+                    // the gate's z tile into L2: the epilogue reads it about two
+                    // tiles from now (rows past a packed sequence's end are
+                    // fetched but never read)
+#pragma unroll
+                    for (int h = 0; h < HG; ++h) tma_prefetch_l2_4d(&mapZ, 0, h0 + h, trow + t0, tb);
+                }
                 // B of this tile (single buffer: free once the previous tile's state
                 // update has read it)
                 if (it >= 1 && !wait_bar(bar(5), (it - 1) & 1, abort_flag, a.err)) break;
@@ -570,7 +591,7 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
             for (int h = 0; h < HG; ++h)
 #pragma unroll
                 for (int i = 0; i < 4; ++i)
-                    dn[h][i] = tok0 + i < w_len() ? ssd_dt<kDtX>(a.dtt, dn[h][i], h0 + h) : 0.f;
+                    dn[h][i] = tok0 + i < w_len() ? dn[h][i] : 0.f;
 #pragma unroll
             for (int h = 0; h < HG; ++h) {
                 float c[4];
@@ -757,7 +778,7 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
                             const int tok = tb + s;
                             const float d =
                                 tok < w_len()
-                                    ? ssd_dt<kDtX>(a.dtt, a.dt[(w_grow0() + tok) * a.H + h0 + hh], h0 + hh)
+                                    ? a.dt[(w_grow0() + tok) * a.H + h0 + hh]
                                     : 0.f;
                             return d > 0.f ? __expf(at[hh] - ah[s] + __logf(d)) : 0.f;
                         };
@@ -812,14 +833,28 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
             // ---- epilogue: y = Yd + exp(a_t) Yo + D x, staged as bf16 in this
             //      stage's C blocks (free once the tile's off-diagonal product is
             //      done; head h in block h) for issuer B's TMA stores
+            // (head, 32-column range) of this warpgroup: HG = 2 -> head wg & 1,
+            // columns 32 (wg >> 1) ..; HG = 1 -> head 0, columns 16 wg ..
+            const int hh = HG == 2 ? (wg & 1) : 0;
+            const int p0 = HG == 2 ? 32 * (wg >> 1) : 16 * wg;
+            constexpr int np = HG == 2 ? 32 : 16;
+            // the output gate's z for this thread's token and columns, loaded
+            // (from L2, where the producer prefetched it) before the wait for
+            // the tile's products; rows past the sequence's end read nothing
+            uint4 zv[np / 8];
+            bool gated = false;
+            if constexpr (kGate) {
+                if (a.fuse.z && t0 + row < w_len()) {
+                    gated = true;
+                    const __nv_bfloat16 *zrow = static_cast<const __nv_bfloat16 *>(a.fuse.z) +
+                                                ((w_grow0() + t0 + row) * a.H + h0 + hh) * kP + p0;
+#pragma unroll
+                    for (int q = 0; q < np / 8; ++q) zv[q] = *reinterpret_cast<const uint4 *>(zrow + 8 * q);
+                }
+            }
             wait_bar_warp(bar(10), it & 1, abort_flag, a.err);
             tc_fence_after();
             {
-                // (head, 32-column range) of this warpgroup: HG = 2 -> head wg & 1,
-                // columns 32 (wg >> 1) ..; HG = 1 -> head 0, columns 16 wg ..
-                const int hh = HG == 2 ? (wg & 1) : 0;
-                const int p0 = HG == 2 ? 32 * (wg >> 1) : 16 * wg;
-                const int np = HG == 2 ? 32 : 16;
                 // selects, not dynamic indexing (which would move the arrays to local memory)
                 const float e_at = (HG == 2 && hh == 1) ? e_at_t[HG - 1] : e_at_t[0];
                 const float dsk = (HG == 2 && hh == 1) ? Dh[HG - 1] : Dh[0];
@@ -848,7 +883,23 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
                             const uint64_t y01 = fma_f32x2(
                                 ea2, pack_f32x2(__uint_as_float(yo[i]), __uint_as_float(yo[i + 1])),
                                 pack_f32x2(__uint_as_float(yd[i]), __uint_as_float(yd[i + 1])));
-                            pk[4 * half + e] = pack_bf16x2_from_f32x2(fma_f32x2(dsk2, x01, y01));
+                            uint64_t v01 = fma_f32x2(dsk2, x01, y01);
+                            if constexpr (kGate) {
+                                if (gated) {
+                                    // silu(z) = h + h tanh(h), h = z / 2 (sigmoid(z) =
+                                    // (1 + tanh(z/2)) / 2): one hardware tanh per
+                                    // element; its 2^-11 error is below the bf16 output's
+                                    const uint4 zq = zv[c16 / 8 + half];
+                                    const uint32_t zw = e == 0 ? zq.x : e == 1 ? zq.y : e == 2 ? zq.z : zq.w;
+                                    const uint64_t h01 = mul_f32x2(
+                                        pack_f32x2(__uint_as_float(zw << 16), __uint_as_float(zw & 0xffff0000u)),
+                                        pack_f32x2(0.5f, 0.5f));
+                                    const uint64_t t01 = pack_f32x2(tanh_approx(__uint_as_float((uint32_t)h01)),
+                                                                    tanh_approx(__uint_as_float((uint32_t)(h01 >> 32))));
+                                    v01 = mul_f32x2(v01, fma_f32x2(h01, t01, h01));
+                                }
+                            }
+                            pk[4 * half + e] = pack_bf16x2_from_f32x2(v01);
                         }
                     }
                     if (!direct) {
@@ -904,7 +955,7 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
 // each X tile in place by its token weights, and warp 10 computes the weights
 // w_s = exp(decay from s to the segment end) dt_s of each tile into a ring
 // with one slot per stage.
-template <int HG, bool kDtX, bool kPacked>
+template <int HG, bool kPacked>
 __global__ void __launch_bounds__(kSegThreads, 1)
 ssd_tc_segment_kernel(const __grid_constant__ CUtensorMap mapB,
                       const __grid_constant__ CUtensorMap mapX, const TcArgs a) {
@@ -1043,7 +1094,7 @@ ssd_tc_segment_kernel(const __grid_constant__ CUtensorMap mapB,
                 for (int i = 0; i < 4; ++i) {
                     // the transform at use keeps the three tiles of loads in flight
                     const int tok = (k1 - 1 - it) * kTile + 4 * lane + i;
-                    d[h][i] = tok < w_len() ? ssd_dt<kDtX>(a.dtt, d0[h][i], h0 + h) : 0.f;
+                    d[h][i] = tok < w_len() ? d0[h][i] : 0.f;
                     d0[h][i] = d1[h][i];
                     d1[h][i] = d2[h][i];
                 }
@@ -1235,19 +1286,19 @@ static_assert(seg_smem<2>() <= 232448, "segment kernel shared memory exceeds 227
 static_assert(seg_smem<4>() <= 232448, "segment kernel shared memory exceeds 227 KB");
 
 // Segment contributions with SG heads per CTA.
-template <int SG, bool kDtX, bool kPacked>
+template <int SG, bool kPacked>
 cudaError_t launch_segment(const SsdTcPlan &plan, const CUtensorMap &mB, const CUtensorMap &mX,
                            const TcArgs &args, int batch, int H, cudaStream_t stream) {
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(attr_once, [] {
-        attr_err = cudaFuncSetAttribute(ssd_tc_segment_kernel<SG, kDtX, kPacked>,
+        attr_err = cudaFuncSetAttribute(ssd_tc_segment_kernel<SG, kPacked>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         (int)seg_smem<SG>());
     });
     if (attr_err != cudaSuccess) return attr_err;
     dim3 g1(H / SG, plan.varlen ? plan.nslots : plan.nseg - 1, plan.varlen ? 1 : batch);
-    ssd_tc_segment_kernel<SG, kDtX, kPacked><<<g1, kSegThreads, seg_smem<SG>(), stream>>>(mB, mX, args);
+    ssd_tc_segment_kernel<SG, kPacked><<<g1, kSegThreads, seg_smem<SG>(), stream>>>(mB, mX, args);
     return cudaGetLastError();
 }
 
@@ -1270,26 +1321,27 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
     return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
-template <int HG, bool kDtX, bool kPacked>
+template <int HG, bool kGate, bool kPacked>
 cudaError_t launch_hg(const SsdTcPlan &plan, const CUtensorMap &mC, const CUtensorMap &mB,
-                      const CUtensorMap &mX, const CUtensorMap &mY, const TcArgs &args,
-                      int batch, int H, SsdProfileEvents prof, cudaStream_t stream) {
+                      const CUtensorMap &mX, const CUtensorMap &mY, const CUtensorMap &mZ,
+                      const TcArgs &args, int batch, int H, SsdProfileEvents prof,
+                      cudaStream_t stream) {
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(attr_once, [] {
-        attr_err = cudaFuncSetAttribute(ssd_tc_scan_kernel<HG, false, kDtX, kPacked>,
+        attr_err = cudaFuncSetAttribute(ssd_tc_scan_kernel<HG, false, kGate, kPacked>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         (int)scan_smem<HG>());
         if (attr_err == cudaSuccess)
-            attr_err = cudaFuncSetAttribute(ssd_tc_scan_kernel<HG, true, kDtX, kPacked>,
+            attr_err = cudaFuncSetAttribute(ssd_tc_scan_kernel<HG, true, kGate, kPacked>,
                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
                                             (int)scan_smem<HG>());
     });
     if (attr_err != cudaSuccess) return attr_err;
     // factor warp on the light sub-partition for long segments, the producer
     // there for short ones (A/B timed on the 130M and 2.7B layers)
-    auto kernel = plan.seg_tiles >= kLongSegTiles ? ssd_tc_scan_kernel<HG, true, kDtX, kPacked>
-                                                  : ssd_tc_scan_kernel<HG, false, kDtX, kPacked>;
+    auto kernel = plan.seg_tiles >= kLongSegTiles ? ssd_tc_scan_kernel<HG, true, kGate, kPacked>
+                                                  : ssd_tc_scan_kernel<HG, false, kGate, kPacked>;
     if (plan.varlen) {
         ssd_varlen_plan_kernel<<<1, 1024, 0, stream>>>(
             args.cu, args.nseq, plan.seg_tiles, const_cast<int *>(args.item0),
@@ -1300,8 +1352,8 @@ cudaError_t launch_hg(const SsdTcPlan &plan, const CUtensorMap &mC, const CUtens
     const bool chained = plan.nslots > 0;
     if (chained) {
         cudaError_t e = plan.seg_heads == 4
-                            ? launch_segment<4, kDtX, kPacked>(plan, mB, mX, args, batch, H, stream)
-                            : launch_segment<HG, kDtX, kPacked>(plan, mB, mX, args, batch, H, stream);
+                            ? launch_segment<4, kPacked>(plan, mB, mX, args, batch, H, stream)
+                            : launch_segment<HG, kPacked>(plan, mB, mX, args, batch, H, stream);
         if (e != cudaSuccess) return e;
         const size_t total = (size_t)plan.nseqs * H * kP * kN / 4;
         e = launch_pdl(ssd_tc_segment_pass_kernel, dim3((unsigned)((total + 255) / 256)),
@@ -1317,9 +1369,10 @@ cudaError_t launch_hg(const SsdTcPlan &plan, const CUtensorMap &mC, const CUtens
     cudaError_t e;
     if (chained) {
         // overlaps the scan kernel's prologue and first tile with the chaining kernel
-        e = launch_pdl(kernel, g2, dim3(kThreads), scan_smem<HG>(), stream, mC, mB, mX, mY, args);
+        e = launch_pdl(kernel, g2, dim3(kThreads), scan_smem<HG>(), stream, mC, mB, mX, mY, mZ,
+                       args);
     } else {
-        kernel<<<g2, kThreads, scan_smem<HG>(), stream>>>(mC, mB, mX, mY, args);
+        kernel<<<g2, kThreads, scan_smem<HG>(), stream>>>(mC, mB, mX, mY, mZ, args);
         e = cudaGetLastError();
     }
     if (e == cudaSuccess && prof.before && prof.after) e = ssd_record_event(prof.after, stream);
@@ -1371,6 +1424,9 @@ SsdTcPlan ssd_tc_plan(int batch, int L, int H, int P, int N, int G, int num_sms)
         p.workspace = ((state + 255) / 256) * 256 + ((decay + 255) / 256) * 256;
         p.launches = 3;
     }
+    // room for the transformed step sizes (used only with a dt transform)
+    p.dt_offset = p.workspace;
+    p.workspace += (((size_t)batch * L * H * sizeof(float) + 255) / 256) * 256;
     return p;
 }
 
@@ -1450,6 +1506,8 @@ SsdTcPlan ssd_tc_plan_varlen(int nseq, const int *cu, int H, int P, int N, int G
     p.workspace = ((state + 255) / 256) * 256 + ((decay + 255) / 256) * 256 +
                   ((table + 255) / 256) * 256;
     p.launches = slots > 0 ? 4 : 2;
+    p.dt_offset = p.workspace;
+    p.workspace += (((size_t)cu[nseq] * H * sizeof(float) + 255) / 256) * 256;
     return p;
 }
 
@@ -1457,19 +1515,32 @@ cudaError_t ssd_launch_scan_tc(const SsdTcPlan &plan, const void *x, const float
                                const float *A, const void *B, const void *C, const float *D,
                                const float *init, void *y, float *fin, int batch, int L, int H,
                                int P, int N, int G, void *workspace, unsigned int *err,
-                               const SsdDt &dtt, SsdProfileEvents prof, cudaStream_t stream,
+                               const SsdFuse &fuse, SsdProfileEvents prof, cudaStream_t stream,
                                const int *cu_dev) {
     (void)P;
     (void)N;
     // packed sequences: one batch row of L = total tokens
     const int mrows = L, mbatch = plan.varlen ? 1 : batch;
-    CUtensorMap mC, mB, mX, mY;
+    CUtensorMap mC, mB, mX, mY, mZ;
     if (!make_map(&mC, C, kN, G, mrows, mbatch) || !make_map(&mB, B, kN, G, mrows, mbatch) ||
-        !make_map(&mX, x, kP, H, mrows, mbatch) || !make_map(&mY, y, kP, H, mrows, mbatch))
+        !make_map(&mX, x, kP, H, mrows, mbatch) || !make_map(&mY, y, kP, H, mrows, mbatch) ||
+        !make_map(&mZ, fuse.z ? fuse.z : x, kP, H, mrows, mbatch))
         return cudaErrorInvalidValue;
     TcArgs args{};
     args.dt = dt;
-    args.dtt = dtt;
+    if (ssd_dt_transform_active(fuse)) {
+        float *dt_eff = reinterpret_cast<float *>(static_cast<char *>(workspace) + plan.dt_offset);
+        const size_t n = (size_t)(plan.varlen ? 1 : batch) * L * H;
+        if (n > 0) {
+            const size_t want = (n + 255) / 256;
+            const unsigned grid = (unsigned)(want < 16u * 152u ? want : 16u * 152u);
+            ssd_dt_prepass_kernel<<<grid, 256, 0, stream>>>(dt, dt_eff, n, H, fuse);
+            const cudaError_t e = cudaGetLastError();
+            if (e != cudaSuccess) return e;
+        }
+        args.dt = dt_eff;
+    }
+    args.fuse = fuse;
     args.A = A;
     args.D = D;
     args.init = init;
@@ -1497,16 +1568,17 @@ cudaError_t ssd_launch_scan_tc(const SsdTcPlan &plan, const void *x, const float
     args.tiles = plan.tiles;
     args.seg_tiles = plan.seg_tiles;
     args.nseg = plan.nseg;
-    // one instantiation per (heads per CTA, dt transform, packed layout): the
-    // batched identity path carries neither the transform nor the packed
-    // bookkeeping (registers it cannot spare)
-    const bool dtx = ssd_dt_active(dtt);
-#define SSD_LAUNCH_HG(HG, X, PK) launch_hg<HG, X, PK>(plan, mC, mB, mX, mY, args, batch, H, prof, stream)
+    // one instantiation per (heads per CTA, output gate, packed layout): the
+    // plain batched path carries neither the gate nor the packed bookkeeping
+    // (registers it cannot spare)
+    const bool fused = fuse.z != nullptr;
+#define SSD_LAUNCH_HG(HG, X, PK) \
+    launch_hg<HG, X, PK>(plan, mC, mB, mX, mY, mZ, args, batch, H, prof, stream)
     if (plan.varlen) {
-        if (plan.heads_per_cta == 2) return dtx ? SSD_LAUNCH_HG(2, true, true) : SSD_LAUNCH_HG(2, false, true);
-        return dtx ? SSD_LAUNCH_HG(1, true, true) : SSD_LAUNCH_HG(1, false, true);
+        if (plan.heads_per_cta == 2) return fused ? SSD_LAUNCH_HG(2, true, true) : SSD_LAUNCH_HG(2, false, true);
+        return fused ? SSD_LAUNCH_HG(1, true, true) : SSD_LAUNCH_HG(1, false, true);
     }
-    if (plan.heads_per_cta == 2) return dtx ? SSD_LAUNCH_HG(2, true, false) : SSD_LAUNCH_HG(2, false, false);
-    return dtx ? SSD_LAUNCH_HG(1, true, false) : SSD_LAUNCH_HG(1, false, false);
+    if (plan.heads_per_cta == 2) return fused ? SSD_LAUNCH_HG(2, true, false) : SSD_LAUNCH_HG(2, false, false);
+    return fused ? SSD_LAUNCH_HG(1, true, false) : SSD_LAUNCH_HG(1, false, false);
 #undef SSD_LAUNCH_HG
 }

@@ -143,6 +143,13 @@ def varlen_inputs(lengths, nheads, headdim, dstate, ngroups, dtype="bf16", seed=
     return out
 
 
+def gate_input(shape, dtype="bf16", seed=0):
+    """The output gate's z ~ N(0, 1) in the workload's input dtype (float32
+    values, bf16-representable for bf16)."""
+    rng = np.random.Generator(np.random.PCG64([seed, 31337]))
+    return _normal(rng, tuple(shape), dtype)
+
+
 def decode_params(nheads, seed=0):
     """Per-head A and D for a decode layer stack (float32)."""
     rng = np.random.Generator(np.random.PCG64(seed + 7919))

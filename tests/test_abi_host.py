@@ -132,12 +132,12 @@ def _cu(vals):
 def _varlen(lib, cu_vals, **kw):
     keep, cu = _cu(cu_vals)
     a = dict(algo=0, x=_fake(0x1000), dt=_fake(0x2000), A=_fake(0x3000), B=_fake(0x4000),
-             C=_fake(0x5000), D=None, tr=None, dtype=1, nseq=len(cu_vals) - 1, cu=cu,
+             C=_fake(0x5000), D=None, tr=None, z=None, dtype=1, nseq=len(cu_vals) - 1, cu=cu,
              cu_dev=_fake(0x8000), H=4, P=64, N=64, G=1, Q=64, init=None, y=_fake(0x6000),
              fin=None, ws=None, wsb=0, stream=None)
     a.update(kw)
     return lib.ssd_scan_fwd_varlen(a["algo"], a["x"], a["dt"], a["A"], a["B"], a["C"], a["D"],
-                                   a["tr"], a["dtype"], a["nseq"], a["cu"], a["cu_dev"],
+                                   a["tr"], a["z"], a["dtype"], a["nseq"], a["cu"], a["cu_dev"],
                                    a["H"], a["P"], a["N"], a["G"], a["Q"], a["init"], a["y"],
                                    a["fin"], a["ws"], a["wsb"], a["stream"])
 
@@ -151,6 +151,7 @@ def _varlen(lib, cu_vals, **kw):
     ([0, 5], dict(cu_dev=_fake(0x8002))),  # int-misaligned device offsets
     ([0, 5], dict(x=None)),              # tokens present: token arrays required
     ([0, 5], dict(H=6, G=4)),
+    ([0, 5], dict(z=_fake(0x9008))),     # gate array 8-byte aligned only
 ])
 def test_varlen_rejects_bad_arguments(lib, cu_vals, kw):
     assert _varlen(lib, cu_vals, **kw) == INVALID

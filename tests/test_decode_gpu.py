@@ -134,3 +134,35 @@ def test_decode_dt_softplus_bias(units):
     assert rel(host(y), y_ref) <= 1e-2
     assert rel(host(s_dev), s_ref) <= 1e-6
 
+
+
+@pytest.mark.parametrize("units,dtype", [((3, 10), "bf16"), ((8, 160), "bf16"),
+                                         ((4, 6), "f32"), ((8, 160), "f32")])
+def test_decode_output_gate(units, dtype):
+    """y <- y * silu(z) in the kernel (classic and streaming launches), with
+    and without the dt transform, against the oracle step and gate; the state
+    is not touched by the gate."""
+    import state_space_model_chunked_gb300 as ssd
+    b, H = units
+    P, N, G = 64, 128, 2
+    state = gen.decode_state(b, H, P, N, seed=13)
+    A, D = gen.decode_params(H, seed=13)
+    tok = gen.decode_token_inputs(b, H, P, N, G, dtype, seed=13, step=0)
+    z = gen.gate_input((b, H, P), dtype, seed=13)
+    y_ref, s_ref = oracle.step(state, tok["x"], tok["dt"], A, tok["B"], tok["C"], D)
+    s_dev = dev(state)
+    y = ssd.state_update(s_dev, dev(tok["x"], dtype), dev(tok["dt"]), dev(A),
+                         dev(tok["B"], dtype), dev(tok["C"], dtype), dev(D), z=dev(z, dtype))
+    torch.cuda.synchronize()
+    assert rel(host(y), oracle.gate(y_ref, z)) <= TOL[dtype]
+    assert rel(host(s_dev), s_ref) <= 1e-6
+    # with the dt transform as well
+    raw = np.log(np.expm1(tok["dt"].astype(np.float64))).astype(np.float32)  # softplus^-1
+    s_dev = dev(state)
+    y = ssd.state_update(s_dev, dev(tok["x"], dtype), dev(raw), dev(A), dev(tok["B"], dtype),
+                         dev(tok["C"], dtype), dev(D), dt_softplus=True, z=dev(z, dtype))
+    torch.cuda.synchronize()
+    d = oracle.dt_transform(raw, None, True)
+    y_ref2, s_ref2 = oracle.step(state, tok["x"], d, A, tok["B"], tok["C"], D)
+    assert rel(host(y), oracle.gate(y_ref2, z)) <= TOL[dtype]
+    assert rel(host(s_dev), s_ref2) <= 1e-6

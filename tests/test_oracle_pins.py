@@ -321,3 +321,20 @@ def test_varlen_empty_sequence_without_init_is_zero_state():
     _, fin = oracle.scan_varlen(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"],
                                 inp["cu"], inp["D"])
     assert not fin[0].any() and fin[1].any()
+
+
+# ---------------------------------------------------------------- output gate
+def test_gate_closed_forms():
+    """silu(0) = 0; silu(1) = 1 / (1 + e^-1); silu(z) - silu(-z) = z (the
+    sigmoid's halves sum to one); silu(z) -> z for large z and -> 0 for very
+    negative z; the gate is y times that, per element."""
+    y = np.array([2.0, -3.0, 0.5, 1.0, 1.0])
+    z = np.array([0.0, 1.0, 40.0, -40.0, -800.0])
+    g = oracle.gate(y, z)
+    assert g[0] == 0.0
+    assert abs(g[1] - (-3.0) / (1.0 + np.exp(-1.0))) < 1e-15
+    assert abs(g[2] - 0.5 * 40.0) < 1e-12
+    assert abs(g[3]) < 1e-15 and g[4] == 0.0 and np.isfinite(g).all()
+    w = np.linspace(-6, 6, 97)
+    ones = np.ones_like(w)
+    assert np.allclose(oracle.gate(ones, w) - oracle.gate(ones, -w), w, rtol=0, atol=1e-14)

@@ -331,3 +331,51 @@ def test_varlen_one_sequence_matches_batched_call():
     packed["cu"] = np.array([0, 3000], np.int32)
     yv, fv = _varlen_on_gpu(packed, "bf16", TC)
     assert rel(yv, yb[0]) <= 1e-3 and rel(fv, fb) <= 1e-3
+
+
+# ---------------------------------------------------------------- output gate
+@pytest.mark.parametrize("b,L,H,G,algo,dtype", [
+    (1, 1000, 4, 1, TC, "bf16"),        # ragged last tile
+    (2, 640, 6, 3, TC, "bf16"),         # one head per CTA, batch 2
+    (1, 4096, 24, 1, AUTO, "bf16"),     # the 130M layer
+    (2, 300, 4, 2, SIMT, "f32"),
+    (1, 200, 3, 1, SIMT, "bf16"),
+])
+def test_output_gate_matches_oracle(b, L, H, G, algo, dtype):
+    inp = gen.scan_inputs(b, L, H, 64, 128, G, dtype, seed=L + H, random_init=True)
+    z = gen.gate_input((b, L, H, 64), dtype, seed=L)
+    y, f = scan_on_gpu(inp, dtype, 256, algo, z=dev(z, dtype))
+    yr, fr = scan_oracle(inp)
+    assert rel(y, oracle.gate(yr, z)) <= TOL[dtype], rel(y, oracle.gate(yr, z))
+    assert rel(f, fr) <= TOL[dtype]
+
+
+def test_output_gate_with_dt_transform_long():
+    """Gate and dt transform together on a sequence long enough to be split
+    into segments (chained states), 8 heads."""
+    inp = gen.scan_inputs(1, 20000, 8, 64, 128, 1, "bf16", seed=31, random_init=True)
+    rng = np.random.default_rng(31)
+    raw = rng.normal(-4.0, 1.0, size=inp["dt"].shape).astype(np.float32)
+    bias = rng.normal(0.0, 0.5, size=(8,)).astype(np.float32)
+    z = gen.gate_input(inp["x"].shape, "bf16", seed=31)
+    d = oracle.dt_transform(raw, bias, True, 1e-4, 0.1)
+    inp_raw = dict(inp, dt=raw)
+    y, f = scan_on_gpu(inp_raw, "bf16", 256, TC, dt_bias=bias, dt_softplus=True,
+                       dt_limit=(1e-4, 0.1), z=dev(z, "bf16"))
+    yr, fr = oracle.scan_seq(inp["x"], d, inp["A"], inp["B"], inp["C"], inp["D"], inp["init"])
+    assert rel(y, oracle.gate(yr, z)) <= 1e-2 and rel(f, fr) <= 1e-2
+
+
+@pytest.mark.parametrize("algo", [TC, SIMT])
+def test_varlen_output_gate(algo):
+    inp = gen.varlen_inputs([1, 300, 129, 2000], 4, 64, 128, 1, "bf16", seed=41,
+                            random_init=True)
+    z = gen.gate_input(inp["x"].shape, "bf16", seed=41)
+    y, f = _varlen_on_gpu(inp, "bf16", algo, z=dev(z, "bf16"))
+    yr, fr = oracle.scan_varlen(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], inp["cu"],
+                                inp["D"], inp["init"])
+    assert rel(y, oracle.gate(yr, z)) <= 1e-2 and rel(f, fr) <= 1e-2
+    cu = inp["cu"]
+    for s in range(len(cu) - 1):
+        a, b = cu[s], cu[s + 1]
+        assert rel(y[a:b], oracle.gate(yr[a:b], z[a:b])) <= 1e-2
