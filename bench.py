@@ -293,15 +293,18 @@ def time_scan_e2e(shape, steps, warmup, device):
     return dt, h2d, d2h
 
 
-def time_decode(batch, steps, device, peaks):
+def time_decode(batch, steps, device, peaks, state_dtype=None):
     """One ssd_state_update per token over the 64-layer 2.7B-shaped stack,
-    layers flattened into heads (one group per layer)."""
+    layers flattened into heads (one group per layer); the state in fp32, or
+    stored as bf16 with state_dtype=torch.bfloat16."""
     import torch
     import state_space_model_chunked_gb300 as ssd
     from state_space_model_chunked_gb300 import inputs as gen
     ds = gen.DECODE_SHAPE
     Hf, G, P, N = ds.layers * ds.nheads, ds.layers, ds.headdim, ds.dstate
     state = gen.device_decode_state(batch, Hf, P, N, seed=batch, device=device)
+    if state_dtype is not None and state_dtype != state.dtype:
+        state = state.to(state_dtype)
     A, D = gen.decode_params(Hf, seed=batch)
     A, D = torch.from_numpy(A).to(device), torch.from_numpy(D).to(device)
     ntok = 4
@@ -321,12 +324,14 @@ def time_decode(batch, steps, device, peaks):
     e1.record(stream)
     torch.cuda.synchronize(device)
     ms = e0.elapsed_time(e1) / steps
-    byts = (2 * batch * Hf * P * N * 4 + 2 * batch * Hf * P * 2 + batch * Hf * 4
-            + 2 * batch * G * N * 2 + 2 * Hf * 4)
+    byts = (2 * batch * Hf * P * N * state.element_size() + 2 * batch * Hf * P * 2
+            + batch * Hf * 4 + 2 * batch * G * N * 2 + 2 * Hf * 4)
     gbs = byts / (ms * 1e-3) / 1e9
+    sdt = str(state.dtype).replace("torch.", "")
     del state, toks
     torch.cuda.empty_cache()
-    return {"batch": batch, "steps": steps, "ms_per_step": ms, "bytes_per_step": byts,
+    return {"batch": batch, "state": sdt, "steps": steps, "ms_per_step": ms,
+            "bytes_per_step": byts,
             "GB_per_s": gbs, "frac_of_measured_hbm": gbs / peaks["hbm_gbs"],
             "frac_of_8TBs_nominal": gbs / 8000.0}
 
@@ -707,6 +712,8 @@ def run_gpu(args):
                 "tensor_tflops": lflops / (lms * 1e-3) / 1e12}
             torch.cuda.empty_cache()
             extra["decode"] = [time_decode(b, 128, device, peaks) for b in (1, 16, 64, 256)]
+            extra["decode_bf16_state"] = [time_decode(b, 128, device, peaks, torch.bfloat16)
+                                          for b in (1, 16, 64, 256)]
             extra["decode_per_layer"] = [time_decode_per_layer(b, 32, device, peaks)
                                          for b in (1, 16)]
             extra["decode_vs_recompute"] = time_decode_vs_recompute(device)

@@ -279,14 +279,24 @@ ssd_status ssd_state_update_dt(float *state, const void *x, const float *dt,
                                int headdim, int dstate, int ngroups, void *y,
                                cudaStream_t stream);
 
-/* ssd_state_update_dt with the output gate of ssd_scan_fwd_fused: z is
- * in_dtype [batch][nheads][headdim] (y's layout), 16-byte aligned, or NULL. */
-ssd_status ssd_state_update_fused(float *state, const void *x, const float *dt,
-                                  const float *A, const void *B, const void *C,
-                                  const float *D, const ssd_dt_transform *dt_transform,
-                                  const void *z, ssd_dtype in_dtype, int batch,
-                                  int nheads, int headdim, int dstate, int ngroups,
-                                  void *y, cudaStream_t stream);
+/* ssd_state_update_dt with the output gate of ssd_scan_fwd_fused and a
+ * choice of state storage.
+ *   state        [batch][nheads][headdim][dstate] of state_dtype, in place.
+ *                SSD_BF16 stores the state as bfloat16 (half the bytes of
+ *                the HBM-bound update): each step reads it, updates it in
+ *                fp32 and writes it rounded to nearest even; y is computed
+ *                from the fp32 update before that rounding.  The pages name
+ *                reduced precision as future work (CGLA sections IV and VI)
+ *                without fixing a format; this is the plainest one.  bf16
+ *                states need in_dtype SSD_BF16 (else SSD_ERR_UNSUPPORTED).
+ *   z            in_dtype [batch][nheads][headdim] (y's layout), 16-byte
+ *                aligned, or NULL: the output gate y <- y * silu(z). */
+ssd_status ssd_state_update_fused(void *state, ssd_dtype state_dtype, const void *x,
+                                  const float *dt, const float *A, const void *B,
+                                  const void *C, const float *D,
+                                  const ssd_dt_transform *dt_transform, const void *z,
+                                  ssd_dtype in_dtype, int batch, int nheads, int headdim,
+                                  int dstate, int ngroups, void *y, cudaStream_t stream);
 
 /* Human-readable name of a status code (static storage). */
 const char *ssd_status_string(ssd_status s);

@@ -183,6 +183,23 @@ def dt_transform(dt, bias=None, softplus=False, lo=-np.inf, hi=np.inf):
     return np.minimum(np.maximum(u, lo), hi)
 
 
+def round_bf16(a):
+    """Each value rounded to the nearest bfloat16 (8 significant bits), ties
+    to even, returned as float64: the significand from frexp scaled to 8 bits
+    and rounded half-to-even.  Finite normal values only."""
+    m, e = np.frexp(np.asarray(a, dtype=np.float64))
+    return np.ldexp(np.rint(m * 256.0) / 256.0, e)
+
+
+def step_bf16_state(state, x, dt, A, B, C, D=None, nthreads=None):
+    """One decode token with the state stored in bfloat16: the fp64 step on
+    the stored (bf16) state, y from the updated state before rounding, and
+    the new state rounded to bf16.  The pages leave the reduced-precision
+    format open (CGLA sections IV and VI); this is the plainest one."""
+    y, st = step(state, x, dt, A, B, C, D, nthreads)
+    return y, round_bf16(st)
+
+
 def gate(y, z):
     """The output gate in fp64: y * silu(z), silu(z) = z * sigmoid(z), with
     sigmoid(z) = exp(-log(1 + e^-z)) (logaddexp, so no overflow).  The pages

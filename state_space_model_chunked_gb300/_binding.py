@@ -95,7 +95,7 @@ def load():
         lib.ssd_state_update_dt.restype = _int
         lib.ssd_state_update_dt.argtypes = [_vp] * 8 + [_int] * 6 + [_vp, _vp]
         lib.ssd_state_update_fused.restype = _int
-        lib.ssd_state_update_fused.argtypes = [_vp] * 9 + [_int] * 6 + [_vp, _vp]
+        lib.ssd_state_update_fused.argtypes = [_vp, _int] + [_vp] * 8 + [_int] * 6 + [_vp, _vp]
         lib.ssd_scan_fwd_static.restype = _int
         lib.ssd_scan_fwd_static.argtypes = [_vp] * 6 + [_int] * 8 + [_vp, _vp, _vp, _vp]
         lib.ssd_scan_profile_events.restype = _int
@@ -445,12 +445,15 @@ class HostScanPipeline:
 
 def state_update(state, x, dt, A, B, C, D=None, *, y=None, dt_bias=None, dt_softplus=False,
                  dt_limit=None, z=None):
-    """One decode token.  state [b,H,P,N] f32 (updated in place), x [b,H,P],
-    dt [b,H] f32, A [H] f32, B/C [b,G,N] (x's dtype), D [H] f32 or None;
-    dt_bias / dt_softplus / dt_limit and the gate z [b,H,P] as in scan_fwd.
-    Returns y [b,H,P] in x's dtype."""
+    """One decode token.  state [b,H,P,N] f32 or bf16 (updated in place; a
+    bf16 state needs bf16 inputs and is rounded to nearest even after each
+    fp32 update), x [b,H,P], dt [b,H] f32, A [H] f32, B/C [b,G,N] (x's dtype),
+    D [H] f32 or None; dt_bias / dt_softplus / dt_limit and the gate
+    z [b,H,P] as in scan_fwd.  Returns y [b,H,P] in x's dtype."""
     lib = load()
-    _need(state, "state", torch.float32)
+    _need(state, "state")
+    if state.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError(f"state must be float32 or bfloat16, got {state.dtype}")
     dev = state.device
     b, H, P, N = state.shape
     _need(x, "x", None, dev, (b, H, P))
@@ -472,9 +475,9 @@ def state_update(state, x, dt, A, B, C, D=None, *, y=None, dt_bias=None, dt_soft
     with torch.cuda.device(dev):
         stream = torch.cuda.current_stream(dev).cuda_stream
         tptr, _keep = _dt_transform(dt_bias, dt_softplus, dt_limit, H, dev)
-        rc = lib.ssd_state_update_fused(_ptr(state), _ptr(x), _ptr(dt), _ptr(A), _ptr(B),
-                                        _ptr(C), _ptr(D), tptr, _ptr(z), code, b, H, P, N, G,
-                                        _ptr(y), ctypes.c_void_p(stream))
+        rc = lib.ssd_state_update_fused(_ptr(state), _dtype_code(state), _ptr(x), _ptr(dt),
+                                        _ptr(A), _ptr(B), _ptr(C), _ptr(D), tptr, _ptr(z), code,
+                                        b, H, P, N, G, _ptr(y), ctypes.c_void_p(stream))
     _check("ssd_state_update", rc)
     return y
 

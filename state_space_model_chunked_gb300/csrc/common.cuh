@@ -105,6 +105,40 @@ __device__ __forceinline__ float ssd_gate(const SsdFuse &f, float y, size_t i) {
     }
 }
 
+// Four consecutive state elements stored as float or as bfloat16 (rounded to
+// nearest even); the arithmetic is fp32 either way.
+__device__ __forceinline__ void ssd_st4(float *p, float4 v) { *reinterpret_cast<float4 *>(p) = v; }
+__device__ __forceinline__ void ssd_st4(__nv_bfloat16 *p, float4 v) {
+    const __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
+    uint2 u;
+    u.x = *reinterpret_cast<const uint32_t *>(&lo);
+    u.y = *reinterpret_cast<const uint32_t *>(&hi);
+    *reinterpret_cast<uint2 *>(p) = u;
+}
+// Streaming (evict-first) forms for state touched once per call.
+__device__ __forceinline__ float4 ssd_ld4_cs(const float *p) {
+    return __ldcs(reinterpret_cast<const float4 *>(p));
+}
+__device__ __forceinline__ float4 ssd_ld4_cs(const __nv_bfloat16 *p) {
+    const uint2 u = __ldcs(reinterpret_cast<const uint2 *>(p));
+    float4 r;
+    r.x = __uint_as_float(u.x << 16);
+    r.y = __uint_as_float(u.x & 0xffff0000u);
+    r.z = __uint_as_float(u.y << 16);
+    r.w = __uint_as_float(u.y & 0xffff0000u);
+    return r;
+}
+__device__ __forceinline__ void ssd_st4_cs(float *p, float4 v) {
+    __stcs(reinterpret_cast<float4 *>(p), v);
+}
+__device__ __forceinline__ void ssd_st4_cs(__nv_bfloat16 *p, float4 v) {
+    const __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
+    uint2 u;
+    u.x = *reinterpret_cast<const uint32_t *>(&lo);
+    u.y = *reinterpret_cast<const uint32_t *>(&hi);
+    __stcs(reinterpret_cast<uint2 *>(p), u);
+}
+
 // Four consecutive elements starting at a 4-element-aligned index.
 __device__ __forceinline__ float4 ssd_ld4(const float *p) {
     return *reinterpret_cast<const float4 *>(p);

@@ -24,9 +24,9 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kBatchRows = 8;   // rows each thread has in flight at once
 
-template <typename T, int VPT, bool kFuse>
+template <typename T, typename S, int VPT, bool kFuse>
 __global__ void __launch_bounds__(kThreads)
-ssd_decode_kernel(float *__restrict__ state, const T *__restrict__ x,
+ssd_decode_kernel(S *__restrict__ state, const T *__restrict__ x,
                   const float *__restrict__ dt, const float *__restrict__ A,
                   const T *__restrict__ Bm, const T *__restrict__ Cm,
                   const float *__restrict__ D, T *__restrict__ y, int H, int P,
@@ -52,7 +52,7 @@ ssd_decode_kernel(float *__restrict__ state, const T *__restrict__ x,
         Bv[v] = ssd_ld4(Bg + n0);
         Cv[v] = ssd_ld4(Cg + n0);
     }
-    float *st = state + (size_t)bh * P * N;
+    S *st = state + (size_t)bh * P * N;
     const T *xr = x + (size_t)bh * P;
     T *yr = y + (size_t)bh * P;
 
@@ -69,8 +69,7 @@ ssd_decode_kernel(float *__restrict__ state, const T *__restrict__ x,
                 xv[i] = ssd_ld(xr + p);
 #pragma unroll
                 for (int v = 0; v < VPT; ++v)
-                    s[i][v] = __ldcs(reinterpret_cast<const float4 *>(
-                        st + (size_t)p * N + 4 * (lane_n + v * tpr)));
+                    s[i][v] = ssd_ld4_cs(st + (size_t)p * N + 4 * (lane_n + v * tpr));
             }
         }
 #pragma unroll
@@ -86,9 +85,7 @@ ssd_decode_kernel(float *__restrict__ state, const T *__restrict__ x,
                     q.y = fmaf(decay, q.y, dx * Bv[v].y);
                     q.z = fmaf(decay, q.z, dx * Bv[v].z);
                     q.w = fmaf(decay, q.w, dx * Bv[v].w);
-                    __stcs(reinterpret_cast<float4 *>(st + (size_t)p * N +
-                                                      4 * (lane_n + v * tpr)),
-                           q);
+                    ssd_st4_cs(st + (size_t)p * N + 4 * (lane_n + v * tpr), q);
                     acc = fmaf(Cv[v].x, q.x, acc);
                     acc = fmaf(Cv[v].y, q.y, acc);
                     acc = fmaf(Cv[v].z, q.z, acc);
@@ -120,9 +117,9 @@ struct StreamLayout {
     uint32_t state_bytes, x_bytes, bc_bytes, stage_bytes;
 };
 
-__host__ __device__ inline StreamLayout stream_layout(int P, int N, int es) {
+__host__ __device__ inline StreamLayout stream_layout(int P, int N, int es, int ss) {
     StreamLayout l;
-    l.state_bytes = (uint32_t)P * N * 4u;
+    l.state_bytes = (uint32_t)P * N * (uint32_t)ss;
     l.x_bytes = (uint32_t)P * es;
     l.bc_bytes = (uint32_t)N * es;
     const uint32_t raw = l.state_bytes + l.x_bytes + 2 * l.bc_bytes;
@@ -130,16 +127,16 @@ __host__ __device__ inline StreamLayout stream_layout(int P, int N, int es) {
     return l;
 }
 
-template <typename T, int VPT, bool kFuse>
+template <typename T, typename S, int VPT, bool kFuse>
 __global__ void __launch_bounds__(kStreamThreads + 32, 1)
-ssd_decode_stream_kernel(float *__restrict__ state, const T *__restrict__ x,
+ssd_decode_stream_kernel(S *__restrict__ state, const T *__restrict__ x,
                          const float *__restrict__ dt, const float *__restrict__ A,
                          const T *__restrict__ Bm, const T *__restrict__ Cm,
                          const float *__restrict__ D, T *__restrict__ y, int batch, int H, int P,
                          int N, int G, int stages, unsigned int *err, const SsdFuse fuse) {
     using namespace ssdptx;
     extern __shared__ __align__(1024) uint8_t smem[];
-    const StreamLayout L = stream_layout(P, N, (int)sizeof(T));
+    const StreamLayout L = stream_layout(P, N, (int)sizeof(T), (int)sizeof(S));
     const long units = (long)batch * H;
     const int tid = threadIdx.x;
     // barriers: full[stages] (bulk loads landed), done[stages] (update finished)
@@ -221,7 +218,7 @@ ssd_decode_stream_kernel(float *__restrict__ state, const T *__restrict__ x,
                 break;
             }
             uint8_t *stage = smem + (size_t)st * L.stage_bytes;
-            float *sm = reinterpret_cast<float *>(stage);
+            S *sm = reinterpret_cast<S *>(stage);
             const T *xs = reinterpret_cast<const T *>(stage + L.state_bytes);
             const T *Bs = reinterpret_cast<const T *>(stage + L.state_bytes + L.x_bytes);
             const T *Cs = reinterpret_cast<const T *>(stage + L.state_bytes + L.x_bytes + L.bc_bytes);
@@ -247,8 +244,7 @@ ssd_decode_stream_kernel(float *__restrict__ state, const T *__restrict__ x,
                         xv[i] = ssd_ld(xs + p);
 #pragma unroll
                         for (int v = 0; v < VPT; ++v)
-                            q[i][v] = *reinterpret_cast<const float4 *>(
-                                sm + (size_t)p * N + 4 * (lane_n + v * tpr));
+                            q[i][v] = ssd_ld4(sm + (size_t)p * N + 4 * (lane_n + v * tpr));
                     }
                 }
 #pragma unroll
@@ -264,7 +260,7 @@ ssd_decode_stream_kernel(float *__restrict__ state, const T *__restrict__ x,
                             w.y = fmaf(decay, w.y, dx * Bv[v].y);
                             w.z = fmaf(decay, w.z, dx * Bv[v].z);
                             w.w = fmaf(decay, w.w, dx * Bv[v].w);
-                            *reinterpret_cast<float4 *>(sm + (size_t)p * N + 4 * (lane_n + v * tpr)) = w;
+                            ssd_st4(sm + (size_t)p * N + 4 * (lane_n + v * tpr), w);
                             acc[i] = fmaf(Cv[v].x, w.x, acc[i]);
                             acc[i] = fmaf(Cv[v].y, w.y, acc[i]);
                             acc[i] = fmaf(Cv[v].z, w.z, acc[i]);
@@ -294,32 +290,32 @@ ssd_decode_stream_kernel(float *__restrict__ state, const T *__restrict__ x,
     __syncthreads();
 }
 
-template <typename T, bool kFuse>
-cudaError_t launch_t(float *state, const void *x, const float *dt, const float *A,
+template <typename T, typename S, bool kFuse>
+cudaError_t launch_t(S *state, const void *x, const float *dt, const float *A,
                      const void *B, const void *C, const float *D, void *y, int batch,
                      int H, int P, int N, int G, int num_sms, unsigned int *err,
                      const SsdFuse &fuse, cudaStream_t stream) {
     const size_t units = (size_t)batch * H;
-    const StreamLayout lay = stream_layout(P, N, (int)sizeof(T));
+    const StreamLayout lay = stream_layout(P, N, (int)sizeof(T), (int)sizeof(S));
     const int stages = (int)std::min<size_t>(8, kStreamRing / lay.stage_bytes);
     // the streaming ring pays off once every SM has several states to walk;
-    // its bulk copies need 16-byte multiples for the x, B and C rows
+    // its bulk copies need 16-byte multiples for the state, x, B and C rows
     if (num_sms > 0 && stages >= 3 && units >= (size_t)num_sms * 4 && lay.x_bytes % 16 == 0 &&
-        lay.bc_bytes % 16 == 0) {
+        lay.bc_bytes % 16 == 0 && lay.state_bytes % 16 == 0) {
         const size_t smem = (size_t)stages * lay.stage_bytes + 16 * stages + 16;
         cudaError_t e;
         if (N <= 128) {
-            e = cudaFuncSetAttribute(ssd_decode_stream_kernel<T, 1, kFuse>,
+            e = cudaFuncSetAttribute(ssd_decode_stream_kernel<T, S, 1, kFuse>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
             if (e != cudaSuccess) return e;
-            ssd_decode_stream_kernel<T, 1, kFuse><<<num_sms, kStreamThreads + 32, smem, stream>>>(
+            ssd_decode_stream_kernel<T, S, 1, kFuse><<<num_sms, kStreamThreads + 32, smem, stream>>>(
                 state, (const T *)x, dt, A, (const T *)B, (const T *)C, D, (T *)y, batch, H, P,
                 N, G, stages, err, fuse);
         } else {
-            e = cudaFuncSetAttribute(ssd_decode_stream_kernel<T, 2, kFuse>,
+            e = cudaFuncSetAttribute(ssd_decode_stream_kernel<T, S, 2, kFuse>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
             if (e != cudaSuccess) return e;
-            ssd_decode_stream_kernel<T, 2, kFuse><<<num_sms, kStreamThreads + 32, smem, stream>>>(
+            ssd_decode_stream_kernel<T, S, 2, kFuse><<<num_sms, kStreamThreads + 32, smem, stream>>>(
                 state, (const T *)x, dt, A, (const T *)B, (const T *)C, D, (T *)y, batch, H, P,
                 N, G, stages, err, fuse);
         }
@@ -327,10 +323,10 @@ cudaError_t launch_t(float *state, const void *x, const float *dt, const float *
     }
     const unsigned grid = (unsigned)units;
     if (N <= 128) {
-        ssd_decode_kernel<T, 1, kFuse><<<grid, kThreads, 0, stream>>>(
+        ssd_decode_kernel<T, S, 1, kFuse><<<grid, kThreads, 0, stream>>>(
             state, (const T *)x, dt, A, (const T *)B, (const T *)C, D, (T *)y, H, P, N, G, fuse);
     } else {
-        ssd_decode_kernel<T, 2, kFuse><<<grid, kThreads, 0, stream>>>(
+        ssd_decode_kernel<T, S, 2, kFuse><<<grid, kThreads, 0, stream>>>(
             state, (const T *)x, dt, A, (const T *)B, (const T *)C, D, (T *)y, H, P, N, G, fuse);
     }
     return cudaGetLastError();
@@ -338,19 +334,28 @@ cudaError_t launch_t(float *state, const void *x, const float *dt, const float *
 
 }  // namespace
 
-cudaError_t ssd_launch_decode(float *state, const void *x, const float *dt,
+cudaError_t ssd_launch_decode(void *state, bool bf16_state, const void *x, const float *dt,
                               const float *A, const void *B, const void *C,
                               const float *D, void *y, bool bf16, int batch,
                               int H, int P, int N, int G, int num_sms, unsigned int *err,
                               const SsdFuse &fuse, cudaStream_t stream) {
     const bool fused = ssd_fuse_active(fuse);
+    using bf = __nv_bfloat16;
+    if (bf16_state) {   // bf16 inputs only (checked by the caller)
+        bf *st = static_cast<bf *>(state);
+        return fused ? launch_t<bf, bf, true>(st, x, dt, A, B, C, D, y, batch, H, P, N, G,
+                                              num_sms, err, fuse, stream)
+                     : launch_t<bf, bf, false>(st, x, dt, A, B, C, D, y, batch, H, P, N, G,
+                                               num_sms, err, fuse, stream);
+    }
+    float *st = static_cast<float *>(state);
     if (bf16)
-        return fused ? launch_t<__nv_bfloat16, true>(state, x, dt, A, B, C, D, y, batch, H, P, N,
-                                                   G, num_sms, err, fuse, stream)
-                   : launch_t<__nv_bfloat16, false>(state, x, dt, A, B, C, D, y, batch, H, P, N,
-                                                    G, num_sms, err, fuse, stream);
-    return fused ? launch_t<float, true>(state, x, dt, A, B, C, D, y, batch, H, P, N, G, num_sms,
-                                       err, fuse, stream)
-               : launch_t<float, false>(state, x, dt, A, B, C, D, y, batch, H, P, N, G, num_sms,
-                                        err, fuse, stream);
+        return fused ? launch_t<bf, float, true>(st, x, dt, A, B, C, D, y, batch, H, P, N, G,
+                                                 num_sms, err, fuse, stream)
+                     : launch_t<bf, float, false>(st, x, dt, A, B, C, D, y, batch, H, P, N, G,
+                                                  num_sms, err, fuse, stream);
+    return fused ? launch_t<float, float, true>(st, x, dt, A, B, C, D, y, batch, H, P, N, G,
+                                                num_sms, err, fuse, stream)
+                 : launch_t<float, float, false>(st, x, dt, A, B, C, D, y, batch, H, P, N, G,
+                                                 num_sms, err, fuse, stream);
 }

@@ -7,7 +7,7 @@
 
 #include "common.cuh"
 
-cudaError_t ssd_launch_decode(float *state, const void *x, const float *dt,
+cudaError_t ssd_launch_decode(void *state, bool bf16_state, const void *x, const float *dt,
                               const float *A, const void *B, const void *C,
                               const float *D, void *y, bool bf16, int batch,
                               int H, int P, int N, int G, int num_sms, unsigned int *err,

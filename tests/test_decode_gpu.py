@@ -166,3 +166,44 @@ def test_decode_output_gate(units, dtype):
     y_ref2, s_ref2 = oracle.step(state, tok["x"], d, A, tok["B"], tok["C"], D)
     assert rel(host(y), oracle.gate(y_ref2, z)) <= TOL[dtype]
     assert rel(host(s_dev), s_ref2) <= 1e-6
+
+
+@pytest.mark.parametrize("units,steps", [((3, 10), 1), ((8, 160), 1), ((2, 12), 16),
+                                         ((8, 160), 8)])
+def test_decode_bf16_state(units, steps):
+    """State stored as bfloat16 (classic and streaming launches): fp32 update,
+    y from it, the state rounded to nearest even; against the oracle's
+    bf16-state step chained over `steps` tokens.  One step must reproduce the
+    oracle's rounded state exactly except for rare last-bit ties decided from
+    fp32 instead of fp64 values."""
+    import state_space_model_chunked_gb300 as ssd
+    b, H = units
+    P, N, G = 64, 128, 2
+    st0 = gen.bf16_round(gen.decode_state(b, H, P, N, seed=17))[0]
+    A, D = gen.decode_params(H, seed=17)
+    s_dev = dev(st0, "bf16")
+    s_ref = st0.astype(np.float64)
+    for k in range(steps):
+        tok = gen.decode_token_inputs(b, H, P, N, G, "bf16", seed=17, step=k)
+        y = ssd.state_update(s_dev, dev(tok["x"], "bf16"), dev(tok["dt"]), dev(A),
+                             dev(tok["B"], "bf16"), dev(tok["C"], "bf16"), dev(D))
+        torch.cuda.synchronize()
+        y_ref, s_ref = oracle.step_bf16_state(s_ref, tok["x"], tok["dt"], A, tok["B"], tok["C"],
+                                              D)
+        assert rel(host(y), y_ref) <= 1e-2, (k, rel(host(y), y_ref))
+    s = host(s_dev)
+    assert s_dev.dtype == torch.bfloat16
+    assert rel(s, s_ref) <= 1e-2, rel(s, s_ref)
+    if steps == 1:
+        assert np.mean(s == s_ref) >= 0.99
+
+
+def test_decode_bf16_state_needs_bf16_inputs():
+    import state_space_model_chunked_gb300 as ssd
+    b, H, P, N, G = 1, 2, 16, 16, 1
+    s_dev = torch.zeros((b, H, P, N), dtype=torch.bfloat16, device="cuda")
+    x = torch.zeros((b, H, P), device="cuda")
+    with pytest.raises(ssd.SsdError):
+        ssd.state_update(s_dev, x, torch.ones((b, H), device="cuda"),
+                         torch.zeros(H, device="cuda"), torch.zeros((b, G, N), device="cuda"),
+                         torch.zeros((b, G, N), device="cuda"))

@@ -338,3 +338,35 @@ def test_gate_closed_forms():
     w = np.linspace(-6, 6, 97)
     ones = np.ones_like(w)
     assert np.allclose(oracle.gate(ones, w) - oracle.gate(ones, -w), w, rtol=0, atol=1e-14)
+
+
+# ---------------------------------------------------------------- bf16 states
+def test_round_bf16_nearest_even():
+    """bf16 keeps 8 significant bits: at 1 the spacing is 2^-7, ties go to the
+    even significand, exactly representable values stay, signs are symmetric,
+    and the rounding agrees with the bit-level encoder of the input module."""
+    u = 2.0 ** -7
+    vals = np.array([1.0, 1 + u / 2, 1 + 1.5 * u, 1 + u / 2 + 2.0 ** -20, -(1 + 1.5 * u), 3.0,
+                     0.1])
+    want = np.array([1.0, 1.0, 1 + 2 * u, 1 + u, -(1 + 2 * u), 3.0, 0.10009765625])
+    np.testing.assert_array_equal(oracle.round_bf16(vals), want)
+    r = np.random.default_rng(4).standard_normal(10000).astype(np.float32)
+    np.testing.assert_array_equal(oracle.round_bf16(r), gen.bf16_round(r)[0].astype(np.float64))
+
+
+def test_step_bf16_state_is_rounded_step():
+    """The bf16-state step: y from the unrounded fp64 update, the state that
+    update rounded; with A = 0, dt = 1 and x = 0 the state is unchanged and
+    already bf16, so rounding is the identity."""
+    b, H, P, N, G = 2, 3, 4, 8, 1
+    st = gen.bf16_round(gen.decode_state(b, H, P, N, seed=2))[0]
+    tok = gen.decode_token_inputs(b, H, P, N, G, "bf16", seed=2)
+    A = np.full(H, -0.5, np.float32)
+    y, s = oracle.step_bf16_state(st, tok["x"], tok["dt"], A, tok["B"], tok["C"])
+    y0, s0 = oracle.step(st, tok["x"], tok["dt"], A, tok["B"], tok["C"])
+    np.testing.assert_array_equal(y, y0)
+    np.testing.assert_array_equal(s, oracle.round_bf16(s0))
+    assert np.abs(s - s0).max() <= np.abs(s0).max() * 2.0 ** -8
+    y1, s1 = oracle.step_bf16_state(st, np.zeros_like(tok["x"]), np.ones_like(tok["dt"]),
+                                    np.zeros(H, np.float32), tok["B"], tok["C"])
+    np.testing.assert_array_equal(s1, st.astype(np.float64))
