@@ -652,7 +652,8 @@ def run_only(args):
     ssd_build.build()
     peaks = load_peaks()
     if args.only == "decode":
-        r = time_decode(args.decode_batch, args.steps, device, peaks)
+        r = time_decode(args.decode_batch, args.steps, device, peaks,
+                        torch.bfloat16 if args.decode_state == "bf16" else None)
     else:
         props = torch.cuda.get_device_properties(device)
         l2 = getattr(props, "L2_cache_size", 126 * 1024 * 1024) or 126 * 1024 * 1024
@@ -781,6 +782,8 @@ def main():
     ap.add_argument("--only", choices=["decode", "long"], default=None,
                     help="run one secondary workload alone (for profiler captures)")
     ap.add_argument("--decode-batch", type=int, default=16)
+    ap.add_argument("--decode-state", choices=["f32", "bf16"], default="f32",
+                    help="state storage of the --only decode run")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     args = ap.parse_args()

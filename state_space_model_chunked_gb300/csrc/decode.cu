@@ -197,18 +197,36 @@ ssd_decode_stream_kernel(S *__restrict__ state, const T *__restrict__ x,
         }
     } else {
         // ---- compute warps
+        // tpr (threads per row) and N are powers of two: rows and offsets by
+        // shifts; a thread's rows advance by kStreamThreads / tpr per step
         const int tpr = N / (4 * VPT);
-        const int lane_n = tid % tpr;
+        const int tsh = __ffs(tpr) - 1, nsh = __ffs(N) - 1;
+        const int lane_n = tid & (tpr - 1);
         const int total = P * tpr;
-        float dt_next = nk > 0 ? dt[unit_of(0)] : 0.f;   // raw; transformed at use
+        const int row0 = tid >> tsh, row_step = kStreamThreads >> tsh;
+        // the next unit's dt, A and D are loaded one unit ahead, so no global
+        // load latency sits between two units' updates (dt raw; transformed at use)
+        float dt_next = 0.f, A_next = 0.f, D_next = 0.f;
+        if (nk > 0) {
+            const int h0 = (int)(unit_of(0) % H);
+            dt_next = dt[unit_of(0)];
+            A_next = A[h0];
+            D_next = D ? D[h0] : 0.0f;
+        }
         for (long k = 0; k < nk; ++k) {
             const int st = (int)(k % stages);
             const long u = unit_of(k);
             const int h = (int)(u % H);
             const float dtv = ssd_dt<kFuse>(fuse, dt_next, ssd_dt_bias<kFuse>(fuse, h));
-            if (k + 1 < nk) dt_next = dt[unit_of(k + 1)];
-            const float decay = expf(dtv * A[h]);
-            const float Dh = D ? D[h] : 0.0f;
+            const float Ah = A_next, Dh = D_next;
+            if (k + 1 < nk) {
+                const long un = unit_of(k + 1);
+                const int hn = (int)(un % H);
+                dt_next = dt[un];
+                A_next = A[hn];
+                D_next = D ? D[hn] : 0.0f;
+            }
+            const float decay = expf(dtv * Ah);
             bool ok = !*abort_flag &&
                       mbar_wait(smem_u32(full + st), (uint32_t)((k / stages) & 1), kStreamWaitNs);
             ok = __all_sync(0xffffffffu, ok);
@@ -232,26 +250,25 @@ ssd_decode_stream_kernel(S *__restrict__ state, const T *__restrict__ x,
             // kStreamRows independent rows per thread per pass: all shared-memory
             // reads first, then the updates, then the interleaved row reductions
             for (int e0 = 0; e0 < total; e0 += kStreamThreads * kStreamRows) {
+                const int pbase = (e0 >> tsh) + row0;   // row of this thread's i = 0
                 float4 q[kStreamRows][VPT];
                 float xv[kStreamRows], acc[kStreamRows];
 #pragma unroll
                 for (int i = 0; i < kStreamRows; ++i) {
-                    const int e = e0 + i * kStreamThreads + tid;
-                    const int p = e / tpr;
+                    const int p = pbase + i * row_step;
                     acc[i] = 0.0f;
                     xv[i] = 0.0f;
-                    if (e < total) {
+                    if (p < P) {
                         xv[i] = ssd_ld(xs + p);
 #pragma unroll
                         for (int v = 0; v < VPT; ++v)
-                            q[i][v] = ssd_ld4(sm + (size_t)p * N + 4 * (lane_n + v * tpr));
+                            q[i][v] = ssd_ld4(sm + (p << nsh) + 4 * (lane_n + v * tpr));
                     }
                 }
 #pragma unroll
                 for (int i = 0; i < kStreamRows; ++i) {
-                    const int e = e0 + i * kStreamThreads + tid;
-                    const int p = e / tpr;
-                    if (e < total) {
+                    const int p = pbase + i * row_step;
+                    if (p < P) {
                         const float dx = dtv * xv[i];
 #pragma unroll
                         for (int v = 0; v < VPT; ++v) {
@@ -260,7 +277,7 @@ ssd_decode_stream_kernel(S *__restrict__ state, const T *__restrict__ x,
                             w.y = fmaf(decay, w.y, dx * Bv[v].y);
                             w.z = fmaf(decay, w.z, dx * Bv[v].z);
                             w.w = fmaf(decay, w.w, dx * Bv[v].w);
-                            ssd_st4(sm + (size_t)p * N + 4 * (lane_n + v * tpr), w);
+                            ssd_st4(sm + (p << nsh) + 4 * (lane_n + v * tpr), w);
                             acc[i] = fmaf(Cv[v].x, w.x, acc[i]);
                             acc[i] = fmaf(Cv[v].y, w.y, acc[i]);
                             acc[i] = fmaf(Cv[v].z, w.z, acc[i]);
@@ -273,13 +290,14 @@ ssd_decode_stream_kernel(S *__restrict__ state, const T *__restrict__ x,
                     for (int i = 0; i < kStreamRows; ++i)
                         acc[i] += __shfl_xor_sync(0xffffffffu, acc[i], off);
                 }
+                if (lane_n == 0) {
 #pragma unroll
-                for (int i = 0; i < kStreamRows; ++i) {
-                    const int e = e0 + i * kStreamThreads + tid;
-                    if (e < total && lane_n == 0)
-                        ssd_st(y + (size_t)u * P + e / tpr,
-                               ssd_gate<kFuse, T>(fuse, acc[i] + Dh * xv[i],
-                                                  (size_t)u * P + e / tpr));
+                    for (int i = 0; i < kStreamRows; ++i) {
+                        const int p = pbase + i * row_step;
+                        if (p < P)
+                            ssd_st(y + (size_t)u * P + p,
+                                   ssd_gate<kFuse, T>(fuse, acc[i] + Dh * xv[i], (size_t)u * P + p));
+                    }
                 }
             }
             fence_proxy_async_smem();
