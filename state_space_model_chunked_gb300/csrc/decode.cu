@@ -145,10 +145,15 @@ ssd_decode_stream_kernel(S *__restrict__ state, const T *__restrict__ x,
     volatile int *abort_flag = reinterpret_cast<volatile int *>(done + stages);
     const uint32_t sbase = smem_u32(smem);
     constexpr int kComputeWarps = kStreamThreads / 32;
+    // bf16 states halve the bytes per unit, so the per-unit update latency
+    // becomes the limit: groups of compute warps then take alternate units
+    // (timed: fp32 states are fastest with one group, bf16 with four: 0.55 ms
+    // a token at batch 16 against 0.61 with two and 0.77 with one)
+    constexpr int kGroups = sizeof(S) < 4 ? 4 : 1;
     if (tid == 0) {
         for (int i = 0; i < stages; ++i) {
             mbar_init(smem_u32(full + i), 1);
-            mbar_init(smem_u32(done + i), kComputeWarps);
+            mbar_init(smem_u32(done + i), kComputeWarps / kGroups);
         }
         *abort_flag = 0;
         fence_mbar_init();
@@ -198,29 +203,31 @@ ssd_decode_stream_kernel(S *__restrict__ state, const T *__restrict__ x,
     } else {
         // ---- compute warps
         // tpr (threads per row) and N are powers of two: rows and offsets by
-        // shifts; a thread's rows advance by kStreamThreads / tpr per step
+        // shifts; a thread's rows advance by kGroupThreads / tpr per step
+        constexpr int kGroupThreads = kStreamThreads / kGroups;
+        const int grp = tid / kGroupThreads, gtid = tid - grp * kGroupThreads;
         const int tpr = N / (4 * VPT);
         const int tsh = __ffs(tpr) - 1, nsh = __ffs(N) - 1;
-        const int lane_n = tid & (tpr - 1);
+        const int lane_n = gtid & (tpr - 1);
         const int total = P * tpr;
-        const int row0 = tid >> tsh, row_step = kStreamThreads >> tsh;
+        const int row0 = gtid >> tsh, row_step = kGroupThreads >> tsh;
         // the next unit's dt, A and D are loaded one unit ahead, so no global
         // load latency sits between two units' updates (dt raw; transformed at use)
         float dt_next = 0.f, A_next = 0.f, D_next = 0.f;
-        if (nk > 0) {
-            const int h0 = (int)(unit_of(0) % H);
-            dt_next = dt[unit_of(0)];
+        if (grp < nk) {
+            const int h0 = (int)(unit_of(grp) % H);
+            dt_next = dt[unit_of(grp)];
             A_next = A[h0];
             D_next = D ? D[h0] : 0.0f;
         }
-        for (long k = 0; k < nk; ++k) {
+        for (long k = grp; k < nk; k += kGroups) {
             const int st = (int)(k % stages);
             const long u = unit_of(k);
             const int h = (int)(u % H);
             const float dtv = ssd_dt<kFuse>(fuse, dt_next, ssd_dt_bias<kFuse>(fuse, h));
             const float Ah = A_next, Dh = D_next;
-            if (k + 1 < nk) {
-                const long un = unit_of(k + 1);
+            if (k + kGroups < nk) {
+                const long un = unit_of(k + kGroups);
                 const int hn = (int)(un % H);
                 dt_next = dt[un];
                 A_next = A[hn];
@@ -249,7 +256,7 @@ ssd_decode_stream_kernel(S *__restrict__ state, const T *__restrict__ x,
             }
             // kStreamRows independent rows per thread per pass: all shared-memory
             // reads first, then the updates, then the interleaved row reductions
-            for (int e0 = 0; e0 < total; e0 += kStreamThreads * kStreamRows) {
+            for (int e0 = 0; e0 < total; e0 += kGroupThreads * kStreamRows) {
                 const int pbase = (e0 >> tsh) + row0;   // row of this thread's i = 0
                 float4 q[kStreamRows][VPT];
                 float xv[kStreamRows], acc[kStreamRows];
