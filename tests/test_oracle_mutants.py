@@ -68,3 +68,113 @@ def test_unmutated_source_passes(tmp_path, monkeypatch):
                              inp["D"], inp["init"])
     assert oracle.rel_l2(y, yq) < 1e-10 and oracle.rel_l2(fin, fq) < 1e-10
     assert np.isfinite(y).all()
+
+
+# ----------------------------------------------------- the numpy-level oracle
+# Planted mistakes in the functions written in Python (packed sequences, the
+# dt transform, the gate, bf16 rounding): each mutant replaces one oracle
+# function for the duration of a pin test, which must then fail.
+import tests.test_oracle_pins as pins
+
+_scan_varlen, _dt_transform, _gate, _round_bf16, _step = (
+    oracle.scan_varlen, oracle.dt_transform, oracle.gate, oracle.round_bf16, oracle.step)
+
+
+def _varlen_shared_init(x, dt, A, B, C, cu, D=None, init=None, nthreads=None):
+    shared = None if init is None else np.repeat(np.asarray(init)[:1], len(cu) - 1, axis=0)
+    return _scan_varlen(x, dt, A, B, C, cu, D, shared, nthreads)
+
+
+def _varlen_state_carried(x, dt, A, B, C, cu, D=None, init=None, nthreads=None):
+    y = np.empty(np.shape(x), np.float64)
+    fin = np.zeros((len(cu) - 1,) + np.shape(x)[1:] + (np.shape(B)[2],), np.float64)
+    h = None if init is None else np.asarray(init, np.float64)[:1]
+    for s in range(len(cu) - 1):
+        a, b = int(cu[s]), int(cu[s + 1])
+        if a < b:
+            ys, h = oracle.scan_seq(x[None, a:b], dt[None, a:b], A, B[None, a:b], C[None, a:b], D, h)
+            y[a:b] = ys[0]
+        fin[s] = 0 if h is None else h[0]
+    return y, fin
+
+
+def _varlen_offset_shift(x, dt, A, B, C, cu, D=None, init=None, nthreads=None):
+    cu2 = np.asarray(cu).copy()
+    cu2[1:-1] += 1
+    return _scan_varlen(x, dt, A, B, C, cu2, D, init, nthreads)
+
+
+def _gate_sigmoid_only(y, z):
+    z = np.asarray(z, np.float64)
+    return np.asarray(y, np.float64) * np.exp(-np.logaddexp(0.0, -z))
+
+
+def _gate_wrong_sign(y, z):
+    z = np.asarray(z, np.float64)
+    return np.asarray(y, np.float64) * (z * np.exp(-np.logaddexp(0.0, z)))
+
+
+def _round_half_up(a):
+    m, e = np.frexp(np.asarray(a, np.float64))
+    return np.ldexp(np.floor(m * 256.0 + 0.5) / 256.0, e)
+
+
+def _round_truncate(a):
+    m, e = np.frexp(np.asarray(a, np.float64))
+    return np.ldexp(np.trunc(m * 256.0) / 256.0, e)
+
+
+def _dt_bias_after_softplus(dt, bias=None, softplus=False, lo=-np.inf, hi=np.inf):
+    u = np.asarray(dt, np.float64)
+    if softplus:
+        u = np.logaddexp(0.0, u)
+    if bias is not None:
+        u = u + np.asarray(bias, np.float64)
+    return np.minimum(np.maximum(u, lo), hi)
+
+
+def _dt_clamp_first(dt, bias=None, softplus=False, lo=-np.inf, hi=np.inf):
+    u = np.asarray(dt, np.float64)
+    if bias is not None:
+        u = u + np.asarray(bias, np.float64)
+    u = np.minimum(np.maximum(u, lo), hi)
+    return np.logaddexp(0.0, u) if softplus else u
+
+
+def _bf16_step_rounds_y(state, x, dt, A, B, C, D=None, nthreads=None):
+    y, st = _step(state, x, dt, A, B, C, D, nthreads)
+    return _round_bf16(y), _round_bf16(st)
+
+
+def _bf16_step_unrounded(state, x, dt, A, B, C, D=None, nthreads=None):
+    return _step(state, x, dt, A, B, C, D, nthreads)
+
+
+PY_MUTANTS = {
+    "varlen_shared_initial_state": ("scan_varlen", _varlen_shared_init,
+                                    pins.test_varlen_is_each_sequence_alone_by_quadratic_form),
+    "varlen_state_leaks_across_sequences": ("scan_varlen", _varlen_state_carried,
+                                            pins.test_varlen_is_each_sequence_alone_by_quadratic_form),
+    "varlen_offsets_shifted": ("scan_varlen", _varlen_offset_shift,
+                               pins.test_varlen_is_each_sequence_alone_by_quadratic_form),
+    "gate_sigmoid_without_z": ("gate", _gate_sigmoid_only, pins.test_gate_closed_forms),
+    "gate_sigmoid_of_minus_z": ("gate", _gate_wrong_sign, pins.test_gate_closed_forms),
+    "bf16_ties_away_from_zero": ("round_bf16", _round_half_up, pins.test_round_bf16_nearest_even),
+    "bf16_truncation": ("round_bf16", _round_truncate, pins.test_round_bf16_nearest_even),
+    "dt_bias_after_softplus": ("dt_transform", _dt_bias_after_softplus,
+                               pins.test_dt_transform_bias_per_head_then_clamp),
+    "dt_clamp_before_softplus": ("dt_transform", _dt_clamp_first,
+                                 pins.test_dt_transform_bias_per_head_then_clamp),
+    "bf16_step_rounds_y": ("step_bf16_state", _bf16_step_rounds_y,
+                           pins.test_step_bf16_state_is_rounded_step),
+    "bf16_step_state_not_rounded": ("step_bf16_state", _bf16_step_unrounded,
+                                    pins.test_step_bf16_state_is_rounded_step),
+}
+
+
+@pytest.mark.parametrize("name", sorted(PY_MUTANTS))
+def test_pins_catch_planted_python_mistake(name, monkeypatch):
+    attr, mutant, pin = PY_MUTANTS[name]
+    monkeypatch.setattr(oracle, attr, mutant)
+    with pytest.raises(AssertionError):
+        pin()
