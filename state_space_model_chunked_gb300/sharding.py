@@ -4,7 +4,9 @@ Every (batch row, head) recurrence is independent, so the scan and the
 decode step shard over batch rows and heads with no exchange in the data
 path: each GPU runs ssd_scan_fwd / ssd_state_update on its own slice.  Heads
 are split on group boundaries so each GPU keeps whole groups (heads of one
-group share B and C, and the tensor-core kernel pairs them).
+group share B and C, and the tensor-core kernel pairs them).  A packed batch
+of sequences splits into contiguous runs of whole sequences with even token
+shares (ssd_scan_fwd_varlen on each run).
 
 Timing across ranks takes the maximum over ranks (the slowest GPU finishes
 the job).
@@ -31,6 +33,36 @@ def batch_range(batch: int, world: int, rank: int):
     if not 0 <= rank < world:
         raise ValueError("rank out of range")
     return (batch * rank) // world, (batch * (rank + 1)) // world
+
+
+def sequence_range(cu_seqlens, world: int, rank: int):
+    """Contiguous [start, stop) range of packed sequences for `rank` of
+    `world`, cut at the sequence boundaries nearest to even shares of the
+    tokens (a sequence is never split: its recurrence is sequential).  Every
+    rank's token count is within the longest sequence of total / world.
+    Returns (s0, s1, offsets): the rank's cu_seqlens rebased to 0."""
+    import numpy as np
+    if not 0 <= rank < world:
+        raise ValueError("rank out of range")
+    cu = np.asarray(cu_seqlens, dtype=np.int64)
+    if cu.ndim != 1 or cu.size < 1 or cu[0] != 0 or np.any(np.diff(cu) < 0):
+        raise ValueError("cu_seqlens must start at 0 and not decrease")
+    nseq, total = cu.size - 1, int(cu[-1])
+
+    def cut(r):
+        if r <= 0:
+            return 0
+        if r >= world:
+            return nseq
+        target = total * r / world
+        i = int(np.searchsorted(cu, target))        # first boundary >= target
+        if i > 0 and target - cu[i - 1] < (cu[i] - target if i <= nseq else np.inf):
+            i -= 1
+        return min(max(i, 0), nseq)
+
+    s0, s1 = cut(rank), cut(rank + 1)
+    s1 = max(s1, s0)
+    return s0, s1, (cu[s0:s1 + 1] - cu[s0]).astype(np.int32)
 
 
 def max_over_ranks(value: float, dist=None, device=None) -> float:

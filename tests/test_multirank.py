@@ -86,3 +86,64 @@ def test_two_gloo_ranks_reassemble_the_scan(tmp_path):
     assert oracle.rel_l2(np.concatenate(fs, axis=1), f_full) < 1e-13
     for r in range(world):
         assert float(np.load(tmp_path / f"t{r}.npy")[0]) == 3.0
+
+
+def test_sequence_ranges_partition_and_balance():
+    from state_space_model_chunked_gb300 import inputs as gen
+    from state_space_model_chunked_gb300.sharding import sequence_range
+    for lengths in ([5, 0, 13, 1, 9], gen.packed_lengths(47, 64, 8192, seed=5), [100], [0, 0]):
+        cu = np.concatenate([[0], np.cumsum(lengths)])
+        T, longest = int(cu[-1]), max(lengths)
+        for world in (1, 2, 3, 4, 8):
+            parts = [sequence_range(cu, world, r) for r in range(world)]
+            assert parts[0][0] == 0 and parts[-1][1] == len(lengths)
+            for (a0, a1, _), (b0, b1, _) in zip(parts, parts[1:]):
+                assert a1 == b0
+            for s0, s1, off in parts:
+                assert off[0] == 0 and off[-1] == cu[s1] - cu[s0]
+                assert off[-1] <= T / world + longest
+
+
+def _varlen_worker(rank, world, port, out_dir):
+    import torch.distributed as dist
+
+    import oracle
+    from state_space_model_chunked_gb300 import inputs as gen
+    from state_space_model_chunked_gb300.sharding import sequence_range
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    inp = gen.varlen_inputs([30, 7, 0, 55, 12, 40], 4, 8, 16, 2, "bf16", seed=9,
+                            random_init=True)
+    s0, s1, off = sequence_range(inp["cu"], world, rank)
+    t0, t1 = int(inp["cu"][s0]), int(inp["cu"][s1])
+    y, fin = oracle.scan_varlen(inp["x"][t0:t1], inp["dt"][t0:t1], inp["A"], inp["B"][t0:t1],
+                                inp["C"][t0:t1], off, inp["D"], inp["init"][s0:s1])
+    np.save(os.path.join(out_dir, f"vy{rank}.npy"), y)
+    np.save(os.path.join(out_dir, f"vf{rank}.npy"), fin)
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_two_gloo_ranks_reassemble_a_packed_batch(tmp_path):
+    world = 2
+    port = _free_port()
+    ctx = mp.get_context("spawn")
+    procs = [ctx.Process(target=_varlen_worker, args=(r, world, port, str(tmp_path)))
+             for r in range(world)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=120)
+        assert p.exitcode == 0
+    import oracle
+    from state_space_model_chunked_gb300 import inputs as gen
+    inp = gen.varlen_inputs([30, 7, 0, 55, 12, 40], 4, 8, 16, 2, "bf16", seed=9,
+                            random_init=True)
+    y_full, f_full = oracle.scan_varlen(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"],
+                                        inp["cu"], inp["D"], inp["init"])
+    ys = [np.load(tmp_path / f"vy{r}.npy") for r in range(world)]
+    fs = [np.load(tmp_path / f"vf{r}.npy") for r in range(world)]
+    assert ys[0].shape[0] > 0 and ys[1].shape[0] > 0
+    np.testing.assert_array_equal(np.concatenate(ys, axis=0), y_full)
+    np.testing.assert_array_equal(np.concatenate(fs, axis=0), f_full)
