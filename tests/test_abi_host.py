@@ -165,3 +165,39 @@ def test_varlen_queries(lib):
     keep, cu = _cu([0, 3, 9])
     assert lib.ssd_scan_varlen_workspace_bytes(2, cu, 4, 64, 64, 1, 64, 0) == 0   # fp32: SIMT
     assert lib.ssd_scan_varlen_kernel_launches(2, cu, 4, 64, 64, 1, 64, 0) == 1
+
+
+def test_fused_scan_rejects_misaligned_gate(lib):
+    a = [_fake(0x1000), _fake(0x2000), _fake(0x3000), _fake(0x4000), _fake(0x5000), None, None,
+         _fake(0x9008), 1, 1, 256, 4, 64, 64, 1, 64, None, _fake(0x6000), None, None, 0, None]
+    assert lib.ssd_scan_fwd_fused(0, *a) == INVALID
+
+
+def _dec_fused(lib, **kw):
+    a = dict(state=_fake(0x1000), sdt=0, x=_fake(0x2000), dt=_fake(0x3000), A=_fake(0x4000),
+             B=_fake(0x5000), C=_fake(0x6000), D=None, tr=None, z=None, dtype=1, b=2, H=4, P=16,
+             N=16, G=1, y=_fake(0x7000), stream=None)
+    a.update(kw)
+    return lib.ssd_state_update_fused(a["state"], a["sdt"], a["x"], a["dt"], a["A"], a["B"],
+                                      a["C"], a["D"], a["tr"], a["z"], a["dtype"], a["b"],
+                                      a["H"], a["P"], a["N"], a["G"], a["y"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(sdt=5), INVALID),                  # unknown state dtype
+    (dict(sdt=1, dtype=0), UNSUPPORTED),     # bf16 state needs bf16 inputs
+    (dict(z=_fake(0x9004)), INVALID),        # gate array not 16-byte aligned
+    (dict(state=None), INVALID),
+])
+def test_fused_decode_rejects_bad_arguments(lib, kw, expect):
+    assert _dec_fused(lib, **kw) == expect
+
+
+def test_dt_transform_rejects_inverted_limits(lib):
+    class Tr(ctypes.Structure):
+        _fields_ = [("dt_bias", ctypes.c_void_p), ("softplus", ctypes.c_int),
+                    ("dt_min", ctypes.c_float), ("dt_max", ctypes.c_float)]
+    tr = Tr(None, 1, 0.5, 0.1)
+    assert _dec_fused(lib, tr=ctypes.cast(ctypes.pointer(tr), ctypes.c_void_p)) == INVALID
+    tr_nan = Tr(None, 1, float("nan"), 0.1)
+    assert _dec_fused(lib, tr=ctypes.cast(ctypes.pointer(tr_nan), ctypes.c_void_p)) == INVALID
