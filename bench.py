@@ -87,9 +87,13 @@ class ClockSampler:
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, index):
+        import tempfile
         self.index = index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{index}.csv")
+        # the raw samples go to SSD_CLOCKS_CSV_DIR when set (to keep them),
+        # else to a temporary file; the JSON line carries their summary
+        out_dir = os.environ.get("SSD_CLOCKS_CSV_DIR") or tempfile.gettempdir()
+        self.path = os.path.join(out_dir, f"ssd_clocks_rank{index}_{os.getpid()}.csv")
 
     def __enter__(self):
         try:
