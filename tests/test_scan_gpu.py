@@ -379,3 +379,11 @@ def test_varlen_output_gate(algo):
     for s in range(len(cu) - 1):
         a, b = cu[s], cu[s + 1]
         assert rel(y[a:b], oracle.gate(yr[a:b], z[a:b])) <= 1e-2
+
+
+def test_varlen_long_sequence_four_head_segments():
+    """A packed batch whose long sequence is split into segments at 80 heads:
+    the segment-contribution kernel then takes four heads per CTA (the packed
+    form of the long-context plan), next to short unsplit sequences."""
+    inp = gen.varlen_inputs([20000, 300, 5], 80, 64, 128, 1, "bf16", seed=51, random_init=True)
+    _check_varlen(inp, "bf16", TC)
