@@ -22,7 +22,8 @@
  *     h_t = exp(dt_t * A_h) * h_{t-1} + dt_t * B_t x_t^T      (state N x P)
  *     y_t = C_t . h_t + D_h * x_t                             (uses updated h)
  * with h_{-1} = init_state (or zero) and final_state = h_{L-1}.  dt is used
- * exactly as given (no softplus or bias).
+ * exactly as given unless a call passes a dt transform (ssd_dt_transform);
+ * the fused entry points can also gate y by silu(z).
  *
  * Layouts (row-major, contiguous, element strides implied by the sizes):
  *     x, y            [batch][seqlen][nheads][headdim]          in_dtype
@@ -31,7 +32,9 @@
  *     B, C            [batch][seqlen][ngroups][dstate]           in_dtype
  *     init_state, final_state, decode state
  *                     [batch][nheads][headdim][dstate]           float
- * For decode, drop the seqlen dimension.
+ *                     (a decode state may be bfloat16: ssd_state_update_fused)
+ * For decode, drop the seqlen dimension.  Packed variable-length batches
+ * (ssd_scan_fwd_varlen) drop the batch dimension of the token arrays.
  *
  * Ownership: every pointer is a DEVICE pointer owned by the caller, except
  * where an entry point says otherwise.  The library allocates no memory;
