@@ -201,3 +201,27 @@ def test_dt_transform_rejects_inverted_limits(lib):
     assert _dec_fused(lib, tr=ctypes.cast(ctypes.pointer(tr), ctypes.c_void_p)) == INVALID
     tr_nan = Tr(None, 1, float("nan"), 0.1)
     assert _dec_fused(lib, tr=ctypes.cast(ctypes.pointer(tr_nan), ctypes.c_void_p)) == INVALID
+
+
+def test_binding_host_offsets_validation():
+    import numpy as np
+    import torch
+    from state_space_model_chunked_gb300._binding import _host_offsets
+    cu, ptr = _host_offsets([0, 3, 3, 10])
+    assert cu.dtype == np.int32 and list(cu) == [0, 3, 3, 10] and ptr.value
+    cu, _ = _host_offsets(torch.tensor([0, 5], dtype=torch.int64))
+    assert list(cu) == [0, 5]
+    for bad in ([0], [[0, 1]], [0, -1], [0, 2 ** 31]):
+        with pytest.raises(ValueError):
+            _host_offsets(bad)
+
+
+def test_binding_refuses_cpu_tensors_for_packed_and_decode():
+    import torch
+    x = torch.zeros(4, 2, 8)
+    with pytest.raises((ValueError, ImportError)):
+        ssd.scan_fwd_varlen(x, torch.zeros(4, 2), torch.zeros(2), torch.zeros(4, 1, 8),
+                            torch.zeros(4, 1, 8), [0, 4])
+    with pytest.raises((ValueError, ImportError)):
+        ssd.state_update(torch.zeros(1, 2, 8, 8), torch.zeros(1, 2, 8), torch.zeros(1, 2),
+                         torch.zeros(2), torch.zeros(1, 1, 8), torch.zeros(1, 1, 8))
