@@ -225,3 +225,28 @@ def test_binding_refuses_cpu_tensors_for_packed_and_decode():
     with pytest.raises((ValueError, ImportError)):
         ssd.state_update(torch.zeros(1, 2, 8, 8), torch.zeros(1, 2, 8), torch.zeros(1, 2),
                          torch.zeros(2), torch.zeros(1, 1, 8), torch.zeros(1, 1, 8))
+
+
+def test_plain_c_caller(tmp_path, lib):
+    """A C program linked against libssd.so gets the same argument errors:
+    the boundary needs neither Python nor torch."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    cuda_inc = None
+    for cand in (os.environ.get("CUDA_HOME"), "/usr/local/cuda"):
+        if cand and os.path.exists(os.path.join(cand, "include", "cuda_runtime_api.h")):
+            cuda_inc = os.path.join(cand, "include")
+            break
+    if cuda_inc is None:
+        pytest.skip("CUDA headers not found")
+    libdir = os.path.dirname(ssd.lib_path())
+    exe = tmp_path / "c_abi_check"
+    subprocess.run([cc, "-std=c11", "-O1", "-I", os.path.join(ROOT, "include"), "-I", cuda_inc,
+                    os.path.join(ROOT, "tests", "c_abi_check.c"), "-o", str(exe),
+                    ssd.lib_path(), f"-Wl,-rpath,{libdir}"], check=True)
+    out = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert out.returncode == 0, out.stdout + out.stderr
+    assert "c abi ok" in out.stdout
