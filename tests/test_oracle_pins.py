@@ -370,3 +370,18 @@ def test_step_bf16_state_is_rounded_step():
     y1, s1 = oracle.step_bf16_state(st, np.zeros_like(tok["x"]), np.ones_like(tok["dt"]),
                                     np.zeros(H, np.float32), tok["B"], tok["C"])
     np.testing.assert_array_equal(s1, st.astype(np.float64))
+
+
+def test_hand_worked_packed_example():
+    """Packed sequences against values worked out by hand (including an empty
+    sequence whose state must come back unchanged)."""
+    g = json.load(open(os.path.join(HERE, "golden", "hand_example_packed.json")))
+    i = g["inputs"]
+    T = len(i["x"])
+    y, fin = oracle.scan_varlen(np.array(i["x"]).reshape(T, 1, 1), np.array(i["dt"]).reshape(T, 1),
+                                np.array(i["A"]), np.array(i["B"]).reshape(T, 1, 1),
+                                np.array(i["C"]).reshape(T, 1, 1), np.array(i["cu"]),
+                                np.array(i["D"]), np.array(i["init"]).reshape(3, 1, 1, 1))
+    tol = g["tolerance"]
+    np.testing.assert_allclose(y.ravel(), g["expected"]["y"], rtol=tol, atol=tol)
+    np.testing.assert_allclose(fin.ravel(), g["expected"]["final_state"], rtol=tol, atol=tol)
