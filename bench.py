@@ -3,25 +3,33 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 
-One step = one ssd_scan_fwd over the Mamba-2-130M-shaped prefill layer
-(batch 1, seqlen 4096, 24 heads, headdim 64, d_state 128, bf16 x/B/C, fp32
-dt/A/D and states): every row of the hot path -- chunk cumsum and decays,
-C.B^T, the decay mask, the intra-chunk product, chunk states, inter-chunk
-state passing, the off-diagonal output and the D skip.  The line also carries
-the decode state update (64-layer 2.7B-shaped stack at batch 1/16/64/256) and
-the long-context 2.7B-shaped prefill, each with its own roofline.
+One step = one ssd_scan_fwd over the Mamba-2-2.7B-shaped long-context prefill
+layer (batch 1, seqlen 65536, 80 heads, headdim 64, d_state 128, one group,
+bf16 x/B/C, fp32 dt/A/D and states): every row of the hot path -- chunk
+cumsum and decays, C.B^T, the decay mask, the intra-chunk product, chunk
+states, inter-chunk state passing, the off-diagonal output and the D skip.
+This is the largest prefill workload that fits one GPU.  The line also
+carries the other prefill workloads (fp32 256-token, 130M 4096-token, 370M
+batch-8 2048-token with a random initial state), each with its own roofline,
+the decode state update (64-layer 2.7B-shaped stack at batch 1/16/64/256,
+fp32 and bf16 states, single- and multi-token), cached decode against
+recompute, a packed batch and the fused layer steps.
 
-Inputs are seeded synthetic data generated on the device.  Between timed
-steps the prefill rotates through enough input/output sets to exceed twice
-the L2 cache, so no step reads another step's data from L2.
+Inputs are seeded synthetic data generated on the device; the long layer's
+inputs (1.4 GB) are larger than the L2 cache, and the smaller workloads
+rotate through enough input/output sets to exceed twice the L2 cache, so no
+step reads another step's data from L2.
 
 --impl reference times the fp64 CPU oracle (the only other program that
 computes this path here) on the host cores, on a bounded sample of the same
-workload, and prints the same line with "impl": "reference".
+workload (whole heads of the layer: every head is an independent
+recurrence), and prints the same line with "impl": "reference".
 
-Under torchrun each rank runs its own copy of the workload on its own GPU
-(independent problems, no collective in the data path): weak scaling, value =
-all ranks' tokens / max over ranks of the timed region.
+Under torchrun the layer's heads are split across the ranks (whole groups,
+or a single group split on head-pair boundaries; B and C are inputs every
+rank reads), each rank scanning its heads on its own GPU with no collective
+in the data path: strong scaling, value = the layer's tokens / max over ranks
+of the timed region.
 """
 from __future__ import annotations
 
@@ -37,14 +45,14 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
-WORKLOAD = "mamba2_130m_L4096"
-LONG_WORKLOAD = "mamba2_2p7b_L65536"
+WORKLOAD = "mamba2_2p7b_L65536"
+EXTRA_SCANS = ("ssd_fp32_L256_H4_P64_N64", "mamba2_130m_L4096", "mamba2_370m_b8_L2048")
 METRIC = "SSD prefill Mtokens/s & decode state-update GB/s, % of roofline"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
 # ----------------------------------------------------------------- helpers
-def ncu_traffic(kernel, workload):
+def ncu_traffic(kernel, workload, key="bytes_per_launch"):
     """DRAM bytes per launch of `kernel` on `workload` from one ncu capture
     (dram__bytes_read.sum + dram__bytes_write.sum), as recorded in
     profiles/dram_traffic.json with the hash of the kernel's sources at capture
@@ -59,7 +67,14 @@ def ncu_traffic(kernel, workload):
                 h.update(f.read())
     except (OSError, ValueError, KeyError, TypeError):
         return None
-    return entry["bytes_per_launch"] if h.hexdigest() == entry["sources_sha256"] else None
+    return entry[key] if h.hexdigest() == entry["sources_sha256"] else None
+
+
+def ncu_call_traffic(workload):
+    """DRAM bytes of one whole call (every kernel it launches) on `workload`
+    from one ncu capture, as recorded under "calls" in
+    profiles/dram_traffic.json; None when absent or the sources have changed."""
+    return ncu_traffic("calls", workload, key="bytes_per_call")
 
 
 def load_peaks():
@@ -533,7 +548,8 @@ def time_fused_steps(shape, device, reps=20):
     bias = torch.randn((shape.nheads,), generator=g, device=device) * 0.5
     ws = torch.empty(max(ssd.scan_workspace_bytes(shape.batch, shape.seqlen, shape.nheads,
                                                   shape.headdim, shape.dstate, shape.ngroups,
-                                                  shape.chunk, device=device), 1),
+                                                  shape.chunk, device=device,
+                                                  dt_transform=True), 1),
                      dtype=torch.uint8, device=device)
     stream = torch.cuda.current_stream(device)
 
@@ -568,33 +584,19 @@ def time_fused_steps(shape, device, reps=20):
             "note": "eager calls (host overhead included in both)"}
 
 
-def cpu_oracle_sample_one_core(shape, heads=2):
-    """The oracle on one host core over `heads` whole heads of the workload,
-    scaled to the full layer (heads are independent recurrences)."""
+def cpu_oracle_sample(shape, heads=None, target_s=10.0, cores=None, max_reps=50):
+    """The oracle as it stands on the host cores, on `heads` whole heads of the
+    workload (all of them by default; every head is an independent
+    recurrence), repeated until `target_s` seconds have passed.  The inputs
+    are drawn before the clock starts.  Returns (Mtokens/s of the whole layer,
+    cores used, sample description)."""
     import oracle
     from state_space_model_chunked_gb300 import inputs as gen
+    cores = cores or os.cpu_count() or 1
+    heads = heads or shape.nheads
     inp = gen.scan_inputs(shape.batch, shape.seqlen, heads, shape.headdim, shape.dstate,
                           min(shape.ngroups, heads), shape.dtype, seed=5,
                           random_init=shape.random_init)
-    t0 = time.perf_counter()
-    oracle.scan_seq(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], inp["D"], inp["init"],
-                    nthreads=1)
-    el = time.perf_counter() - t0
-    tok_s = shape.tokens * heads / shape.nheads / el
-    return tok_s / 1e6, (f"{heads} of {shape.nheads} heads of {shape.name} on 1 core, "
-                         f"{el:.1f} s, scaled to the layer")
-
-
-def cpu_oracle_sample(shape, target_s=10.0):
-    """The oracle as it stands, on all host cores, on whole heads of the
-    workload (every head is an independent recurrence): returns (Mtokens/s
-    scaled to the full layer, cores, sample description)."""
-    import oracle
-    from state_space_model_chunked_gb300 import inputs as gen
-    cores = os.cpu_count() or 1
-    heads = shape.nheads
-    inp = gen.scan_inputs(shape.batch, shape.seqlen, heads, shape.headdim, shape.dstate,
-                          shape.ngroups, shape.dtype, seed=5, random_init=shape.random_init)
     t0 = time.perf_counter()
     reps = 0
     while True:
@@ -602,16 +604,59 @@ def cpu_oracle_sample(shape, target_s=10.0):
                         inp["init"], nthreads=cores)
         reps += 1
         el = time.perf_counter() - t0
-        if el >= target_s or reps >= 50:
+        if el >= target_s or reps >= max_reps:
             break
-    tok_s = reps * shape.tokens / el
-    desc = (f"{reps} full passes of the {shape.name} workload ({shape.tokens} tokens x "
-            f"{heads} heads) through the fp64 oracle, {el:.1f} s")
+    tok_s = reps * shape.tokens * heads / shape.nheads / el
+    desc = (f"{reps} pass(es) of {heads} of the {shape.nheads} heads of {shape.name} "
+            f"({shape.tokens} tokens) through the fp64 oracle on {cores} thread(s), "
+            f"{el:.1f} s, scaled to the whole layer")
     return tok_s / 1e6, cores, desc
+
+
+def executed_tc_flops(shape):
+    """FLOPs the tensor-core scan kernel issues on tcgen05 for one call: per
+    128-token tile and head pair C.B^T, the state update, the off-diagonal
+    product and both heads' masked products, each 2 x 128^3 (a single head
+    per CTA: C.B^T plus three 128 x 64 x 128 products)."""
+    tiles = -(-shape.seqlen // 128)
+    per_group = shape.nheads // shape.ngroups
+    unit = 2 * 128 ** 3
+    if per_group % 2 == 0:
+        return shape.batch * tiles * (shape.nheads // 2) * 4 * unit
+    return shape.batch * tiles * shape.nheads * 2.5 * unit
+
+
+def scan_line_entry(shape, ms, kern_ms, byts, peaks, kernel):
+    """Throughput and roofline of one prefill workload: the y-writing
+    kernel's fraction (compulsory bytes / its time) and the call's (the same
+    bytes / the whole call's time, all its kernels)."""
+    flops, _ = scan_flops_bytes(shape, shape.random_init)
+    achieved = byts / (kern_ms * 1e-3) / 1e9
+    call = byts / (ms * 1e-3) / 1e9
+    return {
+        "workload": shape.name, "ms_per_step": ms,
+        "Mtokens_per_s": shape.tokens / (ms * 1e-3) / 1e6,
+        "roofline": {"bound": "hbm", "kernel": kernel, "kernel_ms": kern_ms,
+                     "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / peaks["hbm_gbs"], "call_achieved": call,
+                     "call_frac": call / peaks["hbm_gbs"], "algorithmic_bytes": byts,
+                     "algorithmic_tflops": flops / (ms * 1e-3) / 1e12},
+    }
+
+
+def sharded_shape(shape, world, rank):
+    """The rank's part of the layer: its heads (and the groups they read)."""
+    import dataclasses
+    from state_space_model_chunked_gb300.sharding import head_shard
+    h0, h1, g0, g1 = head_shard(shape.nheads, shape.ngroups, world, rank)
+    return dataclasses.replace(shape, nheads=max(h1 - h0, 0), ngroups=max(g1 - g0, 1)), (h0, h1)
 
 
 # ------------------------------------------------------------------ arms
 def run_reference(args):
+    """The oracle as it stands, timed on the host cores: each step is one pass
+    over a sample of whole heads of the layer (inputs drawn before timing)."""
+    import numpy as np  # noqa: F401
     world, rank, _ = dist_setup()
     if rank != 0:
         return 0
@@ -619,26 +664,37 @@ def run_reference(args):
     import oracle
     oracle.build()
     shape = gen.SCAN_SHAPES[WORKLOAD]
-    per = []
+    heads = args.reference_heads
     cores = os.cpu_count() or 1
+    inp = gen.scan_inputs(shape.batch, shape.seqlen, heads, shape.headdim, shape.dstate,
+                          min(shape.ngroups, heads), shape.dtype, seed=5,
+                          random_init=shape.random_init)
+
+    def one():
+        oracle.scan_seq(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], inp["D"],
+                        inp["init"], nthreads=cores)
+
     for _ in range(args.warmup):
-        cpu_oracle_sample(shape, target_s=0.0)
+        one()
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        v, cores, desc = cpu_oracle_sample(shape, target_s=0.0)
-        per.append(v)
+        one()
     el = time.perf_counter() - t0
-    value = args.steps * shape.tokens / el / 1e6
+    layer_tokens = shape.tokens * heads / shape.nheads      # whole-layer tokens per step
+    value = args.steps * layer_tokens / el / 1e6
+    sample = (f"each step: {heads} of the {shape.nheads} heads of {WORKLOAD} "
+              f"({shape.tokens} tokens each), scaled to the whole layer; inputs drawn before timing")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "Mtokens/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "ms_per_step": el / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "strong" if world > 1 else "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded PCG64)",
         "config": {"workload": WORKLOAD, "batch": shape.batch, "seqlen": shape.seqlen,
                    "nheads": shape.nheads, "headdim": shape.headdim, "dstate": shape.dstate,
                    "ngroups": shape.ngroups, "chunk": shape.chunk},
         "cpu_baseline": {"value": value, "unit": "Mtokens/s", "cores": cores, "kind": "oracle",
-                         "sample": f"{args.steps} full passes of {WORKLOAD} on the host cores"},
+                         "sample": sample},
         "e2e": {"value": value, "unit": "Mtokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -647,7 +703,7 @@ def run_reference(args):
 
 
 def run_only(args):
-    """One secondary workload alone, a few launches: used for ncu captures."""
+    """One workload alone, a few launches: used for ncu captures."""
     import torch
     device = torch.device("cuda:0")
     torch.cuda.set_device(device)
@@ -658,14 +714,17 @@ def run_only(args):
     if args.only == "decode":
         r = time_decode(args.decode_batch, args.steps, device, peaks,
                         torch.bfloat16 if args.decode_state == "bf16" else None)
+    elif args.only == "decode_multi":
+        r = time_decode_multi(args.decode_batch, args.decode_tokens, args.steps, device, peaks)
     else:
         props = torch.cuda.get_device_properties(device)
         l2 = getattr(props, "L2_cache_size", 126 * 1024 * 1024) or 126 * 1024 * 1024
-        lshape = gen.SCAN_SHAPES[LONG_WORKLOAD]
-        lms, lkern, _, lbytes = time_scan(lshape, args.steps, args.warmup, device, l2,
-                                          graph=False)
-        r = {"workload": LONG_WORKLOAD, "ms_per_step": lms, "scan_kernel_ms": lkern,
-             "GB_per_s": lbytes / (lms * 1e-3) / 1e9}
+        name = {"long": WORKLOAD, "130m": "mamba2_130m_L4096",
+                "370m": "mamba2_370m_b8_L2048"}[args.only]
+        shape = gen.SCAN_SHAPES[name]
+        ms, kern, _, byts = time_scan(shape, args.steps, args.warmup, device, l2, graph=False)
+        r = {"workload": name, "ms_per_step": ms, "scan_kernel_ms": kern,
+             "GB_per_s": byts / (ms * 1e-3) / 1e9}
     print(json.dumps({"only": args.only, **r}), flush=True)
     return 0
 
@@ -693,28 +752,23 @@ def run_gpu(args):
     peaks = load_peaks()
     props = torch.cuda.get_device_properties(device)
     l2 = getattr(props, "L2_cache_size", 126 * 1024 * 1024) or 126 * 1024 * 1024
-    shape = gen.SCAN_SHAPES[WORKLOAD]
-    flops, _ = scan_flops_bytes(shape, shape.random_init)
+    full = gen.SCAN_SHAPES[WORKLOAD]
+    shape, (h0, h1) = sharded_shape(full, world, rank)
+    _, full_bytes = scan_flops_bytes(full, full.random_init)
 
     with ClockSampler(local) as clk:
         ms, kern_ms, nsets, byts = time_scan(shape, args.steps, args.warmup, device, l2, dist)
         ms = max_over_ranks(ms, dist, device)
         kern_ms = max_over_ranks(kern_ms, dist, device)
         extra = {}
-        if rank == 0 and not args.quick:
-            lshape = gen.SCAN_SHAPES[LONG_WORKLOAD]
-            lms, lkern, _, lbytes = time_scan(lshape, 5, 3, device, l2)
-            lflops, _ = scan_flops_bytes(lshape, lshape.random_init)
-            extra["long_prefill"] = {
-                "workload": LONG_WORKLOAD, "ms_per_step": lms, "scan_kernel_ms": lkern,
-                "Mtokens_per_s": lshape.tokens / (lms * 1e-3) / 1e6,
-                "roofline": {"bound": "hbm", "achieved": lbytes / (lkern * 1e-3) / 1e9,
-                             "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                             "frac": lbytes / (lkern * 1e-3) / 1e9 / peaks["hbm_gbs"],
-                             "traffic": ncu_traffic("ssd_tc_scan_kernel", LONG_WORKLOAD),
-                             "kernel": "ssd_tc_scan_kernel",
-                             "call_frac": lbytes / (lms * 1e-3) / 1e9 / peaks["hbm_gbs"]},
-                "tensor_tflops": lflops / (lms * 1e-3) / 1e12}
+        if world == 1 and not args.quick:
+            configs = []
+            for name in EXTRA_SCANS:
+                sh = gen.SCAN_SHAPES[name]
+                sms, skern, _, sbytes = time_scan(sh, 20, 5, device, l2)
+                kname = "ssd_tc_scan_kernel" if sh.dtype == "bf16" else "ssd_scan_simt_kernel"
+                configs.append(scan_line_entry(sh, sms, skern, sbytes, peaks, kname))
+            extra["other_prefill_workloads"] = configs
             torch.cuda.empty_cache()
             extra["decode"] = [time_decode(b, 128, device, peaks) for b in (1, 16, 64, 256)]
             extra["decode_bf16_state"] = [time_decode(b, 128, device, peaks, torch.bfloat16)
@@ -724,14 +778,25 @@ def run_gpu(args):
             extra["decode_vs_recompute"] = time_decode_vs_recompute(device)
             extra["varlen"] = time_varlen(device, peaks)
             extra["fused_steps"] = [time_fused_steps(gen.SCAN_SHAPES[n], device)
-                                    for n in (WORKLOAD, LONG_WORKLOAD)]
+                                    for n in ("mamba2_130m_L4096", WORKLOAD)]
     clocks = clk.summary()
 
     e2e_s, h2d, d2h = time_scan_e2e(shape, max(args.steps // 4, 3), args.warmup, device)
-    tokens = shape.tokens * world
-    value = tokens / (ms * 1e-3) / 1e6
-    achieved = byts / (kern_ms * 1e-3) / 1e9
-    call_achieved = byts / (ms * 1e-3) / 1e9
+    e2e_s = max_over_ranks(e2e_s, dist, device)
+    h2d = int(max_over_ranks(h2d, dist, device)) * world
+    d2h = int(max_over_ranks(d2h, dist, device)) * world
+    value = full.tokens / (ms * 1e-3) / 1e6
+    entry = scan_line_entry(full, ms, kern_ms, full_bytes, peaks, "ssd_tc_scan_kernel")
+    roof = dict(entry["roofline"])
+    roof.update({"peak_source": peaks["source"],
+                 "traffic": ncu_traffic("ssd_tc_scan_kernel", WORKLOAD),
+                 "call_traffic": ncu_call_traffic(WORKLOAD)})
+    if world == 1:
+        tflops = executed_tc_flops(full) / (kern_ms * 1e-3) / 1e12
+        roof["tensor"] = {"executed_tflops": tflops, "peak_tflops": peaks["bf16_tflops"],
+                          "frac": tflops / peaks["bf16_tflops"],
+                          "note": "tcgen05 FLOPs the scan kernel issues (full 128-token "
+                                  "tiles) / its time"}
     launches = ssd.scan_kernel_launches(shape.batch, shape.seqlen, shape.nheads, shape.headdim,
                                         shape.dstate, shape.ngroups, shape.chunk, device=device)
     if rank != 0:
@@ -741,35 +806,34 @@ def run_gpu(args):
     line = {
         "metric": METRIC, "value": value, "unit": "Mtokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": True, "scaling": "strong" if world > 1 else "weak",
+        "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded, generated on device)",
-        "config": {"workload": WORKLOAD, "batch": shape.batch, "seqlen": shape.seqlen,
-                   "nheads": shape.nheads, "headdim": shape.headdim, "dstate": shape.dstate,
-                   "ngroups": shape.ngroups, "chunk": shape.chunk,
-                   "l2": f"rotating {nsets} input/output sets ({nsets * byts / 1e6:.0f} MB > 2x L2)",
+        "config": {"workload": WORKLOAD, "batch": full.batch, "seqlen": full.seqlen,
+                   "nheads": full.nheads, "headdim": full.headdim, "dstate": full.dstate,
+                   "ngroups": full.ngroups, "chunk": full.chunk,
+                   "l2": (f"inputs larger than L2 ({byts / 1e6:.0f} MB per rank)" if nsets == 1
+                          else f"rotating {nsets} input/output sets "
+                               f"({nsets * byts / 1e6:.0f} MB > 2x L2)"),
                    "launch": "K calls captured in one CUDA graph, timed as one replay",
-                   "parallelism": f"replicas x{world}"},
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
-                     "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
-                     "traffic": ncu_traffic("ssd_tc_scan_kernel", WORKLOAD),
-                     "peak_source": peaks["source"], "kernel": "ssd_tc_scan_kernel",
-                     "kernel_ms": kern_ms,
-                     "algorithmic_bytes": byts,
-                     "call_achieved": call_achieved,
-                     "call_frac": call_achieved / peaks["hbm_gbs"],
-                     "tensor_tflops": flops / (kern_ms * 1e-3) / 1e12},
-        "e2e": {"value": shape.tokens / e2e_s / 1e6, "unit": "Mtokens/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": launches * args.steps,
+                   "parallelism": (f"heads split over {world} GPUs ({shape.nheads} each)"
+                                   if world > 1 else "one GPU")},
+        "roofline": roof,
+        "e2e": {"value": full.tokens / e2e_s / 1e6, "unit": "Mtokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "how": "HostScanPipeline: pinned host inputs copied in, the scan, y and the "
+                       "final state copied out, consecutive steps overlapped"},
+        "gpu_launches": launches * args.steps * world,
         "clocks": clocks,
     }
     line.update(extra)
-    if not args.no_cpu:
-        v, cores, desc = cpu_oracle_sample(shape, target_s=args.cpu_seconds)
-        v1, desc1 = cpu_oracle_sample_one_core(shape)
+    if not args.no_cpu and world == 1:
+        v, cores, desc = cpu_oracle_sample(full, target_s=args.cpu_seconds)
+        v1, _, desc1 = cpu_oracle_sample(full, heads=4, target_s=0.0, cores=1, max_reps=1)
         line["cpu_baseline"] = {"value": v, "unit": "Mtokens/s", "cores": cores,
                                 "kind": "oracle", "sample": desc,
-                                "one_core": {"value": v1, "unit": "Mtokens/s", "sample": desc1}}
+                                "one_core": {"value": v1, "unit": "Mtokens/s", "cores": 1,
+                                             "sample": desc1}}
     print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
@@ -783,9 +847,13 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--quick", action="store_true", help="headline workload only")
-    ap.add_argument("--only", choices=["decode", "long"], default=None,
-                    help="run one secondary workload alone (for profiler captures)")
+    ap.add_argument("--only", choices=["decode", "decode_multi", "long", "130m", "370m"],
+                    default=None, help="run one workload alone (for profiler captures)")
     ap.add_argument("--decode-batch", type=int, default=16)
+    ap.add_argument("--decode-tokens", type=int, default=16,
+                    help="tokens per call of the --only decode_multi run")
+    ap.add_argument("--reference-heads", type=int, default=8,
+                    help="heads of the layer per step of the reference arm")
     ap.add_argument("--decode-state", choices=["f32", "bf16"], default="f32",
                     help="state storage of the --only decode run")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")

@@ -77,18 +77,24 @@ typedef enum {
     SSD_ALGO_AUTO = 0,
     SSD_ALGO_SIMT = 1,      /* exact-fp32 FFMA chunked scan, any shape */
     SSD_ALGO_TCGEN05 = 2    /* tcgen05/TMEM/TMA chunked scan: bf16 inputs, headdim 64,
-                               dstate 64 or 128 */
+                               dstate 128 */
 } ssd_algo;
 
-/* Bytes of device workspace a scan call needs for this shape on the CURRENT
- * device (the segment plan depends on its SM count), enough for every entry
- * point: on the tensor-core path it includes batch x seqlen x nheads floats
- * for the transformed step sizes, which only a call with a dt transform uses
- * (a call without one accepts a workspace that much smaller).  Returns 0 when
- * the shape needs none, and (size_t)-1 for invalid sizes. */
+/* Bytes of device workspace ssd_scan_fwd / ssd_scan_fwd_algo need for this
+ * shape on the CURRENT device (the segment plan depends on its SM count), for
+ * either input dtype (fp32 inputs need none; the figure is that of bf16
+ * inputs): the segment states and decays of the tensor-core path.  Returns 0
+ * when the shape needs none, and (size_t)-1 for invalid sizes. */
 size_t ssd_scan_workspace_bytes(int batch, int seqlen, int nheads, int headdim,
-                                int dstate, int ngroups, int chunk,
-                                ssd_dtype in_dtype);
+                                int dstate, int ngroups, int chunk);
+
+/* The exact workspace of a call with this input dtype and, when
+ * with_dt_transform != 0, a dt transform (ssd_scan_fwd_dt, ssd_scan_fwd_fused):
+ * on the tensor-core path a transform adds batch x seqlen x nheads floats for
+ * the transformed step sizes.  (size_t)-1 for invalid sizes. */
+size_t ssd_scan_fused_workspace_bytes(int batch, int seqlen, int nheads, int headdim,
+                                      int dstate, int ngroups, int chunk,
+                                      ssd_dtype in_dtype, int with_dt_transform);
 
 /* Number of kernel launches ssd_scan_fwd enqueues for this shape on the
  * current device (for launch accounting and CUDA-graph planning); -1 for
@@ -104,14 +110,21 @@ int ssd_scan_kernel_launches(int batch, int seqlen, int nheads, int headdim,
  *
  *   x, B, C     in_dtype device arrays (layouts above).
  *   dt, A       float.  D: float [nheads] or NULL (no skip term).
- *   chunk       the chunk length Q: one of 16, 32, 64, 128, 256.  The result
- *               does not depend on Q (the chunked form is an exact
- *               re-association of the recurrence); the kernels tile the
- *               sequence in their own block sizes.
+ *   chunk       the chunk length Q: one of 16, 32, 64, 128, 256, validated
+ *               and otherwise UNUSED.  The result does not depend on Q (the
+ *               chunked form is an exact re-association of the recurrence);
+ *               the kernels tile the sequence in their own block sizes (128
+ *               tokens on the tensor-core path, 64 on the SIMT path).
+ *   dt          any sign is accepted.  dt >= 0 (a time step) is the intended
+ *               use; with dt < 0 the recurrence grows instead of decaying,
+ *               and the tensor-core path stays exact only while that growth
+ *               inside one 128-token tile is below about e^60 (its mask
+ *               factors are fp32); the SIMT path has no such limit.
  *   init_state  float [batch][nheads][headdim][dstate] or NULL (zeros).
  *   y           in_dtype output.  final_state: float output or NULL.
  *   workspace   device scratch of at least ssd_scan_workspace_bytes() bytes
- *               (may be NULL when that is 0), 256-byte aligned.
+ *               (may be NULL when that is 0), 256-byte aligned; its contents
+ *               need no initialisation.
  * Requirements: all sizes > 0, nheads % ngroups == 0, dstate % 4 == 0,
  * dstate <= 256, base pointers 16-byte aligned.  seqlen may be any length
  * (the last block is ragged). */
@@ -144,9 +157,10 @@ ssd_status ssd_scan_fwd_algo(ssd_algo algo, const void *x, const float *dt,
  *   sp(u) = log(1 + e^u) when softplus != 0, else sp(u) = u.
  *
  * dt_bias: float [nheads] device array or NULL (no bias).  dt_min <= dt_max
- * (NaN rejected); use -INFINITY / INFINITY for no clamp.  The tensor-core
- * path needs the transformed dt >= 0 (softplus, or dt_min >= 0, ensures it).
- * The caller owns dt_bias; it is read during the call's kernels. */
+ * (NaN rejected); use -INFINITY / INFINITY for no clamp.  The sign rule of
+ * ssd_scan_fwd applies to the transformed dt (softplus, or dt_min >= 0, makes
+ * it a non-negative time step).  The caller owns dt_bias; it is read during
+ * the call's kernels. */
 typedef struct ssd_dt_transform {
     const float *dt_bias;
     int softplus;
@@ -155,7 +169,8 @@ typedef struct ssd_dt_transform {
 
 /* ssd_scan_fwd_algo with a dt transform (NULL = identity: exactly
  * ssd_scan_fwd_algo).  Returns SSD_ERR_INVALID_ARG when dt_min > dt_max or
- * either is NaN. */
+ * either is NaN.  With a transform the workspace is
+ * ssd_scan_fused_workspace_bytes(..., in_dtype, 1). */
 ssd_status ssd_scan_fwd_dt(ssd_algo algo, const void *x, const float *dt,
                            const float *A, const void *B, const void *C,
                            const float *D, const ssd_dt_transform *dt_transform,
@@ -197,7 +212,10 @@ ssd_status ssd_scan_fwd_varlen(ssd_algo algo, const void *x, const float *dt,
                                size_t workspace_bytes, cudaStream_t stream);
 
 /* Workspace bytes and kernel launches of ssd_scan_fwd_varlen for these
- * offsets on the current device ((size_t)-1 / -1 for invalid arguments). */
+ * offsets on the current device ((size_t)-1 / -1 for invalid arguments).  The
+ * workspace figure covers a call with a dt transform (total tokens x nheads
+ * floats for the transformed step sizes on the tensor-core path); a call
+ * without one uses that much less of it. */
 size_t ssd_scan_varlen_workspace_bytes(int nseq, const int *cu_seqlens_host,
                                        int nheads, int headdim, int dstate,
                                        int ngroups, int chunk, ssd_dtype in_dtype);
@@ -234,7 +252,7 @@ ssd_status ssd_scan_fwd_fused(ssd_algo algo, const void *x, const float *dt,
 ssd_status ssd_scan_profile_events(cudaEvent_t before, cudaEvent_t after);
 
 /* Size of the scratch array built into the library for ssd_scan_fwd_static. */
-#define SSD_STATIC_SCRATCH_BYTES (32u << 20)
+#define SSD_STATIC_SCRATCH_BYTES (64u << 20)
 
 /* ssd_scan_fwd for callers that cannot allocate device memory (the pages
  * have no counterpart: this exists for callers whose memory is fixed at
@@ -245,6 +263,8 @@ ssd_status ssd_scan_profile_events(cudaEvent_t before, cudaEvent_t after);
  * GPU that loads the library until the process exits.  Allocates nothing.
  *   - Returns SSD_ERR_WORKSPACE when the shape needs more scratch than
  *     SSD_STATIC_SCRATCH_BYTES (ssd_scan_workspace_bytes() tells how much).
+ *     The 2.7B-shaped 65536-token layer (80 heads, 45 MiB of segment states
+ *     on a 152-SM GB300) fits.
  *   - The first call on each device looks up the scratch address for that
  *     device; make that first call before any stream capture.
  *   - All calls share the one scratch array: calls whose work overlaps on the
@@ -307,6 +327,24 @@ const char *ssd_status_string(ssd_status s);
 /* Reads and clears the device error word on the current device
  * (synchronises the device).  SSD_OK when no kernel reported a fault. */
 ssd_status ssd_last_device_error(void);
+
+/* Test hook for the bounded device-side waits (the pages have no
+ * counterpart).  Every later launch of the tensor-core scan reads the
+ * setting; it is process-wide and not synchronised with calls in flight on
+ * other host threads.
+ *   fault          SSD_FAULT_NONE: normal operation.  SSD_FAULT_WITHHOLD_SIGNAL:
+ *                  in the CTAs of each sequence's first segment, the warp that
+ *                  computes the decay factors withholds its first "factors
+ *                  ready" signal, so the wait for it runs out; the CTA then
+ *                  lets its issued copies and tensor-core products complete,
+ *                  frees its tensor memory and exits, and the device error
+ *                  word reads SSD_ERR_TIMEOUT.  The outputs of that call are
+ *                  undefined.
+ *   wait_limit_ns  limit of every bounded wait in those kernels; 0 restores
+ *                  the default (2 s).
+ * Returns SSD_ERR_INVALID_ARG for an unknown fault. */
+typedef enum { SSD_FAULT_NONE = 0, SSD_FAULT_WITHHOLD_SIGNAL = 1 } ssd_fault;
+ssd_status ssd_debug_inject_fault(ssd_fault fault, unsigned long long wait_limit_ns);
 
 #ifdef __cplusplus
 }

@@ -20,6 +20,9 @@ from ._binding import (  # noqa: F401
     lib_path,
     load,
     last_device_error,
+    debug_inject_fault,
+    FAULT_NONE,
+    FAULT_WITHHOLD_SIGNAL,
     scan_fwd,
     scan_fwd_host,
     scan_fwd_varlen,

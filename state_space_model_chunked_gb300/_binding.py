@@ -12,6 +12,7 @@ _LIB_PATH = os.path.join(_HERE, "_lib", "libssd.so")
 
 EXPORTED_SYMBOLS = (
     "ssd_scan_workspace_bytes",
+    "ssd_scan_fused_workspace_bytes",
     "ssd_scan_kernel_launches",
     "ssd_scan_fwd",
     "ssd_scan_fwd_algo",
@@ -27,6 +28,7 @@ EXPORTED_SYMBOLS = (
     "ssd_state_update_fused",
     "ssd_status_string",
     "ssd_last_device_error",
+    "ssd_debug_inject_fault",
 )
 
 ALGO_AUTO, ALGO_SIMT, ALGO_TCGEN05 = 0, 1, 2
@@ -71,7 +73,11 @@ def load():
                 "`python -m state_space_model_chunked_gb300.build` (needs nvcc)")
         lib = ctypes.CDLL(_LIB_PATH)
         lib.ssd_scan_workspace_bytes.restype = _sz
-        lib.ssd_scan_workspace_bytes.argtypes = [_int] * 7 + [_int]
+        lib.ssd_scan_workspace_bytes.argtypes = [_int] * 7
+        lib.ssd_scan_fused_workspace_bytes.restype = _sz
+        lib.ssd_scan_fused_workspace_bytes.argtypes = [_int] * 7 + [_int, _int]
+        lib.ssd_debug_inject_fault.restype = _int
+        lib.ssd_debug_inject_fault.argtypes = [_int, ctypes.c_ulonglong]
         lib.ssd_scan_kernel_launches.restype = _int
         lib.ssd_scan_kernel_launches.argtypes = [_int] * 7 + [_int]
         scan_args = [_vp] * 6 + [_int] * 8 + [_vp, _vp, _vp, _vp, _sz, _vp]
@@ -144,15 +150,17 @@ def _need(t, name, dtype=None, device=None, shape=None):
 
 
 def scan_workspace_bytes(batch, seqlen, nheads, headdim, dstate, ngroups, chunk,
-                         dtype=torch.bfloat16, device=None):
+                         dtype=torch.bfloat16, device=None, dt_transform=False):
+    """Workspace bytes of a scan_fwd call of this shape and input dtype on
+    the device, with or without a dt transform."""
     lib = load()
     code = _BF16 if dtype == torch.bfloat16 else _F32
     dev = torch.device("cuda") if device is None else torch.device(device)
     with torch.cuda.device(dev):
-        n = lib.ssd_scan_workspace_bytes(batch, seqlen, nheads, headdim, dstate,
-                                         ngroups, chunk, code)
+        n = lib.ssd_scan_fused_workspace_bytes(batch, seqlen, nheads, headdim, dstate,
+                                               ngroups, chunk, code, 1 if dt_transform else 0)
     if n == ctypes.c_size_t(-1).value:
-        raise SsdError("ssd_scan_workspace_bytes", 1, "invalid sizes")
+        raise SsdError("ssd_scan_fused_workspace_bytes", 1, "invalid sizes")
     return int(n)
 
 
@@ -248,10 +256,12 @@ def scan_fwd(x, dt, A, B, C, D=None, chunk=256, init_state=None, *, y=None,
     elif final_state is not None:
         _need(final_state, "final_state", torch.float32, dev, (b, H, P, N))
     code = _dtype_code(x)
+    with_dt = dt_bias is not None or dt_softplus or dt_limit is not None
     with torch.cuda.device(dev):
-        need = lib.ssd_scan_workspace_bytes(b, L, H, P, N, G, chunk, code)
+        need = lib.ssd_scan_fused_workspace_bytes(b, L, H, P, N, G, chunk, code,
+                                                  1 if with_dt else 0)
         if need == ctypes.c_size_t(-1).value:
-            raise SsdError("ssd_scan_workspace_bytes", 1, "invalid sizes")
+            raise SsdError("ssd_scan_fused_workspace_bytes", 1, "invalid sizes")
         if need > 0 and (workspace is None or workspace.numel() * workspace.element_size() < need):
             workspace = torch.empty(need, dtype=torch.uint8, device=dev)
         wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
@@ -498,3 +508,13 @@ def last_device_error():
     """Reads and clears the device error word (synchronises the device)."""
     rc = load().ssd_last_device_error()
     _check("ssd_last_device_error", rc)
+
+
+FAULT_NONE, FAULT_WITHHOLD_SIGNAL = 0, 1
+
+
+def debug_inject_fault(fault=FAULT_NONE, wait_limit_ns=0):
+    """Test hook of the bounded device waits (ssd_debug_inject_fault):
+    FAULT_WITHHOLD_SIGNAL makes the next tensor-core scans time out after
+    wait_limit_ns; FAULT_NONE (and 0 = the default limit) restores them."""
+    _check("ssd_debug_inject_fault", load().ssd_debug_inject_fault(int(fault), int(wait_limit_ns)))

@@ -39,6 +39,8 @@ int current_sm_count() {
 bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
 SsdProfileEvents g_profile = {nullptr, nullptr};
+// test hooks (ssd_debug_inject_fault): written by the host between calls
+SsdDebug g_debug = {0, kSsdDefaultWaitNs};
 
 bool valid_chunk(int q) {
     return q == 16 || q == 32 || q == 64 || q == 128 || q == 256;
@@ -146,7 +148,24 @@ ssd_status scan_any(ssd_algo algo, const void *x, const float *dt, const float *
     return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
 }
 
+// Workspace of one batched call on the current device: the tensor-core
+// plan's segment states and decays, plus the transformed step sizes only for
+// a call with a dt transform; fp32 inputs take the SIMT path, which needs none.
+size_t scan_workspace(int batch, int seqlen, int nheads, int headdim, int dstate, int ngroups,
+                      int chunk, ssd_dtype in_dtype, bool with_dt) {
+    if (batch <= 0 || seqlen <= 0 || nheads <= 0 || headdim <= 0 || dstate <= 0 ||
+        ngroups <= 0 || nheads % ngroups != 0 || !valid_chunk(chunk))
+        return (size_t)-1;
+    if (in_dtype != SSD_BF16) return 0;
+    const SsdTcPlan plan = ssd_tc_plan(batch, seqlen, nheads, headdim, dstate, ngroups,
+                                       current_sm_count());
+    if (!plan.supported) return 0;
+    return with_dt ? plan.workspace : plan.dt_offset;
+}
+
 }  // namespace
+
+SsdDebug ssd_debug_config() { return g_debug; }
 
 extern "C" {
 
@@ -182,14 +201,23 @@ ssd_status ssd_last_device_error(void) {
 }
 
 size_t ssd_scan_workspace_bytes(int batch, int seqlen, int nheads, int headdim, int dstate,
-                                int ngroups, int chunk, ssd_dtype in_dtype) {
-    if (batch <= 0 || seqlen <= 0 || nheads <= 0 || headdim <= 0 || dstate <= 0 ||
-        ngroups <= 0 || nheads % ngroups != 0 || !valid_chunk(chunk))
-        return (size_t)-1;
-    if (in_dtype != SSD_BF16) return 0;
-    const SsdTcPlan plan = ssd_tc_plan(batch, seqlen, nheads, headdim, dstate, ngroups,
-                                       current_sm_count());
-    return plan.supported ? plan.workspace : 0;
+                                int ngroups, int chunk) {
+    return scan_workspace(batch, seqlen, nheads, headdim, dstate, ngroups, chunk, SSD_BF16,
+                          false);
+}
+
+size_t ssd_scan_fused_workspace_bytes(int batch, int seqlen, int nheads, int headdim,
+                                      int dstate, int ngroups, int chunk, ssd_dtype in_dtype,
+                                      int with_dt_transform) {
+    return scan_workspace(batch, seqlen, nheads, headdim, dstate, ngroups, chunk, in_dtype,
+                          with_dt_transform != 0);
+}
+
+ssd_status ssd_debug_inject_fault(ssd_fault fault, unsigned long long wait_limit_ns) {
+    if (fault != SSD_FAULT_NONE && fault != SSD_FAULT_WITHHOLD_SIGNAL) return SSD_ERR_INVALID_ARG;
+    g_debug.fault = (int)fault;
+    g_debug.wait_ns = wait_limit_ns ? wait_limit_ns : kSsdDefaultWaitNs;
+    return SSD_OK;
 }
 
 int ssd_scan_kernel_launches(int batch, int seqlen, int nheads, int headdim, int dstate,

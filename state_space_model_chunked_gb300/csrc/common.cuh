@@ -17,6 +17,13 @@ __device__ __forceinline__ void ssd_report(unsigned int *err, unsigned int code)
     if (err) atomicCAS(err, 0u, code);
 }
 
+// Limit of a bounded device-side wait unless the host sets another one
+// (nanoseconds of the global timer).
+constexpr unsigned long long kSsdDefaultWaitNs = 2000000000ull;
+// Host-set fault injection for tests of the timeout path (ssd_fault in the C
+// ABI): the tensor-core scan kernel's factor warp withholds its first signal.
+constexpr int kSsdFaultWithholdSignal = 1;
+
 // The neighbouring steps of a Mamba-2 layer fused into the kernels.
 // Input side, the transform of the raw step size (the usual parameterisation
 // of a positive step from the input projection's output):

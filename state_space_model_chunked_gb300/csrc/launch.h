@@ -15,6 +15,14 @@ cudaError_t ssd_launch_decode(void *state, bool bf16_state, const void *x, const
 
 size_t ssd_simt_smem_bytes(int N);
 
+// Test hooks of the ABI layer: the fault to inject (0 = none) and the limit
+// of every bounded device wait, read by the launchers at each launch.
+struct SsdDebug {
+    int fault;
+    unsigned long long wait_ns;
+};
+SsdDebug ssd_debug_config();
+
 // Events recorded around the kernel that writes y (null = none).
 struct SsdProfileEvents {
     cudaEvent_t before, after;

@@ -54,8 +54,10 @@ extern "C" ssd_status ssd_scan_fwd_static(const void *x, const float *dt, const 
                                           int headdim, int dstate, int ngroups, int chunk,
                                           const float *init_state, void *y, float *final_state,
                                           cudaStream_t stream) {
-    const size_t need = ssd_scan_workspace_bytes(batch, seqlen, nheads, headdim, dstate,
-                                                 ngroups, chunk, in_dtype);
+    // this entry point takes no dt transform: the scratch it needs excludes
+    // the transformed step sizes
+    const size_t need = ssd_scan_fused_workspace_bytes(batch, seqlen, nheads, headdim, dstate,
+                                                       ngroups, chunk, in_dtype, 0);
     if (need == (size_t)-1) return SSD_ERR_INVALID_ARG;
     if (need > (size_t)SSD_STATIC_SCRATCH_BYTES) return SSD_ERR_WORKSPACE;
     void *scratch = scratch_address();

@@ -10,17 +10,18 @@
 // space or drop a rank.  Here every step of a 128-token tile stays on chip:
 //
 //   G     = C . B^T                (tcgen05, smem x smem -> TMEM fp32)
-//   M     = G o exp(a_t - a_s) dt_s, s <= t, plus D on the diagonal
+//   M     = G o exp(a_t - a_s) dt_s, s <= t
 //                                  (TMEM -> registers -> TMEM as bf16, in place)
 //   Yd    = M . X                  (tcgen05 with A read from TMEM)
 //   Yo    = C . H_prev^T           (off-diagonal term from the entering state)
 //   H    <- exp(a_end) H + B^T . (w o X),  w_s = exp(a_end - a_s) dt_s
-//   y     = Yd + exp(a_t) Yo       (epilogue, bf16 store)
+//   y     = Yd + exp(a_t) Yo + D x (epilogue, bf16 store)
 //
-// The D skip is folded into the mask diagonal (M[t][t] += D): the skip is the
-// s = t term of the same contraction.  Exponents are always differences or
-// non-positive partial sums; the mask uses exp(a_t + u_s) with
-// u_s = log(dt_s) - a_s, which needs dt >= 0 (a time step).
+// Exponents are differences of the chunk-local cumsum a, taken inside 32-token
+// blocks (the mask factors) or from a tile's start or end: with dt >= 0 and
+// A <= 0 none is positive.  dt enters every factor as a multiplier, so its
+// sign is not assumed; a negative dt makes the factors grow, and they stay
+// finite while that growth inside a tile stays below about e^60.
 //
 // Parallelism over the sequence: a segment is a run of consecutive tiles
 // handled by one CTA with the state carried in TMEM.  When a sequence has more
@@ -79,7 +80,6 @@ constexpr int kSegFacWarp = 2 + kSegXWarps;  // segment kernel: token weight war
 constexpr int kSegThreads = 64 + 32 * kSegXWarps + 32;
 // segment kernel: B + X stages (4 heads per CTA: 96 KB stages, two fit)
 constexpr int seg_stages(int hg) { return hg == 4 ? 2 : 3; }
-constexpr uint64_t kWaitNs = 2000000000ull;
 // Largest decay (in log units) across one 32-token block for which the mask's
 // diagonal block uses the factored form (its R_t factor stays below e^60).
 constexpr float kMaxBlockDecay = 60.f;
@@ -103,7 +103,7 @@ constexpr uint32_t kIdS = idesc_bf16_f32(128, 64, true, true);      // B^T . Xt
 constexpr uint32_t kIdY = idesc_bf16_f32(128, 64, false, true);     // M(TMEM) . X
 
 // control-region offsets (bytes)
-constexpr uint32_t kOffTslot = 192;       // (barriers occupy bytes 0 .. 151)
+constexpr uint32_t kOffTslot = 192;       // (barriers occupy bytes 0 .. 159)
 constexpr uint32_t kOffAbort = 196;
 // scan kernel factor slot, written by the factor warp for one tile at a time
 constexpr uint32_t kOffAch = 256;         // float[2][4]: a at the end of each 32-token block
@@ -125,6 +125,8 @@ struct TcArgs {
     const int *cu;
     const int *item0, *fslot0;
     int nseq;
+    uint64_t wait_ns;         // limit of every bounded wait (ns)
+    int fault;                // host-set fault injection (SSD_FAULT_*), 0 = none
 };
 
 // Where one CTA's segment lies: its sequence, the sequence's first row in the
@@ -252,10 +254,13 @@ ssd_varlen_plan_kernel(const int *__restrict__ cu, int nseq, int seg_tiles, int 
     }
 }
 
+// A bounded wait on an mbarrier phase.  After any wait of the CTA has run out
+// (abort_flag set) every later wait returns false at once, and the caller
+// leaves its loop: the CTA then drains what it has in flight and exits.
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int *abort_flag,
-                                         unsigned int *err) {
+                                         unsigned int *err, uint64_t limit_ns) {
     if (*abort_flag) return false;
-    if (mbar_wait(bar, parity, kWaitNs)) return true;
+    if (mbar_wait(bar, parity, limit_ns)) return true;
     *abort_flag = 1;
     ssd_report(err, SSD_DEVERR_TIMEOUT);
     return false;
@@ -263,9 +268,21 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
 
 // Warp-uniform wait (every lane polls; the warp proceeds only if all saw it).
 __device__ __forceinline__ bool wait_bar_warp(uint32_t bar, uint32_t parity,
-                                              volatile int *abort_flag, unsigned int *err) {
-    const bool ok = wait_bar(bar, parity, abort_flag, err);
+                                              volatile int *abort_flag, unsigned int *err,
+                                              uint64_t limit_ns) {
+    const bool ok = wait_bar(bar, parity, abort_flag, err, limit_ns);
     return __all_sync(0xffffffffu, ok);
+}
+
+// Drain wait: for the CTA's own copies or tensor-core work to complete before
+// it frees tensor memory and exits.  Unlike wait_bar it does not give up when
+// another wait has run out (that work completes regardless of the other
+// warps); it is bounded all the same, and records a timeout if it runs out.
+__device__ __forceinline__ void drain_bar(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                          unsigned int *err, uint64_t limit_ns) {
+    if (mbar_wait(bar, parity, limit_ns)) return;
+    *abort_flag = 1;
+    ssd_report(err, SSD_DEVERR_TIMEOUT);
 }
 
 // Byte offset of element (row, col) in a 128-byte-swizzled tile whose rows are
@@ -353,7 +370,8 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
     //           6 g_full; 7 m_ready; 8 hx_ready; 9 hx_free; 10 y_full;
     //           11 y_done (Yd / Yo read, y staged over C); 12 g_free (the masks
     //           in TMEM have been consumed); 13 fac_ready (factor slot written);
-    //           14,15 fullX[stage]; 16,17 emptyX[stage]
+    //           14,15 fullX[stage]; 16,17 emptyX[stage]; 18, 19 drain of issuer
+    //           A's / issuer B's tensor-core work before the CTA exits
     auto bar = [&](int i) { return sbase + 8u * (uint32_t)i; };
     uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + kOffTslot);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kOffAbort);
@@ -391,6 +409,8 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
         mbar_init(bar(11), kXWarps);
         mbar_init(bar(12), HG);                // one commit per masked-product issuer
         mbar_init(bar(13), 1);
+        mbar_init(bar(18), 1);
+        mbar_init(bar(19), 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -411,6 +431,8 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
             tma_prefetch_desc(&mapC);
             tma_prefetch_desc(&mapB);
             tma_prefetch_desc(&mapX);
+            // the last tile whose X, B and C loads were issued, for the drain
+            int lastX = -1, lastB = -1, lastC = -1;
             for (int it = 0; it < ntile; ++it) {
                 const int stage = it & 1;
                 const int t0 = (k0 + it) * kTile;
@@ -419,8 +441,9 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
                 // then C (by the y store two tiles ago).
                 const uint32_t stg = tiles_base + stage * kStage;
                 // X of this tile
-                if (it >= 2 && !wait_bar(bar(16 + stage), ((it >> 1) - 1) & 1, abort_flag, a.err))
+                if (it >= 2 && !wait_bar(bar(16 + stage), ((it >> 1) - 1) & 1, abort_flag, a.err, a.wait_ns))
                     break;
+                lastX = it;
                 mbar_arrive_expect_tx(bar(14 + stage), HG * kXBytes);
 #pragma unroll
                 for (int h = 0; h < HG; ++h)
@@ -435,17 +458,28 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
                 }
                 // B of this tile (single buffer: free once the previous tile's state
                 // update has read it)
-                if (it >= 1 && !wait_bar(bar(5), (it - 1) & 1, abort_flag, a.err)) break;
+                if (it >= 1 && !wait_bar(bar(5), (it - 1) & 1, abort_flag, a.err, a.wait_ns)) break;
+                lastB = it;
                 mbar_arrive_expect_tx(bar(4), kBBytes);
                 tma_load_4d(b_base, &mapB, bar(4), 0, g, trow + t0, tb);
                 tma_load_4d(b_base + kBlk, &mapB, bar(4), 64, g, trow + t0, tb);
                 // C of this tile (stage last used two tiles ago)
-                if (it >= 2 && !wait_bar(bar(2 + stage), ((it >> 1) - 1) & 1, abort_flag, a.err))
+                if (it >= 2 && !wait_bar(bar(2 + stage), ((it >> 1) - 1) & 1, abort_flag, a.err, a.wait_ns))
                     break;
+                lastC = it;
                 mbar_arrive_expect_tx(bar(stage), kCBytes);
                 tma_load_4d(stg, &mapC, bar(stage), 0, g, trow + t0, tb);
                 tma_load_4d(stg + kBlk, &mapC, bar(stage), 64, g, trow + t0, tb);
             }
+            // every load this thread issued has landed before the CTA exits (after
+            // a wait ran out, its consumers may never have waited for it).  Loads
+            // go out tile by tile, so the last two tiles of X and C (one per
+            // stage) and the last of B hold the only phases that can be pending.
+            for (int k = lastX; k >= 0 && k >= lastX - 1; --k)
+                drain_bar(bar(14 + (k & 1)), (k >> 1) & 1, abort_flag, a.err, a.wait_ns);
+            for (int k = lastC; k >= 0 && k >= lastC - 1; --k)
+                drain_bar(bar(k & 1), (k >> 1) & 1, abort_flag, a.err, a.wait_ns);
+            if (lastB >= 0) drain_bar(bar(4), lastB & 1, abort_flag, a.err, a.wait_ns);
         }
     } else if (warp == kIssuerA) {
         // ------------------------------------------------------ MMA issuer
@@ -465,10 +499,10 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
                 const int stage = it & 1;
                 const uint64_t so = stage ? (uint64_t)(kStage >> 4) : 0ull;
                 const uint64_t cK = cK0 + so;
-                if (!wait_bar(bar(stage), (it >> 1) & 1, abort_flag, a.err)) break;
-                if (!wait_bar(bar(4), it & 1, abort_flag, a.err)) break;
+                if (!wait_bar(bar(stage), (it >> 1) & 1, abort_flag, a.err, a.wait_ns)) break;
+                if (!wait_bar(bar(4), it & 1, abort_flag, a.err, a.wait_ns)) break;
                 // the previous tile's masks (in the G columns) must have been read
-                if (it > 0 && !wait_bar(bar(12), (it - 1) & 1, abort_flag, a.err)) break;
+                if (it > 0 && !wait_bar(bar(12), (it - 1) & 1, abort_flag, a.err, a.wait_ns)) break;
                 tc_fence_after();
                 // G = C . B^T  (M = 128 tokens t, N = 128 tokens s, K = 128 n)
 #pragma unroll
@@ -479,14 +513,14 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
                 mma_commit(bar(6));
                 // all heads' state update: H += B^T . Xt (chunk state onto the decayed
                 // state), then the off-diagonal term Yo = C . Hb from the entering state
-                if (!wait_bar(bar(8), it & 1, abort_flag, a.err)) break;
+                if (!wait_bar(bar(8), it & 1, abort_flag, a.err, a.wait_ns)) break;
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
                     mma_ss(tmem + kColH, bMN + (uint64_t)(kk * 128), xtD + (uint64_t)(kk * 128),
                            kIdSAll, 1);
                 mma_commit(bar(5));                     // B may be reloaded
-                if (it > 0 && !wait_bar(bar(11), (it - 1) & 1, abort_flag, a.err)) break;
+                if (it > 0 && !wait_bar(bar(11), (it - 1) & 1, abort_flag, a.err, a.wait_ns)) break;
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
@@ -497,8 +531,8 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
                 mma_commit(bar(2 + stage));
                 if (HG == 2) {
                     // the second head's masked product, split off issuer B's stream
-                    if (!wait_bar(bar(14 + stage), (it >> 1) & 1, abort_flag, a.err)) break;
-                    if (!wait_bar(bar(7), it & 1, abort_flag, a.err)) break;
+                    if (!wait_bar(bar(14 + stage), (it >> 1) & 1, abort_flag, a.err, a.wait_ns)) break;
+                    if (!wait_bar(bar(7), it & 1, abort_flag, a.err, a.wait_ns)) break;
                     tc_fence_after();
                     const uint64_t xD = xlastD + (stage ? (uint64_t)(kStage >> 4) : 0ull);
 #pragma unroll
@@ -512,6 +546,9 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
                 }
                 mma_commit(bar(10));
             }
+            // every product this thread issued is complete before TMEM is freed
+            mma_commit(bar(18));
+            drain_bar(bar(18), 0, abort_flag, a.err, a.wait_ns);
         }
     } else if (warp == kIssuerB) {
         // ------------------------------------------------ MMA issuer B
@@ -536,11 +573,11 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
                 const uint64_t xD = x00 + (stage ? (uint64_t)(kStage >> 4) : 0ull);
                 if (it > 0) {
                     // tile it-1's y is staged and its Yd read: store it, reuse Yd
-                    if (!wait_bar(bar(11), (it - 1) & 1, abort_flag, a.err)) break;
+                    if (!wait_bar(bar(11), (it - 1) & 1, abort_flag, a.err, a.wait_ns)) break;
                     store_y(it - 1);
                 }
-                if (!wait_bar(bar(14 + stage), (it >> 1) & 1, abort_flag, a.err)) break;
-                if (!wait_bar(bar(7), it & 1, abort_flag, a.err)) break;
+                if (!wait_bar(bar(14 + stage), (it >> 1) & 1, abort_flag, a.err, a.wait_ns)) break;
+                if (!wait_bar(bar(7), it & 1, abort_flag, a.err, a.wait_ns)) break;
                 if (it > 0) {
                     bulk_wait_read<0>();
                     mbar_arrive(bar(2 + (stage ^ 1)));       // tile it-1's C buffer
@@ -557,9 +594,11 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
                 mma_commit(bar(10));
             }
             if (it == ntile && ntile > 0 &&
-                wait_bar(bar(11), (ntile - 1) & 1, abort_flag, a.err))
+                wait_bar(bar(11), (ntile - 1) & 1, abort_flag, a.err, a.wait_ns))
                 store_y(ntile - 1);
             bulk_wait_all();                                 // y stores complete before exit
+            mma_commit(bar(19));
+            drain_bar(bar(19), 0, abort_flag, a.err, a.wait_ns);
         }
     } else if (warp == fac_warp) {
         // ------------------------------------------------------ decay factors
@@ -616,7 +655,7 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
                 for (int i = 0; i < 4; ++i) fv[h][i] = __expf(ae - fa[h][i]) * dn[h][i];
             }
         };
-        auto publish = [&]() {
+        auto publish = [&](bool first) {
 #pragma unroll
             for (int h = 0; h < HG; ++h) {
                 *reinterpret_cast<float4 *>(at_s + h * kTile + 4 * lane) =
@@ -634,19 +673,23 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
                 ach_s[lane] = e;
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(13));
+            // fault injection (host-set, tests only): the first segment's first
+            // signal is withheld, so the transform warps' wait for it runs out
+            const bool withhold = first && a.fault == kSsdFaultWithholdSignal && sigma == 0;
+            if (lane == 0 && !withhold) mbar_arrive(bar(13));
         };
         if (ntile > 0) {
             load_dt4(0);
             factors(0);
-            publish();
+            publish(true);
             if (ntile > 1) load_dt4(1);
         }
         for (int it = 0; it + 1 < ntile; ++it) {
             factors(it + 1);                                 // tile it + 1
             if (it + 2 < ntile) load_dt4(it + 2);            // in flight meanwhile
-            wait_bar_warp(bar(7), it & 1, abort_flag, a.err);       // masks of tile it built
-            publish();
+            if (!wait_bar_warp(bar(7), it & 1, abort_flag, a.err, a.wait_ns))   // masks of tile it built
+                break;
+            publish(false);
         }
     } else {
         // ------------------------------------------- transform / epilogue
@@ -664,8 +707,8 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
         // tile's), a_t, the tile's 32-block ends a_e(j) and the state weight
         // w_t = exp(a_end - a_t) dt_t
         float at[HG], ach[HG][4], wt[HG];
-        auto load_factors = [&](int it) {
-            wait_bar_warp(bar(13), it & 1, abort_flag, a.err);
+        auto load_factors = [&](int it) -> bool {
+            if (!wait_bar_warp(bar(13), it & 1, abort_flag, a.err, a.wait_ns)) return false;
 #pragma unroll
             for (int h = 0; h < HG; ++h) {
                 const float4 e = *reinterpret_cast<const float4 *>(ach_s + 4 * h);
@@ -677,14 +720,17 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
                 const float aq = q == 0 ? e.x : (q == 1 ? e.y : (q == 2 ? e.z : e.w));
                 wt[h] = v_s[h * kTile + row] * __expf(e.w - aq);
             }
+            return true;
         };
 
         // ---- all heads of tile it: entering state -> bf16 operand (MN-major rows n),
         //      state scaled by the tile decay, and Xt = w o X
-        auto prep_tile = [&](int it) {
+        auto prep_tile = [&](int it) -> bool {
             const uint8_t *stg_ptr = tiles_ptr + (it & 1) * kStage;
-            wait_bar_warp(bar(14 + (it & 1)), (it >> 1) & 1, abort_flag, a.err);   // X landed
-            if (it > 0) wait_bar_warp(bar(9), (it - 1) & 1, abort_flag, a.err);
+            if (!wait_bar_warp(bar(14 + (it & 1)), (it >> 1) & 1, abort_flag, a.err, a.wait_ns))
+                return false;                                                   // X landed
+            if (it > 0 && !wait_bar_warp(bar(9), (it - 1) & 1, abort_flag, a.err, a.wait_ns))
+                return false;
             tc_fence_after();
             if (it == 0 && sigma > 0) griddep_wait();   // entering states of later segments
 #pragma unroll
@@ -736,15 +782,14 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(8));
+            return true;
         };
 
         // Software pipeline: the next tile's state prep runs while the tensor core
-        // finishes this tile, then this tile's epilogue.
-        if (ntile > 0) {
-            load_factors(0);
-            prep_tile(0);
-        }
-        for (int it = 0; it < ntile; ++it) {
+        // finishes this tile, then this tile's epilogue.  A wait that fails (one
+        // of the CTA's waits ran out) ends the loop.
+        bool ok = ntile > 0 && load_factors(0) && prep_tile(0);
+        for (int it = 0; ok && it < ntile; ++it) {
             const int t0 = (k0 + it) * kTile;
             const int stage = it & 1;
             const uint8_t *stg_ptr = tiles_ptr + stage * kStage;
@@ -756,7 +801,7 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
             //      the diagonal both factors are <= 1; on the diagonal block R_t is
             //      >= 1 but bounded by the block's own decay, and a block whose decay
             //      exceeds kMaxBlockDecay falls back to one exponential per element.
-            wait_bar_warp(bar(6), it & 1, abort_flag, a.err);
+            if (!wait_bar_warp(bar(6), it & 1, abort_flag, a.err, a.wait_ns)) break;
             tc_fence_after();
             {
                 const int j = wg;
@@ -780,7 +825,7 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
                                 tok < w_len()
                                     ? a.dt[(w_grow0() + tok) * a.H + h0 + hh]
                                     : 0.f;
-                            return d > 0.f ? __expf(at[hh] - ah[s] + __logf(d)) : 0.f;
+                            return __expf(at[hh] - ah[s]) * d;
                         };
 #pragma unroll
                         for (int e = 0; e < 16; ++e) {
@@ -825,10 +870,7 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
             float e_at_t[HG];
 #pragma unroll
             for (int h = 0; h < HG; ++h) e_at_t[h] = __expf(at[h]);
-            if (it + 1 < ntile) {
-                load_factors(it + 1);
-                prep_tile(it + 1);
-            }
+            if (it + 1 < ntile && !(load_factors(it + 1) && prep_tile(it + 1))) break;
 
             // ---- epilogue: y = Yd + exp(a_t) Yo + D x, staged as bf16 in this
             //      stage's C blocks (free once the tile's off-diagonal product is
@@ -852,7 +894,7 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
                     for (int q = 0; q < np / 8; ++q) zv[q] = *reinterpret_cast<const uint4 *>(zrow + 8 * q);
                 }
             }
-            wait_bar_warp(bar(10), it & 1, abort_flag, a.err);
+            if (!wait_bar_warp(bar(10), it & 1, abort_flag, a.err, a.wait_ns)) break;
             tc_fence_after();
             {
                 // selects, not dynamic indexing (which would move the arrays to local memory)
@@ -1023,11 +1065,13 @@ ssd_tc_segment_kernel(const __grid_constant__ CUtensorMap mapB,
         if (lane == 0) {
             tma_prefetch_desc(&mapB);
             tma_prefetch_desc(&mapX);
+            int issued = 0;
             for (int it = 0; it < ntile; ++it) {
                 const int stage = it % kStages;
                 if (it >= kStages &&
-                    !wait_bar(bar(3 + stage), ((it / kStages) - 1) & 1, abort_flag, a.err))
+                    !wait_bar(bar(3 + stage), ((it / kStages) - 1) & 1, abort_flag, a.err, a.wait_ns))
                     break;
+                issued = it + 1;
                 const uint32_t stg = tiles_base + stage * kStage;
                 const int t0 = (k1 - 1 - it) * kTile;
                 mbar_arrive_expect_tx(bar(stage), kStage);
@@ -1037,6 +1081,12 @@ ssd_tc_segment_kernel(const __grid_constant__ CUtensorMap mapB,
                 for (int h = 0; h < HG; ++h)
                     tma_load_4d(stg + kBBytes + h * kXBytes, &mapX, bar(stage), 0, h0 + h,
                                 trow + t0, tb);
+            }
+            // every issued load has landed before the CTA exits: the last load of
+            // each stage (tile issued - 1 - i) completes that stage's phases
+            for (int i = 0; i < kStages && i < issued; ++i) {
+                const int it = issued - 1 - i;
+                drain_bar(bar(it % kStages), (it / kStages) & 1, abort_flag, a.err, a.wait_ns);
             }
         }
     } else if (warp == 1) {
@@ -1048,7 +1098,7 @@ ssd_tc_segment_kernel(const __grid_constant__ CUtensorMap mapB,
             for (int it = 0; it < ntile; ++it) {
                 const int stage = it % kStages;
                 const uint64_t so = (uint64_t)((stage * kStage) >> 4);
-                if (!wait_bar(bar(6 + stage), (it / kStages) & 1, abort_flag, a.err)) break;
+                if (!wait_bar(bar(6 + stage), (it / kStages) & 1, abort_flag, a.err, a.wait_ns)) break;
                 tc_fence_after();
                 // all heads at once: F += B^T . [w o X_0 | w o X_1]  (N = 64 * HG)
 #pragma unroll
@@ -1058,6 +1108,7 @@ ssd_tc_segment_kernel(const __grid_constant__ CUtensorMap mapB,
                 mma_commit(bar(3 + stage));
             }
             mma_commit(bar(12));
+            drain_bar(bar(12), 0, abort_flag, a.err, a.wait_ns);   // all products complete
         }
     } else if (warp == kSegFacWarp) {
         // ------------------------------------------------- token weights
@@ -1121,8 +1172,9 @@ ssd_tc_segment_kernel(const __grid_constant__ CUtensorMap mapB,
                 suf[h] += tot;
             }
             // the slot was last read by the scaling of tile it - kStages
-            if (it >= kStages)
-                wait_bar_warp(bar(6 + stage), ((it / kStages) - 1) & 1, abort_flag, a.err);
+            if (it >= kStages &&
+                !wait_bar_warp(bar(6 + stage), ((it / kStages) - 1) & 1, abort_flag, a.err, a.wait_ns))
+                break;
             float *slot = w_ring + stage * HG * kTile;
 #pragma unroll
             for (int h = 0; h < HG; ++h)
@@ -1146,8 +1198,10 @@ ssd_tc_segment_kernel(const __grid_constant__ CUtensorMap mapB,
         for (int it = 0; it < ntile; ++it) {
             const int stage = it % kStages;
             uint8_t *stg_ptr = tiles_ptr + stage * kStage;
-            wait_bar_warp(bar(9 + stage), (it / kStages) & 1, abort_flag, a.err);   // weights
-            wait_bar_warp(bar(stage), (it / kStages) & 1, abort_flag, a.err);       // X landed
+            if (!wait_bar_warp(bar(9 + stage), (it / kStages) & 1, abort_flag, a.err, a.wait_ns))
+                break;                                                                  // weights
+            if (!wait_bar_warp(bar(stage), (it / kStages) & 1, abort_flag, a.err, a.wait_ns))
+                break;                                                                  // X landed
             const float *slot = w_ring + stage * HG * kTile;
 #pragma unroll
             for (int h = 0; h < HG; ++h) {
@@ -1164,7 +1218,7 @@ ssd_tc_segment_kernel(const __grid_constant__ CUtensorMap mapB,
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(6 + stage));
         }
-        if (ntile > 0) wait_bar_warp(bar(12), 0, abort_flag, a.err);
+        if (ntile > 0) wait_bar_warp(bar(12), 0, abort_flag, a.err, a.wait_ns);
         tc_fence_after();
         if (!*abort_flag) {
 #pragma unroll 1
@@ -1562,6 +1616,9 @@ cudaError_t ssd_launch_scan_tc(const SsdTcPlan &plan, const void *x, const float
     args.y = static_cast<__nv_bfloat16 *>(y);
     args.fin = fin;
     args.err = err;
+    const SsdDebug dbg = ssd_debug_config();
+    args.wait_ns = dbg.wait_ns;
+    args.fault = dbg.fault;
     args.L = L;
     args.H = H;
     args.G = G;

@@ -28,6 +28,29 @@ def head_range(nheads: int, ngroups: int, world: int, rank: int):
     return g0 * per_group, g1 * per_group
 
 
+def head_shard(nheads: int, ngroups: int, world: int, rank: int, pair: int = 2):
+    """Heads [h0, h1) and groups [g0, g1) of `rank`.  With at least as many
+    groups as ranks this is head_range (whole groups).  With fewer groups --
+    the 2.7B layer has one group of 80 heads -- each group is split evenly
+    among world / ngroups ranks on `pair`-head boundaries (the tensor-core
+    kernel pairs the heads of a group); every rank of a group then reads that
+    group's B and C, which are inputs, so nothing is exchanged.  Shapes that
+    do not split that way fall back to head_range."""
+    if nheads % ngroups:
+        raise ValueError("nheads must be a multiple of ngroups")
+    if not 0 <= rank < world:
+        raise ValueError("rank out of range")
+    per_group = nheads // ngroups
+    parts = world // ngroups if world > ngroups and world % ngroups == 0 else 0
+    if parts and per_group % (pair * parts) == 0:
+        g = rank // parts
+        share = per_group // parts
+        h0 = g * per_group + (rank % parts) * share
+        return h0, h0 + share, g, g + 1
+    h0, h1 = head_range(nheads, ngroups, world, rank)
+    return h0, h1, h0 // per_group, h1 // per_group
+
+
 def batch_range(batch: int, world: int, rank: int):
     """Contiguous [start, stop) batch-row range for `rank` of `world`."""
     if not 0 <= rank < world:

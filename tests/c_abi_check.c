@@ -49,7 +49,10 @@ int main(void) {
     EXPECT(ssd_state_update_fused((void *)0x8000, SSD_BF16, x, dt, A, B, C, NULL, NULL, NULL,
                                   SSD_F32, 2, 4, 16, 16, 1, y, 0),
            SSD_ERR_UNSUPPORTED);
-    if (ssd_scan_workspace_bytes(0, 256, 4, 64, 64, 1, 64, SSD_BF16) != (size_t)-1) return 1;
+    if (ssd_scan_workspace_bytes(0, 256, 4, 64, 64, 1, 64) != (size_t)-1) return 1;
+    if (ssd_scan_fused_workspace_bytes(1, 256, 4, 64, 64, 1, 64, SSD_F32, 1) != 0) return 1;
+    EXPECT(ssd_debug_inject_fault((ssd_fault)9, 0), SSD_ERR_INVALID_ARG);
+    EXPECT(ssd_debug_inject_fault(SSD_FAULT_NONE, 0), SSD_OK);
     if (ssd_scan_kernel_launches(1, 256, 6, 64, 64, 4, 64, SSD_BF16) != -1) return 1;
     printf("c abi ok\n");
     return 0;

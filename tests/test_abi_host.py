@@ -109,11 +109,19 @@ def test_decode_rejects_bad_arguments(lib, kw, expect):
 
 def test_workspace_query_rejects_bad_sizes(lib):
     bad = ctypes.c_size_t(-1).value
-    assert lib.ssd_scan_workspace_bytes(0, 256, 4, 64, 64, 1, 64, 1) == bad
-    assert lib.ssd_scan_workspace_bytes(1, 256, 6, 64, 64, 4, 64, 1) == bad
-    assert lib.ssd_scan_workspace_bytes(1, 256, 4, 64, 64, 1, 100, 1) == bad
-    # the fp32 path needs no workspace
-    assert lib.ssd_scan_workspace_bytes(1, 256, 4, 64, 64, 1, 64, 0) == 0
+    assert lib.ssd_scan_workspace_bytes(0, 256, 4, 64, 64, 1, 64) == bad
+    assert lib.ssd_scan_workspace_bytes(1, 256, 6, 64, 64, 4, 64) == bad
+    assert lib.ssd_scan_workspace_bytes(1, 256, 4, 64, 64, 1, 100) == bad
+    assert lib.ssd_scan_fused_workspace_bytes(0, 256, 4, 64, 64, 1, 64, 1, 1) == bad
+    assert lib.ssd_scan_fused_workspace_bytes(1, 256, 4, 64, 64, 1, 48, 1, 0) == bad
+    # the fp32 path needs no workspace, with or without a dt transform
+    assert lib.ssd_scan_fused_workspace_bytes(1, 256, 4, 64, 64, 1, 64, 0, 0) == 0
+    assert lib.ssd_scan_fused_workspace_bytes(1, 256, 4, 64, 64, 1, 64, 0, 1) == 0
+
+
+def test_fault_hook_rejects_unknown_fault(lib):
+    assert lib.ssd_debug_inject_fault(7, 0) == INVALID
+    assert lib.ssd_debug_inject_fault(0, 0) == 0
 
 
 def test_binding_refuses_cpu_tensors():

@@ -9,7 +9,8 @@ import numpy as np
 import pytest
 import torch.multiprocessing as mp
 
-from state_space_model_chunked_gb300.sharding import batch_range, head_range, max_over_ranks
+from state_space_model_chunked_gb300.sharding import (batch_range, head_range, head_shard,
+                                                      max_over_ranks)
 
 
 def test_head_ranges_cover_all_heads_on_group_boundaries():
@@ -21,6 +22,21 @@ def test_head_ranges_cover_all_heads_on_group_boundaries():
                 assert a1 == b0
             for a0, a1 in cuts:
                 assert a0 % (H // G) == 0 and a1 % (H // G) == 0
+
+
+def test_head_shards_split_a_single_group_on_pair_boundaries():
+    for H, G, world in [(80, 1, 2), (80, 1, 4), (80, 1, 8), (24, 1, 4), (32, 2, 4), (48, 2, 8)]:
+        cuts = [head_shard(H, G, world, r) for r in range(world)]
+        assert cuts[0][0] == 0 and cuts[-1][1] == H
+        for a, b in zip(cuts, cuts[1:]):
+            assert a[1] == b[0]
+        for h0, h1, g0, g1 in cuts:
+            assert h1 - h0 == H // world and h0 % 2 == 0
+            assert g1 == g0 + 1 and h0 // (H // G) == g0 and (h1 - 1) // (H // G) == g0
+    # whole groups when there are enough of them, or when a group cannot split evenly
+    assert [head_shard(32, 8, 4, r) for r in range(4)] == \
+        [(h0, h1, h0 // 4, h1 // 4) for h0, h1 in (head_range(32, 8, 4, r) for r in range(4))]
+    assert [head_shard(6, 1, 4, r) for r in range(4)] == [(0, 0, 0, 0)] * 3 + [(0, 6, 0, 1)]
 
 
 def test_batch_ranges_partition():
@@ -147,3 +163,47 @@ def test_two_gloo_ranks_reassemble_a_packed_batch(tmp_path):
     assert ys[0].shape[0] > 0 and ys[1].shape[0] > 0
     np.testing.assert_array_equal(np.concatenate(ys, axis=0), y_full)
     np.testing.assert_array_equal(np.concatenate(fs, axis=0), f_full)
+
+
+def _group_split_worker(rank, world, port, out_dir):
+    import torch.distributed as dist
+
+    import oracle
+    from state_space_model_chunked_gb300 import inputs as gen
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    # one group of 8 heads, as the 2.7B layer's single group of 80: split in two
+    inp = gen.scan_inputs(1, 80, 8, 8, 16, 1, "bf16", seed=321, random_init=True)
+    h0, h1, g0, g1 = head_shard(8, 1, world, rank)
+    sl = slice(h0, h1)
+    y, fin = oracle.scan_seq(inp["x"][:, :, sl], inp["dt"][:, :, sl], inp["A"][sl],
+                             inp["B"][:, :, g0:g1], inp["C"][:, :, g0:g1], inp["D"][sl],
+                             inp["init"][:, sl], nthreads=1)
+    np.save(os.path.join(out_dir, f"gy{rank}.npy"), y)
+    np.save(os.path.join(out_dir, f"gf{rank}.npy"), fin)
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_two_gloo_ranks_split_one_group(tmp_path):
+    world = 2
+    port = _free_port()
+    ctx = mp.get_context("spawn")
+    procs = [ctx.Process(target=_group_split_worker, args=(r, world, port, str(tmp_path)))
+             for r in range(world)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=120)
+        assert p.exitcode == 0
+    import oracle
+    from state_space_model_chunked_gb300 import inputs as gen
+    inp = gen.scan_inputs(1, 80, 8, 8, 16, 1, "bf16", seed=321, random_init=True)
+    y_full, f_full = oracle.scan_seq(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"],
+                                     inp["D"], inp["init"])
+    ys = [np.load(tmp_path / f"gy{r}.npy") for r in range(world)]
+    fs = [np.load(tmp_path / f"gf{r}.npy") for r in range(world)]
+    assert ys[0].shape[2] == 4 and ys[1].shape[2] == 4
+    assert oracle.rel_l2(np.concatenate(ys, axis=2), y_full) < 1e-13
+    assert oracle.rel_l2(np.concatenate(fs, axis=1), f_full) < 1e-13

@@ -150,6 +150,42 @@ def _bf16_step_unrounded(state, x, dt, A, B, C, D=None, nthreads=None):
     return _step(state, x, dt, A, B, C, D, nthreads)
 
 
+def _rel_over_result(got, ref):
+    got, ref = np.asarray(got, np.float64), np.asarray(ref, np.float64)
+    den = float(np.linalg.norm(got.ravel()))
+    num = float(np.linalg.norm((got - ref).ravel()))
+    return num / den if den > 0 else num
+
+
+def _rel_squared(got, ref):
+    return _REL(got, ref) ** 2
+
+
+def _rel_max_norm(got, ref):
+    got, ref = np.asarray(got, np.float64), np.asarray(ref, np.float64)
+    den = float(np.max(np.abs(ref)))
+    num = float(np.max(np.abs(got - ref)))
+    return num / den if den > 0 else num
+
+
+def _rel_matrix_norm(got, ref):
+    got, ref = np.asarray(got, np.float64), np.asarray(ref, np.float64)
+    if got.ndim != 2:
+        return _REL(got, ref)
+    den = float(np.linalg.norm(ref, 2))
+    num = float(np.linalg.norm(got - ref, 2))
+    return num / den if den > 0 else num
+
+
+def _rel_zero_ref_divides(got, ref):
+    got, ref = np.asarray(got, np.float64), np.asarray(ref, np.float64)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        return float(np.float64(np.linalg.norm((got - ref).ravel()))
+                     / np.float64(np.linalg.norm(ref.ravel())))
+
+
+_REL = oracle.rel_l2
+
 PY_MUTANTS = {
     "varlen_shared_initial_state": ("scan_varlen", _varlen_shared_init,
                                     pins.test_varlen_is_each_sequence_alone_by_quadratic_form),
@@ -169,6 +205,13 @@ PY_MUTANTS = {
                            pins.test_step_bf16_state_is_rounded_step),
     "bf16_step_state_not_rounded": ("step_bf16_state", _bf16_step_unrounded,
                                     pins.test_step_bf16_state_is_rounded_step),
+    "rel_l2_divided_by_result_norm": ("rel_l2", _rel_over_result,
+                                      pins.test_rel_l2_on_hand_worked_values),
+    "rel_l2_squared": ("rel_l2", _rel_squared, pins.test_rel_l2_on_hand_worked_values),
+    "rel_l2_max_norm": ("rel_l2", _rel_max_norm, pins.test_rel_l2_on_hand_worked_values),
+    "rel_l2_matrix_norm": ("rel_l2", _rel_matrix_norm, pins.test_rel_l2_on_hand_worked_values),
+    "rel_l2_zero_reference_divides": ("rel_l2", _rel_zero_ref_divides,
+                                      pins.test_rel_l2_on_hand_worked_values),
 }
 
 

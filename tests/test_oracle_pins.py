@@ -385,3 +385,32 @@ def test_hand_worked_packed_example():
     tol = g["tolerance"]
     np.testing.assert_allclose(y.ravel(), g["expected"]["y"], rtol=tol, atol=tol)
     np.testing.assert_allclose(fin.ravel(), g["expected"]["final_state"], rtol=tol, atol=tol)
+
+
+def test_rel_l2_on_hand_worked_values():
+    """The parity measure itself (relative L2 over the whole tensor, reading
+    c11), on values worked out by hand.  Each case separates it from a
+    plausible slip: dividing by the norm of the result under test, squaring
+    the ratio, a max-norm or L1 norm, a per-element mean, a matrix (spectral)
+    norm of a 2-D array, and a division by a zero reference."""
+    # ||(0,0) - (3,4)|| / ||(3,4)|| = 5 / 5
+    assert oracle.rel_l2([0.0, 0.0], [3.0, 4.0]) == 1.0
+    # half the reference: ||(1.5,2)|| / ||(3,4)|| = 2.5 / 5
+    assert oracle.rel_l2([1.5, 2.0], [3.0, 4.0]) == 0.5
+    # error (0,1) against (3,4): 1/5 (max-norm 1/4, L1 1/7, squared 1/25)
+    assert abs(oracle.rel_l2([3.0, 5.0], [3.0, 4.0]) - 0.2) < 1e-15
+    # twice the reference: the error norm equals the reference norm (dividing
+    # by the result's norm would give 1/2)
+    assert oracle.rel_l2([6.0, 8.0], [3.0, 4.0]) == 1.0
+    # 2-D: error all ones (Frobenius 2) against 3 I (Frobenius 3 sqrt 2) ->
+    # sqrt(2)/3; the spectral norms would give 2/3
+    ref = 3.0 * np.eye(2)
+    assert abs(oracle.rel_l2(ref + 1.0, ref) - np.sqrt(2.0) / 3.0) < 1e-15
+    # an all-zero reference: the absolute norm, ||(1,2,2)|| = 3
+    assert oracle.rel_l2([1.0, 2.0, 2.0], [0.0, 0.0, 0.0]) == 3.0
+    # the same elements in another order and shape give the same value
+    a = np.arange(12.0).reshape(3, 4)
+    b = a + np.linspace(-1.0, 1.0, 12).reshape(3, 4)
+    perm = np.random.default_rng(0).permutation(12)
+    assert oracle.rel_l2(b, a) == pytest.approx(oracle.rel_l2(b.ravel()[perm], a.ravel()[perm]),
+                                                rel=1e-15)

@@ -56,11 +56,13 @@ def test_prefill_workloads_full(name):
     _check(inp, s.dtype, s.chunk, AUTO)
 
 
-def test_chunk_parameter_does_not_change_result():
+@pytest.mark.parametrize("chunk", [16, 32, 64, 128, 256])
+@pytest.mark.parametrize("algo", [TC, SIMT])
+def test_every_chunk_value_matches_oracle(chunk, algo):
+    """`chunk` is validated and does not size the kernels' tiles: every
+    allowed value gives the oracle's result on both kernel paths."""
     inp = gen.scan_inputs(1, 512, 4, 64, 128, 1, "bf16", seed=12, random_init=True)
-    outs = [scan_on_gpu(inp, "bf16", q, AUTO) for q in (16, 64, 256)]
-    for y, f in outs[1:]:
-        assert rel(y, outs[0][0]) <= 1e-2 and rel(f, outs[0][1]) <= 1e-2
+    _check(inp, "bf16", chunk, algo)
 
 
 # ---------------------------------------------------------------- tensor-core path
@@ -118,6 +120,21 @@ def test_tc_path_strong_decay(scale):
     inp = gen.scan_inputs(2, 700, 4, 64, 128, 2, "bf16", seed=23, random_init=True)
     inp["dt"] = (inp["dt"] * scale).astype(np.float32)
     _check(inp, "bf16", 256, TC)
+
+
+@pytest.mark.parametrize("algo", [TC, AUTO, SIMT])
+def test_zero_and_negative_step_sizes(algo):
+    """A fifth of the step sizes exactly 0 (that token neither decays the
+    state nor adds to it) and a tenth small and negative (growth): every path,
+    the default one included, follows the recurrence for any sign of dt."""
+    inp = gen.scan_inputs(1, 700, 4, 64, 128, 2, "bf16", seed=31, random_init=True)
+    dt = inp["dt"].astype(np.float64)
+    m = np.random.default_rng(3).random(dt.shape)
+    dt[m < 0.2] = 0.0
+    dt[(m >= 0.2) & (m < 0.3)] *= -0.5
+    inp["dt"] = dt.astype(np.float32)
+    assert (inp["dt"] == 0).any() and (inp["dt"] < 0).any()
+    _check(inp, "bf16", 256, algo)
 
 
 def test_tc_path_without_skip():

@@ -3,8 +3,9 @@
 caller whose memory is fixed up front -- an engine plugin handed only its
 inputs and outputs, a runtime that forbids device allocation after start-up --
 can still run long sequences.  Called through the C ABI and compared with
-ssd_scan_fwd (caller-provided workspace) on two calls in a row with different
-inputs, so the second call runs over the scratch the first one left behind.
+ssd_scan_fwd (caller-provided workspace) and with the fp64 oracle, on two
+calls in a row with different inputs, so the second call runs over the
+scratch the first one left behind.
 
 This file is collected last so that a failure here cannot stop the rest of
 the GPU suite early."""
@@ -13,50 +14,93 @@ import ctypes
 import pytest
 import torch
 
+import oracle
 import state_space_model_chunked_gb300 as ssd
 from state_space_model_chunked_gb300 import inputs as gen
 from tests.gpu_util import TOL, dev, host, rel
 
 pytestmark = pytest.mark.gpu
 
+STATIC_SCRATCH = 64 << 20   # SSD_STATIC_SCRATCH_BYTES
+WORKSPACE_ERR = 5           # SSD_ERR_WORKSPACE
+
 
 def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
-def test_static_scratch_scan_matches_workspace_scan_twice():
-    lib = ssd.load()
-    # 130M-shaped layer: long enough that the scan splits the sequence into
-    # segments and needs scratch (checked below)
-    b, L, H, P, N, G, Q = 1, 4096, 24, 64, 128, 1, 256
-    need = ssd.scan_workspace_bytes(b, L, H, P, N, G, Q)
-    assert 0 < need <= (32 << 20)
+def _static_scan(lib, x, dt, A, Bm, Cm, D, init, Q):
+    b, L, H, P = x.shape
+    G, N = Bm.shape[2], Bm.shape[3]
+    y = torch.empty_like(x)
+    f = torch.empty((b, H, P, N), dtype=torch.float32, device=x.device)
     stream = torch.cuda.current_stream()
+    rc = lib.ssd_scan_fwd_static(_ptr(x), _ptr(dt), _ptr(A), _ptr(Bm), _ptr(Cm), _ptr(D),
+                                 1, b, L, H, P, N, G, Q, _ptr(init), _ptr(y), _ptr(f),
+                                 ctypes.c_void_p(stream.cuda_stream))
+    assert rc == 0, lib.ssd_status_string(rc).decode()
+    torch.cuda.synchronize()
+    return y, f
+
+
+def test_static_scratch_scan_matches_workspace_scan_and_oracle_twice():
+    lib = ssd.load()
+    # 130M-shaped layer: split into segments (three launches), so the scan
+    # keeps segment states in the scratch
+    b, L, H, P, N, G, Q = 1, 4096, 24, 64, 128, 1, 256
+    assert ssd.scan_kernel_launches(b, L, H, P, N, G, Q) == 3
+    need = ssd.scan_workspace_bytes(b, L, H, P, N, G, Q)
+    assert 0 < need <= STATIC_SCRATCH
     for seed in (101, 202):
         inp = gen.scan_inputs(b, L, H, P, N, G, "bf16", seed=seed, random_init=True)
         x, Bm, Cm = dev(inp["x"], "bf16"), dev(inp["B"], "bf16"), dev(inp["C"], "bf16")
         dt, A, D, init = dev(inp["dt"]), dev(inp["A"]), dev(inp["D"]), dev(inp["init"])
         y_ref, f_ref = ssd.scan_fwd(x, dt, A, Bm, Cm, D, Q, init)
-        y = torch.empty_like(x)
-        f = torch.empty((b, H, P, N), dtype=torch.float32, device=x.device)
-        rc = lib.ssd_scan_fwd_static(_ptr(x), _ptr(dt), _ptr(A), _ptr(Bm), _ptr(Cm), _ptr(D),
-                                     1, b, L, H, P, N, G, Q, _ptr(init), _ptr(y), _ptr(f),
-                                     ctypes.c_void_p(stream.cuda_stream))
-        assert rc == 0, lib.ssd_status_string(rc).decode()
-        torch.cuda.synchronize()
+        y, f = _static_scan(lib, x, dt, A, Bm, Cm, D, init, Q)
         assert rel(host(y), host(y_ref)) <= TOL["bf16"]
         assert rel(host(f), host(f_ref)) <= TOL["bf16"]
+        yo, fo = oracle.scan_seq(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], inp["D"],
+                                 inp["init"])
+        assert rel(host(y), yo) <= TOL["bf16"]
+        assert rel(host(f), fo) <= TOL["bf16"]
+    ssd.last_device_error()
+
+
+def test_static_scratch_runs_the_long_2p7b_layer():
+    """The 2.7B-shaped 65536-token layer (80 heads): its segment states fit
+    the built-in scratch; two heads are checked against the oracle."""
+    lib = ssd.load()
+    b, L, H, P, N, G, Q = 1, 65536, 80, 64, 128, 1, 256
+    need = ssd.scan_workspace_bytes(b, L, H, P, N, G, Q)
+    if need > STATIC_SCRATCH:
+        pytest.skip("this device's segment plan needs more than the built-in scratch")
+    inp = gen.scan_inputs(b, L, H, P, N, G, "bf16", seed=7, random_init=True)
+    x, Bm, Cm = dev(inp["x"], "bf16"), dev(inp["B"], "bf16"), dev(inp["C"], "bf16")
+    dt, A, D, init = dev(inp["dt"]), dev(inp["A"]), dev(inp["D"]), dev(inp["init"])
+    y, f = _static_scan(lib, x, dt, A, Bm, Cm, D, init, Q)
+    y_ref, f_ref = ssd.scan_fwd(x, dt, A, Bm, Cm, D, Q, init)
+    torch.cuda.synchronize()
+    assert rel(host(y), host(y_ref)) <= TOL["bf16"]
+    assert rel(host(f), host(f_ref)) <= TOL["bf16"]
+    heads = [0, 79]
+    yo, fo = oracle.scan_seq(inp["x"][:, :, heads], inp["dt"][:, :, heads], inp["A"][heads],
+                             inp["B"], inp["C"], inp["D"][heads], inp["init"][:, heads])
+    assert rel(host(y[:, :, heads]), yo) <= TOL["bf16"]
+    assert rel(host(f[:, heads]), fo) <= TOL["bf16"]
     ssd.last_device_error()
 
 
 def test_static_scratch_scan_rejects_shapes_beyond_its_scratch():
     lib = ssd.load()
-    # the 2.7B-shaped 65536-token layer needs more scratch than the built-in array
-    b, L, H, P, N, G, Q = 1, 65536, 80, 64, 128, 1, 256
-    need = ssd.scan_workspace_bytes(b, L, H, P, N, G, Q)
-    if need <= (32 << 20):
-        pytest.skip("this device's segment plan fits the built-in scratch")
+    # long sequences of many heads: the segment plan depends on the SM count,
+    # so take the first candidate whose segment states exceed the array
+    P, N, G, Q = 64, 128, 1, 256
+    for b, L, H in ((2, 262144, 80), (1, 262144, 160), (1, 1048576, 80), (1, 524288, 160)):
+        if ssd.scan_workspace_bytes(b, L, H, P, N, G, Q) > STATIC_SCRATCH:
+            break
+    else:
+        pytest.skip("no candidate shape exceeds the built-in scratch on this device")
     fake = ctypes.c_void_p(1 << 20)   # never dereferenced: rejected before any launch
     rc = lib.ssd_scan_fwd_static(fake, fake, fake, fake, fake, None, 1, b, L, H, P, N, G, Q,
                                  None, fake, None, None)
-    assert rc == 5   # SSD_ERR_WORKSPACE
+    assert rc == WORKSPACE_ERR
