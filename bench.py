@@ -355,6 +355,51 @@ def time_decode(batch, steps, device, peaks, state_dtype=None):
             "frac_of_8TBs_nominal": gbs / 8000.0}
 
 
+def time_decode_multi(batch, ntok, steps, device, peaks):
+    """The 64-layer 2.7B-shaped decode stack (layers flattened into heads, one
+    group per layer) advanced `ntok` tokens per ssd_state_update_multi call:
+    each state is read and written once per call.  Tokens/s counts batch x
+    ntok tokens through the whole stack per call."""
+    import torch
+    import state_space_model_chunked_gb300 as ssd
+    from state_space_model_chunked_gb300 import inputs as gen
+    ds = gen.DECODE_SHAPE
+    Hf, G, P, N = ds.layers * ds.nheads, ds.layers, ds.headdim, ds.dstate
+    state = gen.device_decode_state(batch, Hf, P, N, seed=batch, device=device)
+    A, D = gen.decode_params(Hf, seed=batch)
+    A, D = torch.from_numpy(A).to(device), torch.from_numpy(D).to(device)
+    g = torch.Generator(device=device)
+    g.manual_seed(1000 + ntok)
+    x = torch.randn((batch, ntok, Hf, P), generator=g, device=device).to(torch.bfloat16)
+    dt = torch.exp(gen.LN_DT_LO + (gen.LN_DT_HI - gen.LN_DT_LO)
+                   * torch.rand((batch, ntok, Hf), generator=g, device=device))
+    B = torch.randn((batch, ntok, G, N), generator=g, device=device).to(torch.bfloat16)
+    C = torch.randn((batch, ntok, G, N), generator=g, device=device).to(torch.bfloat16)
+    y = torch.empty_like(x)
+    for _ in range(3):
+        ssd.state_update_multi(state, x, dt, A, B, C, D, y=y)
+    stream = torch.cuda.current_stream(device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(device)
+    e0.record(stream)
+    for _ in range(steps):
+        ssd.state_update_multi(state, x, dt, A, B, C, D, y=y)
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    ms = e0.elapsed_time(e1) / steps
+    byts = (2 * batch * Hf * P * N * 4
+            + ntok * (2 * batch * Hf * P * 2 + batch * Hf * 4 + 2 * batch * G * N * 2)
+            + 2 * Hf * 4)
+    gbs = byts / (ms * 1e-3) / 1e9
+    del state, x, dt, B, C, y
+    torch.cuda.empty_cache()
+    return {"batch": batch, "tokens_per_call": ntok, "ms_per_call": ms,
+            "ms_per_token": ms / ntok,
+            "tokens_per_s": batch * ntok / (ms * 1e-3),
+            "bytes_per_call": byts, "GB_per_s": gbs,
+            "frac_of_measured_hbm": gbs / peaks["hbm_gbs"]}
+
+
 def time_decode_per_layer(batch, steps, device, peaks):
     """The same decode stack as 64 per-layer ssd_state_update calls per token
     (each layer's state, x, B, C contiguous; 80 heads, one group), the 64 calls
@@ -775,6 +820,8 @@ def run_gpu(args):
                                           for b in (1, 16, 64, 256)]
             extra["decode_per_layer"] = [time_decode_per_layer(b, 32, device, peaks)
                                          for b in (1, 16)]
+            extra["decode_multi_token"] = [time_decode_multi(b, t, 10, device, peaks)
+                                           for b in (1, 16) for t in (4, 16)]
             extra["decode_vs_recompute"] = time_decode_vs_recompute(device)
             extra["varlen"] = time_varlen(device, peaks)
             extra["fused_steps"] = [time_fused_steps(gen.SCAN_SHAPES[n], device)

@@ -321,6 +321,30 @@ ssd_status ssd_state_update_fused(void *state, ssd_dtype state_dtype, const void
                                   ssd_dtype in_dtype, int batch, int nheads, int headdim,
                                   int dstate, int ngroups, void *y, cudaStream_t stream);
 
+/* Decode of `ntokens` consecutive tokens per (batch, head) in one call: the
+ * on-device multi-step loop of the O(1) cached decode (compiler-first SSD
+ * page, abstract).  Equivalent to ntokens calls of ssd_state_update_fused in
+ * token order, except that a bf16 state is rounded once, when it is written
+ * back after the last token, not after every token (the state stays fp32 on
+ * chip in between).  Each state is read once and written once per call, so
+ * its HBM traffic per token falls by ntokens.
+ *   state        [batch][nheads][headdim][dstate] of state_dtype, in place.
+ *   x, y, z      in_dtype [batch][ntokens][nheads][headdim] (z may be NULL).
+ *   dt           float [batch][ntokens][nheads].
+ *   B, C         in_dtype [batch][ntokens][ngroups][dstate].
+ *   A, D, dt_transform as ssd_state_update_fused.
+ * The token arrays have the layouts of ssd_scan_fwd with seqlen = ntokens.
+ * Requirements: those of ssd_state_update_fused, ntokens > 0, and headdim at
+ * most 8 x 256 / (dstate / 4) for dstate <= 128 (64 for dstate 128; 64 for
+ * dstate 256), else SSD_ERR_UNSUPPORTED. */
+ssd_status ssd_state_update_multi(void *state, ssd_dtype state_dtype, const void *x,
+                                  const float *dt, const float *A, const void *B,
+                                  const void *C, const float *D,
+                                  const ssd_dt_transform *dt_transform, const void *z,
+                                  ssd_dtype in_dtype, int batch, int ntokens, int nheads,
+                                  int headdim, int dstate, int ngroups, void *y,
+                                  cudaStream_t stream);
+
 /* Human-readable name of a status code (static storage). */
 const char *ssd_status_string(ssd_status s);
 
@@ -333,13 +357,13 @@ ssd_status ssd_last_device_error(void);
  * setting; it is process-wide and not synchronised with calls in flight on
  * other host threads.
  *   fault          SSD_FAULT_NONE: normal operation.  SSD_FAULT_WITHHOLD_SIGNAL:
- *                  in the CTAs of each sequence's first segment, the warp that
- *                  computes the decay factors withholds its first "factors
- *                  ready" signal, so the wait for it runs out; the CTA then
- *                  lets its issued copies and tensor-core products complete,
- *                  frees its tensor memory and exits, and the device error
- *                  word reads SSD_ERR_TIMEOUT.  The outputs of that call are
- *                  undefined.
+ *                  in the CTAs of each sequence's first segment, the barrier
+ *                  that signals "decay factors ready" waits for one arrival
+ *                  more than the warp computing them gives, so the first wait
+ *                  for it runs out; the CTA then lets its issued copies and
+ *                  tensor-core products complete, frees its tensor memory and
+ *                  exits, and the device error word reads SSD_ERR_TIMEOUT.
+ *                  The outputs of that call are undefined.
  *   wait_limit_ns  limit of every bounded wait in those kernels; 0 restores
  *                  the default (2 s).
  * Returns SSD_ERR_INVALID_ARG for an unknown fault. */

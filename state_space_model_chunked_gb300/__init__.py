@@ -10,6 +10,7 @@ cannot load, every call raises.
     y, final = scan_fwd(x, dt, A, B, C, D, chunk=256, init_state=None)
     y, finals = scan_fwd_varlen(x, dt, A, B, C, cu_seqlens, D)   # packed sequences
     y = state_update(state, x, dt, A, B, C, D)          # state updated in place
+    y = state_update_multi(state, x, dt, A, B, C, D)    # T tokens [b,T,H,P] in one call
     pipe = HostScanPipeline(); pipe.submit(..., out=(y_host, final_host))  # host tensors
 """
 from __future__ import annotations
@@ -32,6 +33,7 @@ from ._binding import (  # noqa: F401
     scan_varlen_workspace_bytes,
     scan_workspace_bytes,
     state_update,
+    state_update_multi,
     ALGO_AUTO,
     ALGO_SIMT,
     ALGO_TCGEN05,

@@ -26,6 +26,7 @@ EXPORTED_SYMBOLS = (
     "ssd_state_update",
     "ssd_state_update_dt",
     "ssd_state_update_fused",
+    "ssd_state_update_multi",
     "ssd_status_string",
     "ssd_last_device_error",
     "ssd_debug_inject_fault",
@@ -102,6 +103,8 @@ def load():
         lib.ssd_state_update_dt.argtypes = [_vp] * 8 + [_int] * 6 + [_vp, _vp]
         lib.ssd_state_update_fused.restype = _int
         lib.ssd_state_update_fused.argtypes = [_vp, _int] + [_vp] * 8 + [_int] * 6 + [_vp, _vp]
+        lib.ssd_state_update_multi.restype = _int
+        lib.ssd_state_update_multi.argtypes = [_vp, _int] + [_vp] * 8 + [_int] * 7 + [_vp, _vp]
         lib.ssd_scan_fwd_static.restype = _int
         lib.ssd_scan_fwd_static.argtypes = [_vp] * 6 + [_int] * 8 + [_vp, _vp, _vp, _vp]
         lib.ssd_scan_profile_events.restype = _int
@@ -489,6 +492,48 @@ def state_update(state, x, dt, A, B, C, D=None, *, y=None, dt_bias=None, dt_soft
                                         _ptr(A), _ptr(B), _ptr(C), _ptr(D), tptr, _ptr(z), code,
                                         b, H, P, N, G, _ptr(y), ctypes.c_void_p(stream))
     _check("ssd_state_update", rc)
+    return y
+
+
+def state_update_multi(state, x, dt, A, B, C, D=None, *, y=None, dt_bias=None,
+                       dt_softplus=False, dt_limit=None, z=None):
+    """`ntokens` decode tokens per (batch, head) in one call (the state is
+    read and written once).  state [b,H,P,N] f32 or bf16 (in place; a bf16
+    state is rounded once, after the last token), x [b,T,H,P], dt [b,T,H]
+    f32, A [H] f32, B/C [b,T,G,N] (x's dtype), D [H] f32 or None; the dt
+    transform and gate z [b,T,H,P] as in state_update.  Returns y [b,T,H,P]."""
+    lib = load()
+    _need(state, "state")
+    if state.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError(f"state must be float32 or bfloat16, got {state.dtype}")
+    dev = state.device
+    b, H, P, N = state.shape
+    _need(x, "x", None, dev)
+    if x.dim() != 4 or x.shape[0] != b or x.shape[2] != H or x.shape[3] != P:
+        raise ValueError(f"x has shape {tuple(x.shape)}, expected ({b}, T, {H}, {P})")
+    T = x.shape[1]
+    _need(dt, "dt", torch.float32, dev, (b, T, H))
+    _need(A, "A", torch.float32, dev, (H,))
+    _need(B, "B", x.dtype, dev)
+    G = B.shape[2]
+    _need(B, "B", x.dtype, dev, (b, T, G, N))
+    _need(C, "C", x.dtype, dev, (b, T, G, N))
+    if D is not None:
+        _need(D, "D", torch.float32, dev, (H,))
+    if z is not None:
+        _need(z, "z", x.dtype, dev, x.shape)
+    if y is None:
+        y = torch.empty_like(x)
+    else:
+        _need(y, "y", x.dtype, dev, x.shape)
+    code = _dtype_code(x)
+    with torch.cuda.device(dev):
+        stream = torch.cuda.current_stream(dev).cuda_stream
+        tptr, _keep = _dt_transform(dt_bias, dt_softplus, dt_limit, H, dev)
+        rc = lib.ssd_state_update_multi(_ptr(state), _dtype_code(state), _ptr(x), _ptr(dt),
+                                        _ptr(A), _ptr(B), _ptr(C), _ptr(D), tptr, _ptr(z), code,
+                                        b, T, H, P, N, G, _ptr(y), ctypes.c_void_p(stream))
+    _check("ssd_state_update_multi", rc)
     return y
 
 

@@ -345,6 +345,37 @@ ssd_status ssd_state_update_fused(void *state, ssd_dtype state_dtype, const void
     return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
 }
 
+ssd_status ssd_state_update_multi(void *state, ssd_dtype state_dtype, const void *x,
+                                  const float *dt, const float *A, const void *B, const void *C,
+                                  const float *D, const ssd_dt_transform *dt_transform,
+                                  const void *z, ssd_dtype in_dtype, int batch, int ntokens,
+                                  int nheads, int headdim, int dstate, int ngroups, void *y,
+                                  cudaStream_t stream) {
+    if (!state || !x || !dt || !A || !B || !C || !y) return SSD_ERR_INVALID_ARG;
+    if (in_dtype != SSD_F32 && in_dtype != SSD_BF16) return SSD_ERR_INVALID_ARG;
+    if (state_dtype != SSD_F32 && state_dtype != SSD_BF16) return SSD_ERR_INVALID_ARG;
+    if (batch <= 0 || ntokens <= 0 || nheads <= 0 || headdim <= 0 || dstate <= 0 ||
+        ngroups <= 0)
+        return SSD_ERR_INVALID_ARG;
+    if (nheads % ngroups != 0) return SSD_ERR_INVALID_ARG;
+    if (!pow2(dstate) || dstate < 4 || dstate > 256) return SSD_ERR_UNSUPPORTED;
+    if (headdim > ssd_decode_multi_max_headdim(dstate)) return SSD_ERR_UNSUPPORTED;
+    if (state_dtype == SSD_BF16 && in_dtype != SSD_BF16) return SSD_ERR_UNSUPPORTED;
+    const void *ptrs[] = {state, x, dt, A, B, C, D, y, z};
+    for (const void *p : ptrs)
+        if (p && !aligned16(p)) return SSD_ERR_INVALID_ARG;
+    if ((size_t)batch * nheads >= ((size_t)1 << 31)) return SSD_ERR_UNSUPPORTED;
+    if ((size_t)batch * ntokens * nheads * headdim >= ((size_t)1 << 40)) return SSD_ERR_UNSUPPORTED;
+    SsdFuse fuse;
+    const ssd_status st = dt_transform_of(dt_transform, &fuse);
+    if (st != SSD_OK) return st;
+    fuse.z = z;
+    cudaError_t e = ssd_launch_decode_multi(state, state_dtype == SSD_BF16, x, dt, A, B, C, D, y,
+                                            in_dtype == SSD_BF16, batch, ntokens, nheads,
+                                            headdim, dstate, ngroups, fuse, stream);
+    return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+}
+
 ssd_status ssd_state_update_dt(float *state, const void *x, const float *dt, const float *A,
                                const void *B, const void *C, const float *D,
                                const ssd_dt_transform *dt_transform, ssd_dtype in_dtype,

@@ -357,6 +357,278 @@ cudaError_t launch_t(S *state, const void *x, const float *dt, const float *A,
     return cudaGetLastError();
 }
 
+// ------------------------------------------------------------ multi-token
+// T consecutive tokens per (batch, head) in one launch: the on-device loop of
+// the O(1) cached decode (compiler-first SSD page, abstract).  Each CTA reads
+// its P x N state once into registers, applies the tokens in order -- for
+// each, the update of every state element and the readout y_t from the
+// updated state -- and writes the state back once, so state traffic per token
+// falls by T.
+//
+// The registers hold a scaled state hs = h / sigma, sigma the product of the
+// decays since the last rescale, so a token's update is one fused
+// multiply-add per element: hs += (dt x / sigma) B.  The readout is
+// y = sigma (C . hs) + D x.  The true state is restored (hs *= sigma) at the
+// end of every group of staged tokens and before any token that would take
+// sigma beyond e^-40 or e^40, so the scaled values stay well inside fp32.
+//
+// The tokens' x, dt x / sigma, B and C (and z when gated) are staged in shared
+// memory kMultiTok at a time as fp32.  A state row of N elements is spread
+// over tpr threads (VPT float4 each); a thread keeps kMultiRows rows r0,
+// r0 + rpp, ...  The per-row sums of y reduce over the tpr threads of a row by
+// exchanging halves of the row set, then plain butterflies.
+constexpr int kMultiTok = 16;      // tokens staged in shared memory at a time
+constexpr int kMultiRows = 4;      // most state rows a thread keeps in registers
+constexpr float kMultiRenorm = 40.f;
+
+// floats of staged token data: x and dt x / sigma (and z) per row, B and C,
+// and four per-token scalars
+__host__ __device__ inline size_t multi_smem_floats(int P, int N, bool gated) {
+    return (size_t)kMultiTok * ((gated ? 3 : 2) * P + 2 * N + 4);
+}
+// threads per CTA and float4 per thread of a row for a state width
+__host__ __device__ inline int multi_threads(int N) { return N > 128 ? 256 : 128; }
+__host__ __device__ inline int multi_vpt(int N) { return N >= 16 ? 4 : N / 4; }
+
+template <typename T, typename S, int VPT, int NT, bool kFuse>
+__global__ void __launch_bounds__(NT, 512 / NT)
+ssd_decode_multi_kernel(S *__restrict__ state, const T *__restrict__ x,
+                        const float *__restrict__ dt, const float *__restrict__ A,
+                        const T *__restrict__ Bm, const T *__restrict__ Cm,
+                        const float *__restrict__ D, T *__restrict__ y, int ntok, int H, int P,
+                        int N, int G, const SsdFuse fuse) {
+    using namespace ssdptx;
+    extern __shared__ float msm[];
+    const int bh = blockIdx.x;             // b * H + h
+    const int b = bh / H, h = bh - b * H;
+    const int g = h / (H / G);
+    const int tpr = N / (4 * VPT);         // threads per row: a power of two <= 16
+    const int rpp = NT / tpr;              // rows per pass
+    const int lane_n = threadIdx.x & (tpr - 1);
+    const int r0 = threadIdx.x / tpr;
+    const float Ah = A[h];
+    const float Dh = D ? D[h] : 0.0f;
+    const float bias = ssd_dt_bias<kFuse>(fuse, h);
+    const bool gated = kFuse && fuse.z != nullptr;
+    float *xs = msm;                         // [kMultiTok][P]  x
+    float *us = xs + kMultiTok * P;          // [kMultiTok][P]  dt x / sigma
+    float *Bs = us + kMultiTok * P;          // [kMultiTok][N]
+    float *Cs = Bs + kMultiTok * N;          // [kMultiTok][N]
+    float *sig = Cs + kMultiTok * N;         // [kMultiTok]: sigma after the token
+    float *pre = sig + kMultiTok;            // [kMultiTok]: rescale before the token (1 = none)
+    float *dsz = pre + kMultiTok;            // [kMultiTok]: step size
+    float *inv = dsz + kMultiTok;            // [kMultiTok]: 1 / sigma
+    float *zs = inv + kMultiTok;             // [kMultiTok][P] when gated
+
+    S *st = state + (size_t)bh * P * N;
+    float4 s[kMultiRows][VPT];
+#pragma unroll
+    for (int i = 0; i < kMultiRows; ++i) {
+        const int p = r0 + i * rpp;
+#pragma unroll
+        for (int v = 0; v < VPT; ++v)
+            s[i][v] = p < P ? ssd_ld4_cs(st + (size_t)p * N + 4 * (lane_n + v * tpr))
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    auto rescale = [&](float f) {
+        const uint64_t f2 = pack_f32x2(f, f);
+#pragma unroll
+        for (int i = 0; i < kMultiRows; ++i)
+#pragma unroll
+            for (int v = 0; v < VPT; ++v) {
+                const uint64_t lo = mul_f32x2(pack_f32x2(s[i][v].x, s[i][v].y), f2);
+                const uint64_t hi = mul_f32x2(pack_f32x2(s[i][v].z, s[i][v].w), f2);
+                s[i][v] = make_float4(__uint_as_float((uint32_t)lo),
+                                      __uint_as_float((uint32_t)(lo >> 32)),
+                                      __uint_as_float((uint32_t)hi),
+                                      __uint_as_float((uint32_t)(hi >> 32)));
+            }
+    };
+
+    for (int t0 = 0; t0 < ntok; t0 += kMultiTok) {
+        const int nt = min(kMultiTok, ntok - t0);
+        __syncthreads();                     // the previous tokens' staging is consumed
+        const size_t row0 = (size_t)b * ntok + t0;   // token row of the [b][T] axis
+        // per-token factors, one thread walking the group's tokens: log sigma
+        // accumulates dt A.  A token that would take it past +-kMultiRenorm
+        // first restores the state (pre = the sigma so far) and restarts
+        // sigma at its own decay; a token whose own decay is that large is
+        // applied to the restored state directly (pre = sigma so far times
+        // it), and sigma restarts at 1.
+        if (threadIdx.x < nt)
+            dsz[threadIdx.x] = ssd_dt<kFuse>(fuse, dt[(row0 + threadIdx.x) * H + h], bias);
+        for (int e = threadIdx.x; e < nt * N; e += NT) {
+            const int t = e / N, n = e - t * N;
+            const size_t o = ((row0 + t) * G + g) * N + n;
+            Bs[e] = ssd_ld(Bm + o);
+            Cs[e] = ssd_ld(Cm + o);
+        }
+        for (int e = threadIdx.x; e < nt * P; e += NT) {
+            const int t = e / P;
+            const size_t o = ((row0 + t) * H + h) * P + (e - t * P);
+            xs[e] = ssd_ld(x + o);
+            if (gated) zs[e] = ssd_ld(static_cast<const T *>(fuse.z) + o);
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            float ls = 0.f;
+            for (int t = 0; t < nt; ++t) {
+                const float l = dsz[t] * Ah;
+                float rs = 1.f;
+                if (fabsf(l) > kMultiRenorm) {
+                    rs = expf(ls + l);
+                    ls = 0.f;
+                } else if (fabsf(ls + l) > kMultiRenorm) {
+                    rs = expf(ls);
+                    ls = l;
+                } else {
+                    ls += l;
+                }
+                pre[t] = rs;
+                sig[t] = expf(ls);
+                inv[t] = expf(-ls);
+            }
+        }
+        __syncthreads();
+        for (int e = threadIdx.x; e < nt * P; e += NT) {
+            const int t = e / P;
+            us[e] = (dsz[t] * xs[e]) * inv[t];
+        }
+        __syncthreads();
+
+        for (int t = 0; t < nt; ++t) {
+            const float rs = pre[t];
+            if (rs != 1.f) rescale(rs);       // uniform: every thread reads the same slot
+            // update hs += u B and the row's partial readout C . hs (packed
+            // pairs), one float4 of B and C at a time for all rows
+            uint64_t u2[kMultiRows], a2[kMultiRows];
+#pragma unroll
+            for (int i = 0; i < kMultiRows; ++i) {
+                const int p = r0 + i * rpp;
+                const float u = p < P ? us[t * P + p] : 0.f;
+                u2[i] = pack_f32x2(u, u);
+                a2[i] = 0;
+            }
+#pragma unroll
+            for (int v = 0; v < VPT; ++v) {
+                const float4 Bv = *reinterpret_cast<const float4 *>(Bs + t * N + 4 * (lane_n + v * tpr));
+                const float4 Cv = *reinterpret_cast<const float4 *>(Cs + t * N + 4 * (lane_n + v * tpr));
+                const uint64_t b01 = pack_f32x2(Bv.x, Bv.y), b23 = pack_f32x2(Bv.z, Bv.w);
+                const uint64_t c01 = pack_f32x2(Cv.x, Cv.y), c23 = pack_f32x2(Cv.z, Cv.w);
+#pragma unroll
+                for (int i = 0; i < kMultiRows; ++i) {
+                    const uint64_t q01 = fma_f32x2(u2[i], b01, pack_f32x2(s[i][v].x, s[i][v].y));
+                    const uint64_t q23 = fma_f32x2(u2[i], b23, pack_f32x2(s[i][v].z, s[i][v].w));
+                    s[i][v] = make_float4(__uint_as_float((uint32_t)q01),
+                                          __uint_as_float((uint32_t)(q01 >> 32)),
+                                          __uint_as_float((uint32_t)q23),
+                                          __uint_as_float((uint32_t)(q23 >> 32)));
+                    a2[i] = fma_f32x2(c01, q01, a2[i]);
+                    a2[i] = fma_f32x2(c23, q23, a2[i]);
+                }
+            }
+            float acc[kMultiRows];
+#pragma unroll
+            for (int i = 0; i < kMultiRows; ++i)
+                acc[i] = __uint_as_float((uint32_t)a2[i]) + __uint_as_float((uint32_t)(a2[i] >> 32));
+            // reduce over the tpr threads of each row: at exchange k (offset
+            // tpr >> (k+1)) a thread keeps one half of its remaining rows and
+            // adds its partner's partials of them; once one row is left, plain
+            // butterflies finish the sum
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int o = tpr >> (k + 1);
+                if (o == 0) break;
+                if (k < 2) {
+                    constexpr int kHalf0 = kMultiRows / 2;
+                    const int half = kHalf0 >> k;
+                    const bool up = (lane_n & o) != 0;
+#pragma unroll
+                    for (int j = 0; j < kHalf0; ++j) {
+                        if (j < half) {
+                            const float send = up ? acc[j] : acc[j + half];
+                            const float keep = up ? acc[j + half] : acc[j];
+                            acc[j] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+                        }
+                    }
+                } else {
+                    acc[0] += __shfl_xor_sync(0xffffffffu, acc[0], o);
+                }
+            }
+            // rows this thread now holds: base + j for j < left, base from the
+            // halves it kept; the lowest thread of each set of equal holders writes
+            int base = 0, left = kMultiRows;
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                const int o = tpr >> (k + 1);
+                if (o > 0) {
+                    left >>= 1;
+                    if (lane_n & o) base += left;
+                }
+            }
+            const int low = tpr > 4 ? tpr / 4 - 1 : 0;
+            if ((lane_n & low) == 0) {
+                const float sg = sig[t];
+#pragma unroll
+                for (int j = 0; j < kMultiRows; ++j) {
+                    const int p = r0 + (base + j) * rpp;
+                    if (j < left && p < P) {
+                        float yv = sg * acc[j] + Dh * xs[t * P + p];
+                        if (gated) yv *= ssd_silu(zs[t * P + p]);
+                        ssd_st(y + ((row0 + t) * H + h) * P + p, yv);
+                    }
+                }
+            }
+        }
+        rescale(sig[nt - 1]);                 // the true state again
+    }
+#pragma unroll
+    for (int i = 0; i < kMultiRows; ++i) {
+        const int p = r0 + i * rpp;
+        if (p < P) {
+#pragma unroll
+            for (int v = 0; v < VPT; ++v)
+                ssd_st4_cs(st + (size_t)p * N + 4 * (lane_n + v * tpr), s[i][v]);
+        }
+    }
+}
+
+template <typename T, typename S, int VPT, int NT, bool kFuse>
+cudaError_t launch_multi_k(S *state, const void *x, const float *dt, const float *A,
+                           const void *B, const void *C, const float *D, void *y, int batch,
+                           int ntok, int H, int P, int N, int G, const SsdFuse &fuse,
+                           cudaStream_t stream) {
+    const size_t smem = multi_smem_floats(P, N, kFuse && fuse.z != nullptr) * sizeof(float);
+    cudaError_t e = cudaFuncSetAttribute(ssd_decode_multi_kernel<T, S, VPT, NT, kFuse>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    ssd_decode_multi_kernel<T, S, VPT, NT, kFuse><<<(unsigned)((size_t)batch * H), NT, smem,
+                                                    stream>>>(
+        state, (const T *)x, dt, A, (const T *)B, (const T *)C, D, (T *)y, ntok, H, P, N, G, fuse);
+    return cudaGetLastError();
+}
+
+template <typename T, typename S, bool kFuse>
+cudaError_t launch_multi_t(S *state, const void *x, const float *dt, const float *A,
+                           const void *B, const void *C, const float *D, void *y, int batch,
+                           int ntok, int H, int P, int N, int G, const SsdFuse &fuse,
+                           cudaStream_t stream) {
+    if (N > 128)
+        return launch_multi_k<T, S, 4, 256, kFuse>(state, x, dt, A, B, C, D, y, batch, ntok, H,
+                                                   P, N, G, fuse, stream);
+    switch (multi_vpt(N)) {
+        case 1:
+            return launch_multi_k<T, S, 1, 128, kFuse>(state, x, dt, A, B, C, D, y, batch, ntok,
+                                                       H, P, N, G, fuse, stream);
+        case 2:
+            return launch_multi_k<T, S, 2, 128, kFuse>(state, x, dt, A, B, C, D, y, batch, ntok,
+                                                       H, P, N, G, fuse, stream);
+        default:
+            return launch_multi_k<T, S, 4, 128, kFuse>(state, x, dt, A, B, C, D, y, batch, ntok,
+                                                       H, P, N, G, fuse, stream);
+    }
+}
+
 }  // namespace
 
 cudaError_t ssd_launch_decode(void *state, bool bf16_state, const void *x, const float *dt,
@@ -383,4 +655,36 @@ cudaError_t ssd_launch_decode(void *state, bool bf16_state, const void *x, const
                                                 num_sms, err, fuse, stream)
                  : launch_t<float, float, false>(st, x, dt, A, B, C, D, y, batch, H, P, N, G,
                                                  num_sms, err, fuse, stream);
+}
+
+int ssd_decode_multi_max_headdim(int N) {
+    if (N < 4 || N > 256 || (N & (N - 1)) != 0) return 0;
+    const int tpr = N / (4 * multi_vpt(N));
+    return kMultiRows * (multi_threads(N) / tpr);
+}
+
+cudaError_t ssd_launch_decode_multi(void *state, bool bf16_state, const void *x, const float *dt,
+                                    const float *A, const void *B, const void *C,
+                                    const float *D, void *y, bool bf16, int batch, int ntok,
+                                    int H, int P, int N, int G, const SsdFuse &fuse,
+                                    cudaStream_t stream) {
+    const bool fused = ssd_fuse_active(fuse);
+    using bf = __nv_bfloat16;
+    if (bf16_state) {   // bf16 inputs only (checked by the caller)
+        bf *st = static_cast<bf *>(state);
+        return fused ? launch_multi_t<bf, bf, true>(st, x, dt, A, B, C, D, y, batch, ntok, H, P,
+                                                    N, G, fuse, stream)
+                     : launch_multi_t<bf, bf, false>(st, x, dt, A, B, C, D, y, batch, ntok, H, P,
+                                                     N, G, fuse, stream);
+    }
+    float *st = static_cast<float *>(state);
+    if (bf16)
+        return fused ? launch_multi_t<bf, float, true>(st, x, dt, A, B, C, D, y, batch, ntok, H,
+                                                       P, N, G, fuse, stream)
+                     : launch_multi_t<bf, float, false>(st, x, dt, A, B, C, D, y, batch, ntok, H,
+                                                        P, N, G, fuse, stream);
+    return fused ? launch_multi_t<float, float, true>(st, x, dt, A, B, C, D, y, batch, ntok, H, P,
+                                                      N, G, fuse, stream)
+                 : launch_multi_t<float, float, false>(st, x, dt, A, B, C, D, y, batch, ntok, H,
+                                                       P, N, G, fuse, stream);
 }

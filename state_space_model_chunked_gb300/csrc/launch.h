@@ -13,6 +13,16 @@ cudaError_t ssd_launch_decode(void *state, bool bf16_state, const void *x, const
                               int H, int P, int N, int G, int num_sms, unsigned int *err,
                               const SsdFuse &fuse, cudaStream_t stream);
 
+// ntok consecutive tokens per (batch, head) in one launch (state read and
+// written once); headdim must not exceed ssd_decode_multi_max_headdim(N)
+// (0 for an unsupported dstate).
+cudaError_t ssd_launch_decode_multi(void *state, bool bf16_state, const void *x, const float *dt,
+                                    const float *A, const void *B, const void *C,
+                                    const float *D, void *y, bool bf16, int batch, int ntok,
+                                    int H, int P, int N, int G, const SsdFuse &fuse,
+                                    cudaStream_t stream);
+int ssd_decode_multi_max_headdim(int N);
+
 size_t ssd_simt_smem_bytes(int N);
 
 // Test hooks of the ABI layer: the fault to inject (0 = none) and the limit

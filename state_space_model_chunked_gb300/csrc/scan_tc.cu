@@ -105,6 +105,7 @@ constexpr uint32_t kIdY = idesc_bf16_f32(128, 64, false, true);     // M(TMEM) .
 // control-region offsets (bytes)
 constexpr uint32_t kOffTslot = 192;       // (barriers occupy bytes 0 .. 159)
 constexpr uint32_t kOffAbort = 196;
+constexpr uint32_t kOffLast = 200;        // int[3]: last tile of X, B, C loads issued
 // scan kernel factor slot, written by the factor warp for one tile at a time
 constexpr uint32_t kOffAch = 256;         // float[2][4]: a at the end of each 32-token block
 constexpr uint32_t kOffAt = 512;          // float[2][128]: a_t, chunk-local inclusive cumsum of dt A
@@ -255,8 +256,11 @@ ssd_varlen_plan_kernel(const int *__restrict__ cu, int nseq, int seg_tiles, int 
 }
 
 // A bounded wait on an mbarrier phase.  After any wait of the CTA has run out
-// (abort_flag set) every later wait returns false at once, and the caller
-// leaves its loop: the CTA then drains what it has in flight and exits.
+// (abort_flag set) every later wait returns false at once.  The producers and
+// the MMA issuers then stop issuing; the transform warps run out their loops
+// without waiting (their tensor-memory loads and stores are synchronous and
+// stay inside the CTA's own allocation, and they store no y by TMA); the CTA
+// drains what it has in flight at its exit and frees its tensor memory.
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int *abort_flag,
                                          unsigned int *err, uint64_t limit_ns) {
     if (*abort_flag) return false;
@@ -408,9 +412,14 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
         mbar_init(bar(10), 2);
         mbar_init(bar(11), kXWarps);
         mbar_init(bar(12), HG);                // one commit per masked-product issuer
-        mbar_init(bar(13), 1);
+        // fault injection (host-set, tests only): in the first segment the
+        // factors-ready barrier waits for a second arrival that never comes,
+        // so the transform warps' first wait for the factors runs out
+        mbar_init(bar(13), (a.fault == kSsdFaultWithholdSignal && sigma == 0) ? 2 : 1);
         mbar_init(bar(18), 1);
         mbar_init(bar(19), 1);
+        int *last = reinterpret_cast<int *>(smem + kOffLast);
+        last[0] = last[1] = last[2] = -1;
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -471,15 +480,11 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
                 tma_load_4d(stg, &mapC, bar(stage), 0, g, trow + t0, tb);
                 tma_load_4d(stg + kBlk, &mapC, bar(stage), 64, g, trow + t0, tb);
             }
-            // every load this thread issued has landed before the CTA exits (after
-            // a wait ran out, its consumers may never have waited for it).  Loads
-            // go out tile by tile, so the last two tiles of X and C (one per
-            // stage) and the last of B hold the only phases that can be pending.
-            for (int k = lastX; k >= 0 && k >= lastX - 1; --k)
-                drain_bar(bar(14 + (k & 1)), (k >> 1) & 1, abort_flag, a.err, a.wait_ns);
-            for (int k = lastC; k >= 0 && k >= lastC - 1; --k)
-                drain_bar(bar(k & 1), (k >> 1) & 1, abort_flag, a.err, a.wait_ns);
-            if (lastB >= 0) drain_bar(bar(4), lastB & 1, abort_flag, a.err, a.wait_ns);
+            // for the drain at exit after a wait ran out
+            int *last = reinterpret_cast<int *>(smem + kOffLast);
+            last[0] = lastX;
+            last[1] = lastB;
+            last[2] = lastC;
         }
     } else if (warp == kIssuerA) {
         // ------------------------------------------------------ MMA issuer
@@ -546,9 +551,6 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
                 }
                 mma_commit(bar(10));
             }
-            // every product this thread issued is complete before TMEM is freed
-            mma_commit(bar(18));
-            drain_bar(bar(18), 0, abort_flag, a.err, a.wait_ns);
         }
     } else if (warp == kIssuerB) {
         // ------------------------------------------------ MMA issuer B
@@ -597,8 +599,6 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
                 wait_bar(bar(11), (ntile - 1) & 1, abort_flag, a.err, a.wait_ns))
                 store_y(ntile - 1);
             bulk_wait_all();                                 // y stores complete before exit
-            mma_commit(bar(19));
-            drain_bar(bar(19), 0, abort_flag, a.err, a.wait_ns);
         }
     } else if (warp == fac_warp) {
         // ------------------------------------------------------ decay factors
@@ -655,7 +655,7 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
                 for (int i = 0; i < 4; ++i) fv[h][i] = __expf(ae - fa[h][i]) * dn[h][i];
             }
         };
-        auto publish = [&](bool first) {
+        auto publish = [&]() {
 #pragma unroll
             for (int h = 0; h < HG; ++h) {
                 *reinterpret_cast<float4 *>(at_s + h * kTile + 4 * lane) =
@@ -675,21 +675,19 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
             __syncwarp();
             // fault injection (host-set, tests only): the first segment's first
             // signal is withheld, so the transform warps' wait for it runs out
-            const bool withhold = first && a.fault == kSsdFaultWithholdSignal && sigma == 0;
-            if (lane == 0 && !withhold) mbar_arrive(bar(13));
+            if (lane == 0) mbar_arrive(bar(13));
         };
         if (ntile > 0) {
             load_dt4(0);
             factors(0);
-            publish(true);
+            publish();
             if (ntile > 1) load_dt4(1);
         }
         for (int it = 0; it + 1 < ntile; ++it) {
             factors(it + 1);                                 // tile it + 1
             if (it + 2 < ntile) load_dt4(it + 2);            // in flight meanwhile
-            if (!wait_bar_warp(bar(7), it & 1, abort_flag, a.err, a.wait_ns))   // masks of tile it built
-                break;
-            publish(false);
+            wait_bar_warp(bar(7), it & 1, abort_flag, a.err, a.wait_ns);
+            publish();
         }
     } else {
         // ------------------------------------------- transform / epilogue
@@ -707,8 +705,8 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
         // tile's), a_t, the tile's 32-block ends a_e(j) and the state weight
         // w_t = exp(a_end - a_t) dt_t
         float at[HG], ach[HG][4], wt[HG];
-        auto load_factors = [&](int it) -> bool {
-            if (!wait_bar_warp(bar(13), it & 1, abort_flag, a.err, a.wait_ns)) return false;
+        auto load_factors = [&](int it) {
+            wait_bar_warp(bar(13), it & 1, abort_flag, a.err, a.wait_ns);
 #pragma unroll
             for (int h = 0; h < HG; ++h) {
                 const float4 e = *reinterpret_cast<const float4 *>(ach_s + 4 * h);
@@ -720,17 +718,14 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
                 const float aq = q == 0 ? e.x : (q == 1 ? e.y : (q == 2 ? e.z : e.w));
                 wt[h] = v_s[h * kTile + row] * __expf(e.w - aq);
             }
-            return true;
         };
 
         // ---- all heads of tile it: entering state -> bf16 operand (MN-major rows n),
         //      state scaled by the tile decay, and Xt = w o X
-        auto prep_tile = [&](int it) -> bool {
+        auto prep_tile = [&](int it) {
             const uint8_t *stg_ptr = tiles_ptr + (it & 1) * kStage;
-            if (!wait_bar_warp(bar(14 + (it & 1)), (it >> 1) & 1, abort_flag, a.err, a.wait_ns))
-                return false;                                                   // X landed
-            if (it > 0 && !wait_bar_warp(bar(9), (it - 1) & 1, abort_flag, a.err, a.wait_ns))
-                return false;
+            wait_bar_warp(bar(14 + (it & 1)), (it >> 1) & 1, abort_flag, a.err, a.wait_ns);
+            if (it > 0) wait_bar_warp(bar(9), (it - 1) & 1, abort_flag, a.err, a.wait_ns);
             tc_fence_after();
             if (it == 0 && sigma > 0) griddep_wait();   // entering states of later segments
 #pragma unroll
@@ -782,14 +777,16 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(8));
-            return true;
         };
 
         // Software pipeline: the next tile's state prep runs while the tensor core
         // finishes this tile, then this tile's epilogue.  A wait that fails (one
         // of the CTA's waits ran out) ends the loop.
-        bool ok = ntile > 0 && load_factors(0) && prep_tile(0);
-        for (int it = 0; ok && it < ntile; ++it) {
+        if (ntile > 0) {
+            load_factors(0);
+            prep_tile(0);
+        }
+        for (int it = 0; it < ntile; ++it) {
             const int t0 = (k0 + it) * kTile;
             const int stage = it & 1;
             const uint8_t *stg_ptr = tiles_ptr + stage * kStage;
@@ -801,7 +798,7 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
             //      the diagonal both factors are <= 1; on the diagonal block R_t is
             //      >= 1 but bounded by the block's own decay, and a block whose decay
             //      exceeds kMaxBlockDecay falls back to one exponential per element.
-            if (!wait_bar_warp(bar(6), it & 1, abort_flag, a.err, a.wait_ns)) break;
+            wait_bar_warp(bar(6), it & 1, abort_flag, a.err, a.wait_ns);
             tc_fence_after();
             {
                 const int j = wg;
@@ -870,7 +867,10 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
             float e_at_t[HG];
 #pragma unroll
             for (int h = 0; h < HG; ++h) e_at_t[h] = __expf(at[h]);
-            if (it + 1 < ntile && !(load_factors(it + 1) && prep_tile(it + 1))) break;
+            if (it + 1 < ntile) {
+                load_factors(it + 1);
+                prep_tile(it + 1);
+            }
 
             // ---- epilogue: y = Yd + exp(a_t) Yo + D x, staged as bf16 in this
             //      stage's C blocks (free once the tile's off-diagonal product is
@@ -894,7 +894,7 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
                     for (int q = 0; q < np / 8; ++q) zv[q] = *reinterpret_cast<const uint4 *>(zrow + 8 * q);
                 }
             }
-            if (!wait_bar_warp(bar(10), it & 1, abort_flag, a.err, a.wait_ns)) break;
+            wait_bar_warp(bar(10), it & 1, abort_flag, a.err, a.wait_ns);
             tc_fence_after();
             {
                 // selects, not dynamic indexing (which would move the arrays to local memory)
@@ -980,6 +980,29 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
     }
     tc_fence_before();
     __syncthreads();
+    if (*abort_flag) {
+        // A wait ran out: before TMEM is freed and the CTA exits, every product
+        // either issuer issued is complete (each commits once more, on barrier
+        // 18 or 19, and waits) and every load the producer issued has landed
+        // (its consumers may never have waited for it).  Loads go out tile by
+        // tile, so the last two tiles of X and C (one per stage) and the last
+        // of B hold the only phases that can still be pending.
+        if (lane == 0 && (warp == kIssuerA || warp == kIssuerB)) {
+            const int b2 = warp == kIssuerA ? 18 : 19;
+            mma_commit(bar(b2));
+            drain_bar(bar(b2), 0, abort_flag, a.err, a.wait_ns);
+        }
+        if (threadIdx.x == 0) {
+            const int *last = reinterpret_cast<const int *>(smem + kOffLast);
+            const int lastX = last[0], lastB = last[1], lastC = last[2];
+            for (int k = lastX; k >= 0 && k >= lastX - 1; --k)
+                drain_bar(bar(14 + (k & 1)), (k >> 1) & 1, abort_flag, a.err, a.wait_ns);
+            for (int k = lastC; k >= 0 && k >= lastC - 1; --k)
+                drain_bar(bar(k & 1), (k >> 1) & 1, abort_flag, a.err, a.wait_ns);
+            if (lastB >= 0) drain_bar(bar(4), lastB & 1, abort_flag, a.err, a.wait_ns);
+        }
+        __syncthreads();
+    }
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
@@ -1048,6 +1071,7 @@ ssd_tc_segment_kernel(const __grid_constant__ CUtensorMap mapB,
             mbar_init(bar(9 + i), 1);
         }
         mbar_init(bar(12), 1);
+        *reinterpret_cast<int *>(smem + kOffLast) = 0;
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -1082,12 +1106,7 @@ ssd_tc_segment_kernel(const __grid_constant__ CUtensorMap mapB,
                     tma_load_4d(stg + kBBytes + h * kXBytes, &mapX, bar(stage), 0, h0 + h,
                                 trow + t0, tb);
             }
-            // every issued load has landed before the CTA exits: the last load of
-            // each stage (tile issued - 1 - i) completes that stage's phases
-            for (int i = 0; i < kStages && i < issued; ++i) {
-                const int it = issued - 1 - i;
-                drain_bar(bar(it % kStages), (it / kStages) & 1, abort_flag, a.err, a.wait_ns);
-            }
+            *reinterpret_cast<int *>(smem + kOffLast) = issued;   // for the drain at exit
         }
     } else if (warp == 1) {
         // ------------------------------------------------------ MMA issuer
@@ -1108,7 +1127,6 @@ ssd_tc_segment_kernel(const __grid_constant__ CUtensorMap mapB,
                 mma_commit(bar(3 + stage));
             }
             mma_commit(bar(12));
-            drain_bar(bar(12), 0, abort_flag, a.err, a.wait_ns);   // all products complete
         }
     } else if (warp == kSegFacWarp) {
         // ------------------------------------------------- token weights
@@ -1236,6 +1254,21 @@ ssd_tc_segment_kernel(const __grid_constant__ CUtensorMap mapB,
     }
     tc_fence_before();
     __syncthreads();
+    if (*abort_flag) {
+        // A wait ran out: every issued load has landed (the last load of each
+        // stage, tile issued - 1 - i, completes that stage's phases) and every
+        // product is complete (the issuer's last commit, on barrier 12) before
+        // TMEM is freed and the CTA exits.
+        if (threadIdx.x == 0) {
+            const int issued = *reinterpret_cast<const int *>(smem + kOffLast);
+            for (int i = 0; i < kStages && i < issued; ++i) {
+                const int it = issued - 1 - i;
+                drain_bar(bar(it % kStages), (it / kStages) & 1, abort_flag, a.err, a.wait_ns);
+            }
+            drain_bar(bar(12), 0, abort_flag, a.err, a.wait_ns);
+        }
+        __syncthreads();
+    }
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, kCols);

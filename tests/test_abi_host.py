@@ -258,3 +258,28 @@ def test_plain_c_caller(tmp_path, lib):
     out = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
     assert out.returncode == 0, out.stdout + out.stderr
     assert "c abi ok" in out.stdout
+
+
+def _dec_multi(lib, **kw):
+    a = dict(state=_fake(0x1000), sdt=0, x=_fake(0x2000), dt=_fake(0x3000), A=_fake(0x4000),
+             B=_fake(0x5000), C=_fake(0x6000), D=None, tr=None, z=None, dtype=1, b=2, T=4, H=4,
+             P=16, N=16, G=1, y=_fake(0x7000), stream=None)
+    a.update(kw)
+    return lib.ssd_state_update_multi(a["state"], a["sdt"], a["x"], a["dt"], a["A"], a["B"],
+                                      a["C"], a["D"], a["tr"], a["z"], a["dtype"], a["b"],
+                                      a["T"], a["H"], a["P"], a["N"], a["G"], a["y"],
+                                      a["stream"])
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(T=0), INVALID),                    # no token
+    (dict(x=None), INVALID),
+    (dict(H=6, G=4), INVALID),
+    (dict(sdt=1, dtype=0), UNSUPPORTED),     # bf16 state needs bf16 inputs
+    (dict(N=24), UNSUPPORTED),               # dstate not a power of two
+    (dict(P=65, N=128), UNSUPPORTED),        # more rows than the kernel keeps on chip
+    (dict(P=129, N=64), UNSUPPORTED),
+    (dict(z=_fake(0x8004)), INVALID),        # misaligned gate
+])
+def test_multi_token_decode_rejects_bad_arguments(lib, kw, expect):
+    assert _dec_multi(lib, **kw) == expect

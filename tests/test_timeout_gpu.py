@@ -1,7 +1,8 @@
 """The bounded device-side waits, made to run out on purpose without any
-GPU fault: a host-set test hook makes the tensor-core scan kernel withhold one
-signal, so the wait for it ends at a short limit; the CTA then lets its issued
-copies and tensor-core products complete, frees its tensor memory and exits.
+GPU fault: a host-set test hook makes one barrier of the tensor-core scan
+kernel wait for an arrival that never comes, so the wait for it ends at a
+short limit; the CTA then lets its issued copies and tensor-core products
+complete, frees its tensor memory and exits.
 The host reads SSD_ERR_TIMEOUT from the device error word, and the next call
 on the same context is correct."""
 import pytest
