@@ -387,23 +387,25 @@ __host__ __device__ inline size_t multi_smem_floats(int P, int N, bool gated) {
     return (size_t)kMultiTok * ((gated ? 3 : 2) * P + 2 * N + 4);
 }
 // threads per CTA and float4 per thread of a row for a state width
-__host__ __device__ inline int multi_threads(int N) { return N > 128 ? 256 : 128; }
-__host__ __device__ inline int multi_vpt(int N) { return N >= 16 ? 4 : N / 4; }
+__host__ __device__ constexpr int multi_threads(int N) { return N > 128 ? 256 : 128; }
+__host__ __device__ constexpr int multi_vpt(int N) { return N >= 16 ? 4 : N / 4; }
 
-template <typename T, typename S, int VPT, int NT, bool kFuse>
-__global__ void __launch_bounds__(NT, 512 / NT)
+template <typename T, typename S, int N, bool kFuse>
+__global__ void __launch_bounds__(multi_threads(N), 512 / multi_threads(N))
 ssd_decode_multi_kernel(S *__restrict__ state, const T *__restrict__ x,
                         const float *__restrict__ dt, const float *__restrict__ A,
                         const T *__restrict__ Bm, const T *__restrict__ Cm,
                         const float *__restrict__ D, T *__restrict__ y, int ntok, int H, int P,
-                        int N, int G, const SsdFuse fuse) {
+                        int G, const SsdFuse fuse) {
     using namespace ssdptx;
     extern __shared__ float msm[];
+    constexpr int NT = multi_threads(N);
+    constexpr int VPT = multi_vpt(N);
+    constexpr int tpr = N / (4 * VPT);     // threads per row: a power of two <= 16
+    constexpr int rpp = NT / tpr;          // rows per pass
     const int bh = blockIdx.x;             // b * H + h
     const int b = bh / H, h = bh - b * H;
     const int g = h / (H / G);
-    const int tpr = N / (4 * VPT);         // threads per row: a power of two <= 16
-    const int rpp = NT / tpr;              // rows per pass
     const int lane_n = threadIdx.x & (tpr - 1);
     const int r0 = threadIdx.x / tpr;
     const float Ah = A[h];
@@ -431,17 +433,14 @@ ssd_decode_multi_kernel(S *__restrict__ state, const T *__restrict__ x,
                             : make_float4(0.f, 0.f, 0.f, 0.f);
     }
     auto rescale = [&](float f) {
-        const uint64_t f2 = pack_f32x2(f, f);
+        const float2 f2 = make_float2(f, f);
 #pragma unroll
         for (int i = 0; i < kMultiRows; ++i)
 #pragma unroll
             for (int v = 0; v < VPT; ++v) {
-                const uint64_t lo = mul_f32x2(pack_f32x2(s[i][v].x, s[i][v].y), f2);
-                const uint64_t hi = mul_f32x2(pack_f32x2(s[i][v].z, s[i][v].w), f2);
-                s[i][v] = make_float4(__uint_as_float((uint32_t)lo),
-                                      __uint_as_float((uint32_t)(lo >> 32)),
-                                      __uint_as_float((uint32_t)hi),
-                                      __uint_as_float((uint32_t)(hi >> 32)));
+                const float2 lo = fmul2(make_float2(s[i][v].x, s[i][v].y), f2);
+                const float2 hi = fmul2(make_float2(s[i][v].z, s[i][v].w), f2);
+                s[i][v] = make_float4(lo.x, lo.y, hi.x, hi.y);
             }
     };
 
@@ -501,46 +500,43 @@ ssd_decode_multi_kernel(S *__restrict__ state, const T *__restrict__ x,
             if (rs != 1.f) rescale(rs);       // uniform: every thread reads the same slot
             // update hs += u B and the row's partial readout C . hs (packed
             // pairs), one float4 of B and C at a time for all rows
-            uint64_t u2[kMultiRows], a2[kMultiRows];
+            float2 u2[kMultiRows], a2[kMultiRows];
 #pragma unroll
             for (int i = 0; i < kMultiRows; ++i) {
                 const int p = r0 + i * rpp;
                 const float u = p < P ? us[t * P + p] : 0.f;
-                u2[i] = pack_f32x2(u, u);
-                a2[i] = 0;
+                u2[i] = make_float2(u, u);
+                a2[i] = make_float2(0.f, 0.f);
             }
 #pragma unroll
             for (int v = 0; v < VPT; ++v) {
                 const float4 Bv = *reinterpret_cast<const float4 *>(Bs + t * N + 4 * (lane_n + v * tpr));
                 const float4 Cv = *reinterpret_cast<const float4 *>(Cs + t * N + 4 * (lane_n + v * tpr));
-                const uint64_t b01 = pack_f32x2(Bv.x, Bv.y), b23 = pack_f32x2(Bv.z, Bv.w);
-                const uint64_t c01 = pack_f32x2(Cv.x, Cv.y), c23 = pack_f32x2(Cv.z, Cv.w);
+                const float2 b01 = make_float2(Bv.x, Bv.y), b23 = make_float2(Bv.z, Bv.w);
+                const float2 c01 = make_float2(Cv.x, Cv.y), c23 = make_float2(Cv.z, Cv.w);
 #pragma unroll
                 for (int i = 0; i < kMultiRows; ++i) {
-                    const uint64_t q01 = fma_f32x2(u2[i], b01, pack_f32x2(s[i][v].x, s[i][v].y));
-                    const uint64_t q23 = fma_f32x2(u2[i], b23, pack_f32x2(s[i][v].z, s[i][v].w));
-                    s[i][v] = make_float4(__uint_as_float((uint32_t)q01),
-                                          __uint_as_float((uint32_t)(q01 >> 32)),
-                                          __uint_as_float((uint32_t)q23),
-                                          __uint_as_float((uint32_t)(q23 >> 32)));
-                    a2[i] = fma_f32x2(c01, q01, a2[i]);
-                    a2[i] = fma_f32x2(c23, q23, a2[i]);
+                    const float2 q01 = ffma2(u2[i], b01, make_float2(s[i][v].x, s[i][v].y));
+                    const float2 q23 = ffma2(u2[i], b23, make_float2(s[i][v].z, s[i][v].w));
+                    s[i][v] = make_float4(q01.x, q01.y, q23.x, q23.y);
+                    a2[i] = ffma2(c01, q01, a2[i]);
+                    a2[i] = ffma2(c23, q23, a2[i]);
                 }
             }
             float acc[kMultiRows];
 #pragma unroll
-            for (int i = 0; i < kMultiRows; ++i)
-                acc[i] = __uint_as_float((uint32_t)a2[i]) + __uint_as_float((uint32_t)(a2[i] >> 32));
+            for (int i = 0; i < kMultiRows; ++i) acc[i] = a2[i].x + a2[i].y;
             // reduce over the tpr threads of each row: at exchange k (offset
             // tpr >> (k+1)) a thread keeps one half of its remaining rows and
             // adds its partner's partials of them; once one row is left, plain
             // butterflies finish the sum
+            // (all of it resolved at compile time from tpr)
+            int base = 0;
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
+                constexpr int kHalf0 = kMultiRows / 2;
                 const int o = tpr >> (k + 1);
-                if (o == 0) break;
-                if (k < 2) {
-                    constexpr int kHalf0 = kMultiRows / 2;
+                if (o > 0 && k < 2) {
                     const int half = kHalf0 >> k;
                     const bool up = (lane_n & o) != 0;
 #pragma unroll
@@ -551,22 +547,15 @@ ssd_decode_multi_kernel(S *__restrict__ state, const T *__restrict__ x,
                             acc[j] = keep + __shfl_xor_sync(0xffffffffu, send, o);
                         }
                     }
-                } else {
+                    if (up) base += half;
+                } else if (o > 0) {
                     acc[0] += __shfl_xor_sync(0xffffffffu, acc[0], o);
                 }
             }
-            // rows this thread now holds: base + j for j < left, base from the
-            // halves it kept; the lowest thread of each set of equal holders writes
-            int base = 0, left = kMultiRows;
-#pragma unroll
-            for (int k = 0; k < 2; ++k) {
-                const int o = tpr >> (k + 1);
-                if (o > 0) {
-                    left >>= 1;
-                    if (lane_n & o) base += left;
-                }
-            }
-            const int low = tpr > 4 ? tpr / 4 - 1 : 0;
+            // rows this thread now holds: base + j for j < left; the lowest
+            // thread of each set of equal holders writes them
+            constexpr int left = tpr >= 4 ? 1 : (tpr == 2 ? 2 : kMultiRows);
+            constexpr int low = tpr > 4 ? tpr / 4 - 1 : 0;
             if ((lane_n & low) == 0) {
                 const float sg = sig[t];
 #pragma unroll
@@ -593,18 +582,18 @@ ssd_decode_multi_kernel(S *__restrict__ state, const T *__restrict__ x,
     }
 }
 
-template <typename T, typename S, int VPT, int NT, bool kFuse>
+template <typename T, typename S, int N, bool kFuse>
 cudaError_t launch_multi_k(S *state, const void *x, const float *dt, const float *A,
                            const void *B, const void *C, const float *D, void *y, int batch,
-                           int ntok, int H, int P, int N, int G, const SsdFuse &fuse,
+                           int ntok, int H, int P, int G, const SsdFuse &fuse,
                            cudaStream_t stream) {
     const size_t smem = multi_smem_floats(P, N, kFuse && fuse.z != nullptr) * sizeof(float);
-    cudaError_t e = cudaFuncSetAttribute(ssd_decode_multi_kernel<T, S, VPT, NT, kFuse>,
+    cudaError_t e = cudaFuncSetAttribute(ssd_decode_multi_kernel<T, S, N, kFuse>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    ssd_decode_multi_kernel<T, S, VPT, NT, kFuse><<<(unsigned)((size_t)batch * H), NT, smem,
-                                                    stream>>>(
-        state, (const T *)x, dt, A, (const T *)B, (const T *)C, D, (T *)y, ntok, H, P, N, G, fuse);
+    ssd_decode_multi_kernel<T, S, N, kFuse><<<(unsigned)((size_t)batch * H), multi_threads(N),
+                                              smem, stream>>>(
+        state, (const T *)x, dt, A, (const T *)B, (const T *)C, D, (T *)y, ntok, H, P, G, fuse);
     return cudaGetLastError();
 }
 
@@ -613,20 +602,22 @@ cudaError_t launch_multi_t(S *state, const void *x, const float *dt, const float
                            const void *B, const void *C, const float *D, void *y, int batch,
                            int ntok, int H, int P, int N, int G, const SsdFuse &fuse,
                            cudaStream_t stream) {
-    if (N > 128)
-        return launch_multi_k<T, S, 4, 256, kFuse>(state, x, dt, A, B, C, D, y, batch, ntok, H,
-                                                   P, N, G, fuse, stream);
-    switch (multi_vpt(N)) {
-        case 1:
-            return launch_multi_k<T, S, 1, 128, kFuse>(state, x, dt, A, B, C, D, y, batch, ntok,
-                                                       H, P, N, G, fuse, stream);
-        case 2:
-            return launch_multi_k<T, S, 2, 128, kFuse>(state, x, dt, A, B, C, D, y, batch, ntok,
-                                                       H, P, N, G, fuse, stream);
+#define SSD_MULTI_N(NN)                                                                    \
+    case NN:                                                                               \
+        return launch_multi_k<T, S, NN, kFuse>(state, x, dt, A, B, C, D, y, batch, ntok, H, P, \
+                                               G, fuse, stream)
+    switch (N) {
+        SSD_MULTI_N(4);
+        SSD_MULTI_N(8);
+        SSD_MULTI_N(16);
+        SSD_MULTI_N(32);
+        SSD_MULTI_N(64);
+        SSD_MULTI_N(128);
+        SSD_MULTI_N(256);
         default:
-            return launch_multi_k<T, S, 4, 128, kFuse>(state, x, dt, A, B, C, D, y, batch, ntok,
-                                                       H, P, N, G, fuse, stream);
+            return cudaErrorInvalidValue;   // dstate is checked by the caller
     }
+#undef SSD_MULTI_N
 }
 
 }  // namespace
