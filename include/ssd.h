@@ -263,8 +263,8 @@ ssd_status ssd_scan_profile_events(cudaEvent_t before, cudaEvent_t after);
  * GPU that loads the library until the process exits.  Allocates nothing.
  *   - Returns SSD_ERR_WORKSPACE when the shape needs more scratch than
  *     SSD_STATIC_SCRATCH_BYTES (ssd_scan_workspace_bytes() tells how much).
- *     The 2.7B-shaped 65536-token layer (80 heads, 45 MiB of segment states
- *     on a 152-SM GB300) fits.
+ *     The 2.7B-shaped 65536-token layer (80 heads, 23 MB of bf16 segment
+ *     states on a 152-SM GB300) fits.
  *   - The first call on each device looks up the scratch address for that
  *     device; make that first call before any stream capture.
  *   - All calls share the one scratch array: calls whose work overlaps on the

@@ -113,7 +113,9 @@ constexpr uint32_t kOffV = 1536;          // float[2][128]: exp(a_end(32-block o
 
 struct TcArgs {
     const float *dt, *A, *D, *init;
-    float *ws_state;       // [b][nseg-1][H][P][N]: segment contributions, then entering states
+    // [b][nseg-1][H][P][N] bf16: segment contributions, then entering states
+    // (fp32 in TMEM and in the chaining arithmetic, rounded to bf16 in HBM)
+    __nv_bfloat16 *ws_state;
     float *ws_decay;       // [b][nseg-1][H]: segment total decay
     __nv_bfloat16 *y;
     float *fin;
@@ -733,15 +735,18 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
                 const float de = __expf(ach[h][3]);
                 const uint32_t colH = kColH + 64 * h + 16 * wg;
                 uint32_t r[16];
-                if (it == 0) {
+                if (it == 0 && sigma == 0) {
                     const float *src =
-                        sigma == 0 ? (a.init ? a.init + ((size_t)w_seq() * a.H + h0 + h) * kP * kN
-                                             : nullptr)
-                                   : a.ws_state +
-                                         ((size_t)(w_fslot() + sigma - 1) * a.H + h0 + h) * kP * kN;
+                        a.init ? a.init + ((size_t)w_seq() * a.H + h0 + h) * kP * kN : nullptr;
 #pragma unroll
                     for (int j = 0; j < 16; ++j)
                         r[j] = __float_as_uint(src ? src[(size_t)(16 * wg + j) * kN + row] : 0.f);
+                } else if (it == 0) {
+                    const __nv_bfloat16 *src =
+                        a.ws_state + ((size_t)(w_fslot() + sigma - 1) * a.H + h0 + h) * kP * kN;
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        r[j] = __float_as_uint(__bfloat162float(src[(size_t)(16 * wg + j) * kN + row]));
                 } else {
                     tmem_ld16(tq + colH, r);
                     tmem_ld_wait();
@@ -1244,11 +1249,11 @@ ssd_tc_segment_kernel(const __grid_constant__ CUtensorMap mapB,
                 uint32_t r[32];
                 tmem_ld32(tq + 64 * h + 32 * wg, r);
                 tmem_ld_wait();
-                float *dst = a.ws_state +
-                             ((size_t)(w_fslot() + sigma) * a.H + h0 + h) * kP * kN;
+                __nv_bfloat16 *dst = a.ws_state +
+                                     ((size_t)(w_fslot() + sigma) * a.H + h0 + h) * kP * kN;
 #pragma unroll
                 for (int j = 0; j < 32; ++j)
-                    dst[(size_t)(32 * wg + j) * kN + row] = __uint_as_float(r[j]);
+                    dst[(size_t)(32 * wg + j) * kN + row] = __float2bfloat16_rn(__uint_as_float(r[j]));
             }
         }
     }
@@ -1282,7 +1287,7 @@ ssd_tc_segment_kernel(const __grid_constant__ CUtensorMap mapB,
 // (batched: sequence q has base q (nseg-1); packed: fslot0[q] .. fslot0[q+1]).
 // Loads are issued a batch ahead of the dependent FMA chain.
 __global__ void __launch_bounds__(256)
-ssd_tc_segment_pass_kernel(float *__restrict__ ws_state, const float *__restrict__ ws_decay,
+ssd_tc_segment_pass_kernel(__nv_bfloat16 *__restrict__ ws_state, const float *__restrict__ ws_decay,
                            const float *__restrict__ init, int nseqs, int H, int nseg,
                            const int *__restrict__ fslot0) {
     constexpr int kBatch = 8;
@@ -1302,9 +1307,12 @@ ssd_tc_segment_pass_kernel(float *__restrict__ ws_state, const float *__restrict
     const int count = fslot0 ? fslot0[q + 1] - base : nseg - 1;
     float4 hv = make_float4(0.f, 0.f, 0.f, 0.f);
     if (init) hv = reinterpret_cast<const float4 *>(init)[((size_t)q * H + h) * per_head + e];
-    float4 *st = reinterpret_cast<float4 *>(ws_state);
+    // four bf16 state elements per thread: contributions in, entering states out
+    uint2 *st = reinterpret_cast<uint2 *>(ws_state);
+    auto lo = [](uint32_t w) { return __uint_as_float(w << 16); };
+    auto hi = [](uint32_t w) { return __uint_as_float(w & 0xffff0000u); };
     for (int s0 = 0; s0 < count; s0 += kBatch) {
-        float4 f[kBatch];
+        uint2 f[kBatch];
         float d[kBatch];
 #pragma unroll
         for (int i = 0; i < kBatch; ++i) {
@@ -1318,11 +1326,11 @@ ssd_tc_segment_pass_kernel(float *__restrict__ ws_state, const float *__restrict
         for (int i = 0; i < kBatch; ++i) {
             if (s0 + i < count) {
                 const size_t slot = (size_t)(base + s0 + i) * H + h;
-                hv.x = fmaf(d[i], hv.x, f[i].x);
-                hv.y = fmaf(d[i], hv.y, f[i].y);
-                hv.z = fmaf(d[i], hv.z, f[i].z);
-                hv.w = fmaf(d[i], hv.w, f[i].w);
-                st[slot * per_head + e] = hv;
+                hv.x = fmaf(d[i], hv.x, lo(f[i].x));
+                hv.y = fmaf(d[i], hv.y, hi(f[i].x));
+                hv.z = fmaf(d[i], hv.z, lo(f[i].y));
+                hv.w = fmaf(d[i], hv.w, hi(f[i].y));
+                st[slot * per_head + e] = make_uint2(pack_bf16x2(hv.x, hv.y), pack_bf16x2(hv.z, hv.w));
             }
         }
     }
@@ -1506,7 +1514,7 @@ SsdTcPlan ssd_tc_plan(int batch, int L, int H, int P, int N, int G, int num_sms)
     p.nslots = batch * (p.nseg - 1);
     p.items = batch * p.nseg;
     if (p.nseg > 1) {
-        const size_t state = (size_t)batch * (p.nseg - 1) * H * kP * kN * sizeof(float);
+        const size_t state = (size_t)batch * (p.nseg - 1) * H * kP * kN * sizeof(__nv_bfloat16);
         const size_t decay = (size_t)batch * (p.nseg - 1) * H * sizeof(float);
         p.workspace = ((state + 255) / 256) * 256 + ((decay + 255) / 256) * 256;
         p.launches = 3;
@@ -1587,7 +1595,7 @@ SsdTcPlan ssd_tc_plan_varlen(int nseq, const int *cu, int H, int P, int N, int G
     p.nseg = 0;                    // per sequence
     p.seg_heads = p.heads_per_cta;
     if ((H / G) % 4 == 0 && (long)(H / 4) * slots >= num_sms) p.seg_heads = 4;
-    const size_t state = (size_t)slots * H * kP * kN * sizeof(float);
+    const size_t state = (size_t)slots * H * kP * kN * sizeof(__nv_bfloat16);
     const size_t decay = (size_t)slots * H * sizeof(float);
     const size_t table = 2 * (size_t)(nseq + 1) * sizeof(int);
     p.workspace = ((state + 255) / 256) * 256 + ((decay + 255) / 256) * 256 +
@@ -1632,10 +1640,10 @@ cudaError_t ssd_launch_scan_tc(const SsdTcPlan &plan, const void *x, const float
     args.D = D;
     args.init = init;
     if (plan.nslots > 0 || plan.varlen) {
-        const size_t state = (size_t)plan.nslots * H * kP * kN * sizeof(float);
+        const size_t state = (size_t)plan.nslots * H * kP * kN * sizeof(__nv_bfloat16);
         const size_t decay = (size_t)plan.nslots * H * sizeof(float);
         char *ws = static_cast<char *>(workspace);
-        args.ws_state = reinterpret_cast<float *>(ws);
+        args.ws_state = reinterpret_cast<__nv_bfloat16 *>(ws);
         args.ws_decay = reinterpret_cast<float *>(ws + ((state + 255) / 256) * 256);
         if (plan.varlen) {
             int *table = reinterpret_cast<int *>(ws + ((state + 255) / 256) * 256 +
