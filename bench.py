@@ -629,6 +629,43 @@ def time_fused_steps(shape, device, reps=20):
             "note": "eager calls (host overhead included in both)"}
 
 
+def time_gated_norm_pass(shape, device, reps=20):
+    """Cost of the step the scan kernels do not fuse: the gated RMS norm over
+    all heads of a token (y * silu(z), then x / rms(x) * w over nheads x
+    headdim), as a separate pass with torch ops on the layer's y and z.  It
+    reads y and z and writes the result: 3 bytes moved per output byte."""
+    import torch
+    import torch.nn.functional as F
+    b, L, H, P = shape.batch, shape.seqlen, shape.nheads, shape.headdim
+    g = torch.Generator(device=device)
+    g.manual_seed(9)
+    y = torch.randn((b, L, H * P), generator=g, device=device).to(torch.bfloat16)
+    z = torch.randn((b, L, H * P), generator=g, device=device).to(torch.bfloat16)
+    w = torch.ones((H * P,), device=device, dtype=torch.bfloat16)
+    out = torch.empty_like(y)
+
+    def one():
+        out.copy_(F.rms_norm(y * F.silu(z), (H * P,), w, eps=1e-5))
+
+    for _ in range(3):
+        one()
+    stream = torch.cuda.current_stream(device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(device)
+    e0.record(stream)
+    for _ in range(reps):
+        one()
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    ms = e0.elapsed_time(e1) / reps
+    byts = 3 * y.numel() * 2
+    del y, z, out
+    torch.cuda.empty_cache()
+    return {"workload": shape.name, "ms": ms, "compulsory_bytes": byts,
+            "roofline_ms": byts / 6.79e12 * 1e3,
+            "note": "torch ops (not this library): the unfused gated normalisation after the scan"}
+
+
 def cpu_oracle_sample(shape, heads=None, target_s=10.0, cores=None, max_reps=50):
     """The oracle as it stands on the host cores, on `heads` whole heads of the
     workload (all of them by default; every head is an independent
@@ -826,6 +863,7 @@ def run_gpu(args):
             extra["varlen"] = time_varlen(device, peaks)
             extra["fused_steps"] = [time_fused_steps(gen.SCAN_SHAPES[n], device)
                                     for n in ("mamba2_130m_L4096", WORKLOAD)]
+            extra["gated_norm_separate_pass"] = time_gated_norm_pass(full, device)
     clocks = clk.summary()
 
     e2e_s, h2d, d2h = time_scan_e2e(shape, max(args.steps // 4, 3), args.warmup, device)
