@@ -103,11 +103,12 @@ ssd_decode_kernel(S *__restrict__ state, const T *__restrict__ x,
 
 // Streaming variant for large stacks: a persistent CTA per SM walks its
 // (batch, head) states through a ring of shared-memory stages.  Each stage
-// receives, by bulk copies, one state (32 KB at P 64, N 128) plus that
-// unit's x row and its group's B and C rows, so no global-memory latency sits
-// between the update of one state and the next; the copy engine keeps several
-// states in flight without occupying registers.  The state is updated in
-// place in shared memory and written back by one bulk store.
+// receives, by bulk copies, one fp32 state (32 KB at P 64, N 128) or two
+// consecutive bf16 states, their x rows and their groups' B and C rows, so no
+// global-memory latency sits between the update of one state and the next;
+// the copy engine keeps several states in flight without occupying registers.
+// The states are updated in place in shared memory and written back by one
+// bulk store per stage.
 constexpr int kStreamThreads = 512;
 constexpr int kStreamRows = 4;          // rows each thread updates per pass
 constexpr uint32_t kStreamRing = 229376;   // ring capacity in bytes
@@ -117,15 +118,20 @@ struct StreamLayout {
     uint32_t state_bytes, x_bytes, bc_bytes, stage_bytes;
 };
 
-__host__ __device__ inline StreamLayout stream_layout(int P, int N, int es, int ss) {
+// A stage holds `per` consecutive states, then their x rows, then each
+// one's B and C rows.
+__host__ __device__ inline StreamLayout stream_layout(int P, int N, int es, int ss, int per) {
     StreamLayout l;
     l.state_bytes = (uint32_t)P * N * (uint32_t)ss;
     l.x_bytes = (uint32_t)P * es;
     l.bc_bytes = (uint32_t)N * es;
-    const uint32_t raw = l.state_bytes + l.x_bytes + 2 * l.bc_bytes;
+    const uint32_t raw = (uint32_t)per * (l.state_bytes + l.x_bytes + 2 * l.bc_bytes);
     l.stage_bytes = (raw + 127u) & ~127u;
     return l;
 }
+// states per ring stage: two with bf16 states (a 32 KB stage, as one fp32 state)
+template <typename S>
+__host__ __device__ constexpr int stream_per_stage() { return sizeof(S) < 4 ? 2 : 1; }
 
 template <typename T, typename S, int N, bool kFuse>
 __global__ void __launch_bounds__(kStreamThreads + 32, 1)
@@ -137,8 +143,10 @@ ssd_decode_stream_kernel(S *__restrict__ state, const T *__restrict__ x,
     constexpr int VPT = N > 128 ? 2 : 1;
     using namespace ssdptx;
     extern __shared__ __align__(1024) uint8_t smem[];
-    const StreamLayout L = stream_layout(P, N, (int)sizeof(T), (int)sizeof(S));
+    constexpr int U = stream_per_stage<S>();
+    const StreamLayout L = stream_layout(P, N, (int)sizeof(T), (int)sizeof(S), U);
     const long units = (long)batch * H;
+    const long items = (units + U - 1) / U;   // stage loads of U consecutive states
     const int tid = threadIdx.x;
     // barriers: full[stages] (bulk loads landed), done[stages] (update finished)
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)stages * L.stage_bytes);
@@ -146,10 +154,11 @@ ssd_decode_stream_kernel(S *__restrict__ state, const T *__restrict__ x,
     volatile int *abort_flag = reinterpret_cast<volatile int *>(done + stages);
     const uint32_t sbase = smem_u32(smem);
     constexpr int kComputeWarps = kStreamThreads / 32;
-    // bf16 states halve the bytes per unit, so the per-unit update latency
-    // becomes the limit: groups of compute warps then take alternate units
-    // (timed: fp32 states are fastest with one group, bf16 with four: 0.55 ms
-    // a token at batch 16 against 0.61 with two and 0.77 with one)
+    // bf16 states halve the bytes per state, so the per-state work becomes the
+    // limit: a ring stage then holds two consecutive states (one 32 KB bulk
+    // copy each way, as one fp32 state), and four groups of compute warps take
+    // alternate stages (timed at batch 16: 0.405 ms a token against 0.487 with
+    // one state per stage, 0.55 with one per stage and two groups fewer)
     constexpr int kGroups = sizeof(S) < 4 ? 4 : 1;
     if (tid == 0) {
         for (int i = 0; i < stages; ++i) {
@@ -160,8 +169,10 @@ ssd_decode_stream_kernel(S *__restrict__ state, const T *__restrict__ x,
         fence_mbar_init();
     }
     __syncthreads();
-    const long nk = blockIdx.x < units ? (units - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
-    auto unit_of = [&](long k) { return (long)blockIdx.x + k * (long)gridDim.x; };
+    const long nk = blockIdx.x < items ? (items - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+    // first state and state count of this CTA's k-th stage load
+    auto unit_of = [&](long k) { return ((long)blockIdx.x + k * (long)gridDim.x) * U; };
+    auto count_of = [&](long k) { return (int)min((long)U, units - unit_of(k)); };
 
     if (tid >= kStreamThreads) {
         // ---- copy warp: loads run stages-1 units ahead; each updated state is
@@ -170,17 +181,22 @@ ssd_decode_stream_kernel(S *__restrict__ state, const T *__restrict__ x,
             const uint64_t evict_first = l2_evict_first_policy();   // states: touched once
             auto issue_load = [&](long k) {
                 const int st = (int)(k % stages);
-                const long u = unit_of(k);
-                const int b = (int)(u / H), h = (int)(u - (long)b * H);
-                const size_t grow = ((size_t)b * G + h / (H / G)) * N;
+                const long u0 = unit_of(k);
+                const int cnt = count_of(k);
                 const uint32_t dst = sbase + st * L.stage_bytes;
                 const uint32_t bar = smem_u32(full + st);
-                mbar_arrive_expect_tx(bar, L.state_bytes + L.x_bytes + 2 * L.bc_bytes);
-                bulk_load_evict_first(dst, state + (size_t)u * P * N, L.state_bytes, bar,
+                mbar_arrive_expect_tx(bar, cnt * (L.state_bytes + L.x_bytes + 2 * L.bc_bytes));
+                bulk_load_evict_first(dst, state + (size_t)u0 * P * N, cnt * L.state_bytes, bar,
                                       evict_first);
-                bulk_load(dst + L.state_bytes, x + (size_t)u * P, L.x_bytes, bar);
-                bulk_load(dst + L.state_bytes + L.x_bytes, Bm + grow, L.bc_bytes, bar);
-                bulk_load(dst + L.state_bytes + L.x_bytes + L.bc_bytes, Cm + grow, L.bc_bytes, bar);
+                bulk_load(dst + U * L.state_bytes, x + (size_t)u0 * P, cnt * L.x_bytes, bar);
+                for (int i = 0; i < cnt; ++i) {
+                    const long u = u0 + i;
+                    const int b = (int)(u / H), h = (int)(u - (long)b * H);
+                    const size_t grow = ((size_t)b * G + h / (H / G)) * N;
+                    const uint32_t bc = dst + U * (L.state_bytes + L.x_bytes) + i * 2 * L.bc_bytes;
+                    bulk_load(bc, Bm + grow, L.bc_bytes, bar);
+                    bulk_load(bc + L.bc_bytes, Cm + grow, L.bc_bytes, bar);
+                }
             };
             for (long k = 0; k < nk && k < stages - 1; ++k) issue_load(k);
             for (long k = 0; k < nk; ++k) {
@@ -191,7 +207,8 @@ ssd_decode_stream_kernel(S *__restrict__ state, const T *__restrict__ x,
                     break;
                 }
                 bulk_store_evict_first(state + (size_t)unit_of(k) * P * N,
-                                       sbase + st * L.stage_bytes, L.state_bytes, evict_first);
+                                       sbase + st * L.stage_bytes, count_of(k) * L.state_bytes,
+                                       evict_first);
                 bulk_commit();
                 if (k + stages - 1 < nk) {
                     // its stage last held unit k-1, whose store must be done reading
@@ -215,40 +232,9 @@ ssd_decode_stream_kernel(S *__restrict__ state, const T *__restrict__ x,
         const int row0 = gtid >> tsh, row_step = kGroupThreads >> tsh;
         // the next unit's dt, A and D are loaded one unit ahead, so no global
         // load latency sits between two units' updates (dt raw; transformed at use)
-        float dt_next = 0.f, A_next = 0.f, D_next = 0.f;
-        if (grp < nk) {
-            const int h0 = (int)(unit_of(grp) % H);
-            dt_next = dt[unit_of(grp)];
-            A_next = A[h0];
-            D_next = D ? D[h0] : 0.0f;
-        }
-        for (long k = grp; k < nk; k += kGroups) {
-            const int st = (int)(k % stages);
-            const long u = unit_of(k);
-            const int h = (int)(u % H);
-            const float dtv = ssd_dt<kFuse>(fuse, dt_next, ssd_dt_bias<kFuse>(fuse, h));
-            const float Ah = A_next, Dh = D_next;
-            if (k + kGroups < nk) {
-                const long un = unit_of(k + kGroups);
-                const int hn = (int)(un % H);
-                dt_next = dt[un];
-                A_next = A[hn];
-                D_next = D ? D[hn] : 0.0f;
-            }
-            const float decay = expf(dtv * Ah);
-            bool ok = !*abort_flag &&
-                      mbar_wait(smem_u32(full + st), (uint32_t)((k / stages) & 1), kStreamWaitNs);
-            ok = __all_sync(0xffffffffu, ok);
-            if (!ok) {
-                *abort_flag = 1;
-                ssd_report(err, SSD_DEVERR_TIMEOUT);
-                break;
-            }
-            uint8_t *stage = smem + (size_t)st * L.stage_bytes;
-            S *sm = reinterpret_cast<S *>(stage);
-            const T *xs = reinterpret_cast<const T *>(stage + L.state_bytes);
-            const T *Bs = reinterpret_cast<const T *>(stage + L.state_bytes + L.x_bytes);
-            const T *Cs = reinterpret_cast<const T *>(stage + L.state_bytes + L.x_bytes + L.bc_bytes);
+        // one state of a stage: its update and readout (S, x, B, C in the stage)
+        auto update = [&](S *sm, const T *xs, const T *Bs, const T *Cs, float dtv, float decay,
+                          float Dh, long u) {
             float4 Bv[VPT], Cv[VPT];
 #pragma unroll
             for (int v = 0; v < VPT; ++v) {
@@ -354,9 +340,104 @@ ssd_decode_stream_kernel(S *__restrict__ state, const T *__restrict__ x,
                 }
                 }
             }
+        };
+        if constexpr (U == 1) {
+            // the next state's dt, A and D are loaded one state ahead, so no
+            // global load latency sits between two states' updates
+            float dt_next = 0.f, A_next = 0.f, D_next = 0.f;
+            if (grp < nk) {
+                const int h0 = (int)(unit_of(grp) % H);
+                dt_next = dt[unit_of(grp)];
+                A_next = A[h0];
+                D_next = D ? D[h0] : 0.0f;
+            }
+            for (long k = grp; k < nk; k += kGroups) {
+                const int st = (int)(k % stages);
+                const long u = unit_of(k);
+                const int h = (int)(u % H);
+                const float dtv = ssd_dt<kFuse>(fuse, dt_next, ssd_dt_bias<kFuse>(fuse, h));
+                const float Ah = A_next, Dh = D_next;
+                if (k + kGroups < nk) {
+                    const long un = unit_of(k + kGroups);
+                    const int hn = (int)(un % H);
+                    dt_next = dt[un];
+                    A_next = A[hn];
+                    D_next = D ? D[hn] : 0.0f;
+                }
+                const float decay = expf(dtv * Ah);
+                bool ok = !*abort_flag &&
+                          mbar_wait(smem_u32(full + st), (uint32_t)((k / stages) & 1), kStreamWaitNs);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) {
+                    *abort_flag = 1;
+                    ssd_report(err, SSD_DEVERR_TIMEOUT);
+                    break;
+                }
+                uint8_t *stage = smem + (size_t)st * L.stage_bytes;
+                S *sm = reinterpret_cast<S *>(stage);
+                const T *xs = reinterpret_cast<const T *>(stage + L.state_bytes);
+                const T *Bs = reinterpret_cast<const T *>(stage + L.state_bytes + L.x_bytes);
+                const T *Cs = Bs + N;
+                update(sm, xs, Bs, Cs, dtv, decay, Dh, u);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if ((tid & 31) == 0) mbar_arrive(smem_u32(done + st));
+            }
+        } else {
+        float dt_next[U], A_next[U], D_next[U];
+        auto load_next = [&](long k) {
+#pragma unroll
+            for (int i = 0; i < U; ++i) {
+                dt_next[i] = A_next[i] = D_next[i] = 0.f;
+                if (k < nk && i < count_of(k)) {
+                    const long un = unit_of(k) + i;
+                    const int hn = (int)(un % H);
+                    dt_next[i] = dt[un];
+                    A_next[i] = A[hn];
+                    D_next[i] = D ? D[hn] : 0.0f;
+                }
+            }
+        };
+        load_next(grp);
+        for (long k = grp; k < nk; k += kGroups) {
+            const int st = (int)(k % stages);
+            const int cnt = count_of(k);
+            float dtc[U], Ac[U], Dc[U];
+#pragma unroll
+            for (int i = 0; i < U; ++i) {
+                dtc[i] = dt_next[i];
+                Ac[i] = A_next[i];
+                Dc[i] = D_next[i];
+            }
+            load_next(k + kGroups);
+            bool ok = !*abort_flag &&
+                      mbar_wait(smem_u32(full + st), (uint32_t)((k / stages) & 1), kStreamWaitNs);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) {
+                *abort_flag = 1;
+                ssd_report(err, SSD_DEVERR_TIMEOUT);
+                break;
+            }
+            uint8_t *stage = smem + (size_t)st * L.stage_bytes;
+#pragma unroll
+            for (int i = 0; i < U; ++i) {
+            if (i >= cnt) break;
+            const long u = unit_of(k) + i;
+            const int h = (int)(u % H);
+            const float dtv = ssd_dt<kFuse>(fuse, dtc[i], ssd_dt_bias<kFuse>(fuse, h));
+            const float Ah = Ac[i], Dh = Dc[i];
+            const float decay = expf(dtv * Ah);
+            S *sm = reinterpret_cast<S *>(stage + i * L.state_bytes);
+            const T *xs = reinterpret_cast<const T *>(stage + U * L.state_bytes + i * L.x_bytes);
+            const T *Bs = reinterpret_cast<const T *>(stage + U * (L.state_bytes + L.x_bytes) +
+                                                      i * 2 * L.bc_bytes);
+            const T *Cs = Bs + N;
+            update(sm, xs, Bs, Cs, dtv, decay, Dh, u);
+            }   // states of the stage
             fence_proxy_async_smem();
             __syncwarp();
             if ((tid & 31) == 0) mbar_arrive(smem_u32(done + st));
+        }
         }
     }
     __syncthreads();
@@ -368,7 +449,8 @@ cudaError_t launch_t(S *state, const void *x, const float *dt, const float *A,
                      int H, int P, int N, int G, int num_sms, unsigned int *err,
                      const SsdFuse &fuse, cudaStream_t stream) {
     const size_t units = (size_t)batch * H;
-    const StreamLayout lay = stream_layout(P, N, (int)sizeof(T), (int)sizeof(S));
+    const StreamLayout lay = stream_layout(P, N, (int)sizeof(T), (int)sizeof(S),
+                                           stream_per_stage<S>());
     const int stages = (int)std::min<size_t>(8, kStreamRing / lay.stage_bytes);
     // the streaming ring pays off once every SM has several states to walk;
     // its bulk copies need 16-byte multiples for the state, x, B and C rows

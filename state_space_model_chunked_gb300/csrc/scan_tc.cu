@@ -675,8 +675,6 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
                 ach_s[lane] = e;
             }
             __syncwarp();
-            // fault injection (host-set, tests only): the first segment's first
-            // signal is withheld, so the transform warps' wait for it runs out
             if (lane == 0) mbar_arrive(bar(13));
         };
         if (ntile > 0) {

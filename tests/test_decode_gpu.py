@@ -207,3 +207,24 @@ def test_decode_bf16_state_needs_bf16_inputs():
         ssd.state_update(s_dev, x, torch.ones((b, H), device="cuda"),
                          torch.zeros(H, device="cuda"), torch.zeros((b, G, N), device="cuda"),
                          torch.zeros((b, G, N), device="cuda"))
+
+
+@pytest.mark.parametrize("b,H,G", [(7, 91, 1), (5, 123, 3)])
+def test_decode_bf16_state_streaming_odd_state_count(b, H, G):
+    """bf16 states through the streaming kernel with an odd number of (batch,
+    head) states (the ring's last stage holds a single state) and stages that
+    cross batch rows and group boundaries."""
+    import state_space_model_chunked_gb300 as ssd
+    P, N = 64, 128
+    st0 = gen.bf16_round(gen.decode_state(b, H, P, N, seed=29))[0]
+    A, D = gen.decode_params(H, seed=29)
+    s_dev = dev(st0, "bf16")
+    tok = gen.decode_token_inputs(b, H, P, N, G, "bf16", seed=29, step=0)
+    y = ssd.state_update(s_dev, dev(tok["x"], "bf16"), dev(tok["dt"]), dev(A),
+                         dev(tok["B"], "bf16"), dev(tok["C"], "bf16"), dev(D))
+    torch.cuda.synchronize()
+    y_ref, s_ref = oracle.step_bf16_state(st0, tok["x"], tok["dt"], A, tok["B"], tok["C"], D)
+    assert rel(host(y), y_ref) <= 1e-2
+    s = host(s_dev)
+    assert rel(s, s_ref) <= 1e-2
+    assert np.mean(s == s_ref) >= 0.99
