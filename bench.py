@@ -735,6 +735,14 @@ def sharded_shape(shape, world, rank):
 
 
 # ------------------------------------------------------------------ arms
+def workload_config(shape):
+    """The line's `config`: the workload, identical in both arms."""
+    return {"workload": shape.name, "batch": shape.batch, "seqlen": shape.seqlen,
+            "nheads": shape.nheads, "headdim": shape.headdim, "dstate": shape.dstate,
+            "ngroups": shape.ngroups, "chunk": shape.chunk,
+            "l2": "inputs and outputs of a step (1.4 GB) larger than L2"}
+
+
 def run_reference(args):
     """The oracle as it stands, timed on the host cores: each step is one pass
     over a sample of whole heads of the layer (inputs drawn before timing)."""
@@ -772,9 +780,7 @@ def run_reference(args):
         "ms_per_step": el / args.steps * 1e3, "higher_is_better": True,
         "scaling": "strong" if world > 1 else "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded PCG64)",
-        "config": {"workload": WORKLOAD, "batch": shape.batch, "seqlen": shape.seqlen,
-                   "nheads": shape.nheads, "headdim": shape.headdim, "dstate": shape.dstate,
-                   "ngroups": shape.ngroups, "chunk": shape.chunk},
+        "config": workload_config(shape),
         "cpu_baseline": {"value": value, "unit": "Mtokens/s", "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": "Mtokens/s", "h2d_bytes_per_step": 0,
@@ -894,13 +900,11 @@ def run_gpu(args):
         "higher_is_better": True, "scaling": "strong" if world > 1 else "weak",
         "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded, generated on device)",
-        "config": {"workload": WORKLOAD, "batch": full.batch, "seqlen": full.seqlen,
-                   "nheads": full.nheads, "headdim": full.headdim, "dstate": full.dstate,
-                   "ngroups": full.ngroups, "chunk": full.chunk,
-                   "l2": (f"inputs larger than L2 ({byts / 1e6:.0f} MB per rank)" if nsets == 1
-                          else f"rotating {nsets} input/output sets "
-                               f"({nsets * byts / 1e6:.0f} MB > 2x L2)"),
-                   "launch": "K calls captured in one CUDA graph, timed as one replay",
+        "config": workload_config(full),
+        "timing": {"launch": "K calls captured in one CUDA graph, timed as one replay",
+                   "inputs": (f"one set per rank ({byts / 1e6:.0f} MB, larger than L2)"
+                              if nsets == 1 else f"rotating {nsets} input/output sets "
+                                                 f"({nsets * byts / 1e6:.0f} MB > 2x L2)"),
                    "parallelism": (f"heads split over {world} GPUs ({shape.nheads} each)"
                                    if world > 1 else "one GPU")},
         "roofline": roof,
@@ -937,7 +941,7 @@ def main():
     ap.add_argument("--decode-batch", type=int, default=16)
     ap.add_argument("--decode-tokens", type=int, default=16,
                     help="tokens per call of the --only decode_multi run")
-    ap.add_argument("--reference-heads", type=int, default=8,
+    ap.add_argument("--reference-heads", type=int, default=16,
                     help="heads of the layer per step of the reference arm")
     ap.add_argument("--decode-state", choices=["f32", "bf16"], default="f32",
                     help="state storage of the --only decode run")
