@@ -404,3 +404,43 @@ def test_varlen_long_sequence_four_head_segments():
     form of the long-context plan), next to short unsplit sequences."""
     inp = gen.varlen_inputs([20000, 300, 5], 80, 64, 128, 1, "bf16", seed=51, random_init=True)
     _check_varlen(inp, "bf16", TC)
+
+
+def test_headline_workload_in_cuda_graph_sampled_heads():
+    """The 2.7B-shaped 65536-token layer (80 heads, one group) exactly as the
+    benchmark times it: inputs drawn on the device by the benchmark's own
+    generator, the calls captured in a CUDA graph and replayed.  Three whole
+    heads (first, middle, last; each an independent recurrence) are checked
+    against the oracle, y and final state."""
+    import sys
+    import os
+    import state_space_model_chunked_gb300 as ssd
+    sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    import bench
+    shape = gen.SCAN_SHAPES["mamba2_2p7b_L65536"]
+    device = torch.device("cuda")
+    s = bench.make_scan_set(shape, 1234, device)
+    ws = torch.empty(max(ssd.scan_workspace_bytes(shape.batch, shape.seqlen, shape.nheads,
+                                                  shape.headdim, shape.dstate, shape.ngroups,
+                                                  shape.chunk), 1),
+                     dtype=torch.uint8, device=device)
+
+    def call():
+        ssd.scan_fwd(s["x"], s["dt"], s["A"], s["B"], s["C"], s["D"], shape.chunk, s["init"],
+                     y=s["y"], final_state=s["final"], workspace=ws)
+
+    call()                                    # outside capture (sets function attributes)
+    torch.cuda.synchronize()
+    s["y"].zero_()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        call()
+    g.replay()
+    torch.cuda.synchronize()
+    heads = [0, 41, 79]
+    hx = host(s["x"][:, :, heads])
+    yo, fo = oracle.scan_seq(hx, host(s["dt"][:, :, heads]), host(s["A"][heads]), host(s["B"]),
+                             host(s["C"]), host(s["D"][heads]), None)
+    assert rel(host(s["y"][:, :, heads]), yo) <= TOL["bf16"]
+    assert rel(host(s["final"][:, heads]), fo) <= TOL["bf16"]
+    ssd.last_device_error()
