@@ -507,23 +507,70 @@ cudaError_t launch_t(S *state, const void *x, const float *dt, const float *A,
 // end of every group of staged tokens and before any token that would take
 // sigma beyond e^-40 or e^40, so the scaled values stay well inside fp32.
 //
-// The tokens' x, dt x / sigma, B and C (and z when gated) are staged in shared
-// memory kMultiTok at a time as fp32.  A state row of N elements is spread
-// over tpr threads (VPT float4 each); a thread keeps kMultiRows rows r0,
-// r0 + rpp, ...  The per-row sums of y reduce over the tpr threads of a row by
-// exchanging halves of the row set, then plain butterflies.
+// The tokens' x, B and C (and z when gated) are staged in shared memory
+// kMultiTok at a time as fp32, with dt x / sigma laid out so that a thread's
+// kMultiRows rows of one token are one float4.  A state row of N elements is
+// spread over tpr threads (VPT float4 each); a thread keeps rows r0, r0 + rpp,
+// ...  The per-row sums C . hs reduce over the tpr threads of a row by
+// exchanging halves of the row set, then plain butterflies, and go to shared
+// memory; once the group's tokens are applied, one vectorised pass forms
+// y = sigma (C . hs) + D x (times silu(z) when gated) and stores it.
 constexpr int kMultiTok = 16;      // tokens staged in shared memory at a time
-constexpr int kMultiRows = 4;      // most state rows a thread keeps in registers
+constexpr int kMultiRows = 4;      // state rows a thread keeps in registers
 constexpr float kMultiRenorm = 40.f;
 
-// floats of staged token data: x and dt x / sigma (and z) per row, B and C,
-// and four per-token scalars
-__host__ __device__ inline size_t multi_smem_floats(int P, int N, bool gated) {
-    return (size_t)kMultiTok * ((gated ? 3 : 2) * P + 2 * N + 4);
-}
 // threads per CTA and float4 per thread of a row for a state width
 __host__ __device__ constexpr int multi_threads(int N) { return N > 128 ? 256 : 128; }
 __host__ __device__ constexpr int multi_vpt(int N) { return N >= 16 ? 4 : N / 4; }
+// most state rows (headdim) one CTA holds for a state width
+__host__ __device__ constexpr int multi_rows(int N) {
+    return kMultiRows * (multi_threads(N) / (N / (4 * multi_vpt(N))));
+}
+// floats of staged token data: x, the row sums (then y) and z when gated per
+// row, dt x / sigma for every row slot, B and C, and four per-token scalars
+__host__ __device__ inline size_t multi_smem_floats(int P, int N, bool gated) {
+    return (size_t)kMultiTok * ((gated ? 3 : 2) * P + multi_rows(N) + 2 * N + 4);
+}
+
+// V consecutive elements (16 bytes or fewer, aligned to their size) as fp32
+// in shared memory.
+template <int V>
+__device__ __forceinline__ void multi_ld_vec(const float *g, float *s) {
+    static_assert(V == 4, "fp32 rows load four at a time");
+    *reinterpret_cast<float4 *>(s) = *reinterpret_cast<const float4 *>(g);
+}
+template <int V>
+__device__ __forceinline__ void multi_ld_vec(const __nv_bfloat16 *g, float *s) {
+    static_assert(V == 4 || V == 8, "bf16 rows load four or eight at a time");
+    if constexpr (V == 8) {
+        const uint4 u = *reinterpret_cast<const uint4 *>(g);
+        *reinterpret_cast<float4 *>(s) =
+            make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u),
+                        __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
+        *reinterpret_cast<float4 *>(s + 4) =
+            make_float4(__uint_as_float(u.z << 16), __uint_as_float(u.z & 0xffff0000u),
+                        __uint_as_float(u.w << 16), __uint_as_float(u.w & 0xffff0000u));
+    } else {
+        *reinterpret_cast<float4 *>(s) = ssd_ld4(g);
+    }
+}
+// V consecutive outputs from fp32 values.
+template <int V>
+__device__ __forceinline__ void multi_st_vec(float *g, const float *v) {
+    static_assert(V == 4, "fp32 rows store four at a time");
+    *reinterpret_cast<float4 *>(g) = make_float4(v[0], v[1], v[2], v[3]);
+}
+template <int V>
+__device__ __forceinline__ void multi_st_vec(__nv_bfloat16 *g, const float *v) {
+    static_assert(V == 8, "bf16 rows store eight at a time");
+    uint32_t w[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const __nv_bfloat162 b = __floats2bfloat162_rn(v[2 * k], v[2 * k + 1]);
+        w[k] = *reinterpret_cast<const uint32_t *>(&b);
+    }
+    *reinterpret_cast<uint4 *>(g) = make_uint4(w[0], w[1], w[2], w[3]);
+}
 
 template <typename T, typename S, int N, bool kFuse>
 __global__ void __launch_bounds__(multi_threads(N), 512 / multi_threads(N))
@@ -538,6 +585,9 @@ ssd_decode_multi_kernel(S *__restrict__ state, const T *__restrict__ x,
     constexpr int VPT = multi_vpt(N);
     constexpr int tpr = N / (4 * VPT);     // threads per row: a power of two <= 16
     constexpr int rpp = NT / tpr;          // rows per pass
+    constexpr int PM = multi_rows(N);      // row slots: kMultiRows per thread of a row
+    static_assert(kMultiRows == 4, "a thread's dt x / sigma of one token is one float4");
+    constexpr int VV = 16 / (int)sizeof(T);          // elements of one 16-byte vector
     const int bh = blockIdx.x;             // b * H + h
     const int b = bh / H, h = bh - b * H;
     const int g = h / (H / G);
@@ -547,9 +597,11 @@ ssd_decode_multi_kernel(S *__restrict__ state, const T *__restrict__ x,
     const float Dh = D ? D[h] : 0.0f;
     const float bias = ssd_dt_bias<kFuse>(fuse, h);
     const bool gated = kFuse && fuse.z != nullptr;
+    const bool xvec = P % VV == 0;         // x, y, z rows in 16-byte vectors
     float *xs = msm;                         // [kMultiTok][P]  x
-    float *us = xs + kMultiTok * P;          // [kMultiTok][P]  dt x / sigma
-    float *Bs = us + kMultiTok * P;          // [kMultiTok][N]
+    float *ys = xs + kMultiTok * P;          // [kMultiTok][P]  C . hs, per row
+    float *us = ys + kMultiTok * P;          // [kMultiTok][rpp][kMultiRows]  dt x / sigma
+    float *Bs = us + kMultiTok * PM;         // [kMultiTok][N]
     float *Cs = Bs + kMultiTok * N;          // [kMultiTok][N]
     float *sig = Cs + kMultiTok * N;         // [kMultiTok]: sigma after the token
     float *pre = sig + kMultiTok;            // [kMultiTok]: rescale before the token (1 = none)
@@ -583,28 +635,59 @@ ssd_decode_multi_kernel(S *__restrict__ state, const T *__restrict__ x,
         const int nt = min(kMultiTok, ntok - t0);
         __syncthreads();                     // the previous tokens' staging is consumed
         const size_t row0 = (size_t)b * ntok + t0;   // token row of the [b][T] axis
-        // per-token factors, one thread walking the group's tokens: log sigma
-        // accumulates dt A.  A token that would take it past +-kMultiRenorm
-        // first restores the state (pre = the sigma so far) and restarts
-        // sigma at its own decay; a token whose own decay is that large is
-        // applied to the restored state directly (pre = sigma so far times
-        // it), and sigma restarts at 1.
         if (threadIdx.x < nt)
             dsz[threadIdx.x] = ssd_dt<kFuse>(fuse, dt[(row0 + threadIdx.x) * H + h], bias);
-        for (int e = threadIdx.x; e < nt * N; e += NT) {
+        // B and C four elements at a time; x in 16-byte vectors only when
+        // every thread gets one (fewer, wider loads on fewer warps measured
+        // slower for short groups)
+        for (int e = threadIdx.x * 4; e < nt * N; e += NT * 4) {
             const int t = e / N, n = e - t * N;
             const size_t o = ((row0 + t) * G + g) * N + n;
-            Bs[e] = ssd_ld(Bm + o);
-            Cs[e] = ssd_ld(Cm + o);
+            multi_ld_vec<4>(Bm + o, Bs + e);
+            multi_ld_vec<4>(Cm + o, Cs + e);
         }
-        for (int e = threadIdx.x; e < nt * P; e += NT) {
-            const int t = e / P;
-            const size_t o = ((row0 + t) * H + h) * P + (e - t * P);
-            xs[e] = ssd_ld(x + o);
-            if (gated) zs[e] = ssd_ld(static_cast<const T *>(fuse.z) + o);
+        if (xvec && nt * P >= NT * VV) {
+            for (int e = threadIdx.x * VV; e < nt * P; e += NT * VV) {
+                const int t = e / P;
+                const size_t o = ((row0 + t) * H + h) * P + (e - t * P);
+                multi_ld_vec<VV>(x + o, xs + e);
+                if (gated) multi_ld_vec<VV>(static_cast<const T *>(fuse.z) + o, zs + e);
+            }
+        } else {
+            for (int e = threadIdx.x; e < nt * P; e += NT) {
+                const int t = e / P;
+                const size_t o = ((row0 + t) * H + h) * P + (e - t * P);
+                xs[e] = ssd_ld(x + o);
+                if (gated) zs[e] = ssd_ld(static_cast<const T *>(fuse.z) + o);
+            }
         }
         __syncthreads();
-        if (threadIdx.x == 0) {
+        // per-token factors: log sigma accumulates dt A.  A token that would
+        // take it past +-kMultiRenorm first restores the state (pre = the
+        // sigma so far) and restarts sigma at its own decay; a token whose own
+        // decay is that large is applied to the restored state directly (pre =
+        // sigma so far times it), and sigma restarts at 1.  When no token of
+        // the group needs either, the first warp forms the factors from a
+        // prefix sum in one step; otherwise one thread walks the tokens.
+        bool walk = false;
+        if (threadIdx.x < 32) {
+            const int ln = threadIdx.x;
+            const float l = ln < nt ? dsz[ln] * Ah : 0.f;
+            float L = l;
+#pragma unroll
+            for (int o = 1; o < kMultiTok; o <<= 1) {
+                const float v = __shfl_up_sync(0xffffffffu, L, o);
+                if (ln >= o) L += v;
+            }
+            const bool big = ln < nt && (fabsf(l) > kMultiRenorm || fabsf(L) > kMultiRenorm);
+            walk = __any_sync(0xffffffffu, big);
+            if (!walk && ln < nt) {
+                pre[ln] = 1.f;
+                sig[ln] = expf(L);
+                inv[ln] = expf(-L);
+            }
+        }
+        if (walk && threadIdx.x == 0) {
             float ls = 0.f;
             for (int t = 0; t < nt; ++t) {
                 const float l = dsz[t] * Ah;
@@ -624,9 +707,12 @@ ssd_decode_multi_kernel(S *__restrict__ state, const T *__restrict__ x,
             }
         }
         __syncthreads();
-        for (int e = threadIdx.x; e < nt * P; e += NT) {
-            const int t = e / P;
-            us[e] = (dsz[t] * xs[e]) * inv[t];
+        // dt x / sigma by row slot: slot r * kMultiRows + i is row r + i * rpp
+        // (zero past the last row)
+        for (int e = threadIdx.x; e < nt * PM; e += NT) {
+            const int t = e / PM, k = e - t * PM;
+            const int p = k / kMultiRows + (k % kMultiRows) * rpp;
+            us[e] = p < P ? (dsz[t] * xs[t * P + p]) * inv[t] : 0.f;
         }
         __syncthreads();
 
@@ -635,14 +721,12 @@ ssd_decode_multi_kernel(S *__restrict__ state, const T *__restrict__ x,
             if (rs != 1.f) rescale(rs);       // uniform: every thread reads the same slot
             // update hs += u B and the row's partial readout C . hs (packed
             // pairs), one float4 of B and C at a time for all rows
-            float2 u2[kMultiRows], a2[kMultiRows];
+            const float4 u4 = *reinterpret_cast<const float4 *>(us + t * PM + kMultiRows * r0);
+            const float2 u2[kMultiRows] = {make_float2(u4.x, u4.x), make_float2(u4.y, u4.y),
+                                           make_float2(u4.z, u4.z), make_float2(u4.w, u4.w)};
+            float2 a2[kMultiRows];
 #pragma unroll
-            for (int i = 0; i < kMultiRows; ++i) {
-                const int p = r0 + i * rpp;
-                const float u = p < P ? us[t * P + p] : 0.f;
-                u2[i] = make_float2(u, u);
-                a2[i] = make_float2(0.f, 0.f);
-            }
+            for (int i = 0; i < kMultiRows; ++i) a2[i] = make_float2(0.f, 0.f);
 #pragma unroll
             for (int v = 0; v < VPT; ++v) {
                 const float4 Bv = *reinterpret_cast<const float4 *>(Bs + t * N + 4 * (lane_n + v * tpr));
@@ -688,31 +772,61 @@ ssd_decode_multi_kernel(S *__restrict__ state, const T *__restrict__ x,
                 }
             }
             // rows this thread now holds: base + j for j < left; the lowest
-            // thread of each set of equal holders writes them
+            // thread of each set of equal holders records them
             constexpr int left = tpr >= 4 ? 1 : (tpr == 2 ? 2 : kMultiRows);
             constexpr int low = tpr > 4 ? tpr / 4 - 1 : 0;
             if ((lane_n & low) == 0) {
-                const float sg = sig[t];
 #pragma unroll
                 for (int j = 0; j < kMultiRows; ++j) {
                     const int p = r0 + (base + j) * rpp;
-                    if (j < left && p < P) {
-                        float yv = sg * acc[j] + Dh * xs[t * P + p];
-                        if (gated) yv *= ssd_silu(zs[t * P + p]);
-                        ssd_st(y + ((row0 + t) * H + h) * P + p, yv);
-                    }
+                    if (j < left && p < P) ys[t * P + p] = acc[j];
                 }
             }
         }
         rescale(sig[nt - 1]);                 // the true state again
-    }
+        if (t0 + nt >= ntok) {                // last group: the state goes out first
 #pragma unroll
-    for (int i = 0; i < kMultiRows; ++i) {
-        const int p = r0 + i * rpp;
-        if (p < P) {
+            for (int i = 0; i < kMultiRows; ++i) {
+                const int p = r0 + i * rpp;
+                if (p < P) {
 #pragma unroll
-            for (int v = 0; v < VPT; ++v)
-                ssd_st4_cs(st + (size_t)p * N + 4 * (lane_n + v * tpr), s[i][v]);
+                    for (int v = 0; v < VPT; ++v)
+                        ssd_st4_cs(st + (size_t)p * N + 4 * (lane_n + v * tpr), s[i][v]);
+                }
+            }
+        }
+        __syncthreads();                      // every row sum of the group recorded
+        // y = sigma (C . hs) + D x, gated: times silu(z)
+        if (xvec) {
+            for (int e = threadIdx.x * VV; e < nt * P; e += NT * VV) {
+                const int t = e / P;
+                const float sg = sig[t];
+                float v[VV];
+#pragma unroll
+                for (int k = 0; k < VV; k += 4) {
+                    const float4 yy = *reinterpret_cast<const float4 *>(ys + e + k);
+                    const float4 xx = *reinterpret_cast<const float4 *>(xs + e + k);
+                    v[k] = sg * yy.x + Dh * xx.x;
+                    v[k + 1] = sg * yy.y + Dh * xx.y;
+                    v[k + 2] = sg * yy.z + Dh * xx.z;
+                    v[k + 3] = sg * yy.w + Dh * xx.w;
+                    if (gated) {
+                        const float4 zz = *reinterpret_cast<const float4 *>(zs + e + k);
+                        v[k] *= ssd_silu(zz.x);
+                        v[k + 1] *= ssd_silu(zz.y);
+                        v[k + 2] *= ssd_silu(zz.z);
+                        v[k + 3] *= ssd_silu(zz.w);
+                    }
+                }
+                multi_st_vec<VV>(y + ((row0 + t) * H + h) * P + (e - t * P), v);
+            }
+        } else {
+            for (int e = threadIdx.x; e < nt * P; e += NT) {
+                const int t = e / P;
+                float v = sig[t] * ys[e] + Dh * xs[e];
+                if (gated) v *= ssd_silu(zs[e]);
+                ssd_st(y + ((row0 + t) * H + h) * P + (e - t * P), v);
+            }
         }
     }
 }
@@ -785,8 +899,7 @@ cudaError_t ssd_launch_decode(void *state, bool bf16_state, const void *x, const
 
 int ssd_decode_multi_max_headdim(int N) {
     if (N < 4 || N > 256 || (N & (N - 1)) != 0) return 0;
-    const int tpr = N / (4 * multi_vpt(N));
-    return kMultiRows * (multi_threads(N) / tpr);
+    return multi_rows(N);
 }
 
 cudaError_t ssd_launch_decode_multi(void *state, bool bf16_state, const void *x, const float *dt,
