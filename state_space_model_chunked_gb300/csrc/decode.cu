@@ -509,18 +509,27 @@ cudaError_t launch_t(S *state, const void *x, const float *dt, const float *A,
 //
 // The tokens' x, B and C (and z when gated) are staged in shared memory
 // kMultiTok at a time as fp32, with dt x / sigma laid out so that a thread's
-// kMultiRows rows of one token are one float4.  A state row of N elements is
+// kMultiRows rows of one token are one vector.  A state row of N elements is
 // spread over tpr threads (VPT float4 each); a thread keeps rows r0, r0 + rpp,
 // ...  The per-row sums C . hs reduce over the tpr threads of a row by
 // exchanging halves of the row set, then plain butterflies, and go to shared
 // memory; once the group's tokens are applied, one vectorised pass forms
 // y = sigma (C . hs) + D x (times silu(z) when gated) and stores it.
 constexpr int kMultiTok = 16;      // tokens staged in shared memory at a time
-constexpr int kMultiRows = 4;      // state rows a thread keeps in registers
+constexpr int kMultiRows = 4;      // state rows a thread keeps in registers (2 or 4)
+constexpr int kLogMultiRows = kMultiRows == 4 ? 2 : 1;
 constexpr float kMultiRenorm = 40.f;
 
 // threads per CTA and float4 per thread of a row for a state width
-__host__ __device__ constexpr int multi_threads(int N) { return N > 128 ? 256 : 128; }
+__host__ __device__ constexpr int multi_threads(int N) {
+    return (N > 128 ? 256 : 128) * (4 / kMultiRows);
+}
+// CTAs per SM the register budget is set for
+__host__ __device__ constexpr int multi_ctas(int N) {
+    return (kMultiRows == 4 ? 512 : 768) / multi_threads(N) > 0
+               ? (kMultiRows == 4 ? 512 : 768) / multi_threads(N)
+               : 1;
+}
 __host__ __device__ constexpr int multi_vpt(int N) { return N >= 16 ? 4 : N / 4; }
 // most state rows (headdim) one CTA holds for a state width
 __host__ __device__ constexpr int multi_rows(int N) {
@@ -573,7 +582,7 @@ __device__ __forceinline__ void multi_st_vec(__nv_bfloat16 *g, const float *v) {
 }
 
 template <typename T, typename S, int N, bool kFuse>
-__global__ void __launch_bounds__(multi_threads(N), 512 / multi_threads(N))
+__global__ void __launch_bounds__(multi_threads(N), multi_ctas(N))
 ssd_decode_multi_kernel(S *__restrict__ state, const T *__restrict__ x,
                         const float *__restrict__ dt, const float *__restrict__ A,
                         const T *__restrict__ Bm, const T *__restrict__ Cm,
@@ -586,7 +595,7 @@ ssd_decode_multi_kernel(S *__restrict__ state, const T *__restrict__ x,
     constexpr int tpr = N / (4 * VPT);     // threads per row: a power of two <= 16
     constexpr int rpp = NT / tpr;          // rows per pass
     constexpr int PM = multi_rows(N);      // row slots: kMultiRows per thread of a row
-    static_assert(kMultiRows == 4, "a thread's dt x / sigma of one token is one float4");
+    static_assert(kMultiRows == 2 || kMultiRows == 4, "a thread's dt x / sigma of one token is one vector");
     constexpr int VV = 16 / (int)sizeof(T);          // elements of one 16-byte vector
     const int bh = blockIdx.x;             // b * H + h
     const int b = bh / H, h = bh - b * H;
@@ -721,9 +730,18 @@ ssd_decode_multi_kernel(S *__restrict__ state, const T *__restrict__ x,
             if (rs != 1.f) rescale(rs);       // uniform: every thread reads the same slot
             // update hs += u B and the row's partial readout C . hs (packed
             // pairs), one float4 of B and C at a time for all rows
-            const float4 u4 = *reinterpret_cast<const float4 *>(us + t * PM + kMultiRows * r0);
-            const float2 u2[kMultiRows] = {make_float2(u4.x, u4.x), make_float2(u4.y, u4.y),
-                                           make_float2(u4.z, u4.z), make_float2(u4.w, u4.w)};
+            float2 u2[kMultiRows];
+            if constexpr (kMultiRows == 4) {
+                const float4 u4 = *reinterpret_cast<const float4 *>(us + t * PM + kMultiRows * r0);
+                u2[0] = make_float2(u4.x, u4.x);
+                u2[1] = make_float2(u4.y, u4.y);
+                u2[kMultiRows - 2] = make_float2(u4.z, u4.z);
+                u2[kMultiRows - 1] = make_float2(u4.w, u4.w);
+            } else {
+                const float2 uv = *reinterpret_cast<const float2 *>(us + t * PM + kMultiRows * r0);
+                u2[0] = make_float2(uv.x, uv.x);
+                u2[kMultiRows - 1] = make_float2(uv.y, uv.y);
+            }
             float2 a2[kMultiRows];
 #pragma unroll
             for (int i = 0; i < kMultiRows; ++i) a2[i] = make_float2(0.f, 0.f);
@@ -755,7 +773,7 @@ ssd_decode_multi_kernel(S *__restrict__ state, const T *__restrict__ x,
             for (int k = 0; k < 4; ++k) {
                 constexpr int kHalf0 = kMultiRows / 2;
                 const int o = tpr >> (k + 1);
-                if (o > 0 && k < 2) {
+                if (o > 0 && k < kLogMultiRows) {
                     const int half = kHalf0 >> k;
                     const bool up = (lane_n & o) != 0;
 #pragma unroll
@@ -773,8 +791,10 @@ ssd_decode_multi_kernel(S *__restrict__ state, const T *__restrict__ x,
             }
             // rows this thread now holds: base + j for j < left; the lowest
             // thread of each set of equal holders records them
-            constexpr int left = tpr >= 4 ? 1 : (tpr == 2 ? 2 : kMultiRows);
-            constexpr int low = tpr > 4 ? tpr / 4 - 1 : 0;
+            constexpr int kLogTpr = tpr >= 16 ? 4 : (tpr >= 8 ? 3 : (tpr >= 4 ? 2 : (tpr >= 2 ? 1 : 0)));
+            constexpr int rounds = kLogTpr < kLogMultiRows ? kLogTpr : kLogMultiRows;
+            constexpr int left = kMultiRows >> rounds;
+            constexpr int low = (1 << (kLogTpr - rounds)) - 1;
             if ((lane_n & low) == 0) {
 #pragma unroll
                 for (int j = 0; j < kMultiRows; ++j) {
