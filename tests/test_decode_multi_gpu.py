@@ -41,6 +41,8 @@ def _oracle_steps(state, tok, A, D, dt_kw=None, z=None):
     (1, 4, 64, 256, 2),         # widest state
     (2, 3, 7, 4, 1),            # narrowest state, odd headdim
     (1, 2, 200, 16, 1),         # long rows of a narrow state
+    (2, 5, 24, 8, 1),           # two float4 per row, one thread per row
+    (2, 4, 128, 64, 2),         # the widest headdim of a 64-wide state
 ])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_multi_token_decode_matches_chained_steps(T, b, H, P, N, G, dtype):
