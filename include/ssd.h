@@ -335,8 +335,8 @@ ssd_status ssd_state_update_fused(void *state, ssd_dtype state_dtype, const void
  *   A, D, dt_transform as ssd_state_update_fused.
  * The token arrays have the layouts of ssd_scan_fwd with seqlen = ntokens.
  * Requirements: those of ssd_state_update_fused, ntokens > 0, and headdim at
- * most 8 x 256 / (dstate / 4) for dstate <= 128 (64 for dstate 128; 64 for
- * dstate 256), else SSD_ERR_UNSUPPORTED. */
+ * most 512 for dstate 4 to 16, 8192 / dstate for dstate 32 to 128 (256, 128,
+ * 64) and 64 for dstate 256, else SSD_ERR_UNSUPPORTED. */
 ssd_status ssd_state_update_multi(void *state, ssd_dtype state_dtype, const void *x,
                                   const float *dt, const float *A, const void *B,
                                   const void *C, const float *D,

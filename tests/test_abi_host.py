@@ -279,6 +279,11 @@ def _dec_multi(lib, **kw):
     (dict(N=24), UNSUPPORTED),               # dstate not a power of two
     (dict(P=65, N=128), UNSUPPORTED),        # more rows than the kernel keeps on chip
     (dict(P=129, N=64), UNSUPPORTED),
+    (dict(P=257, N=32), UNSUPPORTED),
+    (dict(P=513, N=16), UNSUPPORTED),
+    (dict(P=513, N=8), UNSUPPORTED),
+    (dict(P=513, N=4), UNSUPPORTED),
+    (dict(P=65, N=256), UNSUPPORTED),
     (dict(z=_fake(0x8004)), INVALID),        # misaligned gate
 ])
 def test_multi_token_decode_rejects_bad_arguments(lib, kw, expect):
