@@ -201,7 +201,7 @@ ssd_decode_stream_kernel(S *__restrict__ state, const T *__restrict__ x,
             for (long k = 0; k < nk && k < stages - 1; ++k) issue_load(k);
             for (long k = 0; k < nk; ++k) {
                 const int st = (int)(k % stages);
-                if (!mbar_wait(smem_u32(done + st), (uint32_t)((k / stages) & 1), kStreamWaitNs)) {
+                if (!mbar_wait<true>(smem_u32(done + st), (uint32_t)((k / stages) & 1), kStreamWaitNs)) {
                     *abort_flag = 1;
                     ssd_report(err, SSD_DEVERR_TIMEOUT);
                     break;
@@ -366,7 +366,7 @@ ssd_decode_stream_kernel(S *__restrict__ state, const T *__restrict__ x,
                 }
                 const float decay = expf(dtv * Ah);
                 bool ok = !*abort_flag &&
-                          mbar_wait(smem_u32(full + st), (uint32_t)((k / stages) & 1), kStreamWaitNs);
+                          mbar_wait<true>(smem_u32(full + st), (uint32_t)((k / stages) & 1), kStreamWaitNs);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) {
                     *abort_flag = 1;
@@ -411,7 +411,7 @@ ssd_decode_stream_kernel(S *__restrict__ state, const T *__restrict__ x,
             }
             load_next(k + kGroups);
             bool ok = !*abort_flag &&
-                      mbar_wait(smem_u32(full + st), (uint32_t)((k / stages) & 1), kStreamWaitNs);
+                      mbar_wait<true>(smem_u32(full + st), (uint32_t)((k / stages) & 1), kStreamWaitNs);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) {
                 *abort_flag = 1;

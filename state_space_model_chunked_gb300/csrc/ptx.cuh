@@ -34,27 +34,42 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                  : "memory");
 }
 // One bounded poll: the thread may sleep (woken when the phase completes) for
-// up to kPollSuspendNs before the poll returns false.
+// a system-dependent time, or with kLongSleep for up to kPollSuspendNs,
+// before the poll returns false.  Timed: the scan kernel runs 4 % faster on
+// the long layer without the hint (1 us and 0.2 us hints: no change), the
+// bf16-state decode stream 1 % faster with it.
 constexpr uint32_t kPollSuspendNs = 20000;
+template <bool kLongSleep = false>
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity), "n"(kPollSuspendNs)
-        : "memory");
+    if constexpr (kLongSleep) {
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(bar), "r"(parity), "n"(kPollSuspendNs)
+            : "memory");
+    } else {
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(bar), "r"(parity)
+            : "memory");
+    }
     return ok != 0;
 }
 // Waits for the phase with the given parity to complete.  Gives up after
 // limit_ns nanoseconds and returns false, so a protocol error can never hang
 // the GPU; callers then report an error and drain.
+template <bool kLongSleep = false>
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait<kLongSleep>(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (;;) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait<kLongSleep>(bar, parity)) return true;
         if (globaltimer_ns() - t0 > limit_ns) return false;
     }
 }
