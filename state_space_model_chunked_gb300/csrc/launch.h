@@ -65,6 +65,8 @@ struct SsdTcPlan {
     int seg_tiles;        // tiles per segment (the unit of sequence parallelism)
     int nseg;             // segments per sequence
     int seg_heads;        // heads per CTA of the segment-contribution kernel
+    int seg_split;        // batched, seg_heads 4: segments launched at four heads per
+                          // CTA (the rest at two, in a second launch); 0 = one launch
     size_t workspace;     // bytes of workspace required
     int launches;         // kernels enqueued per call
     // work items: sequences, segment contributions (every segment but each

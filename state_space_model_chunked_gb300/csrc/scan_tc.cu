@@ -130,6 +130,7 @@ struct TcArgs {
     int nseq;
     uint64_t wait_ns;         // limit of every bounded wait (ns)
     int fault;                // host-set fault injection (SSD_FAULT_*), 0 = none
+    int sigma0;               // batched segment kernel: segment of grid row y = 0
 };
 
 // Where one CTA's segment lies: its sequence, the sequence's first row in the
@@ -1040,7 +1041,7 @@ ssd_tc_segment_kernel(const __grid_constant__ CUtensorMap mapB,
     auto w_len = [&]() -> int { return kPacked ? w.len : a.L; };
     auto w_tiles = [&]() -> int { return kPacked ? w.tiles : a.tiles; };
     auto w_nseg = [&]() -> int { return kPacked ? w.nseg : a.nseg; };
-    auto w_sigma = [&]() -> int { return kPacked ? w.sigma : (int)blockIdx.y; };
+    auto w_sigma = [&]() -> int { return kPacked ? w.sigma : (int)blockIdx.y + a.sigma0; };
     auto w_fslot = [&]() -> int { return kPacked ? w.fslot : (int)blockIdx.z * (a.nseg - 1); };
     const int sigma = w_sigma();                    // < the sequence's last segment
     const int g = h0 / (a.H / a.G);
@@ -1276,6 +1277,10 @@ ssd_tc_segment_kernel(const __grid_constant__ CUtensorMap mapB,
         tc_fence_after();
         tmem_dealloc(tmem, kCols);
     }
+    // a second segment launch (the last segments, fewer heads per CTA) ends
+    // only after the first: the chaining kernel waits for it alone (a no-op
+    // for a launch with no programmatic predecessor)
+    griddep_wait();
 }
 
 // ============================================ entering state of each segment
@@ -1378,10 +1383,16 @@ static_assert(scan_smem<2>() <= 232448, "scan kernel shared memory exceeds 227 K
 static_assert(seg_smem<2>() <= 232448, "segment kernel shared memory exceeds 227 KB");
 static_assert(seg_smem<4>() <= 232448, "segment kernel shared memory exceeds 227 KB");
 
-// Segment contributions with SG heads per CTA.
+// Segment contributions with SG heads per CTA: all of them, or (batched, with
+// nsig > 0) segments args.sigma0 .. args.sigma0 + nsig - 1, launched after the
+// previous kernel with programmatic stream serialization when `pdl`.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args... args);
 template <int SG, bool kPacked>
 cudaError_t launch_segment(const SsdTcPlan &plan, const CUtensorMap &mB, const CUtensorMap &mX,
-                           const TcArgs &args, int batch, int H, cudaStream_t stream) {
+                           const TcArgs &args, int batch, int H, cudaStream_t stream,
+                           int nsig = 0, bool pdl = false) {
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(attr_once, [] {
@@ -1390,7 +1401,11 @@ cudaError_t launch_segment(const SsdTcPlan &plan, const CUtensorMap &mB, const C
                                         (int)seg_smem<SG>());
     });
     if (attr_err != cudaSuccess) return attr_err;
-    dim3 g1(H / SG, plan.varlen ? plan.nslots : plan.nseg - 1, plan.varlen ? 1 : batch);
+    dim3 g1(H / SG, plan.varlen ? plan.nslots : (nsig > 0 ? nsig : plan.nseg - 1),
+            plan.varlen ? 1 : batch);
+    if (pdl)
+        return launch_pdl(ssd_tc_segment_kernel<SG, kPacked>, g1, dim3(kSegThreads),
+                          seg_smem<SG>(), stream, mB, mX, args);
     ssd_tc_segment_kernel<SG, kPacked><<<g1, kSegThreads, seg_smem<SG>(), stream>>>(mB, mX, args);
     return cudaGetLastError();
 }
@@ -1444,9 +1459,22 @@ cudaError_t launch_hg(const SsdTcPlan &plan, const CUtensorMap &mC, const CUtens
     }
     const bool chained = plan.nslots > 0;
     if (chained) {
-        cudaError_t e = plan.seg_heads == 4
-                            ? launch_segment<4, kPacked>(plan, mB, mX, args, batch, H, stream)
-                            : launch_segment<HG, kPacked>(plan, mB, mX, args, batch, H, stream);
+        cudaError_t e;
+        if (!plan.varlen && plan.seg_heads == 4 && plan.seg_split > 0) {
+            // whole waves of four-head CTAs, then the remaining segments as
+            // two-head CTAs, which fill the last wave with shorter work
+            e = launch_segment<4, kPacked>(plan, mB, mX, args, batch, H, stream, plan.seg_split);
+            if (e == cudaSuccess) {
+                TcArgs rest = args;
+                rest.sigma0 = plan.seg_split;
+                e = launch_segment<2, kPacked>(plan, mB, mX, rest, batch, H, stream,
+                                               plan.nseg - 1 - plan.seg_split, true);
+            }
+        } else {
+            e = plan.seg_heads == 4
+                    ? launch_segment<4, kPacked>(plan, mB, mX, args, batch, H, stream)
+                    : launch_segment<HG, kPacked>(plan, mB, mX, args, batch, H, stream);
+        }
         if (e != cudaSuccess) return e;
         const size_t total = (size_t)plan.nseqs * H * kP * kN / 4;
         e = launch_pdl(ssd_tc_segment_pass_kernel, dim3((unsigned)((total + 255) / 256)),
@@ -1507,6 +1535,15 @@ SsdTcPlan ssd_tc_plan(int batch, int L, int H, int P, int N, int G, int num_sms)
     // grid still covers every SM.
     p.seg_heads = p.heads_per_cta;
     if ((H / G) % 4 == 0 && (long)batch * (H / 4) * (p.nseg - 1) >= num_sms) p.seg_heads = 4;
+    // four-head segment CTAs for as many segments as fill whole waves, the
+    // rest as two-head CTAs (a second launch) when that leaves a partial wave
+    p.seg_split = 0;
+    if (p.seg_heads == 4 && p.nseg > 2) {
+        const long per = (long)batch * (H / 4);          // CTAs per segment
+        const long total = per * (p.nseg - 1);
+        const int split = (int)((total / num_sms) * num_sms / per);
+        if (total % num_sms != 0 && split > 0 && split < p.nseg - 1) p.seg_split = split;
+    }
     p.varlen = false;
     p.nseqs = batch;
     p.nslots = batch * (p.nseg - 1);
@@ -1515,7 +1552,7 @@ SsdTcPlan ssd_tc_plan(int batch, int L, int H, int P, int N, int G, int num_sms)
         const size_t state = (size_t)batch * (p.nseg - 1) * H * kP * kN * sizeof(__nv_bfloat16);
         const size_t decay = (size_t)batch * (p.nseg - 1) * H * sizeof(float);
         p.workspace = ((state + 255) / 256) * 256 + ((decay + 255) / 256) * 256;
-        p.launches = 3;
+        p.launches = p.seg_split > 0 ? 4 : 3;
     }
     // room for the transformed step sizes (used only with a dt transform)
     p.dt_offset = p.workspace;
