@@ -27,8 +27,9 @@
 // handled by one CTA with the state carried in TMEM.  When a sequence has more
 // than one segment, a first kernel computes each segment's own state
 // contribution F (tiles walked backwards so the decay to the segment end is a
-// running sum), a small kernel chains them into every segment's entering
-// state, and the scan kernel starts each segment from it.  Heads that share a
+// running sum; four heads per CTA for the segments that fill whole waves, two
+// for the rest, in a second launch), a small kernel chains them into every
+// segment's entering state, and the scan kernel starts each segment from it.  Heads that share a
 // group (ngroups divides nheads) are paired in one CTA so C.B^T is computed
 // once for both.
 //
@@ -1383,12 +1384,28 @@ static_assert(scan_smem<2>() <= 232448, "scan kernel shared memory exceeds 227 K
 static_assert(seg_smem<2>() <= 232448, "segment kernel shared memory exceeds 227 KB");
 static_assert(seg_smem<4>() <= 232448, "segment kernel shared memory exceeds 227 KB");
 
+// Launch with programmatic stream serialization: the kernel may begin while
+// the previous kernel in the stream finishes; it calls griddepcontrol.wait
+// before touching that kernel's results.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 // Segment contributions with SG heads per CTA: all of them, or (batched, with
 // nsig > 0) segments args.sigma0 .. args.sigma0 + nsig - 1, launched after the
 // previous kernel with programmatic stream serialization when `pdl`.
-template <typename... KArgs, typename... Args>
-cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
-                       cudaStream_t stream, Args... args);
 template <int SG, bool kPacked>
 cudaError_t launch_segment(const SsdTcPlan &plan, const CUtensorMap &mB, const CUtensorMap &mX,
                            const TcArgs &args, int batch, int H, cudaStream_t stream,
@@ -1408,25 +1425,6 @@ cudaError_t launch_segment(const SsdTcPlan &plan, const CUtensorMap &mB, const C
                           seg_smem<SG>(), stream, mB, mX, args);
     ssd_tc_segment_kernel<SG, kPacked><<<g1, kSegThreads, seg_smem<SG>(), stream>>>(mB, mX, args);
     return cudaGetLastError();
-}
-
-// Launch with programmatic stream serialization: the kernel may begin while
-// the previous kernel in the stream finishes; it calls griddepcontrol.wait
-// before touching that kernel's results.
-template <typename... KArgs, typename... Args>
-cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
-                       cudaStream_t stream, Args... args) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = grid;
-    cfg.blockDim = block;
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
 template <int HG, bool kGate, bool kPacked>
