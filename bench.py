@@ -879,7 +879,9 @@ def run_gpu(args):
             extra["gated_norm_separate_pass"] = time_gated_norm_pass(full, device)
     clocks = clk.summary()
 
-    e2e_s, h2d, d2h = ((time_scan_e2e(shape, max(args.steps // 4, 3), args.warmup, device))
+    # the same K steps as the device-timed region, back to back through the
+    # pipeline (its fill and drain, one unpaired copy each way, included once)
+    e2e_s, h2d, d2h = ((time_scan_e2e(shape, max(args.steps, 3), args.warmup, device))
                        if shape.nheads > 0 else (0.0, 0, 0))
     e2e_s = max_over_ranks(e2e_s, dist, device)
     h2d = int(max_over_ranks(h2d, dist, device)) * world
@@ -920,7 +922,8 @@ def run_gpu(args):
         "e2e": {"value": full.tokens / e2e_s / 1e6, "unit": "Mtokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "how": "HostScanPipeline: pinned host inputs copied in, the scan, y and the "
-                       "final state copied out, consecutive steps overlapped"},
+                       "final state copied out, consecutive steps overlapped",
+                "steps": max(args.steps, 3)},
         "gpu_launches": launches * args.steps * world,
         "clocks": clocks,
     }
