@@ -872,22 +872,16 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
             float e_at_t[HG];
 #pragma unroll
             for (int h = 0; h < HG; ++h) e_at_t[h] = __expf(at[h]);
-            if (it + 1 < ntile) {
-                load_factors(it + 1);
-                prep_tile(it + 1);
-            }
-
-            // ---- epilogue: y = Yd + exp(a_t) Yo + D x, staged as bf16 in this
-            //      stage's C blocks (free once the tile's off-diagonal product is
-            //      done; head h in block h) for issuer B's TMA stores
             // (head, 32-column range) of this warpgroup: HG = 2 -> head wg & 1,
             // columns 32 (wg >> 1) ..; HG = 1 -> head 0, columns 16 wg ..
             const int hh = HG == 2 ? (wg & 1) : 0;
             const int p0 = HG == 2 ? 32 * (wg >> 1) : 16 * wg;
             constexpr int np = HG == 2 ? 32 : 16;
             // the output gate's z for this thread's token and columns, loaded
-            // (from L2, where the producer prefetched it) before the wait for
-            // the tile's products; rows past the sequence's end read nothing
+            // (from L2, where the producer prefetched it) before the next
+            // tile's state prep, which hides their latency (loaded just before
+            // the wait for the products, the gated long layer took 913 us
+            // against 727); rows past the sequence's end read nothing
             uint4 zv[np / 8];
             bool gated = false;
             if constexpr (kGate) {
@@ -899,6 +893,14 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
                     for (int q = 0; q < np / 8; ++q) zv[q] = *reinterpret_cast<const uint4 *>(zrow + 8 * q);
                 }
             }
+            if (it + 1 < ntile) {
+                load_factors(it + 1);
+                prep_tile(it + 1);
+            }
+
+            // ---- epilogue: y = Yd + exp(a_t) Yo + D x, staged as bf16 in this
+            //      stage's C blocks (free once the tile's off-diagonal product is
+            //      done; head h in block h) for issuer B's TMA stores
             wait_bar_warp(bar(10), it & 1, abort_flag, a.err, a.wait_ns);
             tc_fence_after();
             {
