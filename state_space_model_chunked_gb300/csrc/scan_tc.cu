@@ -726,7 +726,6 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
         //      state scaled by the tile decay, and Xt = w o X
         auto prep_tile = [&](int it) {
             const uint8_t *stg_ptr = tiles_ptr + (it & 1) * kStage;
-            wait_bar_warp(bar(14 + (it & 1)), (it >> 1) & 1, abort_flag, a.err, a.wait_ns);
             if (it > 0) wait_bar_warp(bar(9), (it - 1) & 1, abort_flag, a.err, a.wait_ns);
             tc_fence_after();
             if (it == 0 && sigma > 0) griddep_wait();   // entering states of later segments
@@ -768,6 +767,11 @@ ssd_tc_scan_kernel(const __grid_constant__ CUtensorMap mapC,
                     r[j + 1] = (uint32_t)(v >> 32);
                 }
                 tmem_st16(tq + colH, r);
+            }
+            // the X tile is needed only now: its landing overlaps the state half
+            wait_bar_warp(bar(14 + (it & 1)), (it >> 1) & 1, abort_flag, a.err, a.wait_ns);
+#pragma unroll
+            for (int h = 0; h < HG; ++h) {
                 const uint8_t *xs = stg_ptr + kCBytes + h * kXBytes;
                 uint8_t *xt = xt_ptr + h * kXBytes;
 #pragma unroll
