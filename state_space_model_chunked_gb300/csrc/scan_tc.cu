@@ -1295,12 +1295,14 @@ ssd_tc_segment_kernel(const __grid_constant__ CUtensorMap mapB,
 // H_in[0] = the sequence's initial state.  Overwrites slot s (F_s) with
 // H_in[s+1].  A sequence's slots are nseg-1 consecutive ones from base
 // (batched: sequence q has base q (nseg-1); packed: fslot0[q] .. fslot0[q+1]).
-// Loads are issued a batch ahead of the dependent FMA chain.
+// The loads of up to kBatch segments are issued before their dependent FMA
+// chain: one round trip for the 18 contributions of the long layer (with 8 a
+// batch the call took 3 us longer).
 __global__ void __launch_bounds__(256)
 ssd_tc_segment_pass_kernel(__nv_bfloat16 *__restrict__ ws_state, const float *__restrict__ ws_decay,
                            const float *__restrict__ init, int nseqs, int H, int nseg,
                            const int *__restrict__ fslot0) {
-    constexpr int kBatch = 8;
+    constexpr int kBatch = 20;
     // let the scan kernel start right away: its first-segment CTAs need nothing
     // from here, the others wait for this grid before reading entering states
     griddep_launch_dependents();
