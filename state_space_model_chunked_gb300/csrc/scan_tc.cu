@@ -1296,13 +1296,14 @@ ssd_tc_segment_kernel(const __grid_constant__ CUtensorMap mapB,
 // H_in[s+1].  A sequence's slots are nseg-1 consecutive ones from base
 // (batched: sequence q has base q (nseg-1); packed: fslot0[q] .. fslot0[q+1]).
 // The loads of up to kBatch segments are issued before their dependent FMA
-// chain: one round trip for the 18 contributions of the long layer (with 8 a
-// batch the call took 3 us longer).
+// chain.  Timed: 20 a batch (one round trip for the long layer's 18
+// contributions, 112 registers) takes 2 us off that call; 8 a batch (fewer
+// registers) is 3 % faster for the 10 contributions of a 4096-token layer.
+template <int kBatch>
 __global__ void __launch_bounds__(256)
 ssd_tc_segment_pass_kernel(__nv_bfloat16 *__restrict__ ws_state, const float *__restrict__ ws_decay,
                            const float *__restrict__ init, int nseqs, int H, int nseg,
                            const int *__restrict__ fslot0) {
-    constexpr int kBatch = 20;
     // let the scan kernel start right away: its first-segment CTAs need nothing
     // from here, the others wait for this grid before reading entering states
     griddep_launch_dependents();
@@ -1483,7 +1484,9 @@ cudaError_t launch_hg(const SsdTcPlan &plan, const CUtensorMap &mC, const CUtens
         }
         if (e != cudaSuccess) return e;
         const size_t total = (size_t)plan.nseqs * H * kP * kN / 4;
-        e = launch_pdl(ssd_tc_segment_pass_kernel, dim3((unsigned)((total + 255) / 256)),
+        auto pass = !plan.varlen && plan.nseg - 1 > 12 ? ssd_tc_segment_pass_kernel<20>
+                                                       : ssd_tc_segment_pass_kernel<8>;
+        e = launch_pdl(pass, dim3((unsigned)((total + 255) / 256)),
                        dim3(256), 0, stream, args.ws_state, args.ws_decay, args.init,
                        plan.nseqs, H, plan.nseg, plan.varlen ? args.fslot0 : nullptr);
         if (e != cudaSuccess) return e;
