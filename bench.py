@@ -169,8 +169,9 @@ def scan_flops_bytes(shape, with_init):
     nc = L // Q
     per_chunk = G * Q * (Q + 1) * N + H * (Q * (Q + 1) * P + 4 * Q * N * P + 2 * N * P)
     flops = b * nc * per_chunk
-    es = 2 if shape.dtype == "bf16" else 4
-    byts = (2 * b * L * H * P * es          # x read, y written
+    es = {"bf16": 2, "fp8": 1}.get(shape.dtype, 4)   # bytes of an x, B or C value
+    ey = 4 if shape.dtype == "f32" else 2            # y: bf16 for bf16 and fp8 inputs
+    byts = (b * L * H * P * (es + ey)       # x read, y written
             + b * L * H * 4                 # dt
             + 2 * b * L * G * N * es        # B, C
             + 2 * H * 4                     # A, D
@@ -184,7 +185,7 @@ def make_scan_set(shape, seed, device):
     g.manual_seed(seed)
     b, L, H, P, N, G = (shape.batch, shape.seqlen, shape.nheads, shape.headdim,
                         shape.dstate, shape.ngroups)
-    dt_ = torch.bfloat16 if shape.dtype == "bf16" else torch.float32
+    dt_ = {"bf16": torch.bfloat16, "fp8": torch.float8_e4m3fn}.get(shape.dtype, torch.float32)
     lo, hi = -6.907755278982137, -2.3025850929940455
     t = {
         "x": torch.randn((b, L, H, P), generator=g, device=device).to(dt_),
@@ -196,9 +197,15 @@ def make_scan_set(shape, seed, device):
         "init": (0.1 * torch.randn((b, H, P, N), generator=g, device=device)
                  if shape.random_init else None),
     }
-    t["y"] = torch.empty_like(t["x"])
+    t["y"] = torch.empty(t["x"].shape, dtype=torch.bfloat16 if shape.dtype == "fp8" else dt_,
+                         device=device)
     t["final"] = torch.empty((b, H, P, N), dtype=torch.float32, device=device)
     return t
+
+
+def torch_input_dtype(shape):
+    import torch
+    return {"bf16": torch.bfloat16, "fp8": torch.float8_e4m3fn}.get(shape.dtype, torch.float32)
 
 
 def time_scan(shape, steps, warmup, device, l2_bytes, dist=None, graph=True):
@@ -217,7 +224,8 @@ def time_scan(shape, steps, warmup, device, l2_bytes, dist=None, graph=True):
     nsets = max(1, -(-2 * l2_bytes // max(byts, 1)))
     sets = [make_scan_set(shape, 1000 + i, device) for i in range(nsets)]
     ws_bytes = ssd.scan_workspace_bytes(shape.batch, shape.seqlen, shape.nheads, shape.headdim,
-                                        shape.dstate, shape.ngroups, shape.chunk, device=device)
+                                        shape.dstate, shape.ngroups, shape.chunk,
+                                        dtype=torch_input_dtype(shape), device=device)
     ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=device)
 
     def step(i):
@@ -629,6 +637,49 @@ def time_fused_steps(shape, device, reps=20):
             "note": "eager calls (host overhead included in both)"}
 
 
+def time_fp8_inputs(device, peaks, l2, bf16_ms, steps=20):
+    """The long-context layer with 8-bit E4M3 x, B, C: the whole call (the
+    widening of x, B, C to bfloat16 copies, then the bf16 path), and the
+    widening kernel alone on as many values, timed with CUDA events on its
+    stream (1 byte read and 2 written per value: its HBM roofline)."""
+    import torch
+    import state_space_model_chunked_gb300 as ssd
+    from state_space_model_chunked_gb300 import inputs as gen
+    sh = gen.SCAN_SHAPES["mamba2_2p7b_L65536_fp8"]
+    ms, kern_ms, _, byts = time_scan(sh, steps, 5, device, l2)
+    entry = scan_line_entry(sh, ms, kern_ms, byts, peaks, "ssd_tc_scan_kernel")
+    torch.cuda.empty_cache()
+    n = sh.batch * sh.seqlen * (sh.nheads * sh.headdim + 2 * sh.ngroups * sh.dstate)
+    g = torch.Generator(device=device)
+    g.manual_seed(3)
+    nbuf = 2                                  # 0.35 GB in, 0.7 GB out each: beyond L2
+    src = [torch.randn(n, generator=g, device=device).to(torch.float8_e4m3fn)
+           for _ in range(nbuf)]
+    dst = [torch.empty(n, dtype=torch.bfloat16, device=device) for _ in range(nbuf)]
+    for i in range(3):
+        ssd.fp8_e4m3_to_bf16(src[i % nbuf], out=dst[i % nbuf])
+    stream = torch.cuda.current_stream(device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(device)
+    e0.record(stream)
+    for i in range(steps):
+        ssd.fp8_e4m3_to_bf16(src[i % nbuf], out=dst[i % nbuf])
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    wms = e0.elapsed_time(e1) / steps
+    del src, dst
+    torch.cuda.empty_cache()
+    achieved = 3 * n / (wms * 1e-3) / 1e9
+    entry.update({
+        "inputs": "x, B, C as float8_e4m3fn; y bfloat16",
+        "vs_bf16_inputs": bf16_ms / ms,
+        "widen": {"kernel": "ssd_fp8_widen_kernel", "values": n, "ms": wms, "bound": "hbm",
+                  "algorithmic_bytes": 3 * n, "achieved": achieved, "peak": peaks["hbm_gbs"],
+                  "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"]},
+    })
+    return entry
+
+
 def time_gated_norm_pass(shape, device, reps=20):
     """Cost of the step the scan kernels do not fuse: the gated RMS norm over
     all heads of a token (y * silu(z), then x / rms(x) * w over nheads x
@@ -808,7 +859,7 @@ def run_only(args):
         props = torch.cuda.get_device_properties(device)
         l2 = getattr(props, "L2_cache_size", 126 * 1024 * 1024) or 126 * 1024 * 1024
         name = {"long": WORKLOAD, "130m": "mamba2_130m_L4096",
-                "370m": "mamba2_370m_b8_L2048"}[args.only]
+                "370m": "mamba2_370m_b8_L2048", "fp8": "mamba2_2p7b_L65536_fp8"}[args.only]
         shape = gen.SCAN_SHAPES[name]
         ms, kern, _, byts = time_scan(shape, args.steps, args.warmup, device, l2, graph=False)
         r = {"workload": name, "ms_per_step": ms, "scan_kernel_ms": kern,
@@ -877,6 +928,7 @@ def run_gpu(args):
             extra["fused_steps"] = [time_fused_steps(gen.SCAN_SHAPES[n], device)
                                     for n in ("mamba2_130m_L4096", WORKLOAD)]
             extra["gated_norm_separate_pass"] = time_gated_norm_pass(full, device)
+            extra["fp8_inputs"] = time_fp8_inputs(device, peaks, l2, ms)
     clocks = clk.summary()
 
     # the same K steps as the device-timed region, back to back through the
@@ -948,7 +1000,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--quick", action="store_true", help="headline workload only")
-    ap.add_argument("--only", choices=["decode", "decode_multi", "long", "130m", "370m"],
+    ap.add_argument("--only", choices=["decode", "decode_multi", "long", "130m", "370m", "fp8"],
                     default=None, help="run one workload alone (for profiler captures)")
     ap.add_argument("--decode-batch", type=int, default=16)
     ap.add_argument("--decode-tokens", type=int, default=16,

@@ -36,6 +36,18 @@
  * For decode, drop the seqlen dimension.  Packed variable-length batches
  * (ssd_scan_fwd_varlen) drop the batch dimension of the token arrays.
  *
+ * fp8 inputs (in_dtype SSD_FP8_E4M3, prefill entry points only): x, B and C
+ * hold one byte per value in the E4M3 encoding -- sign bit, 4 exponent bits
+ * with bias 7, 3 significand bits; exponent field 0 encodes the subnormals
+ * m * 2^-9; no infinities; S.1111.111 is NaN; the largest finite value is
+ * 448.  Every E4M3 value is exactly a bfloat16 value, so each call widens x,
+ * B and C once into bfloat16 copies in its workspace (one elementwise kernel,
+ * ssd_fp8_e4m3_to_bf16) and runs the bf16 path on the copies: the result is
+ * the bf16 path's on the exactly decoded inputs.  y and the gate's z are
+ * bfloat16 in such a call.  The pages name reduced precision as future work
+ * (CGLA sections V.A and VI) without fixing a format; E4M3 is the common
+ * 8-bit one.  The decode entry points return SSD_ERR_UNSUPPORTED for it.
+ *
  * Ownership: every pointer is a DEVICE pointer owned by the caller, except
  * where an entry point says otherwise.  The library allocates no memory;
  * scratch memory is the caller's workspace, sized by
@@ -69,7 +81,7 @@ typedef enum {
     SSD_ERR_WORKSPACE = 5      /* workspace pointer null or smaller than ssd_scan_workspace_bytes() */
 } ssd_status;
 
-typedef enum { SSD_F32 = 0, SSD_BF16 = 1 } ssd_dtype;
+typedef enum { SSD_F32 = 0, SSD_BF16 = 1, SSD_FP8_E4M3 = 2 } ssd_dtype;
 
 /* Which kernels ssd_scan_fwd_algo uses.  AUTO takes the tensor-core path when
  * the shape allows it and the SIMT path otherwise; both run on the GPU. */
@@ -91,7 +103,9 @@ size_t ssd_scan_workspace_bytes(int batch, int seqlen, int nheads, int headdim,
 /* The exact workspace of a call with this input dtype and, when
  * with_dt_transform != 0, a dt transform (ssd_scan_fwd_dt, ssd_scan_fwd_fused):
  * on the tensor-core path a transform adds batch x seqlen x nheads floats for
- * the transformed step sizes.  (size_t)-1 for invalid sizes. */
+ * the transformed step sizes.  SSD_FP8_E4M3 adds the bfloat16 copies of x, B
+ * and C (2 bytes per value, each copy rounded up to 256 bytes) in front of
+ * the workspace of the bf16 call.  (size_t)-1 for invalid sizes. */
 size_t ssd_scan_fused_workspace_bytes(int batch, int seqlen, int nheads, int headdim,
                                       int dstate, int ngroups, int chunk,
                                       ssd_dtype in_dtype, int with_dt_transform);
@@ -99,7 +113,8 @@ size_t ssd_scan_fused_workspace_bytes(int batch, int seqlen, int nheads, int hea
 /* Number of kernel launches ssd_scan_fwd enqueues for this shape on the
  * current device (for launch accounting and CUDA-graph planning); -1 for
  * invalid sizes.  A dt transform on the tensor-core path adds one (the
- * elementwise pass that transforms every dt once). */
+ * elementwise pass that transforms every dt once), and so do fp8 inputs (the
+ * widening of x, B and C). */
 int ssd_scan_kernel_launches(int batch, int seqlen, int nheads, int headdim,
                              int dstate, int ngroups, int chunk,
                              ssd_dtype in_dtype);
@@ -108,7 +123,9 @@ int ssd_scan_kernel_launches(int batch, int seqlen, int nheads, int headdim,
  * CGLA page: Step-1 intra-chunk dual form, chunk states, Step-3 inter-chunk
  * recurrence, plus the off-diagonal output and the D skip).
  *
- *   x, B, C     in_dtype device arrays (layouts above).
+ *   x, B, C     in_dtype device arrays (layouts above; SSD_FP8_E4M3 as
+ *               described there, with its workspace from
+ *               ssd_scan_fused_workspace_bytes).
  *   dt, A       float.  D: float [nheads] or NULL (no skip term).
  *   chunk       the chunk length Q: one of 16, 32, 64, 128, 256, validated
  *               and otherwise UNUSED.  The result does not depend on Q (the
@@ -121,7 +138,8 @@ int ssd_scan_kernel_launches(int batch, int seqlen, int nheads, int headdim,
  *               inside one 128-token tile is below about e^60 (its mask
  *               factors are fp32); the SIMT path has no such limit.
  *   init_state  float [batch][nheads][headdim][dstate] or NULL (zeros).
- *   y           in_dtype output.  final_state: float output or NULL.
+ *   y           in_dtype output (bfloat16 for fp8 inputs).  final_state:
+ *               float output or NULL.
  *   workspace   device scratch of at least ssd_scan_workspace_bytes() bytes
  *               (may be NULL when that is 0), 256-byte aligned; its contents
  *               need no initialisation.
@@ -195,8 +213,8 @@ ssd_status ssd_scan_fwd_dt(ssd_algo algo, const void *x, const float *dt,
  *                    sizes the grid and the workspace.
  *   cu_seqlens_dev   the same nseq + 1 values in a DEVICE int array, read by
  *                    the kernels; the two copies must agree (not checked).
- *   z      in_dtype [T][nheads][headdim] or NULL: the output gate of
- *          ssd_scan_fwd_fused.
+ *   z      in_dtype [T][nheads][headdim] (bfloat16 for fp8 inputs) or
+ *          NULL: the output gate of ssd_scan_fwd_fused.
  * Other arguments and requirements as ssd_scan_fwd_dt.  The workspace is
  * sized by ssd_scan_varlen_workspace_bytes() for the same offsets.
  * Returns SSD_ERR_INVALID_ARG for offsets that do not start at 0 or decrease. */
@@ -230,8 +248,8 @@ int ssd_scan_varlen_kernel_launches(int nseq, const int *cu_seqlens_host,
  *
  *   y <- y * silu(z),   silu(z) = z / (1 + e^-z),
  *
- * applied after the D skip, before y is rounded to in_dtype.  z: in_dtype
- * device array with y's layout, 16-byte aligned, or NULL (no gate).  The
+ * applied after the D skip, before y is rounded to its dtype.  z: a device
+ * array of y's dtype and layout, 16-byte aligned, or NULL (no gate).  The
  * normalisation that may follow the gate in a layer is not fused (it reduces
  * over all heads of a token).  Everything else as ssd_scan_fwd_dt. */
 ssd_status ssd_scan_fwd_fused(ssd_algo algo, const void *x, const float *dt,
@@ -344,6 +362,14 @@ ssd_status ssd_state_update_multi(void *state, ssd_dtype state_dtype, const void
                                   ssd_dtype in_dtype, int batch, int ntokens, int nheads,
                                   int headdim, int dstate, int ngroups, void *y,
                                   cudaStream_t stream);
+
+/* Widens n E4M3 values (the fp8 encoding described at the top) to bfloat16,
+ * exactly: the conversion every fp8 prefill call runs on x, B and C, exported
+ * for callers that keep fp8 copies of other tensors.  NaN codes give a
+ * bfloat16 NaN.  src: n bytes, dst: n bfloat16 values, both device pointers,
+ * 16-byte aligned, not overlapping.  n == 0 enqueues nothing.  Returns
+ * SSD_ERR_INVALID_ARG for a null or misaligned pointer (n > 0). */
+ssd_status ssd_fp8_e4m3_to_bf16(const void *src, void *dst, size_t n, cudaStream_t stream);
 
 /* Human-readable name of a status code (static storage). */
 const char *ssd_status_string(ssd_status s);

@@ -191,6 +191,24 @@ def round_bf16(a):
     return np.ldexp(np.rint(m * 256.0) / 256.0, e)
 
 
+def decode_e4m3(codes):
+    """8-bit E4M3 codes (uint8) -> their float64 values, from the format's
+    definition: bit 7 the sign, bits 6..3 the exponent field e (bias 7), bits
+    2..0 the significand field m.  e = 0 encodes the subnormals m * 2^-9
+    (= (m / 8) * 2^(1 - 7)); e > 0 encodes (1 + m / 8) * 2^(e - 7), except
+    that e = 15 with m = 7 is NaN (the encoding has no infinities, so the
+    largest finite value is (1 + 6/8) * 2^8 = 448).  The pages name reduced
+    precision as future work (CGLA sections V.A and VI) without a format;
+    E4M3 is the common 8-bit floating-point one."""
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    sign = np.where(c >> 7, -1.0, 1.0)
+    e = (c >> 3) & 15
+    m = (c & 7).astype(np.float64)
+    mag = np.where(e == 0, np.ldexp(m, -9), np.ldexp(1.0 + m / 8.0, e - 7))
+    mag = np.where((c & 0x7F) == 0x7F, np.nan, mag)
+    return sign * mag
+
+
 def step_bf16_state(state, x, dt, A, B, C, D=None, nthreads=None):
     """One decode token with the state stored in bfloat16: the fp64 step on
     the stored (bf16) state, y from the updated state before rounding, and

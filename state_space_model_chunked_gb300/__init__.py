@@ -9,6 +9,7 @@ cannot load, every call raises.
 
     y, final = scan_fwd(x, dt, A, B, C, D, chunk=256, init_state=None)
     y, finals = scan_fwd_varlen(x, dt, A, B, C, cu_seqlens, D)   # packed sequences
+    y, final = scan_fwd(x8, dt, A, B8, C8, D)           # float8_e4m3fn x/B/C -> bf16 y
     y = state_update(state, x, dt, A, B, C, D)          # state updated in place
     y = state_update_multi(state, x, dt, A, B, C, D)    # T tokens [b,T,H,P] in one call
     pipe = HostScanPipeline(); pipe.submit(..., out=(y_host, final_host))  # host tensors
@@ -38,4 +39,6 @@ from ._binding import (  # noqa: F401
     ALGO_SIMT,
     ALGO_TCGEN05,
     EXPORTED_SYMBOLS,
+    FP8_E4M3,
+    fp8_e4m3_to_bf16,
 )

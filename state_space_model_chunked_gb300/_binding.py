@@ -30,10 +30,13 @@ EXPORTED_SYMBOLS = (
     "ssd_status_string",
     "ssd_last_device_error",
     "ssd_debug_inject_fault",
+    "ssd_fp8_e4m3_to_bf16",
 )
 
 ALGO_AUTO, ALGO_SIMT, ALGO_TCGEN05 = 0, 1, 2
-_F32, _BF16 = 0, 1
+_F32, _BF16, _FP8 = 0, 1, 2
+# 8-bit E4M3 floats (prefill inputs x, B, C; see include/ssd.h)
+FP8_E4M3 = torch.float8_e4m3fn
 
 _lock = threading.Lock()
 _lib = None
@@ -115,6 +118,8 @@ def load():
         lib.ssd_status_string.argtypes = [_int]
         lib.ssd_last_device_error.restype = _int
         lib.ssd_last_device_error.argtypes = []
+        lib.ssd_fp8_e4m3_to_bf16.restype = _int
+        lib.ssd_fp8_e4m3_to_bf16.argtypes = [_vp, _vp, _sz, _vp]
         _lib = lib
         return lib
 
@@ -134,7 +139,20 @@ def _dtype_code(t):
         return _F32
     if t.dtype == torch.bfloat16:
         return _BF16
-    raise TypeError(f"x/B/C must be float32 or bfloat16, got {t.dtype}")
+    if t.dtype == FP8_E4M3:
+        return _FP8
+    raise TypeError(f"x/B/C must be float32, bfloat16 or float8_e4m3fn, got {t.dtype}")
+
+
+def _code_of(dtype):
+    """ssd_dtype code of a torch dtype given to the size queries."""
+    return {torch.bfloat16: _BF16, FP8_E4M3: _FP8}.get(dtype, _F32)
+
+
+def _out_dtype(x):
+    """dtype of y (and of the gate's z) for inputs of x's dtype: bfloat16 for
+    fp8 inputs, x's own otherwise."""
+    return torch.bfloat16 if x.dtype == FP8_E4M3 else x.dtype
 
 
 def _need(t, name, dtype=None, device=None, shape=None):
@@ -157,7 +175,7 @@ def scan_workspace_bytes(batch, seqlen, nheads, headdim, dstate, ngroups, chunk,
     """Workspace bytes of a scan_fwd call of this shape and input dtype on
     the device, with or without a dt transform."""
     lib = load()
-    code = _BF16 if dtype == torch.bfloat16 else _F32
+    code = _code_of(dtype)
     dev = torch.device("cuda") if device is None else torch.device(device)
     with torch.cuda.device(dev):
         n = lib.ssd_scan_fused_workspace_bytes(batch, seqlen, nheads, headdim, dstate,
@@ -171,7 +189,7 @@ def scan_kernel_launches(batch, seqlen, nheads, headdim, dstate, ngroups, chunk,
                          dtype=torch.bfloat16, device=None):
     """Kernels one scan_fwd call enqueues for this shape on the device."""
     lib = load()
-    code = _BF16 if dtype == torch.bfloat16 else _F32
+    code = _code_of(dtype)
     dev = torch.device("cuda") if device is None else torch.device(device)
     with torch.cuda.device(dev):
         n = lib.ssd_scan_kernel_launches(batch, seqlen, nheads, headdim, dstate, ngroups,
@@ -186,7 +204,7 @@ def scan_varlen_workspace_bytes(cu_seqlens, nheads, headdim, dstate, ngroups, ch
     """Workspace bytes of scan_fwd_varlen for these offsets on the device."""
     lib = load()
     cu, cu_ptr = _host_offsets(cu_seqlens)
-    code = _BF16 if dtype == torch.bfloat16 else _F32
+    code = _code_of(dtype)
     dev = torch.device("cuda") if device is None else torch.device(device)
     with torch.cuda.device(dev):
         n = lib.ssd_scan_varlen_workspace_bytes(cu.size - 1, cu_ptr, nheads, headdim, dstate,
@@ -201,7 +219,7 @@ def scan_varlen_kernel_launches(cu_seqlens, nheads, headdim, dstate, ngroups, ch
     """Kernels one scan_fwd_varlen call enqueues for these offsets."""
     lib = load()
     cu, cu_ptr = _host_offsets(cu_seqlens)
-    code = _BF16 if dtype == torch.bfloat16 else _F32
+    code = _code_of(dtype)
     dev = torch.device("cuda") if device is None else torch.device(device)
     with torch.cuda.device(dev):
         n = lib.ssd_scan_varlen_kernel_launches(cu.size - 1, cu_ptr, nheads, headdim, dstate,
@@ -228,8 +246,9 @@ def scan_fwd(x, dt, A, B, C, D=None, chunk=256, init_state=None, *, y=None,
              final_state=None, workspace=None, algo=ALGO_AUTO, return_final=True,
              dt_bias=None, dt_softplus=False, dt_limit=None, z=None):
     """Chunked SSD scan (prefill).  x [b,L,H,P], dt [b,L,H] f32, A [H] f32,
-    B/C [b,L,G,N] (x's dtype), D [H] f32 or None, init_state [b,H,P,N] f32 or
-    None.  dt_bias [H] f32, dt_softplus and dt_limit = (lo, hi) transform the
+    B/C [b,L,G,N] (x's dtype: float32, bfloat16 or float8_e4m3fn), D [H] f32 or
+    None, init_state [b,H,P,N] f32 or None.  fp8 inputs give a bfloat16 y
+    (the call widens them exactly to bfloat16 in its workspace).  dt_bias [H] f32, dt_softplus and dt_limit = (lo, hi) transform the
     raw dt inside the kernels: dt <- clamp(softplus(dt + dt_bias), lo, hi)
     (softplus only when dt_softplus).  z (x's shape and dtype) gates the
     output inside the kernels: y <- y * silu(z).  Returns (y, final_state) on
@@ -249,11 +268,11 @@ def scan_fwd(x, dt, A, B, C, D=None, chunk=256, init_state=None, *, y=None,
     if init_state is not None:
         _need(init_state, "init_state", torch.float32, dev, (b, H, P, N))
     if z is not None:
-        _need(z, "z", x.dtype, dev, x.shape)
+        _need(z, "z", _out_dtype(x), dev, x.shape)
     if y is None:
-        y = torch.empty_like(x)
+        y = torch.empty(x.shape, dtype=_out_dtype(x), device=dev)
     else:
-        _need(y, "y", x.dtype, dev, x.shape)
+        _need(y, "y", _out_dtype(x), dev, x.shape)
     if final_state is None and return_final:
         final_state = torch.empty((b, H, P, N), dtype=torch.float32, device=dev)
     elif final_state is not None:
@@ -321,11 +340,11 @@ def scan_fwd_varlen(x, dt, A, B, C, cu_seqlens, D=None, chunk=256, init_state=No
     if init_state is not None:
         _need(init_state, "init_state", torch.float32, dev, (nseq, H, P, N))
     if z is not None:
-        _need(z, "z", x.dtype, dev, x.shape)
+        _need(z, "z", _out_dtype(x), dev, x.shape)
     if y is None:
-        y = torch.empty_like(x)
+        y = torch.empty(x.shape, dtype=_out_dtype(x), device=dev)
     else:
-        _need(y, "y", x.dtype, dev, x.shape)
+        _need(y, "y", _out_dtype(x), dev, x.shape)
     if final_state is None and return_final:
         final_state = torch.empty((nseq, H, P, N), dtype=torch.float32, device=dev)
     elif final_state is not None:
@@ -535,6 +554,24 @@ def state_update_multi(state, x, dt, A, B, C, D=None, *, y=None, dt_bias=None,
                                         b, T, H, P, N, G, _ptr(y), ctypes.c_void_p(stream))
     _check("ssd_state_update_multi", rc)
     return y
+
+
+def fp8_e4m3_to_bf16(src, out=None):
+    """Widens a float8_e4m3fn (or uint8 holding E4M3 codes) CUDA tensor to
+    bfloat16, exactly, in the library's kernel; returns the bfloat16 tensor."""
+    lib = load()
+    _need(src, "src")
+    if src.dtype not in (FP8_E4M3, torch.uint8):
+        raise TypeError(f"src must be float8_e4m3fn or uint8, got {src.dtype}")
+    if out is None:
+        out = torch.empty(src.shape, dtype=torch.bfloat16, device=src.device)
+    else:
+        _need(out, "out", torch.bfloat16, src.device, src.shape)
+    with torch.cuda.device(src.device):
+        stream = torch.cuda.current_stream(src.device).cuda_stream
+        rc = lib.ssd_fp8_e4m3_to_bf16(_ptr(src), _ptr(out), src.numel(), ctypes.c_void_p(stream))
+    _check("ssd_fp8_e4m3_to_bf16", rc)
+    return out
 
 
 def scan_profile_events(before=None, after=None):

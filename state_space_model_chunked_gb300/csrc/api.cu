@@ -53,7 +53,7 @@ ssd_status check_scan_args(const void *x, const float *dt, const float *A, const
                            int L, int H, int P, int N, int G, int chunk,
                            const float *init, const void *y, const float *fin) {
     if (!x || !dt || !A || !B || !C || !y) return SSD_ERR_INVALID_ARG;
-    if (dtype != SSD_F32 && dtype != SSD_BF16) return SSD_ERR_INVALID_ARG;
+    if (dtype != SSD_F32 && dtype != SSD_BF16 && dtype != SSD_FP8_E4M3) return SSD_ERR_INVALID_ARG;
     if (batch <= 0 || L <= 0 || H <= 0 || P <= 0 || N <= 0 || G <= 0) return SSD_ERR_INVALID_ARG;
     if (H % G != 0) return SSD_ERR_INVALID_ARG;
     if (!valid_chunk(chunk)) return SSD_ERR_INVALID_ARG;
@@ -90,15 +90,84 @@ ssd_status check_cu(int nseq, const int *cu) {
     return SSD_OK;
 }
 
-// Both scan entry points: batched (cu_host == NULL; `batch` rows of `L`
-// tokens) and packed (`batch` sequences on one axis of L = cu_host[batch]).
+// Workspace carve-out of an fp8 call: bfloat16 copies of x, B and C (each
+// rounded up to 256 bytes) in front of the bf16 call's own workspace.
+struct Fp8Copies {
+    size_t b_off, c_off, total;
+};
+Fp8Copies fp8_copies(size_t rows, int H, int P, int G, int N) {
+    auto up = [](size_t v) { return (v + 255) / 256 * 256; };
+    Fp8Copies c;
+    c.b_off = up(rows * (size_t)H * P * 2);
+    c.c_off = c.b_off + up(rows * (size_t)G * N * 2);
+    c.total = c.c_off + up(rows * (size_t)G * N * 2);
+    return c;
+}
+
 ssd_status scan_any(ssd_algo algo, const void *x, const float *dt, const float *A,
                     const void *B, const void *C, const float *D,
                     const ssd_dt_transform *dt_transform, const void *z, ssd_dtype in_dtype,
                     int batch, int L, int nheads, int headdim, int dstate, int ngroups, int chunk,
                     const int *cu_host, const int *cu_dev, const float *init_state, void *y,
                     float *final_state, void *workspace, size_t workspace_bytes,
+                    cudaStream_t stream, bool launch = true);
+
+// fp8 inputs: x, B and C widened to bfloat16 copies at the front of the
+// workspace, then the bf16 call on the copies with the rest of it.  Every
+// check of that call runs before the widening is enqueued.
+ssd_status scan_fp8(ssd_algo algo, const void *x, const float *dt, const float *A,
+                    const void *B, const void *C, const float *D,
+                    const ssd_dt_transform *dt_transform, const void *z, int batch, int L,
+                    int nheads, int headdim, int dstate, int ngroups, int chunk,
+                    const int *cu_host, const int *cu_dev, const float *init_state, void *y,
+                    float *final_state, void *workspace, size_t workspace_bytes,
                     cudaStream_t stream) {
+    const bool packed = cu_host != nullptr;
+    const size_t rows = packed ? (size_t)L : (size_t)batch * L;
+    if (rows == 0)   // a packed batch of empty sequences: no token values to widen
+        return scan_any(algo, x, dt, A, B, C, D, dt_transform, z, SSD_BF16, batch, L, nheads,
+                        headdim, dstate, ngroups, chunk, cu_host, cu_dev, init_state, y,
+                        final_state, workspace, workspace_bytes, stream);
+    ssd_status st = check_scan_args(x, dt, A, B, C, D, SSD_FP8_E4M3, packed ? 1 : batch, L,
+                                    nheads, headdim, dstate, ngroups, chunk, init_state, y,
+                                    final_state);
+    if (st != SSD_OK) return st;
+    const Fp8Copies cp = fp8_copies(rows, nheads, headdim, ngroups, dstate);
+    if (!workspace || workspace_bytes < cp.total) return SSD_ERR_WORKSPACE;
+    if (((uintptr_t)workspace & 255u) != 0) return SSD_ERR_INVALID_ARG;
+    char *ws = static_cast<char *>(workspace);
+    void *x16 = ws, *b16 = ws + cp.b_off, *c16 = ws + cp.c_off;
+    void *rest = workspace_bytes > cp.total ? ws + cp.total : nullptr;
+    const size_t rest_bytes = workspace_bytes - cp.total;
+    st = scan_any(algo, x16, dt, A, b16, c16, D, dt_transform, z, SSD_BF16, batch, L, nheads,
+                  headdim, dstate, ngroups, chunk, cu_host, cu_dev, init_state, y, final_state,
+                  rest, rest_bytes, stream, false);
+    if (st != SSD_OK) return st;
+    SsdWidenJobs jobs{};
+    jobs.job[0] = {x, x16, rows * (size_t)nheads * headdim};
+    jobs.job[1] = {B, b16, rows * (size_t)ngroups * dstate};
+    jobs.job[2] = {C, c16, rows * (size_t)ngroups * dstate};
+    jobs.count = 3;
+    if (ssd_launch_widen_fp8(jobs, current_sm_count(), stream) != cudaSuccess) return SSD_ERR_CUDA;
+    return scan_any(algo, x16, dt, A, b16, c16, D, dt_transform, z, SSD_BF16, batch, L, nheads,
+                    headdim, dstate, ngroups, chunk, cu_host, cu_dev, init_state, y, final_state,
+                    rest, rest_bytes, stream);
+}
+
+// Both scan entry points: batched (cu_host == NULL; `batch` rows of `L`
+// tokens) and packed (`batch` sequences on one axis of L = cu_host[batch]).
+// With launch == false every check runs and nothing is enqueued.
+ssd_status scan_any(ssd_algo algo, const void *x, const float *dt, const float *A,
+                    const void *B, const void *C, const float *D,
+                    const ssd_dt_transform *dt_transform, const void *z, ssd_dtype in_dtype,
+                    int batch, int L, int nheads, int headdim, int dstate, int ngroups, int chunk,
+                    const int *cu_host, const int *cu_dev, const float *init_state, void *y,
+                    float *final_state, void *workspace, size_t workspace_bytes,
+                    cudaStream_t stream, bool launch) {
+    if (in_dtype == SSD_FP8_E4M3)
+        return scan_fp8(algo, x, dt, A, B, C, D, dt_transform, z, batch, L, nheads, headdim,
+                        dstate, ngroups, chunk, cu_host, cu_dev, init_state, y, final_state,
+                        workspace, workspace_bytes, stream);
     const bool packed = cu_host != nullptr;
     // an all-empty packed batch has no token rows (the token arrays may be
     // NULL): only final states are written
@@ -137,10 +206,12 @@ ssd_status scan_any(ssd_algo algo, const void *x, const float *dt, const float *
             if (!workspace || workspace_bytes < need) return SSD_ERR_WORKSPACE;
             if (((uintptr_t)workspace & 255u) != 0) return SSD_ERR_INVALID_ARG;
         }
+        if (!launch) return SSD_OK;
         e = ssd_launch_scan_tc(plan, x, dt, A, B, C, D, init_state, y, final_state, batch, L,
                                nheads, headdim, dstate, ngroups, workspace, device_error_word(),
                                fuse, g_profile, stream, cu_dev);
     } else {
+        if (!launch) return SSD_OK;
         e = ssd_launch_scan_simt(x, dt, A, B, C, D, init_state, y, final_state, bf16, batch, L,
                                  nheads, headdim, dstate, ngroups, fuse, cu_dev, g_profile,
                                  stream);
@@ -156,6 +227,10 @@ size_t scan_workspace(int batch, int seqlen, int nheads, int headdim, int dstate
     if (batch <= 0 || seqlen <= 0 || nheads <= 0 || headdim <= 0 || dstate <= 0 ||
         ngroups <= 0 || nheads % ngroups != 0 || !valid_chunk(chunk))
         return (size_t)-1;
+    if (in_dtype == SSD_FP8_E4M3)
+        return fp8_copies((size_t)batch * seqlen, nheads, headdim, ngroups, dstate).total +
+               scan_workspace(batch, seqlen, nheads, headdim, dstate, ngroups, chunk, SSD_BF16,
+                              with_dt);
     if (in_dtype != SSD_BF16) return 0;
     const SsdTcPlan plan = ssd_tc_plan(batch, seqlen, nheads, headdim, dstate, ngroups,
                                        current_sm_count());
@@ -213,6 +288,16 @@ size_t ssd_scan_fused_workspace_bytes(int batch, int seqlen, int nheads, int hea
                           with_dt_transform != 0);
 }
 
+ssd_status ssd_fp8_e4m3_to_bf16(const void *src, void *dst, size_t n, cudaStream_t stream) {
+    if (n == 0) return SSD_OK;
+    if (!src || !dst || !aligned16(src) || !aligned16(dst)) return SSD_ERR_INVALID_ARG;
+    SsdWidenJobs jobs{};
+    jobs.job[0] = {src, dst, n};
+    jobs.count = 1;
+    return ssd_launch_widen_fp8(jobs, current_sm_count(), stream) == cudaSuccess ? SSD_OK
+                                                                                 : SSD_ERR_CUDA;
+}
+
 ssd_status ssd_debug_inject_fault(ssd_fault fault, unsigned long long wait_limit_ns) {
     if (fault != SSD_FAULT_NONE && fault != SSD_FAULT_WITHHOLD_SIGNAL) return SSD_ERR_INVALID_ARG;
     g_debug.fault = (int)fault;
@@ -225,6 +310,9 @@ int ssd_scan_kernel_launches(int batch, int seqlen, int nheads, int headdim, int
     if (batch <= 0 || seqlen <= 0 || nheads <= 0 || headdim <= 0 || dstate <= 0 ||
         ngroups <= 0 || nheads % ngroups != 0 || !valid_chunk(chunk))
         return -1;
+    if (in_dtype == SSD_FP8_E4M3)   // the widening, then the bf16 call
+        return 1 + ssd_scan_kernel_launches(batch, seqlen, nheads, headdim, dstate, ngroups,
+                                            chunk, SSD_BF16);
     if (in_dtype != SSD_BF16) return 1;
     const SsdTcPlan plan = ssd_tc_plan(batch, seqlen, nheads, headdim, dstate, ngroups,
                                        current_sm_count());
@@ -260,6 +348,12 @@ size_t ssd_scan_varlen_workspace_bytes(int nseq, const int *cu_seqlens_host, int
     if (check_cu(nseq, cu_seqlens_host) != SSD_OK || nheads <= 0 || headdim <= 0 ||
         dstate <= 0 || ngroups <= 0 || nheads % ngroups != 0 || !valid_chunk(chunk))
         return (size_t)-1;
+    if (in_dtype == SSD_FP8_E4M3) {
+        const size_t rows = (size_t)cu_seqlens_host[nseq];
+        return (rows ? fp8_copies(rows, nheads, headdim, ngroups, dstate).total : 0) +
+               ssd_scan_varlen_workspace_bytes(nseq, cu_seqlens_host, nheads, headdim, dstate,
+                                               ngroups, chunk, SSD_BF16);
+    }
     if (in_dtype != SSD_BF16) return 0;
     const SsdTcPlan plan = ssd_tc_plan_varlen(nseq, cu_seqlens_host, nheads, headdim, dstate,
                                               ngroups, current_sm_count());
@@ -272,6 +366,10 @@ int ssd_scan_varlen_kernel_launches(int nseq, const int *cu_seqlens_host, int nh
     if (check_cu(nseq, cu_seqlens_host) != SSD_OK || nheads <= 0 || headdim <= 0 ||
         dstate <= 0 || ngroups <= 0 || nheads % ngroups != 0 || !valid_chunk(chunk))
         return -1;
+    if (in_dtype == SSD_FP8_E4M3)   // the widening (when there are tokens), then the bf16 call
+        return (cu_seqlens_host[nseq] > 0 ? 1 : 0) +
+               ssd_scan_varlen_kernel_launches(nseq, cu_seqlens_host, nheads, headdim, dstate,
+                                               ngroups, chunk, SSD_BF16);
     if (in_dtype != SSD_BF16) return 1;
     const SsdTcPlan plan = ssd_tc_plan_varlen(nseq, cu_seqlens_host, nheads, headdim, dstate,
                                               ngroups, current_sm_count());
@@ -323,6 +421,7 @@ ssd_status ssd_state_update_fused(void *state, ssd_dtype state_dtype, const void
                                   int headdim, int dstate, int ngroups, void *y,
                                   cudaStream_t stream) {
     if (!state || !x || !dt || !A || !B || !C || !y) return SSD_ERR_INVALID_ARG;
+    if (in_dtype == SSD_FP8_E4M3) return SSD_ERR_UNSUPPORTED;   // prefill only
     if (in_dtype != SSD_F32 && in_dtype != SSD_BF16) return SSD_ERR_INVALID_ARG;
     if (state_dtype != SSD_F32 && state_dtype != SSD_BF16) return SSD_ERR_INVALID_ARG;
     if (batch <= 0 || nheads <= 0 || headdim <= 0 || dstate <= 0 || ngroups <= 0)
@@ -352,6 +451,7 @@ ssd_status ssd_state_update_multi(void *state, ssd_dtype state_dtype, const void
                                   int nheads, int headdim, int dstate, int ngroups, void *y,
                                   cudaStream_t stream) {
     if (!state || !x || !dt || !A || !B || !C || !y) return SSD_ERR_INVALID_ARG;
+    if (in_dtype == SSD_FP8_E4M3) return SSD_ERR_UNSUPPORTED;   // prefill only
     if (in_dtype != SSD_F32 && in_dtype != SSD_BF16) return SSD_ERR_INVALID_ARG;
     if (state_dtype != SSD_F32 && state_dtype != SSD_BF16) return SSD_ERR_INVALID_ARG;
     if (batch <= 0 || ntokens <= 0 || nheads <= 0 || headdim <= 0 || dstate <= 0 ||

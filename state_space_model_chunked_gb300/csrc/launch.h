@@ -25,6 +25,20 @@ int ssd_decode_multi_max_headdim(int N);
 
 size_t ssd_simt_smem_bytes(int N);
 
+// fp8 (E4M3) -> bfloat16 widening of up to three arrays in one launch; every
+// pointer 16-byte aligned (the ABI checks the sources, the workspace
+// carve-out aligns the destinations).
+struct SsdWidenJob {
+    const void *src;
+    void *dst;
+    size_t n;
+};
+struct SsdWidenJobs {
+    SsdWidenJob job[3];
+    int count;
+};
+cudaError_t ssd_launch_widen_fp8(const SsdWidenJobs &jobs, int num_sms, cudaStream_t stream);
+
 // Test hooks of the ABI layer: the fault to inject (0 = none) and the limit
 // of every bounded device wait, read by the launchers at each launch.
 struct SsdDebug {

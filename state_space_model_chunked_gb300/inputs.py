@@ -5,7 +5,8 @@ the method's arithmetic: it only draws random numbers and encodes them.
 
 Distributions (the same for every workload):
   x, B, C ~ N(0, 1), rounded to bfloat16 (round-to-nearest-even) when the
-          workload's input dtype is bf16;
+          workload's input dtype is bf16, encoded as 8-bit E4M3 codes
+          (nearest-even, torch's float8_e4m3fn cast) when it is fp8;
   dt      = exp(U(ln 1e-3, ln 1e-1)), one value per (batch, token, head);
   A_h     = -exp(U(0, ln 16)), one value per head;
   D_h     ~ N(0, 1);
@@ -37,7 +38,7 @@ class ScanShape:
     dstate: int
     ngroups: int
     chunk: int
-    dtype: str            # "f32" or "bf16": dtype of x, B, C and y
+    dtype: str            # "f32", "bf16" or "fp8": dtype of x, B, C (y is bf16 for fp8)
     random_init: bool = False
 
     @property
@@ -64,6 +65,9 @@ SCAN_SHAPES = {
     "mamba2_130m_L4096": ScanShape("mamba2_130m_L4096", 1, 4096, 24, 64, 128, 1, 256, "bf16"),
     "mamba2_370m_b8_L2048": ScanShape("mamba2_370m_b8_L2048", 8, 2048, 32, 64, 128, 1, 256, "bf16", True),
     "mamba2_2p7b_L65536": ScanShape("mamba2_2p7b_L65536", 1, 65536, 80, 64, 128, 1, 256, "bf16"),
+    # the same layer with 8-bit E4M3 x, B, C (bf16 y)
+    "mamba2_2p7b_L65536_fp8": ScanShape("mamba2_2p7b_L65536_fp8", 1, 65536, 80, 64, 128, 1, 256,
+                                        "fp8"),
 }
 DECODE_SHAPE = DecodeShape("mamba2_2p7b_decode_64layers", 64, 80, 64, 128, 1)
 
@@ -79,17 +83,28 @@ def bf16_round(a):
     return vals, bits
 
 
+def e4m3_encode(a):
+    """float32 values -> 8-bit E4M3 codes (uint8), rounded to nearest even by
+    torch's float8_e4m3fn cast on the host.  Values must lie within +-448."""
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(torch.float8_e4m3fn)
+    return t.view(torch.uint8).numpy().copy()
+
+
 def _normal(rng, shape, dtype):
     v = rng.standard_normal(size=shape, dtype=np.float32)
     if dtype == "bf16":
         v, _ = bf16_round(v)
+    elif dtype == "fp8":
+        return e4m3_encode(v)
     return v
 
 
 def scan_inputs(batch, seqlen, nheads, headdim, dstate, ngroups, dtype="bf16",
                 seed=0, random_init=False, with_D=True):
     """Inputs for one scan.  Every array is float32 holding exactly the values
-    the GPU sees (bf16-representable where dtype == 'bf16').
+    the GPU sees (bf16-representable where dtype == 'bf16'), except that for
+    dtype == 'fp8' x, B and C are uint8 arrays of E4M3 codes.
 
     Returns dict with x [b,L,H,P], dt [b,L,H], A [H], B, C [b,L,G,N],
     D [H] (or None), init [b,H,P,N] (or None)."""

@@ -54,6 +54,15 @@ int main(void) {
     EXPECT(ssd_debug_inject_fault((ssd_fault)9, 0), SSD_ERR_INVALID_ARG);
     EXPECT(ssd_debug_inject_fault(SSD_FAULT_NONE, 0), SSD_OK);
     if (ssd_scan_kernel_launches(1, 256, 6, 64, 64, 4, 64, SSD_BF16) != -1) return 1;
+    /* fp8 inputs: the widened copies need a workspace; decode takes no fp8 */
+    EXPECT(ssd_scan_fwd(x, dt, A, B, C, NULL, SSD_FP8_E4M3, 1, 256, 4, 64, 64, 1, 64, NULL, y,
+                        NULL, NULL, 0, 0),
+           SSD_ERR_WORKSPACE);
+    EXPECT(ssd_state_update((float *)0x8000, x, dt, A, B, C, NULL,
+                            SSD_FP8_E4M3, 2, 4, 16, 16, 1, y, 0),
+           SSD_ERR_UNSUPPORTED);
+    EXPECT(ssd_fp8_e4m3_to_bf16(NULL, y, 16, 0), SSD_ERR_INVALID_ARG);
+    EXPECT(ssd_fp8_e4m3_to_bf16(NULL, NULL, 0, 0), SSD_OK);
     printf("c abi ok\n");
     return 0;
 }

@@ -5,14 +5,20 @@ import torch
 
 import oracle
 
-TOL = {"f32": 1e-4, "bf16": 1e-2}   # relative L2 bars: fp32 / bf16-input workloads
+# relative L2 bars: fp32 / bf16-input / fp8-input workloads.  fp8 inputs are
+# widened exactly to bfloat16 and take the bf16 path, so they share its bar.
+TOL = {"f32": 1e-4, "bf16": 1e-2, "fp8": 1e-2}
 
 
 def dev(a, dtype="f32"):
     """numpy float32 -> CUDA tensor; bf16 values are exactly representable so
-    the conversion is exact."""
+    the conversion is exact.  dtype "fp8": `a` holds uint8 E4M3 codes, moved
+    as a float8_e4m3fn tensor."""
     if a is None:
         return None
+    if dtype == "fp8":
+        codes = torch.from_numpy(np.ascontiguousarray(a, dtype=np.uint8))
+        return codes.view(torch.float8_e4m3fn).cuda()
     t = torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32))
     if dtype == "bf16":
         t = t.to(torch.bfloat16)
@@ -34,7 +40,18 @@ def scan_on_gpu(inp, dtype, chunk, algo=0, **dt_kw):
     return host(y), host(fin)
 
 
+def decoded(inp):
+    """The inputs with fp8 x, B, C (uint8 E4M3 codes) replaced by the oracle's
+    fp64 decode of them; other inputs unchanged."""
+    out = dict(inp)
+    for k in ("x", "B", "C"):
+        if out.get(k) is not None and np.asarray(out[k]).dtype == np.uint8:
+            out[k] = oracle.decode_e4m3(out[k])
+    return out
+
+
 def scan_oracle(inp):
+    inp = decoded(inp)
     return oracle.scan_seq(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"],
                            inp["D"], inp["init"])
 

@@ -13,7 +13,8 @@ from state_space_model_chunked_gb300 import build as ssd_build
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "ssd.h")
 
-OK, INVALID, UNSUPPORTED = 0, 1, 2
+OK, INVALID, UNSUPPORTED, WORKSPACE = 0, 1, 2, 5
+FP8 = 2
 
 
 @pytest.fixture(scope="module")
@@ -288,3 +289,58 @@ def _dec_multi(lib, **kw):
 ])
 def test_multi_token_decode_rejects_bad_arguments(lib, kw, expect):
     assert _dec_multi(lib, **kw) == expect
+
+
+# ---------------------------------------------------------------- fp8 (E4M3) inputs
+@pytest.mark.parametrize("kw,expect", [
+    (dict(), WORKSPACE),                          # the bf16 copies need a workspace
+    (dict(ws=_fake(0x9010), wsb=1 << 30), INVALID),   # workspace not 256-byte aligned
+    (dict(x=_fake(0x1008)), INVALID),
+    (dict(C=None), INVALID),
+    (dict(N=66), UNSUPPORTED),
+    (dict(H=6, G=4), INVALID),
+])
+def test_fp8_scan_checks_before_enqueueing(lib, kw, expect):
+    assert _scan(lib, dtype=FP8, **kw) == expect
+
+
+def test_fp8_workspace_adds_the_bf16_copies(lib):
+    """fp8 calls need the bf16 call's workspace plus the bfloat16 copies of x,
+    B and C (2 bytes a value, each rounded up to 256 bytes), and one launch
+    more (the widening)."""
+    def up(v):
+        return (v + 255) // 256 * 256
+    b, L, H, P, N, G = 2, 300, 4, 64, 64, 2
+    copies = up(b * L * H * P * 2) + 2 * up(b * L * G * N * 2)
+    for with_dt in (0, 1):
+        assert (lib.ssd_scan_fused_workspace_bytes(b, L, H, P, N, G, 64, FP8, with_dt) ==
+                copies + lib.ssd_scan_fused_workspace_bytes(b, L, H, P, N, G, 64, 1, with_dt))
+    assert (lib.ssd_scan_kernel_launches(b, L, H, P, N, G, 64, FP8) ==
+            1 + lib.ssd_scan_kernel_launches(b, L, H, P, N, G, 64, 1))
+    keep, cu = _cu([0, 100, 100, 350])
+    T = 350
+    copies = up(T * H * P * 2) + 2 * up(T * G * N * 2)
+    assert (lib.ssd_scan_varlen_workspace_bytes(3, cu, H, P, N, G, 64, FP8) ==
+            copies + lib.ssd_scan_varlen_workspace_bytes(3, cu, H, P, N, G, 64, 1))
+    assert (lib.ssd_scan_varlen_kernel_launches(3, cu, H, P, N, G, 64, FP8) ==
+            1 + lib.ssd_scan_varlen_kernel_launches(3, cu, H, P, N, G, 64, 1))
+    keep, cu = _cu([0, 0])              # no tokens: nothing to widen
+    assert (lib.ssd_scan_varlen_workspace_bytes(1, cu, H, P, N, G, 64, FP8) ==
+            lib.ssd_scan_varlen_workspace_bytes(1, cu, H, P, N, G, 64, 1))
+    assert (lib.ssd_scan_varlen_kernel_launches(1, cu, H, P, N, G, 64, FP8) ==
+            lib.ssd_scan_varlen_kernel_launches(1, cu, H, P, N, G, 64, 1))
+
+
+def test_fp8_decode_is_unsupported(lib):
+    assert _dec(lib, dtype=FP8) == UNSUPPORTED
+    assert _dec_fused(lib, dtype=FP8) == UNSUPPORTED
+    assert _dec_multi(lib, dtype=FP8) == UNSUPPORTED
+
+
+def test_fp8_widening_checks(lib):
+    w = lib.ssd_fp8_e4m3_to_bf16
+    assert w(None, None, 0, None) == OK                       # nothing to do
+    assert w(None, _fake(0x2000), 16, None) == INVALID
+    assert w(_fake(0x1000), None, 16, None) == INVALID
+    assert w(_fake(0x1001), _fake(0x2000), 16, None) == INVALID
+    assert w(_fake(0x1000), _fake(0x2008), 16, None) == INVALID

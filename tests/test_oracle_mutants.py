@@ -184,6 +184,41 @@ def _rel_zero_ref_divides(got, ref):
                      / np.float64(np.linalg.norm(ref.ravel())))
 
 
+def _e4m3_parts(codes):
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    return np.where(c >> 7, -1.0, 1.0), (c >> 3) & 15, (c & 7).astype(np.float64), c
+
+
+def _e4m3_bias_8(codes):
+    sign, e, m, c = _e4m3_parts(codes)
+    mag = np.where(e == 0, np.ldexp(m, -10), np.ldexp(1.0 + m / 8.0, e - 8))
+    return sign * np.where((c & 0x7F) == 0x7F, np.nan, mag)
+
+
+def _e4m3_no_subnormals(codes):
+    sign, e, m, c = _e4m3_parts(codes)
+    mag = np.ldexp(1.0 + m / 8.0, e - 7)
+    return sign * np.where((c & 0x7F) == 0x7F, np.nan, mag)
+
+
+def _e4m3_subnormal_scale_2m10(codes):
+    sign, e, m, c = _e4m3_parts(codes)
+    mag = np.where(e == 0, np.ldexp(m, -10), np.ldexp(1.0 + m / 8.0, e - 7))
+    return sign * np.where((c & 0x7F) == 0x7F, np.nan, mag)
+
+
+def _e4m3_with_infinities(codes):
+    sign, e, m, c = _e4m3_parts(codes)
+    mag = np.where(e == 0, np.ldexp(m, -9), np.ldexp(1.0 + m / 8.0, e - 7))
+    return sign * np.where(e == 15, np.where(m == 0, np.inf, np.nan), mag)
+
+
+def _e4m3_unsigned(codes):
+    sign, e, m, c = _e4m3_parts(codes)
+    mag = np.where(e == 0, np.ldexp(m, -9), np.ldexp(1.0 + m / 8.0, e - 7))
+    return np.where((c & 0x7F) == 0x7F, np.nan, mag)
+
+
 _REL = oracle.rel_l2
 
 PY_MUTANTS = {
@@ -212,6 +247,16 @@ PY_MUTANTS = {
     "rel_l2_matrix_norm": ("rel_l2", _rel_matrix_norm, pins.test_rel_l2_on_hand_worked_values),
     "rel_l2_zero_reference_divides": ("rel_l2", _rel_zero_ref_divides,
                                       pins.test_rel_l2_on_hand_worked_values),
+    "e4m3_exponent_bias_8": ("decode_e4m3", _e4m3_bias_8, pins.test_decode_e4m3_closed_forms),
+    "e4m3_subnormals_as_normals": ("decode_e4m3", _e4m3_no_subnormals,
+                                   pins.test_decode_e4m3_closed_forms),
+    "e4m3_subnormal_scale": ("decode_e4m3", _e4m3_subnormal_scale_2m10,
+                             pins.test_decode_e4m3_closed_forms),
+    "e4m3_top_exponent_reserved": ("decode_e4m3", _e4m3_with_infinities,
+                                   pins.test_decode_e4m3_closed_forms),
+    "e4m3_sign_dropped": ("decode_e4m3", _e4m3_unsigned, pins.test_decode_e4m3_closed_forms),
+    "e4m3_bias_8_against_torch": ("decode_e4m3", _e4m3_bias_8,
+                                  pins.test_decode_e4m3_equals_torch_float8_for_every_code),
 }
 
 

@@ -414,3 +414,63 @@ def test_rel_l2_on_hand_worked_values():
     perm = np.random.default_rng(0).permutation(12)
     assert oracle.rel_l2(b, a) == pytest.approx(oracle.rel_l2(b.ravel()[perm], a.ravel()[perm]),
                                                 rel=1e-15)
+
+
+# ---------------------------------------------------------------- fp8 (E4M3) decode
+def test_decode_e4m3_equals_torch_float8_for_every_code():
+    """All 256 codes against torch's float8_e4m3fn -> float64 conversion (a
+    library routine independent of the oracle): equal values, NaN at the
+    same two codes."""
+    import torch
+    codes = np.arange(256, dtype=np.uint8)
+    got = oracle.decode_e4m3(codes)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(got[ok], ref[ok])
+    assert np.array_equal(np.signbit(got[ok]), np.signbit(ref[ok]))
+
+
+def test_decode_e4m3_closed_forms():
+    """Values the encoding's definition fixes: the subnormals step by 2^-9 up to
+    7 * 2^-9 and meet the smallest normal 2^-6 one step later; 0x38 is
+    exponent field 7 (= the bias) with a zero significand, i.e. 1; the
+    largest finite value (1 + 6/8) 2^8 = 448 sits just below the NaN code; the
+    sign bit only negates."""
+    d = oracle.decode_e4m3
+    assert d(np.uint8(0x00)) == 0.0 and np.signbit(d(np.uint8(0x80)))
+    sub = d(np.arange(0, 8, dtype=np.uint8))
+    np.testing.assert_array_equal(sub, np.arange(8) * 2.0 ** -9)
+    assert d(np.uint8(0x08)) == 2.0 ** -6 == d(np.uint8(0x07)) + 2.0 ** -9
+    assert d(np.uint8(0x38)) == 1.0
+    assert d(np.uint8(0x3C)) == 1.5 and d(np.uint8(0x40)) == 2.0
+    assert d(np.uint8(0x7E)) == 448.0
+    assert np.isnan(d(np.uint8(0x7F))) and np.isnan(d(np.uint8(0xFF)))
+    pos = d(np.arange(0x00, 0x7F, dtype=np.uint8))
+    assert np.all(np.diff(pos) > 0)                       # strictly increasing
+    neg = d(np.arange(0x80, 0xFF, dtype=np.uint8))
+    np.testing.assert_array_equal(neg, -pos)
+
+
+def test_every_e4m3_value_is_a_bfloat16_value():
+    """The fp8 path widens E4M3 to bfloat16 and relies on that being exact:
+    every finite E4M3 value survives rounding to bfloat16 unchanged."""
+    v = oracle.decode_e4m3(np.arange(256, dtype=np.uint8))
+    v = v[np.isfinite(v) & (v != 0)]
+    np.testing.assert_array_equal(oracle.round_bf16(v), v)
+
+
+def test_fp8_inputs_decode_to_the_drawn_distribution():
+    """The seeded fp8 inputs are codes of N(0, 1) draws: decoded, they match
+    the bf16-rounded draws of the same seed within E4M3's half spacing (2^-4
+    relative; 2^-10 absolute for subnormals) plus bfloat16's (2^-9)."""
+    a = gen.scan_inputs(1, 300, 4, 32, 16, 1, "fp8", seed=5)
+    b = gen.scan_inputs(1, 300, 4, 32, 16, 1, "bf16", seed=5)
+    for k in ("x", "B", "C"):
+        assert a[k].dtype == np.uint8
+        v = oracle.decode_e4m3(a[k])
+        assert np.all(np.isfinite(v))
+        err = np.abs(v - b[k])
+        bound = np.maximum(np.abs(b[k]) * (2.0 ** -4 + 2.0 ** -8), 2.0 ** -10 + 2.0 ** -16)
+        assert np.all(err <= bound), k
+    np.testing.assert_array_equal(a["dt"], b["dt"])
