@@ -148,7 +148,7 @@ ssd_status scan_fp8(ssd_algo algo, const void *x, const float *dt, const float *
     jobs.job[1] = {B, b16, rows * (size_t)ngroups * dstate};
     jobs.job[2] = {C, c16, rows * (size_t)ngroups * dstate};
     jobs.count = 3;
-    if (ssd_launch_widen_fp8(jobs, current_sm_count(), stream) != cudaSuccess) return SSD_ERR_CUDA;
+    if (ssd_launch_widen_fp8(jobs, stream) != cudaSuccess) return SSD_ERR_CUDA;
     return scan_any(algo, x16, dt, A, b16, c16, D, dt_transform, z, SSD_BF16, batch, L, nheads,
                     headdim, dstate, ngroups, chunk, cu_host, cu_dev, init_state, y, final_state,
                     rest, rest_bytes, stream);
@@ -294,7 +294,7 @@ ssd_status ssd_fp8_e4m3_to_bf16(const void *src, void *dst, size_t n, cudaStream
     SsdWidenJobs jobs{};
     jobs.job[0] = {src, dst, n};
     jobs.count = 1;
-    return ssd_launch_widen_fp8(jobs, current_sm_count(), stream) == cudaSuccess ? SSD_OK
+    return ssd_launch_widen_fp8(jobs, stream) == cudaSuccess ? SSD_OK
                                                                                  : SSD_ERR_CUDA;
 }
 

@@ -37,7 +37,10 @@ struct SsdWidenJobs {
     SsdWidenJob job[3];
     int count;
 };
-cudaError_t ssd_launch_widen_fp8(const SsdWidenJobs &jobs, int num_sms, cudaStream_t stream);
+struct SsdWidenFirst {     // first CTA of each job in the widening launch
+    size_t cta[3];
+};
+cudaError_t ssd_launch_widen_fp8(const SsdWidenJobs &jobs, cudaStream_t stream);
 
 // Test hooks of the ABI layer: the fault to inject (0 = none) and the limit
 // of every bounded device wait, read by the launchers at each launch.

@@ -7,10 +7,12 @@
 // conversion goes through the hardware E4M3x2 -> f16x2 convert (f16 holds
 // every E4M3 value exactly too) and fp32.
 //
-// The kernel is HBM-bound: 1 byte read and 2 bytes written per value.  Each
-// thread moves four independent 16-value vectors per step (64 bytes in, 128
-// out) so that enough loads are in flight per SM, on a grid of a few CTAs per
-// SM striding over up to three arrays in one launch.
+// The kernel is HBM-bound: 1 byte read and 2 bytes written per value.  It
+// makes one pass over its arrays, CTA after CTA in address order (a grid that
+// strides over them instead reached 0.72 of the HBM copy rate; one pass
+// reaches it): each thread widens two 8-value chunks 256 chunks apart, so a
+// warp's load covers 256 contiguous bytes and its store 512.  Up to three
+// arrays share one launch, each on its own run of CTAs.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
@@ -21,14 +23,14 @@
 namespace {
 
 constexpr int kWidenThreads = 256;
-constexpr int kWidenUnroll = 4;
+constexpr size_t kChunksPerCta = 2 * kWidenThreads;    // 8-value chunks per CTA
 
-// 16 E4M3 values (one 16-byte vector) -> 16 bfloat16 values (two vectors)
-__device__ __forceinline__ void widen16(uint4 v, uint4 &lo, uint4 &hi) {
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    uint32_t o[8];
+// 8 E4M3 values (8 bytes) -> 8 bfloat16 values (16 bytes)
+__device__ __forceinline__ uint4 widen8(uint2 v) {
+    const uint32_t w[2] = {v.x, v.y};
+    uint32_t o[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < 2; ++i) {
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
             const __nv_fp8x2_storage_t pair = (__nv_fp8x2_storage_t)(w[i] >> (16 * k));
@@ -38,8 +40,7 @@ __device__ __forceinline__ void widen16(uint4 v, uint4 &lo, uint4 &hi) {
             o[2 * i + k] = *reinterpret_cast<const uint32_t *>(&b);
         }
     }
-    lo = make_uint4(o[0], o[1], o[2], o[3]);
-    hi = make_uint4(o[4], o[5], o[6], o[7]);
+    return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
 __device__ __forceinline__ __nv_bfloat16 widen1(uint8_t c) {
@@ -47,57 +48,48 @@ __device__ __forceinline__ __nv_bfloat16 widen1(uint8_t c) {
     return __float2bfloat16_rn(__half2float(*reinterpret_cast<const __half *>(&hr)));
 }
 
+size_t ctas_of(size_t n) { return (n / 8 + kChunksPerCta - 1) / kChunksPerCta; }
+
+// CTAs [first[j], first[j + 1]) widen job j; the job's first CTA also takes
+// its ragged tail of fewer than 8 values
 __global__ void __launch_bounds__(kWidenThreads)
-ssd_fp8_widen_kernel(SsdWidenJobs jobs) {
-    const size_t stride = (size_t)gridDim.x * kWidenThreads;
-    const size_t tid = (size_t)blockIdx.x * kWidenThreads + threadIdx.x;
-#pragma unroll
-    for (int j = 0; j < 3; ++j) {
-        if (j >= jobs.count) break;
-        const uint8_t *src = static_cast<const uint8_t *>(jobs.job[j].src);
-        __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(jobs.job[j].dst);
-        const size_t n = jobs.job[j].n;
-        const size_t nv = n / 16;                  // whole 16-value vectors
-        const uint4 *sv = reinterpret_cast<const uint4 *>(src);
-        uint4 *dv = reinterpret_cast<uint4 *>(dst);
-        size_t i = tid;
-        for (; i + (kWidenUnroll - 1) * stride < nv; i += kWidenUnroll * stride) {
-            uint4 v[kWidenUnroll];
-#pragma unroll
-            for (int u = 0; u < kWidenUnroll; ++u) v[u] = __ldcs(sv + i + u * stride);
-#pragma unroll
-            for (int u = 0; u < kWidenUnroll; ++u) {
-                uint4 lo, hi;
-                widen16(v[u], lo, hi);
-                dv[2 * (i + u * stride)] = lo;
-                dv[2 * (i + u * stride) + 1] = hi;
-            }
-        }
-        for (; i < nv; i += stride) {
-            uint4 lo, hi;
-            widen16(__ldcs(sv + i), lo, hi);
-            dv[2 * i] = lo;
-            dv[2 * i + 1] = hi;
-        }
-        // ragged tail of fewer than 16 values
-        const size_t t = 16 * nv + tid;
-        if (t < n) dst[t] = widen1(src[t]);
+ssd_fp8_widen_kernel(SsdWidenJobs jobs, SsdWidenFirst first) {
+    const size_t cta = blockIdx.x;
+    const int j = cta < first.cta[1] ? 0 : (cta < first.cta[2] ? 1 : 2);
+    const SsdWidenJob job = j == 0 ? jobs.job[0] : (j == 1 ? jobs.job[1] : jobs.job[2]);
+    const size_t n8 = job.n / 8;
+    const size_t c0 = (cta - (j == 0 ? first.cta[0] : (j == 1 ? first.cta[1] : first.cta[2]))) *
+                          kChunksPerCta + threadIdx.x;
+    const size_t c1 = c0 + kWidenThreads;
+    const uint2 *src = static_cast<const uint2 *>(job.src);
+    uint4 *dst = static_cast<uint4 *>(job.dst);
+    uint2 a = make_uint2(0u, 0u), b = make_uint2(0u, 0u);
+    if (c0 < n8) a = __ldcs(src + c0);
+    if (c1 < n8) b = __ldcs(src + c1);
+    if (c0 < n8) dst[c0] = widen8(a);
+    if (c1 < n8) dst[c1] = widen8(b);
+    if (c0 < 8 && 8 * n8 + c0 < job.n) {
+        const size_t t = 8 * n8 + c0;
+        static_cast<__nv_bfloat16 *>(job.dst)[t] = widen1(static_cast<const uint8_t *>(job.src)[t]);
     }
 }
 
 }  // namespace
 
-cudaError_t ssd_launch_widen_fp8(const SsdWidenJobs &jobs, int num_sms, cudaStream_t stream) {
-    size_t total = 0, vecs = 0;
-    for (int j = 0; j < jobs.count; ++j) {
-        total += jobs.job[j].n;
-        vecs += jobs.job[j].n / 16;
+cudaError_t ssd_launch_widen_fp8(const SsdWidenJobs &jobs, cudaStream_t stream) {
+    SsdWidenJobs js{};
+    SsdWidenFirst first{};
+    size_t total = 0;
+    for (int j = 0; j < 3; ++j) {
+        // unused slots are empty jobs of no CTAs
+        js.job[j] = j < jobs.count ? jobs.job[j] : SsdWidenJob{nullptr, nullptr, 0};
+        first.cta[j] = total;
+        // a job with values but no whole chunk still needs a CTA for its tail
+        total += js.job[j].n > 0 ? (ctas_of(js.job[j].n) > 0 ? ctas_of(js.job[j].n) : 1) : 0;
     }
+    js.count = jobs.count;
     if (total == 0) return cudaSuccess;
-    // a few CTAs per SM; at least one, whose first 16 threads cover the tails
-    const size_t want = (vecs + kWidenThreads - 1) / kWidenThreads;
-    const size_t cap = (size_t)(num_sms > 0 ? num_sms : 1) * 8;
-    const unsigned grid = (unsigned)(want == 0 ? 1 : (want < cap ? want : cap));
-    ssd_fp8_widen_kernel<<<grid, kWidenThreads, 0, stream>>>(jobs);
+    if (total > 0x7fffffffu) return cudaErrorInvalidValue;
+    ssd_fp8_widen_kernel<<<(unsigned)total, kWidenThreads, 0, stream>>>(js, first);
     return cudaGetLastError();
 }

@@ -31,11 +31,13 @@ def _check(inp, chunk, algo):
     return y, f
 
 
-@pytest.mark.parametrize("n", [1, 15, 16, 256, 4096 + 13, (1 << 20) + 7])
+@pytest.mark.parametrize("n", [1, 7, 8, 15, 16, 256, 4096, 4096 + 13, 8 * 1024 + 3,
+                               (1 << 20) + 7])
 def test_widening_is_the_oracle_decode_bit_for_bit(n):
-    """Every code (each of the 256 appears once before the random rest), ragged
-    lengths below, at and above one 16-value vector and the four-vector
-    unrolled step: equal values, equal signs of zero, NaN at the NaN codes."""
+    """Every code (each of the 256 appears once before the random rest);
+    lengths below, at and above one 8-value chunk and one CTA's 512 chunks,
+    with and without a ragged tail: equal values, equal signs of zero, NaN at
+    the NaN codes."""
     import state_space_model_chunked_gb300 as ssd
     rng = np.random.default_rng(n)
     codes = rng.integers(0, 256, size=n, dtype=np.uint8)
