@@ -670,12 +670,14 @@ def time_fp8_inputs(device, peaks, l2, bf16_ms, steps=20):
     del src, dst
     torch.cuda.empty_cache()
     achieved = 3 * n / (wms * 1e-3) / 1e9
+    entry["roofline"]["call_traffic"] = ncu_call_traffic(sh.name)
     entry.update({
         "inputs": "x, B, C as float8_e4m3fn; y bfloat16",
         "vs_bf16_inputs": bf16_ms / ms,
         "widen": {"kernel": "ssd_fp8_widen_kernel", "values": n, "ms": wms, "bound": "hbm",
                   "algorithmic_bytes": 3 * n, "achieved": achieved, "peak": peaks["hbm_gbs"],
-                  "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"]},
+                  "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                  "traffic": ncu_traffic("ssd_fp8_widen_kernel", sh.name)},
     })
     return entry
 
