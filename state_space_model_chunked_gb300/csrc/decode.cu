@@ -22,7 +22,8 @@
 // memory, and releases the next launch at once.  Per-layer calls of a small
 // batch are launch-bound, and this hides most of a launch per call (timed on
 // 64 per-layer calls a token: 355 -> 274 us at batch 1 with the row split,
-// 1046 -> 1005 us at batch 16).
+// 1046 -> 1005 us at batch 16).  The streaming kernel takes it only for
+// calls of at most 64 states per SM.
 #include <algorithm>
 
 #include "common.cuh"
@@ -493,16 +494,28 @@ cudaError_t launch_t(S *state, const void *x, const float *dt, const float *A,
     if (num_sms > 0 && stages >= 3 && units >= (size_t)num_sms * 4 && lay.x_bytes % 16 == 0 &&
         lay.bc_bytes % 16 == 0 && lay.state_bytes % 16 == 0) {
         const size_t smem = (size_t)stages * lay.stage_bytes + 16 * stages + 16;
+        // programmatic launch hides a launch only where that is worth it: a
+        // short call (its griddepcontrol instructions are no-ops otherwise);
+        // on stacks of hundreds of states per SM it cost ~1 %
+        const bool pdl = units <= (size_t)num_sms * 64;
         cudaError_t e;
 #define SSD_STREAM_N(NN)                                                                   \
     case NN:                                                                               \
         e = cudaFuncSetAttribute(ssd_decode_stream_kernel<T, S, NN, kFuse>,               \
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);   \
         if (e != cudaSuccess) return e;                                                    \
-        e = launch_pdl(ssd_decode_stream_kernel<T, S, NN, kFuse>, dim3(num_sms),             \
-                       dim3(kStreamThreads + 32), smem, stream, state, (const T *)x, dt, A,  \
-                       (const T *)B, (const T *)C, D, (T *)y, batch, H, P, G, stages, err, fuse); \
-        if (e != cudaSuccess) return e;                                                    \
+        if (pdl) {                                                                         \
+            e = launch_pdl(ssd_decode_stream_kernel<T, S, NN, kFuse>, dim3(num_sms),         \
+                           dim3(kStreamThreads + 32), smem, stream, state, (const T *)x, dt, \
+                           A, (const T *)B, (const T *)C, D, (T *)y, batch, H, P, G, stages, \
+                           err, fuse);                                                     \
+            if (e != cudaSuccess) return e;                                                \
+        } else {                                                                           \
+            ssd_decode_stream_kernel<T, S, NN, kFuse><<<num_sms, kStreamThreads + 32, smem,  \
+                                                       stream>>>(                          \
+                state, (const T *)x, dt, A, (const T *)B, (const T *)C, D, (T *)y, batch, H, \
+                P, G, stages, err, fuse);                                                  \
+        }                                                                                  \
         break
         switch (N) {
             SSD_STREAM_N(4);
