@@ -40,3 +40,15 @@ def test_recorded_traffic_is_tied_to_the_sources(tmp_path, monkeypatch):
 def test_peaks_fall_back_when_unmeasured():
     peaks = bench.load_peaks()
     assert peaks["hbm_gbs"] > 0 and peaks["source"] in ("fallback", "measured")
+
+
+def test_fp8_workload_bytes():
+    """The long layer with E4M3 inputs: x, B, C one byte a value, y bf16 (two),
+    dt, A, D and the final state as for bf16 inputs."""
+    s8 = gen.SCAN_SHAPES["mamba2_2p7b_L65536_fp8"]
+    s16 = gen.SCAN_SHAPES["mamba2_2p7b_L65536"]
+    _, b8 = bench.scan_flops_bytes(s8, s8.random_init)
+    _, b16 = bench.scan_flops_bytes(s16, s16.random_init)
+    L, H, P, N = 65536, 80, 64, 128
+    assert b16 - b8 == L * H * P + 2 * L * N       # one byte less per x, B, C value
+    assert b8 == L * H * P * 3 + L * H * 4 + 2 * L * N + 2 * H * 4 + H * P * N * 4
