@@ -228,3 +228,58 @@ def test_decode_bf16_state_streaming_odd_state_count(b, H, G):
     s = host(s_dev)
     assert rel(s, s_ref) <= 1e-2
     assert np.mean(s == s_ref) >= 0.99
+
+
+@pytest.mark.parametrize("b,layers", [(1, 1), (1, 64), (16, 8)])
+@pytest.mark.parametrize("in_graph", [False, True])
+def test_chained_calls_see_the_previous_output(b, layers, in_graph):
+    """Decode calls launched back to back, each reading the previous call's
+    y as its x (x_{k+1} = y_k): the kernels may be scheduled while their
+    predecessor runs, so each must wait for it before reading.  Eight calls,
+    eagerly or captured in one CUDA graph, against the oracle stepping the same
+    chain with the bf16 rounding of y between steps.  One layer of 80 heads at
+    batch 1 takes the row-split single-state kernel; 64 layers at batch 1 the
+    streaming kernel with programmatic launch, 8 layers at batch 16 (67 states
+    per SM) the streaming kernel without it."""
+    import state_space_model_chunked_gb300 as ssd
+    H, P, N, G = 80 * layers, 64, 128, layers
+    state = gen.decode_state(b, H, P, N, seed=7 + b)
+    A, D = gen.decode_params(H, seed=7)
+    toks = [gen.decode_token_inputs(b, H, P, N, G, "bf16", seed=7, step=k) for k in range(8)]
+    s_dev = dev(state)
+    ys = [torch.empty((b, H, P), dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    x0 = dev(toks[0]["x"], "bf16")
+    ins = [(dev(t["dt"]), dev(t["B"], "bf16"), dev(t["C"], "bf16")) for t in toks]
+    A_d, D_d = dev(A), dev(D)
+
+    def chain():
+        x = x0
+        for k in range(8):
+            y = ys[k % 2]
+            ssd.state_update(s_dev, x, ins[k][0], A_d, ins[k][1], ins[k][2], D_d, y=y)
+            x = y
+
+    if in_graph:
+        s0 = s_dev.clone()
+        stream = torch.cuda.Stream()
+        with torch.cuda.stream(stream):
+            chain()                            # warm-up outside capture
+            torch.cuda.synchronize()
+            s_dev.copy_(s0)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                chain()
+            torch.cuda.synchronize()
+            s_dev.copy_(s0)
+            torch.cuda.synchronize()
+            g.replay()
+        torch.cuda.synchronize()
+    else:
+        chain()
+        torch.cuda.synchronize()
+    s_ref, x = state.astype(np.float64), toks[0]["x"]
+    for k in range(8):
+        y_ref, s_ref = oracle.step(s_ref, x, toks[k]["dt"], A, toks[k]["B"], toks[k]["C"], D)
+        x = oracle.round_bf16(y_ref)
+    assert rel(host(s_dev), s_ref) <= TOL["bf16"], rel(host(s_dev), s_ref)
+    assert rel(host(ys[1]), y_ref) <= TOL["bf16"], rel(host(ys[1]), y_ref)
