@@ -344,3 +344,12 @@ def test_fp8_widening_checks(lib):
     assert w(_fake(0x1000), None, 16, None) == INVALID
     assert w(_fake(0x1001), _fake(0x2000), 16, None) == INVALID
     assert w(_fake(0x1000), _fake(0x2008), 16, None) == INVALID
+
+
+def test_fp8_static_entry_rejects_copies_beyond_its_scratch(lib):
+    """The built-in scratch (64 MiB) cannot hold the bfloat16 copies of the
+    65536-token, 80-head layer's x (671 MB): SSD_ERR_WORKSPACE before any
+    launch."""
+    a = [_fake(0x1000), _fake(0x2000), _fake(0x3000), _fake(0x4000), _fake(0x5000), None,
+         FP8, 1, 65536, 80, 64, 128, 1, 256, None, _fake(0x6000), None, None]
+    assert lib.ssd_scan_fwd_static(*a) == WORKSPACE

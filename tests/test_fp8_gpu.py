@@ -150,3 +150,16 @@ def test_fp8_decode_is_refused():
         ssd.state_update(state, x, torch.zeros(1, 2, device="cuda"),
                          torch.zeros(2, device="cuda"), B, B)
     assert e.value.code == 2
+
+
+def test_fp8_varlen_without_tokens_returns_initial_states():
+    """A packed fp8 batch of empty sequences has no values to widen: the call
+    gives each sequence its initial state, as for bf16."""
+    import state_space_model_chunked_gb300 as ssd
+    inp = gen.varlen_inputs([0, 0, 0], 2, 64, 128, 1, "fp8", seed=1, random_init=True)
+    y, f = ssd.scan_fwd_varlen(dev(inp["x"], "fp8"), dev(inp["dt"]), dev(inp["A"]),
+                               dev(inp["B"], "fp8"), dev(inp["C"], "fp8"), inp["cu"],
+                               dev(inp["D"]), 256, dev(inp["init"]))
+    torch.cuda.synchronize()
+    assert y.shape == (0, 2, 64) and y.dtype == torch.bfloat16
+    np.testing.assert_array_equal(host(f), inp["init"])

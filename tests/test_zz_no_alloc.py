@@ -105,3 +105,27 @@ def test_static_scratch_scan_rejects_shapes_beyond_its_scratch():
     rc = lib.ssd_scan_fwd_static(fake, fake, fake, fake, fake, None, 1, b, L, H, P, N, G, Q,
                                  None, fake, None, None)
     assert rc == WORKSPACE_ERR
+
+
+def test_static_scratch_takes_fp8_inputs():
+    """fp8 (E4M3) x/B/C through the built-in scratch: their bfloat16 copies
+    and the segment states share it; checked against the oracle on the
+    decoded inputs."""
+    lib = ssd.load()
+    b, L, H, P, N, G, Q = 1, 4096, 24, 64, 128, 1, 256
+    inp = gen.scan_inputs(b, L, H, P, N, G, "fp8", seed=303, random_init=True)
+    x, Bm, Cm = dev(inp["x"], "fp8"), dev(inp["B"], "fp8"), dev(inp["C"], "fp8")
+    dt, A, D, init = dev(inp["dt"]), dev(inp["A"]), dev(inp["D"]), dev(inp["init"])
+    y = torch.empty(x.shape, dtype=torch.bfloat16, device=x.device)
+    f = torch.empty((b, H, P, N), dtype=torch.float32, device=x.device)
+    stream = torch.cuda.current_stream()
+    rc = lib.ssd_scan_fwd_static(_ptr(x), _ptr(dt), _ptr(A), _ptr(Bm), _ptr(Cm), _ptr(D),
+                                 2, b, L, H, P, N, G, Q, _ptr(init), _ptr(y), _ptr(f),
+                                 ctypes.c_void_p(stream.cuda_stream))
+    assert rc == 0, lib.ssd_status_string(rc).decode()
+    torch.cuda.synchronize()
+    xo, Bo, Co = (oracle.decode_e4m3(inp[k]) for k in ("x", "B", "C"))
+    yo, fo = oracle.scan_seq(xo, inp["dt"], inp["A"], Bo, Co, inp["D"], inp["init"])
+    assert rel(host(y), yo) <= TOL["fp8"]
+    assert rel(host(f), fo) <= TOL["fp8"]
+    ssd.last_device_error()
