@@ -857,6 +857,8 @@ def run_only(args):
                         torch.bfloat16 if args.decode_state == "bf16" else None)
     elif args.only == "decode_multi":
         r = time_decode_multi(args.decode_batch, args.decode_tokens, args.steps, device, peaks)
+    elif args.only == "decode_per_layer":
+        r = time_decode_per_layer(args.decode_batch, args.steps, device, peaks)
     else:
         props = torch.cuda.get_device_properties(device)
         l2 = getattr(props, "L2_cache_size", 126 * 1024 * 1024) or 126 * 1024 * 1024
@@ -1002,7 +1004,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--quick", action="store_true", help="headline workload only")
-    ap.add_argument("--only", choices=["decode", "decode_multi", "long", "130m", "370m", "fp8"],
+    ap.add_argument("--only", choices=["decode", "decode_multi", "decode_per_layer", "long", "130m",
+                                       "370m", "fp8"],
                     default=None, help="run one workload alone (for profiler captures)")
     ap.add_argument("--decode-batch", type=int, default=16)
     ap.add_argument("--decode-tokens", type=int, default=16,
