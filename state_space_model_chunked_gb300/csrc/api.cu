@@ -472,7 +472,8 @@ ssd_status ssd_state_update_multi(void *state, ssd_dtype state_dtype, const void
     fuse.z = z;
     cudaError_t e = ssd_launch_decode_multi(state, state_dtype == SSD_BF16, x, dt, A, B, C, D, y,
                                             in_dtype == SSD_BF16, batch, ntokens, nheads,
-                                            headdim, dstate, ngroups, fuse, stream);
+                                            headdim, dstate, ngroups, current_sm_count(), fuse,
+                                            stream);
     return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
 }
 

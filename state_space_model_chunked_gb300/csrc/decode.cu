@@ -22,8 +22,8 @@
 // memory, and releases the next launch at once.  Per-layer calls of a small
 // batch are launch-bound, and this hides most of a launch per call (timed on
 // 64 per-layer calls a token: 355 -> 274 us at batch 1 with the row split,
-// 1046 -> 1005 us at batch 16).  The streaming kernel takes it only for
-// calls of at most 64 states per SM.
+// 1046 -> 1005 us at batch 16).  The streaming kernel, and the multi-token
+// kernel below, take it only for calls of at most 64 states per SM.
 #include <algorithm>
 
 #include "common.cuh"
@@ -659,6 +659,8 @@ ssd_decode_multi_kernel(S *__restrict__ state, const T *__restrict__ x,
     const int g = h / (H / G);
     const int lane_n = threadIdx.x & (tpr - 1);
     const int r0 = threadIdx.x / tpr;
+    griddep_wait();                        // no-ops unless launched programmatically
+    griddep_launch_dependents();
     const float Ah = A[h];
     const float Dh = D ? D[h] : 0.0f;
     const float bias = ssd_dt_bias<kFuse>(fuse, h);
@@ -911,14 +913,21 @@ ssd_decode_multi_kernel(S *__restrict__ state, const T *__restrict__ x,
 template <typename T, typename S, int N, bool kFuse>
 cudaError_t launch_multi_k(S *state, const void *x, const float *dt, const float *A,
                            const void *B, const void *C, const float *D, void *y, int batch,
-                           int ntok, int H, int P, int G, const SsdFuse &fuse,
+                           int ntok, int H, int P, int G, int num_sms, const SsdFuse &fuse,
                            cudaStream_t stream) {
     const size_t smem = multi_smem_floats(P, N, kFuse && fuse.z != nullptr) * sizeof(float);
     cudaError_t e = cudaFuncSetAttribute(ssd_decode_multi_kernel<T, S, N, kFuse>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    ssd_decode_multi_kernel<T, S, N, kFuse><<<(unsigned)((size_t)batch * H), multi_threads(N),
-                                              smem, stream>>>(
+    const size_t units = (size_t)batch * H;
+    // programmatic launch for short calls only, as for the streaming kernel
+    // (at batch 1 it took 3 % off a 64-layer call of 4 tokens; long calls
+    // lost 0.4 %)
+    if (num_sms > 0 && units <= (size_t)num_sms * 64)
+        return launch_pdl(ssd_decode_multi_kernel<T, S, N, kFuse>, dim3((unsigned)units),
+                          dim3(multi_threads(N)), smem, stream, state, (const T *)x, dt, A,
+                          (const T *)B, (const T *)C, D, (T *)y, ntok, H, P, G, fuse);
+    ssd_decode_multi_kernel<T, S, N, kFuse><<<(unsigned)units, multi_threads(N), smem, stream>>>(
         state, (const T *)x, dt, A, (const T *)B, (const T *)C, D, (T *)y, ntok, H, P, G, fuse);
     return cudaGetLastError();
 }
@@ -926,12 +935,12 @@ cudaError_t launch_multi_k(S *state, const void *x, const float *dt, const float
 template <typename T, typename S, bool kFuse>
 cudaError_t launch_multi_t(S *state, const void *x, const float *dt, const float *A,
                            const void *B, const void *C, const float *D, void *y, int batch,
-                           int ntok, int H, int P, int N, int G, const SsdFuse &fuse,
+                           int ntok, int H, int P, int N, int G, int num_sms, const SsdFuse &fuse,
                            cudaStream_t stream) {
 #define SSD_MULTI_N(NN)                                                                    \
     case NN:                                                                               \
         return launch_multi_k<T, S, NN, kFuse>(state, x, dt, A, B, C, D, y, batch, ntok, H, P, \
-                                               G, fuse, stream)
+                                               G, num_sms, fuse, stream)
     switch (N) {
         SSD_MULTI_N(4);
         SSD_MULTI_N(8);
@@ -982,25 +991,25 @@ int ssd_decode_multi_max_headdim(int N) {
 cudaError_t ssd_launch_decode_multi(void *state, bool bf16_state, const void *x, const float *dt,
                                     const float *A, const void *B, const void *C,
                                     const float *D, void *y, bool bf16, int batch, int ntok,
-                                    int H, int P, int N, int G, const SsdFuse &fuse,
+                                    int H, int P, int N, int G, int num_sms, const SsdFuse &fuse,
                                     cudaStream_t stream) {
     const bool fused = ssd_fuse_active(fuse);
     using bf = __nv_bfloat16;
     if (bf16_state) {   // bf16 inputs only (checked by the caller)
         bf *st = static_cast<bf *>(state);
         return fused ? launch_multi_t<bf, bf, true>(st, x, dt, A, B, C, D, y, batch, ntok, H, P,
-                                                    N, G, fuse, stream)
+                                                    N, G, num_sms, fuse, stream)
                      : launch_multi_t<bf, bf, false>(st, x, dt, A, B, C, D, y, batch, ntok, H, P,
-                                                     N, G, fuse, stream);
+                                                     N, G, num_sms, fuse, stream);
     }
     float *st = static_cast<float *>(state);
     if (bf16)
         return fused ? launch_multi_t<bf, float, true>(st, x, dt, A, B, C, D, y, batch, ntok, H,
-                                                       P, N, G, fuse, stream)
+                                                       P, N, G, num_sms, fuse, stream)
                      : launch_multi_t<bf, float, false>(st, x, dt, A, B, C, D, y, batch, ntok, H,
-                                                        P, N, G, fuse, stream);
+                                                        P, N, G, num_sms, fuse, stream);
     return fused ? launch_multi_t<float, float, true>(st, x, dt, A, B, C, D, y, batch, ntok, H, P,
-                                                      N, G, fuse, stream)
+                                                      N, G, num_sms, fuse, stream)
                  : launch_multi_t<float, float, false>(st, x, dt, A, B, C, D, y, batch, ntok, H,
-                                                       P, N, G, fuse, stream);
+                                                       P, N, G, num_sms, fuse, stream);
 }

@@ -19,7 +19,7 @@ cudaError_t ssd_launch_decode(void *state, bool bf16_state, const void *x, const
 cudaError_t ssd_launch_decode_multi(void *state, bool bf16_state, const void *x, const float *dt,
                                     const float *A, const void *B, const void *C,
                                     const float *D, void *y, bool bf16, int batch, int ntok,
-                                    int H, int P, int N, int G, const SsdFuse &fuse,
+                                    int H, int P, int N, int G, int num_sms, const SsdFuse &fuse,
                                     cudaStream_t stream);
 int ssd_decode_multi_max_headdim(int N);
 
