@@ -371,6 +371,39 @@ ssd_status ssd_state_update_multi(void *state, ssd_dtype state_dtype, const void
  * SSD_ERR_INVALID_ARG for a null or misaligned pointer (n > 0). */
 ssd_status ssd_fp8_e4m3_to_bf16(const void *src, void *dst, size_t n, cudaStream_t stream);
 
+/* One long sequence split over GPUs by tokens (GPU r holds a contiguous
+ * range of its tokens): the exchange step.  Step-3 of the recurrence at the
+ * granularity of a range (CGLA section III.A: the state is carried
+ * sequentially, with the input-dependent diagonal decay):
+ *     H_in[0] = init,   H_in[r+1] = exp(a_r) H_in[r] + F_r,
+ * with a_r the range's log-decay and F_r the state the range reaches from a
+ * zero state (its ssd_scan_fwd with init_state = NULL).  Each GPU scans its
+ * range from zero for F_r, the pairs (a_r, F_r) are gathered from every GPU,
+ * each chains them to its own H_in and scans its range again from H_in for
+ * y; the last range's final state is the sequence's.  The pages do not build
+ * this split (their runs are on one device); the all-gather is the caller's
+ * (torch.distributed in the Python package).
+ *
+ * ssd_range_log_decay: log_decay[b][h] = A[h] * sum over the range's tokens
+ * of dt[b][t][h] (after the dt transform, when one is given, as the scan
+ * applies it), summed in double precision.  dt [batch][seqlen][nheads],
+ * A [nheads], log_decay [batch][nheads]: float device arrays.
+ * SSD_ERR_INVALID_ARG for null pointers, sizes <= 0 or an invalid transform. */
+ssd_status ssd_range_log_decay(const float *dt, const float *A,
+                               const ssd_dt_transform *dt_transform, int batch, int seqlen,
+                               int nheads, float *log_decay, cudaStream_t stream);
+
+/* ssd_chain_states: entering[r] = H_in[r] for r = 0 .. nranges-1 from the
+ * ranges' contributions contrib[r] = F_r and log-decays log_decay[r] = a_r,
+ * starting from init (zeros when NULL).  contrib, entering
+ * [nranges][batch][nheads][headdim][dstate]; log_decay
+ * [nranges][batch][nheads]; init [batch][nheads][headdim][dstate]: float
+ * device arrays; entering must not overlap the inputs.  SSD_ERR_INVALID_ARG
+ * for null required pointers or sizes <= 0. */
+ssd_status ssd_chain_states(const float *contrib, const float *log_decay, const float *init,
+                            int nranges, int batch, int nheads, int headdim, int dstate,
+                            float *entering, cudaStream_t stream);
+
 /* Human-readable name of a status code (static storage). */
 const char *ssd_status_string(ssd_status s);
 

@@ -41,4 +41,6 @@ from ._binding import (  # noqa: F401
     EXPORTED_SYMBOLS,
     FP8_E4M3,
     fp8_e4m3_to_bf16,
+    range_log_decay,
+    chain_states,
 )

@@ -31,6 +31,8 @@ EXPORTED_SYMBOLS = (
     "ssd_last_device_error",
     "ssd_debug_inject_fault",
     "ssd_fp8_e4m3_to_bf16",
+    "ssd_range_log_decay",
+    "ssd_chain_states",
 )
 
 ALGO_AUTO, ALGO_SIMT, ALGO_TCGEN05 = 0, 1, 2
@@ -120,6 +122,10 @@ def load():
         lib.ssd_last_device_error.argtypes = []
         lib.ssd_fp8_e4m3_to_bf16.restype = _int
         lib.ssd_fp8_e4m3_to_bf16.argtypes = [_vp, _vp, _sz, _vp]
+        lib.ssd_range_log_decay.restype = _int
+        lib.ssd_range_log_decay.argtypes = [_vp, _vp, _vp, _int, _int, _int, _vp, _vp]
+        lib.ssd_chain_states.restype = _int
+        lib.ssd_chain_states.argtypes = [_vp, _vp, _vp] + [_int] * 5 + [_vp, _vp]
         _lib = lib
         return lib
 
@@ -571,6 +577,46 @@ def fp8_e4m3_to_bf16(src, out=None):
         stream = torch.cuda.current_stream(src.device).cuda_stream
         rc = lib.ssd_fp8_e4m3_to_bf16(_ptr(src), _ptr(out), src.numel(), ctypes.c_void_p(stream))
     _check("ssd_fp8_e4m3_to_bf16", rc)
+    return out
+
+
+def range_log_decay(dt, A, *, dt_bias=None, dt_softplus=False, dt_limit=None):
+    """A token range's log-decay, [b, H] f32: A[h] times the sum of dt over
+    the range (dt [b, L, H] f32, transformed as scan_fwd would with the same
+    keywords).  One factor of the exchange when a sequence is split over GPUs."""
+    lib = load()
+    _need(dt, "dt", torch.float32)
+    dev = dt.device
+    b, L, H = dt.shape
+    _need(A, "A", torch.float32, dev, (H,))
+    out = torch.empty((b, H), dtype=torch.float32, device=dev)
+    with torch.cuda.device(dev):
+        stream = torch.cuda.current_stream(dev).cuda_stream
+        tptr, _keep = _dt_transform(dt_bias, dt_softplus, dt_limit, H, dev)
+        rc = lib.ssd_range_log_decay(_ptr(dt), _ptr(A), tptr, b, L, H, _ptr(out),
+                                     ctypes.c_void_p(stream))
+    _check("ssd_range_log_decay", rc)
+    return out
+
+
+def chain_states(contrib, log_decay, init=None):
+    """Entering states [R, b, H, P, N] f32 of R consecutive token ranges:
+    entering[0] = init (zeros when None), entering[r+1] = exp(log_decay[r])
+    entering[r] + contrib[r], from contrib [R, b, H, P, N] (each range's state
+    from a zero start) and log_decay [R, b, H]."""
+    lib = load()
+    _need(contrib, "contrib", torch.float32)
+    dev = contrib.device
+    R, b, H, P, N = contrib.shape
+    _need(log_decay, "log_decay", torch.float32, dev, (R, b, H))
+    if init is not None:
+        _need(init, "init", torch.float32, dev, (b, H, P, N))
+    out = torch.empty_like(contrib)
+    with torch.cuda.device(dev):
+        stream = torch.cuda.current_stream(dev).cuda_stream
+        rc = lib.ssd_chain_states(_ptr(contrib), _ptr(log_decay), _ptr(init), R, b, H, P, N,
+                                  _ptr(out), ctypes.c_void_p(stream))
+    _check("ssd_chain_states", rc)
     return out
 
 

@@ -19,7 +19,8 @@ CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_lib")
 LIB = os.path.join(OUT_DIR, "libssd.so")
 OBJ_DIR = os.path.join(HERE, "_build")
-SOURCES = ["api.cu", "decode.cu", "scan_simt.cu", "scan_tc.cu", "scan_static.cu", "widen.cu"]
+SOURCES = ["api.cu", "decode.cu", "scan_simt.cu", "scan_tc.cu", "scan_static.cu", "widen.cu",
+           "seqshard.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -298,6 +298,34 @@ ssd_status ssd_fp8_e4m3_to_bf16(const void *src, void *dst, size_t n, cudaStream
                                                                                  : SSD_ERR_CUDA;
 }
 
+ssd_status ssd_range_log_decay(const float *dt, const float *A,
+                               const ssd_dt_transform *dt_transform, int batch, int seqlen,
+                               int nheads, float *log_decay, cudaStream_t stream) {
+    if (!dt || !A || !log_decay) return SSD_ERR_INVALID_ARG;
+    if (batch <= 0 || seqlen <= 0 || nheads <= 0) return SSD_ERR_INVALID_ARG;
+    if ((nheads + 31) / 32 > 65535) return SSD_ERR_UNSUPPORTED;   // grid rows of 32 heads
+    SsdFuse fuse;
+    const ssd_status st = dt_transform_of(dt_transform, &fuse);
+    if (st != SSD_OK) return st;
+    return ssd_launch_range_log_decay(dt, A, batch, seqlen, nheads, fuse, log_decay, stream) ==
+                   cudaSuccess
+               ? SSD_OK
+               : SSD_ERR_CUDA;
+}
+
+ssd_status ssd_chain_states(const float *contrib, const float *log_decay, const float *init,
+                            int nranges, int batch, int nheads, int headdim, int dstate,
+                            float *entering, cudaStream_t stream) {
+    if (!contrib || !log_decay || !entering) return SSD_ERR_INVALID_ARG;
+    if (nranges <= 0 || batch <= 0 || nheads <= 0 || headdim <= 0 || dstate <= 0)
+        return SSD_ERR_INVALID_ARG;
+    if ((size_t)batch * nheads * headdim * dstate >= ((size_t)1 << 38)) return SSD_ERR_UNSUPPORTED;
+    return ssd_launch_chain_states(contrib, log_decay, init, nranges, batch, nheads, headdim,
+                                   dstate, entering, stream) == cudaSuccess
+               ? SSD_OK
+               : SSD_ERR_CUDA;
+}
+
 ssd_status ssd_debug_inject_fault(ssd_fault fault, unsigned long long wait_limit_ns) {
     if (fault != SSD_FAULT_NONE && fault != SSD_FAULT_WITHHOLD_SIGNAL) return SSD_ERR_INVALID_ARG;
     g_debug.fault = (int)fault;

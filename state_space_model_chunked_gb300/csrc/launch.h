@@ -42,6 +42,15 @@ struct SsdWidenFirst {     // first CTA of each job in the widening launch
 };
 cudaError_t ssd_launch_widen_fp8(const SsdWidenJobs &jobs, cudaStream_t stream);
 
+// Sequence split over GPUs by tokens: a token range's log-decay A_h * sum dt
+// ([batch][H], dt transformed as the scan does), and the chain of R ranges'
+// contributions into each range's entering state ([R][batch][H][P][N]).
+cudaError_t ssd_launch_range_log_decay(const float *dt, const float *A, int batch, int L, int H,
+                                       const SsdFuse &fuse, float *out, cudaStream_t stream);
+cudaError_t ssd_launch_chain_states(const float *contrib, const float *log_decay,
+                                    const float *init, int R, int batch, int H, int P, int N,
+                                    float *entering, cudaStream_t stream);
+
 // Test hooks of the ABI layer: the fault to inject (0 = none) and the limit
 // of every bounded device wait, read by the launchers at each launch.
 struct SsdDebug {

@@ -8,6 +8,12 @@ group share B and C, and the tensor-core kernel pairs them).  A packed batch
 of sequences splits into contiguous runs of whole sequences with even token
 shares (ssd_scan_fwd_varlen on each run).
 
+One long sequence can also split over GPUs by tokens (token_range,
+scan_sequence_sharded), at the cost of one exchange: each GPU scans its range
+from a zero state, the ranges' (log-decay, state) pairs are all-gathered,
+each GPU chains them to the state entering its range, and scans the range
+again from it.
+
 Timing across ranks takes the maximum over ranks (the slowest GPU finishes
 the job).
 """
@@ -97,3 +103,64 @@ def max_over_ranks(value: float, dist=None, device=None) -> float:
                      device=device if device is not None else "cpu")
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def token_range(seqlen: int, world: int, rank: int, align: int = 128):
+    """Contiguous [t0, t1) token range of one sequence for `rank` of `world`:
+    even shares of whole `align`-token tiles (the tensor-core kernels' tile),
+    the ragged tail with the last rank.  With more ranks than tiles the
+    trailing ranks get empty ranges."""
+    if not 0 <= rank < world:
+        raise ValueError("rank out of range")
+    if seqlen < 0 or align <= 0:
+        raise ValueError("seqlen must be >= 0 and align > 0")
+    tiles = -(-seqlen // align)
+    t0 = min(seqlen, (tiles * rank // world) * align)
+    t1 = min(seqlen, (tiles * (rank + 1) // world) * align)
+    return t0, t1
+
+
+def scan_sequence_sharded(x, dt, A, B, C, D=None, init=None, chunk=256, *, group=None,
+                          ops=None, **dt_kw):
+    """This rank's token range of one long sequence, scanned as part of the
+    whole (x [b, Lr, H, P], dt [b, Lr, H], B, C [b, Lr, G, N]: the rank's
+    tokens; A, D, init [b, H, P, N] or None: the same on every rank).
+
+    Step-3 of the recurrence at the granularity of one rank's range: the
+    range's state from a zero start F_r and log-decay a_r = A * sum(dt) are
+    all-gathered, H_in[0] = init and H_in[r+1] = exp(a_r) H_in[r] + F_r give
+    the state entering this range, and the range is scanned again from it.
+    Returns (y, final): y of the rank's tokens and the state at the end of
+    its range (the sequence's final state on the last rank).
+
+    ``ops`` = (scan, range_log_decay, chain_states) with the signatures of the
+    package's functions; the default is the package's own (the library's
+    kernels), and the tests pass CPU stand-ins.  dt transform keywords go to
+    both the scans and the log-decay."""
+    import torch
+    import torch.distributed as dist
+    if ops is None:
+        from . import _binding as ssd
+        ops = (lambda *a, **k: ssd.scan_fwd(*a, **k), ssd.range_log_decay, ssd.chain_states)
+    scan, log_decay_of, chain = ops
+    world = dist.get_world_size(group) if dist.is_initialized() else 1
+    rank = dist.get_rank(group) if dist.is_initialized() else 0
+    b, L, H, P = x.shape
+    N = B.shape[3]
+    if L > 0:
+        _, contrib = scan(x, dt, A, B, C, D, chunk, None, **dt_kw)
+        a = log_decay_of(dt, A, **dt_kw)
+    else:       # an empty range passes the state through unchanged (states in A's dtype)
+        contrib = torch.zeros((b, H, P, N), dtype=A.dtype, device=x.device)
+        a = torch.zeros((b, H), dtype=A.dtype, device=x.device)
+    if world > 1:
+        contribs = [torch.empty_like(contrib) for _ in range(world)]
+        decays = [torch.empty_like(a) for _ in range(world)]
+        dist.all_gather(contribs, contrib.contiguous(), group=group)
+        dist.all_gather(decays, a.contiguous(), group=group)
+    else:
+        contribs, decays = [contrib], [a]
+    entering = chain(torch.stack(contribs), torch.stack(decays), init)[rank].contiguous()
+    if L == 0:
+        return x.new_empty((b, 0, H, P)), entering
+    return scan(x, dt, A, B, C, D, chunk, entering, **dt_kw)

@@ -207,3 +207,92 @@ def test_two_gloo_ranks_split_one_group(tmp_path):
     assert ys[0].shape[2] == 4 and ys[1].shape[2] == 4
     assert oracle.rel_l2(np.concatenate(ys, axis=2), y_full) < 1e-13
     assert oracle.rel_l2(np.concatenate(fs, axis=1), f_full) < 1e-13
+
+
+# ------------------------------------------------ one sequence split by tokens
+def test_token_ranges_partition_on_tile_boundaries():
+    from state_space_model_chunked_gb300.sharding import token_range
+    for L in (1, 127, 128, 129, 1000, 65536):
+        for world in (1, 2, 3, 4, 8):
+            cuts = [token_range(L, world, r) for r in range(world)]
+            assert cuts[0][0] == 0 and cuts[-1][1] == L
+            for (a0, a1), (b0, b1) in zip(cuts, cuts[1:]):
+                assert a1 == b0 and a0 <= a1
+            assert all(a % 128 == 0 for a, _ in cuts)
+
+
+def _cpu_sequence_ops():
+    """CPU stand-ins for the library's scan, range log-decay and state chain
+    (fp64, through the oracle's scan), with the package functions'
+    signatures."""
+    import torch
+
+    import oracle
+
+    def scan(x, dt, A, B, C, D, chunk, init):
+        y, fin = oracle.scan_seq(x.numpy(), dt.numpy(), A.numpy(), B.numpy(), C.numpy(),
+                                 None if D is None else D.numpy(),
+                                 None if init is None else init.numpy(), nthreads=1)
+        return torch.from_numpy(y), torch.from_numpy(fin)
+
+    def log_decay(dt, A):
+        return torch.from_numpy(A.numpy()[None, :].astype(np.float64) *
+                                dt.numpy().astype(np.float64).sum(axis=1))
+
+    def chain(contrib, decays, init):
+        c, d = contrib.numpy(), decays.numpy()
+        h = np.zeros(c.shape[1:]) if init is None else init.numpy().astype(np.float64)
+        out = np.empty(c.shape)
+        for r in range(c.shape[0]):
+            out[r] = h
+            h = np.exp(d[r])[:, :, None, None] * h + c[r]
+        return torch.from_numpy(out)
+
+    return scan, log_decay, chain
+
+
+def _seq_worker(rank, world, port, out_dir, L):
+    import torch
+    import torch.distributed as dist
+
+    from state_space_model_chunked_gb300 import inputs as gen
+    from state_space_model_chunked_gb300.sharding import scan_sequence_sharded, token_range
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    inp = gen.scan_inputs(2, L, 4, 8, 16, 2, "bf16", seed=321, random_init=True)
+    t0, t1 = token_range(L, world, rank)
+    part = {k: torch.from_numpy(np.ascontiguousarray(inp[k][:, t0:t1], dtype=np.float64))
+            for k in ("x", "dt", "B", "C")}
+    whole = {k: torch.from_numpy(inp[k].astype(np.float64)) for k in ("A", "D", "init")}
+    y, fin = scan_sequence_sharded(part["x"], part["dt"], whole["A"], part["B"], part["C"],
+                                   whole["D"], whole["init"], ops=_cpu_sequence_ops())
+    np.save(os.path.join(out_dir, f"sy{rank}.npy"), y.numpy())
+    np.save(os.path.join(out_dir, f"sf{rank}.npy"), fin.numpy())
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("world,L", [(2, 700), (3, 200)])
+def test_gloo_ranks_split_one_sequence_by_tokens(tmp_path, world, L):
+    """Ranks hold contiguous token ranges of one sequence (with 3 ranks and 2
+    tiles, the first range is empty); after the all-gather and the chain,
+    their outputs reassemble the unsplit scan and the last rank holds its
+    final state."""
+    port = _free_port()
+    ctx = mp.get_context("spawn")
+    procs = [ctx.Process(target=_seq_worker, args=(r, world, port, str(tmp_path), L))
+             for r in range(world)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=120)
+        assert p.exitcode == 0
+    import oracle
+    from state_space_model_chunked_gb300 import inputs as gen
+    inp = gen.scan_inputs(2, L, 4, 8, 16, 2, "bf16", seed=321, random_init=True)
+    y_full, f_full = oracle.scan_seq(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"],
+                                     inp["D"], inp["init"])
+    ys = [np.load(tmp_path / f"sy{r}.npy") for r in range(world)]
+    assert oracle.rel_l2(np.concatenate(ys, axis=1), y_full) < 1e-12
+    assert oracle.rel_l2(np.load(tmp_path / f"sf{world - 1}.npy"), f_full) < 1e-12
