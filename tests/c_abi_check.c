@@ -63,6 +63,10 @@ int main(void) {
            SSD_ERR_UNSUPPORTED);
     EXPECT(ssd_fp8_e4m3_to_bf16(NULL, y, 16, 0), SSD_ERR_INVALID_ARG);
     EXPECT(ssd_fp8_e4m3_to_bf16(NULL, NULL, 0, 0), SSD_OK);
+    /* the exchange of a sequence split over GPUs */
+    EXPECT(ssd_range_log_decay(NULL, A, NULL, 1, 16, 4, (float *)0x9000, 0), SSD_ERR_INVALID_ARG);
+    EXPECT(ssd_chain_states((const float *)0x9000, NULL, NULL, 2, 1, 4, 8, 8, (float *)0xa000, 0),
+           SSD_ERR_INVALID_ARG);
     printf("c abi ok\n");
     return 0;
 }

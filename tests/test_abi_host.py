@@ -353,3 +353,26 @@ def test_fp8_static_entry_rejects_copies_beyond_its_scratch(lib):
     a = [_fake(0x1000), _fake(0x2000), _fake(0x3000), _fake(0x4000), _fake(0x5000), None,
          FP8, 1, 65536, 80, 64, 128, 1, 256, None, _fake(0x6000), None, None]
     assert lib.ssd_scan_fwd_static(*a) == WORKSPACE
+
+
+def test_sequence_split_calls_reject_bad_arguments(lib):
+    """The exchange of a sequence split over GPUs: null pointers, sizes <= 0
+    and inverted transform limits come back before any launch."""
+    dt, A, out = _fake(0x1000), _fake(0x2000), _fake(0x3000)
+    assert lib.ssd_range_log_decay(None, A, None, 1, 16, 4, out, None) == INVALID
+    assert lib.ssd_range_log_decay(dt, A, None, 1, 0, 4, out, None) == INVALID
+    assert lib.ssd_range_log_decay(dt, A, None, 1, 16, 0, out, None) == INVALID
+    assert lib.ssd_range_log_decay(dt, A, None, 1, 16, 4, None, None) == INVALID
+
+    class Tr(ctypes.Structure):
+        _fields_ = [("dt_bias", ctypes.c_void_p), ("softplus", ctypes.c_int),
+                    ("dt_min", ctypes.c_float), ("dt_max", ctypes.c_float)]
+    tr = Tr(None, 1, 0.5, 0.1)
+    assert lib.ssd_range_log_decay(dt, A, ctypes.cast(ctypes.pointer(tr), ctypes.c_void_p),
+                                   1, 16, 4, out, None) == INVALID
+    c, d, e = _fake(0x4000), _fake(0x5000), _fake(0x6000)
+    assert lib.ssd_chain_states(None, d, None, 2, 1, 4, 8, 8, e, None) == INVALID
+    assert lib.ssd_chain_states(c, None, None, 2, 1, 4, 8, 8, e, None) == INVALID
+    assert lib.ssd_chain_states(c, d, None, 2, 1, 4, 8, 8, None, None) == INVALID
+    assert lib.ssd_chain_states(c, d, None, 0, 1, 4, 8, 8, e, None) == INVALID
+    assert lib.ssd_chain_states(c, d, None, 2, 1, 4, 0, 8, e, None) == INVALID
